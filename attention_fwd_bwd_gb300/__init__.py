@@ -1,0 +1,210 @@
+"""GB300 (sm_103a) fused attention forward and backward.
+
+A thin ctypes binding over libattn.so, whose C ABI is declared in
+include/attn.h. Each function here only marshals arguments: it checks the
+torch tensors' dtype, device and layout, reads the sizes off their shapes and
+passes raw device pointers and the current CUDA stream to the library of the
+same name. All compute runs in the library's CUDA kernels; there is no other
+code path. If libattn.so is missing the first call raises.
+
+Layout: q, o, o_lo, dO are [B, S, Hq, D] bf16; k, v are [B, S, Hkv, D] bf16;
+dq is [B, S, Hq, D] fp32; dk, dv are [B, S, Hkv, D] fp32; lse is [B, Hq, S]
+fp32; all contiguous on one CUDA device.
+"""
+import ctypes
+import os
+
+__all__ = [
+    "AttnError",
+    "lib",
+    "attn_fwd",
+    "attn_fwd_residual",
+    "attn_bwd",
+    "attn_bwd_preprocess",
+    "attn_bwd_main",
+    "attn_bwd_workspace_size",
+    "attn_check_status",
+    "attn_set_wait_timeout_ns",
+    "attn_status_string",
+    "STATUS",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libattn.so")
+
+STATUS = {
+    0: "ATTN_OK",
+    1: "ATTN_ERR_INVALID_ARG",
+    2: "ATTN_ERR_UNSUPPORTED",
+    3: "ATTN_ERR_CUDA",
+    4: "ATTN_ERR_TIMEOUT",
+    5: "ATTN_ERR_WORKSPACE",
+}
+
+_lib = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, fn, code):
+        self.code = code
+        super().__init__(f"{fn} failed: {STATUS.get(code, code)} ({attn_status_string(code)})")
+
+
+def lib():
+    """The loaded libattn.so with argument types set (raises if it is missing)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"libattn.so not found at {LIB_PATH}; build it with "
+            "`python -c 'import __graft_entry__ as g; g.build()'` "
+            "or `python attention_fwd_bwd_gb300/_build.py`")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    L.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
+    L.attn_fwd.restype = i
+    L.attn_fwd_residual.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
+    L.attn_fwd_residual.restype = i
+    L.attn_bwd_workspace_size.argtypes = [i, i, i, i, i]
+    L.attn_bwd_workspace_size.restype = sz
+    L.attn_bwd.argtypes = [vp] * 10 + [i] * 6 + [f, vp, sz, vp]
+    L.attn_bwd.restype = i
+    L.attn_bwd_preprocess.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, vp, sz, vp]
+    L.attn_bwd_preprocess.restype = i
+    L.attn_bwd_main.argtypes = [vp] * 7 + [i] * 6 + [f, vp, sz, vp]
+    L.attn_bwd_main.restype = i
+    L.attn_status_string.argtypes = [i]
+    L.attn_status_string.restype = ctypes.c_char_p
+    L.attn_check_status.argtypes = [vp]
+    L.attn_check_status.restype = i
+    L.attn_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
+    L.attn_set_wait_timeout_ns.restype = None
+    _lib = L
+    return L
+
+
+def attn_status_string(code):
+    return lib().attn_status_string(int(code)).decode()
+
+
+def _check(fn, code):
+    if code != 0:
+        raise AttnError(fn, code)
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _sizes(q, k):
+    import torch
+    for t in (q, k):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError("q, k, v, o, o_lo, dO must be contiguous 4-D bf16 CUDA tensors [B,S,H,D]")
+    B, S, Hq, D = q.shape
+    Bk, Sk, Hkv, Dk = k.shape
+    if (Bk, Sk, Dk) != (B, S, D):
+        raise ValueError(f"k shape {tuple(k.shape)} does not match q shape {tuple(q.shape)}")
+    return B, Hq, Hkv, S, D
+
+
+def _like(t, ref, what, dtype=None):
+    dtype = ref.dtype if dtype is None else dtype
+    if t.shape != ref.shape or t.dtype != dtype or not t.is_contiguous() or t.device != ref.device:
+        raise ValueError(f"{what} must be a contiguous {dtype} tensor of shape {tuple(ref.shape)}")
+
+
+def _lse_ok(lse, B, Hq, S, dev):
+    import torch
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, Hq, S) or not lse.is_contiguous() or lse.device != dev:
+        raise ValueError(f"lse must be a contiguous fp32 tensor of shape {(B, Hq, S)}")
+
+
+def _opt(t):
+    return None if t is None else _ptr(t)
+
+
+def attn_fwd(q, k, v, o, lse, causal, scale, stream=None):
+    """o, lse <- attention(q, k, v); see attn_fwd in include/attn.h."""
+    B, Hq, Hkv, S, D = _sizes(q, k)
+    _like(v, k, "v")
+    _like(o, q, "o")
+    _lse_ok(lse, B, Hq, S, q.device)
+    _check("attn_fwd", lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, S, D,
+                                      int(bool(causal)), float(scale), _stream(stream)))
+
+
+def attn_fwd_residual(q, k, v, o, o_lo, lse, causal, scale, stream=None):
+    """o, o_lo, lse <- attention(q, k, v); see attn_fwd_residual in include/attn.h."""
+    B, Hq, Hkv, S, D = _sizes(q, k)
+    _like(v, k, "v")
+    _like(o, q, "o")
+    _like(o_lo, q, "o_lo")
+    _lse_ok(lse, B, Hq, S, q.device)
+    _check("attn_fwd_residual", lib().attn_fwd_residual(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(o_lo), _ptr(lse),
+                                                        B, Hq, Hkv, S, D, int(bool(causal)), float(scale),
+                                                        _stream(stream)))
+
+
+def attn_bwd_workspace_size(B, Hq, Hkv, S, D):
+    return int(lib().attn_bwd_workspace_size(B, Hq, Hkv, S, D))
+
+
+def _ws(workspace):
+    return ctypes.c_void_p(workspace.data_ptr()), workspace.numel() * workspace.element_size()
+
+
+def _grads_ok(q, k, dq, dk, dv):
+    import torch
+    _like(dq, q, "dq", torch.float32)
+    _like(dk, k, "dk", torch.float32)
+    _like(dv, k, "dv", torch.float32)
+
+
+def attn_bwd(q, k, v, o, dO, lse, dq, dk, dv, causal, scale, workspace, o_lo=None, stream=None):
+    """dq, dk, dv (fp32) <- gradients of sum(dO * o); see attn_bwd in include/attn.h."""
+    B, Hq, Hkv, S, D = _sizes(q, k)
+    for t, ref, n in ((v, k, "v"), (o, q, "o"), (dO, q, "dO")):
+        _like(t, ref, n)
+    if o_lo is not None:
+        _like(o_lo, q, "o_lo")
+    _grads_ok(q, k, dq, dk, dv)
+    _lse_ok(lse, B, Hq, S, q.device)
+    wp, wb = _ws(workspace)
+    _check("attn_bwd", lib().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(dq),
+                                      _ptr(dk), _ptr(dv), _opt(o_lo), B, Hq, Hkv, S, D, int(bool(causal)),
+                                      float(scale), wp, wb, _stream(stream)))
+
+
+def attn_bwd_preprocess(q, k, o, dO, lse, dq, workspace, o_lo=None, stream=None):
+    """Stage 1 of attn_bwd (q and k only supply the sizes)."""
+    B, Hq, Hkv, S, D = _sizes(q, k)
+    wp, wb = _ws(workspace)
+    _check("attn_bwd_preprocess", lib().attn_bwd_preprocess(_ptr(o), _opt(o_lo), _ptr(dO), _ptr(lse), _ptr(dq),
+                                                            B, Hq, Hkv, S, D, wp, wb, _stream(stream)))
+
+
+def attn_bwd_main(q, k, v, dO, dq, dk, dv, causal, scale, workspace, stream=None):
+    """Stage 2 of attn_bwd."""
+    B, Hq, Hkv, S, D = _sizes(q, k)
+    wp, wb = _ws(workspace)
+    _check("attn_bwd_main", lib().attn_bwd_main(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(dq), _ptr(dk),
+                                                _ptr(dv), B, Hq, Hkv, S, D, int(bool(causal)), float(scale),
+                                                wp, wb, _stream(stream)))
+
+
+def attn_check_status(workspace=None):
+    """Synchronises and returns the device status code (0 = ok, 4 = a wait timed out)."""
+    return int(lib().attn_check_status(None if workspace is None else ctypes.c_void_p(workspace.data_ptr())))
+
+
+def attn_set_wait_timeout_ns(ns):
+    lib().attn_set_wait_timeout_ns(int(ns))

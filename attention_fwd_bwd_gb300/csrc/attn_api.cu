@@ -1,0 +1,323 @@
+// C ABI of the attention library: argument validation, TMA tensor-map
+// encoding, launch of the forward and backward kernels, status reporting.
+// The declarations and their contracts are in include/attn.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/attn.h"
+#include "attn_common.cuh"
+
+namespace attn {
+namespace {
+
+// Status word of the forward kernels (one per device that loads the library).
+__device__ int g_fwd_status;
+
+constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;
+unsigned long long g_timeout_ns = kDefaultTimeoutNs;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+bool check_status_env() {
+  static int v = -1;
+  if (v < 0) {
+    const char* e = std::getenv("ATTN_CHECK_STATUS");
+    v = (e && e[0] == '1') ? 1 : 0;
+  }
+  return v == 1;
+}
+
+// 0 = unknown, 1 = supported, 2 = not supported.
+int g_dev_ok[64];
+
+attn_status_t check_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (dev >= 0 && dev < 64 && g_dev_ok[dev]) return g_dev_ok[dev] == 1 ? ATTN_OK : ATTN_ERR_UNSUPPORTED;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  // The kernels are built for sm_103a only.
+  const bool ok = (major == 10 && minor == 3);
+  if (dev >= 0 && dev < 64) g_dev_ok[dev] = ok ? 1 : 2;
+  return ok ? ATTN_OK : ATTN_ERR_UNSUPPORTED;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+attn_status_t validate_sizes(int B, int Hq, int Hkv, int S, int D) {
+  if (B < 0 || S < 0 || Hq <= 0 || Hkv <= 0) return ATTN_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  // Element offsets stay within what the TMA coordinates and 64-bit indices hold.
+  if (static_cast<long long>(S) > (1ll << 24)) return ATTN_ERR_UNSUPPORTED;
+  return ATTN_OK;
+}
+
+// 4-D bf16 map over a [B, S, H, D] tensor; a box is `rows` sequence rows of
+// one head and 64 columns (128 bytes), stored with 128-byte swizzle.
+bool make_bshd_map(CUtensorMap* m, const void* base, int B, int S, int H, int D, int rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
+                              static_cast<cuuint64_t>(S), static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2,
+                                 static_cast<cuuint64_t>(H) * D * 2,
+                                 static_cast<cuuint64_t>(S) * H * D * 2};
+  const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(rows), 1};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 4-D fp32 map over the [B, S, Hq, D] dq output; a box is 64 sequence rows of
+// one head, all D columns, unswizzled (the layout the dQ staging tile uses).
+bool make_dq_map(CUtensorMap* m, void* base, int B, int S, int H, int D) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
+                              static_cast<cuuint64_t>(S), static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 4,
+                                 static_cast<cuuint64_t>(H) * D * 4,
+                                 static_cast<cuuint64_t>(S) * H * D * 4};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(D), 1, 64, 1};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int* fwd_status_ptr() {
+  static int* ptrs[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return nullptr;
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_fwd_status) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<int*>(p);
+  }
+  return ptrs[dev];
+}
+
+attn_status_t finish(cudaError_t e, cudaStream_t stream, const int* status_dev) {
+  if (e != cudaSuccess) return ATTN_ERR_CUDA;
+  if (check_status_env()) {
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return ATTN_ERR_CUDA;
+    int st = 0;
+    if (status_dev && cudaMemcpy(&st, status_dev, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    if (st != 0) return ATTN_ERR_TIMEOUT;
+  }
+  return ATTN_OK;
+}
+
+attn_status_t check_workspace(void* ws, size_t bytes, int B, int Hq, int S, int D) {
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return ATTN_ERR_WORKSPACE;
+  (void)D;
+  if (bytes < bwd_workspace_layout(B, Hq, S).total) return ATTN_ERR_WORKSPACE;
+  return ATTN_OK;
+}
+
+}  // namespace
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" {
+
+const char* attn_status_string(attn_status_t s) {
+  switch (s) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported configuration or device";
+    case ATTN_ERR_CUDA: return "CUDA error";
+    case ATTN_ERR_TIMEOUT: return "kernel pipeline wait timed out";
+    case ATTN_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+  }
+  return "unknown status";
+}
+
+void attn_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns = ns ? ns : kDefaultTimeoutNs; }
+
+size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int S, int D) {
+  if (validate_sizes(B, Hq, Hkv, S, D) != ATTN_OK || B == 0 || S == 0) return 0;
+  return bwd_workspace_layout(B, Hq, S).total;
+}
+
+static attn_status_t fwd_impl(const void* q, const void* k, const void* v, void* o, void* o_lo,
+                              float* lse, int B, int Hq, int Hkv, int S, int D, int causal,
+                              float scale, void* stream) {
+  attn_status_t st = validate_sizes(B, Hq, Hkv, S, D);
+  if (st != ATTN_OK) return st;
+  if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (B == 0 || S == 0) return ATTN_OK;
+  if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+      !aligned16(o_lo))
+    return ATTN_ERR_INVALID_ARG;
+  if ((st = check_device()) != ATTN_OK) return st;
+  CUtensorMap tq, tk, tv;
+  if (!make_bshd_map(&tq, q, B, S, Hq, D, FwdCfg<128>::BQ) ||
+      !make_bshd_map(&tk, k, B, S, Hkv, D, FwdCfg<128>::BK) ||
+      !make_bshd_map(&tv, v, B, S, Hkv, D, FwdCfg<128>::BK))
+    return ATTN_ERR_CUDA;
+  int* status = fwd_status_ptr();
+  if (!status) return ATTN_ERR_CUDA;
+  FwdParams p;
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.o_lo = static_cast<__nv_bfloat16*>(o_lo);
+  p.lse = lse;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.S = S;
+  p.G = Hq / Hkv;
+  p.causal = causal ? 1 : 0;
+  p.scale_log2 = scale * kLog2e;
+  p.n_qtiles = (S + FwdCfg<128>::BQ - 1) / FwdCfg<128>::BQ;
+  p.status = status;
+  p.timeout_ns = g_timeout_ns;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return finish(launch_fwd(D, tq, tk, tv, p, s), s, status);
+}
+
+attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                       int Hq, int Hkv, int S, int D, int causal, float scale, void* stream) {
+  return fwd_impl(q, k, v, o, nullptr, lse, B, Hq, Hkv, S, D, causal, scale, stream);
+}
+
+attn_status_t attn_fwd_residual(const void* q, const void* k, const void* v, void* o, void* o_lo,
+                                float* lse, int B, int Hq, int Hkv, int S, int D, int causal,
+                                float scale, void* stream) {
+  if (B > 0 && S > 0 && !o_lo) return ATTN_ERR_INVALID_ARG;
+  return fwd_impl(q, k, v, o, o_lo, lse, B, Hq, Hkv, S, D, causal, scale, stream);
+}
+
+attn_status_t attn_bwd_preprocess(const void* o, const void* o_lo, const void* dO,
+                                  const float* lse, void* dq, int B, int Hq, int Hkv, int S, int D,
+                                  void* workspace, size_t workspace_bytes, void* stream) {
+  attn_status_t st = validate_sizes(B, Hq, Hkv, S, D);
+  if (st != ATTN_OK) return st;
+  if (B == 0 || S == 0) return ATTN_OK;
+  if (!o || !dO || !lse || !dq) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(o) || !aligned16(o_lo) || !aligned16(dO) || !aligned16(lse) || !aligned16(dq))
+    return ATTN_ERR_INVALID_ARG;
+  if ((st = check_workspace(workspace, workspace_bytes, B, Hq, S, D)) != ATTN_OK) return st;
+  if ((st = check_device()) != ATTN_OK) return st;
+  const BwdWorkspace w = bwd_workspace_layout(B, Hq, S);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_bwd_preprocess(
+      static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(o_lo),
+      static_cast<const __nv_bfloat16*>(dO), lse, reinterpret_cast<float*>(ws + w.off_lse2),
+      reinterpret_cast<float*>(ws + w.off_dvec), static_cast<float*>(dq),
+      reinterpret_cast<int*>(ws + w.off_status), B, Hq, S, D, s);
+  return finish(e, s, nullptr);
+}
+
+attn_status_t attn_bwd_main(const void* q, const void* k, const void* v, const void* dO, void* dq,
+                            void* dk, void* dv, int B, int Hq, int Hkv, int S, int D, int causal,
+                            float scale, void* workspace, size_t workspace_bytes, void* stream) {
+  attn_status_t st = validate_sizes(B, Hq, Hkv, S, D);
+  if (st != ATTN_OK) return st;
+  if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (B == 0 || S == 0) return ATTN_OK;
+  if (!q || !k || !v || !dO || !dq || !dk || !dv) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(dq) ||
+      !aligned16(dk) || !aligned16(dv))
+    return ATTN_ERR_INVALID_ARG;
+  if ((st = check_workspace(workspace, workspace_bytes, B, Hq, S, D)) != ATTN_OK) return st;
+  if ((st = check_device()) != ATTN_OK) return st;
+  const BwdWorkspace w = bwd_workspace_layout(B, Hq, S);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const int BQ = BwdCfg<128>::BQ;
+  CUtensorMap tq, tk, tv, tdo, tdq;
+  if (!make_bshd_map(&tq, q, B, S, Hq, D, BQ) || !make_bshd_map(&tdo, dO, B, S, Hq, D, BQ) ||
+      !make_bshd_map(&tk, k, B, S, Hkv, D, 128) || !make_bshd_map(&tv, v, B, S, Hkv, D, 128) ||
+      !make_dq_map(&tdq, dq, B, S, Hq, D))
+    return ATTN_ERR_CUDA;
+  BwdParams p;
+  p.lse2 = reinterpret_cast<const float*>(ws + w.off_lse2);
+  p.dvec = reinterpret_cast<const float*>(ws + w.off_dvec);
+  p.dk = static_cast<float*>(dk);
+  p.dv = static_cast<float*>(dv);
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.S = S;
+  p.S_pad = seq_pad(S);
+  p.G = Hq / Hkv;
+  p.causal = causal ? 1 : 0;
+  p.scale_log2 = scale * kLog2e;
+  p.scale = scale;
+  p.n_ktiles = (S + 127) / 128;
+  p.status = reinterpret_cast<int*>(ws + w.off_status);
+  p.timeout_ns = g_timeout_ns;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return finish(launch_bwd_main(D, tq, tk, tv, tdo, tdq, p, s), s, p.status);
+}
+
+attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                       const float* lse, void* dq, void* dk, void* dv, const void* o_lo, int B,
+                       int Hq, int Hkv, int S, int D, int causal, float scale, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  // Validate everything up front so a failure launches nothing.
+  attn_status_t st = validate_sizes(B, Hq, Hkv, S, D);
+  if (st != ATTN_OK) return st;
+  if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (B == 0 || S == 0) return ATTN_OK;
+  if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) ||
+      !aligned16(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(o_lo))
+    return ATTN_ERR_INVALID_ARG;
+  if ((st = check_workspace(workspace, workspace_bytes, B, Hq, S, D)) != ATTN_OK) return st;
+  if ((st = check_device()) != ATTN_OK) return st;
+  st = attn_bwd_preprocess(o, o_lo, dO, lse, dq, B, Hq, Hkv, S, D, workspace, workspace_bytes,
+                           stream);
+  if (st != ATTN_OK) return st;
+  return attn_bwd_main(q, k, v, dO, dq, dk, dv, B, Hq, Hkv, S, D, causal, scale, workspace,
+                       workspace_bytes, stream);
+}
+
+attn_status_t attn_check_status(void* workspace) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return ATTN_ERR_CUDA;
+  int* fs = fwd_status_ptr();
+  if (!fs) return ATTN_ERR_CUDA;
+  int a = 0, b = 0;
+  if (cudaMemcpy(&a, fs, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (a != 0 && cudaMemset(fs, 0, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (workspace) {
+    if (cudaMemcpy(&b, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    if (b != 0 && cudaMemset(workspace, 0, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
+  }
+  return (a != 0 || b != 0) ? ATTN_ERR_TIMEOUT : ATTN_OK;
+}
+
+}  // extern "C"

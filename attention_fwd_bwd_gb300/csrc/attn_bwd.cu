@@ -1,0 +1,490 @@
+// Backward attention kernels for sm_103a: the exact gradient of
+// O = softmax(scale * Q K^T) V ("Scheduling Data to Compute: Hierarchical Data
+// Pipelining for LLM Training on AMD GPUs", section 2.1, Eq. (1)) for the loss
+// L = sum(dO * O). With P = exp(scale * Q K^T - LSE):
+//   dV = P^T dO,  dP = dO V^T,  Dvec_i = rowsum(dO * O)_i,  dS = P * (dP - Dvec),
+//   dK = scale * dS^T Q,  dQ = scale * dS K.
+// The paper's Table 3 lists the scores, query-gradient and key-gradient
+// products with their transposed operands; here every transposed operand is a
+// shared-memory descriptor in MN-major form, so no tile is ever transposed.
+//
+// Two kernels run in order on one stream:
+//   1. preprocess: Dvec (from o, plus the forward's low-order residual o_lo
+//      when given) and log2-scaled LSE rows into the workspace; the fp32 dq
+//      output zeroed (HBM-bound).
+//   2. main: one CTA per (batch, kv head, 128-key tile). K_j and V_j stay in
+//      shared memory while Q_i, dO_i, LSE_i and Dvec_i of every 64-row query
+//      tile of the group's query heads stream through a two-stage TMA ring:
+//        S^T = K_j Q_i^T and dP^T = V_j dO_i^T         (TMEM)
+//        P^T (TMEM) and scale * dS^T (shared memory) as bf16 hi/lo pairs
+//        dV += P^T dO_i, dK += dS^T Q_i                 (TMEM, whole loop)
+//        dQ_i^T = K_j^T dS^T                            (TMEM)
+//      The dQ tile is drained by warps 8-11 into shared memory and added into
+//      dq with an asynchronous TMA tensor reduction (fp32 add in L2).
+#include "attn_common.cuh"
+#include "sm100_ptx.cuh"
+
+namespace attn {
+using namespace ptx;
+
+namespace {
+
+// ------------------------------------------------------------------ preprocess
+__global__ void __launch_bounds__(256) attn_bwd_preprocess_kernel(
+    const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ o_lo,
+    const __nv_bfloat16* __restrict__ dO, const float* __restrict__ lse, float* __restrict__ lse2,
+    float* __restrict__ dvec, float4* __restrict__ dq, int* __restrict__ status, int B, int Hq,
+    int S, int S_pad, int D) {
+  if (blockIdx.x == 0 && threadIdx.x == 0) *status = 0;  // status word of the main kernel
+  const int tpr = D / 8;  // threads per row, 8 bf16 (16 bytes) each
+  const int rows_per_warp = 32 / tpr;
+  const long long nrows = static_cast<long long>(B) * S * Hq;
+  const long long gthreads = static_cast<long long>(gridDim.x) * blockDim.x;
+  const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long gwarp = tid / 32, nwarps = gthreads / 32;
+  const int lane = threadIdx.x % 32;
+  const int sub = lane % tpr;
+  // Rows in [B, S, Hq] order, so a warp reads consecutive memory. The loop
+  // condition is warp-uniform so the shuffles below see the whole warp.
+  for (long long base = gwarp * rows_per_warp; base < nrows; base += nwarps * rows_per_warp) {
+    const long long row = base + lane / tpr;
+    const bool valid = row < nrows;
+    float acc = 0.f;
+    if (valid) {
+      const uint4 a = reinterpret_cast<const uint4*>(o + row * D)[sub];
+      const uint4 c = reinterpret_cast<const uint4*>(dO + row * D)[sub];
+      uint4 r = make_uint4(0u, 0u, 0u, 0u);
+      if (o_lo) r = reinterpret_cast<const uint4*>(o_lo + row * D)[sub];
+      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+      const __nv_bfloat162* c2 = reinterpret_cast<const __nv_bfloat162*>(&c);
+      const __nv_bfloat162* r2 = reinterpret_cast<const __nv_bfloat162*>(&r);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 fa = __bfloat1622float2(a2[i]);
+        const float2 fr = __bfloat1622float2(r2[i]);
+        const float2 fc = __bfloat1622float2(c2[i]);
+        acc = fmaf(fa.x + fr.x, fc.x, acc);
+        acc = fmaf(fa.y + fr.y, fc.y, acc);
+      }
+    }
+    for (int off = tpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (valid && sub == 0) {
+      const int h = static_cast<int>(row % Hq);
+      const long long bs = row / Hq;
+      const int s = static_cast<int>(bs % S);
+      const int b = static_cast<int>(bs / S);
+      const long long bh = static_cast<long long>(b) * Hq + h;
+      dvec[bh * S_pad + s] = acc;
+      lse2[bh * S_pad + s] = lse[bh * S + s] * kLog2e;
+    }
+  }
+  // Padding rows S..S_pad-1 of every (b, h): probability 0 (lse2 = +inf), Dvec 0.
+  const long long npad = static_cast<long long>(B) * Hq * (S_pad - S);
+  for (long long i = tid; i < npad; i += gthreads) {
+    const long long bh = i / (S_pad - S);
+    const int s = S + static_cast<int>(i % (S_pad - S));
+    dvec[bh * S_pad + s] = 0.f;
+    lse2[bh * S_pad + s] = INFINITY;
+  }
+  // dq is accumulated by reductions in the main kernel.
+  const long long n4 = nrows * D / 4;
+  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (long long i = tid; i < n4; i += gthreads) dq[i] = z;
+}
+
+// ------------------------------------------------------------------ main
+// Adds a [rows x D] fp32 box from shared memory into the 4-D (D, H, S, B) map.
+__device__ __forceinline__ void tma_reduce_add_4d(const CUtensorMap* m, int c0, int c1, int c2,
+                                                  int c3, uint32_t src) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.4d.global.shared::cta.add.tile.bulk_group"
+      " [%0, {%1, %2, %3, %4}], [%5];" ::"l"(reinterpret_cast<uint64_t>(m)),
+      "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(src)
+      : "memory");
+}
+
+// Writes 16 bytes to unit `u` (0..7) of 128-byte row `row` of a tile stored
+// with 128-byte swizzle (8-row atoms on 1024-byte boundaries).
+__device__ __forceinline__ void st_sw128(uint32_t tile, int row, int u, uint4 v) {
+  const uint32_t addr = tile + row * 128 + ((u ^ (row & 7)) << 4);
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// x as a pair of bf16 values hi + lo with hi = bf16(x), lo = bf16(x - hi).
+__device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  hi = pack_bf16x2(x0, x1);
+  const float h0 = __uint_as_float(hi << 16);
+  const float h1 = __uint_as_float(hi & 0xFFFF0000u);
+  lo = pack_bf16x2(x0 - h0, x1 - h1);
+}
+
+template <int D>
+__global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
+    attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q,
+                         const __grid_constant__ CUtensorMap tm_k,
+                         const __grid_constant__ CUtensorMap tm_v,
+                         const __grid_constant__ CUtensorMap tm_do,
+                         const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
+  using C = BwdCfg<D>;
+  constexpr int BQ = C::BQ, BK = C::BK, ST = C::STAGES;
+  constexpr int HALF = BQ / 2;  // query columns per compute warpgroup
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+
+  __shared__ uint64_t bar_kv_full, bar_mma_done;
+  __shared__ uint64_t bar_st_full[ST], bar_st_empty[ST];
+  __shared__ uint64_t bar_sdp_full, bar_sdp_free, bar_pds_full, bar_pds_free, bar_dq_full,
+      bar_dq_free;
+  __shared__ uint32_t tmem_base_s;
+  __shared__ int abort_flag;
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const int bg = blockIdx.x;  // b * Hkv + g
+  const int g = bg % p.Hkv;
+  const int b = bg / p.Hkv;
+  const int j = blockIdx.y;   // key tile; j = 0 has the most causal work
+  const int k0 = j * BK;
+  const int nq = (p.S + BQ - 1) / BQ;
+  const int i_start = p.causal ? (k0 / BQ) : 0;
+  const int niq = nq - i_start;
+  const int n_it = p.G * niq;
+
+  const uint32_t sK = smem_u32(smem + C::SMEM_K);
+  const uint32_t sV = smem_u32(smem + C::SMEM_V);
+  const uint32_t sStage = smem_u32(smem + C::SMEM_STAGE);
+  const uint32_t sDsHi = smem_u32(smem + C::SMEM_DS_HI);
+  const uint32_t sDsLo = smem_u32(smem + C::SMEM_DS_LO);
+  const uint32_t sDQS = smem_u32(smem + C::SMEM_DQS);
+
+  if (D == 64) {
+    // Rows 64..127 of K^T (the second 64-column chunk of K) are zero, so the
+    // M = 128 dQ^T product carries zeros in its unused upper half.
+    uint4* z = reinterpret_cast<uint4*>(smem + C::SMEM_K + BK * 128);
+    for (int i = threadIdx.x; i < BK * 128 / 16; i += blockDim.x) z[i] = make_uint4(0u, 0u, 0u, 0u);
+    fence_async_smem();
+  }
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(smem_u32(&bar_kv_full), 1);
+    mbar_init(smem_u32(&bar_mma_done), 1);
+    for (int s = 0; s < ST; ++s) {
+      mbar_init(smem_u32(&bar_st_full[s]), 1);
+      mbar_init(smem_u32(&bar_st_empty[s]), 1);
+    }
+    mbar_init(smem_u32(&bar_sdp_full), 1);
+    mbar_init(smem_u32(&bar_sdp_free), 256);
+    mbar_init(smem_u32(&bar_pds_full), 256);
+    mbar_init(smem_u32(&bar_pds_free), 1);
+    mbar_init(smem_u32(&bar_dq_full), 1);
+    mbar_init(smem_u32(&bar_dq_free), 128);
+    fence_barrier_init();
+  }
+  if (warp == 13) {
+    tmem_alloc(smem_u32(&tmem_base_s), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_s;
+  const WaitCtl ctl{&abort_flag, p.status, p.timeout_ns};
+
+  auto stage_q = [&](int s) { return sStage + s * C::STAGE_BYTES; };
+  auto stage_do = [&](int s) { return sStage + s * C::STAGE_BYTES + C::Q_BYTES; };
+  auto stage_rows = [&](int s) {  // lse2 then dvec, BQ floats each
+    return reinterpret_cast<const float*>(smem + C::SMEM_STAGE + s * C::STAGE_BYTES +
+                                          2 * C::Q_BYTES);
+  };
+
+  if (warp == 12) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&tm_q);
+      prefetch_tmap(&tm_k);
+      prefetch_tmap(&tm_v);
+      prefetch_tmap(&tm_do);
+      mbar_arrive_expect_tx(smem_u32(&bar_kv_full), 2 * C::V_BYTES);
+      for (int c = 0; c < C::KCH; ++c) {
+        tma_load_4d(sK + c * (BK * 128), &tm_k, smem_u32(&bar_kv_full), c * 64, g, k0, b);
+        tma_load_4d(sV + c * (BK * 128), &tm_v, smem_u32(&bar_kv_full), c * 64, g, k0, b);
+      }
+      bool ok = true;
+      int issued = 0;
+      for (int it = 0; it < n_it; ++it) {
+        const int s = it % ST, round = it / ST;
+        if (round > 0) ok = mbar_wait(smem_u32(&bar_st_empty[s]), (round - 1) & 1, ctl);
+        if (!ok) break;
+        const int h = g * p.G + it / niq;
+        const int q0 = (i_start + it % niq) * BQ;
+        const uint32_t full = smem_u32(&bar_st_full[s]);
+        mbar_arrive_expect_tx(full, 2 * C::Q_BYTES + 2 * C::ROWVEC_BYTES);
+        for (int c = 0; c < C::KCH; ++c) {
+          tma_load_4d(stage_q(s) + c * (BQ * 128), &tm_q, full, c * 64, h, q0, b);
+          tma_load_4d(stage_do(s) + c * (BQ * 128), &tm_do, full, c * 64, h, q0, b);
+        }
+        const size_t rowoff = (static_cast<size_t>(b) * p.Hq + h) * p.S_pad + q0;
+        bulk_load(stage_do(s) + C::Q_BYTES, p.lse2 + rowoff, C::ROWVEC_BYTES, full);
+        bulk_load(stage_do(s) + C::Q_BYTES + C::ROWVEC_BYTES, p.dvec + rowoff, C::ROWVEC_BYTES,
+                  full);
+        issued = it + 1;
+      }
+      if (!ok) {
+        for (int it = max(0, issued - ST); it < issued; ++it)
+          mbar_wait_drain(smem_u32(&bar_st_full[it % ST]), (it / ST) & 1, 50000000ull);
+      }
+      mbar_wait_drain(smem_u32(&bar_kv_full), 0, 50000000ull);
+    }
+  } else if (warp == 13) {
+    // ------------------------------------------------------------ MMA issuer
+    bool ok = mbar_wait_warp(smem_u32(&bar_kv_full), 0, ctl);
+    if (lane == 0 && ok) {
+      constexpr uint32_t idesc_sdp = idesc_bf16_f32(128, BQ, 0, 0);
+      constexpr uint32_t idesc_kv = idesc_bf16_f32(128, D, 0, 1);
+      constexpr uint32_t idesc_dq = idesc_bf16_f32(128, BQ, 1, 1);
+      auto issue_sdp = [&](int s) {
+        const uint32_t sq = stage_q(s), sdo = stage_do(s);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t ka = (kk >> 2) * (BK * 128) + (kk & 3) * 32;
+          const uint32_t kb = (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
+          mma_ss(tmem + C::TM_ST, sw128_desc(sK + ka, 16, 1024), sw128_desc(sq + kb, 16, 1024),
+                 idesc_sdp, kk > 0);
+          mma_ss(tmem + C::TM_DPT, sw128_desc(sV + ka, 16, 1024), sw128_desc(sdo + kb, 16, 1024),
+                 idesc_sdp, kk > 0);
+        }
+        mma_commit(smem_u32(&bar_sdp_full));
+      };
+      if (n_it > 0) {
+        ok = mbar_wait(smem_u32(&bar_st_full[0]), 0, ctl);
+        if (ok) {
+          tc_fence_after();
+          issue_sdp(0);
+        }
+      }
+      for (int it = 0; it < n_it && ok; ++it) {
+        const int s = it % ST;
+        if (it + 1 < n_it) {
+          const int s1 = (it + 1) % ST;
+          ok = mbar_wait(smem_u32(&bar_st_full[s1]), ((it + 1) / ST) & 1, ctl);
+          if (ok) ok = mbar_wait(smem_u32(&bar_sdp_free), it & 1, ctl);
+          if (!ok) break;
+          tc_fence_after();
+          issue_sdp(s1);
+        }
+        ok = mbar_wait(smem_u32(&bar_pds_full), it & 1, ctl);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t sq = stage_q(s), sdo = stage_do(s);
+        // dV += (P_hi + P_lo)^T dO_i  (A from TMEM: 16 query columns = 8 TMEM columns a step)
+        // dK += (dS_hi + dS_lo)^T Q_i
+#pragma unroll
+        for (int kk = 0; kk < BQ / 16; ++kk) {
+          const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
+          const uint64_t bdo = sw128_desc(sdo + kk * 2048, BQ * 128, 1024);
+          const uint64_t bq = sw128_desc(sq + kk * 2048, BQ * 128, 1024);
+          mma_ts(tmem + C::TM_DV, tmem + C::TM_P_HI + kk * 8, bdo, idesc_kv, acc);
+          mma_ts(tmem + C::TM_DV, tmem + C::TM_P_LO + kk * 8, bdo, idesc_kv, 1u);
+          mma_ss(tmem + C::TM_DK, sw128_desc(sDsHi + kk * 32, 16, 1024), bq, idesc_kv, acc);
+          mma_ss(tmem + C::TM_DK, sw128_desc(sDsLo + kk * 32, 16, 1024), bq, idesc_kv, 1u);
+        }
+        if (it >= 1) {
+          ok = mbar_wait(smem_u32(&bar_dq_free), (it - 1) & 1, ctl);
+          if (!ok) break;
+          tc_fence_after();
+        }
+        // dQ^T[d][q] = sum over keys of K[key][d] (dS_hi + dS_lo)^T[key][q]
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk) {
+          const uint64_t ak = sw128_desc(sK + kk * 2048, BK * 128, 1024);
+          mma_ss(tmem + C::TM_DQ, ak, sw128_desc(sDsHi + kk * 2048, BK * 128, 1024), idesc_dq,
+                 kk > 0);
+          mma_ss(tmem + C::TM_DQ, ak, sw128_desc(sDsLo + kk * 2048, BK * 128, 1024), idesc_dq,
+                 1u);
+        }
+        mma_commit(smem_u32(&bar_dq_full));
+        mma_commit(smem_u32(&bar_pds_free));
+        mma_commit(smem_u32(&bar_st_empty[s]));
+      }
+      mma_commit(smem_u32(&bar_mma_done));
+      if (!ok) mbar_wait_drain(smem_u32(&bar_mma_done), 0, 50000000ull);
+    }
+    __syncwarp();
+  } else if (warp < 8) {
+    // ------------------------------------------------------------ P^T / dS^T warps 0-7
+    const int r = threadIdx.x % 128;  // key row within the tile == TMEM lane
+    const int cg = warp / 4;          // query-column half
+    const int key = k0 + r;
+    const uint32_t lane_base = static_cast<uint32_t>((warp % 4) * 32) << 16;
+    const bool key_valid = key < p.S;
+    bool ok = true;
+    for (int it = 0; it < n_it; ++it) {
+      const int s = it % ST;
+      const int q0 = (i_start + it % niq) * BQ;
+      ok = mbar_wait_warp(smem_u32(&bar_sdp_full), it & 1, ctl);
+      if (ok) ok = mbar_wait_warp(smem_u32(&bar_st_full[s]), (it / ST) & 1, ctl);
+      if (!ok) break;
+      tc_fence_after();
+      const float* lse2 = stage_rows(s);
+      const float* dvec = lse2 + BQ;
+      const bool need_mask = p.causal && (q0 < k0 + BK - 1);
+      uint32_t us[HALF], ud[HALF];
+      tmem_ld32(tmem + lane_base + C::TM_ST + cg * HALF, us);
+      tmem_ld32(tmem + lane_base + C::TM_DPT + cg * HALF, ud);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&bar_sdp_free));
+      uint32_t ph[HALF / 2], pl[HALF / 2], dh[HALF / 2], dl[HALF / 2];
+#pragma unroll
+      for (int c = 0; c < HALF; c += 2) {
+        float pr[2], dr[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int col = cg * HALF + c + e;
+          float pv = ex2(fmaf(__uint_as_float(us[c + e]), p.scale_log2, -lse2[col]));
+          if (!key_valid || (need_mask && key > q0 + col)) pv = 0.f;
+          pr[e] = pv;
+          dr[e] = p.scale * pv * (__uint_as_float(ud[c + e]) - dvec[col]);
+        }
+        split_bf16x2(pr[0], pr[1], ph[c / 2], pl[c / 2]);
+        split_bf16x2(dr[0], dr[1], dh[c / 2], dl[c / 2]);
+      }
+      // The MMAs of the previous tile must be done with P (TMEM) and dS (smem).
+      if (it >= 1) {
+        ok = mbar_wait_warp(smem_u32(&bar_pds_free), (it - 1) & 1, ctl);
+        if (!ok) break;
+      }
+      tmem_st16(tmem + lane_base + C::TM_P_HI + cg * (HALF / 2), ph);
+      tmem_st16(tmem + lane_base + C::TM_P_LO + cg * (HALF / 2), pl);
+      // Row r of dS^T, K-major with 128-byte swizzle: 64 query columns per
+      // 128-byte row, 8 per 16-byte unit; this half owns units cg*4..cg*4+3.
+#pragma unroll
+      for (int u = 0; u < HALF / 8; ++u) {
+        const int unit = cg * (HALF / 8) + u;
+        st_sw128(sDsHi, r, unit, make_uint4(dh[u * 4], dh[u * 4 + 1], dh[u * 4 + 2], dh[u * 4 + 3]));
+        st_sw128(sDsLo, r, unit, make_uint4(dl[u * 4], dl[u * 4 + 1], dl[u * 4 + 2], dl[u * 4 + 3]));
+      }
+      tmem_wait_st();
+      fence_async_smem();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&bar_pds_full));
+    }
+    if (ok) ok = mbar_wait_warp(smem_u32(&bar_mma_done), 0, ctl);
+    if (ok) {
+      tc_fence_after();
+      // dK and dV rows in fp32; this warpgroup stores columns [cg*D/2, (cg+1)*D/2).
+      const size_t rowoff = ((static_cast<size_t>(b) * p.S + key) * p.Hkv + g) * D;
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        const uint32_t col0 = (t == 0 ? C::TM_DK : C::TM_DV) + cg * (D / 2);
+        float* dst = (t == 0 ? p.dk : p.dv) + rowoff + cg * (D / 2);
+#pragma unroll
+        for (int c = 0; c < D / 2; c += 32) {
+          uint32_t u[32];
+          tmem_ld32(tmem + lane_base + col0 + c, u);
+          tmem_wait_ld();
+          if (key_valid) {
+            float4* d4 = reinterpret_cast<float4*>(dst + c);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              d4[i] = make_float4(__uint_as_float(u[4 * i]), __uint_as_float(u[4 * i + 1]),
+                                  __uint_as_float(u[4 * i + 2]), __uint_as_float(u[4 * i + 3]));
+          }
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ dQ drain warps 8-11
+    const int t = threadIdx.x - 256;  // TMEM lane = head-dim index d of dQ^T
+    const uint32_t lane_base = static_cast<uint32_t>((warp % 4) * 32) << 16;
+    float* stg = reinterpret_cast<float*>(smem + C::SMEM_DQS);
+    bool ok = true;
+    for (int it = 0; it < n_it; ++it) {
+      const int h = g * p.G + it / niq;
+      const int q0 = (i_start + it % niq) * BQ;
+      ok = mbar_wait_warp(smem_u32(&bar_dq_full), it & 1, ctl);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t u[BQ];
+      tmem_ld32(tmem + lane_base + C::TM_DQ, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
+      tmem_ld32(tmem + lane_base + C::TM_DQ + 32, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&bar_dq_free));
+      if (t == 0) bulk_wait_read_all();  // the previous reduction has read the staging tile
+      named_bar_sync(1, 128);
+      if (t < D) {
+        // staging [q][d] fp32, row-major (the TMA box layout); lane t holds column d = t.
+#pragma unroll
+        for (int q = 0; q < BQ; ++q) stg[q * D + t] = __uint_as_float(u[q]);
+      }
+      fence_async_smem();
+      named_bar_sync(1, 128);
+      if (t == 0) {
+        tma_reduce_add_4d(&tm_dq, 0, h, q0, b, sDQS);
+        bulk_commit_group();
+      }
+    }
+    if (t == 0) bulk_wait_all();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 13) tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+template <int D>
+cudaError_t launch_bwd_main_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                              const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p,
+                              cudaStream_t stream) {
+  using C = BwdCfg<D>;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(attn_bwd_main_kernel<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM_ALLOC);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  dim3 grid(p.B * p.Hkv, p.n_ktiles);
+  attn_bwd_main_kernel<D><<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(tq, tk, tv, tdo, tdq, p);
+  return cudaGetLastError();
+}
+
+int grid_for(long long work_items) {
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  long long blocks = (work_items + 255) / 256;
+  const long long cap = static_cast<long long>(sms) * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  return static_cast<int>(blocks);
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_preprocess(const __nv_bfloat16* o, const __nv_bfloat16* o_lo,
+                                  const __nv_bfloat16* dO, const float* lse, float* lse2,
+                                  float* dvec, float* dq, int* status, int B, int Hq, int S,
+                                  int D, cudaStream_t stream) {
+  const int S_pad = seq_pad(S);
+  const long long work = static_cast<long long>(B) * Hq * S * D / 4;
+  attn_bwd_preprocess_kernel<<<grid_for(work), 256, 0, stream>>>(
+      o, o_lo, dO, lse, lse2, dvec, reinterpret_cast<float4*>(dq), status, B, Hq, S, S_pad, D);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_main(int D, const CUtensorMap& tq, const CUtensorMap& tk,
+                            const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
+                            const BwdParams& p, cudaStream_t stream) {
+  if (D == 128) return launch_bwd_main_t<128>(tq, tk, tv, tdo, tdq, p, stream);
+  return launch_bwd_main_t<64>(tq, tk, tv, tdo, tdq, p, stream);
+}
+
+}  // namespace attn

@@ -1,0 +1,148 @@
+// Shared definitions of the attention kernels: tile shapes, shared-memory and
+// tensor-memory plans, kernel parameter blocks, and the host-side launchers
+// the C ABI calls.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace attn {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Rows of a tile in the sequence dimension are padded up to this multiple in
+// the backward workspace arrays (Dvec, log2-scaled LSE, dQ accumulator).
+constexpr int kSeqPad = 128;
+__host__ __device__ constexpr int seq_pad(int S) { return (S + kSeqPad - 1) / kSeqPad * kSeqPad; }
+
+// ---------------------------------------------------------------- forward
+// One CTA per (batch, query head, 128-row query tile); K/V tiles of 128 keys
+// stream through a ring of shared-memory slots (K_j and V_j take one slot
+// each). Warps 0-3: softmax / rescale / epilogue (one query row per thread,
+// the row's TMEM lane); warp 4: TMA producer; warp 5: MMA issuer.
+template <int D>
+struct FwdCfg {
+  static constexpr int BQ = 128;
+  static constexpr int BK = 128;
+  static constexpr int KCH = D / 64;                 // 64-wide (128-byte) column chunks
+  static constexpr int Q_BYTES = BQ * D * 2;
+  static constexpr int KV_BYTES = BK * D * 2;        // one K or V tile
+  static constexpr int NSLOT = (D == 128) ? 5 : 8;   // ring slots
+  static constexpr int SMEM_Q = 0;
+  static constexpr int SMEM_RING = Q_BYTES;
+  static constexpr int SMEM_BYTES = Q_BYTES + NSLOT * KV_BYTES;
+  static constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;  // slack for 1024-byte alignment
+  // Tensor-memory columns (fp32 unless noted).
+  static constexpr int TM_S0 = 0;      // scores, buffer 0 (128 cols)
+  static constexpr int TM_S1 = 128;    // scores, buffer 1
+  static constexpr int TM_O = 256;     // output accumulator (D cols)
+  static constexpr int TM_P0 = 384;    // bf16 probabilities, buffer 0 (64 cols)
+  static constexpr int TM_P1 = 448;    // buffer 1
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int THREADS = 192;
+};
+
+struct FwdParams {
+  __nv_bfloat16* o;
+  __nv_bfloat16* o_lo;  // optional: bf16(O - o), the part of O that bf16 o drops
+  float* lse;
+  int B, Hq, Hkv, S, G;
+  int causal;
+  float scale_log2;  // scale * log2(e)
+  int n_qtiles;
+  int* status;
+  unsigned long long timeout_ns;
+};
+
+// ---------------------------------------------------------------- backward
+// One CTA per (batch, kv head, 128-key tile): K_j and V_j stay resident, the
+// group's query heads and their 64-row query tiles stream through a two-stage
+// ring holding Q_i, dO_i and the rows' log2-scaled LSE and Dvec. dK_j and dV_j
+// accumulate in TMEM over the whole loop; dQ tiles are added into the fp32
+// dq output with TMA tensor reductions.
+// Warps 0-7: P^T / dS^T and the dK/dV epilogue (one key row per thread; warps
+// w and w+4 share TMEM lanes and split the 64 query columns); warps 8-11: dQ
+// drain; warp 12: TMA producer; warp 13: MMA issuer.
+//
+// P and dS enter the gradient MMAs as a pair of bf16 values (hi = bf16(x),
+// lo = bf16(x - hi)), i.e. with about 16 significant bits: dV += P_hi^T dO +
+// P_lo^T dO and likewise for dK and dQ. dQ is produced transposed
+// (dQ^T = K_j^T dS^T, M = 128 head-dim rows) so every MMA has M = 128; for
+// D = 64 the upper 64 rows of K^T are zero in shared memory and ignored.
+template <int D>
+struct BwdCfg {
+  static constexpr int BK = 128;
+  static constexpr int BQ = 64;
+  static constexpr int KCH = D / 64;
+  static constexpr int K_BYTES = BK * 128 * 2;       // always two 64-column chunks
+  static constexpr int V_BYTES = BK * D * 2;
+  static constexpr int Q_BYTES = BQ * D * 2;
+  static constexpr int STAGES = 2;
+  static constexpr int ROWVEC_BYTES = BQ * 4;
+  static constexpr int STAGE_BYTES = ((2 * Q_BYTES + 2 * ROWVEC_BYTES) + 1023) / 1024 * 1024;
+  static constexpr int DS_BYTES = BK * BQ * 2;       // one bf16 dS^T tile (hi or lo)
+  static constexpr int DQS_BYTES = BQ * D * 4;       // dQ staging tile, fp32
+  static constexpr int SMEM_K = 0;
+  static constexpr int SMEM_V = SMEM_K + K_BYTES;
+  static constexpr int SMEM_STAGE = SMEM_V + V_BYTES;
+  static constexpr int SMEM_DS_HI = SMEM_STAGE + STAGES * STAGE_BYTES;
+  static constexpr int SMEM_DS_LO = SMEM_DS_HI + DS_BYTES;
+  static constexpr int SMEM_DQS = SMEM_DS_LO + DS_BYTES;
+  static constexpr int SMEM_BYTES = SMEM_DQS + DQS_BYTES;
+  static constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;
+  // Tensor-memory columns.
+  static constexpr int TM_ST = 0;      // S^T  fp32 (64 cols)
+  static constexpr int TM_DPT = 64;    // dP^T fp32 (64 cols)
+  static constexpr int TM_DV = 128;    // dV   fp32 (D cols)
+  static constexpr int TM_DK = 256;    // dK   fp32 (D cols)
+  static constexpr int TM_DQ = 384;    // dQ^T fp32 (64 cols)
+  static constexpr int TM_P_HI = 448;  // P^T hi, bf16 pairs (32 cols)
+  static constexpr int TM_P_LO = 480;  // P^T lo, bf16 pairs (32 cols)
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int THREADS = 448;
+  static_assert(SMEM_ALLOC <= 232448, "shared-memory plan exceeds 227 KB");
+};
+
+struct BwdParams {
+  const float* lse2;   // [B, Hq, S_pad] lse * log2(e); +inf on padding rows
+  const float* dvec;   // [B, Hq, S_pad] rowsum(dO * O); 0 on padding rows
+  float* dk;           // [B, S, Hkv, D] fp32
+  float* dv;           // [B, S, Hkv, D] fp32
+  int B, Hq, Hkv, S, S_pad, G;
+  int causal;
+  float scale_log2;
+  float scale;
+  int n_ktiles;
+  int* status;
+  unsigned long long timeout_ns;
+};
+
+// Workspace layout of the backward pass (all offsets 256-byte aligned).
+struct BwdWorkspace {
+  size_t off_status, off_lse2, off_dvec, total;
+};
+inline BwdWorkspace bwd_workspace_layout(int B, int Hq, int S) {
+  auto al = [](size_t x) { return (x + 255) / 256 * 256; };
+  BwdWorkspace w;
+  const size_t rows = static_cast<size_t>(B) * Hq * seq_pad(S);
+  w.off_status = 0;
+  w.off_lse2 = 256;
+  w.off_dvec = w.off_lse2 + al(rows * 4);
+  w.total = w.off_dvec + al(rows * 4);
+  return w;
+}
+
+// ---------------------------------------------------------------- launchers
+cudaError_t launch_fwd(int D, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const FwdParams& p, cudaStream_t stream);
+cudaError_t launch_bwd_preprocess(const __nv_bfloat16* o, const __nv_bfloat16* o_lo,
+                                  const __nv_bfloat16* dO, const float* lse, float* lse2,
+                                  float* dvec, float* dq, int* status, int B, int Hq, int S,
+                                  int D, cudaStream_t stream);
+cudaError_t launch_bwd_main(int D, const CUtensorMap& tq, const CUtensorMap& tk,
+                            const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
+                            const BwdParams& p, cudaStream_t stream);
+
+}  // namespace attn

@@ -1,0 +1,357 @@
+// Forward attention kernel for sm_103a: O = softmax(scale * Q K^T) V and the
+// row log-sum-exp, per (batch, query head) -- "Scheduling Data to Compute:
+// Hierarchical Data Pipelining for LLM Training on AMD GPUs", section 2.1,
+// Eq. (1), computed as that section's Algorithm 0 describes (K/V tiles stream
+// through on-chip memory, online softmax, output accumulator kept on chip),
+// with the query-tile loop outside and the key/value loop inside so the state
+// never leaves the SM.
+//
+// Per CTA (one 128-row query tile of one head):
+//   warp 4 (TMA producer): Q once, then K_0, V_0, K_1, V_1, ... into a ring of
+//       shared-memory slots, each slot guarded by a full/empty mbarrier pair
+//       (the GB300 counterpart of the paper's "issue N+1 loads, wait until at
+//       most N are outstanding" rule for its Tensor Data Mover, section 3.1.1).
+//   warp 5 (MMA issuer): S_j = Q K_j^T into one of two TMEM score buffers
+//       (both operands K-major, so K^T needs no transpose -- Table 3's first
+//       row), then O += P_j V_j with P read from TMEM and V_j described
+//       MN-major (the transposed-operand case of section 3.1.2, handled by
+//       the descriptor instead of a transpose).
+//   warps 0-3 (softmax): thread r owns query row r (TMEM lane r); it reads its
+//       score row, updates the running max m and sum l, writes bf16 P to TMEM
+//       and, when m grew by more than 2^8, rescales its O row in TMEM first.
+//       The final m and l give O = acc / l and LSE = (m + log2 l) ln 2.
+// When the caller asks for the output residual o_lo = bf16(O - o) (training,
+// where the backward needs rowsum(dO * O) beyond bf16 accuracy), P also goes
+// through a second MMA as its low-order bf16 part, O += P_lo V_j.
+#include "attn_common.cuh"
+#include "sm100_ptx.cuh"
+
+namespace attn {
+using namespace ptx;
+
+namespace {
+
+// Rescale threshold in log2 units: the running max used for exponentiation
+// only moves when the true max exceeds it by more than this, which keeps every
+// p <= 2^8 and leaves the result exact after the final division by l.
+constexpr float kRescaleThreshold = 8.0f;
+
+template <int D>
+__global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+  using C = FwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+
+  __shared__ uint64_t bar_q_full;
+  __shared__ uint64_t bar_kv_full[C::NSLOT], bar_kv_empty[C::NSLOT];
+  __shared__ uint64_t bar_s_full[2], bar_p_full[2], bar_pv_done[2];
+  __shared__ uint32_t tmem_base_s;
+  __shared__ int abort_flag;
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+
+  const int bh = blockIdx.x;  // b * Hq + hq
+  const int hq = bh % p.Hq;
+  const int b = bh / p.Hq;
+  const int g = hq / p.G;
+  const int qt = p.n_qtiles - 1 - static_cast<int>(blockIdx.y);  // longest causal rows first
+  const int q0 = qt * C::BQ;
+  const int nkv_all = (p.S + C::BK - 1) / C::BK;
+  const int n_kv = p.causal ? min(qt + 1, nkv_all) : nkv_all;
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(smem_u32(&bar_q_full), 1);
+    for (int i = 0; i < C::NSLOT; ++i) {
+      mbar_init(smem_u32(&bar_kv_full[i]), 1);
+      mbar_init(smem_u32(&bar_kv_empty[i]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&bar_s_full[i]), 1);
+      mbar_init(smem_u32(&bar_p_full[i]), 128);
+      mbar_init(smem_u32(&bar_pv_done[i]), 1);
+    }
+    fence_barrier_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(&tmem_base_s), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_s;
+  const WaitCtl ctl{&abort_flag, p.status, p.timeout_ns};
+  // With the residual output requested, P enters O += P V as a bf16 hi/lo
+  // pair, so O (and o + o_lo) carries about 16 significant bits.
+  const bool split = p.o_lo != nullptr;
+
+  const uint32_t sQ = smem_u32(smem + C::SMEM_Q);
+  const uint32_t sRing = smem_u32(smem + C::SMEM_RING);
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&tm_q);
+      prefetch_tmap(&tm_k);
+      prefetch_tmap(&tm_v);
+      const uint64_t keep = policy_evict_last();  // K/V tiles are re-read by G heads x tiles
+      mbar_arrive_expect_tx(smem_u32(&bar_q_full), C::Q_BYTES);
+      for (int c = 0; c < C::KCH; ++c)
+        tma_load_4d(sQ + c * (C::BQ * 128), &tm_q, smem_u32(&bar_q_full), c * 64, hq, q0, b);
+      int issued = 0;
+      bool ok = true;
+      for (int idx = 0; idx < 2 * n_kv && ok; ++idx) {
+        const int slot = idx % C::NSLOT, round = idx / C::NSLOT;
+        if (round > 0) ok = mbar_wait(smem_u32(&bar_kv_empty[slot]), (round - 1) & 1, ctl);
+        if (!ok) break;
+        const uint32_t full = smem_u32(&bar_kv_full[slot]);
+        const uint32_t dst = sRing + slot * C::KV_BYTES;
+        const CUtensorMap* m = (idx & 1) ? &tm_v : &tm_k;
+        mbar_arrive_expect_tx(full, C::KV_BYTES);
+        for (int c = 0; c < C::KCH; ++c)
+          tma_load_4d_hint(dst + c * (C::BK * 128), m, full, c * 64, g, (idx >> 1) * C::BK, b,
+                           keep);
+        issued = idx + 1;
+      }
+      if (!ok) {
+        // Let in-flight copies land before the CTA's shared memory goes away.
+        for (int idx = max(0, issued - C::NSLOT); idx < issued; ++idx)
+          mbar_wait_drain(smem_u32(&bar_kv_full[idx % C::NSLOT]), (idx / C::NSLOT) & 1,
+                          50000000ull);
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    bool ok = mbar_wait_warp(smem_u32(&bar_q_full), 0, ctl);
+    if (lane == 0 && ok) {
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
+      constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, 0, 1);
+      for (int j = 0; j <= n_kv && ok; ++j) {
+        if (j < n_kv) {
+          const int idx = 2 * j, slot = idx % C::NSLOT;
+          ok = mbar_wait(smem_u32(&bar_kv_full[slot]), (idx / C::NSLOT) & 1, ctl);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t sK = sRing + slot * C::KV_BYTES;
+          const uint32_t d_s = tmem + ((j & 1) ? C::TM_S1 : C::TM_S0);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t koff = (kk >> 2) * (128 * 128) + (kk & 3) * 32;
+            mma_ss(d_s, sw128_desc(sQ + koff, 16, 1024), sw128_desc(sK + koff, 16, 1024),
+                   idesc_s, kk > 0);
+          }
+          mma_commit(smem_u32(&bar_s_full[j & 1]));
+          mma_commit(smem_u32(&bar_kv_empty[slot]));
+        }
+        if (j >= 1) {
+          const int jj = j - 1, pb = jj & 1;
+          ok = mbar_wait(smem_u32(&bar_p_full[pb]), (jj >> 1) & 1, ctl);
+          if (!ok) break;
+          const int idx = 2 * jj + 1, slot = idx % C::NSLOT;
+          ok = mbar_wait(smem_u32(&bar_kv_full[slot]), (idx / C::NSLOT) & 1, ctl);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t sV = sRing + slot * C::KV_BYTES;
+          const uint32_t a_p = tmem + (pb ? C::TM_P1 : C::TM_P0);
+#pragma unroll
+          for (int kk = 0; kk < C::BK / 16; ++kk) {
+            mma_ts(tmem + C::TM_O, a_p + kk * 8, sw128_desc(sV + kk * 2048, C::BK * 128, 1024),
+                   idesc_o, (jj > 0 || kk > 0) ? 1u : 0u);
+          }
+          if (split) {
+            // O += P_lo V_j: the low-order bf16 part of P, stored over the
+            // first 64 columns of the score buffer it was computed from.
+            const uint32_t a_lo = tmem + (pb ? C::TM_S1 : C::TM_S0);
+#pragma unroll
+            for (int kk = 0; kk < C::BK / 16; ++kk)
+              mma_ts(tmem + C::TM_O, a_lo + kk * 8, sw128_desc(sV + kk * 2048, C::BK * 128, 1024),
+                     idesc_o, 1u);
+          }
+          mma_commit(smem_u32(&bar_pv_done[pb]));
+          mma_commit(smem_u32(&bar_kv_empty[slot]));
+        }
+      }
+      if (!ok) {
+        // Wait for the MMAs already issued before TMEM is released. bar_q_full
+        // has completed its only phase, so this commit completes phase 1.
+        mma_commit(smem_u32(&bar_q_full));
+        mbar_wait_drain(smem_u32(&bar_q_full), 1, 50000000ull);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax warps 0-3
+    const int r = threadIdx.x;  // query row within the tile == TMEM lane
+    const int qrow = q0 + r;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    float m = -INFINITY;  // running max in log2 units (scaled scores)
+    float l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_kv; ++j) {
+      const int sb = j & 1;
+      ok = mbar_wait_warp(smem_u32(&bar_s_full[sb]), (j >> 1) & 1, ctl);
+      if (!ok) break;
+      tc_fence_after();
+      float x[C::BK];
+      {
+        const uint32_t ts = tmem + lane_base + (sb ? C::TM_S1 : C::TM_S0);
+        uint32_t u[C::BK];
+#pragma unroll
+        for (int c = 0; c < C::BK; c += 32)
+          tmem_ld32(ts + c, *reinterpret_cast<uint32_t(*)[32]>(&u[c]));
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < C::BK; ++c) x[c] = __uint_as_float(u[c]) * p.scale_log2;
+      }
+      const int k0 = j * C::BK;
+      const bool need_mask = (p.causal && k0 + C::BK - 1 > q0) || (k0 + C::BK > p.S);
+      if (need_mask) {
+        const int lim = p.causal ? min(qrow, p.S - 1) : (p.S - 1);
+#pragma unroll
+        for (int c = 0; c < C::BK; ++c)
+          if (k0 + c > lim) x[c] = -INFINITY;
+      }
+      float mx = x[0];
+#pragma unroll
+      for (int c = 1; c < C::BK; ++c) mx = fmaxf(mx, x[c]);
+      float alpha = 1.f;
+      const bool rescale = mx > m + kRescaleThreshold;
+      if (rescale) {
+        alpha = ex2(m - mx);  // m = -inf on the first tile gives 0
+        m = mx;
+      }
+      float sum = 0.f;
+      uint32_t pk[C::BK / 2];
+#pragma unroll
+      for (int c = 0; c < C::BK; c += 2) {
+        const float p0 = ex2(x[c] - m);
+        const float p1 = ex2(x[c + 1] - m);
+        sum += p0 + p1;
+        pk[c / 2] = pack_bf16x2(p0, p1);
+        // Keep what bf16 dropped, in x (x is not needed any more).
+        x[c] = p0 - __uint_as_float(pk[c / 2] << 16);
+        x[c + 1] = p1 - __uint_as_float(pk[c / 2] & 0xFFFF0000u);
+      }
+      l = l * alpha + sum;
+      // P buffer sb was last read by PV_{j-2}.
+      if (j >= 2) {
+        ok = mbar_wait_warp(smem_u32(&bar_pv_done[sb]), ((j - 2) >> 1) & 1, ctl);
+        if (!ok) break;
+      }
+      {
+        const uint32_t tp = tmem + lane_base + (sb ? C::TM_P1 : C::TM_P0);
+        tmem_st32(tp, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+        tmem_st32(tp + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+        if (split) {
+          // P_lo over columns 0..63 of this tile's score buffer, whose scores
+          // this thread has already read; the next MMA to write the buffer
+          // (S_{j+2}) issues after PV_j and tcgen05 MMAs run in issue order.
+#pragma unroll
+          for (int c = 0; c < C::BK; c += 2) pk[c / 2] = pack_bf16x2(x[c], x[c + 1]);
+          const uint32_t tl = tmem + lane_base + (sb ? C::TM_S1 : C::TM_S0);
+          tmem_st32(tl, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+          tmem_st32(tl + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+        }
+      }
+      // Rescale this warp's O rows once PV_{j-1} has landed in TMEM.
+      if (j >= 1 && __any_sync(0xffffffffu, rescale)) {
+        ok = mbar_wait_warp(smem_u32(&bar_pv_done[(j - 1) & 1]), ((j - 1) >> 1) & 1, ctl);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t to = tmem + lane_base + C::TM_O;
+#pragma unroll
+        for (int c = 0; c < D; c += 32) {
+          uint32_t u[32];
+          tmem_ld32(to + c, u);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
+          tmem_st32(to + c, u);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&bar_p_full[sb]));
+    }
+    if (ok && n_kv > 0) {
+      const int jl = n_kv - 1;
+      ok = mbar_wait_warp(smem_u32(&bar_pv_done[jl & 1]), (jl >> 1) & 1, ctl);
+    }
+    if (ok) {
+      tc_fence_after();
+      const float inv_l = 1.f / l;
+      const bool valid = qrow < p.S;
+      const size_t rowoff = ((static_cast<size_t>(b) * p.S + qrow) * p.Hq + hq) * D;
+      const uint32_t to = tmem + lane_base + C::TM_O;
+#pragma unroll
+      for (int c = 0; c < D; c += 32) {
+        uint32_t u[32];
+        tmem_ld32(to + c, u);
+        tmem_wait_ld();
+        uint4 w[4], wl[4];
+        uint32_t* wp = reinterpret_cast<uint32_t*>(w);
+        uint32_t* wlp = reinterpret_cast<uint32_t*>(wl);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float x0 = __uint_as_float(u[2 * i]) * inv_l;
+          const float x1 = __uint_as_float(u[2 * i + 1]) * inv_l;
+          wp[i] = pack_bf16x2(x0, x1);
+          // what bf16 rounding dropped, itself rounded to bf16
+          wlp[i] = pack_bf16x2(x0 - __uint_as_float(wp[i] << 16),
+                               x1 - __uint_as_float(wp[i] & 0xFFFF0000u));
+        }
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(p.o + rowoff + c);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) dst[i] = w[i];
+          if (p.o_lo) {
+            uint4* dl = reinterpret_cast<uint4*>(p.o_lo + rowoff + c);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dl[i] = wl[i];
+          }
+        }
+      }
+      if (valid)
+        p.lse[(static_cast<size_t>(b) * p.Hq + hq) * p.S + qrow] = (m + __log2f(l)) * kLn2;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+template <int D>
+cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                         const FwdParams& p, cudaStream_t stream) {
+  using C = FwdCfg<D>;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM_ALLOC);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  dim3 grid(p.B * p.Hq, p.n_qtiles);
+  attn_fwd_kernel<D><<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(int D, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const FwdParams& p, cudaStream_t stream) {
+  if (D == 128) return launch_fwd_t<128>(tq, tk, tv, p, stream);
+  return launch_fwd_t<64>(tq, tk, tv, p, stream);
+}
+
+}  // namespace attn

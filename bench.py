@@ -1,0 +1,363 @@
+"""Benchmark: causal bf16 attention forward + backward on GB300.
+
+One step = the whole hot path over one batch: attn_fwd_residual (forward with
+the output residual), then the backward's preprocess and main kernels. The
+default workload is the Llama-3-8B-shaped attention layer (B=2, Hq=32, Hkv=8,
+S=4096, D=128, causal). Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME]
+
+--impl reference times the fp64 CPU oracle (the only reference this method
+has) on the host cores, on a bounded sample of the same workload.
+Under torchrun (N > 1) each rank runs an independent replica on its own GPU
+(the path has no exchange step); rank 0 prints the line.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "causal bf16 attention fwd+bwd TFLOP/s at 1 GB300; % of dense BF16 tensor peak"
+DEFAULT_WORKLOAD = "llama3_8b_s4096"
+
+# DRAM traffic of the backward main kernel per launch, from an ncu capture,
+# keyed by the hash of the kernel sources it was taken on (null once they change).
+TRAFFIC = {}
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for name in ("attn_bwd.cu", "attn_common.cuh", "sm100_ptx.cuh"):
+        with open(os.path.join(ROOT, "attention_fwd_bwd_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def reduce_max(value, world):
+    """Max of a float over ranks (identity on one rank)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([float(value)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(units_per_rank, seconds_max, world):
+    """Throughput of the whole job: units all ranks processed / slowest rank's time."""
+    return units_per_rank * world / seconds_max
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi during a region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        mhz, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    mhz.append(float(parts[1]))
+                    mx = float(parts[2])
+                except ValueError:
+                    continue
+                for n, val in zip(names, parts[5:9]):
+                    if val.lower().startswith("active"):
+                        reasons.add(n)
+        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(mhz)}
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline: the fp64 oracle on the host cores, on a bounded sample.
+# ---------------------------------------------------------------------------
+def oracle_sample(w, budget_s=12.0, max_heads=None):
+    """Time the oracle's forward + backward on query heads of batch 0, one at a
+    time against their kv head, until `budget_s` has passed. Returns
+    (convention FLOP/s, sample description, seconds)."""
+    import numpy as np
+    from attention_fwd_bwd_gb300.inputs import make_inputs
+    from oracle import attn_ref_bwd, attn_ref_fwd
+    q, k, v, do = make_inputs(1, w.Hq, w.Hkv, w.S, w.D, w.seed, w.qk_std)
+    f64 = lambda t: t.double().numpy()
+    G = w.Hq // w.Hkv
+    heads, t0 = 0, time.perf_counter()
+    max_heads = max_heads or w.Hq
+    while heads < max_heads:
+        h = heads
+        g = h // G
+        qs, ks, vs, ds = (f64(q[:, :, h:h + 1]), f64(k[:, :, g:g + 1]), f64(v[:, :, g:g + 1]), f64(do[:, :, h:h + 1]))
+        attn_ref_fwd(qs, ks, vs, w.causal, w.scale)
+        attn_ref_bwd(qs, ks, vs, ds, w.causal, w.scale)
+        heads += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    secs = time.perf_counter() - t0
+    per_head = (w.flops_fwd() + w.flops_bwd()) / (w.B * w.Hq)
+    return per_head * heads / secs, f"{heads} of {w.B * w.Hq} (batch, query head) slices, full S={w.S}", secs
+
+
+def cpu_cores():
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
+    return os.cpu_count()
+
+
+# ---------------------------------------------------------------------------
+def run_reference(args, w, world, rank):
+    if rank != 0:
+        return 0
+    rates, secs = [], 0.0
+    sample = ""
+    for i in range(args.warmup + args.steps):
+        r, sample, s = oracle_sample(w, budget_s=args.ref_budget, max_heads=1)
+        if i >= args.warmup:
+            rates.append(r)
+            secs += s
+    value = statistics.mean(rates) / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / max(1, args.steps),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) bf16 inputs of the workload's shape)",
+        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "S": w.S, "D": w.D,
+                   "causal": w.causal, "parallelism": "replicas"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": f"per step: {sample}"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, w, world, rank, local):
+    import torch
+    import attention_fwd_bwd_gb300 as attn
+    from attention_fwd_bwd_gb300._build import build
+    from attention_fwd_bwd_gb300.inputs import workload_inputs
+
+    build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    L = attn.lib()
+    q_h, k_h, v_h, do_h = workload_inputs(w)
+    q, k, v, do = (t.to(dev) for t in (q_h, k_h, v_h, do_h))
+    B, S, Hq, Hkv, D = w.B, w.S, w.Hq, w.Hkv, w.D
+    o, o_lo = torch.empty_like(q), torch.empty_like(q)
+    lse = torch.empty(B, Hq, S, dtype=torch.float32, device=dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty(q.shape, **f32), torch.empty(k.shape, **f32), torch.empty(k.shape, **f32)
+    ws = torch.empty(attn.attn_bwd_workspace_size(B, Hq, Hkv, S, D), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        attn.attn_fwd_residual(q, k, v, o, o_lo, lse, w.causal, w.scale, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        attn.attn_bwd_preprocess(q, k, o, do, lse, dq, ws, o_lo=o_lo, stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+        attn.attn_bwd_main(q, k, v, do, dq, dk, dv, w.causal, w.scale, ws, stream=stream)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if attn.attn_check_status(ws) != 0:
+        raise RuntimeError("kernel pipeline timeout during warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        start.record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+        stop.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    if attn.attn_check_status(ws) != 0:
+        raise RuntimeError("kernel pipeline timeout during the timed steps")
+    total_ms = start.elapsed_time(stop)
+    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    pre_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    main_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+    total_ms = reduce_max(total_ms, world)
+    ms_per_step = total_ms / args.steps
+    flops = w.flops_fwd() + w.flops_bwd()
+    value = whole_job_value(flops, ms_per_step / 1e3, world) / 1e12
+
+    # End to end through the public API with host buffers: pinned inputs copied
+    # in, forward + backward, outputs and gradients copied back, every step.
+    pin = lambda t: t.pin_memory()
+    hq_, hk_, hv_, hdo_ = (pin(t) for t in (q_h, k_h, v_h, do_h))
+    ho, hlse = pin(torch.empty(o.shape, dtype=o.dtype)), pin(torch.empty(lse.shape, dtype=lse.dtype))
+    hdq, hdk, hdv = (pin(torch.empty(t.shape, dtype=t.dtype)) for t in (dq, dk, dv))
+    h2d = sum(t.numel() * t.element_size() for t in (hq_, hk_, hv_, hdo_))
+    d2h = sum(t.numel() * t.element_size() for t in (ho, hlse, hdq, hdk, hdv))
+
+    def e2e_step():
+        for dst, src in ((q, hq_), (k, hk_), (v, hv_), (do, hdo_)):
+            dst.copy_(src, non_blocking=True)
+        attn.attn_fwd_residual(q, k, v, o, o_lo, lse, w.causal, w.scale, stream=stream)
+        attn.attn_bwd(q, k, v, o, do, lse, dq, dk, dv, w.causal, w.scale, ws, o_lo=o_lo, stream=stream)
+        for dst, src in ((ho, o), (hlse, lse), (hdq, dq), (hdk, dk), (hdv, dv)):
+            dst.copy_(src, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e_start, e_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_steps = max(1, min(args.steps, 10))
+    e_start.record(stream)
+    for _ in range(e_steps):
+        e2e_step()
+    e_stop.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max(e_start.elapsed_time(e_stop), world) / e_steps
+    e2e_value = whole_job_value(flops, e2e_ms / 1e3, world) / 1e12
+
+    peaks, peak_src = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    main_tf = w.flops_bwd() / (main_ms / 1e3) / 1e12
+    fwd_tf = w.flops_fwd() / (fwd_ms / 1e3) / 1e12
+    pre_bytes = (3 * B * S * Hq * D * 2 + B * Hq * S * 4 + 2 * B * Hq * S * 4 + B * S * Hq * D * 4)
+    traffic = TRAFFIC.get(kernel_source_hash())
+    sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) bf16 q, k, v, dO of the workload's shape)",
+            "config": {"workload": w.name, "B": B, "Hq": Hq, "Hkv": Hkv, "S": S, "D": D, "causal": w.causal,
+                       "parallelism": f"replicas x{world}",
+                       "l2": "no flush: q, k, v, dO (168 MB) exceed the 129 MB L2",
+                       "flops_per_step": flops, "sm_count": sm_count},
+            "gpu_launches": 3 * args.steps,
+            "passes": {
+                "fwd": {"ms": fwd_ms, "tflops": fwd_tf, "frac_of_peak": fwd_tf / peak},
+                "bwd_preprocess": {"ms": pre_ms, "gbs": pre_bytes / (pre_ms / 1e3) / 1e9,
+                                   "frac_of_hbm": pre_bytes / (pre_ms / 1e3) / 1e9 / float(peaks["hbm_gbs"])},
+                "bwd_main": {"ms": main_ms, "tflops": main_tf, "frac_of_peak": main_tf / peak},
+                "bwd": {"ms": pre_ms + main_ms,
+                        "tflops": w.flops_bwd() / ((pre_ms + main_ms) / 1e3) / 1e12,
+                        "frac_of_peak": w.flops_bwd() / ((pre_ms + main_ms) / 1e3) / 1e12 / peak},
+            },
+            "roofline": {"kernel": "attn_bwd_main_kernel", "bound": "tensor", "achieved": main_tf, "peak": peak,
+                         "unit": "TFLOP/s", "frac": main_tf / peak, "traffic": traffic,
+                         "peak_source": f"{peak_src} bf16_tflops (burst)"},
+            "clocks": clocks.summary(),
+            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": e2e_ms},
+        }
+        if not args.no_cpu_baseline:
+            rate, sample, secs = oracle_sample(w, budget_s=args.ref_budget)
+            line["cpu_baseline"] = {"value": rate / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+                                    "sample": f"{sample}; {secs:.1f} s"}
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--ref-budget", type=float, default=12.0, help="seconds of oracle work per sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    from attention_fwd_bwd_gb300.inputs import BY_NAME
+    w = BY_NAME[args.workload]
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if (args.impl == "ours" and torch.cuda.is_available()) else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    try:
+        if args.impl == "reference":
+            return run_reference(args, w, world, rank)
+        return run_ours(args, w, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

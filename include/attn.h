@@ -1,0 +1,165 @@
+/*
+ * attn.h -- C ABI of the GB300 (sm_103a) fused attention library, libattn.so.
+ *
+ * The operation is scaled dot-product attention, O = softmax(scale * Q K^T) V
+ * per (batch, query head), from "Scheduling Data to Compute: Hierarchical Data
+ * Pipelining for LLM Training on AMD GPUs", section 2.1, Eq. (1), computed the
+ * FlashAttention way that the same section's Algorithm 0 describes: K/V tiles
+ * stream through on-chip memory while the softmax state and the output
+ * accumulator stay on chip. The backward pass is the exact gradient of Eq. (1)
+ * for the three products whose operand layouts the paper's Table 3 lists
+ * (scores, query gradient dS*K, key gradient dS^T*Q) plus dV = P^T*dO.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All tensor pointers are DEVICE pointers on the current CUDA device,
+ *    owned by the caller, contiguous, 16-byte aligned.
+ *  - bf16 tensors use the [B, S, H, D] layout ("BSHD"): q, o, dO, dq are
+ *    [B, S, Hq, D]; k, v, dk, dv are [B, S, Hkv, D].
+ *  - lse is fp32 [B, Hq, S]: LSE_i = ln sum_j exp(scale * q_i . k_j) over the
+ *    keys row i sees (natural log, scaled scores).
+ *  - Grouped-query attention: Hq must be a multiple of Hkv; query head h
+ *    reads key/value head h / (Hq / Hkv) (contiguous groups).
+ *  - causal != 0: query i sees keys j <= i. causal == 0: all keys.
+ *  - D must be 64 or 128. Any S >= 0 up to 2^24 is accepted. B == 0 or
+ *    S == 0 (with otherwise valid sizes) is a no-op that returns ATTN_OK; the
+ *    pointers are then not read and may be NULL.
+ *  - Checks run in this order: sizes (INVALID_ARG / UNSUPPORTED), scale, the
+ *    empty-problem no-op, pointers, workspace, device.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream). The library allocates no memory per call and never
+ *    synchronises the host, except under ATTN_CHECK_STATUS=1 in the
+ *    environment, where each call waits for its kernels and reads back the
+ *    device status word.
+ *  - Arguments are validated before any launch; a failed check launches
+ *    nothing and returns the code named below.
+ */
+#ifndef ATTN_GB300_ATTN_H_
+#define ATTN_GB300_ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1, /* null or misaligned pointer, bad size or scale */
+  ATTN_ERR_UNSUPPORTED = 2, /* valid but unsupported: D not in {64,128}, no sm_100-family GPU */
+  ATTN_ERR_CUDA = 3,        /* a CUDA runtime or driver call failed */
+  ATTN_ERR_TIMEOUT = 4,     /* a kernel's bounded pipeline wait ran out (reported via status) */
+  ATTN_ERR_WORKSPACE = 5    /* workspace null, misaligned or smaller than attn_bwd_workspace_size */
+} attn_status_t;
+
+/*
+ * Forward: o = softmax(scale * q k^T) v and the row log-sum-exp.
+ *
+ *   q     [B,S,Hq,D]  bf16, in
+ *   k, v  [B,S,Hkv,D] bf16, in
+ *   o     [B,S,Hq,D]  bf16, out (overwritten): O rounded to nearest bf16
+ *   lse   [B,Hq,S]    fp32, out (overwritten); needed by attn_bwd
+ *   scale finite, e.g. 1/sqrt(D)
+ *
+ * Errors: ATTN_ERR_INVALID_ARG for a null or non-16-byte-aligned pointer,
+ * B, S < 0, Hq, Hkv <= 0, Hq % Hkv != 0, or a non-finite scale;
+ * ATTN_ERR_UNSUPPORTED for D not in {64, 128}, S > 2^24, or a device that is
+ * not sm_103; ATTN_ERR_CUDA if tensor-map encoding or a launch fails.
+ */
+attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                       int Hq, int Hkv, int S, int D, int causal, float scale, void* stream);
+
+/*
+ * Forward that also writes the low-order part of the output:
+ *
+ *   o_lo  [B,S,Hq,D]  bf16, out (overwritten): bf16(O_fp32 - o), so o + o_lo
+ *                     carries O to about 16 significant bits.
+ *
+ * Passing o_lo on to attn_bwd makes the backward's Dvec = rowsum(dO * O)
+ * accurate to about 16 bits instead of bf16's 8; the gradient tolerance of
+ * the test suite (max-abs error <= 5e-2 of the exact gradient's rms) needs
+ * it at long causal sequences. Other arguments and errors as attn_fwd
+ * (o_lo may not be NULL here).
+ */
+attn_status_t attn_fwd_residual(const void* q, const void* k, const void* v, void* o, void* o_lo,
+                                float* lse, int B, int Hq, int Hkv, int S, int D, int causal,
+                                float scale, void* stream);
+
+/*
+ * Size in bytes of the device workspace attn_bwd needs for these sizes (the
+ * status word, and fp32 Dvec and log2-scaled LSE rows with the sequence
+ * padded to a multiple of 128). Returns 0 for invalid or unsupported sizes,
+ * and for empty problems.
+ */
+size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int S, int D);
+
+/*
+ * Backward: the gradients of L = sum(dO * O) with respect to q, k and v,
+ * written in fp32.
+ *
+ *   q, k, v, o, lse  as passed to / returned by attn_fwd (in)
+ *   dO    [B,S,Hq,D]  bf16, in
+ *   dq    [B,S,Hq,D]  fp32, out (overwritten)
+ *   dk,dv [B,S,Hkv,D] fp32, out (overwritten; for GQA each sums over the
+ *                     Hq/Hkv query heads of its group)
+ *   o_lo  [B,S,Hq,D]  bf16, in, optional (NULL allowed): the residual from
+ *                     attn_fwd_residual; with NULL, Dvec uses o alone.
+ *   workspace        device memory of at least attn_bwd_workspace_size()
+ *                    bytes, 256-byte aligned, owned by the caller; its
+ *                    contents on entry do not matter and are clobbered.
+ *
+ * Runs two kernels in order on `stream`: the preprocess pass
+ * (Dvec = rowsum(dO * O), log2-scaled LSE, dq zeroed) and the KV-parallel main
+ * kernel (dK and dV per key tile; dQ added into dq by fp32 reductions, so dq
+ * is reproducible only up to fp32 summation order). Inside the main kernel P
+ * and dS enter the gradient products as bf16 hi/lo pairs (about 16
+ * significant bits).
+ *
+ * Errors: as attn_fwd, plus ATTN_ERR_WORKSPACE for a null or misaligned
+ * workspace or one smaller than attn_bwd_workspace_size().
+ */
+attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                       const float* lse, void* dq, void* dk, void* dv, const void* o_lo, int B,
+                       int Hq, int Hkv, int S, int D, int causal, float scale, void* workspace,
+                       size_t workspace_bytes, void* stream);
+
+/*
+ * The two stages of attn_bwd as separate calls, in the order attn_bwd runs
+ * them, for callers that time or schedule them one by one. Arguments and
+ * errors are those of attn_bwd; the main stage reads what the preprocess
+ * stage left in `workspace` and `dq`, so they must run in order on one
+ * stream with the same arguments.
+ */
+attn_status_t attn_bwd_preprocess(const void* o, const void* o_lo, const void* dO,
+                                  const float* lse, void* dq, int B, int Hq, int Hkv, int S, int D,
+                                  void* workspace, size_t workspace_bytes, void* stream);
+attn_status_t attn_bwd_main(const void* q, const void* k, const void* v, const void* dO, void* dq,
+                            void* dk, void* dv, int B, int Hq, int Hkv, int S, int D, int causal,
+                            float scale, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Static, human-readable name of a status code. */
+const char* attn_status_string(attn_status_t status);
+
+/*
+ * Reads (and clears) the device status word that the forward kernels of the
+ * current device, or the backward kernels using `workspace` (may be NULL for
+ * the forward word only), set when a bounded pipeline wait ran out.
+ * Synchronises the device. Returns ATTN_OK or ATTN_ERR_TIMEOUT (or
+ * ATTN_ERR_CUDA if the read itself failed).
+ */
+attn_status_t attn_check_status(void* workspace);
+
+/*
+ * Sets the time limit of every bounded wait inside the kernels launched after
+ * this call on this process, in nanoseconds (default 2e9, i.e. 2 s; 0 restores
+ * the default). A limit shorter than a pipeline step makes the kernels give
+ * up and report ATTN_ERR_TIMEOUT instead of computing; it exists for testing
+ * that path.
+ */
+void attn_set_wait_timeout_ns(uint64_t ns);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* ATTN_GB300_ATTN_H_ */

@@ -1,0 +1,125 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Small shapes are compared element by element on every output; they span
+several tiles and ragged tails, GQA and MHA, causal and not, D = 64 and 128.
+The five named workloads run at full size in the same launch configuration
+the benchmark uses, and are compared on seeded samples of rows that the
+oracle computes one by one, plus exact gradient invariants over every row.
+"""
+import numpy as np
+import pytest
+import torch
+
+from attention_fwd_bwd_gb300.inputs import WORKLOADS, make_inputs, workload_inputs
+from oracle import attn_ref_bwd, attn_ref_fwd, attn_ref_keys_dkdv, attn_ref_rows_dq, attn_ref_rows_fwd
+from tests.helpers import (TOL_GRAD_REL_RMS, assert_close_fwd, assert_close_grad, gpu_fwd_bwd, np64)
+
+pytestmark = pytest.mark.gpu
+
+SMALL = [
+    # B, Hq, Hkv, S, D, causal
+    (1, 1, 1, 128, 64, False),
+    (1, 1, 1, 128, 128, True),
+    (1, 2, 1, 384, 128, True),
+    (2, 4, 2, 256, 64, True),
+    (1, 4, 1, 512, 128, False),
+    (1, 2, 2, 300, 128, True),    # ragged tail
+    (2, 2, 1, 200, 64, False),    # ragged tail, non-causal
+    (1, 3, 3, 129, 64, True),     # one row into a second tile
+    (1, 2, 1, 1, 128, True),      # single row
+    (1, 2, 2, 77, 128, False),    # shorter than one tile
+    (1, 8, 2, 640, 128, True),
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,S,D,causal", SMALL)
+def test_small_shapes_elementwise(B, Hq, Hkv, S, D, causal):
+    scale = 1.0 / np.sqrt(D)
+    q, k, v, do = make_inputs(B, Hq, Hkv, S, D, seed=100 + S + D + Hq)
+    got = gpu_fwd_bwd(q, k, v, do, causal, scale)
+    o_ref, lse_ref = attn_ref_fwd(np64(q), np64(k), np64(v), causal, scale)
+    dq_ref, dk_ref, dv_ref = attn_ref_bwd(np64(q), np64(k), np64(v), np64(do), causal, scale)
+    what = f"B{B} Hq{Hq} Hkv{Hkv} S{S} D{D} causal={causal}"
+    assert_close_fwd(got["o"], got["lse"], o_ref, lse_ref, what)
+    assert_close_grad(got["dq"], dq_ref, "dQ", what)
+    assert_close_grad(got["dk"], dk_ref, "dK", what)
+    assert_close_grad(got["dv"], dv_ref, "dV", what)
+
+
+def test_tiny_workload_full():
+    w = WORKLOADS[0]
+    q, k, v, do = workload_inputs(w)
+    got = gpu_fwd_bwd(q, k, v, do, w.causal, w.scale)
+    o_ref, lse_ref = attn_ref_fwd(np64(q), np64(k), np64(v), w.causal, w.scale)
+    dq_ref, dk_ref, dv_ref = attn_ref_bwd(np64(q), np64(k), np64(v), np64(do), w.causal, w.scale)
+    assert_close_fwd(got["o"], got["lse"], o_ref, lse_ref, w.name)
+    assert_close_grad(got["dq"], dq_ref, "dQ", w.name)
+    assert_close_grad(got["dk"], dk_ref, "dK", w.name)
+    assert_close_grad(got["dv"], dv_ref, "dV", w.name)
+
+
+def _sampled_check(w, n_rows=64, n_key_groups=1):
+    q, k, v, do = workload_inputs(w)
+    got = gpu_fwd_bwd(q, k, v, do, w.causal, w.scale)
+    do_t = do
+    # float32 copies are exact for bf16 values; the oracle upcasts to fp64.
+    q, k, v, do = (t.float().numpy() for t in (q, k, v, do))
+    rng = np.random.default_rng(w.seed)
+    rows = [(int(rng.integers(w.B)), int(rng.integers(w.Hq)), int(rng.integers(w.S))) for _ in range(n_rows)]
+    # always include the first and last rows of the first head
+    rows[0] = (0, 0, 0)
+    rows[1] = (w.B - 1, w.Hq - 1, w.S - 1)
+    o_ref, lse_ref = attn_ref_rows_fwd(q, k, v, w.causal, w.scale, rows)
+    dq_ref = attn_ref_rows_dq(q, k, v, do, w.causal, w.scale, rows)
+    o_g = np.stack([np64(got["o"][b, i, h]) for b, h, i in rows])
+    l_g = np.array([float(got["lse"][b, h, i]) for b, h, i in rows])
+    dq_g = np.stack([np64(got["dq"][b, i, h]) for b, h, i in rows])
+    assert_close_fwd(o_g, l_g, o_ref, lse_ref, w.name)
+    assert_close_grad(dq_g, dq_ref, "dQ rows", w.name)
+    for _ in range(n_key_groups):
+        b, g = int(rng.integers(w.B)), int(rng.integers(w.Hkv))
+        keys = sorted(set(int(x) for x in rng.integers(0, w.S, 64)) | {0, w.S - 1})
+        dk_ref, dv_ref = attn_ref_keys_dkdv(q, k, v, do, w.causal, w.scale, b, g, keys)
+        assert_close_grad(np64(got["dk"][b, keys, g]), dk_ref, "dK rows", w.name)
+        assert_close_grad(np64(got["dv"][b, keys, g]), dv_ref, "dV rows", w.name)
+    # Exact invariants over all rows: sum_j dK_j = 0, sum_j dV_j = sum of the group's dO.
+    G = w.Hq // w.Hkv
+    dk_sum = got["dk"].to(torch.float64).sum(dim=1)          # [B, Hkv, D]
+    dv_sum = got["dv"].to(torch.float64).sum(dim=1)
+    do_sum = do_t.to(torch.float64).sum(dim=1).reshape(w.B, w.Hkv, G, w.D).sum(dim=2)
+    dk_rms = float(got["dk"].to(torch.float64).pow(2).mean().sqrt())
+    dv_rms = float(got["dv"].to(torch.float64).pow(2).mean().sqrt())
+    # bf16 rounding of each dK/dV row is an independent error of about
+    # 2^-9 * rms, so the row sums drift by about sqrt(S) of that.
+    bound_k = 4 * np.sqrt(w.S) * 2.0 ** -8 * dk_rms
+    bound_v = 4 * np.sqrt(w.S) * 2.0 ** -8 * dv_rms + 1e-3 * float(do_sum.abs().max())
+    assert float(dk_sum.abs().max()) <= bound_k, (float(dk_sum.abs().max()), bound_k)
+    assert float((dv_sum - do_sum).abs().max()) <= bound_v, (float((dv_sum - do_sum).abs().max()), bound_v)
+
+
+@pytest.mark.parametrize("name", [w.name for w in WORKLOADS[1:]])
+def test_workload_sampled(name):
+    w = {x.name: x for x in WORKLOADS}[name]
+    _sampled_check(w)
+
+
+def test_repeatable_outputs():
+    """O, LSE, dK and dV are bitwise repeatable; dQ (fp32 reductions in
+    varying order) agrees within the gradient tolerance."""
+    q, k, v, do = make_inputs(1, 4, 2, 512, 128, seed=7)
+    a = gpu_fwd_bwd(q, k, v, do, True, 128 ** -0.5)
+    b = gpu_fwd_bwd(q, k, v, do, True, 128 ** -0.5)
+    for n in ("o", "lse", "dk", "dv"):
+        assert torch.equal(a[n], b[n]), n
+    rms = float(a["dq"].float().pow(2).mean().sqrt())
+    assert float((a["dq"].float() - b["dq"].float()).abs().max()) <= TOL_GRAD_REL_RMS * rms
+
+
+def test_empty_inputs_are_noops():
+    # B == 0 or S == 0 returns ATTN_OK without reading any pointer.
+    import attention_fwd_bwd_gb300 as attn
+    L = attn.lib()
+    for B, S in ((0, 128), (1, 0)):
+        assert L.attn_fwd(None, None, None, None, None, B, 2, 1, S, 64, 1, 0.125, None) == 0
+        assert L.attn_bwd(*([None] * 10), B, 2, 1, S, 64, 1, 0.125, None, 0, None) == 0
+    torch.cuda.synchronize()

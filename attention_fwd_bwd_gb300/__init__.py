@@ -22,6 +22,7 @@ __all__ = [
     "attn_bwd",
     "attn_bwd_preprocess",
     "attn_bwd_main",
+    "attn_bwd_noalloc",
     "attn_bwd_workspace_size",
     "attn_check_status",
     "attn_set_wait_timeout_ns",
@@ -74,6 +75,8 @@ def lib():
     L.attn_bwd_preprocess.restype = i
     L.attn_bwd_main.argtypes = [vp] * 7 + [i] * 6 + [f, vp, sz, vp]
     L.attn_bwd_main.restype = i
+    L.attn_bwd_noalloc.argtypes = [vp] * 10 + [i] * 6 + [f, vp]
+    L.attn_bwd_noalloc.restype = i
     L.attn_status_string.argtypes = [i]
     L.attn_status_string.restype = ctypes.c_char_p
     L.attn_check_status.argtypes = [vp]
@@ -199,6 +202,22 @@ def attn_bwd_main(q, k, v, dO, dq, dk, dv, causal, scale, workspace, stream=None
     _check("attn_bwd_main", lib().attn_bwd_main(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(dq), _ptr(dk),
                                                 _ptr(dv), B, Hq, Hkv, S, D, int(bool(causal)), float(scale),
                                                 wp, wb, _stream(stream)))
+
+
+def attn_bwd_noalloc(q, k, v, o, dO, lse, dq, dk, dv, causal, scale, o_lo=None, stream=None):
+    """attn_bwd without a workspace, for callers that cannot allocate device
+    memory: it uses the library's built-in 16 MiB scratch array (see
+    attn_bwd_noalloc in include/attn.h)."""
+    B, Hq, Hkv, S, D = _sizes(q, k)
+    for t, ref, n in ((v, k, "v"), (o, q, "o"), (dO, q, "dO")):
+        _like(t, ref, n)
+    if o_lo is not None:
+        _like(o_lo, q, "o_lo")
+    _grads_ok(q, k, dq, dk, dv)
+    _lse_ok(lse, B, Hq, S, q.device)
+    _check("attn_bwd_noalloc", lib().attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse),
+                                                      _ptr(dq), _ptr(dk), _ptr(dv), _opt(o_lo), B, Hq, Hkv, S, D,
+                                                      int(bool(causal)), float(scale), _stream(stream)))
 
 
 def attn_check_status(workspace=None):

@@ -138,6 +138,41 @@ attn_status_t attn_bwd_main(const void* q, const void* k, const void* v, const v
                             void* dk, void* dv, int B, int Hq, int Hkv, int S, int D, int causal,
                             float scale, void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * attn_bwd without a workspace argument, for callers that cannot allocate
+ * device memory. The paper has no counterpart: this is a packaging variant of
+ * attn_bwd, not part of the method.
+ *
+ * Who needs it: code that runs inside a host framework or plugin interface
+ * which hands it only the tensors of one call and owns every allocation
+ * itself, and code on a latency-critical path where a cudaMalloc (which can
+ * synchronise the device) is not allowed. Such callers cannot provide the
+ * workspace that attn_bwd asks for.
+ *
+ * Instead of a caller workspace the call uses one scratch array compiled into
+ * the library: 16 MiB of device memory, reserved on every GPU that loads the
+ * library until the process exits. Problems whose
+ * attn_bwd_workspace_size(B, Hq, Hkv, S, D) exceeds 16 MiB (about
+ * B * Hq * ceil(S/128)*128 > 2,097,000 query rows) are rejected with
+ * ATTN_ERR_WORKSPACE before anything is launched.
+ *
+ * The first call on a device looks up the array's device address with that
+ * device current (cudaGetSymbolAddress); make that first call before any
+ * stream capture. The call allocates nothing: no cudaMalloc, cudaFree or
+ * allocating library routine.
+ *
+ * All calls on a device share the one array, and it keeps the last call's
+ * contents; each call rewrites every word it reads before reading it. Calls
+ * whose kernels overlap on the GPU (different streams without ordering
+ * between them) race on the array and give wrong results: order them.
+ *
+ * Arguments, results and the other errors are those of attn_bwd.
+ */
+attn_status_t attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
+                               const void* dO, const float* lse, void* dq, void* dk, void* dv,
+                               const void* o_lo, int B, int Hq, int Hkv, int S, int D, int causal,
+                               float scale, void* stream);
+
 /* Static, human-readable name of a status code. */
 const char* attn_status_string(attn_status_t status);
 

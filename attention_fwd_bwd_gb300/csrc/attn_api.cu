@@ -95,7 +95,7 @@ bool make_bshd_map(CUtensorMap* m, const void* base, int B, int S, int H, int D,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 4-D fp32 map over the [B, S, Hq, D] dq output; a box is 64 sequence rows of
+// 4-D fp32 map over the [B, S, Hq, D] dq output; a box is 32 sequence rows of
 // one head, all D columns, unswizzled (the layout the dQ staging tile uses).
 bool make_dq_map(CUtensorMap* m, void* base, int B, int S, int H, int D) {
   EncodeTiledFn fn = encode_fn();
@@ -105,7 +105,8 @@ bool make_dq_map(CUtensorMap* m, void* base, int B, int S, int H, int D) {
   const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 4,
                                  static_cast<cuuint64_t>(H) * D * 4,
                                  static_cast<cuuint64_t>(S) * H * D * 4};
-  const cuuint32_t box[4] = {static_cast<cuuint32_t>(D), 1, 64, 1};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(D), 1,
+                             static_cast<cuuint32_t>(BwdCfg<128>::DQ_ROWS), 1};
   const cuuint32_t es[4] = {1, 1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,

@@ -14,7 +14,7 @@
 //      output zeroed (HBM-bound).
 //   2. main: one CTA per (batch, kv head, 128-key tile). K_j and V_j stay in
 //      shared memory while Q_i, dO_i, LSE_i and Dvec_i of every 64-row query
-//      tile of the group's query heads stream through a two-stage TMA ring:
+//      tile of the group's query heads stream through a three-stage TMA ring:
 //        S^T = K_j Q_i^T and dP^T = V_j dO_i^T         (TMEM)
 //        P^T (TMEM) and scale * dS^T (shared memory) as bf16 hi/lo pairs
 //        dV += P^T dO_i, dK += dS^T Q_i                 (TMEM, whole loop)
@@ -28,6 +28,10 @@ namespace attn {
 using namespace ptx;
 
 namespace {
+
+#ifdef ATTN_TRACE
+static __device__ unsigned long long g_attn_trace[kTraceCtas * kTraceRoles * kTraceEvents];
+#endif
 
 // ------------------------------------------------------------------ preprocess
 __global__ void __launch_bounds__(256) attn_bwd_preprocess_kernel(
@@ -202,114 +206,142 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 
   if (warp == 12) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      prefetch_tmap(&tm_q);
-      prefetch_tmap(&tm_k);
-      prefetch_tmap(&tm_v);
-      prefetch_tmap(&tm_do);
-      mbar_arrive_expect_tx(smem_u32(&bar_kv_full), 2 * C::V_BYTES);
+    // The whole warp runs this loop; each copy is issued by one elected lane.
+    {
+      TraceCursor tc;
+      if (lane == 0) ATTN_TRACE_INIT(tc, 0);
+      ATTN_TRACE_EV(tc, 1, 0);
+      if (lane == 0) {
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+        prefetch_tmap(&tm_do);
+      }
+      mbar_arrive_expect_tx_el(smem_u32(&bar_kv_full), 2 * C::V_BYTES);
       for (int c = 0; c < C::KCH; ++c) {
-        tma_load_4d(sK + c * (BK * 128), &tm_k, smem_u32(&bar_kv_full), c * 64, g, k0, b);
-        tma_load_4d(sV + c * (BK * 128), &tm_v, smem_u32(&bar_kv_full), c * 64, g, k0, b);
+        tma_load_4d_el(sK + c * (BK * 128), &tm_k, smem_u32(&bar_kv_full), c * 64, g, k0, b);
+        tma_load_4d_el(sV + c * (BK * 128), &tm_v, smem_u32(&bar_kv_full), c * 64, g, k0, b);
       }
       bool ok = true;
       int issued = 0;
       for (int it = 0; it < n_it; ++it) {
         const int s = it % ST, round = it / ST;
-        if (round > 0) ok = mbar_wait(smem_u32(&bar_st_empty[s]), (round - 1) & 1, ctl);
+        if (round > 0) ok = mbar_wait_warp(smem_u32(&bar_st_empty[s]), (round - 1) & 1, ctl);
         if (!ok) break;
+        ATTN_TRACE_EV(tc, 2, it);  // stage free, issuing loads
         const int h = g * p.G + it / niq;
         const int q0 = (i_start + it % niq) * BQ;
         const uint32_t full = smem_u32(&bar_st_full[s]);
-        mbar_arrive_expect_tx(full, 2 * C::Q_BYTES + 2 * C::ROWVEC_BYTES);
+        mbar_arrive_expect_tx_el(full, 2 * C::Q_BYTES + 2 * C::ROWVEC_BYTES);
         for (int c = 0; c < C::KCH; ++c) {
-          tma_load_4d(stage_q(s) + c * (BQ * 128), &tm_q, full, c * 64, h, q0, b);
-          tma_load_4d(stage_do(s) + c * (BQ * 128), &tm_do, full, c * 64, h, q0, b);
+          tma_load_4d_el(stage_q(s) + c * (BQ * 128), &tm_q, full, c * 64, h, q0, b);
+          tma_load_4d_el(stage_do(s) + c * (BQ * 128), &tm_do, full, c * 64, h, q0, b);
         }
         const size_t rowoff = (static_cast<size_t>(b) * p.Hq + h) * p.S_pad + q0;
-        bulk_load(stage_do(s) + C::Q_BYTES, p.lse2 + rowoff, C::ROWVEC_BYTES, full);
-        bulk_load(stage_do(s) + C::Q_BYTES + C::ROWVEC_BYTES, p.dvec + rowoff, C::ROWVEC_BYTES,
-                  full);
+        bulk_load_el(stage_do(s) + C::Q_BYTES, p.lse2 + rowoff, C::ROWVEC_BYTES, full);
+        bulk_load_el(stage_do(s) + C::Q_BYTES + C::ROWVEC_BYTES, p.dvec + rowoff,
+                     C::ROWVEC_BYTES, full);
         issued = it + 1;
       }
-      if (!ok) {
-        for (int it = max(0, issued - ST); it < issued; ++it)
-          mbar_wait_drain(smem_u32(&bar_st_full[it % ST]), (it / ST) & 1, 50000000ull);
+      if (lane == 0) {
+        if (!ok) {
+          for (int it = max(0, issued - ST); it < issued; ++it)
+            mbar_wait_drain(smem_u32(&bar_st_full[it % ST]), (it / ST) & 1, 50000000ull);
+        }
+        mbar_wait_drain(smem_u32(&bar_kv_full), 0, 50000000ull);
       }
-      mbar_wait_drain(smem_u32(&bar_kv_full), 0, 50000000ull);
+      __syncwarp();
     }
   } else if (warp == 13) {
     // ------------------------------------------------------------ MMA issuer
+    TraceCursor tc;
+    if (lane == 0) ATTN_TRACE_INIT(tc, 1);
+    // The whole warp runs this loop and builds the (warp-uniform) descriptors;
+    // each MMA and commit is issued by one elected lane.
     bool ok = mbar_wait_warp(smem_u32(&bar_kv_full), 0, ctl);
-    if (lane == 0 && ok) {
+    if (ok) {
+      ATTN_TRACE_EV(tc, 1, 0);
       constexpr uint32_t idesc_sdp = idesc_bf16_f32(128, BQ, 0, 0);
       constexpr uint32_t idesc_kv = idesc_bf16_f32(128, D, 0, 1);
       constexpr uint32_t idesc_dq = idesc_bf16_f32(128, BQ, 1, 1);
+      // Descriptor bases; each step below only adds a constant byte offset
+      // (>> 4) to the start-address field.
+      const uint64_t dK_kmaj = sw128_desc(sK, 16, 1024);
+      const uint64_t dV_kmaj = sw128_desc(sV, 16, 1024);
+      const uint64_t dK_mn = sw128_desc(sK, BK * 128, 1024);
+      const uint64_t dDsHi_k = sw128_desc(sDsHi, 16, 1024);
+      const uint64_t dDsLo_k = sw128_desc(sDsLo, 16, 1024);
+      const uint64_t dDsHi_mn = sw128_desc(sDsHi, BK * 128, 1024);
+      const uint64_t dDsLo_mn = sw128_desc(sDsLo, BK * 128, 1024);
+      auto add = [](uint64_t d, uint32_t bytes) { return d + (bytes >> 4); };
       auto issue_sdp = [&](int s) {
-        const uint32_t sq = stage_q(s), sdo = stage_do(s);
+        const uint64_t dq_k = sw128_desc(stage_q(s), 16, 1024);
+        const uint64_t ddo_k = sw128_desc(stage_do(s), 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t ka = (kk >> 2) * (BK * 128) + (kk & 3) * 32;
           const uint32_t kb = (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
-          mma_ss(tmem + C::TM_ST, sw128_desc(sK + ka, 16, 1024), sw128_desc(sq + kb, 16, 1024),
-                 idesc_sdp, kk > 0);
-          mma_ss(tmem + C::TM_DPT, sw128_desc(sV + ka, 16, 1024), sw128_desc(sdo + kb, 16, 1024),
-                 idesc_sdp, kk > 0);
+          mma_ss_el(tmem + C::TM_ST, add(dK_kmaj, ka), add(dq_k, kb), idesc_sdp, kk > 0);
+          mma_ss_el(tmem + C::TM_DPT, add(dV_kmaj, ka), add(ddo_k, kb), idesc_sdp, kk > 0);
         }
-        mma_commit(smem_u32(&bar_sdp_full));
+        mma_commit_el(smem_u32(&bar_sdp_full));
       };
       if (n_it > 0) {
-        ok = mbar_wait(smem_u32(&bar_st_full[0]), 0, ctl);
+        ok = mbar_wait_warp(smem_u32(&bar_st_full[0]), 0, ctl);
         if (ok) {
           tc_fence_after();
           issue_sdp(0);
         }
       }
-      for (int it = 0; it < n_it && ok; ++it) {
+      for (int it = 0; it < n_it && ok; ++it) {  // ok is warp-uniform
         const int s = it % ST;
         if (it + 1 < n_it) {
           const int s1 = (it + 1) % ST;
-          ok = mbar_wait(smem_u32(&bar_st_full[s1]), ((it + 1) / ST) & 1, ctl);
-          if (ok) ok = mbar_wait(smem_u32(&bar_sdp_free), it & 1, ctl);
+          ok = mbar_wait_warp(smem_u32(&bar_st_full[s1]), ((it + 1) / ST) & 1, ctl);
+          if (ok) ok = mbar_wait_warp(smem_u32(&bar_sdp_free), it & 1, ctl);
           if (!ok) break;
           tc_fence_after();
           issue_sdp(s1);
+          ATTN_TRACE_EV(tc, 3, it + 1);  // S^T, dP^T issued
         }
-        ok = mbar_wait(smem_u32(&bar_pds_full), it & 1, ctl);
+        ok = mbar_wait_warp(smem_u32(&bar_pds_full), it & 1, ctl);
         if (!ok) break;
+        ATTN_TRACE_EV(tc, 4, it);  // P, dS ready seen
         tc_fence_after();
-        const uint32_t sq = stage_q(s), sdo = stage_do(s);
+        const uint64_t dq_mn = sw128_desc(stage_q(s), BQ * 128, 1024);
+        const uint64_t ddo_mn = sw128_desc(stage_do(s), BQ * 128, 1024);
         // dV += (P_hi + P_lo)^T dO_i  (A from TMEM: 16 query columns = 8 TMEM columns a step)
         // dK += (dS_hi + dS_lo)^T Q_i
 #pragma unroll
         for (int kk = 0; kk < BQ / 16; ++kk) {
           const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
-          const uint64_t bdo = sw128_desc(sdo + kk * 2048, BQ * 128, 1024);
-          const uint64_t bq = sw128_desc(sq + kk * 2048, BQ * 128, 1024);
-          mma_ts(tmem + C::TM_DV, tmem + C::TM_P_HI + kk * 8, bdo, idesc_kv, acc);
-          mma_ts(tmem + C::TM_DV, tmem + C::TM_P_LO + kk * 8, bdo, idesc_kv, 1u);
-          mma_ss(tmem + C::TM_DK, sw128_desc(sDsHi + kk * 32, 16, 1024), bq, idesc_kv, acc);
-          mma_ss(tmem + C::TM_DK, sw128_desc(sDsLo + kk * 32, 16, 1024), bq, idesc_kv, 1u);
+          const uint64_t bdo = add(ddo_mn, kk * 2048);
+          const uint64_t bq = add(dq_mn, kk * 2048);
+          mma_ts_el(tmem + C::TM_DV, tmem + C::TM_P_HI + kk * 8, bdo, idesc_kv, acc);
+          mma_ts_el(tmem + C::TM_DV, tmem + C::TM_P_LO + kk * 8, bdo, idesc_kv, 1u);
+          mma_ss_el(tmem + C::TM_DK, add(dDsHi_k, kk * 32), bq, idesc_kv, acc);
+          mma_ss_el(tmem + C::TM_DK, add(dDsLo_k, kk * 32), bq, idesc_kv, 1u);
         }
+        // Q_i and dO_i are not read again: hand the stage back to the producer.
+        mma_commit_el(smem_u32(&bar_st_empty[s]));
+        ATTN_TRACE_EV(tc, 5, it);  // dV, dK issued
         if (it >= 1) {
-          ok = mbar_wait(smem_u32(&bar_dq_free), (it - 1) & 1, ctl);
+          ok = mbar_wait_warp(smem_u32(&bar_dq_free), (it - 1) & 1, ctl);
           if (!ok) break;
           tc_fence_after();
         }
         // dQ^T[d][q] = sum over keys of K[key][d] (dS_hi + dS_lo)^T[key][q]
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk) {
-          const uint64_t ak = sw128_desc(sK + kk * 2048, BK * 128, 1024);
-          mma_ss(tmem + C::TM_DQ, ak, sw128_desc(sDsHi + kk * 2048, BK * 128, 1024), idesc_dq,
-                 kk > 0);
-          mma_ss(tmem + C::TM_DQ, ak, sw128_desc(sDsLo + kk * 2048, BK * 128, 1024), idesc_dq,
-                 1u);
+          const uint64_t ak = add(dK_mn, kk * 2048);
+          mma_ss_el(tmem + C::TM_DQ, ak, add(dDsHi_mn, kk * 2048), idesc_dq, kk > 0);
+          mma_ss_el(tmem + C::TM_DQ, ak, add(dDsLo_mn, kk * 2048), idesc_dq, 1u);
         }
-        mma_commit(smem_u32(&bar_dq_full));
-        mma_commit(smem_u32(&bar_pds_free));
-        mma_commit(smem_u32(&bar_st_empty[s]));
+        mma_commit_el(smem_u32(&bar_dq_full));
+        mma_commit_el(smem_u32(&bar_pds_free));
+        ATTN_TRACE_EV(tc, 6, it);  // dQ issued
       }
-      mma_commit(smem_u32(&bar_mma_done));
+      mma_commit_el(smem_u32(&bar_mma_done));
       if (!ok) mbar_wait_drain(smem_u32(&bar_mma_done), 0, 50000000ull);
     }
     __syncwarp();
@@ -321,9 +353,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     const uint32_t lane_base = static_cast<uint32_t>((warp % 4) * 32) << 16;
     const bool key_valid = key < p.S;
     bool ok = true;
+    TraceCursor tc;
+    if (lane == 0 && (warp == 0 || warp == 4)) ATTN_TRACE_INIT(tc, 2 + warp / 4);
     for (int it = 0; it < n_it; ++it) {
       const int s = it % ST;
       const int q0 = (i_start + it % niq) * BQ;
+      ATTN_TRACE_EV(tc, 1, it);
       ok = mbar_wait_warp(smem_u32(&bar_sdp_full), it & 1, ctl);
       if (ok) ok = mbar_wait_warp(smem_u32(&bar_st_full[s]), (it / ST) & 1, ctl);
       if (!ok) break;
@@ -337,6 +372,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(smem_u32(&bar_sdp_free));
+      ATTN_TRACE_EV(tc, 2, it);  // S^T, dP^T loaded
       uint32_t ph[HALF / 2], pl[HALF / 2], dh[HALF / 2], dl[HALF / 2];
 #pragma unroll
       for (int c = 0; c < HALF; c += 2) {
@@ -352,11 +388,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         split_bf16x2(pr[0], pr[1], ph[c / 2], pl[c / 2]);
         split_bf16x2(dr[0], dr[1], dh[c / 2], dl[c / 2]);
       }
+      ATTN_TRACE_EV(tc, 3, it);  // P, dS computed
       // The MMAs of the previous tile must be done with P (TMEM) and dS (smem).
       if (it >= 1) {
         ok = mbar_wait_warp(smem_u32(&bar_pds_free), (it - 1) & 1, ctl);
         if (!ok) break;
       }
+      ATTN_TRACE_EV(tc, 4, it);  // previous MMAs done
       tmem_st16(tmem + lane_base + C::TM_P_HI + cg * (HALF / 2), ph);
       tmem_st16(tmem + lane_base + C::TM_P_LO + cg * (HALF / 2), pl);
       // Row r of dS^T, K-major with 128-byte swizzle: 64 query columns per
@@ -371,6 +409,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       fence_async_smem();
       tc_fence_before();
       mbar_arrive(smem_u32(&bar_pds_full));
+      ATTN_TRACE_EV(tc, 5, it);  // P, dS stored and signalled
     }
     if (ok) ok = mbar_wait_warp(smem_u32(&bar_mma_done), 0, ctl);
     if (ok) {
@@ -402,11 +441,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     const uint32_t lane_base = static_cast<uint32_t>((warp % 4) * 32) << 16;
     float* stg = reinterpret_cast<float*>(smem + C::SMEM_DQS);
     bool ok = true;
+    TraceCursor tc;
+    if (t == 0) ATTN_TRACE_INIT(tc, 4);
     for (int it = 0; it < n_it; ++it) {
       const int h = g * p.G + it / niq;
       const int q0 = (i_start + it % niq) * BQ;
       ok = mbar_wait_warp(smem_u32(&bar_dq_full), it & 1, ctl);
       if (!ok) break;
+      ATTN_TRACE_EV(tc, 1, it);  // dQ landed
       tc_fence_after();
       uint32_t u[BQ];
       tmem_ld32(tmem + lane_base + C::TM_DQ, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
@@ -414,19 +456,24 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(smem_u32(&bar_dq_free));
-      if (t == 0) bulk_wait_read_all();  // the previous reduction has read the staging tile
-      named_bar_sync(1, 128);
-      if (t < D) {
-        // staging [q][d] fp32, row-major (the TMA box layout); lane t holds column d = t.
 #pragma unroll
-        for (int q = 0; q < BQ; ++q) stg[q * D + t] = __uint_as_float(u[q]);
+      for (int half = 0; half < 2; ++half) {
+        if (t == 0) bulk_wait_read_all();  // the previous reduction has read the staging tile
+        named_bar_sync(1, 128);
+        if (t < D) {
+          // staging [32 q][D] fp32, row-major (the TMA box layout); lane t holds column d = t.
+#pragma unroll
+          for (int q = 0; q < C::DQ_ROWS; ++q)
+            stg[q * D + t] = __uint_as_float(u[half * C::DQ_ROWS + q]);
+        }
+        fence_async_smem();
+        named_bar_sync(1, 128);
+        if (t == 0) {
+          tma_reduce_add_4d(&tm_dq, 0, h, q0 + half * C::DQ_ROWS, b, sDQS);
+          bulk_commit_group();
+        }
       }
-      fence_async_smem();
-      named_bar_sync(1, 128);
-      if (t == 0) {
-        tma_reduce_add_4d(&tm_dq, 0, h, q0, b, sDQS);
-        bulk_commit_group();
-      }
+      ATTN_TRACE_EV(tc, 2, it);  // both halves handed to the reduction
     }
     if (t == 0) bulk_wait_all();
   }
@@ -488,3 +535,17 @@ cudaError_t launch_bwd_main(int D, const CUtensorMap& tq, const CUtensorMap& tk,
 }
 
 }  // namespace attn
+
+#ifdef ATTN_TRACE
+// Trace build only: copies the backward main kernel's timeline records out and clears them.
+extern "C" int attn_trace_copy_bwd(void* host, size_t bytes) {
+  const size_t total = sizeof(attn::g_attn_trace);
+  if (bytes < total) return 1;
+  if (cudaDeviceSynchronize() != cudaSuccess) return 3;
+  if (cudaMemcpyFromSymbol(host, attn::g_attn_trace, total) != cudaSuccess) return 3;
+  static unsigned long long zeros[4096];
+  for (size_t off = 0; off < total; off += sizeof(zeros))
+    if (cudaMemcpyToSymbol(attn::g_attn_trace, zeros, sizeof(zeros), off) != cudaSuccess) return 3;
+  return 0;
+}
+#endif

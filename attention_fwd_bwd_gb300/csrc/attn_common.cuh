@@ -58,7 +58,7 @@ struct FwdParams {
 
 // ---------------------------------------------------------------- backward
 // One CTA per (batch, kv head, 128-key tile): K_j and V_j stay resident, the
-// group's query heads and their 64-row query tiles stream through a two-stage
+// group's query heads and their 64-row query tiles stream through a three-stage
 // ring holding Q_i, dO_i and the rows' log2-scaled LSE and Dvec. dK_j and dV_j
 // accumulate in TMEM over the whole loop; dQ tiles are added into the fp32
 // dq output with TMA tensor reductions.
@@ -79,11 +79,12 @@ struct BwdCfg {
   static constexpr int K_BYTES = BK * 128 * 2;       // always two 64-column chunks
   static constexpr int V_BYTES = BK * D * 2;
   static constexpr int Q_BYTES = BQ * D * 2;
-  static constexpr int STAGES = 2;
+  static constexpr int STAGES = 3;
   static constexpr int ROWVEC_BYTES = BQ * 4;
   static constexpr int STAGE_BYTES = ((2 * Q_BYTES + 2 * ROWVEC_BYTES) + 1023) / 1024 * 1024;
   static constexpr int DS_BYTES = BK * BQ * 2;       // one bf16 dS^T tile (hi or lo)
-  static constexpr int DQS_BYTES = BQ * D * 4;       // dQ staging tile, fp32
+  static constexpr int DQ_ROWS = BQ / 2;            // dQ leaves in two halves of 32 rows
+  static constexpr int DQS_BYTES = DQ_ROWS * D * 4;  // dQ staging half-tile, fp32
   static constexpr int SMEM_K = 0;
   static constexpr int SMEM_V = SMEM_K + K_BYTES;
   static constexpr int SMEM_STAGE = SMEM_V + V_BYTES;
@@ -133,6 +134,40 @@ inline BwdWorkspace bwd_workspace_layout(int B, int Hq, int S) {
   w.total = w.off_dvec + al(rows * 4);
   return w;
 }
+
+// ---------------------------------------------------------------- tracing
+// Timeline tracing for kernel tuning, compiled in only with -DATTN_TRACE (the
+// regular build has none of it). Each traced CTA (blockIdx.x == 0, first
+// kTraceCtas values of blockIdx.y) gets kTraceRoles streams of
+// kTraceEvents 64-bit records: event code (bits 56..63), iteration
+// (bits 40..55) and the SM clock (bits 0..39).
+constexpr int kTraceCtas = 64;
+constexpr int kTraceRoles = 8;
+constexpr int kTraceEvents = 2048;
+#ifdef ATTN_TRACE
+// Each kernel source that traces defines its own buffer named g_attn_trace.
+struct TraceCursor {
+  unsigned long long* base = nullptr;
+  int n = 0;
+  __device__ void init(unsigned long long* buf, int role) {
+    if (blockIdx.x == 0 && blockIdx.y < kTraceCtas)
+      base = buf + (static_cast<size_t>(blockIdx.y) * kTraceRoles + role) * kTraceEvents;
+  }
+  __device__ void ev(int code, int it) {
+    if (base && n < kTraceEvents) {
+      const unsigned long long c = clock64();
+      base[n++] = (static_cast<unsigned long long>(code) << 56) |
+                  (static_cast<unsigned long long>(it & 0xFFFF) << 40) | (c & 0xFFFFFFFFFFull);
+    }
+  }
+};
+#define ATTN_TRACE_INIT(tc, role) (tc).init(g_attn_trace, role)
+#define ATTN_TRACE_EV(tc, code, it) (tc).ev((code), (it))
+#else
+struct TraceCursor {};
+#define ATTN_TRACE_INIT(tc, role) ((void)0)
+#define ATTN_TRACE_EV(tc, code, it) ((void)0)
+#endif
 
 // ---------------------------------------------------------------- launchers
 cudaError_t launch_fwd(int D, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,

@@ -31,6 +31,10 @@ using namespace ptx;
 
 namespace {
 
+#ifdef ATTN_TRACE
+static __device__ unsigned long long g_attn_trace[kTraceCtas * kTraceRoles * kTraceEvents];
+#endif
+
 // Rescale threshold in log2 units: the running max used for exponentiation
 // only moves when the true max exceeds it by more than this, which keeps every
 // p <= 2^8 and leaves the result exact after the final division by l.
@@ -96,73 +100,86 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
 
   if (warp == 4) {
     // ------------------------------------------------------------ producer
+    // The whole warp runs this loop; each copy is issued by one elected lane.
+    TraceCursor tc;
+    if (lane == 0) ATTN_TRACE_INIT(tc, 0);
+    ATTN_TRACE_EV(tc, 1, 0);
     if (lane == 0) {
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
-      const uint64_t keep = policy_evict_last();  // K/V tiles are re-read by G heads x tiles
-      mbar_arrive_expect_tx(smem_u32(&bar_q_full), C::Q_BYTES);
-      for (int c = 0; c < C::KCH; ++c)
-        tma_load_4d(sQ + c * (C::BQ * 128), &tm_q, smem_u32(&bar_q_full), c * 64, hq, q0, b);
-      int issued = 0;
-      bool ok = true;
-      for (int idx = 0; idx < 2 * n_kv && ok; ++idx) {
-        const int slot = idx % C::NSLOT, round = idx / C::NSLOT;
-        if (round > 0) ok = mbar_wait(smem_u32(&bar_kv_empty[slot]), (round - 1) & 1, ctl);
-        if (!ok) break;
-        const uint32_t full = smem_u32(&bar_kv_full[slot]);
-        const uint32_t dst = sRing + slot * C::KV_BYTES;
-        const CUtensorMap* m = (idx & 1) ? &tm_v : &tm_k;
-        mbar_arrive_expect_tx(full, C::KV_BYTES);
-        for (int c = 0; c < C::KCH; ++c)
-          tma_load_4d_hint(dst + c * (C::BK * 128), m, full, c * 64, g, (idx >> 1) * C::BK, b,
-                           keep);
-        issued = idx + 1;
-      }
-      if (!ok) {
-        // Let in-flight copies land before the CTA's shared memory goes away.
-        for (int idx = max(0, issued - C::NSLOT); idx < issued; ++idx)
-          mbar_wait_drain(smem_u32(&bar_kv_full[idx % C::NSLOT]), (idx / C::NSLOT) & 1,
-                          50000000ull);
-      }
     }
+    const uint64_t keep = policy_evict_last();  // K/V tiles are re-read by G heads x tiles
+    mbar_arrive_expect_tx_el(smem_u32(&bar_q_full), C::Q_BYTES);
+    for (int c = 0; c < C::KCH; ++c)
+      tma_load_4d_el(sQ + c * (C::BQ * 128), &tm_q, smem_u32(&bar_q_full), c * 64, hq, q0, b);
+    int issued = 0;
+    bool ok = true;
+    for (int idx = 0; idx < 2 * n_kv; ++idx) {
+      const int slot = idx % C::NSLOT, round = idx / C::NSLOT;
+      if (round > 0) ok = mbar_wait_warp(smem_u32(&bar_kv_empty[slot]), (round - 1) & 1, ctl);
+      if (!ok) break;
+      ATTN_TRACE_EV(tc, 2, idx);  // slot free, issuing the load
+      const uint32_t full = smem_u32(&bar_kv_full[slot]);
+      const uint32_t dst = sRing + slot * C::KV_BYTES;
+      const CUtensorMap* m = (idx & 1) ? &tm_v : &tm_k;
+      mbar_arrive_expect_tx_el(full, C::KV_BYTES);
+      for (int c = 0; c < C::KCH; ++c)
+        tma_load_4d_hint_el(dst + c * (C::BK * 128), m, full, c * 64, g, (idx >> 1) * C::BK, b,
+                            keep);
+      issued = idx + 1;
+    }
+    if (!ok && lane == 0) {
+      // Let in-flight copies land before the CTA's shared memory goes away.
+      for (int idx = max(0, issued - C::NSLOT); idx < issued; ++idx)
+        mbar_wait_drain(smem_u32(&bar_kv_full[idx % C::NSLOT]), (idx / C::NSLOT) & 1,
+                        50000000ull);
+    }
+    __syncwarp();
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
+    // The whole warp runs this loop and builds the (warp-uniform) descriptors;
+    // each MMA and commit is issued by one elected lane.
+    TraceCursor tc;
+    if (lane == 0) ATTN_TRACE_INIT(tc, 1);
     bool ok = mbar_wait_warp(smem_u32(&bar_q_full), 0, ctl);
-    if (lane == 0 && ok) {
+    if (ok) {
+      ATTN_TRACE_EV(tc, 1, 0);
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
       constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, 0, 1);
-      for (int j = 0; j <= n_kv && ok; ++j) {
+      const uint64_t dq_desc = sw128_desc(sQ, 16, 1024);
+      for (int j = 0; j <= n_kv; ++j) {
         if (j < n_kv) {
           const int idx = 2 * j, slot = idx % C::NSLOT;
-          ok = mbar_wait(smem_u32(&bar_kv_full[slot]), (idx / C::NSLOT) & 1, ctl);
+          ok = mbar_wait_warp(smem_u32(&bar_kv_full[slot]), (idx / C::NSLOT) & 1, ctl);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t sK = sRing + slot * C::KV_BYTES;
+          const uint64_t dk = sw128_desc(sRing + slot * C::KV_BYTES, 16, 1024);
           const uint32_t d_s = tmem + ((j & 1) ? C::TM_S1 : C::TM_S0);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t koff = (kk >> 2) * (128 * 128) + (kk & 3) * 32;
-            mma_ss(d_s, sw128_desc(sQ + koff, 16, 1024), sw128_desc(sK + koff, 16, 1024),
-                   idesc_s, kk > 0);
+            const uint32_t koff = ((kk >> 2) * (128 * 128) + (kk & 3) * 32) >> 4;
+            mma_ss_el(d_s, dq_desc + koff, dk + koff, idesc_s, kk > 0);
           }
-          mma_commit(smem_u32(&bar_s_full[j & 1]));
-          mma_commit(smem_u32(&bar_kv_empty[slot]));
+          mma_commit_el(smem_u32(&bar_s_full[j & 1]));
+          mma_commit_el(smem_u32(&bar_kv_empty[slot]));
+          ATTN_TRACE_EV(tc, 3, j);  // S_j issued
         }
         if (j >= 1) {
           const int jj = j - 1, pb = jj & 1;
-          ok = mbar_wait(smem_u32(&bar_p_full[pb]), (jj >> 1) & 1, ctl);
+          ok = mbar_wait_warp(smem_u32(&bar_p_full[pb]), (jj >> 1) & 1, ctl);
           if (!ok) break;
+          ATTN_TRACE_EV(tc, 4, jj);  // P_jj ready seen
           const int idx = 2 * jj + 1, slot = idx % C::NSLOT;
-          ok = mbar_wait(smem_u32(&bar_kv_full[slot]), (idx / C::NSLOT) & 1, ctl);
+          ok = mbar_wait_warp(smem_u32(&bar_kv_full[slot]), (idx / C::NSLOT) & 1, ctl);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t sV = sRing + slot * C::KV_BYTES;
+          const uint64_t dv = sw128_desc(sRing + slot * C::KV_BYTES, C::BK * 128, 1024);
           const uint32_t a_p = tmem + (pb ? C::TM_P1 : C::TM_P0);
 #pragma unroll
           for (int kk = 0; kk < C::BK / 16; ++kk) {
-            mma_ts(tmem + C::TM_O, a_p + kk * 8, sw128_desc(sV + kk * 2048, C::BK * 128, 1024),
-                   idesc_o, (jj > 0 || kk > 0) ? 1u : 0u);
+            mma_ts_el(tmem + C::TM_O, a_p + kk * 8, dv + ((kk * 2048) >> 4), idesc_o,
+                      (jj > 0 || kk > 0) ? 1u : 0u);
           }
           if (split) {
             // O += P_lo V_j: the low-order bf16 part of P, stored over the
@@ -170,17 +187,17 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
             const uint32_t a_lo = tmem + (pb ? C::TM_S1 : C::TM_S0);
 #pragma unroll
             for (int kk = 0; kk < C::BK / 16; ++kk)
-              mma_ts(tmem + C::TM_O, a_lo + kk * 8, sw128_desc(sV + kk * 2048, C::BK * 128, 1024),
-                     idesc_o, 1u);
+              mma_ts_el(tmem + C::TM_O, a_lo + kk * 8, dv + ((kk * 2048) >> 4), idesc_o, 1u);
           }
-          mma_commit(smem_u32(&bar_pv_done[pb]));
-          mma_commit(smem_u32(&bar_kv_empty[slot]));
+          mma_commit_el(smem_u32(&bar_pv_done[pb]));
+          mma_commit_el(smem_u32(&bar_kv_empty[slot]));
+          ATTN_TRACE_EV(tc, 5, jj);  // PV_jj issued
         }
       }
       if (!ok) {
         // Wait for the MMAs already issued before TMEM is released. bar_q_full
         // has completed its only phase, so this commit completes phase 1.
-        mma_commit(smem_u32(&bar_q_full));
+        mma_commit_el(smem_u32(&bar_q_full));
         mbar_wait_drain(smem_u32(&bar_q_full), 1, 50000000ull);
       }
     }
@@ -192,12 +209,19 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     float m = -INFINITY;  // running max in log2 units (scaled scores)
     float l = 0.f;
+    const float sl2 = p.scale_log2;
+    const bool pos = sl2 >= 0.f;
+    TraceCursor tc;
+    if (lane == 0) ATTN_TRACE_INIT(tc, 2 + warp);
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
       const int sb = j & 1;
+      ATTN_TRACE_EV(tc, 1, j);  // start waiting for S_j
       ok = mbar_wait_warp(smem_u32(&bar_s_full[sb]), (j >> 1) & 1, ctl);
       if (!ok) break;
+      ATTN_TRACE_EV(tc, 2, j);  // S_j landed
       tc_fence_after();
+      // Raw scores of this row; the scale is folded into the exponent below.
       float x[C::BK];
       {
         const uint32_t ts = tmem + lane_base + (sb ? C::TM_S1 : C::TM_S0);
@@ -207,38 +231,78 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           tmem_ld32(ts + c, *reinterpret_cast<uint32_t(*)[32]>(&u[c]));
         tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < C::BK; ++c) x[c] = __uint_as_float(u[c]) * p.scale_log2;
+        for (int c = 0; c < C::BK; ++c) x[c] = __uint_as_float(u[c]);
       }
       const int k0 = j * C::BK;
       const bool need_mask = (p.causal && k0 + C::BK - 1 > q0) || (k0 + C::BK > p.S);
-      if (need_mask) {
-        const int lim = p.causal ? min(qrow, p.S - 1) : (p.S - 1);
+      const int lim = p.causal ? min(qrow, p.S - 1) : (p.S - 1);  // last visible key
+      // Largest scaled score: the max of the raw scores for scale >= 0, the min
+      // for scale < 0 (masked keys pushed to the losing end).
+      float mraw;
+      {
+        const float lose = pos ? -INFINITY : INFINITY;
+        if (need_mask) {
 #pragma unroll
-        for (int c = 0; c < C::BK; ++c)
-          if (k0 + c > lim) x[c] = -INFINITY;
+          for (int c = 0; c < C::BK; ++c)
+            if (k0 + c > lim) x[c] = lose;
+        }
+        float a[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) a[i] = x[i];
+        if (pos) {
+#pragma unroll
+          for (int c = 8; c < C::BK; c += 8)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) a[i] = fmaxf(a[i], x[c + i]);
+#pragma unroll
+          for (int w = 4; w > 0; w >>= 1)
+#pragma unroll
+            for (int i = 0; i < w; ++i) a[i] = fmaxf(a[i], a[i + w]);
+        } else {
+#pragma unroll
+          for (int c = 8; c < C::BK; c += 8)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) a[i] = fminf(a[i], x[c + i]);
+#pragma unroll
+          for (int w = 4; w > 0; w >>= 1)
+#pragma unroll
+            for (int i = 0; i < w; ++i) a[i] = fminf(a[i], a[i + w]);
+        }
+        mraw = a[0];
       }
-      float mx = x[0];
-#pragma unroll
-      for (int c = 1; c < C::BK; ++c) mx = fmaxf(mx, x[c]);
+      const float mx = mraw * sl2;
       float alpha = 1.f;
       const bool rescale = mx > m + kRescaleThreshold;
       if (rescale) {
         alpha = ex2(m - mx);  // m = -inf on the first tile gives 0
         m = mx;
       }
-      float sum = 0.f;
+      const float neg_m = -m;
+      float sums[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) sums[i] = 0.f;
       uint32_t pk[C::BK / 2];
 #pragma unroll
       for (int c = 0; c < C::BK; c += 2) {
-        const float p0 = ex2(x[c] - m);
-        const float p1 = ex2(x[c + 1] - m);
-        sum += p0 + p1;
+        float p0 = ex2(fmaf(x[c], sl2, neg_m));
+        float p1 = ex2(fmaf(x[c + 1], sl2, neg_m));
+        if (need_mask) {
+          if (k0 + c > lim) p0 = 0.f;
+          if (k0 + c + 1 > lim) p1 = 0.f;
+        }
+        sums[(c / 2) & 7] += p0 + p1;
         pk[c / 2] = pack_bf16x2(p0, p1);
         // Keep what bf16 dropped, in x (x is not needed any more).
         x[c] = p0 - __uint_as_float(pk[c / 2] << 16);
         x[c + 1] = p1 - __uint_as_float(pk[c / 2] & 0xFFFF0000u);
       }
+#pragma unroll
+      for (int w = 4; w > 0; w >>= 1)
+#pragma unroll
+        for (int i = 0; i < w; ++i) sums[i] += sums[i + w];
+      const float sum = sums[0];
       l = l * alpha + sum;
+      ATTN_TRACE_EV(tc, 3, j);  // exponentials done
       // P buffer sb was last read by PV_{j-2}.
       if (j >= 2) {
         ok = mbar_wait_warp(smem_u32(&bar_pv_done[sb]), ((j - 2) >> 1) & 1, ctl);
@@ -278,6 +342,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(smem_u32(&bar_p_full[sb]));
+      ATTN_TRACE_EV(tc, 4, j);  // P_j stored and signalled
     }
     if (ok && n_kv > 0) {
       const int jl = n_kv - 1;
@@ -355,3 +420,17 @@ cudaError_t launch_fwd(int D, const CUtensorMap& tq, const CUtensorMap& tk, cons
 }
 
 }  // namespace attn
+
+#ifdef ATTN_TRACE
+// Trace build only: copies the forward kernel's timeline records out and clears them.
+extern "C" int attn_trace_copy_fwd(void* host, size_t bytes) {
+  const size_t total = sizeof(attn::g_attn_trace);
+  if (bytes < total) return 1;
+  if (cudaDeviceSynchronize() != cudaSuccess) return 3;
+  if (cudaMemcpyFromSymbol(host, attn::g_attn_trace, total) != cudaSuccess) return 3;
+  static unsigned long long zeros[4096];
+  for (size_t off = 0; off < total; off += sizeof(zeros))
+    if (cudaMemcpyToSymbol(attn::g_attn_trace, zeros, sizeof(zeros), off) != cudaSuccess) return 3;
+  return 0;
+}
+#endif

@@ -116,14 +116,6 @@ __device__ __forceinline__ void st_sw128(uint32_t tile, int row, int u, uint4 v)
                : "memory");
 }
 
-// x as a pair of bf16 values hi + lo with hi = bf16(x), lo = bf16(x - hi).
-__device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
-  hi = pack_bf16x2(x0, x1);
-  const float h0 = __uint_as_float(hi << 16);
-  const float h1 = __uint_as_float(hi & 0xFFFF0000u);
-  lo = pack_bf16x2(x0 - h0, x1 - h1);
-}
-
 template <int D>
 __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -385,8 +377,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           pr[e] = pv;
           dr[e] = p.scale * pv * (__uint_as_float(ud[c + e]) - dvec[col]);
         }
-        split_bf16x2(pr[0], pr[1], ph[c / 2], pl[c / 2]);
-        split_bf16x2(dr[0], dr[1], dh[c / 2], dl[c / 2]);
+        split_bf16x2_trunc(pr[0], pr[1], ph[c / 2], pl[c / 2]);
+        split_bf16x2_trunc(dr[0], dr[1], dh[c / 2], dl[c / 2]);
       }
       ATTN_TRACE_EV(tc, 3, it);  // P, dS computed
       // The MMAs of the previous tile must be done with P (TMEM) and dS (smem).

@@ -21,8 +21,9 @@
 //       and, when m grew by more than 2^8, rescales its O row in TMEM first.
 //       The final m and l give O = acc / l and LSE = (m + log2 l) ln 2.
 // When the caller asks for the output residual o_lo = bf16(O - o) (training,
-// where the backward needs rowsum(dO * O) beyond bf16 accuracy), P also goes
-// through a second MMA as its low-order bf16 part, O += P_lo V_j.
+// where the backward needs rowsum(dO * O) beyond bf16 accuracy), P is split
+// into bf16 hi (P truncated) and lo (the truncated residual) parts and goes
+// through a second MMA, O += P_lo V_j, so O carries about 16 significant bits.
 #include "attn_common.cuh"
 #include "sm100_ptx.cuh"
 
@@ -40,7 +41,7 @@ static __device__ unsigned long long g_attn_trace[kTraceCtas * kTraceRoles * kTr
 // p <= 2^8 and leaves the result exact after the final division by l.
 constexpr float kRescaleThreshold = 8.0f;
 
-template <int D>
+template <int D, bool SPLIT>
 __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
@@ -91,9 +92,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_base_s;
   const WaitCtl ctl{&abort_flag, p.status, p.timeout_ns};
-  // With the residual output requested, P enters O += P V as a bf16 hi/lo
-  // pair, so O (and o + o_lo) carries about 16 significant bits.
-  const bool split = p.o_lo != nullptr;
+  // SPLIT (the residual output o_lo is requested): P enters O += P V as a
+  // bf16 hi/lo pair, so O (and o + o_lo) carries about 16 significant bits.
+  constexpr bool split = SPLIT;
 
   const uint32_t sQ = smem_u32(smem + C::SMEM_Q);
   const uint32_t sRing = smem_u32(smem + C::SMEM_RING);
@@ -181,7 +182,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
             mma_ts_el(tmem + C::TM_O, a_p + kk * 8, dv + ((kk * 2048) >> 4), idesc_o,
                       (jj > 0 || kk > 0) ? 1u : 0u);
           }
-          if (split) {
+          if constexpr (SPLIT) {
             // O += P_lo V_j: the low-order bf16 part of P, stored over the
             // first 64 columns of the score buffer it was computed from.
             const uint32_t a_lo = tmem + (pb ? C::TM_S1 : C::TM_S0);
@@ -278,23 +279,40 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         m = mx;
       }
       const float neg_m = -m;
+      // P buffer sb was last read by PV_{j-2}.
+      if (j >= 2) {
+        ok = mbar_wait_warp(smem_u32(&bar_pv_done[sb]), ((j - 2) >> 1) & 1, ctl);
+        if (!ok) break;
+      }
       float sums[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) sums[i] = 0.f;
-      uint32_t pk[C::BK / 2];
+      const uint32_t tp = tmem + lane_base + (sb ? C::TM_P1 : C::TM_P0);
+      // With SPLIT, P_lo goes over columns 0..63 of this tile's score buffer,
+      // whose scores this thread has already read; the next MMA to write that
+      // buffer (S_{j+2}) issues after PV_j and tcgen05 MMAs run in issue order.
+      const uint32_t tl = tmem + lane_base + (sb ? C::TM_S1 : C::TM_S0);
 #pragma unroll
-      for (int c = 0; c < C::BK; c += 2) {
-        float p0 = ex2(fmaf(x[c], sl2, neg_m));
-        float p1 = ex2(fmaf(x[c + 1], sl2, neg_m));
-        if (need_mask) {
-          if (k0 + c > lim) p0 = 0.f;
-          if (k0 + c + 1 > lim) p1 = 0.f;
+      for (int ch = 0; ch < C::BK; ch += 32) {
+        uint32_t pk[16];
+        uint32_t pl[SPLIT ? 16 : 1];
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          float p0 = ex2(fmaf(x[ch + c], sl2, neg_m));
+          float p1 = ex2(fmaf(x[ch + c + 1], sl2, neg_m));
+          if (need_mask) {
+            if (k0 + ch + c > lim) p0 = 0.f;
+            if (k0 + ch + c + 1 > lim) p1 = 0.f;
+          }
+          sums[(c / 2) & 7] += p0 + p1;
+          if constexpr (SPLIT) {
+            split_bf16x2_trunc(p0, p1, pk[c / 2], pl[c / 2]);
+          } else {
+            pk[c / 2] = pack_bf16x2(p0, p1);
+          }
         }
-        sums[(c / 2) & 7] += p0 + p1;
-        pk[c / 2] = pack_bf16x2(p0, p1);
-        // Keep what bf16 dropped, in x (x is not needed any more).
-        x[c] = p0 - __uint_as_float(pk[c / 2] << 16);
-        x[c + 1] = p1 - __uint_as_float(pk[c / 2] & 0xFFFF0000u);
+        tmem_st16(tp + ch / 2, pk);
+        if constexpr (SPLIT) tmem_st16(tl + ch / 2, *reinterpret_cast<uint32_t(*)[16]>(&pl[0]));
       }
 #pragma unroll
       for (int w = 4; w > 0; w >>= 1)
@@ -303,26 +321,6 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       const float sum = sums[0];
       l = l * alpha + sum;
       ATTN_TRACE_EV(tc, 3, j);  // exponentials done
-      // P buffer sb was last read by PV_{j-2}.
-      if (j >= 2) {
-        ok = mbar_wait_warp(smem_u32(&bar_pv_done[sb]), ((j - 2) >> 1) & 1, ctl);
-        if (!ok) break;
-      }
-      {
-        const uint32_t tp = tmem + lane_base + (sb ? C::TM_P1 : C::TM_P0);
-        tmem_st32(tp, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-        tmem_st32(tp + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
-        if (split) {
-          // P_lo over columns 0..63 of this tile's score buffer, whose scores
-          // this thread has already read; the next MMA to write the buffer
-          // (S_{j+2}) issues after PV_j and tcgen05 MMAs run in issue order.
-#pragma unroll
-          for (int c = 0; c < C::BK; c += 2) pk[c / 2] = pack_bf16x2(x[c], x[c + 1]);
-          const uint32_t tl = tmem + lane_base + (sb ? C::TM_S1 : C::TM_S0);
-          tmem_st32(tl, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-          tmem_st32(tl + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
-        }
-      }
       // Rescale this warp's O rows once PV_{j-1} has landed in TMEM.
       if (j >= 1 && __any_sync(0xffffffffu, rescale)) {
         ok = mbar_wait_warp(smem_u32(&bar_pv_done[(j - 1) & 1]), ((j - 1) >> 1) & 1, ctl);
@@ -392,7 +390,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   if (warp == 5) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
-template <int D>
+template <int D, bool SPLIT>
 cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const FwdParams& p, cudaStream_t stream) {
   using C = FwdCfg<D>;
@@ -400,14 +398,14 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D>,
+    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D, SPLIT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
   dim3 grid(p.B * p.Hq, p.n_qtiles);
-  attn_fwd_kernel<D><<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(tq, tk, tv, p);
+  attn_fwd_kernel<D, SPLIT><<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 
@@ -415,8 +413,12 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
 
 cudaError_t launch_fwd(int D, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const FwdParams& p, cudaStream_t stream) {
-  if (D == 128) return launch_fwd_t<128>(tq, tk, tv, p, stream);
-  return launch_fwd_t<64>(tq, tk, tv, p, stream);
+  const bool split = p.o_lo != nullptr;
+  if (D == 128)
+    return split ? launch_fwd_t<128, true>(tq, tk, tv, p, stream)
+                 : launch_fwd_t<128, false>(tq, tk, tv, p, stream);
+  return split ? launch_fwd_t<64, true>(tq, tk, tv, p, stream)
+               : launch_fwd_t<64, false>(tq, tk, tv, p, stream);
 }
 
 }  // namespace attn

@@ -403,6 +403,18 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
+// x as a pair of bf16 values hi + lo: hi = x with its low 16 bits cleared
+// (bf16 rounded toward zero), lo = the same truncation of the exact fp32
+// residual x - hi. hi + lo equals x to within 2^-14 relative. Both pairs are
+// packed with a byte permute (low half from x0), with no conversion instructions.
+__device__ __forceinline__ void split_bf16x2_trunc(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  const uint32_t u0 = __float_as_uint(x0), u1 = __float_as_uint(x1);
+  hi = __byte_perm(u0, u1, 0x7632);
+  const float r0 = x0 - __uint_as_float(u0 & 0xFFFF0000u);
+  const float r1 = x1 - __uint_as_float(u1 & 0xFFFF0000u);
+  lo = __byte_perm(__float_as_uint(r0), __float_as_uint(r1), 0x7632);
+}
+
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

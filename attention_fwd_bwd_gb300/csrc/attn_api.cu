@@ -201,7 +201,7 @@ static attn_status_t fwd_impl(const void* q, const void* k, const void* v, void*
   p.G = Hq / Hkv;
   p.causal = causal ? 1 : 0;
   p.scale_log2 = scale * kLog2e;
-  p.n_qtiles = (S + FwdCfg<128>::BQ - 1) / FwdCfg<128>::BQ;
+  p.n_qblocks = (S + 2 * FwdCfg<128>::BQ - 1) / (2 * FwdCfg<128>::BQ);
   p.status = status;
   p.timeout_ns = g_timeout_ns;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

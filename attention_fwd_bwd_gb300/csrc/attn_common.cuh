@@ -18,30 +18,31 @@ constexpr int kSeqPad = 128;
 __host__ __device__ constexpr int seq_pad(int S) { return (S + kSeqPad - 1) / kSeqPad * kSeqPad; }
 
 // ---------------------------------------------------------------- forward
-// One CTA per (batch, query head, 128-row query tile); K/V tiles of 128 keys
-// stream through a ring of shared-memory slots (K_j and V_j take one slot
-// each). Warps 0-3: softmax / rescale / epilogue (one query row per thread,
-// the row's TMEM lane); warp 4: TMA producer; warp 5: MMA issuer.
+// One CTA per (batch, query head, block of two 128-row query tiles); K/V tiles
+// of 128 keys stream through a ring of shared-memory slots (K_j and V_j take
+// one slot each) and serve both query tiles. Warps 0-3 / 4-7: softmax, rescale
+// and epilogue of query tile A / B (one query row per thread, the row's TMEM
+// lane); warp 8: TMA producer; warp 9: MMA issuer.
 template <int D>
 struct FwdCfg {
-  static constexpr int BQ = 128;
+  static constexpr int BQ = 128;                     // rows per query tile (two per CTA)
   static constexpr int BK = 128;
   static constexpr int KCH = D / 64;                 // 64-wide (128-byte) column chunks
-  static constexpr int Q_BYTES = BQ * D * 2;
+  static constexpr int Q_BYTES = BQ * D * 2;         // one query tile
   static constexpr int KV_BYTES = BK * D * 2;        // one K or V tile
-  static constexpr int NSLOT = (D == 128) ? 5 : 8;   // ring slots
+  static constexpr int NSLOT = (D == 128) ? 4 : 8;   // ring slots
   static constexpr int SMEM_Q = 0;
-  static constexpr int SMEM_RING = Q_BYTES;
-  static constexpr int SMEM_BYTES = Q_BYTES + NSLOT * KV_BYTES;
+  static constexpr int SMEM_RING = 2 * Q_BYTES;
+  static constexpr int SMEM_BYTES = 2 * Q_BYTES + NSLOT * KV_BYTES;
   static constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;  // slack for 1024-byte alignment
-  // Tensor-memory columns (fp32 unless noted).
-  static constexpr int TM_S0 = 0;      // scores, buffer 0 (128 cols)
-  static constexpr int TM_S1 = 128;    // scores, buffer 1
-  static constexpr int TM_O = 256;     // output accumulator (D cols)
-  static constexpr int TM_P0 = 384;    // bf16 probabilities, buffer 0 (64 cols)
-  static constexpr int TM_P1 = 448;    // buffer 1
+  // Tensor-memory columns per query tile t: scores S_t (128 fp32 columns,
+  // later overwritten by P_t: bf16 hi pairs in the first 64, lo pairs in the
+  // next 64) and the output accumulator O_t (D fp32 columns).
+  __host__ __device__ static constexpr int tm_s(int t) { return 256 * t; }
+  __host__ __device__ static constexpr int tm_o(int t) { return 256 * t + 128; }
   static constexpr int TMEM_COLS = 512;
-  static constexpr int THREADS = 192;
+  static constexpr int THREADS = 320;
+  static_assert(SMEM_ALLOC <= 232448, "shared-memory plan exceeds 227 KB");
 };
 
 struct FwdParams {
@@ -51,7 +52,7 @@ struct FwdParams {
   int B, Hq, Hkv, S, G;
   int causal;
   float scale_log2;  // scale * log2(e)
-  int n_qtiles;
+  int n_qblocks;     // blocks of two 128-row query tiles
   int* status;
   unsigned long long timeout_ns;
 };

@@ -6,20 +6,24 @@
 // with the query-tile loop outside and the key/value loop inside so the state
 // never leaves the SM.
 //
-// Per CTA (one 128-row query tile of one head):
-//   warp 4 (TMA producer): Q once, then K_0, V_0, K_1, V_1, ... into a ring of
-//       shared-memory slots, each slot guarded by a full/empty mbarrier pair
-//       (the GB300 counterpart of the paper's "issue N+1 loads, wait until at
-//       most N are outstanding" rule for its Tensor Data Mover, section 3.1.1).
-//   warp 5 (MMA issuer): S_j = Q K_j^T into one of two TMEM score buffers
-//       (both operands K-major, so K^T needs no transpose -- Table 3's first
-//       row), then O += P_j V_j with P read from TMEM and V_j described
-//       MN-major (the transposed-operand case of section 3.1.2, handled by
-//       the descriptor instead of a transpose).
-//   warps 0-3 (softmax): thread r owns query row r (TMEM lane r); it reads its
-//       score row, updates the running max m and sum l, writes bf16 P to TMEM
-//       and, when m grew by more than 2^8, rescales its O row in TMEM first.
-//       The final m and l give O = acc / l and LSE = (m + log2 l) ln 2.
+// Per CTA: two 128-row query tiles (A and B) of one head, sharing every K/V
+// tile that streams in.
+//   warp 8 (TMA producer): Q_A and Q_B once, then K_0, V_0, K_1, V_1, ... into
+//       a ring of shared-memory slots, each guarded by a full/empty mbarrier
+//       pair (the GB300 counterpart of the paper's "issue N+1 loads, wait
+//       until at most N are outstanding" rule for its Tensor Data Mover,
+//       section 3.1.1).
+//   warp 9 (MMA issuer): S_t = Q_t K_j^T into tile t's TMEM score buffer (both
+//       operands K-major, so K^T needs no transpose -- Table 3's first row),
+//       and O_t += P_t V_j with P read from TMEM and V_j described MN-major
+//       (the transposed-operand case of section 3.1.2, handled by the
+//       descriptor instead of a transpose). The two tiles alternate on the
+//       tensor core: while one tile's softmax runs, the other tile's MMAs do.
+//   warps 0-3 / 4-7 (softmax of tile A / B): thread r owns query row r of its
+//       tile (TMEM lane r); it reads its score row, updates the running max m
+//       and sum l, writes bf16 P over the scores in TMEM and, when m grew by
+//       more than 2^8, first rescales its O row. The final m and l give
+//       O = acc / l and LSE = (m + log2 l) ln 2.
 // When the caller asks for the output residual o_lo = bf16(O - o) (training,
 // where the backward needs rowsum(dO * O) beyond bf16 accuracy), P is split
 // into bf16 hi (P truncated) and lo (the truncated residual) parts and goes
@@ -64,10 +68,15 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   const int hq = bh % p.Hq;
   const int b = bh / p.Hq;
   const int g = hq / p.G;
-  const int qt = p.n_qtiles - 1 - static_cast<int>(blockIdx.y);  // longest causal rows first
-  const int q0 = qt * C::BQ;
+  const int qb = p.n_qblocks - 1 - static_cast<int>(blockIdx.y);  // longest causal rows first
+  const int q0 = qb * (2 * C::BQ);                                 // first row of tile A
   const int nkv_all = (p.S + C::BK - 1) / C::BK;
-  const int n_kv = p.causal ? min(qt + 1, nkv_all) : nkv_all;
+  // K/V tiles each query tile needs (tile t covers rows q0 + 128 t ...).
+  int n_kv_t[2];
+#pragma unroll
+  for (int t = 0; t < 2; ++t)
+    n_kv_t[t] = p.causal ? min((q0 + t * C::BQ) / C::BK + 1, nkv_all) : nkv_all;
+  const int n_kv = n_kv_t[1];  // tile B needs the most
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
@@ -76,14 +85,14 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       mbar_init(smem_u32(&bar_kv_full[i]), 1);
       mbar_init(smem_u32(&bar_kv_empty[i]), 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(&bar_s_full[i]), 1);
-      mbar_init(smem_u32(&bar_p_full[i]), 128);
-      mbar_init(smem_u32(&bar_pv_done[i]), 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(smem_u32(&bar_s_full[t]), 1);
+      mbar_init(smem_u32(&bar_p_full[t]), 128);
+      mbar_init(smem_u32(&bar_pv_done[t]), 1);
     }
     fence_barrier_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(smem_u32(&tmem_base_s), C::TMEM_COLS);
     tmem_relinquish();
   }
@@ -92,14 +101,11 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_base_s;
   const WaitCtl ctl{&abort_flag, p.status, p.timeout_ns};
-  // SPLIT (the residual output o_lo is requested): P enters O += P V as a
-  // bf16 hi/lo pair, so O (and o + o_lo) carries about 16 significant bits.
-  constexpr bool split = SPLIT;
 
-  const uint32_t sQ = smem_u32(smem + C::SMEM_Q);
+  const uint32_t sQ = smem_u32(smem + C::SMEM_Q);  // tile t at sQ + t * Q_BYTES
   const uint32_t sRing = smem_u32(smem + C::SMEM_RING);
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------------ producer
     // The whole warp runs this loop; each copy is issued by one elected lane.
     TraceCursor tc;
@@ -111,9 +117,11 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       prefetch_tmap(&tm_v);
     }
     const uint64_t keep = policy_evict_last();  // K/V tiles are re-read by G heads x tiles
-    mbar_arrive_expect_tx_el(smem_u32(&bar_q_full), C::Q_BYTES);
-    for (int c = 0; c < C::KCH; ++c)
-      tma_load_4d_el(sQ + c * (C::BQ * 128), &tm_q, smem_u32(&bar_q_full), c * 64, hq, q0, b);
+    mbar_arrive_expect_tx_el(smem_u32(&bar_q_full), 2 * C::Q_BYTES);
+    for (int t = 0; t < 2; ++t)
+      for (int c = 0; c < C::KCH; ++c)
+        tma_load_4d_el(sQ + t * C::Q_BYTES + c * (C::BQ * 128), &tm_q, smem_u32(&bar_q_full),
+                       c * 64, hq, q0 + t * C::BQ, b);
     int issued = 0;
     bool ok = true;
     for (int idx = 0; idx < 2 * n_kv; ++idx) {
@@ -137,7 +145,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
                         50000000ull);
     }
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     // The whole warp runs this loop and builds the (warp-uniform) descriptors;
     // each MMA and commit is issued by one elected lane.
@@ -149,51 +157,75 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
       constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, 0, 1);
       const uint64_t dq_desc = sw128_desc(sQ, 16, 1024);
-      for (int j = 0; j <= n_kv; ++j) {
-        if (j < n_kv) {
-          const int idx = 2 * j, slot = idx % C::NSLOT;
-          ok = mbar_wait_warp(smem_u32(&bar_kv_full[slot]), (idx / C::NSLOT) & 1, ctl);
-          if (!ok) break;
-          tc_fence_after();
-          const uint64_t dk = sw128_desc(sRing + slot * C::KV_BYTES, 16, 1024);
-          const uint32_t d_s = tmem + ((j & 1) ? C::TM_S1 : C::TM_S0);
+      // S_t = Q_t K_j^T into tile t's score buffer.
+      auto issue_s = [&](int t, int j) {
+        const int slot = (2 * j) % C::NSLOT;
+        const uint64_t dk = sw128_desc(sRing + slot * C::KV_BYTES, 16, 1024);
+        const uint64_t dq = dq_desc + ((t * C::Q_BYTES) >> 4);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t koff = ((kk >> 2) * (128 * 128) + (kk & 3) * 32) >> 4;
-            mma_ss_el(d_s, dq_desc + koff, dk + koff, idesc_s, kk > 0);
-          }
-          mma_commit_el(smem_u32(&bar_s_full[j & 1]));
-          mma_commit_el(smem_u32(&bar_kv_empty[slot]));
-          ATTN_TRACE_EV(tc, 3, j);  // S_j issued
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t koff = ((kk >> 2) * (128 * 128) + (kk & 3) * 32) >> 4;
+          mma_ss_el(tmem + C::tm_s(t), dq + koff, dk + koff, idesc_s, kk > 0);
         }
-        if (j >= 1) {
-          const int jj = j - 1, pb = jj & 1;
-          ok = mbar_wait_warp(smem_u32(&bar_p_full[pb]), (jj >> 1) & 1, ctl);
+        mma_commit_el(smem_u32(&bar_s_full[t]));
+      };
+      auto wait_kv = [&](int idx) {
+        return mbar_wait_warp(smem_u32(&bar_kv_full[idx % C::NSLOT]), (idx / C::NSLOT) & 1, ctl);
+      };
+      ok = wait_kv(0);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0, 0);
+        issue_s(1, 0);
+        mma_commit_el(smem_u32(&bar_kv_empty[0]));  // K_0 is done once both S_t(0) ran
+        ATTN_TRACE_EV(tc, 3, 0);
+      }
+      for (int j = 0; j < n_kv && ok; ++j) {
+        bool v_ready = false, k_next_ready = false;
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (j >= n_kv_t[t]) continue;
+          ok = mbar_wait_warp(smem_u32(&bar_p_full[t]), j & 1, ctl);
           if (!ok) break;
-          ATTN_TRACE_EV(tc, 4, jj);  // P_jj ready seen
-          const int idx = 2 * jj + 1, slot = idx % C::NSLOT;
-          ok = mbar_wait_warp(smem_u32(&bar_kv_full[slot]), (idx / C::NSLOT) & 1, ctl);
-          if (!ok) break;
-          tc_fence_after();
-          const uint64_t dv = sw128_desc(sRing + slot * C::KV_BYTES, C::BK * 128, 1024);
-          const uint32_t a_p = tmem + (pb ? C::TM_P1 : C::TM_P0);
-#pragma unroll
-          for (int kk = 0; kk < C::BK / 16; ++kk) {
-            mma_ts_el(tmem + C::TM_O, a_p + kk * 8, dv + ((kk * 2048) >> 4), idesc_o,
-                      (jj > 0 || kk > 0) ? 1u : 0u);
+          ATTN_TRACE_EV(tc, 4 + t, j);  // P_t(j) ready seen
+          if (!v_ready) {
+            ok = wait_kv(2 * j + 1);
+            if (!ok) break;
+            v_ready = true;
           }
+          tc_fence_after();
+          const int vslot = (2 * j + 1) % C::NSLOT;
+          const uint64_t dv = sw128_desc(sRing + vslot * C::KV_BYTES, C::BK * 128, 1024);
+          // P hi over columns 0..63 of the score buffer, P lo over 64..127.
+          const uint32_t a_p = tmem + C::tm_s(t);
+#pragma unroll
+          for (int kk = 0; kk < C::BK / 16; ++kk)
+            mma_ts_el(tmem + C::tm_o(t), a_p + kk * 8, dv + ((kk * 2048) >> 4), idesc_o,
+                      (j > 0 || kk > 0) ? 1u : 0u);
           if constexpr (SPLIT) {
-            // O += P_lo V_j: the low-order bf16 part of P, stored over the
-            // first 64 columns of the score buffer it was computed from.
-            const uint32_t a_lo = tmem + (pb ? C::TM_S1 : C::TM_S0);
 #pragma unroll
             for (int kk = 0; kk < C::BK / 16; ++kk)
-              mma_ts_el(tmem + C::TM_O, a_lo + kk * 8, dv + ((kk * 2048) >> 4), idesc_o, 1u);
+              mma_ts_el(tmem + C::tm_o(t), a_p + 64 + kk * 8, dv + ((kk * 2048) >> 4), idesc_o,
+                        1u);
           }
-          mma_commit_el(smem_u32(&bar_pv_done[pb]));
-          mma_commit_el(smem_u32(&bar_kv_empty[slot]));
-          ATTN_TRACE_EV(tc, 5, jj);  // PV_jj issued
+          if (j + 1 == n_kv_t[t]) mma_commit_el(smem_u32(&bar_pv_done[t]));
+          ATTN_TRACE_EV(tc, 6 + t, j);  // PV_t(j) issued
+          // The next score tile of t overwrites P_t(j) in TMEM; MMAs execute in
+          // issue order, so it runs after PV_t(j) has read P_t(j).
+          if (j + 1 < n_kv_t[t]) {
+            if (!k_next_ready) {
+              ok = wait_kv(2 * j + 2);
+              if (!ok) break;
+              k_next_ready = true;
+              tc_fence_after();
+            }
+            issue_s(t, j + 1);
+          }
         }
+        if (!ok) break;
+        // Every use of V_j (and of K_{j+1}) has been issued: release the slots
+        // when those MMAs complete.
+        mma_commit_el(smem_u32(&bar_kv_empty[(2 * j + 1) % C::NSLOT]));
+        if (k_next_ready) mma_commit_el(smem_u32(&bar_kv_empty[(2 * j + 2) % C::NSLOT]));
       }
       if (!ok) {
         // Wait for the MMAs already issued before TMEM is released. bar_q_full
@@ -204,28 +236,30 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------ softmax warps 0-3
-    const int r = threadIdx.x;  // query row within the tile == TMEM lane
-    const int qrow = q0 + r;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    // ------------------------------------------------------------ softmax warps 0-7
+    const int t = warp / 4;           // query tile of this warpgroup
+    const int r = threadIdx.x % 128;  // query row within the tile == TMEM lane
+    const int qrow = q0 + t * C::BQ + r;
+    const int my_kv = n_kv_t[t];
+    const uint32_t lane_base = static_cast<uint32_t>((warp % 4) * 32) << 16;
+    const uint32_t ts = tmem + lane_base + C::tm_s(t);
     float m = -INFINITY;  // running max in log2 units (scaled scores)
     float l = 0.f;
     const float sl2 = p.scale_log2;
     const bool pos = sl2 >= 0.f;
     TraceCursor tc;
-    if (lane == 0) ATTN_TRACE_INIT(tc, 2 + warp);
+    if (lane == 0 && (warp == 0 || warp == 4)) ATTN_TRACE_INIT(tc, 2 + t);
     bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
-      const int sb = j & 1;
-      ATTN_TRACE_EV(tc, 1, j);  // start waiting for S_j
-      ok = mbar_wait_warp(smem_u32(&bar_s_full[sb]), (j >> 1) & 1, ctl);
+    for (int j = 0; j < my_kv; ++j) {
+      ATTN_TRACE_EV(tc, 1, j);  // start waiting for S_t(j)
+      // S_t(j) landed; its commit also covers PV_t(j-1), so O_t is current.
+      ok = mbar_wait_warp(smem_u32(&bar_s_full[t]), j & 1, ctl);
       if (!ok) break;
-      ATTN_TRACE_EV(tc, 2, j);  // S_j landed
+      ATTN_TRACE_EV(tc, 2, j);  // S_t(j) landed
       tc_fence_after();
       // Raw scores of this row; the scale is folded into the exponent below.
       float x[C::BK];
       {
-        const uint32_t ts = tmem + lane_base + (sb ? C::TM_S1 : C::TM_S0);
         uint32_t u[C::BK];
 #pragma unroll
         for (int c = 0; c < C::BK; c += 32)
@@ -235,7 +269,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         for (int c = 0; c < C::BK; ++c) x[c] = __uint_as_float(u[c]);
       }
       const int k0 = j * C::BK;
-      const bool need_mask = (p.causal && k0 + C::BK - 1 > q0) || (k0 + C::BK > p.S);
+      const int qt0 = q0 + t * C::BQ;
+      const bool need_mask = (p.causal && k0 + C::BK - 1 > qt0) || (k0 + C::BK > p.S);
       const int lim = p.causal ? min(qrow, p.S - 1) : (p.S - 1);  // last visible key
       // Largest scaled score: the max of the raw scores for scale >= 0, the min
       // for scale < 0 (masked keys pushed to the losing end).
@@ -279,19 +314,11 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         m = mx;
       }
       const float neg_m = -m;
-      // P buffer sb was last read by PV_{j-2}.
-      if (j >= 2) {
-        ok = mbar_wait_warp(smem_u32(&bar_pv_done[sb]), ((j - 2) >> 1) & 1, ctl);
-        if (!ok) break;
-      }
       float sums[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) sums[i] = 0.f;
-      const uint32_t tp = tmem + lane_base + (sb ? C::TM_P1 : C::TM_P0);
-      // With SPLIT, P_lo goes over columns 0..63 of this tile's score buffer,
-      // whose scores this thread has already read; the next MMA to write that
-      // buffer (S_{j+2}) issues after PV_j and tcgen05 MMAs run in issue order.
-      const uint32_t tl = tmem + lane_base + (sb ? C::TM_S1 : C::TM_S0);
+      // P (hi, and with SPLIT lo) over this row's scores, 32 columns at a time;
+      // this thread has read all its scores already.
 #pragma unroll
       for (int ch = 0; ch < C::BK; ch += 32) {
         uint32_t pk[16];
@@ -311,22 +338,19 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
             pk[c / 2] = pack_bf16x2(p0, p1);
           }
         }
-        tmem_st16(tp + ch / 2, pk);
-        if constexpr (SPLIT) tmem_st16(tl + ch / 2, *reinterpret_cast<uint32_t(*)[16]>(&pl[0]));
+        tmem_st16(ts + ch / 2, pk);
+        if constexpr (SPLIT)
+          tmem_st16(ts + 64 + ch / 2, *reinterpret_cast<uint32_t(*)[16]>(&pl[0]));
       }
 #pragma unroll
       for (int w = 4; w > 0; w >>= 1)
 #pragma unroll
         for (int i = 0; i < w; ++i) sums[i] += sums[i + w];
-      const float sum = sums[0];
-      l = l * alpha + sum;
+      l = l * alpha + sums[0];
       ATTN_TRACE_EV(tc, 3, j);  // exponentials done
-      // Rescale this warp's O rows once PV_{j-1} has landed in TMEM.
+      // Rescale this warp's O rows (PV_t(j-1) has completed, see above).
       if (j >= 1 && __any_sync(0xffffffffu, rescale)) {
-        ok = mbar_wait_warp(smem_u32(&bar_pv_done[(j - 1) & 1]), ((j - 1) >> 1) & 1, ctl);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t to = tmem + lane_base + C::TM_O;
+        const uint32_t to = tmem + lane_base + C::tm_o(t);
 #pragma unroll
         for (int c = 0; c < D; c += 32) {
           uint32_t u[32];
@@ -339,19 +363,16 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(smem_u32(&bar_p_full[sb]));
-      ATTN_TRACE_EV(tc, 4, j);  // P_j stored and signalled
+      mbar_arrive(smem_u32(&bar_p_full[t]));
+      ATTN_TRACE_EV(tc, 4, j);  // P_t(j) stored and signalled
     }
-    if (ok && n_kv > 0) {
-      const int jl = n_kv - 1;
-      ok = mbar_wait_warp(smem_u32(&bar_pv_done[jl & 1]), (jl >> 1) & 1, ctl);
-    }
+    if (ok && my_kv > 0) ok = mbar_wait_warp(smem_u32(&bar_pv_done[t]), 0, ctl);
     if (ok) {
       tc_fence_after();
       const float inv_l = 1.f / l;
       const bool valid = qrow < p.S;
       const size_t rowoff = ((static_cast<size_t>(b) * p.S + qrow) * p.Hq + hq) * D;
-      const uint32_t to = tmem + lane_base + C::TM_O;
+      const uint32_t to = tmem + lane_base + C::tm_o(t);
 #pragma unroll
       for (int c = 0; c < D; c += 32) {
         uint32_t u[32];
@@ -373,7 +394,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           uint4* dst = reinterpret_cast<uint4*>(p.o + rowoff + c);
 #pragma unroll
           for (int i = 0; i < 4; ++i) dst[i] = w[i];
-          if (p.o_lo) {
+          if (SPLIT) {
             uint4* dl = reinterpret_cast<uint4*>(p.o_lo + rowoff + c);
 #pragma unroll
             for (int i = 0; i < 4; ++i) dl[i] = wl[i];
@@ -387,7 +408,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) tmem_dealloc(tmem, C::TMEM_COLS);
+  if (warp == 9) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
 template <int D, bool SPLIT>
@@ -404,7 +425,7 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  dim3 grid(p.B * p.Hq, p.n_qtiles);
+  dim3 grid(p.B * p.Hq, p.n_qblocks);
   attn_fwd_kernel<D, SPLIT><<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }

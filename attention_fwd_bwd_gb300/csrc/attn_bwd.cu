@@ -255,7 +255,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       ATTN_TRACE_EV(tc, 1, 0);
       constexpr uint32_t idesc_sdp = idesc_bf16_f32(128, BQ, 0, 0);
       constexpr uint32_t idesc_kv = idesc_bf16_f32(128, D, 0, 1);
-      constexpr uint32_t idesc_dq = idesc_bf16_f32(128, BQ, 1, 1);
+      constexpr uint32_t idesc_dq = idesc_bf16_f32(128, 2 * BQ, 1, 1);
       // Descriptor bases; each step below only adds a constant byte offset
       // (>> 4) to the start-address field.
       const uint64_t dK_kmaj = sw128_desc(sK, 16, 1024);
@@ -263,8 +263,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       const uint64_t dK_mn = sw128_desc(sK, BK * 128, 1024);
       const uint64_t dDsHi_k = sw128_desc(sDsHi, 16, 1024);
       const uint64_t dDsLo_k = sw128_desc(sDsLo, 16, 1024);
-      const uint64_t dDsHi_mn = sw128_desc(sDsHi, BK * 128, 1024);
-      const uint64_t dDsLo_mn = sw128_desc(sDsLo, BK * 128, 1024);
+      // [dS_hi^T | dS_lo^T] as one MN-major operand of N = 128: the second
+      // 64-column block (dS_lo^T) sits DS_BYTES after the first.
+      const uint64_t dDs_mn = sw128_desc(sDsHi, C::DS_BYTES, 1024);
       auto add = [](uint64_t d, uint32_t bytes) { return d + (bytes >> 4); };
       auto issue_sdp = [&](int s) {
         const uint64_t dq_k = sw128_desc(stage_q(s), 16, 1024);
@@ -322,13 +323,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           if (!ok) break;
           tc_fence_after();
         }
-        // dQ^T[d][q] = sum over keys of K[key][d] (dS_hi + dS_lo)^T[key][q]
+        // dQ^T[d][q] (+ 64 columns for the lo part) = sum over keys of
+        // K[key][d] [dS_hi^T | dS_lo^T][key][q]. It overwrites P^T, which
+        // dV(it) above has read (MMAs run in issue order).
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk) {
-          const uint64_t ak = add(dK_mn, kk * 2048);
-          mma_ss_el(tmem + C::TM_DQ, ak, add(dDsHi_mn, kk * 2048), idesc_dq, kk > 0);
-          mma_ss_el(tmem + C::TM_DQ, ak, add(dDsLo_mn, kk * 2048), idesc_dq, 1u);
-        }
+        for (int kk = 0; kk < BK / 16; ++kk)
+          mma_ss_el(tmem + C::TM_DQ, add(dK_mn, kk * 2048), add(dDs_mn, kk * 2048), idesc_dq,
+                    kk > 0);
         mma_commit_el(smem_u32(&bar_dq_full));
         mma_commit_el(smem_u32(&bar_pds_free));
         ATTN_TRACE_EV(tc, 6, it);  // dQ issued
@@ -381,9 +382,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         split_bf16x2_trunc(dr[0], dr[1], dh[c / 2], dl[c / 2]);
       }
       ATTN_TRACE_EV(tc, 3, it);  // P, dS computed
-      // The MMAs of the previous tile must be done with P (TMEM) and dS (smem).
+      // The MMAs of the previous tile must be done with dS (smem), and the
+      // drain must have read dQ^T(it-1), whose TMEM columns P^T now takes.
       if (it >= 1) {
         ok = mbar_wait_warp(smem_u32(&bar_pds_free), (it - 1) & 1, ctl);
+        if (ok) ok = mbar_wait_warp(smem_u32(&bar_dq_free), (it - 1) & 1, ctl);
         if (!ok) break;
       }
       ATTN_TRACE_EV(tc, 4, it);  // previous MMAs done
@@ -442,10 +445,17 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       if (!ok) break;
       ATTN_TRACE_EV(tc, 1, it);  // dQ landed
       tc_fence_after();
-      uint32_t u[BQ];
-      tmem_ld32(tmem + lane_base + C::TM_DQ, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
-      tmem_ld32(tmem + lane_base + C::TM_DQ + 32, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
-      tmem_wait_ld();
+      // dQ^T = hi part (columns 0..63) + lo part (64..127).
+      float u[BQ];
+#pragma unroll
+      for (int c = 0; c < BQ; c += 32) {
+        uint32_t a[32], bl[32];
+        tmem_ld32(tmem + lane_base + C::TM_DQ + c, a);
+        tmem_ld32(tmem + lane_base + C::TM_DQ + BQ + c, bl);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) u[c + i] = __uint_as_float(a[i]) + __uint_as_float(bl[i]);
+      }
       tc_fence_before();
       mbar_arrive(smem_u32(&bar_dq_free));
 #pragma unroll
@@ -456,7 +466,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           // staging [32 q][D] fp32, row-major (the TMA box layout); lane t holds column d = t.
 #pragma unroll
           for (int q = 0; q < C::DQ_ROWS; ++q)
-            stg[q * D + t] = __uint_as_float(u[half * C::DQ_ROWS + q]);
+            stg[q * D + t] = u[half * C::DQ_ROWS + q];
         }
         fence_async_smem();
         named_bar_sync(1, 128);

@@ -94,14 +94,18 @@ struct BwdCfg {
   static constexpr int SMEM_DQS = SMEM_DS_LO + DS_BYTES;
   static constexpr int SMEM_BYTES = SMEM_DQS + DQS_BYTES;
   static constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;
-  // Tensor-memory columns.
+  // Tensor-memory columns. dQ^T is produced as one N = 128 product over the
+  // adjacent [dS_hi^T | dS_lo^T] tiles: its columns 0..63 hold K^T dS_hi^T and
+  // 64..127 hold K^T dS_lo^T, summed by the drain. P^T hi/lo live over the
+  // first half of that region between the drain reading dQ^T(i-1) and the
+  // dQ MMA of tile i (which runs after dV(i) has read them).
   static constexpr int TM_ST = 0;      // S^T  fp32 (64 cols)
   static constexpr int TM_DPT = 64;    // dP^T fp32 (64 cols)
   static constexpr int TM_DV = 128;    // dV   fp32 (D cols)
   static constexpr int TM_DK = 256;    // dK   fp32 (D cols)
-  static constexpr int TM_DQ = 384;    // dQ^T fp32 (64 cols)
-  static constexpr int TM_P_HI = 448;  // P^T hi, bf16 pairs (32 cols)
-  static constexpr int TM_P_LO = 480;  // P^T lo, bf16 pairs (32 cols)
+  static constexpr int TM_DQ = 384;    // dQ^T fp32 (2 x 64 cols: hi part, lo part)
+  static constexpr int TM_P_HI = 384;  // P^T hi, bf16 pairs (32 cols)
+  static constexpr int TM_P_LO = 416;  // P^T lo, bf16 pairs (32 cols)
   static constexpr int TMEM_COLS = 512;
   static constexpr int THREADS = 448;
   static_assert(SMEM_ALLOC <= 232448, "shared-memory plan exceeds 227 KB");

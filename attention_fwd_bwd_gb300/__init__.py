@@ -26,6 +26,7 @@ __all__ = [
     "attn_bwd_workspace_size",
     "attn_check_status",
     "attn_set_wait_timeout_ns",
+    "attn_set_fault_injection",
     "attn_status_string",
     "STATUS",
 ]
@@ -83,6 +84,8 @@ def lib():
     L.attn_check_status.restype = i
     L.attn_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
     L.attn_set_wait_timeout_ns.restype = None
+    L.attn_set_fault_injection.argtypes = [i]
+    L.attn_set_fault_injection.restype = None
     _lib = L
     return L
 
@@ -227,3 +230,8 @@ def attn_check_status(workspace=None):
 
 def attn_set_wait_timeout_ns(ns):
     lib().attn_set_wait_timeout_ns(int(ns))
+
+
+def attn_set_fault_injection(mask):
+    """Testing hook: bit 0 stalls the forward's MMA warp, bit 1 the backward's."""
+    lib().attn_set_fault_injection(int(mask))

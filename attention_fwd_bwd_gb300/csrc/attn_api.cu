@@ -21,6 +21,7 @@ __device__ int g_fwd_status;
 
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;
 unsigned long long g_timeout_ns = kDefaultTimeoutNs;
+int g_inject_stall = 0;
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -166,6 +167,8 @@ const char* attn_status_string(attn_status_t s) {
 
 void attn_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns = ns ? ns : kDefaultTimeoutNs; }
 
+void attn_set_fault_injection(int mask) { g_inject_stall = mask & 3; }
+
 size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int S, int D) {
   if (validate_sizes(B, Hq, Hkv, S, D) != ATTN_OK || B == 0 || S == 0) return 0;
   return bwd_workspace_layout(B, Hq, S).total;
@@ -204,6 +207,7 @@ static attn_status_t fwd_impl(const void* q, const void* k, const void* v, void*
   p.n_qblocks = (S + 2 * FwdCfg<128>::BQ - 1) / (2 * FwdCfg<128>::BQ);
   p.status = status;
   p.timeout_ns = g_timeout_ns;
+  p.inject_stall = g_inject_stall & 1;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   return finish(launch_fwd(D, tq, tk, tv, p, s), s, status);
 }
@@ -280,6 +284,7 @@ attn_status_t attn_bwd_main(const void* q, const void* k, const void* v, const v
   p.n_ktiles = (S + 127) / 128;
   p.status = reinterpret_cast<int*>(ws + w.off_status);
   p.timeout_ns = g_timeout_ns;
+  p.inject_stall = (g_inject_stall >> 1) & 1;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   return finish(launch_bwd_main(D, tq, tk, tv, tdo, tdq, p, s), s, p.status);
 }

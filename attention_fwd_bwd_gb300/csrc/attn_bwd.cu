@@ -236,12 +236,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         issued = it + 1;
       }
       if (lane == 0) {
-        if (!ok) {
-          for (int it = max(0, issued - ST); it < issued; ++it)
-            mbar_wait_drain(smem_u32(&bar_st_full[it % ST]), (it / ST) & 1, 50000000ull);
-        }
+        // Let every copy issued land before the CTA's shared memory goes away
+        // (immediate in a normal run, where the MMA warp consumed them all).
+        for (int it = max(0, issued - ST); it < issued; ++it)
+          mbar_wait_drain(smem_u32(&bar_st_full[it % ST]), (it / ST) & 1, 50000000ull);
         mbar_wait_drain(smem_u32(&bar_kv_full), 0, 50000000ull);
       }
+      (void)ok;
       __syncwarp();
     }
   } else if (warp == 13) {
@@ -250,7 +251,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     if (lane == 0) ATTN_TRACE_INIT(tc, 1);
     // The whole warp runs this loop and builds the (warp-uniform) descriptors;
     // each MMA and commit is issued by one elected lane.
-    bool ok = mbar_wait_warp(smem_u32(&bar_kv_full), 0, ctl);
+    bool ok = !p.inject_stall && mbar_wait_warp(smem_u32(&bar_kv_full), 0, ctl);
     if (ok) {
       ATTN_TRACE_EV(tc, 1, 0);
       constexpr uint32_t idesc_sdp = idesc_bf16_f32(128, BQ, 0, 0);
@@ -335,7 +336,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         ATTN_TRACE_EV(tc, 6, it);  // dQ issued
       }
       mma_commit_el(smem_u32(&bar_mma_done));
-      if (!ok) mbar_wait_drain(smem_u32(&bar_mma_done), 0, 50000000ull);
+      // Every MMA issued finishes before TMEM is released.
+      mbar_wait_drain(smem_u32(&bar_mma_done), 0, 50000000ull);
     }
     __syncwarp();
   } else if (warp < 8) {
@@ -442,6 +444,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       const int h = g * p.G + it / niq;
       const int q0 = (i_start + it % niq) * BQ;
       ok = mbar_wait_warp(smem_u32(&bar_dq_full), it & 1, ctl);
+      // The four drain warps meet at bar.sync below: agree first on going on.
+      ok = named_bar_and(1, 128, ok);
       if (!ok) break;
       ATTN_TRACE_EV(tc, 1, it);  // dQ landed
       tc_fence_after();

@@ -55,6 +55,7 @@ struct FwdParams {
   int n_qblocks;     // blocks of two 128-row query tiles
   int* status;
   unsigned long long timeout_ns;
+  int inject_stall;  // testing hook: the MMA warp issues nothing (waits then run out)
 };
 
 // ---------------------------------------------------------------- backward
@@ -123,6 +124,7 @@ struct BwdParams {
   int n_ktiles;
   int* status;
   unsigned long long timeout_ns;
+  int inject_stall;  // testing hook: the MMA warp issues nothing (waits then run out)
 };
 
 // Workspace layout of the backward pass (all offsets 256-byte aligned).

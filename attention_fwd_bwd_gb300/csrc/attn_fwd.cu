@@ -138,12 +138,14 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
                             keep);
       issued = idx + 1;
     }
-    if (!ok && lane == 0) {
-      // Let in-flight copies land before the CTA's shared memory goes away.
+    if (lane == 0) {
+      // Let every copy issued land before the CTA's shared memory goes away
+      // (immediate in a normal run, where the MMA warp consumed them all).
       for (int idx = max(0, issued - C::NSLOT); idx < issued; ++idx)
         mbar_wait_drain(smem_u32(&bar_kv_full[idx % C::NSLOT]), (idx / C::NSLOT) & 1,
                         50000000ull);
     }
+    (void)ok;
     __syncwarp();
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
@@ -151,7 +153,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     // each MMA and commit is issued by one elected lane.
     TraceCursor tc;
     if (lane == 0) ATTN_TRACE_INIT(tc, 1);
-    bool ok = mbar_wait_warp(smem_u32(&bar_q_full), 0, ctl);
+    bool ok = !p.inject_stall && mbar_wait_warp(smem_u32(&bar_q_full), 0, ctl);
     if (ok) {
       ATTN_TRACE_EV(tc, 1, 0);
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
@@ -227,12 +229,13 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         mma_commit_el(smem_u32(&bar_kv_empty[(2 * j + 1) % C::NSLOT]));
         if (k_next_ready) mma_commit_el(smem_u32(&bar_kv_empty[(2 * j + 2) % C::NSLOT]));
       }
-      if (!ok) {
-        // Wait for the MMAs already issued before TMEM is released. bar_q_full
-        // has completed its only phase, so this commit completes phase 1.
-        mma_commit_el(smem_u32(&bar_q_full));
-        mbar_wait_drain(smem_u32(&bar_q_full), 1, 50000000ull);
-      }
+      // Wait for every MMA issued to finish before TMEM is released (in a
+      // normal run the epilogue has already waited for them). bar_q_full has
+      // completed its only phase, so this commit completes phase 1.
+      mma_commit_el(smem_u32(&bar_q_full));
+      mbar_wait_drain(smem_u32(&bar_q_full), 1, 50000000ull);
+    } else {
+      mbar_wait_drain(smem_u32(&bar_q_full), 0, 50000000ull);  // let the Q copy land
     }
     __syncwarp();
   } else {

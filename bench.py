@@ -30,7 +30,7 @@ DEFAULT_WORKLOAD = "llama3_8b_s4096"
 
 # DRAM traffic of the backward main kernel per launch, from an ncu capture,
 # keyed by the hash of the kernel sources it was taken on (null once they change).
-TRAFFIC = {}
+TRAFFIC = {"cfbe5ec9f2d68660": 961.89e6}  # dram__bytes_read.sum + dram__bytes_write.sum, one launch
 
 
 def kernel_source_hash():

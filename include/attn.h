@@ -194,6 +194,16 @@ attn_status_t attn_check_status(void* workspace);
  */
 void attn_set_wait_timeout_ns(uint64_t ns);
 
+/*
+ * Testing hook for the failure path (not part of the method): with bit 0 of
+ * mask set, the forward kernels' MMA warp issues nothing; with bit 1 set, the
+ * backward main kernel's does. The other warps' bounded waits then run out
+ * after the wait time limit, the kernels stop early without touching their
+ * outputs, and attn_check_status() reports ATTN_ERR_TIMEOUT. No fault, trap
+ * or hang is involved; 0 restores normal operation.
+ */
+void attn_set_fault_injection(int mask);
+
 #ifdef __cplusplus
 }
 #endif

@@ -240,7 +240,7 @@ attn_status_t attn_bwd_preprocess(const void* o, const void* o_lo, const void* d
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch_bwd_preprocess(
       static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(o_lo),
-      static_cast<const __nv_bfloat16*>(dO), lse, reinterpret_cast<float*>(ws + w.off_lse2),
+      static_cast<const __nv_bfloat16*>(dO), lse, reinterpret_cast<float*>(ws + w.off_nlse2),
       reinterpret_cast<float*>(ws + w.off_dvec), static_cast<float*>(dq),
       reinterpret_cast<int*>(ws + w.off_status), B, Hq, S, D, s);
   return finish(e, s, nullptr);
@@ -268,7 +268,7 @@ attn_status_t attn_bwd_main(const void* q, const void* k, const void* v, const v
       !make_dq_map(&tdq, dq, B, S, Hq, D))
     return ATTN_ERR_CUDA;
   BwdParams p;
-  p.lse2 = reinterpret_cast<const float*>(ws + w.off_lse2);
+  p.nlse2 = reinterpret_cast<const float*>(ws + w.off_nlse2);
   p.dvec = reinterpret_cast<const float*>(ws + w.off_dvec);
   p.dk = static_cast<float*>(dk);
   p.dv = static_cast<float*>(dv);

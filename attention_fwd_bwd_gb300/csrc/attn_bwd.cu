@@ -36,7 +36,7 @@ static __device__ unsigned long long g_attn_trace[kTraceCtas * kTraceRoles * kTr
 // ------------------------------------------------------------------ preprocess
 __global__ void __launch_bounds__(256) attn_bwd_preprocess_kernel(
     const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ o_lo,
-    const __nv_bfloat16* __restrict__ dO, const float* __restrict__ lse, float* __restrict__ lse2,
+    const __nv_bfloat16* __restrict__ dO, const float* __restrict__ lse, float* __restrict__ nlse2,
     float* __restrict__ dvec, float4* __restrict__ dq, int* __restrict__ status, int B, int Hq,
     int S, int S_pad, int D) {
   if (blockIdx.x == 0 && threadIdx.x == 0) *status = 0;  // status word of the main kernel
@@ -79,16 +79,16 @@ __global__ void __launch_bounds__(256) attn_bwd_preprocess_kernel(
       const int b = static_cast<int>(bs / S);
       const long long bh = static_cast<long long>(b) * Hq + h;
       dvec[bh * S_pad + s] = acc;
-      lse2[bh * S_pad + s] = lse[bh * S + s] * kLog2e;
+      nlse2[bh * S_pad + s] = -lse[bh * S + s] * kLog2e;
     }
   }
-  // Padding rows S..S_pad-1 of every (b, h): probability 0 (lse2 = +inf), Dvec 0.
+  // Padding rows S..S_pad-1 of every (b, h): probability 0 (nlse2 = -inf), Dvec 0.
   const long long npad = static_cast<long long>(B) * Hq * (S_pad - S);
   for (long long i = tid; i < npad; i += gthreads) {
     const long long bh = i / (S_pad - S);
     const int s = S + static_cast<int>(i % (S_pad - S));
     dvec[bh * S_pad + s] = 0.f;
-    lse2[bh * S_pad + s] = INFINITY;
+    nlse2[bh * S_pad + s] = -INFINITY;
   }
   // dq is accumulated by reductions in the main kernel.
   const long long n4 = nrows * D / 4;
@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 
   auto stage_q = [&](int s) { return sStage + s * C::STAGE_BYTES; };
   auto stage_do = [&](int s) { return sStage + s * C::STAGE_BYTES + C::Q_BYTES; };
-  auto stage_rows = [&](int s) {  // lse2 then dvec, BQ floats each
+  auto stage_rows = [&](int s) {  // nlse2 then dvec, BQ floats each
     return reinterpret_cast<const float*>(smem + C::SMEM_STAGE + s * C::STAGE_BYTES +
                                           2 * C::Q_BYTES);
   };
@@ -230,7 +230,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           tma_load_4d_el(stage_do(s) + c * (BQ * 128), &tm_do, full, c * 64, h, q0, b);
         }
         const size_t rowoff = (static_cast<size_t>(b) * p.Hq + h) * p.S_pad + q0;
-        bulk_load_el(stage_do(s) + C::Q_BYTES, p.lse2 + rowoff, C::ROWVEC_BYTES, full);
+        bulk_load_el(stage_do(s) + C::Q_BYTES, p.nlse2 + rowoff, C::ROWVEC_BYTES, full);
         bulk_load_el(stage_do(s) + C::Q_BYTES + C::ROWVEC_BYTES, p.dvec + rowoff,
                      C::ROWVEC_BYTES, full);
         issued = it + 1;
@@ -262,8 +262,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       const uint64_t dK_kmaj = sw128_desc(sK, 16, 1024);
       const uint64_t dV_kmaj = sw128_desc(sV, 16, 1024);
       const uint64_t dK_mn = sw128_desc(sK, BK * 128, 1024);
-      const uint64_t dDsHi_k = sw128_desc(sDsHi, 16, 1024);
-      const uint64_t dDsLo_k = sw128_desc(sDsLo, 16, 1024);
       // [dS_hi^T | dS_lo^T] as one MN-major operand of N = 128: the second
       // 64-column block (dS_lo^T) sits DS_BYTES after the first.
       const uint64_t dDs_mn = sw128_desc(sDsHi, C::DS_BYTES, 1024);
@@ -291,6 +289,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         const int s = it % ST;
         if (it + 1 < n_it) {
           const int s1 = (it + 1) % ST;
+          ATTN_TRACE_EV(tc, 7, it + 1);  // start waiting for stage / sdp_free
           ok = mbar_wait_warp(smem_u32(&bar_st_full[s1]), ((it + 1) / ST) & 1, ctl);
           if (ok) ok = mbar_wait_warp(smem_u32(&bar_sdp_free), it & 1, ctl);
           if (!ok) break;
@@ -298,14 +297,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           issue_sdp(s1);
           ATTN_TRACE_EV(tc, 3, it + 1);  // S^T, dP^T issued
         }
+        ATTN_TRACE_EV(tc, 8, it);  // start waiting for P, dS
         ok = mbar_wait_warp(smem_u32(&bar_pds_full), it & 1, ctl);
         if (!ok) break;
         ATTN_TRACE_EV(tc, 4, it);  // P, dS ready seen
         tc_fence_after();
         const uint64_t dq_mn = sw128_desc(stage_q(s), BQ * 128, 1024);
         const uint64_t ddo_mn = sw128_desc(stage_do(s), BQ * 128, 1024);
-        // dV += (P_hi + P_lo)^T dO_i  (A from TMEM: 16 query columns = 8 TMEM columns a step)
-        // dK += (dS_hi + dS_lo)^T Q_i
+        // dV += (P_hi + P_lo)^T dO_i and dK += (dS_hi + dS_lo)^T Q_i, A from
+        // TMEM: 16 query columns = 8 TMEM columns a step.
 #pragma unroll
         for (int kk = 0; kk < BQ / 16; ++kk) {
           const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
@@ -313,8 +313,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           const uint64_t bq = add(dq_mn, kk * 2048);
           mma_ts_el(tmem + C::TM_DV, tmem + C::TM_P_HI + kk * 8, bdo, idesc_kv, acc);
           mma_ts_el(tmem + C::TM_DV, tmem + C::TM_P_LO + kk * 8, bdo, idesc_kv, 1u);
-          mma_ss_el(tmem + C::TM_DK, add(dDsHi_k, kk * 32), bq, idesc_kv, acc);
-          mma_ss_el(tmem + C::TM_DK, add(dDsLo_k, kk * 32), bq, idesc_kv, 1u);
+          mma_ts_el(tmem + C::TM_DK, tmem + C::TM_DS_HI + kk * 8, bq, idesc_kv, acc);
+          mma_ts_el(tmem + C::TM_DK, tmem + C::TM_DS_LO + kk * 8, bq, idesc_kv, 1u);
         }
         // Q_i and dO_i are not read again: hand the stage back to the producer.
         mma_commit_el(smem_u32(&bar_st_empty[s]));
@@ -324,6 +324,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           if (!ok) break;
           tc_fence_after();
         }
+        ATTN_TRACE_EV(tc, 9, it);  // dq_free seen, issuing dQ
         // dQ^T[d][q] (+ 64 columns for the lo part) = sum over keys of
         // K[key][d] [dS_hi^T | dS_lo^T][key][q]. It overwrites P^T, which
         // dV(it) above has read (MMAs run in issue order).
@@ -349,7 +350,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     const bool key_valid = key < p.S;
     bool ok = true;
     TraceCursor tc;
-    if (lane == 0 && (warp == 0 || warp == 4)) ATTN_TRACE_INIT(tc, 2 + warp / 4);
+    if (lane == 0) ATTN_TRACE_INIT(tc, 2 + warp);
     for (int it = 0; it < n_it; ++it) {
       const int s = it % ST;
       const int q0 = (i_start + it % niq) * BQ;
@@ -358,9 +359,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       if (ok) ok = mbar_wait_warp(smem_u32(&bar_st_full[s]), (it / ST) & 1, ctl);
       if (!ok) break;
       tc_fence_after();
-      const float* lse2 = stage_rows(s);
-      const float* dvec = lse2 + BQ;
-      const bool need_mask = p.causal && (q0 < k0 + BK - 1);
+      // This warpgroup's query columns of -LSE*log2(e) and Dvec, four at a time.
+      const float4* nl4 = reinterpret_cast<const float4*>(stage_rows(s) + cg * HALF);
+      const float4* dv4 = reinterpret_cast<const float4*>(stage_rows(s) + BQ + cg * HALF);
+      // Only tiles that cross the causal diagonal or hold keys past S mask.
+      const bool need_mask = (p.causal && (q0 < k0 + BK - 1)) || (k0 + BK > p.S);
       uint32_t us[HALF], ud[HALF];
       tmem_ld32(tmem + lane_base + C::TM_ST + cg * HALF, us);
       tmem_ld32(tmem + lane_base + C::TM_DPT + cg * HALF, ud);
@@ -369,20 +372,41 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       mbar_arrive(smem_u32(&bar_sdp_free));
       ATTN_TRACE_EV(tc, 2, it);  // S^T, dP^T loaded
       uint32_t ph[HALF / 2], pl[HALF / 2], dh[HALF / 2], dl[HALF / 2];
+      // P = exp2(S * scale*log2(e) - LSE*log2(e)); dS = scale * P * (dP - Dvec),
+      // two query columns per packed instruction.
+      const uint64_t sl2 = f32x2(p.scale_log2, p.scale_log2);
+      const uint64_t sc2 = f32x2(p.scale, p.scale);
+      auto p_ds = [&](auto masked) {
 #pragma unroll
-      for (int c = 0; c < HALF; c += 2) {
-        float pr[2], dr[2];
+        for (int c = 0; c < HALF; c += 4) {
+          const float4 nl = nl4[c / 4];
+          const float4 dv = dv4[c / 4];
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int col = cg * HALF + c + e;
-          float pv = ex2(fmaf(__uint_as_float(us[c + e]), p.scale_log2, -lse2[col]));
-          if (!key_valid || (need_mask && key > q0 + col)) pv = 0.f;
-          pr[e] = pv;
-          dr[e] = p.scale * pv * (__uint_as_float(ud[c + e]) - dvec[col]);
+          for (int h = 0; h < 2; ++h) {
+            const int cc = c + 2 * h;  // columns cc, cc + 1 of this half
+            float x0, x1;
+            unpack_f32x2(fma_f32x2(f32x2(__uint_as_float(us[cc]), __uint_as_float(us[cc + 1])), sl2,
+                                   h ? f32x2(nl.z, nl.w) : f32x2(nl.x, nl.y)),
+                         x0, x1);
+            float p0 = ex2(x0), p1 = ex2(x1);
+            if (decltype(masked)::value) {
+              const int col = cg * HALF + cc;
+              if (!key_valid || (p.causal && key > q0 + col)) p0 = 0.f;
+              if (!key_valid || (p.causal && key > q0 + col + 1)) p1 = 0.f;
+            }
+            const uint64_t t = sub_f32x2(f32x2(__uint_as_float(ud[cc]), __uint_as_float(ud[cc + 1])),
+                                         h ? f32x2(dv.z, dv.w) : f32x2(dv.x, dv.y));
+            float d0, d1;
+            unpack_f32x2(mul_f32x2(mul_f32x2(f32x2(p0, p1), sc2), t), d0, d1);
+            split_bf16x2(p0, p1, ph[cc / 2], pl[cc / 2]);
+            split_bf16x2(d0, d1, dh[cc / 2], dl[cc / 2]);
+          }
         }
-        split_bf16x2_trunc(pr[0], pr[1], ph[c / 2], pl[c / 2]);
-        split_bf16x2_trunc(dr[0], dr[1], dh[c / 2], dl[c / 2]);
-      }
+      };
+      if (need_mask)
+        p_ds(BoolConst<true>{});
+      else
+        p_ds(BoolConst<false>{});
       ATTN_TRACE_EV(tc, 3, it);  // P, dS computed
       // The MMAs of the previous tile must be done with dS (smem), and the
       // drain must have read dQ^T(it-1), whose TMEM columns P^T now takes.
@@ -394,6 +418,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       ATTN_TRACE_EV(tc, 4, it);  // previous MMAs done
       tmem_st16(tmem + lane_base + C::TM_P_HI + cg * (HALF / 2), ph);
       tmem_st16(tmem + lane_base + C::TM_P_LO + cg * (HALF / 2), pl);
+      tmem_st16(tmem + lane_base + C::TM_DS_HI + cg * (HALF / 2), dh);
+      tmem_st16(tmem + lane_base + C::TM_DS_LO + cg * (HALF / 2), dl);
       // Row r of dS^T, K-major with 128-byte swizzle: 64 query columns per
       // 128-byte row, 8 per 16-byte unit; this half owns units cg*4..cg*4+3.
 #pragma unroll
@@ -432,6 +458,32 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         }
       }
     }
+#ifdef ATTN_TRACE
+  } else if (warp == 14) {
+    // ------------------------------------------------------------ trace observer
+    // Timestamps the completion of S^T/dP^T (1), dV/dK (2) and dQ^T (3) of
+    // every tile by polling their barriers without blocking.
+    TraceCursor tc;
+    if (lane == 0) ATTN_TRACE_INIT(tc, 14);
+    auto done = [](uint32_t bar, uint32_t parity) {
+      uint32_t ok;
+      asm volatile(
+          "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+          "selp.u32 %0, 1, 0, p;\n\t}"
+          : "=r"(ok)
+          : "r"(bar), "r"(parity)
+          : "memory");
+      return ok != 0;
+    };
+    int i1 = 0, i2 = 0, i3 = 0;
+    const uint64_t t0 = globaltimer();
+    while (i1 < n_it || i2 < n_it || i3 < n_it) {
+      if (i1 < n_it && done(smem_u32(&bar_sdp_full), i1 & 1)) ATTN_TRACE_EV(tc, 1, i1++);
+      if (i2 < n_it && done(smem_u32(&bar_st_empty[i2 % ST]), (i2 / ST) & 1)) ATTN_TRACE_EV(tc, 2, i2++);
+      if (i3 < n_it && done(smem_u32(&bar_dq_full), i3 & 1)) ATTN_TRACE_EV(tc, 3, i3++);
+      if (abort_flag || globaltimer() - t0 > 2000000000ull) break;
+    }
+#endif
   } else {
     // ------------------------------------------------------------ dQ drain warps 8-11
     const int t = threadIdx.x - 256;  // TMEM lane = head-dim index d of dQ^T
@@ -439,7 +491,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     float* stg = reinterpret_cast<float*>(smem + C::SMEM_DQS);
     bool ok = true;
     TraceCursor tc;
-    if (t == 0) ATTN_TRACE_INIT(tc, 4);
+    if (lane == 0) ATTN_TRACE_INIT(tc, 10 + (warp - 8));
     for (int it = 0; it < n_it; ++it) {
       const int h = g * p.G + it / niq;
       const int q0 = (i_start + it % niq) * BQ;
@@ -462,6 +514,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       }
       tc_fence_before();
       mbar_arrive(smem_u32(&bar_dq_free));
+      ATTN_TRACE_EV(tc, 3, it);  // dQ^T read, TMEM handed back
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         if (t == 0) bulk_wait_read_all();  // the previous reduction has read the staging tile
@@ -523,13 +576,13 @@ int grid_for(long long work_items) {
 }  // namespace
 
 cudaError_t launch_bwd_preprocess(const __nv_bfloat16* o, const __nv_bfloat16* o_lo,
-                                  const __nv_bfloat16* dO, const float* lse, float* lse2,
+                                  const __nv_bfloat16* dO, const float* lse, float* nlse2,
                                   float* dvec, float* dq, int* status, int B, int Hq, int S,
                                   int D, cudaStream_t stream) {
   const int S_pad = seq_pad(S);
   const long long work = static_cast<long long>(B) * Hq * S * D / 4;
   attn_bwd_preprocess_kernel<<<grid_for(work), 256, 0, stream>>>(
-      o, o_lo, dO, lse, lse2, dvec, reinterpret_cast<float4*>(dq), status, B, Hq, S, S_pad, D);
+      o, o_lo, dO, lse, nlse2, dvec, reinterpret_cast<float4*>(dq), status, B, Hq, S, S_pad, D);
   return cudaGetLastError();
 }
 

@@ -97,23 +97,31 @@ struct BwdCfg {
   static constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;
   // Tensor-memory columns. dQ^T is produced as one N = 128 product over the
   // adjacent [dS_hi^T | dS_lo^T] tiles: its columns 0..63 hold K^T dS_hi^T and
-  // 64..127 hold K^T dS_lo^T, summed by the drain. P^T hi/lo live over the
-  // first half of that region between the drain reading dQ^T(i-1) and the
-  // dQ MMA of tile i (which runs after dV(i) has read them).
-  static constexpr int TM_ST = 0;      // S^T  fp32 (64 cols)
-  static constexpr int TM_DPT = 64;    // dP^T fp32 (64 cols)
-  static constexpr int TM_DV = 128;    // dV   fp32 (D cols)
-  static constexpr int TM_DK = 256;    // dK   fp32 (D cols)
-  static constexpr int TM_DQ = 384;    // dQ^T fp32 (2 x 64 cols: hi part, lo part)
-  static constexpr int TM_P_HI = 384;  // P^T hi, bf16 pairs (32 cols)
-  static constexpr int TM_P_LO = 416;  // P^T lo, bf16 pairs (32 cols)
+  // 64..127 hold K^T dS_lo^T, summed by the drain. P^T and dS^T (hi/lo, bf16
+  // pairs) live in that region between the drain reading dQ^T(i-1) and the
+  // dQ MMA of tile i, which runs after dV(i) and dK(i) have read them. dV and
+  // dK take their A operand from tensor memory, so only their B operand
+  // (dO, Q) is read from shared memory.
+  static constexpr int TM_ST = 0;       // S^T  fp32 (64 cols)
+  static constexpr int TM_DPT = 64;     // dP^T fp32 (64 cols)
+  static constexpr int TM_DV = 128;     // dV   fp32 (D cols)
+  static constexpr int TM_DK = 256;     // dK   fp32 (D cols)
+  static constexpr int TM_DQ = 384;     // dQ^T fp32 (2 x 64 cols: hi part, lo part)
+  static constexpr int TM_P_HI = 384;   // P^T hi, bf16 pairs (32 cols)
+  static constexpr int TM_P_LO = 416;   // P^T lo, bf16 pairs (32 cols)
+  static constexpr int TM_DS_HI = 448;  // dS^T hi, bf16 pairs (32 cols)
+  static constexpr int TM_DS_LO = 480;  // dS^T lo, bf16 pairs (32 cols)
   static constexpr int TMEM_COLS = 512;
+#ifdef ATTN_TRACE
+  static constexpr int THREADS = 480;  // + one warp that timestamps MMA completions
+#else
   static constexpr int THREADS = 448;
+#endif
   static_assert(SMEM_ALLOC <= 232448, "shared-memory plan exceeds 227 KB");
 };
 
 struct BwdParams {
-  const float* lse2;   // [B, Hq, S_pad] lse * log2(e); +inf on padding rows
+  const float* nlse2;  // [B, Hq, S_pad] -lse * log2(e); -inf on padding rows
   const float* dvec;   // [B, Hq, S_pad] rowsum(dO * O); 0 on padding rows
   float* dk;           // [B, S, Hkv, D] fp32
   float* dv;           // [B, S, Hkv, D] fp32
@@ -129,15 +137,15 @@ struct BwdParams {
 
 // Workspace layout of the backward pass (all offsets 256-byte aligned).
 struct BwdWorkspace {
-  size_t off_status, off_lse2, off_dvec, total;
+  size_t off_status, off_nlse2, off_dvec, total;
 };
 inline BwdWorkspace bwd_workspace_layout(int B, int Hq, int S) {
   auto al = [](size_t x) { return (x + 255) / 256 * 256; };
   BwdWorkspace w;
   const size_t rows = static_cast<size_t>(B) * Hq * seq_pad(S);
   w.off_status = 0;
-  w.off_lse2 = 256;
-  w.off_dvec = w.off_lse2 + al(rows * 4);
+  w.off_nlse2 = 256;
+  w.off_dvec = w.off_nlse2 + al(rows * 4);
   w.total = w.off_dvec + al(rows * 4);
   return w;
 }
@@ -148,8 +156,8 @@ inline BwdWorkspace bwd_workspace_layout(int B, int Hq, int S) {
 // kTraceCtas values of blockIdx.y) gets kTraceRoles streams of
 // kTraceEvents 64-bit records: event code (bits 56..63), iteration
 // (bits 40..55) and the SM clock (bits 0..39).
-constexpr int kTraceCtas = 64;
-constexpr int kTraceRoles = 8;
+constexpr int kTraceCtas = 32;
+constexpr int kTraceRoles = 16;
 constexpr int kTraceEvents = 2048;
 #ifdef ATTN_TRACE
 // Each kernel source that traces defines its own buffer named g_attn_trace.
@@ -180,7 +188,7 @@ struct TraceCursor {};
 cudaError_t launch_fwd(int D, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const FwdParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_preprocess(const __nv_bfloat16* o, const __nv_bfloat16* o_lo,
-                                  const __nv_bfloat16* dO, const float* lse, float* lse2,
+                                  const __nv_bfloat16* dO, const float* lse, float* nlse2,
                                   float* dvec, float* dq, int* status, int B, int Hq, int S,
                                   int D, cudaStream_t stream);
 cudaError_t launch_bwd_main(int D, const CUtensorMap& tq, const CUtensorMap& tk,

@@ -336,7 +336,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           }
           sums[(c / 2) & 7] += p0 + p1;
           if constexpr (SPLIT) {
-            split_bf16x2_trunc(p0, p1, pk[c / 2], pl[c / 2]);
+            split_bf16x2(p0, p1, pk[c / 2], pl[c / 2]);
           } else {
             pk[c / 2] = pack_bf16x2(p0, p1);
           }

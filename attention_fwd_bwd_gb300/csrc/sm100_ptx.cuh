@@ -71,12 +71,13 @@ struct WaitCtl {
 // Error codes written to the status word (match attn_status_t).
 constexpr int kStatusTimeout = 4;
 
-// Waits for the phase with the given parity to complete. Returns false if the
-// CTA was told to abort or the time limit ran out (then it raises the abort
-// flag and records a timeout in the status word).
-static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl& ctl) {
-  if (mbar_try_wait(bar, parity)) return true;
-  uint64_t t0 = globaltimer();
+// Slow path of mbar_wait: keeps polling, checking the abort flag and the time
+// limit every 64 polls. Returns false if the CTA was told to abort or the time
+// limit ran out (then it raises the abort flag and records a timeout in the
+// status word).
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity,
+                                                   const WaitCtl& ctl) {
+  const uint64_t t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0) {
@@ -88,6 +89,15 @@ static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, con
       }
     }
   }
+}
+
+// Waits for the phase with the given parity to complete. The common case -- a
+// phase that completes within a few polls -- stays inline, with no call.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl& ctl) {
+#pragma unroll 1
+  for (int i = 0; i < 16; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, ctl);
 }
 
 // Warp-uniform form: every lane polls, and the warp agrees on the outcome, so
@@ -417,17 +427,51 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
+// ------------------------------------------------------------------ packed fp32 pairs
+// Two fp32 values in one 64-bit register pair, operands of the f32x2
+// instructions (two lanes of fp32 arithmetic per instruction).
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void unpack_f32x2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t sub_f32x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 // x as a pair of bf16 values hi + lo: hi = x with its low 16 bits cleared
 // (bf16 rounded toward zero), lo = the same truncation of the exact fp32
 // residual x - hi. hi + lo equals x to within 2^-14 relative. Both pairs are
-// packed with a byte permute (low half from x0), with no conversion instructions.
-__device__ __forceinline__ void split_bf16x2_trunc(float x0, float x1, uint32_t& hi, uint32_t& lo) {
-  const uint32_t u0 = __float_as_uint(x0), u1 = __float_as_uint(x1);
-  hi = __byte_perm(u0, u1, 0x7632);
-  const float r0 = x0 - __uint_as_float(u0 & 0xFFFF0000u);
-  const float r1 = x1 - __uint_as_float(u1 & 0xFFFF0000u);
+// packed with a byte permute (low half from x0), with no conversion
+// instructions; the two residuals come from one packed subtraction.
+__device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  hi = __byte_perm(__float_as_uint(x0), __float_as_uint(x1), 0x7632);
+  const uint64_t h = f32x2(__uint_as_float(hi << 16), __uint_as_float(hi & 0xFFFF0000u));
+  float r0, r1;
+  unpack_f32x2(sub_f32x2(f32x2(x0, x1), h), r0, r1);
   lo = __byte_perm(__float_as_uint(r0), __float_as_uint(r1), 0x7632);
 }
+
+// Compile-time bool carried as a type, to instantiate a lambda body twice.
+template <bool V>
+struct BoolConst {
+  static constexpr bool value = V;
+};
 
 __device__ __forceinline__ float ex2(float x) {
   float y;

@@ -203,7 +203,12 @@ static attn_status_t fwd_impl(const void* q, const void* k, const void* v, void*
   p.S = S;
   p.G = Hq / Hkv;
   p.causal = causal ? 1 : 0;
-  p.scale_log2 = scale * kLog2e;
+  // The kernel masks a key by giving it an infinite score, which a zero scale
+  // would turn into NaN. A scale below 2^-100 in magnitude is taken as
+  // +-2^-100: that moves no exponent by one fp32 ulp unless |q.k| > 2^70.
+  float sl2 = scale * kLog2e;
+  if (std::fabs(sl2) < 0x1p-100f) sl2 = std::signbit(sl2) ? -0x1p-100f : 0x1p-100f;
+  p.scale_log2 = sl2;
   p.n_qblocks = (S + 2 * FwdCfg<128>::BQ - 1) / (2 * FwdCfg<128>::BQ);
   p.status = status;
   p.timeout_ns = g_timeout_ns;

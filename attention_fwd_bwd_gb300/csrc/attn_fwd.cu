@@ -45,6 +45,26 @@ static __device__ unsigned long long g_attn_trace[kTraceCtas * kTraceRoles * kTr
 // p <= 2^8 and leaves the result exact after the final division by l.
 constexpr float kRescaleThreshold = 8.0f;
 
+// Largest (MAX) or smallest value of a 128-entry row, mostly with
+// three-input max / min instructions.
+template <bool MAX>
+__device__ __forceinline__ float row_extreme128(const float (&x)[128]) {
+  auto f3 = [](float a, float b, float c) { return MAX ? fmax3(a, b, c) : fmin3(a, b, c); };
+  float a[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) a[i] = f3(x[i], x[16 + i], x[32 + i]);
+#pragma unroll
+  for (int c = 48; c < 112; c += 32)
+#pragma unroll
+    for (int i = 0; i < 16; ++i) a[i] = f3(a[i], x[c + i], x[c + 16 + i]);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) a[i] = MAX ? fmaxf(a[i], x[112 + i]) : fminf(a[i], x[112 + i]);
+  const float b0 = f3(a[0], a[1], a[2]), b1 = f3(a[3], a[4], a[5]), b2 = f3(a[6], a[7], a[8]);
+  const float b3 = f3(a[9], a[10], a[11]), b4 = f3(a[12], a[13], a[14]);
+  const float c0 = f3(b0, b1, b2), c1 = f3(b3, b4, a[15]);
+  return MAX ? fmaxf(c0, c1) : fminf(c0, c1);
+}
+
 template <int D, bool SPLIT>
 __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -275,81 +295,62 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       const int qt0 = q0 + t * C::BQ;
       const bool need_mask = (p.causal && k0 + C::BK - 1 > qt0) || (k0 + C::BK > p.S);
       const int lim = p.causal ? min(qrow, p.S - 1) : (p.S - 1);  // last visible key
-      // Largest scaled score: the max of the raw scores for scale >= 0, the min
-      // for scale < 0 (masked keys pushed to the losing end).
-      float mraw;
+      float alpha = 1.f;
+      bool rescale = false;
+      // One tile of the online softmax: row max, exponentials, row sum and P
+      // (hi, and with SPLIT lo) into TMEM over the scores, 16 columns at a
+      // time; this thread has read all its scores already. Instantiated once
+      // for tiles that mask (the causal diagonal, keys past S) and once for
+      // tiles that do not.
       {
-        const float lose = pos ? -INFINITY : INFINITY;
-        if (need_mask) {
+        const bool MASKED = need_mask;
+        // Largest scaled score: the max of the raw scores for scale >= 0, the
+        // min for scale < 0 (masked keys pushed to the losing end).
+        if (MASKED) {
+          const float lose = pos ? -INFINITY : INFINITY;
 #pragma unroll
           for (int c = 0; c < C::BK; ++c)
             if (k0 + c > lim) x[c] = lose;
         }
-        float a[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) a[i] = x[i];
-        if (pos) {
-#pragma unroll
-          for (int c = 8; c < C::BK; c += 8)
-#pragma unroll
-            for (int i = 0; i < 8; ++i) a[i] = fmaxf(a[i], x[c + i]);
-#pragma unroll
-          for (int w = 4; w > 0; w >>= 1)
-#pragma unroll
-            for (int i = 0; i < w; ++i) a[i] = fmaxf(a[i], a[i + w]);
-        } else {
-#pragma unroll
-          for (int c = 8; c < C::BK; c += 8)
-#pragma unroll
-            for (int i = 0; i < 8; ++i) a[i] = fminf(a[i], x[c + i]);
-#pragma unroll
-          for (int w = 4; w > 0; w >>= 1)
-#pragma unroll
-            for (int i = 0; i < w; ++i) a[i] = fminf(a[i], a[i + w]);
+        static_assert(C::BK == 128, "row_extreme128 covers one 128-key tile");
+        const float mraw = pos ? row_extreme128<true>(x) : row_extreme128<false>(x);
+        const float mx = mraw * sl2;
+        rescale = mx > m + kRescaleThreshold;
+        if (rescale) {
+          alpha = ex2(m - mx);  // m = -inf on the first tile gives 0
+          m = mx;
         }
-        mraw = a[0];
-      }
-      const float mx = mraw * sl2;
-      float alpha = 1.f;
-      const bool rescale = mx > m + kRescaleThreshold;
-      if (rescale) {
-        alpha = ex2(m - mx);  // m = -inf on the first tile gives 0
-        m = mx;
-      }
-      const float neg_m = -m;
-      float sums[8];
+        const uint64_t sl2x2 = f32x2(sl2, sl2);
+        const uint64_t negm2 = f32x2(-m, -m);
+        uint64_t sums[4];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) sums[i] = 0.f;
-      // P (hi, and with SPLIT lo) over this row's scores, 32 columns at a time;
-      // this thread has read all its scores already.
+        for (int i = 0; i < 4; ++i) sums[i] = f32x2(0.f, 0.f);
 #pragma unroll
-      for (int ch = 0; ch < C::BK; ch += 32) {
-        uint32_t pk[16];
-        uint32_t pl[SPLIT ? 16 : 1];
+        for (int ch = 0; ch < C::BK; ch += 16) {
+          uint32_t pk[8];
+          uint32_t pl[SPLIT ? 8 : 1];
 #pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          float p0 = ex2(fmaf(x[ch + c], sl2, neg_m));
-          float p1 = ex2(fmaf(x[ch + c + 1], sl2, neg_m));
-          if (need_mask) {
-            if (k0 + ch + c > lim) p0 = 0.f;
-            if (k0 + ch + c + 1 > lim) p1 = 0.f;
+          for (int c = 0; c < 16; c += 2) {
+            float e0, e1;
+            unpack_f32x2(fma_f32x2(f32x2(x[ch + c], x[ch + c + 1]), sl2x2, negm2), e0, e1);
+            // A masked score is -inf (or +inf with a negative scale): its
+            // exponent is -inf and its probability 0 (the scale is never 0).
+            const float p0 = ex2(e0), p1 = ex2(e1);
+            sums[(c / 2) & 3] = add_f32x2(sums[(c / 2) & 3], f32x2(p0, p1));
+            if constexpr (SPLIT) {
+              split_bf16x2(p0, p1, pk[c / 2], pl[c / 2]);
+            } else {
+              pk[c / 2] = pack_bf16x2(p0, p1);
+            }
           }
-          sums[(c / 2) & 7] += p0 + p1;
-          if constexpr (SPLIT) {
-            split_bf16x2(p0, p1, pk[c / 2], pl[c / 2]);
-          } else {
-            pk[c / 2] = pack_bf16x2(p0, p1);
-          }
+          tmem_st8(ts + ch / 2, pk);
+          if constexpr (SPLIT)
+            tmem_st8(ts + 64 + ch / 2, *reinterpret_cast<uint32_t(*)[8]>(&pl[0]));
         }
-        tmem_st16(ts + ch / 2, pk);
-        if constexpr (SPLIT)
-          tmem_st16(ts + 64 + ch / 2, *reinterpret_cast<uint32_t(*)[16]>(&pl[0]));
+        float s0, s1;
+        unpack_f32x2(add_f32x2(add_f32x2(sums[0], sums[1]), add_f32x2(sums[2], sums[3])), s0, s1);
+        l = l * alpha + (s0 + s1);
       }
-#pragma unroll
-      for (int w = 4; w > 0; w >>= 1)
-#pragma unroll
-        for (int i = 0; i < w; ++i) sums[i] += sums[i + w];
-      l = l * alpha + sums[0];
       ATTN_TRACE_EV(tc, 3, j);  // exponentials done
       // Rescale this warp's O rows (PV_t(j-1) has completed, see above).
       if (j >= 1 && __any_sync(0xffffffffu, rescale)) {

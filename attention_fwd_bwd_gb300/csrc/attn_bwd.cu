@@ -311,10 +311,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
           const uint64_t bdo = add(ddo_mn, kk * 2048);
           const uint64_t bq = add(dq_mn, kk * 2048);
-          mma_ts_el(tmem + C::TM_DV, tmem + C::TM_P_HI + kk * 8, bdo, idesc_kv, acc);
-          mma_ts_el(tmem + C::TM_DV, tmem + C::TM_P_LO + kk * 8, bdo, idesc_kv, 1u);
-          mma_ts_el(tmem + C::TM_DK, tmem + C::TM_DS_HI + kk * 8, bq, idesc_kv, acc);
-          mma_ts_el(tmem + C::TM_DK, tmem + C::TM_DS_LO + kk * 8, bq, idesc_kv, 1u);
+          const uint32_t hi = (kk >> 1) * 32 + (kk & 1) * 8, lo = hi + 16;
+          mma_ts_el(tmem + C::TM_DV, tmem + C::TM_P + hi, bdo, idesc_kv, acc);
+          mma_ts_el(tmem + C::TM_DV, tmem + C::TM_P + lo, bdo, idesc_kv, 1u);
+          mma_ts_el(tmem + C::TM_DK, tmem + C::TM_DS + hi, bq, idesc_kv, acc);
+          mma_ts_el(tmem + C::TM_DK, tmem + C::TM_DS + lo, bq, idesc_kv, 1u);
         }
         // Q_i and dO_i are not read again: hand the stage back to the producer.
         mma_commit_el(smem_u32(&bar_st_empty[s]));
@@ -371,7 +372,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       tc_fence_before();
       mbar_arrive(smem_u32(&bar_sdp_free));
       ATTN_TRACE_EV(tc, 2, it);  // S^T, dP^T loaded
-      uint32_t ph[HALF / 2], pl[HALF / 2], dh[HALF / 2], dl[HALF / 2];
+      // bf16 pairs of this half's 32 query columns: P hi then P lo, dS hi then dS lo.
+      uint32_t pp[HALF], dd[HALF];
       // P = exp2(S * scale*log2(e) - LSE*log2(e)); dS = scale * P * (dP - Dvec),
       // two query columns per packed instruction.
       const uint64_t sl2 = f32x2(p.scale_log2, p.scale_log2);
@@ -398,8 +400,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
                                          h ? f32x2(dv.z, dv.w) : f32x2(dv.x, dv.y));
             float d0, d1;
             unpack_f32x2(mul_f32x2(mul_f32x2(f32x2(p0, p1), sc2), t), d0, d1);
-            split_bf16x2(p0, p1, ph[cc / 2], pl[cc / 2]);
-            split_bf16x2(d0, d1, dh[cc / 2], dl[cc / 2]);
+            split_bf16x2(p0, p1, pp[cc / 2], pp[HALF / 2 + cc / 2]);
+            split_bf16x2(d0, d1, dd[cc / 2], dd[HALF / 2 + cc / 2]);
           }
         }
       };
@@ -416,17 +418,17 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         if (!ok) break;
       }
       ATTN_TRACE_EV(tc, 4, it);  // previous MMAs done
-      tmem_st16(tmem + lane_base + C::TM_P_HI + cg * (HALF / 2), ph);
-      tmem_st16(tmem + lane_base + C::TM_P_LO + cg * (HALF / 2), pl);
-      tmem_st16(tmem + lane_base + C::TM_DS_HI + cg * (HALF / 2), dh);
-      tmem_st16(tmem + lane_base + C::TM_DS_LO + cg * (HALF / 2), dl);
+      tmem_st32(tmem + lane_base + C::TM_P + cg * HALF, pp);
+      tmem_st32(tmem + lane_base + C::TM_DS + cg * HALF, dd);
       // Row r of dS^T, K-major with 128-byte swizzle: 64 query columns per
       // 128-byte row, 8 per 16-byte unit; this half owns units cg*4..cg*4+3.
 #pragma unroll
       for (int u = 0; u < HALF / 8; ++u) {
         const int unit = cg * (HALF / 8) + u;
-        st_sw128(sDsHi, r, unit, make_uint4(dh[u * 4], dh[u * 4 + 1], dh[u * 4 + 2], dh[u * 4 + 3]));
-        st_sw128(sDsLo, r, unit, make_uint4(dl[u * 4], dl[u * 4 + 1], dl[u * 4 + 2], dl[u * 4 + 3]));
+        const uint32_t* h = dd + u * 4;
+        const uint32_t* lo = dd + HALF / 2 + u * 4;
+        st_sw128(sDsHi, r, unit, make_uint4(h[0], h[1], h[2], h[3]));
+        st_sw128(sDsLo, r, unit, make_uint4(lo[0], lo[1], lo[2], lo[3]));
       }
       tmem_wait_st();
       fence_async_smem();

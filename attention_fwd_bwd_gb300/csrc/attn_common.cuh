@@ -36,8 +36,9 @@ struct FwdCfg {
   static constexpr int SMEM_BYTES = 2 * Q_BYTES + NSLOT * KV_BYTES;
   static constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;  // slack for 1024-byte alignment
   // Tensor-memory columns per query tile t: scores S_t (128 fp32 columns,
-  // later overwritten by P_t: bf16 hi pairs in the first 64, lo pairs in the
-  // next 64) and the output accumulator O_t (D fp32 columns).
+  // later overwritten by P_t: for keys 16k..16k+15, bf16 hi pairs in columns
+  // 16k..16k+7 and lo pairs in 16k+8..16k+15) and the output accumulator O_t
+  // (D fp32 columns).
   __host__ __device__ static constexpr int tm_s(int t) { return 256 * t; }
   __host__ __device__ static constexpr int tm_o(int t) { return 256 * t + 128; }
   static constexpr int TMEM_COLS = 512;
@@ -107,10 +108,10 @@ struct BwdCfg {
   static constexpr int TM_DV = 128;     // dV   fp32 (D cols)
   static constexpr int TM_DK = 256;     // dK   fp32 (D cols)
   static constexpr int TM_DQ = 384;     // dQ^T fp32 (2 x 64 cols: hi part, lo part)
-  static constexpr int TM_P_HI = 384;   // P^T hi, bf16 pairs (32 cols)
-  static constexpr int TM_P_LO = 416;   // P^T lo, bf16 pairs (32 cols)
-  static constexpr int TM_DS_HI = 448;  // dS^T hi, bf16 pairs (32 cols)
-  static constexpr int TM_DS_LO = 480;  // dS^T lo, bf16 pairs (32 cols)
+  // P^T and dS^T, bf16 pairs, 64 cols each: query columns 32c..32c+31 take
+  // 32 cols from 32c on, hi pairs first (16 cols) then lo pairs (16 cols).
+  static constexpr int TM_P = 384;
+  static constexpr int TM_DS = 448;
   static constexpr int TMEM_COLS = 512;
 #ifdef ATTN_TRACE
   static constexpr int THREADS = 480;  // + one warp that timestamps MMA completions

@@ -217,16 +217,17 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           tc_fence_after();
           const int vslot = (2 * j + 1) % C::NSLOT;
           const uint64_t dv = sw128_desc(sRing + vslot * C::KV_BYTES, C::BK * 128, 1024);
-          // P hi over columns 0..63 of the score buffer, P lo over 64..127.
+          // Keys 16kk..16kk+15: P hi in score columns 16kk..16kk+7, P lo in
+          // 16kk+8..16kk+15.
           const uint32_t a_p = tmem + C::tm_s(t);
 #pragma unroll
           for (int kk = 0; kk < C::BK / 16; ++kk)
-            mma_ts_el(tmem + C::tm_o(t), a_p + kk * 8, dv + ((kk * 2048) >> 4), idesc_o,
+            mma_ts_el(tmem + C::tm_o(t), a_p + kk * 16, dv + ((kk * 2048) >> 4), idesc_o,
                       (j > 0 || kk > 0) ? 1u : 0u);
           if constexpr (SPLIT) {
 #pragma unroll
             for (int kk = 0; kk < C::BK / 16; ++kk)
-              mma_ts_el(tmem + C::tm_o(t), a_p + 64 + kk * 8, dv + ((kk * 2048) >> 4), idesc_o,
+              mma_ts_el(tmem + C::tm_o(t), a_p + kk * 16 + 8, dv + ((kk * 2048) >> 4), idesc_o,
                         1u);
           }
           if (j + 1 == n_kv_t[t]) mma_commit_el(smem_u32(&bar_pv_done[t]));
@@ -327,8 +328,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         for (int i = 0; i < 4; ++i) sums[i] = f32x2(0.f, 0.f);
 #pragma unroll
         for (int ch = 0; ch < C::BK; ch += 16) {
-          uint32_t pk[8];
-          uint32_t pl[SPLIT ? 8 : 1];
+          uint32_t pkl[16];  // P hi pairs, then (with SPLIT) P lo pairs
 #pragma unroll
           for (int c = 0; c < 16; c += 2) {
             float e0, e1;
@@ -338,14 +338,16 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
             const float p0 = ex2(e0), p1 = ex2(e1);
             sums[(c / 2) & 3] = add_f32x2(sums[(c / 2) & 3], f32x2(p0, p1));
             if constexpr (SPLIT) {
-              split_bf16x2(p0, p1, pk[c / 2], pl[c / 2]);
+              split_bf16x2(p0, p1, pkl[c / 2], pkl[8 + c / 2]);
             } else {
-              pk[c / 2] = pack_bf16x2(p0, p1);
+              pkl[c / 2] = pack_bf16x2(p0, p1);
             }
           }
-          tmem_st8(ts + ch / 2, pk);
+          // Columns ch..ch+15 of the scores (already read) take these keys' P.
           if constexpr (SPLIT)
-            tmem_st8(ts + 64 + ch / 2, *reinterpret_cast<uint32_t(*)[8]>(&pl[0]));
+            tmem_st16(ts + ch, pkl);
+          else
+            tmem_st8(ts + ch, *reinterpret_cast<uint32_t(*)[8]>(&pkl[0]));
         }
         float s0, s1;
         unpack_f32x2(add_f32x2(add_f32x2(sums[0], sums[1]), add_f32x2(sums[2], sums[3])), s0, s1);

@@ -14,6 +14,7 @@ Under torchrun (N > 1) each rank runs an independent replica on its own GPU
 (the path has no exchange step); rank 0 prints the line.
 """
 import argparse
+import datetime
 import hashlib
 import json
 import os
@@ -30,7 +31,7 @@ DEFAULT_WORKLOAD = "llama3_8b_s4096"
 
 # DRAM traffic of the backward main kernel per launch, from an ncu capture,
 # keyed by the hash of the kernel sources it was taken on (null once they change).
-TRAFFIC = {"cfbe5ec9f2d68660": 961.89e6}  # dram__bytes_read.sum + dram__bytes_write.sum, one launch
+TRAFFIC = {"e029742ebb941c59": 997.25e6}  # dram__bytes_read.sum + dram__bytes_write.sum, one launch
 
 
 def kernel_source_hash():
@@ -75,7 +76,7 @@ def whole_job_value(units_per_rank, seconds_max, world):
 
 class ClockSampler:
     """Samples SM clocks and throttle reasons with nvidia-smi during a region."""
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -90,13 +91,15 @@ class ClockSampler:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=self.fh, stderr=subprocess.DEVNULL)
+                 "-lms", "50"], stdout=self.fh, stderr=subprocess.DEVNULL)
             time.sleep(0.3)
         except OSError:
             self.proc = None
+        self.t_begin = datetime.datetime.now()
         return self
 
     def __exit__(self, *exc):
+        self.t_end = datetime.datetime.now()
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -108,22 +111,24 @@ class ClockSampler:
     def summary(self):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        mhz, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        rows = []
         with open(self.path) as f:
             for line in f:
                 parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 9:
+                if len(parts) < 10:
                     continue
                 try:
-                    mhz.append(float(parts[1]))
-                    mx = float(parts[2])
+                    t = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f")
+                    rows.append((t, float(parts[2]), float(parts[3]), parts[6:10]))
                 except ValueError:
                     continue
-                for n, val in zip(names, parts[5:9]):
-                    if val.lower().startswith("active"):
-                        reasons.add(n)
-        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": mx,
+        # samples taken while the timed steps ran (all of them if none fell inside)
+        inside = [r for r in rows if self.t_begin <= r[0] <= self.t_end] or rows
+        reasons = {n for r in inside for n, val in zip(names, r[3]) if val.lower().startswith("active")}
+        mhz = [r[1] for r in inside]
+        return {"sm_mhz": statistics.median(mhz) if mhz else None,
+                "sm_max_mhz": inside[-1][2] if inside else None,
                 "reasons": sorted(reasons), "samples": len(mhz)}
 
 
@@ -330,7 +335,7 @@ def run_ours(args, w, world, rank, local):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)

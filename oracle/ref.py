@@ -18,6 +18,12 @@ design notes of the repository):
     workload here passes exactly that value).
   * causal: key j is visible to query i iff j <= i (equal query and key
     lengths, so no row is fully masked).
+  * sliding window (the dense part of the sparse attention on the same page:
+    §4.1, Table 7 caption, "every query attends to a 128-token sliding
+    window", and §3's cr0 kernels, where consecutive tokens attend to almost
+    the same window rows): with window W > 0 and causal, key j is visible to
+    query i iff i - W < j <= i, so a query sees at most W keys, its own
+    included. window = 0 means no window; a window needs causal.
   * grouped-query attention: query head h reads key/value head h // (Hq/Hkv).
   * LSE_i = ln sum_j exp(scale * q_i . k_j) over the visible keys: the natural
     log-sum-exp of the scaled, masked scores.
@@ -55,16 +61,24 @@ def _group(Hq, Hkv):
     return Hq // Hkv
 
 
-def _scores(qh, kh, scale, causal, row0=0):
+def _check_window(causal, window):
+    if window < 0 or (window > 0 and not causal):
+        raise ValueError(f"window={window} needs causal attention and must be >= 0")
+
+
+def _scores(qh, kh, scale, causal, row0=0, window=0):
     """S = scale * Q K^T for query rows row0.. of one head, masked entries -inf.
 
     qh: [n, D] query rows (absolute positions row0..row0+n-1), kh: [S, D].
     """
+    _check_window(causal, window)
     s = scale * (qh @ kh.T)
     if causal:
         rows = row0 + np.arange(qh.shape[0])[:, None]
         cols = np.arange(kh.shape[0])[None, :]
         s[cols > rows] = -np.inf
+        if window > 0:
+            s[cols <= rows - window] = -np.inf
     return s
 
 
@@ -77,16 +91,16 @@ def _softmax_rows(s):
     return p, m + np.log(l)
 
 
-def attn_ref_probs(q, k, causal, scale, b=0, h=0):
+def attn_ref_probs(q, k, causal, scale, b=0, h=0, window=0):
     """The full attention-probability matrix P = softmax(scale Q K^T) of one
     (batch, query head), Eq. (1). Returned for the oracle's own pins."""
     q, k = _f64(q), _f64(k)
     G = _group(q.shape[2], k.shape[2])
-    p, _ = _softmax_rows(_scores(q[b, :, h, :], k[b, :, h // G, :], scale, causal))
+    p, _ = _softmax_rows(_scores(q[b, :, h, :], k[b, :, h // G, :], scale, causal, window=window))
     return p
 
 
-def attn_ref_fwd(q, k, v, causal, scale):
+def attn_ref_fwd(q, k, v, causal, scale, window=0):
     """Forward attention, Eq. (1), per (batch, query head).
 
     Returns (o [B,S,Hq,D] float64, lse [B,Hq,S] float64).
@@ -99,12 +113,13 @@ def attn_ref_fwd(q, k, v, causal, scale):
     for b in range(B):
         for h in range(Hq):
             g = h // G
-            p, lse[b, h] = _softmax_rows(_scores(q[b, :, h, :], k[b, :, g, :], scale, causal))
+            p, lse[b, h] = _softmax_rows(_scores(q[b, :, h, :], k[b, :, g, :], scale, causal,
+                                                 window=window))
             o[b, :, h, :] = p @ v[b, :, g, :]
     return o, lse
 
 
-def attn_ref_bwd(q, k, v, do, causal, scale):
+def attn_ref_bwd(q, k, v, do, causal, scale, window=0):
     """Exact gradients of L = sum(dO * O) with respect to q, k, v.
 
     Recomputes P from q, k (it takes nothing from a forward run) and returns
@@ -121,7 +136,7 @@ def attn_ref_bwd(q, k, v, do, causal, scale):
         for h in range(Hq):
             g = h // G
             qh, kh, vh, doh = q[b, :, h, :], k[b, :, g, :], v[b, :, g, :], do[b, :, h, :]
-            p, _ = _softmax_rows(_scores(qh, kh, scale, causal))
+            p, _ = _softmax_rows(_scores(qh, kh, scale, causal, window=window))
             dp = doh @ vh.T
             dvec = np.sum(p * dp, axis=1)
             ds = p * (dp - dvec[:, None])
@@ -137,7 +152,7 @@ def attn_ref_bwd(q, k, v, do, causal, scale):
 # selected rows; the test suite checks that agreement at moderate sizes.
 # ---------------------------------------------------------------------------
 
-def attn_ref_rows_fwd(q, k, v, causal, scale, rows):
+def attn_ref_rows_fwd(q, k, v, causal, scale, rows, window=0):
     """O_i and LSE_i for selected query rows.
 
     rows: iterable of (b, h, i). Returns (o [n, D], lse [n]) in float64.
@@ -148,13 +163,13 @@ def attn_ref_rows_fwd(q, k, v, causal, scale, rows):
         g = h // G
         qi = _f64(q[b, i, h, :])[None, :]
         kh = _f64(k[b, :, g, :])
-        p, l = _softmax_rows(_scores(qi, kh, scale, causal, row0=i))
+        p, l = _softmax_rows(_scores(qi, kh, scale, causal, row0=i, window=window))
         out_o.append((p @ _f64(v[b, :, g, :]))[0])
         out_l.append(l[0])
     return np.array(out_o), np.array(out_l)
 
 
-def attn_ref_rows_dq(q, k, v, do, causal, scale, rows):
+def attn_ref_rows_dq(q, k, v, do, causal, scale, rows, window=0):
     """dQ_i for selected query rows: scale * sum_j P_ij (dP_ij - Dvec_i) k_j.
 
     Row i's gradient needs only that row's probabilities, so each row is
@@ -166,7 +181,7 @@ def attn_ref_rows_dq(q, k, v, do, causal, scale, rows):
         g = h // G
         kh, vh = _f64(k[b, :, g, :]), _f64(v[b, :, g, :])
         qi = _f64(q[b, i, h, :])[None, :]
-        p, _ = _softmax_rows(_scores(qi, kh, scale, causal, row0=i))
+        p, _ = _softmax_rows(_scores(qi, kh, scale, causal, row0=i, window=window))
         dp = _f64(do[b, i, h, :])[None, :] @ vh.T
         dvec = np.sum(p * dp, axis=1)
         ds = p * (dp - dvec[:, None])
@@ -174,7 +189,7 @@ def attn_ref_rows_dq(q, k, v, do, causal, scale, rows):
     return np.array(out)
 
 
-def attn_ref_keys_dkdv(q, k, v, do, causal, scale, b, g, keys, row_block=512):
+def attn_ref_keys_dkdv(q, k, v, do, causal, scale, b, g, keys, row_block=512, window=0):
     """dK_j and dV_j for selected key rows j of key/value head g in batch b.
 
     The gradients of a key row sum over every query row of the G query heads
@@ -192,7 +207,7 @@ def attn_ref_keys_dkdv(q, k, v, do, causal, scale, b, g, keys, row_block=512):
             r1 = min(S, r0 + row_block)
             qh = _f64(q[b, r0:r1, h, :])
             doh = _f64(do[b, r0:r1, h, :])
-            p, _ = _softmax_rows(_scores(qh, kh, scale, causal, row0=r0))
+            p, _ = _softmax_rows(_scores(qh, kh, scale, causal, row0=r0, window=window))
             dp = doh @ vh.T
             dvec = np.sum(p * dp, axis=1)
             ds = p * (dp - dvec[:, None])

@@ -19,7 +19,10 @@ __all__ = [
     "lib",
     "attn_fwd",
     "attn_fwd_residual",
+    "attn_fwd_ex",
     "attn_bwd",
+    "attn_bwd_ex",
+    "attn_bwd_main_ex",
     "attn_bwd_preprocess",
     "attn_bwd_main",
     "attn_bwd_noalloc",
@@ -76,6 +79,12 @@ def lib():
     L.attn_bwd_preprocess.restype = i
     L.attn_bwd_main.argtypes = [vp] * 7 + [i] * 6 + [f, vp, sz, vp]
     L.attn_bwd_main.restype = i
+    L.attn_fwd_ex.argtypes = [vp] * 6 + [i] * 7 + [f, vp]
+    L.attn_fwd_ex.restype = i
+    L.attn_bwd_ex.argtypes = [vp] * 10 + [i] * 7 + [f, vp, sz, vp]
+    L.attn_bwd_ex.restype = i
+    L.attn_bwd_main_ex.argtypes = [vp] * 7 + [i] * 7 + [f, vp, sz, vp]
+    L.attn_bwd_main_ex.restype = i
     L.attn_bwd_noalloc.argtypes = [vp] * 10 + [i] * 6 + [f, vp]
     L.attn_bwd_noalloc.restype = i
     L.attn_status_string.argtypes = [i]
@@ -160,6 +169,21 @@ def attn_fwd_residual(q, k, v, o, o_lo, lse, causal, scale, stream=None):
                                                         _stream(stream)))
 
 
+def attn_fwd_ex(q, k, v, o, lse, causal, window, scale, o_lo=None, stream=None):
+    """Forward with a sliding window (window > 0: query i sees keys i-window+1..i,
+    needs causal); with o_lo it is the residual forward. See attn_fwd_ex in
+    include/attn.h."""
+    B, Hq, Hkv, S, D = _sizes(q, k)
+    _like(v, k, "v")
+    _like(o, q, "o")
+    if o_lo is not None:
+        _like(o_lo, q, "o_lo")
+    _lse_ok(lse, B, Hq, S, q.device)
+    _check("attn_fwd_ex", lib().attn_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _opt(o_lo), _ptr(lse),
+                                            B, Hq, Hkv, S, D, int(bool(causal)), int(window), float(scale),
+                                            _stream(stream)))
+
+
 def attn_bwd_workspace_size(B, Hq, Hkv, S, D):
     return int(lib().attn_bwd_workspace_size(B, Hq, Hkv, S, D))
 
@@ -190,6 +214,21 @@ def attn_bwd(q, k, v, o, dO, lse, dq, dk, dv, causal, scale, workspace, o_lo=Non
                                       float(scale), wp, wb, _stream(stream)))
 
 
+def attn_bwd_ex(q, k, v, o, dO, lse, dq, dk, dv, causal, window, scale, workspace, o_lo=None, stream=None):
+    """attn_bwd with a sliding window; see attn_bwd_ex in include/attn.h."""
+    B, Hq, Hkv, S, D = _sizes(q, k)
+    for t, ref, n in ((v, k, "v"), (o, q, "o"), (dO, q, "dO")):
+        _like(t, ref, n)
+    if o_lo is not None:
+        _like(o_lo, q, "o_lo")
+    _grads_ok(q, k, dq, dk, dv)
+    _lse_ok(lse, B, Hq, S, q.device)
+    wp, wb = _ws(workspace)
+    _check("attn_bwd_ex", lib().attn_bwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(dq),
+                                            _ptr(dk), _ptr(dv), _opt(o_lo), B, Hq, Hkv, S, D, int(bool(causal)),
+                                            int(window), float(scale), wp, wb, _stream(stream)))
+
+
 def attn_bwd_preprocess(q, k, o, dO, lse, dq, workspace, o_lo=None, stream=None):
     """Stage 1 of attn_bwd (q and k only supply the sizes)."""
     B, Hq, Hkv, S, D = _sizes(q, k)
@@ -205,6 +244,15 @@ def attn_bwd_main(q, k, v, dO, dq, dk, dv, causal, scale, workspace, stream=None
     _check("attn_bwd_main", lib().attn_bwd_main(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(dq), _ptr(dk),
                                                 _ptr(dv), B, Hq, Hkv, S, D, int(bool(causal)), float(scale),
                                                 wp, wb, _stream(stream)))
+
+
+def attn_bwd_main_ex(q, k, v, dO, dq, dk, dv, causal, window, scale, workspace, stream=None):
+    """Stage 2 of attn_bwd_ex."""
+    B, Hq, Hkv, S, D = _sizes(q, k)
+    wp, wb = _ws(workspace)
+    _check("attn_bwd_main_ex", lib().attn_bwd_main_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(dq), _ptr(dk),
+                                                      _ptr(dv), B, Hq, Hkv, S, D, int(bool(causal)), int(window),
+                                                      float(scale), wp, wb, _stream(stream)))
 
 
 def attn_bwd_noalloc(q, k, v, o, dO, lse, dq, dk, dv, causal, scale, o_lo=None, stream=None):

@@ -174,11 +174,18 @@ size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int S, int D) {
   return bwd_workspace_layout(B, Hq, S).total;
 }
 
+// A sliding window (window > 0) is defined for causal attention only.
+static attn_status_t validate_window(int causal, int window) {
+  if (window < 0 || (window > 0 && !causal)) return ATTN_ERR_INVALID_ARG;
+  return ATTN_OK;
+}
+
 static attn_status_t fwd_impl(const void* q, const void* k, const void* v, void* o, void* o_lo,
                               float* lse, int B, int Hq, int Hkv, int S, int D, int causal,
-                              float scale, void* stream) {
+                              int window, float scale, void* stream) {
   attn_status_t st = validate_sizes(B, Hq, Hkv, S, D);
   if (st != ATTN_OK) return st;
+  if ((st = validate_window(causal, window)) != ATTN_OK) return st;
   if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
   if (B == 0 || S == 0) return ATTN_OK;
   if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
@@ -203,6 +210,7 @@ static attn_status_t fwd_impl(const void* q, const void* k, const void* v, void*
   p.S = S;
   p.G = Hq / Hkv;
   p.causal = causal ? 1 : 0;
+  p.window = window;
   // The kernel masks a key by giving it an infinite score, which a zero scale
   // would turn into NaN. A scale below 2^-100 in magnitude is taken as
   // +-2^-100: that moves no exponent by one fp32 ulp unless |q.k| > 2^70.
@@ -219,14 +227,20 @@ static attn_status_t fwd_impl(const void* q, const void* k, const void* v, void*
 
 attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                        int Hq, int Hkv, int S, int D, int causal, float scale, void* stream) {
-  return fwd_impl(q, k, v, o, nullptr, lse, B, Hq, Hkv, S, D, causal, scale, stream);
+  return fwd_impl(q, k, v, o, nullptr, lse, B, Hq, Hkv, S, D, causal, 0, scale, stream);
 }
 
 attn_status_t attn_fwd_residual(const void* q, const void* k, const void* v, void* o, void* o_lo,
                                 float* lse, int B, int Hq, int Hkv, int S, int D, int causal,
                                 float scale, void* stream) {
   if (B > 0 && S > 0 && !o_lo) return ATTN_ERR_INVALID_ARG;
-  return fwd_impl(q, k, v, o, o_lo, lse, B, Hq, Hkv, S, D, causal, scale, stream);
+  return fwd_impl(q, k, v, o, o_lo, lse, B, Hq, Hkv, S, D, causal, 0, scale, stream);
+}
+
+attn_status_t attn_fwd_ex(const void* q, const void* k, const void* v, void* o, void* o_lo,
+                          float* lse, int B, int Hq, int Hkv, int S, int D, int causal, int window,
+                          float scale, void* stream) {
+  return fwd_impl(q, k, v, o, o_lo, lse, B, Hq, Hkv, S, D, causal, window, scale, stream);
 }
 
 attn_status_t attn_bwd_preprocess(const void* o, const void* o_lo, const void* dO,
@@ -251,11 +265,13 @@ attn_status_t attn_bwd_preprocess(const void* o, const void* o_lo, const void* d
   return finish(e, s, nullptr);
 }
 
-attn_status_t attn_bwd_main(const void* q, const void* k, const void* v, const void* dO, void* dq,
-                            void* dk, void* dv, int B, int Hq, int Hkv, int S, int D, int causal,
-                            float scale, void* workspace, size_t workspace_bytes, void* stream) {
+attn_status_t attn_bwd_main_ex(const void* q, const void* k, const void* v, const void* dO,
+                               void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int S, int D,
+                               int causal, int window, float scale, void* workspace,
+                               size_t workspace_bytes, void* stream) {
   attn_status_t st = validate_sizes(B, Hq, Hkv, S, D);
   if (st != ATTN_OK) return st;
+  if ((st = validate_window(causal, window)) != ATTN_OK) return st;
   if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
   if (B == 0 || S == 0) return ATTN_OK;
   if (!q || !k || !v || !dO || !dq || !dk || !dv) return ATTN_ERR_INVALID_ARG;
@@ -284,6 +300,7 @@ attn_status_t attn_bwd_main(const void* q, const void* k, const void* v, const v
   p.S_pad = seq_pad(S);
   p.G = Hq / Hkv;
   p.causal = causal ? 1 : 0;
+  p.window = window;
   p.scale_log2 = scale * kLog2e;
   p.scale = scale;
   p.n_ktiles = (S + 127) / 128;
@@ -294,13 +311,22 @@ attn_status_t attn_bwd_main(const void* q, const void* k, const void* v, const v
   return finish(launch_bwd_main(D, tq, tk, tv, tdo, tdq, p, s), s, p.status);
 }
 
-attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
-                       const float* lse, void* dq, void* dk, void* dv, const void* o_lo, int B,
-                       int Hq, int Hkv, int S, int D, int causal, float scale, void* workspace,
-                       size_t workspace_bytes, void* stream) {
+attn_status_t attn_bwd_main(const void* q, const void* k, const void* v, const void* dO, void* dq,
+                            void* dk, void* dv, int B, int Hq, int Hkv, int S, int D, int causal,
+                            float scale, void* workspace, size_t workspace_bytes, void* stream) {
+  return attn_bwd_main_ex(q, k, v, dO, dq, dk, dv, B, Hq, Hkv, S, D, causal, 0, scale, workspace,
+                          workspace_bytes, stream);
+}
+
+attn_status_t attn_bwd_ex(const void* q, const void* k, const void* v, const void* o,
+                          const void* dO, const float* lse, void* dq, void* dk, void* dv,
+                          const void* o_lo, int B, int Hq, int Hkv, int S, int D, int causal,
+                          int window, float scale, void* workspace, size_t workspace_bytes,
+                          void* stream) {
   // Validate everything up front so a failure launches nothing.
   attn_status_t st = validate_sizes(B, Hq, Hkv, S, D);
   if (st != ATTN_OK) return st;
+  if ((st = validate_window(causal, window)) != ATTN_OK) return st;
   if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
   if (B == 0 || S == 0) return ATTN_OK;
   if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return ATTN_ERR_INVALID_ARG;
@@ -312,8 +338,16 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
   st = attn_bwd_preprocess(o, o_lo, dO, lse, dq, B, Hq, Hkv, S, D, workspace, workspace_bytes,
                            stream);
   if (st != ATTN_OK) return st;
-  return attn_bwd_main(q, k, v, dO, dq, dk, dv, B, Hq, Hkv, S, D, causal, scale, workspace,
-                       workspace_bytes, stream);
+  return attn_bwd_main_ex(q, k, v, dO, dq, dk, dv, B, Hq, Hkv, S, D, causal, window, scale,
+                          workspace, workspace_bytes, stream);
+}
+
+attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                       const float* lse, void* dq, void* dk, void* dv, const void* o_lo, int B,
+                       int Hq, int Hkv, int S, int D, int causal, float scale, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  return attn_bwd_ex(q, k, v, o, dO, lse, dq, dk, dv, o_lo, B, Hq, Hkv, S, D, causal, 0, scale,
+                     workspace, workspace_bytes, stream);
 }
 
 attn_status_t attn_check_status(void* workspace) {

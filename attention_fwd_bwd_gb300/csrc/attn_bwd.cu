@@ -116,7 +116,8 @@ __device__ __forceinline__ void st_sw128(uint32_t tile, int row, int u, uint4 v)
                : "memory");
 }
 
-template <int D>
+// WIN: sliding-window instantiation (p.window > 0).
+template <int D, bool WIN>
 __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k,
@@ -146,7 +147,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   const int k0 = j * BK;
   const int nq = (p.S + BQ - 1) / BQ;
   const int i_start = p.causal ? (k0 / BQ) : 0;
-  const int niq = nq - i_start;
+  // With a window of W keys, the last row that sees this tile's keys is
+  // k0 + BK - 1 + W - 1.
+  const int i_end = WIN ? min(nq, (k0 + BK + p.window - 2) / BQ + 1) : nq;
+  const int niq = i_end - i_start;
   const int n_it = p.G * niq;
 
   const uint32_t sK = smem_u32(smem + C::SMEM_K);
@@ -363,8 +367,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       // This warpgroup's query columns of -LSE*log2(e) and Dvec, four at a time.
       const float4* nl4 = reinterpret_cast<const float4*>(stage_rows(s) + cg * HALF);
       const float4* dv4 = reinterpret_cast<const float4*>(stage_rows(s) + BQ + cg * HALF);
-      // Only tiles that cross the causal diagonal or hold keys past S mask.
-      const bool need_mask = (p.causal && (q0 < k0 + BK - 1)) || (k0 + BK > p.S);
+      // Only tiles that cross the causal diagonal, hold keys past S, or hold
+      // keys below some row's window mask.
+      const bool need_mask = (p.causal && (q0 < k0 + BK - 1)) || (k0 + BK > p.S) ||
+                             (WIN && k0 <= q0 + BQ - 1 - p.window);
       uint32_t us[HALF], ud[HALF];
       tmem_ld32(tmem + lane_base + C::TM_ST + cg * HALF, us);
       tmem_ld32(tmem + lane_base + C::TM_DPT + cg * HALF, ud);
@@ -378,6 +384,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       // two query columns per packed instruction.
       const uint64_t sl2 = f32x2(p.scale_log2, p.scale_log2);
       const uint64_t sc2 = f32x2(p.scale, p.scale);
+      // Key position relative to this half's first query row, and the first
+      // query column past the key's window (no window: never).
+      const int rel = key - (q0 + cg * HALF);
+      const int relw = WIN ? rel + p.window : (1 << 30);
       auto p_ds = [&](auto masked) {
 #pragma unroll
         for (int c = 0; c < HALF; c += 4) {
@@ -392,9 +402,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
                          x0, x1);
             float p0 = ex2(x0), p1 = ex2(x1);
             if (decltype(masked)::value) {
-              const int col = cg * HALF + cc;
-              if (!key_valid || (p.causal && key > q0 + col)) p0 = 0.f;
-              if (!key_valid || (p.causal && key > q0 + col + 1)) p1 = 0.f;
+              // Query column cc of this half sees the key iff rel <= cc
+              // (causal) and cc < rel + W (window); rel, relw below.
+              if (!key_valid || (p.causal && cc < rel) || cc >= relw) p0 = 0.f;
+              if (!key_valid || (p.causal && cc + 1 < rel) || cc + 1 >= relw) p1 = 0.f;
             }
             const uint64_t t = sub_f32x2(f32x2(__uint_as_float(ud[cc]), __uint_as_float(ud[cc + 1])),
                                          h ? f32x2(dv.z, dv.w) : f32x2(dv.x, dv.y));
@@ -544,7 +555,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   if (warp == 13) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
-template <int D>
+template <int D, bool WIN>
 cudaError_t launch_bwd_main_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                               const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p,
                               cudaStream_t stream) {
@@ -553,14 +564,14 @@ cudaError_t launch_bwd_main_t(const CUtensorMap& tq, const CUtensorMap& tk, cons
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(attn_bwd_main_kernel<D>,
+    cudaError_t e = cudaFuncSetAttribute(attn_bwd_main_kernel<D, WIN>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
   dim3 grid(p.B * p.Hkv, p.n_ktiles);
-  attn_bwd_main_kernel<D><<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(tq, tk, tv, tdo, tdq, p);
+  attn_bwd_main_kernel<D, WIN><<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(tq, tk, tv, tdo, tdq, p);
   return cudaGetLastError();
 }
 
@@ -591,8 +602,12 @@ cudaError_t launch_bwd_preprocess(const __nv_bfloat16* o, const __nv_bfloat16* o
 cudaError_t launch_bwd_main(int D, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
                             const BwdParams& p, cudaStream_t stream) {
-  if (D == 128) return launch_bwd_main_t<128>(tq, tk, tv, tdo, tdq, p, stream);
-  return launch_bwd_main_t<64>(tq, tk, tv, tdo, tdq, p, stream);
+  const bool win = p.window > 0;
+  if (D == 128)
+    return win ? launch_bwd_main_t<128, true>(tq, tk, tv, tdo, tdq, p, stream)
+               : launch_bwd_main_t<128, false>(tq, tk, tv, tdo, tdq, p, stream);
+  return win ? launch_bwd_main_t<64, true>(tq, tk, tv, tdo, tdq, p, stream)
+             : launch_bwd_main_t<64, false>(tq, tk, tv, tdo, tdq, p, stream);
 }
 
 }  // namespace attn

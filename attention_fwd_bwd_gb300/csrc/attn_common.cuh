@@ -52,6 +52,7 @@ struct FwdParams {
   float* lse;
   int B, Hq, Hkv, S, G;
   int causal;
+  int window;        // > 0: query i sees keys i-window+1..i (needs causal); 0: no window
   float scale_log2;  // scale * log2(e)
   int n_qblocks;     // blocks of two 128-row query tiles
   int* status;
@@ -128,6 +129,7 @@ struct BwdParams {
   float* dv;           // [B, S, Hkv, D] fp32
   int B, Hq, Hkv, S, S_pad, G;
   int causal;
+  int window;  // > 0: query i sees keys i-window+1..i (needs causal); 0: no window
   float scale_log2;
   float scale;
   int n_ktiles;

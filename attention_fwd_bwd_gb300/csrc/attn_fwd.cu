@@ -65,7 +65,9 @@ __device__ __forceinline__ float row_extreme128(const float (&x)[128]) {
   return MAX ? fmaxf(c0, c1) : fminf(c0, c1);
 }
 
-template <int D, bool SPLIT>
+// WIN: sliding-window instantiation (p.window > 0); without it the window
+// code compiles away.
+template <int D, bool SPLIT, bool WIN>
 __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
@@ -91,12 +93,20 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   const int qb = p.n_qblocks - 1 - static_cast<int>(blockIdx.y);  // longest causal rows first
   const int q0 = qb * (2 * C::BQ);                                 // first row of tile A
   const int nkv_all = (p.S + C::BK - 1) / C::BK;
-  // K/V tiles each query tile needs (tile t covers rows q0 + 128 t ...).
-  int n_kv_t[2];
+  // K/V tiles each query tile needs: [j_lo_t, n_kv_t) for tile t, which
+  // covers rows q0 + 128 t ... A sliding window of W keys starts row r's keys
+  // at r - W + 1.
+  int n_kv_t[2], j_lo_t[2];
 #pragma unroll
-  for (int t = 0; t < 2; ++t)
-    n_kv_t[t] = p.causal ? min((q0 + t * C::BQ) / C::BK + 1, nkv_all) : nkv_all;
-  const int n_kv = n_kv_t[1];  // tile B needs the most
+  for (int t = 0; t < 2; ++t) {
+    const int qt0 = q0 + t * C::BQ;
+    n_kv_t[t] = p.causal ? min(qt0 / C::BK + 1, nkv_all) : nkv_all;
+    // (A tile wholly past S still runs one K/V tile; its rows are not stored.)
+    j_lo_t[t] = WIN ? min(max(0, qt0 - p.window + 1) / C::BK, n_kv_t[t] - 1) : 0;
+  }
+  const int n_kv = n_kv_t[1];  // tile B ends last
+  const int jb = WIN ? j_lo_t[0] : 0;  // tile A starts first; the ring carries tiles jb..n_kv-1
+  auto jlo = [&](int t) { return WIN ? j_lo_t[t] : 0; };
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
@@ -144,7 +154,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
                        c * 64, hq, q0 + t * C::BQ, b);
     int issued = 0;
     bool ok = true;
-    for (int idx = 0; idx < 2 * n_kv; ++idx) {
+    for (int idx = 0; idx < 2 * (n_kv - jb); ++idx) {
       const int slot = idx % C::NSLOT, round = idx / C::NSLOT;
       if (round > 0) ok = mbar_wait_warp(smem_u32(&bar_kv_empty[slot]), (round - 1) & 1, ctl);
       if (!ok) break;
@@ -154,8 +164,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       const CUtensorMap* m = (idx & 1) ? &tm_v : &tm_k;
       mbar_arrive_expect_tx_el(full, C::KV_BYTES);
       for (int c = 0; c < C::KCH; ++c)
-        tma_load_4d_hint_el(dst + c * (C::BK * 128), m, full, c * 64, g, (idx >> 1) * C::BK, b,
-                            keep);
+        tma_load_4d_hint_el(dst + c * (C::BK * 128), m, full, c * 64, g, (jb + (idx >> 1)) * C::BK,
+                            b, keep);
       issued = idx + 1;
     }
     if (lane == 0) {
@@ -179,9 +189,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
       constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, 0, 1);
       const uint64_t dq_desc = sw128_desc(sQ, 16, 1024);
+      // Ring position of K_j is 2 (j - jb), of V_j the one after it.
       // S_t = Q_t K_j^T into tile t's score buffer.
       auto issue_s = [&](int t, int j) {
-        const int slot = (2 * j) % C::NSLOT;
+        const int slot = (2 * (j - jb)) % C::NSLOT;
         const uint64_t dk = sw128_desc(sRing + slot * C::KV_BYTES, 16, 1024);
         const uint64_t dq = dq_desc + ((t * C::Q_BYTES) >> 4);
 #pragma unroll
@@ -197,46 +208,47 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       ok = wait_kv(0);
       if (ok) {
         tc_fence_after();
-        issue_s(0, 0);
-        issue_s(1, 0);
-        mma_commit_el(smem_u32(&bar_kv_empty[0]));  // K_0 is done once both S_t(0) ran
+        issue_s(0, jb);
+        if (jlo(1) == jb) issue_s(1, jb);
+        mma_commit_el(smem_u32(&bar_kv_empty[0]));  // K_jb is done once its S products ran
         ATTN_TRACE_EV(tc, 3, 0);
       }
-      for (int j = 0; j < n_kv && ok; ++j) {
+      for (int j = jb; j < n_kv && ok; ++j) {
         bool v_ready = false, k_next_ready = false;
         for (int t = 0; t < 2 && ok; ++t) {
-          if (j >= n_kv_t[t]) continue;
-          ok = mbar_wait_warp(smem_u32(&bar_p_full[t]), j & 1, ctl);
-          if (!ok) break;
-          ATTN_TRACE_EV(tc, 4 + t, j);  // P_t(j) ready seen
-          if (!v_ready) {
-            ok = wait_kv(2 * j + 1);
+          if (j >= jlo(t) && j < n_kv_t[t]) {
+            ok = mbar_wait_warp(smem_u32(&bar_p_full[t]), (j - jlo(t)) & 1, ctl);
             if (!ok) break;
-            v_ready = true;
-          }
-          tc_fence_after();
-          const int vslot = (2 * j + 1) % C::NSLOT;
-          const uint64_t dv = sw128_desc(sRing + vslot * C::KV_BYTES, C::BK * 128, 1024);
-          // Keys 16kk..16kk+15: P hi in score columns 16kk..16kk+7, P lo in
-          // 16kk+8..16kk+15.
-          const uint32_t a_p = tmem + C::tm_s(t);
-#pragma unroll
-          for (int kk = 0; kk < C::BK / 16; ++kk)
-            mma_ts_el(tmem + C::tm_o(t), a_p + kk * 16, dv + ((kk * 2048) >> 4), idesc_o,
-                      (j > 0 || kk > 0) ? 1u : 0u);
-          if constexpr (SPLIT) {
+            ATTN_TRACE_EV(tc, 4 + t, j);  // P_t(j) ready seen
+            if (!v_ready) {
+              ok = wait_kv(2 * (j - jb) + 1);
+              if (!ok) break;
+              v_ready = true;
+            }
+            tc_fence_after();
+            const int vslot = (2 * (j - jb) + 1) % C::NSLOT;
+            const uint64_t dv = sw128_desc(sRing + vslot * C::KV_BYTES, C::BK * 128, 1024);
+            // Keys 16kk..16kk+15: P hi in score columns 16kk..16kk+7, P lo in
+            // 16kk+8..16kk+15.
+            const uint32_t a_p = tmem + C::tm_s(t);
 #pragma unroll
             for (int kk = 0; kk < C::BK / 16; ++kk)
-              mma_ts_el(tmem + C::tm_o(t), a_p + kk * 16 + 8, dv + ((kk * 2048) >> 4), idesc_o,
-                        1u);
+              mma_ts_el(tmem + C::tm_o(t), a_p + kk * 16, dv + ((kk * 2048) >> 4), idesc_o,
+                        (j > jlo(t) || kk > 0) ? 1u : 0u);
+            if constexpr (SPLIT) {
+#pragma unroll
+              for (int kk = 0; kk < C::BK / 16; ++kk)
+                mma_ts_el(tmem + C::tm_o(t), a_p + kk * 16 + 8, dv + ((kk * 2048) >> 4), idesc_o,
+                          1u);
+            }
+            if (j + 1 == n_kv_t[t]) mma_commit_el(smem_u32(&bar_pv_done[t]));
+            ATTN_TRACE_EV(tc, 6 + t, j);  // PV_t(j) issued
           }
-          if (j + 1 == n_kv_t[t]) mma_commit_el(smem_u32(&bar_pv_done[t]));
-          ATTN_TRACE_EV(tc, 6 + t, j);  // PV_t(j) issued
           // The next score tile of t overwrites P_t(j) in TMEM; MMAs execute in
           // issue order, so it runs after PV_t(j) has read P_t(j).
-          if (j + 1 < n_kv_t[t]) {
+          if (j + 1 < n_kv_t[t] && j + 1 >= jlo(t)) {
             if (!k_next_ready) {
-              ok = wait_kv(2 * j + 2);
+              ok = wait_kv(2 * (j - jb) + 2);
               if (!ok) break;
               k_next_ready = true;
               tc_fence_after();
@@ -245,10 +257,20 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           }
         }
         if (!ok) break;
-        // Every use of V_j (and of K_{j+1}) has been issued: release the slots
-        // when those MMAs complete.
-        mma_commit_el(smem_u32(&bar_kv_empty[(2 * j + 1) % C::NSLOT]));
-        if (k_next_ready) mma_commit_el(smem_u32(&bar_kv_empty[(2 * j + 2) % C::NSLOT]));
+        // Release V_j and K_{j+1} when the MMAs issued on them complete. Every
+        // ring tile has a use (with a window too, the tiles' ranges leave no
+        // gap), so with a window these waits only make sure that no copy is in
+        // flight when its slot is handed back.
+        if constexpr (WIN) {
+          if (!v_ready) ok = wait_kv(2 * (j - jb) + 1);
+          if (ok && j + 1 < n_kv && !k_next_ready) {
+            ok = wait_kv(2 * (j - jb) + 2);
+            k_next_ready = ok;
+          }
+          if (!ok) break;
+        }
+        mma_commit_el(smem_u32(&bar_kv_empty[(2 * (j - jb) + 1) % C::NSLOT]));
+        if (k_next_ready) mma_commit_el(smem_u32(&bar_kv_empty[(2 * (j - jb) + 2) % C::NSLOT]));
       }
       // Wait for every MMA issued to finish before TMEM is released (in a
       // normal run the epilogue has already waited for them). bar_q_full has
@@ -274,10 +296,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     TraceCursor tc;
     if (lane == 0 && (warp == 0 || warp == 4)) ATTN_TRACE_INIT(tc, 2 + t);
     bool ok = true;
-    for (int j = 0; j < my_kv; ++j) {
+    for (int j = jlo(t); j < my_kv; ++j) {
       ATTN_TRACE_EV(tc, 1, j);  // start waiting for S_t(j)
       // S_t(j) landed; its commit also covers PV_t(j-1), so O_t is current.
-      ok = mbar_wait_warp(smem_u32(&bar_s_full[t]), j & 1, ctl);
+      ok = mbar_wait_warp(smem_u32(&bar_s_full[t]), (j - jlo(t)) & 1, ctl);
       if (!ok) break;
       ATTN_TRACE_EV(tc, 2, j);  // S_t(j) landed
       tc_fence_after();
@@ -294,8 +316,13 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       }
       const int k0 = j * C::BK;
       const int qt0 = q0 + t * C::BQ;
-      const bool need_mask = (p.causal && k0 + C::BK - 1 > qt0) || (k0 + C::BK > p.S);
-      const int lim = p.causal ? min(qrow, p.S - 1) : (p.S - 1);  // last visible key
+      // Tiles that cross the causal diagonal, hold keys past S, or hold keys
+      // below some row's window mask; the rest skip masking.
+      const bool need_mask = (p.causal && k0 + C::BK - 1 > qt0) || (k0 + C::BK > p.S) ||
+                             (WIN && k0 < qt0 + C::BQ - p.window);
+      // Visible columns of this tile for this row: c_lo <= c <= c_hi.
+      const int c_hi = (p.causal ? min(qrow, p.S - 1) : (p.S - 1)) - k0;
+      const int c_lo = WIN ? qrow - p.window + 1 - k0 : 0;
       float alpha = 1.f;
       bool rescale = false;
       // One tile of the online softmax: row max, exponentials, row sum and P
@@ -311,7 +338,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           const float lose = pos ? -INFINITY : INFINITY;
 #pragma unroll
           for (int c = 0; c < C::BK; ++c)
-            if (k0 + c > lim) x[c] = lose;
+            if (c > c_hi || (WIN && c < c_lo)) x[c] = lose;
         }
         static_assert(C::BK == 128, "row_extreme128 covers one 128-key tile");
         const float mraw = pos ? row_extreme128<true>(x) : row_extreme128<false>(x);
@@ -322,7 +349,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           m = mx;
         }
         const uint64_t sl2x2 = f32x2(sl2, sl2);
-        const uint64_t negm2 = f32x2(-m, -m);
+        // A row whose keys in this tile are all outside its window keeps
+        // m = -inf; an offset of 0 then gives its masked scores p = 0.
+        const float neg_m = (WIN && m == -INFINITY) ? 0.f : -m;
+        const uint64_t negm2 = f32x2(neg_m, neg_m);
         uint64_t sums[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) sums[i] = f32x2(0.f, 0.f);
@@ -355,7 +385,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       }
       ATTN_TRACE_EV(tc, 3, j);  // exponentials done
       // Rescale this warp's O rows (PV_t(j-1) has completed, see above).
-      if (j >= 1 && __any_sync(0xffffffffu, rescale)) {
+      if (j > jlo(t) && __any_sync(0xffffffffu, rescale)) {
         const uint32_t to = tmem + lane_base + C::tm_o(t);
 #pragma unroll
         for (int c = 0; c < D; c += 32) {
@@ -417,7 +447,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   if (warp == 9) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
-template <int D, bool SPLIT>
+template <int D, bool SPLIT, bool WIN>
 cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const FwdParams& p, cudaStream_t stream) {
   using C = FwdCfg<D>;
@@ -425,14 +455,14 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D, SPLIT>,
+    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D, SPLIT, WIN>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
   dim3 grid(p.B * p.Hq, p.n_qblocks);
-  attn_fwd_kernel<D, SPLIT><<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(tq, tk, tv, p);
+  attn_fwd_kernel<D, SPLIT, WIN><<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 
@@ -440,12 +470,19 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
 
 cudaError_t launch_fwd(int D, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const FwdParams& p, cudaStream_t stream) {
-  const bool split = p.o_lo != nullptr;
-  if (D == 128)
-    return split ? launch_fwd_t<128, true>(tq, tk, tv, p, stream)
-                 : launch_fwd_t<128, false>(tq, tk, tv, p, stream);
-  return split ? launch_fwd_t<64, true>(tq, tk, tv, p, stream)
-               : launch_fwd_t<64, false>(tq, tk, tv, p, stream);
+  const bool split = p.o_lo != nullptr, win = p.window > 0;
+  if (D == 128) {
+    if (win)
+      return split ? launch_fwd_t<128, true, true>(tq, tk, tv, p, stream)
+                   : launch_fwd_t<128, false, true>(tq, tk, tv, p, stream);
+    return split ? launch_fwd_t<128, true, false>(tq, tk, tv, p, stream)
+                 : launch_fwd_t<128, false, false>(tq, tk, tv, p, stream);
+  }
+  if (win)
+    return split ? launch_fwd_t<64, true, true>(tq, tk, tv, p, stream)
+                 : launch_fwd_t<64, false, true>(tq, tk, tv, p, stream);
+  return split ? launch_fwd_t<64, true, false>(tq, tk, tv, p, stream)
+               : launch_fwd_t<64, false, false>(tq, tk, tv, p, stream);
 }
 
 }  // namespace attn

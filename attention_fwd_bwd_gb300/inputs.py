@@ -27,13 +27,19 @@ class Workload:
     causal: bool
     qk_std: float = 1.0
     seed: int = 1234
+    window: int = 0  # > 0: sliding-window causal attention over the last `window` keys
 
     @property
     def scale(self) -> float:
         return 1.0 / math.sqrt(self.D)
 
     def flops_fwd(self) -> float:
-        """4 * B * Hq * S^2 * D, halved when causal."""
+        """4 * B * Hq * S^2 * D, halved when causal; with a window of W keys,
+        4 * B * Hq * D times the visible (query, key) pairs, sum_i min(i+1, W)."""
+        if self.window > 0:
+            W, S = min(self.window, self.S), self.S
+            pairs = W * (W + 1) / 2 + (S - W) * W
+            return 4.0 * self.B * self.Hq * self.D * pairs
         f = 4.0 * self.B * self.Hq * self.S * self.S * self.D
         return f / 2 if self.causal else f
 
@@ -52,7 +58,14 @@ WORKLOADS = [
     Workload("llama3_70b_s8192", 1, 64, 8, 8192, 128, True, 2.0, 1237),
     Workload("long_s32768", 1, 32, 8, 32768, 128, True, 1.0, 1238),
 ]
-BY_NAME = {w.name: w for w in WORKLOADS}
+# Beyond those: sliding-window causal attention with a 128-key window and 64
+# query heads, the dense part (cr0) of the sparse attention the pages study
+# (Table 7: "Flash cr0", 64 heads, every query over a 128-token window), at
+# the Llama-3-8B sequence length.
+EXTRA_WORKLOADS = [
+    Workload("swa_w128_s4096", 2, 64, 8, 4096, 128, True, 1.0, 1240, 128),
+]
+BY_NAME = {w.name: w for w in WORKLOADS + EXTRA_WORKLOADS}
 
 
 def make_inputs(B, Hq, Hkv, S, D, seed, qk_std=1.0):

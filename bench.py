@@ -151,8 +151,8 @@ def oracle_sample(w, budget_s=12.0, max_heads=None):
         h = heads
         g = h // G
         qs, ks, vs, ds = (f64(q[:, :, h:h + 1]), f64(k[:, :, g:g + 1]), f64(v[:, :, g:g + 1]), f64(do[:, :, h:h + 1]))
-        attn_ref_fwd(qs, ks, vs, w.causal, w.scale)
-        attn_ref_bwd(qs, ks, vs, ds, w.causal, w.scale)
+        attn_ref_fwd(qs, ks, vs, w.causal, w.scale, window=w.window)
+        attn_ref_bwd(qs, ks, vs, ds, w.causal, w.scale, window=w.window)
         heads += 1
         if time.perf_counter() - t0 >= budget_s:
             break
@@ -186,6 +186,7 @@ def run_reference(args, w, world, rank):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded N(0,1) bf16 inputs of the workload's shape)",
         "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "S": w.S, "D": w.D,
+                   "window": w.window,
                    "causal": w.causal, "parallelism": "replicas"},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
                          "sample": f"per step: {sample}"},
@@ -218,13 +219,13 @@ def run_ours(args, w, world, rank, local):
     def step(ev=None):
         if ev is not None:
             ev[0].record(stream)
-        attn.attn_fwd_residual(q, k, v, o, o_lo, lse, w.causal, w.scale, stream=stream)
+        attn.attn_fwd_ex(q, k, v, o, lse, w.causal, w.window, w.scale, o_lo=o_lo, stream=stream)
         if ev is not None:
             ev[1].record(stream)
         attn.attn_bwd_preprocess(q, k, o, do, lse, dq, ws, o_lo=o_lo, stream=stream)
         if ev is not None:
             ev[2].record(stream)
-        attn.attn_bwd_main(q, k, v, do, dq, dk, dv, w.causal, w.scale, ws, stream=stream)
+        attn.attn_bwd_main_ex(q, k, v, do, dq, dk, dv, w.causal, w.window, w.scale, ws, stream=stream)
         if ev is not None:
             ev[3].record(stream)
 
@@ -271,8 +272,9 @@ def run_ours(args, w, world, rank, local):
     def e2e_step():
         for dst, src in ((q, hq_), (k, hk_), (v, hv_), (do, hdo_)):
             dst.copy_(src, non_blocking=True)
-        attn.attn_fwd_residual(q, k, v, o, o_lo, lse, w.causal, w.scale, stream=stream)
-        attn.attn_bwd(q, k, v, o, do, lse, dq, dk, dv, w.causal, w.scale, ws, o_lo=o_lo, stream=stream)
+        attn.attn_fwd_ex(q, k, v, o, lse, w.causal, w.window, w.scale, o_lo=o_lo, stream=stream)
+        attn.attn_bwd_ex(q, k, v, o, do, lse, dq, dk, dv, w.causal, w.window, w.scale, ws, o_lo=o_lo,
+                         stream=stream)
         for dst, src in ((ho, o), (hlse, lse), (hdq, dq), (hdk, dk), (hdv, dv)):
             dst.copy_(src, non_blocking=True)
 
@@ -294,7 +296,9 @@ def run_ours(args, w, world, rank, local):
     main_tf = w.flops_bwd() / (main_ms / 1e3) / 1e12
     fwd_tf = w.flops_fwd() / (fwd_ms / 1e3) / 1e12
     pre_bytes = (3 * B * S * Hq * D * 2 + B * Hq * S * 4 + 2 * B * Hq * S * 4 + B * S * Hq * D * 4)
-    traffic = TRAFFIC.get(kernel_source_hash())
+    # The ncu traffic figure is for the default workload's launch.
+    traffic = TRAFFIC.get(kernel_source_hash()) if w.name == DEFAULT_WORKLOAD else None
+    in_bytes = sum(t.numel() * t.element_size() for t in (q, k, v, do))
     sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
 
     if rank == 0:
@@ -304,8 +308,9 @@ def run_ours(args, w, world, rank, local):
             "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded N(0,1) bf16 q, k, v, dO of the workload's shape)",
             "config": {"workload": w.name, "B": B, "Hq": Hq, "Hkv": Hkv, "S": S, "D": D, "causal": w.causal,
+                       "window": w.window,
                        "parallelism": f"replicas x{world}",
-                       "l2": "no flush: q, k, v, dO (168 MB) exceed the 129 MB L2",
+                       "l2": f"no flush: q, k, v, dO ({in_bytes / 1e6:.0f} MB) exceed the 129 MB L2",
                        "flops_per_step": flops, "sm_count": sm_count},
             "gpu_launches": 3 * args.steps,
             "passes": {

@@ -139,6 +139,39 @@ attn_status_t attn_bwd_main(const void* q, const void* k, const void* v, const v
                             float scale, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Sliding-window causal attention: forms of attn_fwd / attn_fwd_residual,
+ * attn_bwd and attn_bwd_main with a `window` argument. The window is the
+ * dense part of the sparse attention in "Scheduling Data to Compute:
+ * Hierarchical Data Pipelining for LLM Training on AMD GPUs" (§4.1, Table 7
+ * caption: every query attends to a 128-token sliding window; §3's cr0
+ * kernels). With window = W > 0, query i sees keys i-W+1..i (at most W keys,
+ * its own included); the kernels skip key tiles that no row of a query tile
+ * sees. window = 0 is plain attention and gives the results of the calls
+ * without `window`.
+ *
+ *   window  >= 0; a window > 0 needs causal != 0 (else ATTN_ERR_INVALID_ARG,
+ *           checked right after the sizes). W >= S is plain causal attention.
+ *   o_lo    (attn_fwd_ex) NULL for the inference forward of attn_fwd, or the
+ *           residual output of attn_fwd_residual.
+ *
+ * Other arguments, results and errors are those of the calls without
+ * `window`. The backward must get the same causal and window values as the
+ * forward that produced lse (and o, o_lo).
+ */
+attn_status_t attn_fwd_ex(const void* q, const void* k, const void* v, void* o, void* o_lo,
+                          float* lse, int B, int Hq, int Hkv, int S, int D, int causal, int window,
+                          float scale, void* stream);
+attn_status_t attn_bwd_ex(const void* q, const void* k, const void* v, const void* o,
+                          const void* dO, const float* lse, void* dq, void* dk, void* dv,
+                          const void* o_lo, int B, int Hq, int Hkv, int S, int D, int causal,
+                          int window, float scale, void* workspace, size_t workspace_bytes,
+                          void* stream);
+attn_status_t attn_bwd_main_ex(const void* q, const void* k, const void* v, const void* dO,
+                               void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int S, int D,
+                               int causal, int window, float scale, void* workspace,
+                               size_t workspace_bytes, void* stream);
+
+/*
  * attn_bwd without a workspace argument, for callers that cannot allocate
  * device memory. The paper has no counterpart: this is a packaging variant of
  * attn_bwd, not part of the method.

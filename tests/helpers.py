@@ -12,9 +12,10 @@ TOL_LSE = 1e-3
 TOL_GRAD_REL_RMS = 5e-2
 
 
-def gpu_fwd_bwd(q, k, v, do, causal, scale, with_bwd=True):
+def gpu_fwd_bwd(q, k, v, do, causal, scale, with_bwd=True, window=0):
     """Run attn_fwd_residual (and attn_bwd with the residual) on cuda:0 for
-    bf16 CPU tensors; returns a dict of CPU tensors (o, lse, dq, dk, dv)."""
+    bf16 CPU tensors; returns a dict of CPU tensors (o, lse, dq, dk, dv).
+    With window > 0 the sliding-window forms (attn_fwd_ex, attn_bwd_ex) run."""
     dev = torch.device("cuda", 0)
     qd, kd, vd, dod = (t.to(dev).contiguous() for t in (q, k, v, do))
     B, S, Hq, D = q.shape
@@ -22,7 +23,10 @@ def gpu_fwd_bwd(q, k, v, do, causal, scale, with_bwd=True):
     o = torch.empty_like(qd)
     o_lo = torch.empty_like(qd)
     lse = torch.empty(B, Hq, S, dtype=torch.float32, device=dev)
-    attn.attn_fwd_residual(qd, kd, vd, o, o_lo, lse, causal, scale)
+    if window:
+        attn.attn_fwd_ex(qd, kd, vd, o, lse, causal, window, scale, o_lo=o_lo)
+    else:
+        attn.attn_fwd_residual(qd, kd, vd, o, o_lo, lse, causal, scale)
     out = {"o": o, "lse": lse}
     ws = None
     if with_bwd:
@@ -30,7 +34,10 @@ def gpu_fwd_bwd(q, k, v, do, causal, scale, with_bwd=True):
         f32 = dict(dtype=torch.float32, device=dev)
         dq = torch.empty(qd.shape, **f32)
         dk, dv = torch.empty(kd.shape, **f32), torch.empty(vd.shape, **f32)
-        attn.attn_bwd(qd, kd, vd, o, dod, lse, dq, dk, dv, causal, scale, ws, o_lo=o_lo)
+        if window:
+            attn.attn_bwd_ex(qd, kd, vd, o, dod, lse, dq, dk, dv, causal, window, scale, ws, o_lo=o_lo)
+        else:
+            attn.attn_bwd(qd, kd, vd, o, dod, lse, dq, dk, dv, causal, scale, ws, o_lo=o_lo)
         out.update(dq=dq, dk=dk, dv=dv)
     torch.cuda.synchronize()
     st = attn.attn_check_status(ws)

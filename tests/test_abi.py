@@ -67,6 +67,23 @@ def test_fwd_argument_validation(L):
     assert _fwd(L, S=0, q=None, k=None, v=None, o=None, lse=None) == 0
 
 
+def test_window_argument_validation(L):
+    fwd = lambda window, causal=1, B=1: L.attn_fwd_ex(FAKE, FAKE, FAKE, FAKE, None, FAKE, B, 2, 1, 128, 64,
+                                                     causal, window, 0.125, None)
+    assert fwd(-1) == 1                       # negative window
+    assert fwd(4, causal=0) == 1              # a window needs causal
+    assert fwd(-1, B=0) == 1                  # checked with the sizes, before the empty no-op
+    assert fwd(4, B=0) == 0                   # empty: no-op
+    bwd = lambda window, causal=1: L.attn_bwd_ex(*([FAKE] * 9 + [None]), 1, 2, 1, 128, 64, causal, window,
+                                                 0.125, FAKE * 16, 1 << 30, None)
+    assert bwd(-3) == 1
+    assert bwd(128, causal=0) == 1
+    main = lambda window, causal=1: L.attn_bwd_main_ex(*([FAKE] * 7), 1, 2, 1, 128, 64, causal, window,
+                                                       0.125, FAKE * 16, 1 << 30, None)
+    assert main(-3) == 1
+    assert main(128, causal=0) == 1
+
+
 def test_bwd_argument_validation(L):
     def bwd(ws=FAKE * 16, wsb=1 << 30, B=1, S=128, D=64, ptrs=None, Hq=2, Hkv=1):
         p = ptrs if ptrs is not None else [FAKE] * 9 + [None]

@@ -46,6 +46,26 @@ def test_small_shapes_elementwise(B, Hq, Hkv, S, D, causal):
     assert_close_grad(got["dv"], dv_ref, "dV", what)
 
 
+@pytest.mark.parametrize("scale", [0.0, -0.25, 1e-35, 0.6])
+@pytest.mark.parametrize("causal", [True, False])
+def test_special_scales(scale, causal):
+    # scale 0: uniform attention over the visible keys (dQ = dK = 0); a
+    # negative scale flips which keys dominate; 1e-35 is below the forward's
+    # smallest exponent scale; 0.6 gives a sharp softmax.
+    B, Hq, Hkv, S, D = 1, 2, 1, 200, 128
+    q, k, v, do = make_inputs(B, Hq, Hkv, S, D, seed=7)
+    got = gpu_fwd_bwd(q, k, v, do, causal, scale)
+    o_ref, lse_ref = attn_ref_fwd(np64(q), np64(k), np64(v), causal, scale)
+    dq_ref, dk_ref, dv_ref = attn_ref_bwd(np64(q), np64(k), np64(v), np64(do), causal, scale)
+    what = f"scale={scale} causal={causal}"
+    for name in ("o", "lse", "dq", "dk", "dv"):
+        assert np.isfinite(np64(got[name])).all(), f"{what}: non-finite {name}"
+    assert_close_fwd(got["o"], got["lse"], o_ref, lse_ref, what)
+    assert_close_grad(got["dq"], dq_ref, "dQ", what)
+    assert_close_grad(got["dk"], dk_ref, "dK", what)
+    assert_close_grad(got["dv"], dv_ref, "dV", what)
+
+
 def test_tiny_workload_full():
     w = WORKLOADS[0]
     q, k, v, do = workload_inputs(w)

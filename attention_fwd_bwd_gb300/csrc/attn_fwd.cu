@@ -67,6 +67,48 @@ __device__ __forceinline__ float row_extreme128(const float (&x)[128]) {
 
 // WIN: sliding-window instantiation (p.window > 0); without it the window
 // code compiles away.
+// One work item: batch b, query head hq, and the two 128-row query tiles
+// starting at q0; tile t needs K/V tiles [j_lo[t], n_kv[t]). A sliding
+// window of W keys starts row r's keys at r - W + 1.
+struct FwdItem {
+  int b, hq, g, q0;
+  int n_kv[2], j_lo[2];
+};
+
+// Items in longest-first order: index i takes head i % (B Hq) of query-block
+// pair n_qblocks - 1 - i / (B Hq) (the causal rows get shorter down the list).
+template <bool WIN>
+__device__ __forceinline__ FwdItem fwd_item(const FwdParams& p, int i) {
+  constexpr int BQ = 128, BK = 128;
+  FwdItem it;
+  const int bhq = p.B * p.Hq;
+  const int bh = i % bhq;
+  it.hq = bh % p.Hq;
+  it.b = bh / p.Hq;
+  it.g = it.hq / p.G;
+  it.q0 = (p.n_qblocks - 1 - i / bhq) * (2 * BQ);
+  const int nkv_all = (p.S + BK - 1) / BK;
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int qt0 = it.q0 + t * BQ;
+    it.n_kv[t] = p.causal ? min(qt0 / BK + 1, nkv_all) : nkv_all;
+    // (A tile wholly past S still runs one K/V tile; its rows are not stored.)
+    it.j_lo[t] = WIN ? min(max(0, qt0 - p.window + 1) / BK, it.n_kv[t] - 1) : 0;
+  }
+  return it;
+}
+
+// The r-th item of CTA c among G CTAs: round r hands items r G .. r G + G - 1
+// to the CTAs, in reverse order on odd rounds, which balances the
+// longest-first list (a negative result: no item left).
+__device__ __forceinline__ int fwd_item_index(int r, int c, int G, int n_items) {
+  const int i = r * G + ((r & 1) ? (G - 1 - c) : c);
+  return i < n_items ? i : -1;
+}
+
+// WIN: sliding-window instantiation (p.window > 0); without it the window
+// code compiles away. The kernel is persistent: each CTA loops over its work
+// items, and every barrier keeps counting phases across items.
 template <int D, bool SPLIT, bool WIN>
 __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -77,7 +119,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
 
-  __shared__ uint64_t bar_q_full;
+  __shared__ uint64_t bar_q_full, bar_q_empty, bar_mma_done;
   __shared__ uint64_t bar_kv_full[C::NSLOT], bar_kv_empty[C::NSLOT];
   __shared__ uint64_t bar_s_full[2], bar_p_full[2], bar_pv_done[2];
   __shared__ uint32_t tmem_base_s;
@@ -85,32 +127,15 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
-
-  const int bh = blockIdx.x;  // b * Hq + hq
-  const int hq = bh % p.Hq;
-  const int b = bh / p.Hq;
-  const int g = hq / p.G;
-  const int qb = p.n_qblocks - 1 - static_cast<int>(blockIdx.y);  // longest causal rows first
-  const int q0 = qb * (2 * C::BQ);                                 // first row of tile A
-  const int nkv_all = (p.S + C::BK - 1) / C::BK;
-  // K/V tiles each query tile needs: [j_lo_t, n_kv_t) for tile t, which
-  // covers rows q0 + 128 t ... A sliding window of W keys starts row r's keys
-  // at r - W + 1.
-  int n_kv_t[2], j_lo_t[2];
-#pragma unroll
-  for (int t = 0; t < 2; ++t) {
-    const int qt0 = q0 + t * C::BQ;
-    n_kv_t[t] = p.causal ? min(qt0 / C::BK + 1, nkv_all) : nkv_all;
-    // (A tile wholly past S still runs one K/V tile; its rows are not stored.)
-    j_lo_t[t] = WIN ? min(max(0, qt0 - p.window + 1) / C::BK, n_kv_t[t] - 1) : 0;
-  }
-  const int n_kv = n_kv_t[1];  // tile B ends last
-  const int jb = WIN ? j_lo_t[0] : 0;  // tile A starts first; the ring carries tiles jb..n_kv-1
-  auto jlo = [&](int t) { return WIN ? j_lo_t[t] : 0; };
+  const int n_items = p.B * p.Hq * p.n_qblocks;
+  const int cta = blockIdx.x, n_cta = gridDim.x;
+  auto jlo = [&](const FwdItem& it, int t) { return WIN ? it.j_lo[t] : 0; };
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(smem_u32(&bar_q_full), 1);
+    mbar_init(smem_u32(&bar_q_empty), 1);
+    mbar_init(smem_u32(&bar_mma_done), 1);
     for (int i = 0; i < C::NSLOT; ++i) {
       mbar_init(smem_u32(&bar_kv_full[i]), 1);
       mbar_init(smem_u32(&bar_kv_empty[i]), 1);
@@ -138,6 +163,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   if (warp == 8) {
     // ------------------------------------------------------------ producer
     // The whole warp runs this loop; each copy is issued by one elected lane.
+    // Per item: the first K/V tile pair, then Q_A and Q_B once the previous
+    // item's last S product has read the Q buffer, then the remaining K/V
+    // tiles. Ring positions run on across items.
     TraceCursor tc;
     if (lane == 0) ATTN_TRACE_INIT(tc, 0);
     ATTN_TRACE_EV(tc, 1, 0);
@@ -147,33 +175,49 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       prefetch_tmap(&tm_v);
     }
     const uint64_t keep = policy_evict_last();  // K/V tiles are re-read by G heads x tiles
-    mbar_arrive_expect_tx_el(smem_u32(&bar_q_full), 2 * C::Q_BYTES);
-    for (int t = 0; t < 2; ++t)
-      for (int c = 0; c < C::KCH; ++c)
-        tma_load_4d_el(sQ + t * C::Q_BYTES + c * (C::BQ * 128), &tm_q, smem_u32(&bar_q_full),
-                       c * 64, hq, q0 + t * C::BQ, b);
-    int issued = 0;
+    int issued = 0;   // ring positions issued
+    int q_loads = 0;  // Q loads issued
     bool ok = true;
-    for (int idx = 0; idx < 2 * (n_kv - jb); ++idx) {
-      const int slot = idx % C::NSLOT, round = idx / C::NSLOT;
-      if (round > 0) ok = mbar_wait_warp(smem_u32(&bar_kv_empty[slot]), (round - 1) & 1, ctl);
+    for (int r = 0; ok; ++r) {
+      const int ii = fwd_item_index(r, cta, n_cta, n_items);
+      if (ii < 0) break;
+      const FwdItem it = fwd_item<WIN>(p, ii);
+      const int jb = jlo(it, 0);
+      const int n_pos = 2 * (it.n_kv[1] - jb);
+      auto load_kv = [&](int idx) {
+        const int pos = issued;
+        const int slot = pos % C::NSLOT, round = pos / C::NSLOT;
+        if (round > 0) ok = mbar_wait_warp(smem_u32(&bar_kv_empty[slot]), (round - 1) & 1, ctl);
+        if (!ok) return;
+        ATTN_TRACE_EV(tc, 2, pos);  // slot free, issuing the load
+        const uint32_t full = smem_u32(&bar_kv_full[slot]);
+        const uint32_t dst = sRing + slot * C::KV_BYTES;
+        const CUtensorMap* m = (idx & 1) ? &tm_v : &tm_k;
+        mbar_arrive_expect_tx_el(full, C::KV_BYTES);
+        for (int c = 0; c < C::KCH; ++c)
+          tma_load_4d_hint_el(dst + c * (C::BK * 128), m, full, c * 64, it.g,
+                              (jb + (idx >> 1)) * C::BK, it.b, keep);
+        issued = pos + 1;
+      };
+      const int pre = (r == 0) ? 0 : min(2, n_pos);
+      for (int idx = 0; idx < pre && ok; ++idx) load_kv(idx);
       if (!ok) break;
-      ATTN_TRACE_EV(tc, 2, idx);  // slot free, issuing the load
-      const uint32_t full = smem_u32(&bar_kv_full[slot]);
-      const uint32_t dst = sRing + slot * C::KV_BYTES;
-      const CUtensorMap* m = (idx & 1) ? &tm_v : &tm_k;
-      mbar_arrive_expect_tx_el(full, C::KV_BYTES);
-      for (int c = 0; c < C::KCH; ++c)
-        tma_load_4d_hint_el(dst + c * (C::BK * 128), m, full, c * 64, g, (jb + (idx >> 1)) * C::BK,
-                            b, keep);
-      issued = idx + 1;
+      if (r > 0) ok = mbar_wait_warp(smem_u32(&bar_q_empty), (r - 1) & 1, ctl);
+      if (!ok) break;
+      mbar_arrive_expect_tx_el(smem_u32(&bar_q_full), 2 * C::Q_BYTES);
+      for (int t = 0; t < 2; ++t)
+        for (int c = 0; c < C::KCH; ++c)
+          tma_load_4d_el(sQ + t * C::Q_BYTES + c * (C::BQ * 128), &tm_q, smem_u32(&bar_q_full),
+                         c * 64, it.hq, it.q0 + t * C::BQ, it.b);
+      ++q_loads;
+      for (int idx = pre; idx < n_pos && ok; ++idx) load_kv(idx);
     }
     if (lane == 0) {
       // Let every copy issued land before the CTA's shared memory goes away
       // (immediate in a normal run, where the MMA warp consumed them all).
-      for (int idx = max(0, issued - C::NSLOT); idx < issued; ++idx)
-        mbar_wait_drain(smem_u32(&bar_kv_full[idx % C::NSLOT]), (idx / C::NSLOT) & 1,
-                        50000000ull);
+      for (int pos = max(0, issued - C::NSLOT); pos < issued; ++pos)
+        mbar_wait_drain(smem_u32(&bar_kv_full[pos % C::NSLOT]), (pos / C::NSLOT) & 1, 50000000ull);
+      if (q_loads > 0) mbar_wait_drain(smem_u32(&bar_q_full), (q_loads - 1) & 1, 50000000ull);
     }
     (void)ok;
     __syncwarp();
@@ -183,16 +227,27 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     // each MMA and commit is issued by one elected lane.
     TraceCursor tc;
     if (lane == 0) ATTN_TRACE_INIT(tc, 1);
-    bool ok = !p.inject_stall && mbar_wait_warp(smem_u32(&bar_q_full), 0, ctl);
-    if (ok) {
-      ATTN_TRACE_EV(tc, 1, 0);
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
-      constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, 0, 1);
-      const uint64_t dq_desc = sw128_desc(sQ, 16, 1024);
-      // Ring position of K_j is 2 (j - jb), of V_j the one after it.
+    bool ok = !p.inject_stall;
+    constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
+    constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, 0, 1);
+    const uint64_t dq_desc = sw128_desc(sQ, 16, 1024);
+    int ring = 0;                // ring position of the item's first K/V tile
+    int p_cnt[2] = {0, 0};       // P tiles consumed per query tile, over all items
+    for (int r = 0; ok; ++r) {
+      const int ii = fwd_item_index(r, cta, n_cta, n_items);
+      if (ii < 0) break;
+      const FwdItem it = fwd_item<WIN>(p, ii);
+      const int jb = jlo(it, 0);
+      const int n_kv = it.n_kv[1];  // tile B ends last; tile A starts first
+      ok = mbar_wait_warp(smem_u32(&bar_q_full), r & 1, ctl);
+      if (!ok) break;
+      ATTN_TRACE_EV(tc, 1, r);
+      // S products left in this item; the last one hands the Q buffer back.
+      int s_left = (it.n_kv[0] - jlo(it, 0)) + (it.n_kv[1] - jlo(it, 1));
+      // Ring position of K_j is ring + 2 (j - jb), of V_j the one after it.
       // S_t = Q_t K_j^T into tile t's score buffer.
       auto issue_s = [&](int t, int j) {
-        const int slot = (2 * (j - jb)) % C::NSLOT;
+        const int slot = (ring + 2 * (j - jb)) % C::NSLOT;
         const uint64_t dk = sw128_desc(sRing + slot * C::KV_BYTES, 16, 1024);
         const uint64_t dq = dq_desc + ((t * C::Q_BYTES) >> 4);
 #pragma unroll
@@ -201,24 +256,27 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           mma_ss_el(tmem + C::tm_s(t), dq + koff, dk + koff, idesc_s, kk > 0);
         }
         mma_commit_el(smem_u32(&bar_s_full[t]));
+        if (--s_left == 0) mma_commit_el(smem_u32(&bar_q_empty));
       };
       auto wait_kv = [&](int idx) {
-        return mbar_wait_warp(smem_u32(&bar_kv_full[idx % C::NSLOT]), (idx / C::NSLOT) & 1, ctl);
+        const int pos = ring + idx;
+        return mbar_wait_warp(smem_u32(&bar_kv_full[pos % C::NSLOT]), (pos / C::NSLOT) & 1, ctl);
       };
+      auto kv_slot = [&](int idx) { return (ring + idx) % C::NSLOT; };
       ok = wait_kv(0);
-      if (ok) {
-        tc_fence_after();
-        issue_s(0, jb);
-        if (jlo(1) == jb) issue_s(1, jb);
-        mma_commit_el(smem_u32(&bar_kv_empty[0]));  // K_jb is done once its S products ran
-        ATTN_TRACE_EV(tc, 3, 0);
-      }
+      if (!ok) break;
+      tc_fence_after();
+      issue_s(0, jb);
+      if (jlo(it, 1) == jb) issue_s(1, jb);
+      mma_commit_el(smem_u32(&bar_kv_empty[kv_slot(0)]));  // K_jb is done once its S products ran
+      ATTN_TRACE_EV(tc, 3, r);
       for (int j = jb; j < n_kv && ok; ++j) {
         bool v_ready = false, k_next_ready = false;
         for (int t = 0; t < 2 && ok; ++t) {
-          if (j >= jlo(t) && j < n_kv_t[t]) {
-            ok = mbar_wait_warp(smem_u32(&bar_p_full[t]), (j - jlo(t)) & 1, ctl);
+          if (j >= jlo(it, t) && j < it.n_kv[t]) {
+            ok = mbar_wait_warp(smem_u32(&bar_p_full[t]), p_cnt[t] & 1, ctl);
             if (!ok) break;
+            ++p_cnt[t];
             ATTN_TRACE_EV(tc, 4 + t, j);  // P_t(j) ready seen
             if (!v_ready) {
               ok = wait_kv(2 * (j - jb) + 1);
@@ -226,7 +284,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
               v_ready = true;
             }
             tc_fence_after();
-            const int vslot = (2 * (j - jb) + 1) % C::NSLOT;
+            const int vslot = kv_slot(2 * (j - jb) + 1);
             const uint64_t dv = sw128_desc(sRing + vslot * C::KV_BYTES, C::BK * 128, 1024);
             // Keys 16kk..16kk+15: P hi in score columns 16kk..16kk+7, P lo in
             // 16kk+8..16kk+15.
@@ -234,19 +292,19 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
 #pragma unroll
             for (int kk = 0; kk < C::BK / 16; ++kk)
               mma_ts_el(tmem + C::tm_o(t), a_p + kk * 16, dv + ((kk * 2048) >> 4), idesc_o,
-                        (j > jlo(t) || kk > 0) ? 1u : 0u);
+                        (j > jlo(it, t) || kk > 0) ? 1u : 0u);
             if constexpr (SPLIT) {
 #pragma unroll
               for (int kk = 0; kk < C::BK / 16; ++kk)
                 mma_ts_el(tmem + C::tm_o(t), a_p + kk * 16 + 8, dv + ((kk * 2048) >> 4), idesc_o,
                           1u);
             }
-            if (j + 1 == n_kv_t[t]) mma_commit_el(smem_u32(&bar_pv_done[t]));
+            if (j + 1 == it.n_kv[t]) mma_commit_el(smem_u32(&bar_pv_done[t]));
             ATTN_TRACE_EV(tc, 6 + t, j);  // PV_t(j) issued
           }
           // The next score tile of t overwrites P_t(j) in TMEM; MMAs execute in
           // issue order, so it runs after PV_t(j) has read P_t(j).
-          if (j + 1 < n_kv_t[t] && j + 1 >= jlo(t)) {
+          if (j + 1 < it.n_kv[t] && j + 1 >= jlo(it, t)) {
             if (!k_next_ready) {
               ok = wait_kv(2 * (j - jb) + 2);
               if (!ok) break;
@@ -269,176 +327,185 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           }
           if (!ok) break;
         }
-        mma_commit_el(smem_u32(&bar_kv_empty[(2 * (j - jb) + 1) % C::NSLOT]));
-        if (k_next_ready) mma_commit_el(smem_u32(&bar_kv_empty[(2 * (j - jb) + 2) % C::NSLOT]));
+        mma_commit_el(smem_u32(&bar_kv_empty[kv_slot(2 * (j - jb) + 1)]));
+        if (k_next_ready) mma_commit_el(smem_u32(&bar_kv_empty[kv_slot(2 * (j - jb) + 2)]));
       }
-      // Wait for every MMA issued to finish before TMEM is released (in a
-      // normal run the epilogue has already waited for them). bar_q_full has
-      // completed its only phase, so this commit completes phase 1.
-      mma_commit_el(smem_u32(&bar_q_full));
-      mbar_wait_drain(smem_u32(&bar_q_full), 1, 50000000ull);
-    } else {
-      mbar_wait_drain(smem_u32(&bar_q_full), 0, 50000000ull);  // let the Q copy land
+      ring += 2 * (n_kv - jb);
     }
+    // Every MMA issued finishes before TMEM is released (in a normal run the
+    // epilogues have already waited for them).
+    mma_commit_el(smem_u32(&bar_mma_done));
+    mbar_wait_drain(smem_u32(&bar_mma_done), 0, 50000000ull);
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax warps 0-7
     const int t = warp / 4;           // query tile of this warpgroup
     const int r = threadIdx.x % 128;  // query row within the tile == TMEM lane
-    const int qrow = q0 + t * C::BQ + r;
-    const int my_kv = n_kv_t[t];
     const uint32_t lane_base = static_cast<uint32_t>((warp % 4) * 32) << 16;
     const uint32_t ts = tmem + lane_base + C::tm_s(t);
-    float m = -INFINITY;  // running max in log2 units (scaled scores)
-    float l = 0.f;
     const float sl2 = p.scale_log2;
     const bool pos = sl2 >= 0.f;
     TraceCursor tc;
     if (lane == 0 && (warp == 0 || warp == 4)) ATTN_TRACE_INIT(tc, 2 + t);
     bool ok = true;
-    for (int j = jlo(t); j < my_kv; ++j) {
-      ATTN_TRACE_EV(tc, 1, j);  // start waiting for S_t(j)
-      // S_t(j) landed; its commit also covers PV_t(j-1), so O_t is current.
-      ok = mbar_wait_warp(smem_u32(&bar_s_full[t]), (j - jlo(t)) & 1, ctl);
-      if (!ok) break;
-      ATTN_TRACE_EV(tc, 2, j);  // S_t(j) landed
-      tc_fence_after();
-      // Raw scores of this row; the scale is folded into the exponent below.
-      float x[C::BK];
-      {
-        uint32_t u[C::BK];
+    int s_cnt = 0;  // score tiles of this query tile, over all items
+    for (int item = 0; ok; ++item) {
+      const int ii = fwd_item_index(item, cta, n_cta, n_items);
+      if (ii < 0) break;
+      const FwdItem it = fwd_item<WIN>(p, ii);
+      const int q0 = it.q0, b = it.b, hq = it.hq;
+      const int qrow = q0 + t * C::BQ + r;
+      const int my_kv = it.n_kv[t];
+      float m = -INFINITY;  // running max in log2 units (scaled scores)
+      float l = 0.f;
+      for (int j = jlo(it, t); j < my_kv; ++j) {
+        ATTN_TRACE_EV(tc, 1, j);  // start waiting for S_t(j)
+        // S_t(j) landed; its commit also covers PV_t(j-1), so O_t is current.
+        ok = mbar_wait_warp(smem_u32(&bar_s_full[t]), s_cnt & 1, ctl);
+        if (!ok) break;
+        ++s_cnt;
+        ATTN_TRACE_EV(tc, 2, j);  // S_t(j) landed
+        tc_fence_after();
+        // Raw scores of this row; the scale is folded into the exponent below.
+        float x[C::BK];
+        {
+          uint32_t u[C::BK];
 #pragma unroll
-        for (int c = 0; c < C::BK; c += 32)
-          tmem_ld32(ts + c, *reinterpret_cast<uint32_t(*)[32]>(&u[c]));
-        tmem_wait_ld();
+          for (int c = 0; c < C::BK; c += 32)
+            tmem_ld32(ts + c, *reinterpret_cast<uint32_t(*)[32]>(&u[c]));
+          tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < C::BK; ++c) x[c] = __uint_as_float(u[c]);
-      }
-      const int k0 = j * C::BK;
-      const int qt0 = q0 + t * C::BQ;
-      // Tiles that cross the causal diagonal, hold keys past S, or hold keys
-      // below some row's window mask; the rest skip masking.
-      const bool need_mask = (p.causal && k0 + C::BK - 1 > qt0) || (k0 + C::BK > p.S) ||
-                             (WIN && k0 < qt0 + C::BQ - p.window);
-      // Visible columns of this tile for this row: c_lo <= c <= c_hi.
-      const int c_hi = (p.causal ? min(qrow, p.S - 1) : (p.S - 1)) - k0;
-      const int c_lo = WIN ? qrow - p.window + 1 - k0 : 0;
-      float alpha = 1.f;
-      bool rescale = false;
-      // One tile of the online softmax: row max, exponentials, row sum and P
-      // (hi, and with SPLIT lo) into TMEM over the scores, 16 columns at a
-      // time; this thread has read all its scores already. Instantiated once
-      // for tiles that mask (the causal diagonal, keys past S) and once for
-      // tiles that do not.
-      {
-        const bool MASKED = need_mask;
-        // Largest scaled score: the max of the raw scores for scale >= 0, the
-        // min for scale < 0 (masked keys pushed to the losing end).
-        if (MASKED) {
-          const float lose = pos ? -INFINITY : INFINITY;
-#pragma unroll
-          for (int c = 0; c < C::BK; ++c)
-            if (c > c_hi || (WIN && c < c_lo)) x[c] = lose;
+          for (int c = 0; c < C::BK; ++c) x[c] = __uint_as_float(u[c]);
         }
-        static_assert(C::BK == 128, "row_extreme128 covers one 128-key tile");
-        const float mraw = pos ? row_extreme128<true>(x) : row_extreme128<false>(x);
-        const float mx = mraw * sl2;
-        rescale = mx > m + kRescaleThreshold;
-        if (rescale) {
-          alpha = ex2(m - mx);  // m = -inf on the first tile gives 0
-          m = mx;
-        }
-        const uint64_t sl2x2 = f32x2(sl2, sl2);
-        // A row whose keys in this tile are all outside its window keeps
-        // m = -inf; an offset of 0 then gives its masked scores p = 0.
-        const float neg_m = (WIN && m == -INFINITY) ? 0.f : -m;
-        const uint64_t negm2 = f32x2(neg_m, neg_m);
-        uint64_t sums[4];
+        const int k0 = j * C::BK;
+        const int qt0 = q0 + t * C::BQ;
+        // Tiles that cross the causal diagonal, hold keys past S, or hold keys
+        // below some row's window mask; the rest skip masking.
+        const bool need_mask = (p.causal && k0 + C::BK - 1 > qt0) || (k0 + C::BK > p.S) ||
+                               (WIN && k0 < qt0 + C::BQ - p.window);
+        // Visible columns of this tile for this row: c_lo <= c <= c_hi.
+        const int c_hi = (p.causal ? min(qrow, p.S - 1) : (p.S - 1)) - k0;
+        const int c_lo = WIN ? qrow - p.window + 1 - k0 : 0;
+        float alpha = 1.f;
+        bool rescale = false;
+        // One tile of the online softmax: row max, exponentials, row sum and P
+        // (hi, and with SPLIT lo) into TMEM over the scores, 16 columns at a
+        // time; this thread has read all its scores already. Instantiated once
+        // for tiles that mask (the causal diagonal, keys past S) and once for
+        // tiles that do not.
+        {
+          const bool MASKED = need_mask;
+          // Largest scaled score: the max of the raw scores for scale >= 0, the
+          // min for scale < 0 (masked keys pushed to the losing end).
+          if (MASKED) {
+            const float lose = pos ? -INFINITY : INFINITY;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) sums[i] = f32x2(0.f, 0.f);
-#pragma unroll
-        for (int ch = 0; ch < C::BK; ch += 16) {
-          uint32_t pkl[16];  // P hi pairs, then (with SPLIT) P lo pairs
-#pragma unroll
-          for (int c = 0; c < 16; c += 2) {
-            float e0, e1;
-            unpack_f32x2(fma_f32x2(f32x2(x[ch + c], x[ch + c + 1]), sl2x2, negm2), e0, e1);
-            // A masked score is -inf (or +inf with a negative scale): its
-            // exponent is -inf and its probability 0 (the scale is never 0).
-            const float p0 = ex2(e0), p1 = ex2(e1);
-            sums[(c / 2) & 3] = add_f32x2(sums[(c / 2) & 3], f32x2(p0, p1));
-            if constexpr (SPLIT) {
-              split_bf16x2(p0, p1, pkl[c / 2], pkl[8 + c / 2]);
-            } else {
-              pkl[c / 2] = pack_bf16x2(p0, p1);
-            }
+            for (int c = 0; c < C::BK; ++c)
+              if (c > c_hi || (WIN && c < c_lo)) x[c] = lose;
           }
-          // Columns ch..ch+15 of the scores (already read) take these keys' P.
-          if constexpr (SPLIT)
-            tmem_st16(ts + ch, pkl);
-          else
-            tmem_st8(ts + ch, *reinterpret_cast<uint32_t(*)[8]>(&pkl[0]));
+          static_assert(C::BK == 128, "row_extreme128 covers one 128-key tile");
+          const float mraw = pos ? row_extreme128<true>(x) : row_extreme128<false>(x);
+          const float mx = mraw * sl2;
+          rescale = mx > m + kRescaleThreshold;
+          if (rescale) {
+            alpha = ex2(m - mx);  // m = -inf on the first tile gives 0
+            m = mx;
+          }
+          const uint64_t sl2x2 = f32x2(sl2, sl2);
+          // A row whose keys in this tile are all outside its window keeps
+          // m = -inf; an offset of 0 then gives its masked scores p = 0.
+          const float neg_m = (WIN && m == -INFINITY) ? 0.f : -m;
+          const uint64_t negm2 = f32x2(neg_m, neg_m);
+          uint64_t sums[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) sums[i] = f32x2(0.f, 0.f);
+#pragma unroll
+          for (int ch = 0; ch < C::BK; ch += 16) {
+            uint32_t pkl[16];  // P hi pairs, then (with SPLIT) P lo pairs
+#pragma unroll
+            for (int c = 0; c < 16; c += 2) {
+              float e0, e1;
+              unpack_f32x2(fma_f32x2(f32x2(x[ch + c], x[ch + c + 1]), sl2x2, negm2), e0, e1);
+              // A masked score is -inf (or +inf with a negative scale): its
+              // exponent is -inf and its probability 0 (the scale is never 0).
+              const float p0 = ex2(e0), p1 = ex2(e1);
+              sums[(c / 2) & 3] = add_f32x2(sums[(c / 2) & 3], f32x2(p0, p1));
+              if constexpr (SPLIT) {
+                split_bf16x2(p0, p1, pkl[c / 2], pkl[8 + c / 2]);
+              } else {
+                pkl[c / 2] = pack_bf16x2(p0, p1);
+              }
+            }
+            // Columns ch..ch+15 of the scores (already read) take these keys' P.
+            if constexpr (SPLIT)
+              tmem_st16(ts + ch, pkl);
+            else
+              tmem_st8(ts + ch, *reinterpret_cast<uint32_t(*)[8]>(&pkl[0]));
+          }
+          float s0, s1;
+          unpack_f32x2(add_f32x2(add_f32x2(sums[0], sums[1]), add_f32x2(sums[2], sums[3])), s0, s1);
+          l = l * alpha + (s0 + s1);
         }
-        float s0, s1;
-        unpack_f32x2(add_f32x2(add_f32x2(sums[0], sums[1]), add_f32x2(sums[2], sums[3])), s0, s1);
-        l = l * alpha + (s0 + s1);
+        ATTN_TRACE_EV(tc, 3, j);  // exponentials done
+        // Rescale this warp's O rows (PV_t(j-1) has completed, see above).
+        if (j > jlo(it, t) && __any_sync(0xffffffffu, rescale)) {
+          const uint32_t to = tmem + lane_base + C::tm_o(t);
+#pragma unroll
+          for (int c = 0; c < D; c += 32) {
+            uint32_t u[32];
+            tmem_ld32(to + c, u);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
+            tmem_st32(to + c, u);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bar_p_full[t]));
+        ATTN_TRACE_EV(tc, 4, j);  // P_t(j) stored and signalled
       }
-      ATTN_TRACE_EV(tc, 3, j);  // exponentials done
-      // Rescale this warp's O rows (PV_t(j-1) has completed, see above).
-      if (j > jlo(t) && __any_sync(0xffffffffu, rescale)) {
+      // The item's last P.V product of this tile has run: O_t is final. (Its
+      // TMEM columns are free again once this epilogue has read them, which
+      // is before this warpgroup signals the next item's first P.)
+      if (ok) ok = mbar_wait_warp(smem_u32(&bar_pv_done[t]), item & 1, ctl);
+      if (ok) {
+        tc_fence_after();
+        const float inv_l = 1.f / l;
+        const bool valid = qrow < p.S;
+        const size_t rowoff = ((static_cast<size_t>(b) * p.S + qrow) * p.Hq + hq) * D;
         const uint32_t to = tmem + lane_base + C::tm_o(t);
 #pragma unroll
         for (int c = 0; c < D; c += 32) {
           uint32_t u[32];
           tmem_ld32(to + c, u);
           tmem_wait_ld();
+          uint4 w[4], wl[4];
+          uint32_t* wp = reinterpret_cast<uint32_t*>(w);
+          uint32_t* wlp = reinterpret_cast<uint32_t*>(wl);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
-          tmem_st32(to + c, u);
-        }
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(smem_u32(&bar_p_full[t]));
-      ATTN_TRACE_EV(tc, 4, j);  // P_t(j) stored and signalled
-    }
-    if (ok && my_kv > 0) ok = mbar_wait_warp(smem_u32(&bar_pv_done[t]), 0, ctl);
-    if (ok) {
-      tc_fence_after();
-      const float inv_l = 1.f / l;
-      const bool valid = qrow < p.S;
-      const size_t rowoff = ((static_cast<size_t>(b) * p.S + qrow) * p.Hq + hq) * D;
-      const uint32_t to = tmem + lane_base + C::tm_o(t);
+          for (int i = 0; i < 16; ++i) {
+            const float x0 = __uint_as_float(u[2 * i]) * inv_l;
+            const float x1 = __uint_as_float(u[2 * i + 1]) * inv_l;
+            wp[i] = pack_bf16x2(x0, x1);
+            // what bf16 rounding dropped, itself rounded to bf16
+            wlp[i] = pack_bf16x2(x0 - __uint_as_float(wp[i] << 16),
+                                 x1 - __uint_as_float(wp[i] & 0xFFFF0000u));
+          }
+          if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(p.o + rowoff + c);
 #pragma unroll
-      for (int c = 0; c < D; c += 32) {
-        uint32_t u[32];
-        tmem_ld32(to + c, u);
-        tmem_wait_ld();
-        uint4 w[4], wl[4];
-        uint32_t* wp = reinterpret_cast<uint32_t*>(w);
-        uint32_t* wlp = reinterpret_cast<uint32_t*>(wl);
+            for (int i = 0; i < 4; ++i) dst[i] = w[i];
+            if (SPLIT) {
+              uint4* dl = reinterpret_cast<uint4*>(p.o_lo + rowoff + c);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float x0 = __uint_as_float(u[2 * i]) * inv_l;
-          const float x1 = __uint_as_float(u[2 * i + 1]) * inv_l;
-          wp[i] = pack_bf16x2(x0, x1);
-          // what bf16 rounding dropped, itself rounded to bf16
-          wlp[i] = pack_bf16x2(x0 - __uint_as_float(wp[i] << 16),
-                               x1 - __uint_as_float(wp[i] & 0xFFFF0000u));
-        }
-        if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(p.o + rowoff + c);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) dst[i] = w[i];
-          if (SPLIT) {
-            uint4* dl = reinterpret_cast<uint4*>(p.o_lo + rowoff + c);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) dl[i] = wl[i];
+              for (int i = 0; i < 4; ++i) dl[i] = wl[i];
+            }
           }
         }
+        if (valid)
+          p.lse[(static_cast<size_t>(b) * p.Hq + hq) * p.S + qrow] = (m + __log2f(l)) * kLn2;
       }
-      if (valid)
-        p.lse[(static_cast<size_t>(b) * p.Hq + hq) * p.S + qrow] = (m + __log2f(l)) * kLn2;
     }
   }
 
@@ -461,7 +528,14 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  dim3 grid(p.B * p.Hq, p.n_qblocks);
+  // Persistent: one CTA per SM (or per item, if fewer), each looping over its
+  // items.
+  static int sm_count[64] = {};
+  if (dev < 64 && sm_count[dev] == 0)
+    cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
+  const long long n_items = static_cast<long long>(p.B) * p.Hq * p.n_qblocks;
+  const int sms = (dev < 64 && sm_count[dev] > 0) ? sm_count[dev] : 148;
+  const dim3 grid(static_cast<unsigned>(n_items < sms ? n_items : sms));
   attn_fwd_kernel<D, SPLIT, WIN><<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }

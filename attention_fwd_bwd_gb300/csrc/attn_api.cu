@@ -193,10 +193,12 @@ static attn_status_t fwd_impl(const void* q, const void* k, const void* v, void*
       !aligned16(o_lo))
     return ATTN_ERR_INVALID_ARG;
   if ((st = check_device()) != ATTN_OK) return st;
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to, tolo;
   if (!make_bshd_map(&tq, q, B, S, Hq, D, FwdCfg<128>::BQ) ||
       !make_bshd_map(&tk, k, B, S, Hkv, D, FwdCfg<128>::BK) ||
-      !make_bshd_map(&tv, v, B, S, Hkv, D, FwdCfg<128>::BK))
+      !make_bshd_map(&tv, v, B, S, Hkv, D, FwdCfg<128>::BK) ||
+      !make_bshd_map(&to, o, B, S, Hq, D, FwdCfg<128>::BQ) ||
+      !make_bshd_map(&tolo, o_lo ? o_lo : o, B, S, Hq, D, FwdCfg<128>::BQ))
     return ATTN_ERR_CUDA;
   int* status = fwd_status_ptr();
   if (!status) return ATTN_ERR_CUDA;
@@ -222,7 +224,7 @@ static attn_status_t fwd_impl(const void* q, const void* k, const void* v, void*
   p.timeout_ns = g_timeout_ns;
   p.inject_stall = g_inject_stall & 1;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  return finish(launch_fwd(D, tq, tk, tv, p, s), s, status);
+  return finish(launch_fwd(D, tq, tk, tv, to, tolo, p, s), s, status);
 }
 
 attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,

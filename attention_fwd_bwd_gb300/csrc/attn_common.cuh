@@ -33,7 +33,11 @@ struct FwdCfg {
   static constexpr int NSLOT = (D == 128) ? 4 : 8;   // ring slots
   static constexpr int SMEM_Q = 0;
   static constexpr int SMEM_RING = 2 * Q_BYTES;
-  static constexpr int SMEM_BYTES = 2 * Q_BYTES + NSLOT * KV_BYTES;
+  // Output staging, one 128-row x 64-column bf16 tile (128-byte swizzle) per
+  // query tile: the epilogue writes O (and o_lo) through it with TMA stores.
+  static constexpr int STG_BYTES = BQ * 64 * 2;
+  static constexpr int SMEM_STG = SMEM_RING + NSLOT * KV_BYTES;
+  static constexpr int SMEM_BYTES = SMEM_STG + 2 * STG_BYTES;
   static constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;  // slack for 1024-byte alignment
   // Tensor-memory columns per query tile t: scores S_t (128 fp32 columns,
   // later overwritten by P_t: for keys 16k..16k+15, bf16 hi pairs in columns
@@ -189,7 +193,8 @@ struct TraceCursor {};
 
 // ---------------------------------------------------------------- launchers
 cudaError_t launch_fwd(int D, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const FwdParams& p, cudaStream_t stream);
+                       const CUtensorMap& to, const CUtensorMap& tolo, const FwdParams& p,
+                       cudaStream_t stream);
 cudaError_t launch_bwd_preprocess(const __nv_bfloat16* o, const __nv_bfloat16* o_lo,
                                   const __nv_bfloat16* dO, const float* lse, float* nlse2,
                                   float* dvec, float* dq, int* status, int B, int Hq, int S,

@@ -113,7 +113,9 @@ template <int D, bool SPLIT, bool WIN>
 __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+                    const __grid_constant__ CUtensorMap tm_v,
+                    const __grid_constant__ CUtensorMap tm_o,
+                    const __grid_constant__ CUtensorMap tm_olo, const FwdParams p) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -159,6 +161,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
 
   const uint32_t sQ = smem_u32(smem + C::SMEM_Q);  // tile t at sQ + t * Q_BYTES
   const uint32_t sRing = smem_u32(smem + C::SMEM_RING);
+  const uint32_t sStg = smem_u32(smem + C::SMEM_STG);  // tile t at sStg + t * STG_BYTES
 
   if (warp == 8) {
     // ------------------------------------------------------------ producer
@@ -469,46 +472,67 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       // TMEM columns are free again once this epilogue has read them, which
       // is before this warpgroup signals the next item's first P.)
       if (ok) ok = mbar_wait_warp(smem_u32(&bar_pv_done[t]), item & 1, ctl);
+      // The tile's four warps meet at named barriers in the epilogue: agree
+      // first on going on.
+      ok = named_bar_and(1 + t, 128, ok);
       if (ok) {
         tc_fence_after();
+        // O = acc / l (and o_lo, what bf16 rounding of O dropped, itself in
+        // bf16) leave 64 columns at a time through this tile's staging buffer
+        // and a TMA store; rows past S are clipped by the store.
         const float inv_l = 1.f / l;
-        const bool valid = qrow < p.S;
-        const size_t rowoff = ((static_cast<size_t>(b) * p.S + qrow) * p.Hq + hq) * D;
         const uint32_t to = tmem + lane_base + C::tm_o(t);
+        const uint32_t stg = sStg + t * C::STG_BYTES;
+        const uint32_t bar_id = 1 + t;  // named barrier of this tile's 128 threads
+        const bool leader = (r == 0);
 #pragma unroll
-        for (int c = 0; c < D; c += 32) {
-          uint32_t u[32];
-          tmem_ld32(to + c, u);
-          tmem_wait_ld();
-          uint4 w[4], wl[4];
-          uint32_t* wp = reinterpret_cast<uint32_t*>(w);
-          uint32_t* wlp = reinterpret_cast<uint32_t*>(wl);
+        for (int c = 0; c < D; c += 64) {
+          uint32_t hi[32], lo[32];  // bf16 pairs of this row's 64 columns
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float x0 = __uint_as_float(u[2 * i]) * inv_l;
-            const float x1 = __uint_as_float(u[2 * i + 1]) * inv_l;
-            wp[i] = pack_bf16x2(x0, x1);
-            // what bf16 rounding dropped, itself rounded to bf16
-            wlp[i] = pack_bf16x2(x0 - __uint_as_float(wp[i] << 16),
-                                 x1 - __uint_as_float(wp[i] & 0xFFFF0000u));
+          for (int h = 0; h < 2; ++h) {
+            uint32_t u[32];
+            tmem_ld32(to + c + 32 * h, u);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float x0 = __uint_as_float(u[2 * i]) * inv_l;
+              const float x1 = __uint_as_float(u[2 * i + 1]) * inv_l;
+              const uint32_t w = pack_bf16x2(x0, x1);
+              hi[16 * h + i] = w;
+              lo[16 * h + i] = pack_bf16x2(x0 - __uint_as_float(w << 16),
+                                           x1 - __uint_as_float(w & 0xFFFF0000u));
+            }
           }
-          if (valid) {
-            uint4* dst = reinterpret_cast<uint4*>(p.o + rowoff + c);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) dst[i] = w[i];
-            if (SPLIT) {
-              uint4* dl = reinterpret_cast<uint4*>(p.o_lo + rowoff + c);
+          for (int part = 0; part < (SPLIT ? 2 : 1); ++part) {
+            const uint32_t* v = part ? lo : hi;
+            // The previous store from this buffer has read it.
+            if (leader) bulk_wait_read_all();
+            named_bar_sync(bar_id, 128);
+            // Row r: 128 bytes, 16-byte unit u at (u ^ (r % 8)) (128-byte swizzle).
 #pragma unroll
-              for (int i = 0; i < 4; ++i) dl[i] = wl[i];
+            for (int u8 = 0; u8 < 8; ++u8) {
+              const uint32_t addr = stg + r * 128 + ((u8 ^ (r & 7)) << 4);
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v[4 * u8]),
+                           "r"(v[4 * u8 + 1]), "r"(v[4 * u8 + 2]), "r"(v[4 * u8 + 3])
+                           : "memory");
+            }
+            fence_async_smem();
+            named_bar_sync(bar_id, 128);
+            if (leader) {
+              tma_store_4d(part ? &tm_olo : &tm_o, c, hq, q0 + t * C::BQ, b, stg);
+              bulk_commit_group();
             }
           }
         }
-        if (valid)
+        if (qrow < p.S)
           p.lse[(static_cast<size_t>(b) * p.Hq + hq) * p.S + qrow] = (m + __log2f(l)) * kLn2;
       }
     }
   }
 
+  // The epilogue's TMA stores finish before the CTA (and its staging buffers) go away.
+  if (warp < 8 && threadIdx.x % 128 == 0) bulk_wait_all();
   tc_fence_before();
   __syncthreads();
   if (warp == 9) tmem_dealloc(tmem, C::TMEM_COLS);
@@ -516,7 +540,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
 
 template <int D, bool SPLIT, bool WIN>
 cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                         const FwdParams& p, cudaStream_t stream) {
+                         const CUtensorMap& to, const CUtensorMap& tolo, const FwdParams& p,
+                         cudaStream_t stream) {
   using C = FwdCfg<D>;
   static bool attr_set[64] = {};
   int dev = 0;
@@ -536,27 +561,29 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   const long long n_items = static_cast<long long>(p.B) * p.Hq * p.n_qblocks;
   const int sms = (dev < 64 && sm_count[dev] > 0) ? sm_count[dev] : 148;
   const dim3 grid(static_cast<unsigned>(n_items < sms ? n_items : sms));
-  attn_fwd_kernel<D, SPLIT, WIN><<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(tq, tk, tv, p);
+  attn_fwd_kernel<D, SPLIT, WIN><<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(tq, tk, tv, to, tolo,
+                                                                                 p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_fwd(int D, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const FwdParams& p, cudaStream_t stream) {
+                       const CUtensorMap& to, const CUtensorMap& tolo, const FwdParams& p,
+                       cudaStream_t stream) {
   const bool split = p.o_lo != nullptr, win = p.window > 0;
   if (D == 128) {
     if (win)
-      return split ? launch_fwd_t<128, true, true>(tq, tk, tv, p, stream)
-                   : launch_fwd_t<128, false, true>(tq, tk, tv, p, stream);
-    return split ? launch_fwd_t<128, true, false>(tq, tk, tv, p, stream)
-                 : launch_fwd_t<128, false, false>(tq, tk, tv, p, stream);
+      return split ? launch_fwd_t<128, true, true>(tq, tk, tv, to, tolo, p, stream)
+                   : launch_fwd_t<128, false, true>(tq, tk, tv, to, tolo, p, stream);
+    return split ? launch_fwd_t<128, true, false>(tq, tk, tv, to, tolo, p, stream)
+                 : launch_fwd_t<128, false, false>(tq, tk, tv, to, tolo, p, stream);
   }
   if (win)
-    return split ? launch_fwd_t<64, true, true>(tq, tk, tv, p, stream)
-                 : launch_fwd_t<64, false, true>(tq, tk, tv, p, stream);
-  return split ? launch_fwd_t<64, true, false>(tq, tk, tv, p, stream)
-               : launch_fwd_t<64, false, false>(tq, tk, tv, p, stream);
+    return split ? launch_fwd_t<64, true, true>(tq, tk, tv, to, tolo, p, stream)
+                 : launch_fwd_t<64, false, true>(tq, tk, tv, to, tolo, p, stream);
+  return split ? launch_fwd_t<64, true, false>(tq, tk, tv, to, tolo, p, stream)
+               : launch_fwd_t<64, false, false>(tq, tk, tv, to, tolo, p, stream);
 }
 
 }  // namespace attn

@@ -421,16 +421,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       else
         p_ds(BoolConst<false>{});
       ATTN_TRACE_EV(tc, 3, it);  // P, dS computed
-      // The MMAs of the previous tile must be done with dS (smem), and the
-      // drain must have read dQ^T(it-1), whose TMEM columns P^T now takes.
+      // dS^T goes to shared memory once the MMAs of the previous tile are done
+      // with it (dQ^T(it-1) is its last reader), and P^T, dS^T to TMEM once
+      // the drain has read dQ^T(it-1), whose columns they take; the drain's
+      // read overlaps the shared-memory stores.
       if (it >= 1) {
         ok = mbar_wait_warp(smem_u32(&bar_pds_free), (it - 1) & 1, ctl);
-        if (ok) ok = mbar_wait_warp(smem_u32(&bar_dq_free), (it - 1) & 1, ctl);
         if (!ok) break;
       }
-      ATTN_TRACE_EV(tc, 4, it);  // previous MMAs done
-      tmem_st32(tmem + lane_base + C::TM_P + cg * HALF, pp);
-      tmem_st32(tmem + lane_base + C::TM_DS + cg * HALF, dd);
       // Row r of dS^T, K-major with 128-byte swizzle: 64 query columns per
       // 128-byte row, 8 per 16-byte unit; this half owns units cg*4..cg*4+3.
 #pragma unroll
@@ -441,6 +439,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         st_sw128(sDsHi, r, unit, make_uint4(h[0], h[1], h[2], h[3]));
         st_sw128(sDsLo, r, unit, make_uint4(lo[0], lo[1], lo[2], lo[3]));
       }
+      if (it >= 1) {
+        ok = mbar_wait_warp(smem_u32(&bar_dq_free), (it - 1) & 1, ctl);
+        if (!ok) break;
+      }
+      ATTN_TRACE_EV(tc, 4, it);  // previous MMAs done
+      tc_fence_after();
+      tmem_st32(tmem + lane_base + C::TM_P + cg * HALF, pp);
+      tmem_st32(tmem + lane_base + C::TM_DS + cg * HALF, dd);
       tmem_wait_st();
       fence_async_smem();
       tc_fence_before();

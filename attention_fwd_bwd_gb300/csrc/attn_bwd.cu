@@ -19,8 +19,10 @@
 //        P^T (TMEM) and scale * dS^T (shared memory) as bf16 hi/lo pairs
 //        dV += P^T dO_i, dK += dS^T Q_i                 (TMEM, whole loop)
 //        dQ_i^T = K_j^T dS^T                            (TMEM)
-//      The dQ tile is drained by warps 8-11 into shared memory and added into
-//      dq with an asynchronous TMA tensor reduction (fp32 add in L2).
+//      dQ^T(i) is read out of TMEM (D = 64: by the P^T / dS^T warps, just
+//      before they store P^T(i+1) / dS^T(i+1) over it; D = 128: by four drain
+//      warps), staged in shared memory and added into dq with asynchronous
+//      TMA tensor reductions (fp32 add in L2).
 #include "attn_common.cuh"
 #include "sm100_ptx.cuh"
 
@@ -134,7 +136,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   __shared__ uint64_t bar_kv_full, bar_mma_done;
   __shared__ uint64_t bar_st_full[ST], bar_st_empty[ST];
   __shared__ uint64_t bar_sdp_full, bar_sdp_free, bar_pds_full, bar_pds_free, bar_dq_full,
-      bar_dq_free;
+      bar_dq_free, bar_stg_full[2], bar_stg_free[2];
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_flag;
 
@@ -181,9 +183,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     mbar_init(smem_u32(&bar_pds_free), 1);
     mbar_init(smem_u32(&bar_dq_full), 1);
     mbar_init(smem_u32(&bar_dq_free), 128);
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(smem_u32(&bar_stg_full[h]), 128);
+      mbar_init(smem_u32(&bar_stg_free[h]), 1);
+    }
     fence_barrier_init();
   }
-  if (warp == 13) {
+  if (warp == C::W_MMA) {
     tmem_alloc(smem_u32(&tmem_base_s), C::TMEM_COLS);
     tmem_relinquish();
   }
@@ -196,11 +202,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   auto stage_q = [&](int s) { return sStage + s * C::STAGE_BYTES; };
   auto stage_do = [&](int s) { return sStage + s * C::STAGE_BYTES + C::Q_BYTES; };
   auto stage_rows = [&](int s) {  // nlse2 then dvec, BQ floats each
-    return reinterpret_cast<const float*>(smem + C::SMEM_STAGE + s * C::STAGE_BYTES +
-                                          2 * C::Q_BYTES);
+    return reinterpret_cast<const float*>(
+        C::DQ_IN_COMPUTE ? smem + C::SMEM_ROWS + s * 2 * C::ROWVEC_BYTES
+                         : smem + C::SMEM_STAGE + s * C::STAGE_BYTES + 2 * C::Q_BYTES);
   };
 
-  if (warp == 12) {
+  if (warp == C::W_PROD) {
     // ------------------------------------------------------------ producer
     // The whole warp runs this loop; each copy is issued by one elected lane.
     {
@@ -234,9 +241,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           tma_load_4d_el(stage_do(s) + c * (BQ * 128), &tm_do, full, c * 64, h, q0, b);
         }
         const size_t rowoff = (static_cast<size_t>(b) * p.Hq + h) * p.S_pad + q0;
-        bulk_load_el(stage_do(s) + C::Q_BYTES, p.nlse2 + rowoff, C::ROWVEC_BYTES, full);
-        bulk_load_el(stage_do(s) + C::Q_BYTES + C::ROWVEC_BYTES, p.dvec + rowoff,
-                     C::ROWVEC_BYTES, full);
+        const uint32_t rows = smem_u32(stage_rows(s));
+        bulk_load_el(rows, p.nlse2 + rowoff, C::ROWVEC_BYTES, full);
+        bulk_load_el(rows + C::ROWVEC_BYTES, p.dvec + rowoff, C::ROWVEC_BYTES, full);
         issued = it + 1;
       }
       if (lane == 0) {
@@ -249,7 +256,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       (void)ok;
       __syncwarp();
     }
-  } else if (warp == 13) {
+  } else if (warp == C::W_MMA) {
     // ------------------------------------------------------------ MMA issuer
     TraceCursor tc;
     if (lane == 0) ATTN_TRACE_INIT(tc, 1);
@@ -324,20 +331,24 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         // Q_i and dO_i are not read again: hand the stage back to the producer.
         mma_commit_el(smem_u32(&bar_st_empty[s]));
         ATTN_TRACE_EV(tc, 5, it);  // dV, dK issued
-        if (it >= 1) {
-          ok = mbar_wait_warp(smem_u32(&bar_dq_free), (it - 1) & 1, ctl);
-          if (!ok) break;
-          tc_fence_after();
+        if constexpr (!C::DQ_IN_COMPUTE) {
+          if (it >= 1) {
+            ok = mbar_wait_warp(smem_u32(&bar_dq_free), (it - 1) & 1, ctl);
+            if (!ok) break;
+            tc_fence_after();
+          }
         }
-        ATTN_TRACE_EV(tc, 9, it);  // dq_free seen, issuing dQ
+        ATTN_TRACE_EV(tc, 9, it);  // issuing dQ
         // dQ^T[d][q] (+ 64 columns for the lo part) = sum over keys of
-        // K[key][d] [dS_hi^T | dS_lo^T][key][q]. It overwrites P^T, which
-        // dV(it) above has read (MMAs run in issue order).
+        // K[key][d] [dS_hi^T | dS_lo^T][key][q]. It overwrites P^T and dS^T,
+        // which dV(it) and dK(it) above have read (MMAs run in issue order).
+        // dQ^T(it-1) has been read out of these columns before P/dS(it) were
+        // stored (pds_full above) or, with drain warps, before dq_free.
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk)
           mma_ss_el(tmem + C::TM_DQ, add(dK_mn, kk * 2048), add(dDs_mn, kk * 2048), idesc_dq,
                     kk > 0);
-        mma_commit_el(smem_u32(&bar_dq_full));
+        if constexpr (!C::DQ_IN_COMPUTE) mma_commit_el(smem_u32(&bar_dq_full));
         mma_commit_el(smem_u32(&bar_pds_free));
         ATTN_TRACE_EV(tc, 6, it);  // dQ issued
       }
@@ -356,6 +367,33 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     bool ok = true;
     TraceCursor tc;
     if (lane == 0) ATTN_TRACE_INIT(tc, 2 + warp);
+    float* stg = reinterpret_cast<float*>(smem + C::SMEM_DQS + cg * C::DQS_BYTES);
+    // dQ^T = hi part (columns TM_DQ..+63) + lo part (TM_DQ+64..+127); this
+    // thread takes TMEM lane r (head dim d = r) and this half's 32 query
+    // columns of each part. The hi part sits where P^T goes and the lo part
+    // where dS^T goes, so each store below follows the read of its cells.
+    static_assert(C::TM_DQ == C::TM_P && C::TM_DQ + BQ == C::TM_DS, "dQ^T shares P^T/dS^T columns");
+    auto read_dq_part = [&](int part, float (&v)[HALF], bool add) {
+      uint32_t a[HALF];
+      tmem_ld32(tmem + lane_base + C::TM_DQ + part * BQ + cg * HALF, a);
+      tmem_wait_ld();
+#pragma unroll
+      for (int i = 0; i < HALF; ++i) v[i] = add ? v[i] + __uint_as_float(a[i]) : __uint_as_float(a[i]);
+    };
+    // Hand dQ(itq)'s rows cg*32.. (this half) to the reduction warp through
+    // this half's staging tile [32 q][D] fp32, once the reduction has read
+    // the half's previous tile out of it.
+    auto stage_dq = [&](int itq, const float (&v)[HALF]) {
+      if (itq >= 1 && !mbar_wait_warp(smem_u32(&bar_stg_free[cg]), (itq - 1) & 1, ctl))
+        return false;
+      if (r < D) {
+#pragma unroll
+        for (int i = 0; i < HALF; ++i) stg[i * D + r] = v[i];
+      }
+      fence_async_smem();
+      mbar_arrive(smem_u32(&bar_stg_full[cg]));
+      return true;
+    };
     for (int it = 0; it < n_it; ++it) {
       const int s = it % ST;
       const int q0 = (i_start + it % niq) * BQ;
@@ -421,10 +459,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       else
         p_ds(BoolConst<false>{});
       ATTN_TRACE_EV(tc, 3, it);  // P, dS computed
-      // dS^T goes to shared memory once the MMAs of the previous tile are done
-      // with it (dQ^T(it-1) is its last reader), and P^T, dS^T to TMEM once
-      // the drain has read dQ^T(it-1), whose columns they take; the drain's
-      // read overlaps the shared-memory stores.
+      // pds_free(it-1): the MMAs of tile it-1 are done, so dS^T in shared
+      // memory is free and dQ^T(it-1) is complete in TMEM. This thread reads
+      // its part of dQ^T(it-1) (lane = head dim d, this half's query columns)
+      // before storing P/dS(it) over those same TMEM cells.
+      float dqv[HALF];
       if (it >= 1) {
         ok = mbar_wait_warp(smem_u32(&bar_pds_free), (it - 1) & 1, ctl);
         if (!ok) break;
@@ -439,19 +478,39 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         st_sw128(sDsHi, r, unit, make_uint4(h[0], h[1], h[2], h[3]));
         st_sw128(sDsLo, r, unit, make_uint4(lo[0], lo[1], lo[2], lo[3]));
       }
-      if (it >= 1) {
-        ok = mbar_wait_warp(smem_u32(&bar_dq_free), (it - 1) & 1, ctl);
-        if (!ok) break;
-      }
       ATTN_TRACE_EV(tc, 4, it);  // previous MMAs done
+      if constexpr (!C::DQ_IN_COMPUTE) {
+        // The drain warps hand back the dQ^T(it-1) columns.
+        if (it >= 1) {
+          ok = mbar_wait_warp(smem_u32(&bar_dq_free), (it - 1) & 1, ctl);
+          if (!ok) break;
+        }
+      }
       tc_fence_after();
+      if (C::DQ_IN_COMPUTE && it >= 1) read_dq_part(0, dqv, false);
       tmem_st32(tmem + lane_base + C::TM_P + cg * HALF, pp);
+      if (C::DQ_IN_COMPUTE && it >= 1) read_dq_part(1, dqv, true);
       tmem_st32(tmem + lane_base + C::TM_DS + cg * HALF, dd);
       tmem_wait_st();
       fence_async_smem();
       tc_fence_before();
       mbar_arrive(smem_u32(&bar_pds_full));
       ATTN_TRACE_EV(tc, 5, it);  // P, dS stored and signalled
+      if (C::DQ_IN_COMPUTE && it >= 1) {
+        ok = stage_dq(it - 1, dqv);
+        if (!ok) break;
+      }
+    }
+    // The last tile's dQ^T, once its MMA has run.
+    if (C::DQ_IN_COMPUTE && ok && n_it > 0) {
+      ok = mbar_wait_warp(smem_u32(&bar_pds_free), (n_it - 1) & 1, ctl);
+      if (ok) {
+        tc_fence_after();
+        float dqv[HALF];
+        read_dq_part(0, dqv, false);
+        read_dq_part(1, dqv, true);
+        ok = stage_dq(n_it - 1, dqv);
+      }
     }
     if (ok) ok = mbar_wait_warp(smem_u32(&bar_mma_done), 0, ctl);
     if (ok) {
@@ -478,7 +537,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       }
     }
 #ifdef ATTN_TRACE
-  } else if (warp == 14) {
+  } else if (warp == C::W_MMA + 1) {
     // ------------------------------------------------------------ trace observer
     // Timestamps the completion of S^T/dP^T (1), dV/dK (2) and dQ^T (3) of
     // every tile by polling their barriers without blocking.
@@ -499,15 +558,40 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     while (i1 < n_it || i2 < n_it || i3 < n_it) {
       if (i1 < n_it && done(smem_u32(&bar_sdp_full), i1 & 1)) ATTN_TRACE_EV(tc, 1, i1++);
       if (i2 < n_it && done(smem_u32(&bar_st_empty[i2 % ST]), (i2 / ST) & 1)) ATTN_TRACE_EV(tc, 2, i2++);
-      if (i3 < n_it && done(smem_u32(&bar_dq_full), i3 & 1)) ATTN_TRACE_EV(tc, 3, i3++);
+      if (i3 < n_it && done(smem_u32(&bar_pds_free), i3 & 1)) ATTN_TRACE_EV(tc, 3, i3++);
       if (abort_flag || globaltimer() - t0 > 2000000000ull) break;
     }
 #endif
+  } else if (C::DQ_IN_COMPUTE) {
+    // ------------------------------------------------------------ dQ reduction warp
+    // Adds each staged half tile of dQ into dq with an fp32 TMA reduction,
+    // then hands the staging tile back once the reduction has read it.
+    bool ok = true;
+    TraceCursor tc;
+    if (lane == 0) ATTN_TRACE_INIT(tc, 10);
+    // Half 0 of each tile, then half 1; each half's staging tile cycles
+    // through its own pair of barriers.
+    for (int n = 0; n < 2 * n_it && ok; ++n) {
+      const int itq = n >> 1, half = n & 1;
+      ok = mbar_wait_warp(smem_u32(&bar_stg_full[half]), itq & 1, ctl);
+      if (!ok) break;
+      ATTN_TRACE_EV(tc, 1, n);  // half staged
+      if (lane == 0) {
+        const int h = g * p.G + itq / niq;
+        const int q0 = (i_start + itq % niq) * BQ;
+        tma_reduce_add_4d(&tm_dq, 0, h, q0 + half * C::DQ_ROWS, b, sDQS + half * C::DQS_BYTES);
+        bulk_commit_group();
+        bulk_wait_read_all();
+        mbar_arrive(smem_u32(&bar_stg_free[half]));
+      }
+      __syncwarp();
+    }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   } else {
     // ------------------------------------------------------------ dQ drain warps 8-11
     const int t = threadIdx.x - 256;  // TMEM lane = head-dim index d of dQ^T
     const uint32_t lane_base = static_cast<uint32_t>((warp % 4) * 32) << 16;
-    float* stg = reinterpret_cast<float*>(smem + C::SMEM_DQS);
     bool ok = true;
     TraceCursor tc;
     if (lane == 0) ATTN_TRACE_INIT(tc, 10 + (warp - 8));
@@ -538,11 +622,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       for (int half = 0; half < 2; ++half) {
         if (t == 0) bulk_wait_read_all();  // the previous reduction has read the staging tile
         named_bar_sync(1, 128);
+        float* stg = reinterpret_cast<float*>(smem + C::SMEM_DQS);
         if (t < D) {
           // staging [32 q][D] fp32, row-major (the TMA box layout); lane t holds column d = t.
 #pragma unroll
-          for (int q = 0; q < C::DQ_ROWS; ++q)
-            stg[q * D + t] = u[half * C::DQ_ROWS + q];
+          for (int q = 0; q < C::DQ_ROWS; ++q) stg[q * D + t] = u[half * C::DQ_ROWS + q];
         }
         fence_async_smem();
         named_bar_sync(1, 128);
@@ -558,7 +642,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 13) tmem_dealloc(tmem, C::TMEM_COLS);
+  if (warp == C::W_MMA) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
 template <int D, bool WIN>

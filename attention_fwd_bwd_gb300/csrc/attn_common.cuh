@@ -71,8 +71,8 @@ struct FwdParams {
 // accumulate in TMEM over the whole loop; dQ tiles are added into the fp32
 // dq output with TMA tensor reductions.
 // Warps 0-7: P^T / dS^T and the dK/dV epilogue (one key row per thread; warps
-// w and w+4 share TMEM lanes and split the 64 query columns); warps 8-11: dQ
-// drain; warp 12: TMA producer; warp 13: MMA issuer.
+// w and w+4 share TMEM lanes and split the 64 query columns); the dQ warps
+// from 8 on (see DQ_IN_COMPUTE); then the TMA producer and the MMA issuer.
 //
 // P and dS enter the gradient MMAs as a pair of bf16 values (hi = bf16(x),
 // lo = bf16(x - hi)), i.e. with about 16 significant bits: dV += P_hi^T dO +
@@ -89,7 +89,16 @@ struct BwdCfg {
   static constexpr int Q_BYTES = BQ * D * 2;
   static constexpr int STAGES = 3;
   static constexpr int ROWVEC_BYTES = BQ * 4;
-  static constexpr int STAGE_BYTES = ((2 * Q_BYTES + 2 * ROWVEC_BYTES) + 1023) / 1024 * 1024;
+  // Who reads dQ^T out of TMEM. D = 64: the P^T / dS^T warps, just before
+  // storing P^T / dS^T over it, each staging its 32-row half tile in its own
+  // shared-memory tile, and one warp issues the reductions. D = 128: four
+  // drain warps, which also stage the tile, so that the twice larger staging
+  // stores stay off the P^T / dS^T warps (measured faster there).
+  static constexpr bool DQ_IN_COMPUTE = (D == 64);
+  // Per stage: Q, dO, then -LSE*log2(e) and Dvec of the stage's BQ query rows
+  // (1024-byte multiple) when the row vectors sit in the stage, as for D = 128.
+  static constexpr int STAGE_BYTES =
+      DQ_IN_COMPUTE ? 2 * Q_BYTES : (2 * Q_BYTES + 2 * ROWVEC_BYTES + 1023) / 1024 * 1024;
   static constexpr int DS_BYTES = BK * BQ * 2;       // one bf16 dS^T tile (hi or lo)
   static constexpr int DQ_ROWS = BQ / 2;            // dQ leaves in two halves of 32 rows
   static constexpr int DQS_BYTES = DQ_ROWS * D * 4;  // dQ staging half-tile, fp32
@@ -98,13 +107,16 @@ struct BwdCfg {
   static constexpr int SMEM_STAGE = SMEM_V + V_BYTES;
   static constexpr int SMEM_DS_HI = SMEM_STAGE + STAGES * STAGE_BYTES;
   static constexpr int SMEM_DS_LO = SMEM_DS_HI + DS_BYTES;
+  static constexpr int N_DQS = DQ_IN_COMPUTE ? 2 : 1;  // dQ staging tiles
   static constexpr int SMEM_DQS = SMEM_DS_LO + DS_BYTES;
-  static constexpr int SMEM_BYTES = SMEM_DQS + DQS_BYTES;
+  // D = 64: the row vectors of every stage, after the staging tiles.
+  static constexpr int SMEM_ROWS = SMEM_DQS + N_DQS * DQS_BYTES;
+  static constexpr int SMEM_BYTES = SMEM_ROWS + (DQ_IN_COMPUTE ? STAGES * 2 * ROWVEC_BYTES : 0);
   static constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;
   // Tensor-memory columns. dQ^T is produced as one N = 128 product over the
   // adjacent [dS_hi^T | dS_lo^T] tiles: its columns 0..63 hold K^T dS_hi^T and
-  // 64..127 hold K^T dS_lo^T, summed by the drain. P^T and dS^T (hi/lo, bf16
-  // pairs) live in that region between the drain reading dQ^T(i-1) and the
+  // 64..127 hold K^T dS_lo^T, summed when read back. P^T and dS^T (hi/lo,
+  // bf16 pairs) live in that region between the read of dQ^T(i-1) and the
   // dQ MMA of tile i, which runs after dV(i) and dK(i) have read them. dV and
   // dK take their A operand from tensor memory, so only their B operand
   // (dO, Q) is read from shared memory.
@@ -118,10 +130,13 @@ struct BwdCfg {
   static constexpr int TM_P = 384;
   static constexpr int TM_DS = 448;
   static constexpr int TMEM_COLS = 512;
+  static constexpr int N_DQW = DQ_IN_COMPUTE ? 1 : 4;  // warps 8 .. 8 + N_DQW - 1
+  static constexpr int W_PROD = 8 + N_DQW;               // TMA producer warp
+  static constexpr int W_MMA = W_PROD + 1;               // MMA issuer warp
 #ifdef ATTN_TRACE
-  static constexpr int THREADS = 480;  // + one warp that timestamps MMA completions
+  static constexpr int THREADS = 32 * (W_MMA + 2);  // + one warp that timestamps MMA completions
 #else
-  static constexpr int THREADS = 448;
+  static constexpr int THREADS = 32 * (W_MMA + 1);
 #endif
   static_assert(SMEM_ALLOC <= 232448, "shared-memory plan exceeds 227 KB");
 };

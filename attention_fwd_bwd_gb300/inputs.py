@@ -83,3 +83,96 @@ def make_inputs(B, Hq, Hkv, S, D, seed, qk_std=1.0):
 
 def workload_inputs(w: Workload):
     return make_inputs(w.B, w.Hq, w.Hkv, w.S, w.D, w.seed, w.qk_std)
+
+
+# ---------------------------------------------------------------- sparse top-k
+# Synthetic stand-in for the top-k lists of the pages' compressed sparse
+# attention (Table 7, "cr4": every query attends to a 128-token sliding window
+# plus the top-k rows of a pool compressed 4:1). No trained model or real
+# top-k map is available, so the lists are drawn at random with the same
+# structure:
+#   * pool rows 0..T-1 are the tokens' own rows; rows T..T+T/r-1 are the
+#     compressed rows, row T+c summarising tokens r*c..r*c+r-1;
+#   * token t's list is its window, rows t-W+1..t (-1 where negative), then
+#     `topk` compressed rows: all visible ones (those whose r tokens end at or
+#     before t) when there are at most `topk`, else a uniformly random subset
+#     of `topk` of them, in ascending order; -1 pads the rest.
+# q, kp, vp and dO are N(0,1) draws rounded to bf16, in that order, from the
+# same seeded generator, followed by the random keys that pick the subsets.
+
+
+@dataclass(frozen=True)
+class SparseWorkload:
+    name: str
+    B: int
+    T: int
+    H: int
+    DK: int
+    DV: int
+    window: int
+    topk: int
+    ratio: int
+    seed: int = 2024
+
+    @property
+    def P(self) -> int:
+        return self.T + self.T // self.ratio
+
+    @property
+    def K(self) -> int:
+        return self.window + self.topk
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.DK)
+
+
+SPARSE_WORKLOADS = [
+    # Pro cr4 (Table 7): 128 heads, top-k 1152 = 128 window + top-1024 of T/4.
+    SparseWorkload("csa_pro_cr4_t16384", 1, 16384, 128, 128, 128, 128, 1024, 4, 2024),
+    # Flash cr4 (Table 7): 64 heads, top-k 640 = 128 window + top-512 of T/4.
+    SparseWorkload("csa_flash_cr4_t8192", 1, 8192, 64, 128, 128, 128, 512, 4, 2025),
+    # Small case the oracle finishes in seconds; d_v != d.
+    SparseWorkload("csa_small_t512", 2, 512, 128, 128, 64, 128, 96, 4, 2026),
+]
+SPARSE_BY_NAME = {w.name: w for w in SPARSE_WORKLOADS}
+
+
+def make_sparse_index(T, window, topk, ratio, g):
+    """idx [T, window + topk] int32 as the recipe above says (torch.Generator g)."""
+    nc = T // ratio
+    idx = torch.full((T, window + topk), -1, dtype=torch.int32)
+    t = torch.arange(T, dtype=torch.int64)
+    w = t[:, None] - (window - 1) + torch.arange(window, dtype=torch.int64)[None, :]
+    idx[:, :window] = torch.where(w >= 0, w, torch.full_like(w, -1)).to(torch.int32)
+    if nc == 0 or topk == 0:
+        return idx
+    keys = torch.rand(T, nc, generator=g, dtype=torch.float32)
+    visible = (torch.arange(nc, dtype=torch.int64)[None, :] + 1) * ratio <= (t[:, None] + 1)
+    keys = torch.where(visible, keys, torch.full_like(keys, -1.0))
+    n_vis = visible.sum(dim=1)
+    kk = min(topk, nc)
+    pick = keys.topk(kk, dim=1).indices  # the kk largest keys; invisible rows rank last
+    pick, _ = pick.sort(dim=1)
+    # Rows that are not visible only fill lists with fewer than kk visible rows:
+    # drop them, keeping the visible ones in ascending order.
+    ok = visible.gather(1, pick)
+    rows = torch.where(ok, pick + T, torch.full_like(pick, -1))
+    # Move the filled entries to the front (stable), -1 after them.
+    order = torch.argsort((~ok).to(torch.int8), dim=1, stable=True)
+    rows = rows.gather(1, order)
+    idx[:, window:window + kk] = rows.to(torch.int32)
+    assert int((rows >= 0).sum(dim=1).max()) <= int(n_vis.max())
+    return idx
+
+
+def make_sparse_inputs(w: SparseWorkload):
+    """bf16 CPU tensors (q [B,T,H,DK], kp [B,P,DK], vp [B,P,DV], do [B,T,H,DV])
+    and idx [B,T,K] int32, drawn as the recipe above says."""
+    g = torch.Generator(device="cpu").manual_seed(int(w.seed))
+    q = torch.randn(w.B, w.T, w.H, w.DK, generator=g, dtype=torch.float32)
+    kp = torch.randn(w.B, w.P, w.DK, generator=g, dtype=torch.float32)
+    vp = torch.randn(w.B, w.P, w.DV, generator=g, dtype=torch.float32)
+    do = torch.randn(w.B, w.T, w.H, w.DV, generator=g, dtype=torch.float32)
+    idx = torch.stack([make_sparse_index(w.T, w.window, w.topk, w.ratio, g) for _ in range(w.B)])
+    return tuple(t.to(torch.bfloat16) for t in (q, kp, vp, do)) + (idx,)

@@ -26,6 +26,7 @@ __all__ = [
     "attn_bwd_preprocess",
     "attn_bwd_main",
     "attn_bwd_noalloc",
+    "attn_sparse_fwd",
     "attn_bwd_workspace_size",
     "attn_check_status",
     "attn_set_wait_timeout_ns",
@@ -87,6 +88,8 @@ def lib():
     L.attn_bwd_main_ex.restype = i
     L.attn_bwd_noalloc.argtypes = [vp] * 10 + [i] * 6 + [f, vp]
     L.attn_bwd_noalloc.restype = i
+    L.attn_sparse_fwd.argtypes = [vp] * 7 + [i] * 7 + [f, vp]
+    L.attn_sparse_fwd.restype = i
     L.attn_status_string.argtypes = [i]
     L.attn_status_string.restype = ctypes.c_char_p
     L.attn_check_status.argtypes = [vp]
@@ -182,6 +185,38 @@ def attn_fwd_ex(q, k, v, o, lse, causal, window, scale, o_lo=None, stream=None):
     _check("attn_fwd_ex", lib().attn_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _opt(o_lo), _ptr(lse),
                                             B, Hq, Hkv, S, D, int(bool(causal)), int(window), float(scale),
                                             _stream(stream)))
+
+
+def _sparse_sizes(q, kp, vp, idx):
+    import torch
+    for t in (q, kp, vp):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, kp, vp, o, o_lo, dO must be contiguous bf16 CUDA tensors")
+    if q.dim() != 4 or kp.dim() != 3 or vp.dim() != 3:
+        raise ValueError("q is [B,T,H,DK], kp [B,P,DK], vp [B,P,DV]")
+    B, T, H, DK = q.shape
+    if kp.shape[0] != B or kp.shape[2] != DK or tuple(vp.shape[:2]) != tuple(kp.shape[:2]):
+        raise ValueError(f"kp {tuple(kp.shape)} / vp {tuple(vp.shape)} do not match q {tuple(q.shape)}")
+    if (idx.dtype != torch.int32 or not idx.is_contiguous() or idx.dim() != 3
+            or tuple(idx.shape[:2]) != (B, T) or idx.device != q.device):
+        raise ValueError("idx must be a contiguous int32 tensor [B, T, K] on q's device")
+    return B, T, H, kp.shape[1], idx.shape[2], DK, vp.shape[2]
+
+
+def attn_sparse_fwd(q, kp, vp, idx, o, lse, scale, o_lo=None, stream=None):
+    """o (and o_lo), lse <- sparse top-k gather attention; see attn_sparse_fwd
+    in include/attn.h."""
+    import torch
+    B, T, H, P, K, DK, DV = _sparse_sizes(q, kp, vp, idx)
+    ref = torch.empty((B, T, H, DV), dtype=torch.bfloat16, device="meta")
+    for t, what in ((o, "o"), (o_lo, "o_lo")):
+        if t is not None and (tuple(t.shape) != tuple(ref.shape) or t.dtype != torch.bfloat16
+                              or not t.is_contiguous() or t.device != q.device):
+            raise ValueError(f"{what} must be a contiguous bf16 tensor of shape {tuple(ref.shape)}")
+    _lse_ok(lse, B, H, T, q.device)
+    _check("attn_sparse_fwd", lib().attn_sparse_fwd(_ptr(q), _ptr(kp), _ptr(vp), _ptr(idx), _ptr(o), _opt(o_lo),
+                                                    _ptr(lse), B, T, H, P, K, DK, DV, float(scale),
+                                                    _stream(stream)))
 
 
 def attn_bwd_workspace_size(B, Hq, Hkv, S, D):

@@ -12,6 +12,7 @@
 
 #include "../../include/attn.h"
 #include "attn_common.cuh"
+#include "attn_sparse.cuh"
 
 namespace attn {
 namespace {
@@ -111,6 +112,20 @@ bool make_dq_map(CUtensorMap* m, void* base, int B, int S, int H, int D) {
   const cuuint32_t es[4] = {1, 1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 2-D bf16 map over `rows` rows of `cols` columns (row-major, contiguous); a
+// box is `box_rows` rows of 64 columns (128 bytes), 128-byte swizzle.
+bool make_rows_map(CUtensorMap* m, const void* base, long long rows, int cols, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -350,6 +365,54 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
                        size_t workspace_bytes, void* stream) {
   return attn_bwd_ex(q, k, v, o, dO, lse, dq, dk, dv, o_lo, B, Hq, Hkv, S, D, causal, 0, scale,
                      workspace, workspace_bytes, stream);
+}
+
+attn_status_t attn_sparse_fwd(const void* q, const void* kp, const void* vp, const int* idx,
+                              void* o, void* o_lo, float* lse, int B, int T, int H, int P, int K,
+                              int DK, int DV, float scale, void* stream) {
+  if (B < 0 || T < 0 || H <= 0 || H > 128 || P <= 0 || K <= 0 || (K % 4) != 0)
+    return ATTN_ERR_INVALID_ARG;
+  if ((DK != 64 && DK != 128) || (DV != 64 && DV != 128)) return ATTN_ERR_UNSUPPORTED;
+  if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  // Row counts of the 2-D views stay within what the TMA coordinates hold.
+  if (static_cast<long long>(B) * T * H >= (1ll << 31) || static_cast<long long>(B) * P >= (1ll << 31))
+    return ATTN_ERR_UNSUPPORTED;
+  if (B == 0 || T == 0) return ATTN_OK;
+  if (!q || !kp || !vp || !idx || !o || !lse) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(kp) || !aligned16(vp) || !aligned16(idx) || !aligned16(o) ||
+      !aligned16(o_lo) || !aligned16(lse))
+    return ATTN_ERR_INVALID_ARG;
+  attn_status_t st = check_device();
+  if (st != ATTN_OK) return st;
+  const long long qrows = static_cast<long long>(B) * T * H, prows = static_cast<long long>(B) * P;
+  CUtensorMap tq, to, tolo;
+  (void)prows;
+  if (!make_rows_map(&tq, q, qrows, DK, 128) || !make_rows_map(&to, o, qrows, DV, H) ||
+      !make_rows_map(&tolo, o_lo ? o_lo : o, qrows, DV, H))
+    return ATTN_ERR_CUDA;
+  int* status = fwd_status_ptr();
+  if (!status) return ATTN_ERR_CUDA;
+  SparseFwdParams p;
+  p.kp = static_cast<const __nv_bfloat16*>(kp);
+  p.vp = static_cast<const __nv_bfloat16*>(vp);
+  p.idx = idx;
+  p.lse = lse;
+  p.B = B;
+  p.T = T;
+  p.H = H;
+  p.P = P;
+  p.K = K;
+  p.n_chunks = (K + 127) / 128;
+  // As in the dense forward: empty slots get an infinite score, which a zero
+  // scale would turn into NaN, so a scale below 2^-100 is taken as +-2^-100.
+  float sl2 = scale * kLog2e;
+  if (std::fabs(sl2) < 0x1p-100f) sl2 = std::signbit(sl2) ? -0x1p-100f : 0x1p-100f;
+  p.scale_log2 = sl2;
+  p.status = status;
+  p.timeout_ns = g_timeout_ns;
+  p.inject_stall = g_inject_stall & 1;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return finish(launch_sparse_fwd(DK, DV, tq, to, tolo, o_lo != nullptr, p, s), s, status);
 }
 
 attn_status_t attn_check_status(void* workspace) {

@@ -206,6 +206,38 @@ attn_status_t attn_bwd_noalloc(const void* q, const void* k, const void* v, cons
                                const void* o_lo, int B, int Hq, int Hkv, int S, int D, int causal,
                                float scale, void* stream);
 
+/*
+ * Sparse top-k gather attention, forward ("Scheduling Data to Compute:
+ * Hierarchical Data Pipelining for LLM Training on AMD GPUs", section 2.1:
+ * each query token receives a top-k list of KV rows; the forward gathers them,
+ * scores them and streams their values into the output; section 3 and
+ * Table 7 for the list shapes: a 128-row window plus top-k compressed rows).
+ *
+ * For every batch b, token t and head h:
+ *   O[b,t,h,:] = sum_j softmax_j(scale * q[b,t,h,:] . kp[b,idx[b,t,j],:])
+ *                      * vp[b,idx[b,t,j],:]
+ * over the slots j whose entry lies in [0, P); any other entry (e.g. -1) is an
+ * empty slot. All heads of a token share its list and the one key/value pool
+ * of its batch. A row listed twice counts twice.
+ *   q   [B, T, H, DK] bf16      kp [B, P, DK] bf16     vp [B, P, DV] bf16
+ *   idx [B, T, K] int32 (K a multiple of 4)
+ *   o   [B, T, H, DV] bf16 (out)
+ *   o_lo [B, T, H, DV] bf16 (out, optional): bf16(O - o), so that o + o_lo
+ *        carries O to about 16 significant bits; NULL to skip.
+ *   lse [B, H, T] fp32 (out): natural log-sum-exp of the scaled scores over
+ *        the filled slots; a token with no filled slot gets O = 0 and
+ *        LSE = -inf.
+ * H is 1..128, DK and DV are 64 or 128 each (they may differ). Device
+ * pointers, contiguous, 16-byte aligned; the caller owns every buffer.
+ * Errors: ATTN_ERR_INVALID_ARG for bad sizes, null or misaligned pointers or
+ * a non-finite scale; ATTN_ERR_UNSUPPORTED for other head dimensions or a
+ * non-sm_103a device; ATTN_ERR_CUDA for a failed launch. B = 0 or T = 0 is a
+ * no-op. Bounded pipeline waits report through attn_check_status(NULL).
+ */
+attn_status_t attn_sparse_fwd(const void* q, const void* kp, const void* vp, const int* idx,
+                              void* o, void* o_lo, float* lse, int B, int T, int H, int P, int K,
+                              int DK, int DV, float scale, void* stream);
+
 /* Static, human-readable name of a status code. */
 const char* attn_status_string(attn_status_t status);
 

@@ -84,6 +84,24 @@ def test_window_argument_validation(L):
     assert main(128, causal=0) == 1
 
 
+def test_sparse_argument_validation(L):
+    def fwd(B=1, T=4, H=128, P=10, K=8, DK=128, DV=64, scale=0.1, ptrs=None):
+        p = ptrs if ptrs is not None else [FAKE] * 5 + [None, FAKE]
+        return L.attn_sparse_fwd(*p, B, T, H, P, K, DK, DV, scale, None)
+    assert fwd(H=0) == 1
+    assert fwd(H=129) == 1                    # one token's heads fill at most one 128-row tile
+    assert fwd(K=6) == 1                      # K a multiple of 4
+    assert fwd(K=0) == 1
+    assert fwd(P=0) == 1
+    assert fwd(T=-1) == 1
+    assert fwd(DK=96) == 2
+    assert fwd(DV=256) == 2
+    assert fwd(scale=float("nan")) == 1
+    assert fwd(B=0, ptrs=[None] * 7) == 0     # empty: no-op
+    assert fwd(ptrs=[FAKE, FAKE, FAKE, None, FAKE, None, FAKE]) == 1   # null idx
+    assert fwd(ptrs=[FAKE, FAKE, FAKE, FAKE + 4, FAKE, None, FAKE]) == 1  # misaligned idx
+
+
 def test_bwd_argument_validation(L):
     def bwd(ws=FAKE * 16, wsb=1 << 30, B=1, S=128, D=64, ptrs=None, Hq=2, Hkv=1):
         p = ptrs if ptrs is not None else [FAKE] * 9 + [None]

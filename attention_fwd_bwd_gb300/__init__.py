@@ -27,6 +27,8 @@ __all__ = [
     "attn_bwd_main",
     "attn_bwd_noalloc",
     "attn_sparse_fwd",
+    "attn_sparse_bwd",
+    "attn_sparse_bwd_workspace_size",
     "attn_bwd_workspace_size",
     "attn_check_status",
     "attn_set_wait_timeout_ns",
@@ -90,6 +92,10 @@ def lib():
     L.attn_bwd_noalloc.restype = i
     L.attn_sparse_fwd.argtypes = [vp] * 7 + [i] * 7 + [f, vp]
     L.attn_sparse_fwd.restype = i
+    L.attn_sparse_bwd_workspace_size.argtypes = [i, i, i]
+    L.attn_sparse_bwd_workspace_size.restype = sz
+    L.attn_sparse_bwd.argtypes = [vp] * 11 + [i] * 7 + [f, vp, sz, vp]
+    L.attn_sparse_bwd.restype = i
     L.attn_status_string.argtypes = [i]
     L.attn_status_string.restype = ctypes.c_char_p
     L.attn_check_status.argtypes = [vp]
@@ -216,6 +222,30 @@ def attn_sparse_fwd(q, kp, vp, idx, o, lse, scale, o_lo=None, stream=None):
     _lse_ok(lse, B, H, T, q.device)
     _check("attn_sparse_fwd", lib().attn_sparse_fwd(_ptr(q), _ptr(kp), _ptr(vp), _ptr(idx), _ptr(o), _opt(o_lo),
                                                     _ptr(lse), B, T, H, P, K, DK, DV, float(scale),
+                                                    _stream(stream)))
+
+
+def attn_sparse_bwd_workspace_size(B, T, H):
+    return int(lib().attn_sparse_bwd_workspace_size(B, T, H))
+
+
+def attn_sparse_bwd(q, kp, vp, idx, o, dO, lse, dq, dkp, dvp, scale, workspace, o_lo=None, stream=None):
+    """dq, dkp, dvp <- gradient of sparse top-k gather attention; see
+    attn_sparse_bwd in include/attn.h."""
+    import torch
+    B, T, H, P, K, DK, DV = _sparse_sizes(q, kp, vp, idx)
+    for t, what, shape, dt in ((o, "o", (B, T, H, DV), torch.bfloat16), (dO, "dO", (B, T, H, DV), torch.bfloat16),
+                               (o_lo, "o_lo", (B, T, H, DV), torch.bfloat16),
+                               (dq, "dq", (B, T, H, DK), torch.float32), (dkp, "dkp", (B, P, DK), torch.float32),
+                               (dvp, "dvp", (B, P, DV), torch.float32)):
+        if t is not None and (tuple(t.shape) != shape or t.dtype != dt or not t.is_contiguous()
+                              or t.device != q.device):
+            raise ValueError(f"{what} must be a contiguous {dt} tensor of shape {shape}")
+    _lse_ok(lse, B, H, T, q.device)
+    ws, wsb = _ws(workspace)
+    _check("attn_sparse_bwd", lib().attn_sparse_bwd(_ptr(q), _ptr(kp), _ptr(vp), _ptr(idx), _ptr(o), _opt(o_lo),
+                                                    _ptr(dO), _ptr(lse), _ptr(dq), _ptr(dkp), _ptr(dvp),
+                                                    B, T, H, P, K, DK, DV, float(scale), ws, wsb,
                                                     _stream(stream)))
 
 

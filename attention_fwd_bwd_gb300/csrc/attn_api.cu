@@ -415,6 +415,71 @@ attn_status_t attn_sparse_fwd(const void* q, const void* kp, const void* vp, con
   return finish(launch_sparse_fwd(DK, DV, tq, to, tolo, o_lo != nullptr, p, s), s, status);
 }
 
+size_t attn_sparse_bwd_workspace_size(int B, int T, int H) {
+  if (B <= 0 || T <= 0 || H <= 0 || H > 128) return 0;
+  return sparse_bwd_workspace_bytes(static_cast<long long>(B) * T * H);
+}
+
+attn_status_t attn_sparse_bwd(const void* q, const void* kp, const void* vp, const int* idx,
+                              const void* o, const void* o_lo, const void* dO, const float* lse,
+                              float* dq, float* dkp, float* dvp, int B, int T, int H, int P, int K,
+                              int DK, int DV, float scale, void* workspace, size_t workspace_bytes,
+                              void* stream) {
+  if (B < 0 || T < 0 || H <= 0 || H > 128 || P <= 0 || K <= 0 || (K % 4) != 0)
+    return ATTN_ERR_INVALID_ARG;
+  if ((DK != 64 && DK != 128) || (DV != 64 && DV != 128)) return ATTN_ERR_UNSUPPORTED;
+  if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * T * H >= (1ll << 31) || static_cast<long long>(B) * P >= (1ll << 31))
+    return ATTN_ERR_UNSUPPORTED;
+  if (B == 0 || T == 0) return ATTN_OK;
+  if (!q || !kp || !vp || !idx || !o || !dO || !lse || !dq || !dkp || !dvp) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(kp) || !aligned16(vp) || !aligned16(idx) || !aligned16(o) ||
+      !aligned16(o_lo) || !aligned16(dO) || !aligned16(lse) || !aligned16(dq) || !aligned16(dkp) ||
+      !aligned16(dvp))
+    return ATTN_ERR_INVALID_ARG;
+  const long long rows = static_cast<long long>(B) * T * H;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+      workspace_bytes < sparse_bwd_workspace_bytes(rows))
+    return ATTN_ERR_WORKSPACE;
+  attn_status_t st = check_device();
+  if (st != ATTN_OK) return st;
+  CUtensorMap tq, tdo;
+  if (!make_rows_map(&tq, q, rows, DK, 128) || !make_rows_map(&tdo, dO, rows, DV, 128))
+    return ATTN_ERR_CUDA;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const size_t vec_bytes = (static_cast<size_t>(rows) * 4 + 255) / 256 * 256;
+  float* nlse2 = reinterpret_cast<float*>(ws + 256);
+  float* dvec = reinterpret_cast<float*>(ws + 256 + vec_bytes);
+  SparseBwdParams p;
+  p.kp = static_cast<const __nv_bfloat16*>(kp);
+  p.vp = static_cast<const __nv_bfloat16*>(vp);
+  p.idx = idx;
+  p.nlse2 = nlse2;
+  p.dvec = dvec;
+  p.dq = dq;
+  p.dkp = dkp;
+  p.dvp = dvp;
+  p.B = B;
+  p.T = T;
+  p.H = H;
+  p.P = P;
+  p.K = K;
+  p.n_chunks = (K + 127) / 128;
+  float sl2 = scale * kLog2e;
+  if (std::fabs(sl2) < 0x1p-100f) sl2 = std::signbit(sl2) ? -0x1p-100f : 0x1p-100f;
+  p.scale_log2 = sl2;
+  p.scale = scale;
+  p.status = static_cast<int*>(workspace);
+  p.timeout_ns = g_timeout_ns;
+  p.inject_stall = (g_inject_stall >> 1) & 1;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return finish(launch_sparse_bwd(DK, DV, static_cast<const __nv_bfloat16*>(o),
+                                  static_cast<const __nv_bfloat16*>(o_lo),
+                                  static_cast<const __nv_bfloat16*>(dO), lse, nlse2, dvec, tq, tdo, p,
+                                  s),
+                s, p.status);
+}
+
 attn_status_t attn_check_status(void* workspace) {
   if (cudaDeviceSynchronize() != cudaSuccess) return ATTN_ERR_CUDA;
   int* fs = fwd_status_ptr();

@@ -70,3 +70,80 @@ cudaError_t launch_sparse_fwd(int DK, int DV, const CUtensorMap& tq, const CUten
                               cudaStream_t stream);
 
 }  // namespace attn
+
+namespace attn {
+
+// Backward: one work item per (batch, token), as in the forward. The token's
+// Q (H x DK) and dO (H x DV) rows stay in shared memory; the gathered K and V
+// rows of each 128-slot chunk stream through the ring. Products are taken
+// slot-major (TMEM lane = slot): S^T = K_c Q^T, dP^T = V_c dO^T, then
+// dV_c = P^T dO and dK_c = dS^T Q (A from TMEM), scatter-added into the pool
+// gradients, and dQ^T += K_c^T dS^T (dS^T from shared memory), which stays in
+// TMEM over the token's chunks.
+template <int DK, int DV>
+struct SparseBwdCfg {
+  static constexpr int BQ = 128;  // head rows
+  static constexpr int BK = 128;  // slots per chunk
+  static constexpr int KCH = DK / 64;
+  static constexpr int VCH = DV / 64;
+  static constexpr int Q_BYTES = BQ * DK * 2;
+  static constexpr int DO_BYTES = BQ * DV * 2;
+  static constexpr int K_BYTES = BK * DK * 2;
+  static constexpr int V_BYTES = BK * DV * 2;
+  // A K slot is read as a 128-row (two 64-column block) MN-major operand by
+  // the dQ^T product even when DK = 64 (rows past DK are ignored), so a slot
+  // is never smaller than two blocks.
+  static constexpr int SLOT_BYTES = 2 * BK * 128;
+  static constexpr int DS_BYTES = BK * BQ * 2;     // one bf16 dS^T tile (hi or lo)
+  static constexpr int ROWS_BYTES = 2 * BQ * 4;    // -LSE*log2(e) and Dvec per head
+  static constexpr int IDX_BYTES = BK * 4;
+  static constexpr int SMEM_Q = 0;
+  static constexpr int SMEM_DO = SMEM_Q + Q_BYTES;
+  static constexpr int SMEM_DS = SMEM_DO + DO_BYTES;  // hi tile, then lo tile
+  static constexpr int SMEM_RING = SMEM_DS + 2 * DS_BYTES;
+  static constexpr int FIXED = SMEM_RING + ROWS_BYTES + IDX_BYTES + 1024;
+  static constexpr int NSLOT_FIT = (232448 - FIXED) / SLOT_BYTES;
+  static constexpr int NSLOT = NSLOT_FIT > 8 ? 8 : NSLOT_FIT;
+  static constexpr int SMEM_ROWS = SMEM_RING + NSLOT * SLOT_BYTES;
+  static constexpr int SMEM_IDX = SMEM_ROWS + ROWS_BYTES;
+  static constexpr int SMEM_BYTES = SMEM_IDX + IDX_BYTES;
+  static constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;
+  // Releasing K_c's position needs V_c's (the dQ^T product that frees K_c
+  // follows dP^T), so copies in flight stay below NSLOT - 1 positions.
+  static constexpr int COPY_DEPTH = NSLOT - 2;
+  // TMEM columns: S^T (then P^T, then dK_c), dP^T (then dS^T), dV_c, dQ^T.
+  static constexpr int TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DQ = 384;
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int THREADS = 192;  // 4 compute warps, producer, MMA issuer
+  static_assert(NSLOT >= 3, "the ring needs K and V of one chunk plus one");
+  static_assert(SMEM_ALLOC <= 232448, "shared-memory plan exceeds 227 KB");
+};
+
+struct SparseBwdParams {
+  const __nv_bfloat16* kp;  // [B, P, DK]
+  const __nv_bfloat16* vp;  // [B, P, DV]
+  const int* idx;           // [B, T, K]
+  const float* nlse2;       // [B, T, H] -LSE * log2(e) (-inf for a token without filled slots)
+  const float* dvec;        // [B, T, H] rowsum(dO * O)
+  float* dq;                // [B, T, H, DK]
+  float* dkp;               // [B, P, DK] (zeroed by the preprocess)
+  float* dvp;               // [B, P, DV] (zeroed by the preprocess)
+  int B, T, H, P, K;
+  int n_chunks;
+  float scale_log2, scale;
+  int* status;
+  unsigned long long timeout_ns;
+  int inject_stall;
+};
+
+// Workspace of the sparse backward: status word, then nlse2 and dvec rows.
+inline size_t sparse_bwd_workspace_bytes(long long rows) {
+  return 256 + 2 * ((static_cast<size_t>(rows) * 4 + 255) / 256 * 256);
+}
+
+cudaError_t launch_sparse_bwd(int DK, int DV, const __nv_bfloat16* o, const __nv_bfloat16* o_lo,
+                              const __nv_bfloat16* dO, const float* lse, float* nlse2, float* dvec,
+                              const CUtensorMap& tq, const CUtensorMap& tdo,
+                              const SparseBwdParams& p, cudaStream_t stream);
+
+}  // namespace attn

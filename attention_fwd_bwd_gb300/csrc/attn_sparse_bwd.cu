@@ -1,0 +1,491 @@
+// Sparse top-k gather attention, backward, for sm_103a ("Scheduling Data to
+// Compute: Hierarchical Data Pipelining for LLM Training on AMD GPUs", section
+// 2.1: the backward gathers the same sparse vectors to form dQ, produces a
+// per-slot intermediate for dKV and reduces it through the inverse of the
+// top-k map). The gradient of sum(dO * O) for
+// O[t, h] = softmax_j(scale * q[t, h] . kp[idx[t, j]]) vp[idx[t, j]]:
+//   P = softmax, dP = dO V^T, Dvec = rowsum(dO * O), dS = P * (dP - Dvec),
+//   dq = scale * dS K, per-slot dK = scale * dS^T Q and dV = P^T dO,
+//   dkp / dvp of a pool row = sum of the per-slot terms of every slot naming it.
+//
+// Two kernels on one stream:
+//   1. preprocess: Dvec from o (+ o_lo) and dO, -LSE*log2(e) per (token, head),
+//      and zeroed dkp / dvp (HBM-bound).
+//   2. main, one persistent CTA per SM over (batch, token) items:
+//      warp 4 (producer): the token's Q and dO rows (TMA tiles) and row
+//          vectors, then each chunk's K and V rows gathered with cp.async into
+//          a ring (as in the forward).
+//      warp 5 (MMA issuer), per chunk c: S^T = K_c Q^T and dP^T = V_c dO^T
+//          (slot-major: TMEM lane = slot), then dV_c = P^T dO and
+//          dK_c = dS^T Q with A from TMEM, and dQ^T += K_c^T dS^T with dS^T
+//          from shared memory (dQ^T stays in TMEM over the token's chunks).
+//      warps 0-3 (thread = slot): P^T and scale * dS^T as bf16 hi/lo pairs
+//          into TMEM and (dS^T) shared memory; then the per-slot dV_c and dK_c
+//          rows are added into the pool gradients with vector fp32 reductions
+//          (red.global.add.v4.f32); after the token's last chunk, dQ^T
+//          (thread = head-dim index) is written to dq.
+// The phases of one chunk run one after another; the gathers of the next
+// chunks overlap them.
+#include <type_traits>
+
+#include "attn_common.cuh"
+#include "attn_sparse.cuh"
+#include "sm100_ptx.cuh"
+
+namespace attn {
+using namespace ptx;
+
+namespace {
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, uint32_t bar,
+                                            int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+// dst[0..3] += v (fp32, one 16-byte vector reduction in L2).
+__device__ __forceinline__ void red_add_v4(float* dst, float a, float b, float c, float d) {
+  asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(a),
+               "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+
+// ------------------------------------------------------------------ preprocess
+// One warp per (batch, token, head) row: Dvec = sum_k dO * (o + o_lo) and
+// -LSE*log2(e) (-inf when LSE is -inf: no filled slot), plus the zeroing of
+// dkp and dvp and of the status word by a grid-stride loop.
+__global__ void __launch_bounds__(256) attn_sparse_bwd_preprocess_kernel(
+    const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ o_lo,
+    const __nv_bfloat16* __restrict__ dO, const float* __restrict__ lse, float* __restrict__ nlse2,
+    float* __restrict__ dvec, float4* __restrict__ dkp, long long n_dkp4, float4* __restrict__ dvp,
+    long long n_dvp4, int* __restrict__ status, int B, int T, int H, int DV) {
+  const long long gt = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long nthreads = static_cast<long long>(gridDim.x) * blockDim.x;
+  if (gt == 0) *status = 0;
+  for (long long i = gt; i < n_dkp4; i += nthreads) dkp[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (long long i = gt; i < n_dvp4; i += nthreads) dvp[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  const long long rows = static_cast<long long>(B) * T * H;
+  const int lane = threadIdx.x % 32;
+  for (long long row = gt / 32; row < rows; row += nthreads / 32) {
+    const __nv_bfloat16* orow = o + row * DV;
+    const __nv_bfloat16* drow = dO + row * DV;
+    float acc = 0.f;
+    for (int k = lane; k < DV; k += 32) {
+      float ov = __bfloat162float(orow[k]);
+      if (o_lo) ov += __bfloat162float(o_lo[row * DV + k]);
+      acc = fmaf(__bfloat162float(drow[k]), ov, acc);
+    }
+#pragma unroll
+    for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+    if (lane == 0) {
+      const long long bt = row / H;
+      const int h = static_cast<int>(row % H);
+      const int b = static_cast<int>(bt / T), t = static_cast<int>(bt % T);
+      const float l = lse[(static_cast<long long>(b) * H + h) * T + t];
+      dvec[row] = acc;
+      nlse2[row] = (l == -INFINITY) ? -INFINITY : -l * kLog2e;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ main
+template <int DK, int DV>
+__global__ void __launch_bounds__(SparseBwdCfg<DK, DV>::THREADS, 1)
+    attn_sparse_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
+                           const __grid_constant__ CUtensorMap tm_do, const SparseBwdParams p) {
+  using C = SparseBwdCfg<DK, DV>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+
+  __shared__ uint64_t bar_q_full, bar_q_empty, bar_mma_done;
+  __shared__ uint64_t bar_kv_full[C::NSLOT], bar_kv_empty[C::NSLOT];
+  __shared__ uint64_t bar_sdp_full, bar_pds_full, bar_grads_full, bar_drain_done;
+  __shared__ uint32_t tmem_base_s;
+  __shared__ int abort_flag;
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const int n_items = p.B * p.T;
+  const int nch = p.n_chunks;
+  const int cta = blockIdx.x, n_cta = gridDim.x;
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(smem_u32(&bar_q_full), 1);
+    mbar_init(smem_u32(&bar_q_empty), 1);
+    mbar_init(smem_u32(&bar_mma_done), 1);
+    for (int i = 0; i < C::NSLOT; ++i) {
+      mbar_init(smem_u32(&bar_kv_full[i]), 32);
+      mbar_init(smem_u32(&bar_kv_empty[i]), 1);
+    }
+    mbar_init(smem_u32(&bar_sdp_full), 1);
+    mbar_init(smem_u32(&bar_pds_full), 128);
+    mbar_init(smem_u32(&bar_grads_full), 1);
+    mbar_init(smem_u32(&bar_drain_done), 128);
+    fence_barrier_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(&tmem_base_s), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_s;
+  const WaitCtl ctl{&abort_flag, p.status, p.timeout_ns};
+
+  const uint32_t sQ = smem_u32(smem + C::SMEM_Q);
+  const uint32_t sDO = smem_u32(smem + C::SMEM_DO);
+  const uint32_t sDsHi = smem_u32(smem + C::SMEM_DS);
+  const uint32_t sDsLo = sDsHi + C::DS_BYTES;
+  const uint32_t sRing = smem_u32(smem + C::SMEM_RING);
+  float* rows_s = reinterpret_cast<float*>(smem + C::SMEM_ROWS);  // nlse2[128], then dvec[128]
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    int* idx_s = reinterpret_cast<int*>(smem + C::SMEM_IDX);
+    if (lane == 0) {
+      prefetch_tmap(&tm_q);
+      prefetch_tmap(&tm_do);
+    }
+    int issued = 0, signalled = 0, q_loads = 0;
+    bool ok = true;
+    auto signal_oldest = [&]() {
+      fence_async_smem();
+      mbar_arrive(smem_u32(&bar_kv_full[signalled % C::NSLOT]));
+      ++signalled;
+    };
+    for (int r = 0; ok; ++r) {
+      const int item = r * n_cta + cta;
+      if (item >= n_items) break;
+      const int b = item / p.T;
+      const int* lst = p.idx + static_cast<size_t>(item) * p.K;
+      auto load_pos = [&](int pos) {
+        const int c = pos >> 1;
+        const bool is_v = pos & 1;
+        const int slot = issued % C::NSLOT, round = issued / C::NSLOT;
+        if (!is_v) {
+          __syncwarp();
+          const int s0 = c * C::BK + 4 * lane;
+          int4 e = make_int4(-1, -1, -1, -1);
+          if (s0 < p.K) e = __ldg(reinterpret_cast<const int4*>(lst + s0));
+          auto chk = [&](int x) { return (x >= 0 && x < p.P) ? x : -1; };
+          reinterpret_cast<int4*>(idx_s)[lane] = make_int4(chk(e.x), chk(e.y), chk(e.z), chk(e.w));
+          __syncwarp();
+        }
+        if (round > 0) ok = mbar_wait_warp(smem_u32(&bar_kv_empty[slot]), (round - 1) & 1, ctl);
+        if (!ok) return;
+        const uint32_t dst = sRing + slot * C::SLOT_BYTES;
+        auto gather = [&](const __nv_bfloat16* pool, auto dcols) {
+          constexpr int DC = decltype(dcols)::value;
+          constexpr int UNITS = DC / 8;
+          constexpr int RPI = 32 / UNITS;
+          const int u = lane % UNITS, jr = lane / UNITS;
+          const uint32_t ublk = (u / 8) * (C::BK * 128);
+          const __nv_bfloat16* base = pool + static_cast<size_t>(b) * p.P * DC + u * 8;
+#pragma unroll 8
+          for (int j0 = 0; j0 < C::BK; j0 += RPI) {
+            const int j = j0 + jr;
+            const int x = idx_s[j];
+            const uint32_t d = dst + ublk + j * 128 + (((u % 8) ^ (j & 7)) << 4);
+            cp_async16(d, base + static_cast<size_t>(x < 0 ? 0 : x) * DC, x < 0 ? 0u : 16u);
+          }
+        };
+        if (is_v)
+          gather(p.vp, std::integral_constant<int, DV>{});
+        else
+          gather(p.kp, std::integral_constant<int, DK>{});
+        cp_async_commit();
+        ++issued;
+        if (issued - signalled > C::COPY_DEPTH) {
+          cp_async_wait<C::COPY_DEPTH>();
+          signal_oldest();
+        }
+      };
+      // The first chunk's K and V; then every copy in flight is reported (the
+      // previous item's last products need its last positions), and Q, dO and
+      // the row vectors follow once those products are done with them.
+      const int pre = (r == 0) ? 0 : 2;
+      for (int pos = 0; pos < pre && ok; ++pos) load_pos(pos);
+      if (!ok) break;
+      cp_async_wait<0>();
+      while (signalled < issued) signal_oldest();
+      if (r > 0) ok = mbar_wait_warp(smem_u32(&bar_q_empty), (r - 1) & 1, ctl);
+      if (!ok) break;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int h = 4 * lane + k;
+        const bool in = h < p.H;
+        const size_t rr = static_cast<size_t>(item) * p.H + h;
+        // Heads past H (the next token's rows, or zeros) get P = 0 and dS = 0.
+        rows_s[h] = in ? p.nlse2[rr] : -INFINITY;
+        rows_s[C::BQ + h] = in ? p.dvec[rr] : 0.f;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive_expect_tx(smem_u32(&bar_q_full), C::Q_BYTES + C::DO_BYTES);
+        for (int cb = 0; cb < C::KCH; ++cb)
+          tma_load_2d(sQ + cb * (C::BQ * 128), &tm_q, smem_u32(&bar_q_full), cb * 64, item * p.H);
+        for (int cb = 0; cb < C::VCH; ++cb)
+          tma_load_2d(sDO + cb * (C::BQ * 128), &tm_do, smem_u32(&bar_q_full), cb * 64, item * p.H);
+      }
+      __syncwarp();
+      ++q_loads;
+      for (int pos = pre; pos < 2 * nch && ok; ++pos) load_pos(pos);
+    }
+    cp_async_wait<0>();
+    while (signalled < issued) signal_oldest();
+    if (lane == 0 && q_loads > 0)
+      mbar_wait_drain(smem_u32(&bar_q_full), (q_loads - 1) & 1, 50000000ull);
+    __syncwarp();
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    bool ok = !p.inject_stall;
+    constexpr uint32_t idesc_sdp = idesc_bf16_f32(128, 128, 0, 0);  // K-major A and B
+    constexpr uint32_t idesc_dv = idesc_bf16_f32(128, DV, 0, 1);    // B = dO, MN-major
+    constexpr uint32_t idesc_dk = idesc_bf16_f32(128, DK, 0, 1);    // B = Q, MN-major
+    constexpr uint32_t idesc_dq = idesc_bf16_f32(128, 128, 1, 1);   // A = K^T, B = dS^T, MN-major
+    const uint64_t dq_k = sw128_desc(sQ, 16, 1024);
+    const uint64_t ddo_k = sw128_desc(sDO, 16, 1024);
+    const uint64_t dq_mn = sw128_desc(sQ, C::BQ * 128, 1024);
+    const uint64_t ddo_mn = sw128_desc(sDO, C::BQ * 128, 1024);
+    const uint64_t dds_hi = sw128_desc(sDsHi, C::BK * 128, 1024);
+    const uint64_t dds_lo = sw128_desc(sDsLo, C::BK * 128, 1024);
+    auto add = [](uint64_t d, uint32_t bytes) { return d + (bytes >> 4); };
+    int ring = 0, chunk = 0;  // ring position and chunk count, over all items
+    for (int r = 0; ok; ++r) {
+      const int item = r * n_cta + cta;
+      if (item >= n_items) break;
+      ok = mbar_wait_warp(smem_u32(&bar_q_full), r & 1, ctl);
+      if (!ok) break;
+      for (int c = 0; c < nch && ok; ++c, ++chunk) {
+        const int pk = ring + 2 * c, pv = pk + 1;
+        const int sk = pk % C::NSLOT, sv = pv % C::NSLOT;
+        // S^T / P^T / dK columns and dV's are free once the compute warps have
+        // drained the previous chunk.
+        if (chunk > 0) ok = mbar_wait_warp(smem_u32(&bar_drain_done), (chunk - 1) & 1, ctl);
+        if (ok) ok = mbar_wait_warp(smem_u32(&bar_kv_full[sk]), (pk / C::NSLOT) & 1, ctl);
+        if (ok) ok = mbar_wait_warp(smem_u32(&bar_kv_full[sv]), (pv / C::NSLOT) & 1, ctl);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t kb = sRing + sk * C::SLOT_BYTES, vb = sRing + sv * C::SLOT_BYTES;
+        const uint64_t dk_k = sw128_desc(kb, 16, 1024), dv_k = sw128_desc(vb, 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < DK / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * (128 * 128) + (kk & 3) * 32;
+          mma_ss_el(tmem + C::TM_S, add(dk_k, off), add(dq_k, off), idesc_sdp, kk > 0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < DV / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * (128 * 128) + (kk & 3) * 32;
+          mma_ss_el(tmem + C::TM_DP, add(dv_k, off), add(ddo_k, off), idesc_sdp, kk > 0);
+        }
+        mma_commit_el(smem_u32(&bar_sdp_full));
+        mma_commit_el(smem_u32(&bar_kv_empty[sv]));  // V_c is not read again
+        ok = mbar_wait_warp(smem_u32(&bar_pds_full), chunk & 1, ctl);
+        if (!ok) break;
+        tc_fence_after();
+        // dV_c = P^T dO and dK_c = dS^T Q: heads 16kk..16kk+15 are TMEM columns
+        // 16kk..16kk+7 (hi pairs) and 16kk+8..16kk+15 (lo pairs). dK_c goes into
+        // the S^T columns, which dV_c above has read (MMAs run in issue order).
+#pragma unroll
+        for (int kk = 0; kk < C::BQ / 16; ++kk) {
+          const uint32_t acc = kk > 0 ? 1u : 0u;
+          mma_ts_el(tmem + C::TM_DV, tmem + C::TM_S + 16 * kk, add(ddo_mn, kk * 2048), idesc_dv, acc);
+          mma_ts_el(tmem + C::TM_DV, tmem + C::TM_S + 16 * kk + 8, add(ddo_mn, kk * 2048), idesc_dv, 1u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < C::BQ / 16; ++kk) {
+          const uint32_t acc = kk > 0 ? 1u : 0u;
+          mma_ts_el(tmem + C::TM_S, tmem + C::TM_DP + 16 * kk, add(dq_mn, kk * 2048), idesc_dk, acc);
+          mma_ts_el(tmem + C::TM_S, tmem + C::TM_DP + 16 * kk + 8, add(dq_mn, kk * 2048), idesc_dk, 1u);
+        }
+        // dQ^T[d][h] += sum over slots of K_c[slot][d] (dS_hi + dS_lo)^T[slot][h].
+        const uint64_t dk_mn = sw128_desc(kb, C::BK * 128, 1024);
+#pragma unroll
+        for (int kk = 0; kk < C::BK / 16; ++kk) {
+          const uint32_t acc = (c > 0 || kk > 0) ? 1u : 0u;
+          mma_ss_el(tmem + C::TM_DQ, add(dk_mn, kk * 2048), add(dds_hi, kk * 2048), idesc_dq, acc);
+          mma_ss_el(tmem + C::TM_DQ, add(dk_mn, kk * 2048), add(dds_lo, kk * 2048), idesc_dq, 1u);
+        }
+        mma_commit_el(smem_u32(&bar_grads_full));
+        mma_commit_el(smem_u32(&bar_kv_empty[sk]));  // K_c is not read again
+        if (c + 1 == nch) mma_commit_el(smem_u32(&bar_q_empty));
+      }
+      ring += 2 * nch;
+    }
+    mma_commit_el(smem_u32(&bar_mma_done));
+    mbar_wait_drain(smem_u32(&bar_mma_done), 0, 50000000ull);
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ compute warps 0-3
+    const int j = threadIdx.x;  // slot within the chunk == TMEM lane (later: head-dim index)
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const float sl2 = p.scale_log2, scale = p.scale;
+    const float* nlse2_s = rows_s;
+    const float* dvec_s = rows_s + C::BQ;
+    bool ok = true;
+    int chunk = 0;
+    for (int r = 0; ok; ++r) {
+      const int item = r * n_cta + cta;
+      if (item >= n_items) break;
+      const int b = item / p.T;
+      const int* lst = p.idx + static_cast<size_t>(item) * p.K;
+      ok = mbar_wait_warp(smem_u32(&bar_q_full), r & 1, ctl);  // the row vectors are in
+      if (!ok) break;
+      for (int c = 0; c < nch && ok; ++c, ++chunk) {
+        const int s = c * C::BK + j;
+        const int e = s < p.K ? __ldg(lst + s) : -1;
+        const bool filled = e >= 0 && e < p.P;
+        ok = mbar_wait_warp(smem_u32(&bar_sdp_full), chunk & 1, ctl);
+        if (!ok) break;
+        tc_fence_after();
+        // Row j of S^T and dP^T, 16 heads at a time: P^T and scale * dS^T as
+        // bf16 hi/lo pairs into TMEM over the scores, and dS^T into shared
+        // memory (row j of the MN-major B operand of dQ^T: heads 0..63 in the
+        // first 64-column block, 64..127 in the second, 128-byte swizzle).
+#pragma unroll 1
+        for (int h0 = 0; h0 < C::BQ; h0 += 16) {
+          uint32_t su[16], du[16];
+          tmem_ld16(tmem + lane_base + C::TM_S + h0, su);
+          tmem_ld16(tmem + lane_base + C::TM_DP + h0, du);
+          tmem_wait_ld();
+          uint32_t pp[16], dd[16];
+#pragma unroll
+          for (int k = 0; k < 16; k += 2) {
+            float p0 = ex2(fmaf(__uint_as_float(su[k]), sl2, nlse2_s[h0 + k]));
+            float p1 = ex2(fmaf(__uint_as_float(su[k + 1]), sl2, nlse2_s[h0 + k + 1]));
+            if (!filled) p0 = p1 = 0.f;
+            const float d0 = p0 * (__uint_as_float(du[k]) - dvec_s[h0 + k]) * scale;
+            const float d1 = p1 * (__uint_as_float(du[k + 1]) - dvec_s[h0 + k + 1]) * scale;
+            split_bf16x2(p0, p1, pp[k / 2], pp[8 + k / 2]);
+            split_bf16x2(d0, d1, dd[k / 2], dd[8 + k / 2]);
+          }
+          tmem_st16(tmem + lane_base + C::TM_S + h0, pp);
+          tmem_st16(tmem + lane_base + C::TM_DP + h0, dd);
+          // Heads h0..h0+15: two 16-byte units of row j in block h0 / 64.
+          const uint32_t blk = (h0 / 64) * (C::BK * 128) + j * 128;
+          const int u0 = (h0 % 64) / 8;
+#pragma unroll
+          for (int q2 = 0; q2 < 2; ++q2) {
+            const uint32_t off = blk + (((u0 + q2) ^ (j & 7)) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(sDsHi + off),
+                         "r"(dd[4 * q2]), "r"(dd[4 * q2 + 1]), "r"(dd[4 * q2 + 2]), "r"(dd[4 * q2 + 3])
+                         : "memory");
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(sDsLo + off),
+                         "r"(dd[8 + 4 * q2]), "r"(dd[8 + 4 * q2 + 1]), "r"(dd[8 + 4 * q2 + 2]),
+                         "r"(dd[8 + 4 * q2 + 3])
+                         : "memory");
+          }
+        }
+        tmem_wait_st();
+        fence_async_smem();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bar_pds_full));
+        // The chunk's products are done: add row j of dV_c and dK_c into the
+        // pool gradients of pool row e.
+        ok = mbar_wait_warp(smem_u32(&bar_grads_full), chunk & 1, ctl);
+        if (!ok) break;
+        tc_fence_after();
+        auto drain = [&](uint32_t col, float* dst_row, auto dcols) {
+          constexpr int DC = decltype(dcols)::value;
+#pragma unroll 1
+          for (int k0 = 0; k0 < DC; k0 += 32) {
+            uint32_t u[32];
+            tmem_ld32(tmem + lane_base + col + k0, u);
+            tmem_wait_ld();
+            if (filled) {
+#pragma unroll
+              for (int k = 0; k < 32; k += 4)
+                red_add_v4(dst_row + k0 + k, __uint_as_float(u[k]), __uint_as_float(u[k + 1]),
+                           __uint_as_float(u[k + 2]), __uint_as_float(u[k + 3]));
+            }
+          }
+        };
+        const size_t prow = static_cast<size_t>(b) * p.P + (filled ? e : 0);
+        drain(C::TM_DV, p.dvp + prow * DV, std::integral_constant<int, DV>{});
+        drain(C::TM_S, p.dkp + prow * DK, std::integral_constant<int, DK>{});
+        if (c + 1 == nch) {
+          // dQ^T is complete for this token: thread j < DK writes column j of
+          // dq for every head (row j of dQ^T). j < DK is warp-uniform.
+          if (j < DK) {
+            float* dqb = p.dq + static_cast<size_t>(item) * p.H * DK + j;
+#pragma unroll 1
+            for (int h0 = 0; h0 < C::BQ; h0 += 32) {
+              uint32_t u[32];
+              tmem_ld32(tmem + lane_base + C::TM_DQ + h0, u);
+              tmem_wait_ld();
+#pragma unroll
+              for (int k = 0; k < 32; ++k)
+                if (h0 + k < p.H) dqb[static_cast<size_t>(h0 + k) * DK] = __uint_as_float(u[k]);
+            }
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bar_drain_done));
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+template <int DK, int DV>
+cudaError_t launch_sparse_bwd_t(const CUtensorMap& tq, const CUtensorMap& tdo,
+                                const SparseBwdParams& p, cudaStream_t stream) {
+  using C = SparseBwdCfg<DK, DV>;
+  static bool attr_set[64] = {};
+  static int sm_count[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(attn_sparse_bwd_kernel<DK, DV>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM_ALLOC);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  if (dev < 64 && sm_count[dev] == 0)
+    cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
+  const long long n_items = static_cast<long long>(p.B) * p.T;
+  const int sms = (dev < 64 && sm_count[dev] > 0) ? sm_count[dev] : 148;
+  const dim3 grid(static_cast<unsigned>(n_items < sms ? n_items : sms));
+  attn_sparse_bwd_kernel<DK, DV><<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(tq, tdo, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_sparse_bwd(int DK, int DV, const __nv_bfloat16* o, const __nv_bfloat16* o_lo,
+                              const __nv_bfloat16* dO, const float* lse, float* nlse2, float* dvec,
+                              const CUtensorMap& tq, const CUtensorMap& tdo,
+                              const SparseBwdParams& p, cudaStream_t stream) {
+  const long long n_dkp4 = static_cast<long long>(p.B) * p.P * DK / 4;
+  const long long n_dvp4 = static_cast<long long>(p.B) * p.P * DV / 4;
+  attn_sparse_bwd_preprocess_kernel<<<1024, 256, 0, stream>>>(
+      o, o_lo, dO, lse, nlse2, dvec, reinterpret_cast<float4*>(p.dkp), n_dkp4,
+      reinterpret_cast<float4*>(p.dvp), n_dvp4, p.status, p.B, p.T, p.H, DV);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (DK == 128 && DV == 128) return launch_sparse_bwd_t<128, 128>(tq, tdo, p, stream);
+  if (DK == 128 && DV == 64) return launch_sparse_bwd_t<128, 64>(tq, tdo, p, stream);
+  if (DK == 64 && DV == 128) return launch_sparse_bwd_t<64, 128>(tq, tdo, p, stream);
+  if (DK == 64 && DV == 64) return launch_sparse_bwd_t<64, 64>(tq, tdo, p, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace attn

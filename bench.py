@@ -337,6 +337,159 @@ def run_ours(args, w, world, rank, local):
     return 0
 
 
+# ---------------------------------------------------------------------------
+# Sparse top-k gather attention (forward), on its own workloads.
+# ---------------------------------------------------------------------------
+SPARSE_METRIC = "sparse top-k gather attention forward TFLOP/s over filled slots at 1 GB300"
+
+
+def sparse_flops(w, idx):
+    """2 * H * (DK + DV) per filled (token, slot): the scores and the P.V product."""
+    return 2.0 * w.H * (w.DK + w.DV) * float((idx >= 0).sum())
+
+
+def sparse_oracle_sample(w, q, kp, vp, idx, budget_s=12.0):
+    """Time the sparse oracle's forward over tokens of batch 0 (from the last,
+    the longest lists, down) until `budget_s` has passed."""
+    from oracle.sparse import sparse_ref_tokens_fwd
+    f64 = lambda t: t.double().numpy()
+    qn, kn, vn, ix = f64(q[:1]), f64(kp[:1]), f64(vp[:1]), idx[:1].numpy()
+    done, flops, t0 = 0, 0.0, time.perf_counter()
+    for t in range(w.T - 1, -1, -1):
+        sparse_ref_tokens_fwd(qn, kn, vn, ix, w.scale, 0, [t])
+        flops += 2.0 * w.H * (w.DK + w.DV) * float((ix[0, t] >= 0).sum())
+        done += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    secs = time.perf_counter() - t0
+    return flops / secs, f"{done} of {w.B * w.T} tokens (the last ones of batch 0, full lists)", secs
+
+
+def run_sparse(args, w, world, rank, local):
+    import torch
+    import attention_fwd_bwd_gb300 as attn
+    from attention_fwd_bwd_gb300._build import build
+    from attention_fwd_bwd_gb300.inputs import make_sparse_inputs
+
+    q_h, kp_h, vp_h, _, idx_h = make_sparse_inputs(w)
+    flops = sparse_flops(w, idx_h)
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        rates, secs, sample = [], 0.0, ""
+        for i in range(args.warmup + args.steps):
+            r, sample, sc = sparse_oracle_sample(w, q_h, kp_h, vp_h, idx_h, budget_s=args.ref_budget / 4)
+            if i >= args.warmup:
+                rates.append(r)
+                secs += sc
+        value = statistics.mean(rates) / 1e12
+        print(json.dumps({
+            "impl": "reference", "metric": SPARSE_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / max(1, args.steps),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded CSA-shaped top-k lists, N(0,1) bf16 tensors)",
+            "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "DK": w.DK, "DV": w.DV, "K": w.K,
+                       "parallelism": "replicas"},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+                             "sample": f"per step: {sample}"},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+            flush=True)
+        return 0
+
+    build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    attn.lib()
+    q, kp, vp, idx = (t.to(dev) for t in (q_h, kp_h, vp_h, idx_h))
+    o = torch.empty(w.B, w.T, w.H, w.DV, dtype=torch.bfloat16, device=dev)
+    o_lo = torch.empty_like(o)
+    lse = torch.empty(w.B, w.H, w.T, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        attn.attn_sparse_fwd(q, kp, vp, idx, o, lse, w.scale, o_lo=o_lo, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if attn.attn_check_status(None) != 0:
+        raise RuntimeError("kernel pipeline timeout during warm-up")
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        start.record(stream)
+        for _ in range(args.steps):
+            step()
+        stop.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    if attn.attn_check_status(None) != 0:
+        raise RuntimeError("kernel pipeline timeout during the timed steps")
+    ms = reduce_max(start.elapsed_time(stop), world) / args.steps
+    value = whole_job_value(flops, ms / 1e3, world) / 1e12
+
+    pin = lambda t: t.pin_memory()
+    hq_, hk_, hv_, hi_ = (pin(t) for t in (q_h, kp_h, vp_h, idx_h))
+    ho, hlo, hlse = (pin(torch.empty(t.shape, dtype=t.dtype)) for t in (o, o_lo, lse))
+    h2d = sum(t.numel() * t.element_size() for t in (hq_, hk_, hv_, hi_))
+    d2h = sum(t.numel() * t.element_size() for t in (ho, hlo, hlse))
+
+    def e2e_step():
+        for dst, src in ((q, hq_), (kp, hk_), (vp, hv_), (idx, hi_)):
+            dst.copy_(src, non_blocking=True)
+        step()
+        for dst, src in ((ho, o), (hlo, o_lo), (hlse, lse)):
+            dst.copy_(src, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e_steps = max(1, min(args.steps, 10))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max(e0.elapsed_time(e1), world) / e_steps
+
+    peaks, peak_src = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    tf = flops / (ms / 1e3) / 1e12
+    gathered = w.B * w.T * w.K * (w.DK + w.DV) * 2
+    if rank == 0:
+        line = {
+            "metric": SPARSE_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded CSA-shaped top-k lists, N(0,1) bf16 tensors)",
+            "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "P": w.P, "K": w.K, "DK": w.DK,
+                       "DV": w.DV, "window": w.window, "topk": w.topk, "ratio": w.ratio,
+                       "parallelism": f"replicas x{world}",
+                       "l2": "no flush: q and o (1 GB and more) exceed the 129 MB L2; the pool is L2-resident",
+                       "flops_per_step": flops},
+            "gpu_launches": args.steps,
+            "passes": {"sparse_fwd": {"ms": ms, "tflops": tf, "frac_of_peak": tf / peak,
+                                      "gathered_gbs": gathered / (ms / 1e3) / 1e9}},
+            "roofline": {"kernel": "attn_sparse_fwd_kernel", "bound": "tensor", "achieved": tf, "peak": peak,
+                         "unit": "TFLOP/s", "frac": tf / peak, "traffic": None,
+                         "peak_source": f"{peak_src} bf16_tflops (burst)"},
+            "clocks": clocks.summary(),
+            "e2e": {"value": whole_job_value(flops, e2e_ms / 1e3, world) / 1e12, "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        }
+        if not args.no_cpu_baseline:
+            rate, sample, secs = sparse_oracle_sample(w, q_h, kp_h, vp_h, idx_h, budget_s=args.ref_budget)
+            line["cpu_baseline"] = {"value": rate / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+                                    "sample": f"{sample}; {secs:.1f} s"}
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -349,8 +502,9 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
-    from attention_fwd_bwd_gb300.inputs import BY_NAME
-    w = BY_NAME[args.workload]
+    from attention_fwd_bwd_gb300.inputs import BY_NAME, SPARSE_BY_NAME
+    sparse = args.workload in SPARSE_BY_NAME
+    w = SPARSE_BY_NAME[args.workload] if sparse else BY_NAME[args.workload]
     world, rank, local = dist_env()
     if world > 1:
         import torch
@@ -360,6 +514,8 @@ def main():
             torch.cuda.set_device(local)
         dist.init_process_group(backend=backend)
     try:
+        if sparse:
+            return run_sparse(args, w, world, rank, local)
         if args.impl == "reference":
             return run_reference(args, w, world, rank)
         return run_ours(args, w, world, rank, local)

@@ -238,6 +238,37 @@ attn_status_t attn_sparse_fwd(const void* q, const void* kp, const void* vp, con
                               void* o, void* o_lo, float* lse, int B, int T, int H, int P, int K,
                               int DK, int DV, float scale, void* stream);
 
+/*
+ * Sparse top-k gather attention, backward (same pages, section 2.1: the
+ * backward gathers the listed vectors again for dQ and reduces a per-slot
+ * dK/dV intermediate through the inverse of the top-k map).
+ *
+ * The exact gradient of sum(dO * O) for attn_sparse_fwd's O:
+ *   dq  [B, T, H, DK] fp32 (out): scale * sum_j dS[h, j] kp[idx_j]
+ *   dkp [B, P, DK] fp32 (out): for each pool row, the sum over every
+ *       (token, slot) naming it of scale * sum_h dS[h, j] q[h]
+ *   dvp [B, P, DV] fp32 (out): likewise of sum_h P[h, j] dO[h]
+ * with P the forward's probabilities (recomputed from q, kp, vp and lse),
+ * dS = P * (dP - Dvec), dP = dO vp^T, Dvec = rowsum(dO * O).
+ * o [B, T, H, DV] bf16 and lse [B, H, T] are attn_sparse_fwd's outputs; o_lo
+ * (optional, NULL to skip) its residual, which makes Dvec exact to about 16
+ * bits; dO [B, T, H, DV] bf16. Empty slots and tokens without a filled slot
+ * contribute nothing. Sizes, layouts and the other arguments are those of
+ * attn_sparse_fwd. dkp and dvp are overwritten (zeroed, then accumulated);
+ * repeated rows accumulate every occurrence.
+ * workspace: device memory, 256-byte aligned, of at least
+ * attn_sparse_bwd_workspace_size(B, T, H) bytes, owned by the caller; it also
+ * holds the status word that attn_check_status(workspace) reads.
+ * Errors: those of attn_sparse_fwd, and ATTN_ERR_WORKSPACE for a missing,
+ * misaligned or small workspace.
+ */
+size_t attn_sparse_bwd_workspace_size(int B, int T, int H);
+attn_status_t attn_sparse_bwd(const void* q, const void* kp, const void* vp, const int* idx,
+                              const void* o, const void* o_lo, const void* dO, const float* lse,
+                              float* dq, float* dkp, float* dvp, int B, int T, int H, int P, int K,
+                              int DK, int DV, float scale, void* workspace, size_t workspace_bytes,
+                              void* stream);
+
 /* Static, human-readable name of a status code. */
 const char* attn_status_string(attn_status_t status);
 

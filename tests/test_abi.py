@@ -102,6 +102,21 @@ def test_sparse_argument_validation(L):
     assert fwd(ptrs=[FAKE, FAKE, FAKE, FAKE + 4, FAKE, None, FAKE]) == 1  # misaligned idx
 
 
+def test_sparse_bwd_argument_validation(L):
+    def bwd(B=1, T=4, H=128, P=10, K=8, DK=128, DV=64, ws=FAKE * 16, wsb=1 << 30, ptrs=None):
+        p = ptrs if ptrs is not None else [FAKE] * 5 + [None] + [FAKE] * 5
+        return L.attn_sparse_bwd(*p, B, T, H, P, K, DK, DV, 0.1, ws, wsb, None)
+    assert bwd(H=200) == 1
+    assert bwd(K=5) == 1
+    assert bwd(DK=32) == 2
+    assert bwd(ws=None) == 5                  # workspace missing
+    assert bwd(ws=FAKE * 16 + 16) == 5        # not 256-byte aligned
+    assert bwd(wsb=16) == 5                   # too small
+    assert bwd(B=0, ptrs=[None] * 11) == 0
+    assert L.attn_sparse_bwd_workspace_size(1, 4, 128) == 256 + 2 * 2048
+    assert L.attn_sparse_bwd_workspace_size(1, 4, 0) == 0
+
+
 def test_bwd_argument_validation(L):
     def bwd(ws=FAKE * 16, wsb=1 << 30, B=1, S=128, D=64, ptrs=None, Hq=2, Hkv=1):
         p = ptrs if ptrs is not None else [FAKE] * 9 + [None]

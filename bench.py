@@ -340,24 +340,26 @@ def run_ours(args, w, world, rank, local):
 # ---------------------------------------------------------------------------
 # Sparse top-k gather attention (forward), on its own workloads.
 # ---------------------------------------------------------------------------
-SPARSE_METRIC = "sparse top-k gather attention forward TFLOP/s over filled slots at 1 GB300"
+SPARSE_METRIC = "sparse top-k gather attention fwd+bwd TFLOP/s over filled slots at 1 GB300"
 
 
 def sparse_flops(w, idx):
-    """2 * H * (DK + DV) per filled (token, slot): the scores and the P.V product."""
+    """Forward: 2 * H * (DK + DV) per filled (token, slot), the scores and the
+    P.V product; the backward counts 2.5 times that (the dense convention)."""
     return 2.0 * w.H * (w.DK + w.DV) * float((idx >= 0).sum())
 
 
-def sparse_oracle_sample(w, q, kp, vp, idx, budget_s=12.0):
-    """Time the sparse oracle's forward over tokens of batch 0 (from the last,
-    the longest lists, down) until `budget_s` has passed."""
-    from oracle.sparse import sparse_ref_tokens_fwd
+def sparse_oracle_sample(w, q, kp, vp, idx, do, budget_s=12.0):
+    """Time the sparse oracle's forward and backward over tokens of batch 0
+    (from the last, the longest lists, down) until `budget_s` has passed."""
+    from oracle.sparse import sparse_ref_bwd, sparse_ref_tokens_fwd
     f64 = lambda t: t.double().numpy()
-    qn, kn, vn, ix = f64(q[:1]), f64(kp[:1]), f64(vp[:1]), idx[:1].numpy()
+    qn, kn, vn, dn, ix = f64(q[:1]), f64(kp[:1]), f64(vp[:1]), f64(do[:1]), idx[:1].numpy()
     done, flops, t0 = 0, 0.0, time.perf_counter()
     for t in range(w.T - 1, -1, -1):
         sparse_ref_tokens_fwd(qn, kn, vn, ix, w.scale, 0, [t])
-        flops += 2.0 * w.H * (w.DK + w.DV) * float((ix[0, t] >= 0).sum())
+        sparse_ref_bwd(qn[:, t:t + 1], kn, vn, ix[:, t:t + 1], dn[:, t:t + 1], w.scale)
+        flops += 3.5 * 2.0 * w.H * (w.DK + w.DV) * float((ix[0, t] >= 0).sum())
         done += 1
         if time.perf_counter() - t0 >= budget_s:
             break
@@ -371,14 +373,15 @@ def run_sparse(args, w, world, rank, local):
     from attention_fwd_bwd_gb300._build import build
     from attention_fwd_bwd_gb300.inputs import make_sparse_inputs
 
-    q_h, kp_h, vp_h, _, idx_h = make_sparse_inputs(w)
-    flops = sparse_flops(w, idx_h)
+    q_h, kp_h, vp_h, do_h, idx_h = make_sparse_inputs(w)
+    fwd_flops = sparse_flops(w, idx_h)
+    flops = 3.5 * fwd_flops
     if args.impl == "reference":
         if rank != 0:
             return 0
         rates, secs, sample = [], 0.0, ""
         for i in range(args.warmup + args.steps):
-            r, sample, sc = sparse_oracle_sample(w, q_h, kp_h, vp_h, idx_h, budget_s=args.ref_budget / 4)
+            r, sample, sc = sparse_oracle_sample(w, q_h, kp_h, vp_h, idx_h, do_h, budget_s=args.ref_budget / 4)
             if i >= args.warmup:
                 rates.append(r)
                 secs += sc
@@ -400,20 +403,32 @@ def run_sparse(args, w, world, rank, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     attn.lib()
-    q, kp, vp, idx = (t.to(dev) for t in (q_h, kp_h, vp_h, idx_h))
+    q, kp, vp, do, idx = (t.to(dev) for t in (q_h, kp_h, vp_h, do_h, idx_h))
     o = torch.empty(w.B, w.T, w.H, w.DV, dtype=torch.bfloat16, device=dev)
     o_lo = torch.empty_like(o)
     lse = torch.empty(w.B, w.H, w.T, dtype=torch.float32, device=dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    dq = torch.empty(w.B, w.T, w.H, w.DK, **f32)
+    dkp, dvp = torch.empty(w.B, w.P, w.DK, **f32), torch.empty(w.B, w.P, w.DV, **f32)
+    ws = torch.empty(attn.attn_sparse_bwd_workspace_size(w.B, w.T, w.H), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
-    def step():
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
         attn.attn_sparse_fwd(q, kp, vp, idx, o, lse, w.scale, o_lo=o_lo, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        attn.attn_sparse_bwd(q, kp, vp, idx, o, do, lse, dq, dkp, dvp, w.scale, ws, o_lo=o_lo, stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
-    if attn.attn_check_status(None) != 0:
+    if attn.attn_check_status(ws) != 0:
         raise RuntimeError("kernel pipeline timeout during warm-up")
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         import torch.distributed as dist
@@ -421,28 +436,30 @@ def run_sparse(args, w, world, rank, local):
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
         start.record(stream)
-        for _ in range(args.steps):
-            step()
+        for i in range(args.steps):
+            step(evs[i])
         stop.record(stream)
         torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    if attn.attn_check_status(None) != 0:
+    if attn.attn_check_status(ws) != 0:
         raise RuntimeError("kernel pipeline timeout during the timed steps")
     ms = reduce_max(start.elapsed_time(stop), world) / args.steps
+    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
     value = whole_job_value(flops, ms / 1e3, world) / 1e12
 
     pin = lambda t: t.pin_memory()
-    hq_, hk_, hv_, hi_ = (pin(t) for t in (q_h, kp_h, vp_h, idx_h))
-    ho, hlo, hlse = (pin(torch.empty(t.shape, dtype=t.dtype)) for t in (o, o_lo, lse))
-    h2d = sum(t.numel() * t.element_size() for t in (hq_, hk_, hv_, hi_))
-    d2h = sum(t.numel() * t.element_size() for t in (ho, hlo, hlse))
+    hq_, hk_, hv_, hd_, hi_ = (pin(t) for t in (q_h, kp_h, vp_h, do_h, idx_h))
+    ho, hlse, hdq, hdk, hdv = (pin(torch.empty(t.shape, dtype=t.dtype)) for t in (o, lse, dq, dkp, dvp))
+    h2d = sum(t.numel() * t.element_size() for t in (hq_, hk_, hv_, hd_, hi_))
+    d2h = sum(t.numel() * t.element_size() for t in (ho, hlse, hdq, hdk, hdv))
 
     def e2e_step():
-        for dst, src in ((q, hq_), (kp, hk_), (vp, hv_), (idx, hi_)):
+        for dst, src in ((q, hq_), (kp, hk_), (vp, hv_), (do, hd_), (idx, hi_)):
             dst.copy_(src, non_blocking=True)
         step()
-        for dst, src in ((ho, o), (hlo, o_lo), (hlse, lse)):
+        for dst, src in ((ho, o), (hlse, lse), (hdq, dq), (hdk, dkp), (hdv, dvp)):
             dst.copy_(src, non_blocking=True)
 
     for _ in range(2):
@@ -459,7 +476,8 @@ def run_sparse(args, w, world, rank, local):
 
     peaks, peak_src = load_peaks()
     peak = float(peaks["bf16_tflops"])
-    tf = flops / (ms / 1e3) / 1e12
+    fwd_tf = fwd_flops / (fwd_ms / 1e3) / 1e12
+    bwd_tf = 2.5 * fwd_flops / (bwd_ms / 1e3) / 1e12
     gathered = w.B * w.T * w.K * (w.DK + w.DV) * 2
     if rank == 0:
         line = {
@@ -472,18 +490,20 @@ def run_sparse(args, w, world, rank, local):
                        "parallelism": f"replicas x{world}",
                        "l2": "no flush: q and o (1 GB and more) exceed the 129 MB L2; the pool is L2-resident",
                        "flops_per_step": flops},
-            "gpu_launches": args.steps,
-            "passes": {"sparse_fwd": {"ms": ms, "tflops": tf, "frac_of_peak": tf / peak,
-                                      "gathered_gbs": gathered / (ms / 1e3) / 1e9}},
-            "roofline": {"kernel": "attn_sparse_fwd_kernel", "bound": "tensor", "achieved": tf, "peak": peak,
-                         "unit": "TFLOP/s", "frac": tf / peak, "traffic": None,
+            "gpu_launches": 3 * args.steps,
+            "passes": {"sparse_fwd": {"ms": fwd_ms, "tflops": fwd_tf, "frac_of_peak": fwd_tf / peak,
+                                      "gathered_gbs": gathered / (fwd_ms / 1e3) / 1e9},
+                       "sparse_bwd": {"ms": bwd_ms, "tflops": bwd_tf, "frac_of_peak": bwd_tf / peak,
+                                      "gathered_gbs": gathered / (bwd_ms / 1e3) / 1e9}},
+            "roofline": {"kernel": "attn_sparse_bwd_kernel", "bound": "tensor", "achieved": bwd_tf, "peak": peak,
+                         "unit": "TFLOP/s", "frac": bwd_tf / peak, "traffic": None,
                          "peak_source": f"{peak_src} bf16_tflops (burst)"},
             "clocks": clocks.summary(),
             "e2e": {"value": whole_job_value(flops, e2e_ms / 1e3, world) / 1e12, "unit": "TFLOP/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         }
         if not args.no_cpu_baseline:
-            rate, sample, secs = sparse_oracle_sample(w, q_h, kp_h, vp_h, idx_h, budget_s=args.ref_budget)
+            rate, sample, secs = sparse_oracle_sample(w, q_h, kp_h, vp_h, idx_h, do_h, budget_s=args.ref_budget)
             line["cpu_baseline"] = {"value": rate / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
                                     "sample": f"{sample}; {secs:.1f} s"}
         print(json.dumps(line), flush=True)

@@ -108,9 +108,14 @@ struct SparseBwdCfg {
   static constexpr int SMEM_IDX = SMEM_ROWS + ROWS_BYTES;
   static constexpr int SMEM_BYTES = SMEM_IDX + IDX_BYTES;
   static constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;
-  // Releasing K_c's position needs V_c's (the dQ^T product that frees K_c
-  // follows dP^T), so copies in flight stay below NSLOT - 1 positions.
-  static constexpr int COPY_DEPTH = NSLOT - 2;
+  // Slots NSLOT - 1 hold V chunks (one slot: V_c is free again after dP^T(c),
+  // early in chunk c), the others K chunks in turn (K_c is read until dQ^T(c),
+  // at the end of chunk c). So V_{c+1} and K_{c+1} both load while chunk c is
+  // processed. The producer keeps one position's copies in flight: releasing
+  // V_c needs K_c and V_c reported, releasing K_c needs V_c.
+  static constexpr int KSLOTS = NSLOT - 1;
+  static constexpr int VSLOT = NSLOT - 1;
+  static constexpr int COPY_DEPTH = 1;
   // TMEM columns: S^T (then P^T, then dK_c), dP^T (then dS^T), dV_c, dQ^T.
   static constexpr int TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DQ = 384;
   static constexpr int TMEM_COLS = 512;

@@ -13,8 +13,8 @@
 //      and zeroed dkp / dvp (HBM-bound).
 //   2. main, one persistent CTA per SM over (batch, token) items:
 //      warp 4 (producer): the token's Q and dO rows (TMA tiles) and row
-//          vectors, then each chunk's K and V rows gathered with cp.async into
-//          a ring (as in the forward).
+//          vectors, then each chunk's K and V rows gathered with cp.async (as
+//          in the forward) into K slots used in turn and one V slot.
 //      warp 5 (MMA issuer), per chunk c: S^T = K_c Q^T and dP^T = V_c dO^T
 //          (slot-major: TMEM lane = slot), then dV_c = P^T dO and
 //          dK_c = dS^T Q with A from TMEM, and dQ^T += K_c^T dS^T with dS^T
@@ -161,10 +161,11 @@ __global__ void __launch_bounds__(SparseBwdCfg<DK, DV>::THREADS, 1)
       prefetch_tmap(&tm_do);
     }
     int issued = 0, signalled = 0, q_loads = 0;
+    int pend[4];  // slot of each position not yet reported (at most COPY_DEPTH + 1)
     bool ok = true;
     auto signal_oldest = [&]() {
       fence_async_smem();
-      mbar_arrive(smem_u32(&bar_kv_full[signalled % C::NSLOT]));
+      mbar_arrive(smem_u32(&bar_kv_full[pend[signalled & 3]]));
       ++signalled;
     };
     for (int r = 0; ok; ++r) {
@@ -175,7 +176,9 @@ __global__ void __launch_bounds__(SparseBwdCfg<DK, DV>::THREADS, 1)
       auto load_pos = [&](int pos) {
         const int c = pos >> 1;
         const bool is_v = pos & 1;
-        const int slot = issued % C::NSLOT, round = issued / C::NSLOT;
+        const int gc = r * nch + c;  // chunk index over this CTA's items
+        const int slot = is_v ? C::VSLOT : gc % C::KSLOTS;
+        const int round = is_v ? gc : gc / C::KSLOTS;
         if (!is_v) {
           __syncwarp();
           const int s0 = c * C::BK + 4 * lane;
@@ -208,6 +211,7 @@ __global__ void __launch_bounds__(SparseBwdCfg<DK, DV>::THREADS, 1)
         else
           gather(p.kp, std::integral_constant<int, DK>{});
         cp_async_commit();
+        pend[issued & 3] = slot;
         ++issued;
         if (issued - signalled > C::COPY_DEPTH) {
           cp_async_wait<C::COPY_DEPTH>();
@@ -264,20 +268,19 @@ __global__ void __launch_bounds__(SparseBwdCfg<DK, DV>::THREADS, 1)
     const uint64_t dds_hi = sw128_desc(sDsHi, C::BK * 128, 1024);
     const uint64_t dds_lo = sw128_desc(sDsLo, C::BK * 128, 1024);
     auto add = [](uint64_t d, uint32_t bytes) { return d + (bytes >> 4); };
-    int ring = 0, chunk = 0;  // ring position and chunk count, over all items
+    int chunk = 0;  // chunk count over this CTA's items
     for (int r = 0; ok; ++r) {
       const int item = r * n_cta + cta;
       if (item >= n_items) break;
       ok = mbar_wait_warp(smem_u32(&bar_q_full), r & 1, ctl);
       if (!ok) break;
       for (int c = 0; c < nch && ok; ++c, ++chunk) {
-        const int pk = ring + 2 * c, pv = pk + 1;
-        const int sk = pk % C::NSLOT, sv = pv % C::NSLOT;
+        const int sk = chunk % C::KSLOTS, sv = C::VSLOT;
         // S^T / P^T / dK columns and dV's are free once the compute warps have
         // drained the previous chunk.
         if (chunk > 0) ok = mbar_wait_warp(smem_u32(&bar_drain_done), (chunk - 1) & 1, ctl);
-        if (ok) ok = mbar_wait_warp(smem_u32(&bar_kv_full[sk]), (pk / C::NSLOT) & 1, ctl);
-        if (ok) ok = mbar_wait_warp(smem_u32(&bar_kv_full[sv]), (pv / C::NSLOT) & 1, ctl);
+        if (ok) ok = mbar_wait_warp(smem_u32(&bar_kv_full[sk]), (chunk / C::KSLOTS) & 1, ctl);
+        if (ok) ok = mbar_wait_warp(smem_u32(&bar_kv_full[sv]), chunk & 1, ctl);
         if (!ok) break;
         tc_fence_after();
         const uint32_t kb = sRing + sk * C::SLOT_BYTES, vb = sRing + sv * C::SLOT_BYTES;
@@ -324,7 +327,6 @@ __global__ void __launch_bounds__(SparseBwdCfg<DK, DV>::THREADS, 1)
         mma_commit_el(smem_u32(&bar_kv_empty[sk]));  // K_c is not read again
         if (c + 1 == nch) mma_commit_el(smem_u32(&bar_q_empty));
       }
-      ring += 2 * nch;
     }
     mma_commit_el(smem_u32(&bar_mma_done));
     mbar_wait_drain(smem_u32(&bar_mma_done), 0, 50000000ull);

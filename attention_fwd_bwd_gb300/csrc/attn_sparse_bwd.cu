@@ -401,24 +401,48 @@ __global__ void __launch_bounds__(SparseBwdCfg<DK, DV>::THREADS, 1)
         ok = mbar_wait_warp(smem_u32(&bar_grads_full), chunk & 1, ctl);
         if (!ok) break;
         tc_fence_after();
-        auto drain = [&](uint32_t col, float* dst_row, auto dcols) {
+        // Each warp stages its 32 rows in its quarter of the dS^T tiles (free
+        // until the next chunk: dQ^T, their last reader, has run), 16-byte unit
+        // u of row i at unit position u ^ (i mod UNITS), then adds one whole
+        // row per instruction -- lane l takes unit l -- so each reduction
+        // covers one contiguous row instead of 32 scattered ones.
+        const uint32_t stage = sDsHi + warp * (32 * 512);
+        auto drain = [&](uint32_t col, float* pool, auto dcols) {
           constexpr int DC = decltype(dcols)::value;
+          constexpr int UNITS = DC / 4;  // 16-byte units per fp32 row
+          constexpr int ROWB = DC * 4;
 #pragma unroll 1
           for (int k0 = 0; k0 < DC; k0 += 32) {
             uint32_t u[32];
             tmem_ld32(tmem + lane_base + col + k0, u);
             tmem_wait_ld();
-            if (filled) {
 #pragma unroll
-              for (int k = 0; k < 32; k += 4)
-                red_add_v4(dst_row + k0 + k, __uint_as_float(u[k]), __uint_as_float(u[k + 1]),
-                           __uint_as_float(u[k + 2]), __uint_as_float(u[k + 3]));
+            for (int q = 0; q < 8; ++q) {
+              const int unit = k0 / 4 + q;
+              const uint32_t addr = stage + lane * ROWB + ((unit ^ (lane & (UNITS - 1))) << 4);
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(u[4 * q]),
+                           "r"(u[4 * q + 1]), "r"(u[4 * q + 2]), "r"(u[4 * q + 3])
+                           : "memory");
             }
           }
+          __syncwarp();
+#pragma unroll 1
+          for (int i = 0; i < 32; ++i) {
+            const int ei = __shfl_sync(0xffffffffu, e, i);
+            const bool fi = __shfl_sync(0xffffffffu, filled ? 1 : 0, i) != 0;
+            if (fi && lane < UNITS) {
+              const uint32_t addr = stage + i * ROWB + ((lane ^ (i & (UNITS - 1))) << 4);
+              float4 v;
+              asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                           : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                           : "r"(addr));
+              red_add_v4(pool + (static_cast<size_t>(b) * p.P + ei) * DC + 4 * lane, v.x, v.y, v.z, v.w);
+            }
+          }
+          __syncwarp();
         };
-        const size_t prow = static_cast<size_t>(b) * p.P + (filled ? e : 0);
-        drain(C::TM_DV, p.dvp + prow * DV, std::integral_constant<int, DV>{});
-        drain(C::TM_S, p.dkp + prow * DK, std::integral_constant<int, DK>{});
+        drain(C::TM_DV, p.dvp, std::integral_constant<int, DV>{});
+        drain(C::TM_S, p.dkp, std::integral_constant<int, DK>{});
         if (c + 1 == nch) {
           // dQ^T is complete for this token: thread j < DK writes column j of
           // dq for every head (row j of dQ^T). j < DK is warp-uniform.

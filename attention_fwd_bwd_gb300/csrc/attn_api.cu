@@ -385,10 +385,9 @@ attn_status_t attn_sparse_fwd(const void* q, const void* kp, const void* vp, con
   attn_status_t st = check_device();
   if (st != ATTN_OK) return st;
   const long long qrows = static_cast<long long>(B) * T * H, prows = static_cast<long long>(B) * P;
-  CUtensorMap tq, to, tolo;
-  (void)prows;
-  if (!make_rows_map(&tq, q, qrows, DK, 128) || !make_rows_map(&to, o, qrows, DV, H) ||
-      !make_rows_map(&tolo, o_lo ? o_lo : o, qrows, DV, H))
+  CUtensorMap tq, tk, to, tolo;
+  if (!make_rows_map(&tq, q, qrows, DK, 128) || !make_rows_map(&tk, kp, prows, DK, 1) ||
+      !make_rows_map(&to, o, qrows, DV, H) || !make_rows_map(&tolo, o_lo ? o_lo : o, qrows, DV, H))
     return ATTN_ERR_CUDA;
   int* status = fwd_status_ptr();
   if (!status) return ATTN_ERR_CUDA;
@@ -412,7 +411,7 @@ attn_status_t attn_sparse_fwd(const void* q, const void* kp, const void* vp, con
   p.timeout_ns = g_timeout_ns;
   p.inject_stall = g_inject_stall & 1;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  return finish(launch_sparse_fwd(DK, DV, tq, to, tolo, o_lo != nullptr, p, s), s, status);
+  return finish(launch_sparse_fwd(DK, DV, tq, tk, to, tolo, o_lo != nullptr, p, s), s, status);
 }
 
 size_t attn_sparse_bwd_workspace_size(int B, int T, int H) {

@@ -9,14 +9,16 @@
 // tensor load; Table 7 for the list shapes).
 //
 // Per work item (batch b, token t), in a persistent CTA:
-//   warp 8 (producer): the token's H x DK query rows once (one TMA tile), then
-//       for every chunk of 128 slots its K rows and V rows, gathered with
-//       16-byte asynchronous copies (cp.async) straight into the
-//       128-byte-swizzled layout the MMAs read, through a ring of slots with
-//       full/empty mbarriers; a few ring positions stay in flight. Empty slots
-//       copy nothing (zero fill) and are masked. (Gathering with the tensor
-//       engine's four-row gather mode was measured 2.3x slower here: its
-//       small requests cap the bytes in flight per SM.)
+//   warp 8 (K producer): the token's H x DK query rows once (one TMA tile),
+//       then every chunk's 128 K rows, gathered four pool rows per TMA
+//       instruction (tile::gather4) straight into the 128-byte-swizzled
+//       layout the MMAs read; empty slots fetch row 0 and are masked.
+//   warp 10 (V producer): every chunk's V rows, gathered with 16-byte
+//       cp.async copies into the same layout (empty slots copy nothing).
+//       K and V thus arrive through two separate copy paths, each of which
+//       moves about as many bytes per clock as one path alone did. K chunks
+//       go through KSLOTS slots in turn and V chunks through the others, each
+//       slot with a full/empty mbarrier pair.
 //   warp 9 (MMA issuer): S_w = Q K_c^T for chunk c into warpgroup w = c % 2,
 //       O_w += P_w V_c (P hi and lo bf16 parts from TMEM, V described
 //       MN-major). The warpgroups alternate on the tensor core.
@@ -46,6 +48,20 @@ __device__ __forceinline__ void tma_load_2d_el(uint32_t dst, const CUtensorMap* 
       "@e cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4}], [%2];\n\t}" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+// Four rows r0..r3 of a 2-D map (box: one row of 64 columns), columns
+// col..col+63, into 4 consecutive 128-byte rows of shared memory. Issued by
+// the calling thread.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* m, uint32_t bar,
+                                            int col, int r0, int r1, int r2, int r3,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
+      "l"(policy)
       : "memory");
 }
 
@@ -98,6 +114,7 @@ __device__ __forceinline__ int chunks_of(int n, int w) { return n > w ? (n - w +
 template <int DK, int DV>
 __global__ void __launch_bounds__(SparseFwdCfg<DK, DV>::THREADS, 1)
     attn_sparse_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
+                           const __grid_constant__ CUtensorMap tm_k,
                            const __grid_constant__ CUtensorMap tm_o,
                            const __grid_constant__ CUtensorMap tm_olo, const int write_lo,
                            const SparseFwdParams p) {
@@ -127,7 +144,7 @@ __global__ void __launch_bounds__(SparseFwdCfg<DK, DV>::THREADS, 1)
     mbar_init(smem_u32(&bar_merge), 128);
     mbar_init(smem_u32(&bar_o1_free), 128);
     for (int i = 0; i < C::NSLOT; ++i) {
-      mbar_init(smem_u32(&bar_kv_full[i]), 32);  // every producer lane, once its copies landed
+      mbar_init(smem_u32(&bar_kv_full[i]), 1);
       mbar_init(smem_u32(&bar_kv_empty[i]), 1);
     }
     for (int w = 0; w < 2; ++w) {
@@ -154,75 +171,43 @@ __global__ void __launch_bounds__(SparseFwdCfg<DK, DV>::THREADS, 1)
   float* merge_l = merge_m + C::BQ;
 
   if (warp == 8) {
-    // ------------------------------------------------------------ producer
-    // Ring position 2c holds K of chunk c, 2c + 1 its V; positions run on
-    // across items. Each copy instruction of the warp moves UNITS 16-byte
-    // units of each of 32 / UNITS rows (whole rows, contiguous in global
-    // memory); row j's unit u lands at j * 128 + ((u % 8) ^ (j % 8)) * 16 in
-    // 64-column block u / 8 (the 128-byte swizzle the MMA descriptors expect).
-    int* idx_s = reinterpret_cast<int*>(smem + C::SMEM_IDX);
-    if (lane == 0) prefetch_tmap(&tm_q);
-    int issued = 0, signalled = 0, q_loads = 0;
+    // ------------------------------------------------------------ K producer
+    // Chunk c of this CTA's item r is its chunk r n + c: K slot (r n + c) % KSLOTS.
+    if (lane == 0) {
+      prefetch_tmap(&tm_q);
+      prefetch_tmap(&tm_k);
+    }
+    const uint64_t keep = policy_evict_last();  // pool rows recur in nearby tokens' lists
+    int q_loads = 0, last_k = -1;
     bool ok = true;
-    // Position `signalled` has landed (for this lane): make its bytes visible
-    // to the tensor core and report it.
-    auto signal_oldest = [&]() {
-      fence_async_smem();
-      mbar_arrive(smem_u32(&bar_kv_full[signalled % C::NSLOT]));
-      ++signalled;
-    };
     for (int r = 0; ok; ++r) {
       const int item = r * n_cta + cta;
       if (item >= n_items) break;
       const int b = item / p.T;
       const int* lst = p.idx + static_cast<size_t>(item) * p.K;
-      auto load_chunk = [&](int pos) {
-        const int c = pos >> 1;
-        const bool is_v = pos & 1;
-        const int slot = issued % C::NSLOT, round = issued / C::NSLOT;
-        if (!is_v) {
-          // The chunk's 128 pool rows (-1: empty) for both of its positions.
-          __syncwarp();
-          const int s0 = c * C::BK + 4 * lane;
-          int4 e = make_int4(-1, -1, -1, -1);
-          if (s0 < p.K) e = __ldg(reinterpret_cast<const int4*>(lst + s0));
-          auto chk = [&](int x) { return (x >= 0 && x < p.P) ? x : -1; };
-          reinterpret_cast<int4*>(idx_s)[lane] = make_int4(chk(e.x), chk(e.y), chk(e.z), chk(e.w));
-          __syncwarp();
-        }
+      const int row0 = b * p.P;
+      auto load_k = [&](int c) {
+        const int g = r * nch + c;  // chunk index over this CTA's items
+        const int slot = g % C::KSLOTS, round = g / C::KSLOTS;
+        const int s0 = c * C::BK + 4 * lane;
+        int4 e = make_int4(-1, -1, -1, -1);
+        if (s0 < p.K) e = __ldg(reinterpret_cast<const int4*>(lst + s0));
+        auto row = [&](int x) { return row0 + ((x >= 0 && x < p.P) ? x : 0); };
         if (round > 0) ok = mbar_wait_warp(smem_u32(&bar_kv_empty[slot]), (round - 1) & 1, ctl);
         if (!ok) return;
-        const uint32_t dst = sRing + slot * C::SLOT_BYTES;
-        auto gather = [&](const __nv_bfloat16* pool, auto dcols) {
-          constexpr int DC = decltype(dcols)::value;
-          constexpr int UNITS = DC / 8;          // 16-byte units per row
-          constexpr int RPI = 32 / UNITS;        // rows per warp instruction
-          const int u = lane % UNITS, jr = lane / UNITS;
-          const uint32_t ublk = (u / 8) * (C::BK * 128);
-          const __nv_bfloat16* base = pool + static_cast<size_t>(b) * p.P * DC + u * 8;
-#pragma unroll 8
-          for (int j0 = 0; j0 < C::BK; j0 += RPI) {
-            const int j = j0 + jr;
-            const int x = idx_s[j];
-            const uint32_t d = dst + ublk + j * 128 + (((u % 8) ^ (j & 7)) << 4);
-            cp_async16(d, base + static_cast<size_t>(x < 0 ? 0 : x) * DC, x < 0 ? 0u : 16u);
-          }
-        };
-        if (is_v)
-          gather(p.vp, std::integral_constant<int, DV>{});
-        else
-          gather(p.kp, std::integral_constant<int, DK>{});
-        cp_async_commit();
-        ++issued;
-        if (issued - signalled > C::COPY_DEPTH) {
-          cp_async_wait<C::COPY_DEPTH>();
-          signal_oldest();
-        }
+        const uint32_t full = smem_u32(&bar_kv_full[slot]);
+        const uint32_t dst = sRing + slot * C::SLOT_BYTES + lane * 4 * 128;
+        mbar_arrive_expect_tx_el(full, C::K_BYTES);
+        __syncwarp();
+#pragma unroll
+        for (int cb = 0; cb < C::KCH; ++cb)
+          tma_gather4(dst + cb * (C::BK * 128), &tm_k, full, cb * 64, row(e.x), row(e.y), row(e.z),
+                      row(e.w), keep);
+        last_k = g;
       };
-      // The first chunk's K and V, then Q once the previous item's last S
-      // product has read the Q buffer, then the remaining chunks.
-      const int pre = (r == 0) ? 0 : 2;
-      for (int pos = 0; pos < pre && ok; ++pos) load_chunk(pos);
+      // The first chunk's K, then Q once the previous item's last S product
+      // has read the Q buffer, then the remaining chunks' K.
+      if (r > 0) load_k(0);
       if (!ok) break;
       if (r > 0) ok = mbar_wait_warp(smem_u32(&bar_q_empty), (r - 1) & 1, ctl);
       if (!ok) break;
@@ -231,14 +216,73 @@ __global__ void __launch_bounds__(SparseFwdCfg<DK, DV>::THREADS, 1)
         tma_load_2d_el(sQ + cb * (C::BQ * 128), &tm_q, smem_u32(&bar_q_full), cb * 64,
                        item * p.H);
       ++q_loads;
-      for (int pos = pre; pos < 2 * nch && ok; ++pos) load_chunk(pos);
+      for (int c = (r > 0 ? 1 : 0); c < nch && ok; ++c) load_k(c);
     }
-    // Report the positions still in flight, then let every copy land before
-    // the CTA's shared memory goes away.
+    if (lane == 0) {
+      // Let every copy issued land before the CTA's shared memory goes away.
+      for (int g = max(0, last_k - C::KSLOTS + 1); g <= last_k; ++g)
+        mbar_wait_drain(smem_u32(&bar_kv_full[g % C::KSLOTS]), (g / C::KSLOTS) & 1, 50000000ull);
+      if (q_loads > 0) mbar_wait_drain(smem_u32(&bar_q_full), (q_loads - 1) & 1, 50000000ull);
+    }
+    __syncwarp();
+  } else if (warp == 10) {
+    // ------------------------------------------------------------ V producer
+    // Each copy instruction of the warp moves UNITS 16-byte units of each of
+    // 32 / UNITS rows (whole rows, contiguous in global memory); row j's unit
+    // u lands at j * 128 + ((u % 8) ^ (j % 8)) * 16 in 64-column block u / 8.
+    // One position's copies stay in flight: V_c is reported once V_{c+1} has
+    // been issued (releasing any earlier position needs nothing later).
+    int* idx_s = reinterpret_cast<int*>(smem + C::SMEM_IDX);
+    int issued = 0, signalled = 0;
+    int pend[4];
+    bool ok = true;
+    auto signal_oldest = [&]() {
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bar_kv_full[pend[signalled & 3]]));
+      ++signalled;
+    };
+    for (int r = 0; ok; ++r) {
+      const int item = r * n_cta + cta;
+      if (item >= n_items) break;
+      const int b = item / p.T;
+      const int* lst = p.idx + static_cast<size_t>(item) * p.K;
+      for (int c = 0; c < nch && ok; ++c) {
+        const int g = r * nch + c;
+        const int slot = C::KSLOTS + g % C::VSLOTS, round = g / C::VSLOTS;
+        __syncwarp();
+        const int s0 = c * C::BK + 4 * lane;
+        int4 e = make_int4(-1, -1, -1, -1);
+        if (s0 < p.K) e = __ldg(reinterpret_cast<const int4*>(lst + s0));
+        auto chk = [&](int x) { return (x >= 0 && x < p.P) ? x : -1; };
+        reinterpret_cast<int4*>(idx_s)[lane] = make_int4(chk(e.x), chk(e.y), chk(e.z), chk(e.w));
+        __syncwarp();
+        if (round > 0) ok = mbar_wait_warp(smem_u32(&bar_kv_empty[slot]), (round - 1) & 1, ctl);
+        if (!ok) break;
+        const uint32_t dst = sRing + slot * C::SLOT_BYTES;
+        constexpr int UNITS = DV / 8;
+        constexpr int RPI = 32 / UNITS;
+        const int u = lane % UNITS, jr = lane / UNITS;
+        const uint32_t ublk = (u / 8) * (C::BK * 128);
+        const __nv_bfloat16* base = p.vp + static_cast<size_t>(b) * p.P * DV + u * 8;
+#pragma unroll 8
+        for (int j0 = 0; j0 < C::BK; j0 += RPI) {
+          const int j = j0 + jr;
+          const int x = idx_s[j];
+          const uint32_t d = dst + ublk + j * 128 + (((u % 8) ^ (j & 7)) << 4);
+          cp_async16(d, base + static_cast<size_t>(x < 0 ? 0 : x) * DV, x < 0 ? 0u : 16u);
+        }
+        cp_async_commit();
+        pend[issued & 3] = slot;
+        ++issued;
+        if (issued - signalled > 1) {
+          cp_async_wait<1>();
+          signal_oldest();
+        }
+      }
+    }
     cp_async_wait<0>();
     while (signalled < issued) signal_oldest();
-    if (lane == 0 && q_loads > 0)
-      mbar_wait_drain(smem_u32(&bar_q_full), (q_loads - 1) & 1, 50000000ull);
     __syncwarp();
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
@@ -246,7 +290,6 @@ __global__ void __launch_bounds__(SparseFwdCfg<DK, DV>::THREADS, 1)
     constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
     constexpr uint32_t idesc_o = idesc_bf16_f32(128, DV, 0, 1);
     const uint64_t dq_desc = sw128_desc(sQ, 16, 1024);
-    int ring = 0;           // ring position of the item's first chunk
     int p_cnt[2] = {0, 0};  // P tiles consumed per warpgroup, over all items
     for (int r = 0; ok; ++r) {
       const int item = r * n_cta + cta;
@@ -254,26 +297,30 @@ __global__ void __launch_bounds__(SparseFwdCfg<DK, DV>::THREADS, 1)
       ok = mbar_wait_warp(smem_u32(&bar_q_full), r & 1, ctl);
       if (!ok) break;
       int s_left = nch;  // the last S product of the item hands the Q buffer back
-      auto slot_of = [&](int pos) { return (ring + pos) % C::NSLOT; };
-      auto wait_kv = [&](int pos) {
-        const int q = ring + pos;
-        return mbar_wait_warp(smem_u32(&bar_kv_full[q % C::NSLOT]), (q / C::NSLOT) & 1, ctl);
+      // Chunk c of this item is chunk r n + c of the CTA: its K slot and V slot.
+      auto kslot = [&](int c) { return (r * nch + c) % C::KSLOTS; };
+      auto vslot = [&](int c) { return C::KSLOTS + (r * nch + c) % C::VSLOTS; };
+      auto wait_k = [&](int c) {
+        return mbar_wait_warp(smem_u32(&bar_kv_full[kslot(c)]), ((r * nch + c) / C::KSLOTS) & 1, ctl);
+      };
+      auto wait_v = [&](int c) {
+        return mbar_wait_warp(smem_u32(&bar_kv_full[vslot(c)]), ((r * nch + c) / C::VSLOTS) & 1, ctl);
       };
       // S_w = Q K_c^T; K_c's slot is released once the product has run.
       auto issue_s = [&](int c) {
         const int w = c & 1;
-        const uint64_t dk = sw128_desc(sRing + slot_of(2 * c) * C::SLOT_BYTES, 16, 1024);
+        const uint64_t dk = sw128_desc(sRing + kslot(c) * C::SLOT_BYTES, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < DK / 16; ++kk) {
           const uint32_t koff = ((kk >> 2) * (128 * 128) + (kk & 3) * 32) >> 4;
           mma_ss_el(tmem + C::tm_s(w), dq_desc + koff, dk + koff, idesc_s, kk > 0);
         }
         mma_commit_el(smem_u32(&bar_s_full[w]));
-        mma_commit_el(smem_u32(&bar_kv_empty[slot_of(2 * c)]));
+        mma_commit_el(smem_u32(&bar_kv_empty[kslot(c)]));
         if (--s_left == 0) mma_commit_el(smem_u32(&bar_q_empty));
       };
       for (int c = 0; c < 2 && c < nch && ok; ++c) {
-        ok = wait_kv(2 * c);
+        ok = wait_k(c);
         if (!ok) break;
         tc_fence_after();
         issue_s(c);
@@ -283,12 +330,12 @@ __global__ void __launch_bounds__(SparseFwdCfg<DK, DV>::THREADS, 1)
         ok = mbar_wait_warp(smem_u32(&bar_p_full[w]), p_cnt[w] & 1, ctl);
         if (!ok) break;
         ++p_cnt[w];
-        ok = wait_kv(2 * c + 1);
+        ok = wait_v(c);
         if (!ok) break;
         tc_fence_after();
         // O_w += P_hi V_c + P_lo V_c: slots 16kk..16kk+15 hold P hi pairs in
         // score columns 16kk..16kk+7 and lo pairs in 16kk+8..16kk+15.
-        const uint64_t dv = sw128_desc(sRing + slot_of(2 * c + 1) * C::SLOT_BYTES, C::BK * 128, 1024);
+        const uint64_t dv = sw128_desc(sRing + vslot(c) * C::SLOT_BYTES, C::BK * 128, 1024);
         const uint32_t a_p = tmem + C::tm_s(w);
 #pragma unroll
         for (int kk = 0; kk < C::BK / 16; ++kk)
@@ -297,17 +344,16 @@ __global__ void __launch_bounds__(SparseFwdCfg<DK, DV>::THREADS, 1)
 #pragma unroll
         for (int kk = 0; kk < C::BK / 16; ++kk)
           mma_ts_el(tmem + C::tm_o(w), a_p + kk * 16 + 8, dv + ((kk * 2048) >> 4), idesc_o, 1u);
-        mma_commit_el(smem_u32(&bar_kv_empty[slot_of(2 * c + 1)]));
+        mma_commit_el(smem_u32(&bar_kv_empty[vslot(c)]));
         if (c + 2 >= nch) mma_commit_el(smem_u32(&bar_pv_done[w]));
         // The next score tile of w overwrites P_w; MMAs run in issue order.
         if (c + 2 < nch) {
-          ok = wait_kv(2 * (c + 2));
+          ok = wait_k(c + 2);
           if (!ok) break;
           tc_fence_after();
           issue_s(c + 2);
         }
       }
-      ring += 2 * nch;
     }
     mma_commit_el(smem_u32(&bar_mma_done));
     mbar_wait_drain(smem_u32(&bar_mma_done), 0, 50000000ull);
@@ -528,7 +574,7 @@ __global__ void __launch_bounds__(SparseFwdCfg<DK, DV>::THREADS, 1)
 }
 
 template <int DK, int DV>
-cudaError_t launch_sparse_fwd_t(const CUtensorMap& tq, const CUtensorMap& to,
+cudaError_t launch_sparse_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& to,
                                 const CUtensorMap& tolo, bool write_lo,
                                 const SparseFwdParams& p, cudaStream_t stream) {
   using C = SparseFwdCfg<DK, DV>;
@@ -549,19 +595,19 @@ cudaError_t launch_sparse_fwd_t(const CUtensorMap& tq, const CUtensorMap& to,
   const int sms = (dev < 64 && sm_count[dev] > 0) ? sm_count[dev] : 148;
   const dim3 grid(static_cast<unsigned>(n_items < sms ? n_items : sms));
   attn_sparse_fwd_kernel<DK, DV><<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(
-      tq, to, tolo, write_lo ? 1 : 0, p);
+      tq, tk, to, tolo, write_lo ? 1 : 0, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_sparse_fwd(int DK, int DV, const CUtensorMap& tq, const CUtensorMap& to,
-                              const CUtensorMap& tolo, bool write_lo, const SparseFwdParams& p,
-                              cudaStream_t stream) {
-  if (DK == 128 && DV == 128) return launch_sparse_fwd_t<128, 128>(tq, to, tolo, write_lo, p, stream);
-  if (DK == 128 && DV == 64) return launch_sparse_fwd_t<128, 64>(tq, to, tolo, write_lo, p, stream);
-  if (DK == 64 && DV == 128) return launch_sparse_fwd_t<64, 128>(tq, to, tolo, write_lo, p, stream);
-  if (DK == 64 && DV == 64) return launch_sparse_fwd_t<64, 64>(tq, to, tolo, write_lo, p, stream);
+cudaError_t launch_sparse_fwd(int DK, int DV, const CUtensorMap& tq, const CUtensorMap& tk,
+                              const CUtensorMap& to, const CUtensorMap& tolo, bool write_lo,
+                              const SparseFwdParams& p, cudaStream_t stream) {
+  if (DK == 128 && DV == 128) return launch_sparse_fwd_t<128, 128>(tq, tk, to, tolo, write_lo, p, stream);
+  if (DK == 128 && DV == 64) return launch_sparse_fwd_t<128, 64>(tq, tk, to, tolo, write_lo, p, stream);
+  if (DK == 64 && DV == 128) return launch_sparse_fwd_t<64, 128>(tq, tk, to, tolo, write_lo, p, stream);
+  if (DK == 64 && DV == 64) return launch_sparse_fwd_t<64, 64>(tq, tk, to, tolo, write_lo, p, stream);
   return cudaErrorInvalidValue;
 }
 

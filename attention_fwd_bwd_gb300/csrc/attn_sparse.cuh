@@ -45,7 +45,12 @@ struct SparseFwdCfg {
   __host__ __device__ static constexpr int tm_s(int w) { return 256 * w; }
   __host__ __device__ static constexpr int tm_o(int w) { return 256 * w + 128; }
   static constexpr int TMEM_COLS = 512;
-  static constexpr int THREADS = 320;
+  // K and V come from two producers, so they use separate slots: slots
+  // 0..KSLOTS-1 hold K chunks in turn, the rest V chunks in turn. Each slot's
+  // barriers then see their phases in order.
+  static constexpr int KSLOTS = 2;
+  static constexpr int VSLOTS = NSLOT - KSLOTS;
+  static constexpr int THREADS = 352;  // 8 softmax warps, K producer, MMA issuer, V producer
   static_assert(NSLOT >= 4, "the ring needs at least two chunks of K and V");
   static_assert(COPY_DEPTH < NSLOT - 1, "copies in flight would block the ring");
   static_assert(SMEM_ALLOC <= 232448, "shared-memory plan exceeds 227 KB");
@@ -64,10 +69,11 @@ struct SparseFwdParams {
   int inject_stall;  // testing hook: the MMA warp issues nothing (waits then run out)
 };
 
-// tq: [B*T*H, DK] rows, box 128 x 64; to / tolo: [B*T*H, DV] rows, box H x 64.
-cudaError_t launch_sparse_fwd(int DK, int DV, const CUtensorMap& tq, const CUtensorMap& to,
-                              const CUtensorMap& tolo, bool write_lo, const SparseFwdParams& p,
-                              cudaStream_t stream);
+// tq: [B*T*H, DK] rows, box 128 x 64; tk: [B*P, DK] rows, box 1 x 64 (gathered
+// four rows at a time); to / tolo: [B*T*H, DV] rows, box H x 64.
+cudaError_t launch_sparse_fwd(int DK, int DV, const CUtensorMap& tq, const CUtensorMap& tk,
+                              const CUtensorMap& to, const CUtensorMap& tolo, bool write_lo,
+                              const SparseFwdParams& p, cudaStream_t stream);
 
 }  // namespace attn
 

@@ -442,8 +442,9 @@ attn_status_t attn_sparse_bwd(const void* q, const void* kp, const void* vp, con
     return ATTN_ERR_WORKSPACE;
   attn_status_t st = check_device();
   if (st != ATTN_OK) return st;
-  CUtensorMap tq, tdo;
-  if (!make_rows_map(&tq, q, rows, DK, 128) || !make_rows_map(&tdo, dO, rows, DV, 128))
+  CUtensorMap tq, tdo, tk;
+  if (!make_rows_map(&tq, q, rows, DK, 128) || !make_rows_map(&tdo, dO, rows, DV, 128) ||
+      !make_rows_map(&tk, kp, static_cast<long long>(B) * P, DK, 1))
     return ATTN_ERR_CUDA;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const size_t vec_bytes = (static_cast<size_t>(rows) * 4 + 255) / 256 * 256;
@@ -474,8 +475,8 @@ attn_status_t attn_sparse_bwd(const void* q, const void* kp, const void* vp, con
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   return finish(launch_sparse_bwd(DK, DV, static_cast<const __nv_bfloat16*>(o),
                                   static_cast<const __nv_bfloat16*>(o_lo),
-                                  static_cast<const __nv_bfloat16*>(dO), lse, nlse2, dvec, tq, tdo, p,
-                                  s),
+                                  static_cast<const __nv_bfloat16*>(dO), lse, nlse2, dvec, tq, tdo, tk,
+                                  p, s),
                 s, p.status);
 }
 

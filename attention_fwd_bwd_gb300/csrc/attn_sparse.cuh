@@ -114,18 +114,19 @@ struct SparseBwdCfg {
   static constexpr int SMEM_IDX = SMEM_ROWS + ROWS_BYTES;
   static constexpr int SMEM_BYTES = SMEM_IDX + IDX_BYTES;
   static constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;
-  // Slots NSLOT - 1 hold V chunks (one slot: V_c is free again after dP^T(c),
+  // Slot NSLOT - 1 holds V chunks (one slot: V_c is free again after dP^T(c),
   // early in chunk c), the others K chunks in turn (K_c is read until dQ^T(c),
   // at the end of chunk c). So V_{c+1} and K_{c+1} both load while chunk c is
-  // processed. The producer keeps one position's copies in flight: releasing
-  // V_c needs K_c and V_c reported, releasing K_c needs V_c.
+  // processed. K comes from one producer warp, V from another; each slot set
+  // has a single producer, so its barriers see their phases in order. The V
+  // producer reports each chunk as soon as it has landed: with one V slot, its
+  // next load waits for the release of the chunk it has just issued.
   static constexpr int KSLOTS = NSLOT - 1;
   static constexpr int VSLOT = NSLOT - 1;
-  static constexpr int COPY_DEPTH = 1;
   // TMEM columns: S^T (then P^T, then dK_c), dP^T (then dS^T), dV_c, dQ^T.
   static constexpr int TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DQ = 384;
   static constexpr int TMEM_COLS = 512;
-  static constexpr int THREADS = 192;  // 4 compute warps, producer, MMA issuer
+  static constexpr int THREADS = 224;  // 4 compute warps, K producer, MMA issuer, V producer
   static_assert(NSLOT >= 3, "the ring needs K and V of one chunk plus one");
   static_assert(SMEM_ALLOC <= 232448, "shared-memory plan exceeds 227 KB");
 };
@@ -154,7 +155,7 @@ inline size_t sparse_bwd_workspace_bytes(long long rows) {
 
 cudaError_t launch_sparse_bwd(int DK, int DV, const __nv_bfloat16* o, const __nv_bfloat16* o_lo,
                               const __nv_bfloat16* dO, const float* lse, float* nlse2, float* dvec,
-                              const CUtensorMap& tq, const CUtensorMap& tdo,
+                              const CUtensorMap& tq, const CUtensorMap& tdo, const CUtensorMap& tk,
                               const SparseBwdParams& p, cudaStream_t stream);
 
 }  // namespace attn

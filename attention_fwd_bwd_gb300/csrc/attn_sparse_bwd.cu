@@ -12,9 +12,11 @@
 //   1. preprocess: Dvec from o (+ o_lo) and dO, -LSE*log2(e) per (token, head),
 //      and zeroed dkp / dvp (HBM-bound).
 //   2. main, one persistent CTA per SM over (batch, token) items:
-//      warp 4 (producer): the token's Q and dO rows (TMA tiles) and row
-//          vectors, then each chunk's K and V rows gathered with cp.async (as
-//          in the forward) into K slots used in turn and one V slot.
+//      warp 4 (K producer): the token's Q and dO rows (TMA tiles) and row
+//          vectors, then each chunk's K rows through the tensor engine's
+//          four-row gather, into K slots used in turn.
+//      warp 6 (V producer): each chunk's V rows through cp.async, into one V
+//          slot. (Two copy paths at once, as in the forward.)
 //      warp 5 (MMA issuer), per chunk c: S^T = K_c Q^T and dP^T = V_c dO^T
 //          (slot-major: TMEM lane = slot), then dV_c = P^T dO and
 //          dK_c = dS^T Q with A from TMEM, and dQ^T += K_c^T dS^T with dS^T
@@ -43,6 +45,18 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, 
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+// Four rows r0..r3 of a 2-D map (box: one row of 64 columns), columns
+// col..col+63, into 4 consecutive 128-byte rows of shared memory.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* m, uint32_t bar,
+                                            int col, int r0, int r1, int r2, int r3,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
+      "l"(policy)
       : "memory");
 }
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
@@ -103,7 +117,8 @@ __global__ void __launch_bounds__(256) attn_sparse_bwd_preprocess_kernel(
 template <int DK, int DV>
 __global__ void __launch_bounds__(SparseBwdCfg<DK, DV>::THREADS, 1)
     attn_sparse_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
-                           const __grid_constant__ CUtensorMap tm_do, const SparseBwdParams p) {
+                           const __grid_constant__ CUtensorMap tm_do,
+                           const __grid_constant__ CUtensorMap tm_k, const SparseBwdParams p) {
   using C = SparseBwdCfg<DK, DV>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -127,7 +142,7 @@ __global__ void __launch_bounds__(SparseBwdCfg<DK, DV>::THREADS, 1)
     mbar_init(smem_u32(&bar_q_empty), 1);
     mbar_init(smem_u32(&bar_mma_done), 1);
     for (int i = 0; i < C::NSLOT; ++i) {
-      mbar_init(smem_u32(&bar_kv_full[i]), 32);
+      mbar_init(smem_u32(&bar_kv_full[i]), 1);
       mbar_init(smem_u32(&bar_kv_empty[i]), 1);
     }
     mbar_init(smem_u32(&bar_sdp_full), 1);
@@ -154,78 +169,45 @@ __global__ void __launch_bounds__(SparseBwdCfg<DK, DV>::THREADS, 1)
   float* rows_s = reinterpret_cast<float*>(smem + C::SMEM_ROWS);  // nlse2[128], then dvec[128]
 
   if (warp == 4) {
-    // ------------------------------------------------------------ producer
-    int* idx_s = reinterpret_cast<int*>(smem + C::SMEM_IDX);
+    // ------------------------------------------------------------ K producer
     if (lane == 0) {
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_do);
+      prefetch_tmap(&tm_k);
     }
-    int issued = 0, signalled = 0, q_loads = 0;
-    int pend[4];  // slot of each position not yet reported (at most COPY_DEPTH + 1)
+    const uint64_t keep = policy_evict_last();  // pool rows recur in nearby tokens' lists
+    int q_loads = 0, last_k = -1;
     bool ok = true;
-    auto signal_oldest = [&]() {
-      fence_async_smem();
-      mbar_arrive(smem_u32(&bar_kv_full[pend[signalled & 3]]));
-      ++signalled;
-    };
     for (int r = 0; ok; ++r) {
       const int item = r * n_cta + cta;
       if (item >= n_items) break;
       const int b = item / p.T;
       const int* lst = p.idx + static_cast<size_t>(item) * p.K;
-      auto load_pos = [&](int pos) {
-        const int c = pos >> 1;
-        const bool is_v = pos & 1;
+      const int row0 = b * p.P;
+      auto load_k = [&](int c) {
         const int gc = r * nch + c;  // chunk index over this CTA's items
-        const int slot = is_v ? C::VSLOT : gc % C::KSLOTS;
-        const int round = is_v ? gc : gc / C::KSLOTS;
-        if (!is_v) {
-          __syncwarp();
-          const int s0 = c * C::BK + 4 * lane;
-          int4 e = make_int4(-1, -1, -1, -1);
-          if (s0 < p.K) e = __ldg(reinterpret_cast<const int4*>(lst + s0));
-          auto chk = [&](int x) { return (x >= 0 && x < p.P) ? x : -1; };
-          reinterpret_cast<int4*>(idx_s)[lane] = make_int4(chk(e.x), chk(e.y), chk(e.z), chk(e.w));
-          __syncwarp();
-        }
+        const int slot = gc % C::KSLOTS, round = gc / C::KSLOTS;
+        const int s0 = c * C::BK + 4 * lane;
+        int4 e = make_int4(-1, -1, -1, -1);
+        if (s0 < p.K) e = __ldg(reinterpret_cast<const int4*>(lst + s0));
+        // Empty slots fetch row 0; the compute warps give them P = dS = 0.
+        auto row = [&](int x) { return row0 + ((x >= 0 && x < p.P) ? x : 0); };
         if (round > 0) ok = mbar_wait_warp(smem_u32(&bar_kv_empty[slot]), (round - 1) & 1, ctl);
         if (!ok) return;
-        const uint32_t dst = sRing + slot * C::SLOT_BYTES;
-        auto gather = [&](const __nv_bfloat16* pool, auto dcols) {
-          constexpr int DC = decltype(dcols)::value;
-          constexpr int UNITS = DC / 8;
-          constexpr int RPI = 32 / UNITS;
-          const int u = lane % UNITS, jr = lane / UNITS;
-          const uint32_t ublk = (u / 8) * (C::BK * 128);
-          const __nv_bfloat16* base = pool + static_cast<size_t>(b) * p.P * DC + u * 8;
-#pragma unroll 8
-          for (int j0 = 0; j0 < C::BK; j0 += RPI) {
-            const int j = j0 + jr;
-            const int x = idx_s[j];
-            const uint32_t d = dst + ublk + j * 128 + (((u % 8) ^ (j & 7)) << 4);
-            cp_async16(d, base + static_cast<size_t>(x < 0 ? 0 : x) * DC, x < 0 ? 0u : 16u);
-          }
-        };
-        if (is_v)
-          gather(p.vp, std::integral_constant<int, DV>{});
-        else
-          gather(p.kp, std::integral_constant<int, DK>{});
-        cp_async_commit();
-        pend[issued & 3] = slot;
-        ++issued;
-        if (issued - signalled > C::COPY_DEPTH) {
-          cp_async_wait<C::COPY_DEPTH>();
-          signal_oldest();
-        }
+        const uint32_t full = smem_u32(&bar_kv_full[slot]);
+        const uint32_t dst = sRing + slot * C::SLOT_BYTES + lane * 4 * 128;
+        mbar_arrive_expect_tx_el(full, C::K_BYTES);
+        __syncwarp();
+#pragma unroll
+        for (int cb = 0; cb < C::KCH; ++cb)
+          tma_gather4(dst + cb * (C::BK * 128), &tm_k, full, cb * 64, row(e.x), row(e.y), row(e.z),
+                      row(e.w), keep);
+        last_k = gc;
       };
-      // The first chunk's K and V; then every copy in flight is reported (the
-      // previous item's last products need its last positions), and Q, dO and
-      // the row vectors follow once those products are done with them.
-      const int pre = (r == 0) ? 0 : 2;
-      for (int pos = 0; pos < pre && ok; ++pos) load_pos(pos);
+      // The first chunk's K, then Q, dO and the row vectors once the previous
+      // item's products are done with them, then the remaining chunks' K.
+      if (r > 0) load_k(0);
       if (!ok) break;
-      cp_async_wait<0>();
-      while (signalled < issued) signal_oldest();
       if (r > 0) ok = mbar_wait_warp(smem_u32(&bar_q_empty), (r - 1) & 1, ctl);
       if (!ok) break;
 #pragma unroll
@@ -247,12 +229,58 @@ __global__ void __launch_bounds__(SparseBwdCfg<DK, DV>::THREADS, 1)
       }
       __syncwarp();
       ++q_loads;
-      for (int pos = pre; pos < 2 * nch && ok; ++pos) load_pos(pos);
+      for (int c = (r > 0 ? 1 : 0); c < nch && ok; ++c) load_k(c);
+    }
+    if (lane == 0) {
+      // Let every copy issued land before the CTA's shared memory goes away.
+      for (int g = max(0, last_k - C::KSLOTS + 1); g <= last_k; ++g)
+        mbar_wait_drain(smem_u32(&bar_kv_full[g % C::KSLOTS]), (g / C::KSLOTS) & 1, 50000000ull);
+      if (q_loads > 0) mbar_wait_drain(smem_u32(&bar_q_full), (q_loads - 1) & 1, 50000000ull);
+    }
+    __syncwarp();
+  } else if (warp == 6) {
+    // ------------------------------------------------------------ V producer
+    // Row j's 16-byte unit u lands at j * 128 + ((u % 8) ^ (j % 8)) * 16 in
+    // 64-column block u / 8 (the 128-byte swizzle the MMA descriptors expect).
+    int* idx_s = reinterpret_cast<int*>(smem + C::SMEM_IDX);
+    bool ok = true;
+    for (int r = 0; ok; ++r) {
+      const int item = r * n_cta + cta;
+      if (item >= n_items) break;
+      const int b = item / p.T;
+      const int* lst = p.idx + static_cast<size_t>(item) * p.K;
+      for (int c = 0; c < nch && ok; ++c) {
+        const int gc = r * nch + c;
+        __syncwarp();
+        const int s0 = c * C::BK + 4 * lane;
+        int4 e = make_int4(-1, -1, -1, -1);
+        if (s0 < p.K) e = __ldg(reinterpret_cast<const int4*>(lst + s0));
+        auto chk = [&](int x) { return (x >= 0 && x < p.P) ? x : -1; };
+        reinterpret_cast<int4*>(idx_s)[lane] = make_int4(chk(e.x), chk(e.y), chk(e.z), chk(e.w));
+        __syncwarp();
+        if (gc > 0) ok = mbar_wait_warp(smem_u32(&bar_kv_empty[C::VSLOT]), (gc - 1) & 1, ctl);
+        if (!ok) break;
+        const uint32_t dst = sRing + C::VSLOT * C::SLOT_BYTES;
+        constexpr int UNITS = DV / 8;
+        constexpr int RPI = 32 / UNITS;
+        const int u = lane % UNITS, jr = lane / UNITS;
+        const uint32_t ublk = (u / 8) * (C::BK * 128);
+        const __nv_bfloat16* base = p.vp + static_cast<size_t>(b) * p.P * DV + u * 8;
+#pragma unroll 8
+        for (int j0 = 0; j0 < C::BK; j0 += RPI) {
+          const int j = j0 + jr;
+          const int x = idx_s[j];
+          const uint32_t d = dst + ublk + j * 128 + (((u % 8) ^ (j & 7)) << 4);
+          cp_async16(d, base + static_cast<size_t>(x < 0 ? 0 : x) * DV, x < 0 ? 0u : 16u);
+        }
+        cp_async_commit();
+        cp_async_wait<0>();
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bar_kv_full[C::VSLOT]));
+      }
     }
     cp_async_wait<0>();
-    while (signalled < issued) signal_oldest();
-    if (lane == 0 && q_loads > 0)
-      mbar_wait_drain(smem_u32(&bar_q_full), (q_loads - 1) & 1, 50000000ull);
     __syncwarp();
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
@@ -471,7 +499,7 @@ __global__ void __launch_bounds__(SparseBwdCfg<DK, DV>::THREADS, 1)
 }
 
 template <int DK, int DV>
-cudaError_t launch_sparse_bwd_t(const CUtensorMap& tq, const CUtensorMap& tdo,
+cudaError_t launch_sparse_bwd_t(const CUtensorMap& tq, const CUtensorMap& tdo, const CUtensorMap& tk,
                                 const SparseBwdParams& p, cudaStream_t stream) {
   using C = SparseBwdCfg<DK, DV>;
   static bool attr_set[64] = {};
@@ -490,7 +518,7 @@ cudaError_t launch_sparse_bwd_t(const CUtensorMap& tq, const CUtensorMap& tdo,
   const long long n_items = static_cast<long long>(p.B) * p.T;
   const int sms = (dev < 64 && sm_count[dev] > 0) ? sm_count[dev] : 148;
   const dim3 grid(static_cast<unsigned>(n_items < sms ? n_items : sms));
-  attn_sparse_bwd_kernel<DK, DV><<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(tq, tdo, p);
+  attn_sparse_bwd_kernel<DK, DV><<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(tq, tdo, tk, p);
   return cudaGetLastError();
 }
 
@@ -498,7 +526,7 @@ cudaError_t launch_sparse_bwd_t(const CUtensorMap& tq, const CUtensorMap& tdo,
 
 cudaError_t launch_sparse_bwd(int DK, int DV, const __nv_bfloat16* o, const __nv_bfloat16* o_lo,
                               const __nv_bfloat16* dO, const float* lse, float* nlse2, float* dvec,
-                              const CUtensorMap& tq, const CUtensorMap& tdo,
+                              const CUtensorMap& tq, const CUtensorMap& tdo, const CUtensorMap& tk,
                               const SparseBwdParams& p, cudaStream_t stream) {
   const long long n_dkp4 = static_cast<long long>(p.B) * p.P * DK / 4;
   const long long n_dvp4 = static_cast<long long>(p.B) * p.P * DV / 4;
@@ -507,10 +535,10 @@ cudaError_t launch_sparse_bwd(int DK, int DV, const __nv_bfloat16* o, const __nv
       reinterpret_cast<float4*>(p.dvp), n_dvp4, p.status, p.B, p.T, p.H, DV);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  if (DK == 128 && DV == 128) return launch_sparse_bwd_t<128, 128>(tq, tdo, p, stream);
-  if (DK == 128 && DV == 64) return launch_sparse_bwd_t<128, 64>(tq, tdo, p, stream);
-  if (DK == 64 && DV == 128) return launch_sparse_bwd_t<64, 128>(tq, tdo, p, stream);
-  if (DK == 64 && DV == 64) return launch_sparse_bwd_t<64, 64>(tq, tdo, p, stream);
+  if (DK == 128 && DV == 128) return launch_sparse_bwd_t<128, 128>(tq, tdo, tk, p, stream);
+  if (DK == 128 && DV == 64) return launch_sparse_bwd_t<128, 64>(tq, tdo, tk, p, stream);
+  if (DK == 64 && DV == 128) return launch_sparse_bwd_t<64, 128>(tq, tdo, tk, p, stream);
+  if (DK == 64 && DV == 64) return launch_sparse_bwd_t<64, 64>(tq, tdo, tk, p, stream);
   return cudaErrorInvalidValue;
 }
 

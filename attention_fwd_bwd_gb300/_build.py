@@ -1,6 +1,6 @@
 """Builds libattn.so in-tree with nvcc for sm_103a.
 
-The three CUDA translation units compile in parallel and link into
+The CUDA translation units compile in parallel and link into
 attention_fwd_bwd_gb300/_lib/libattn.so. A content hash of the sources and
 flags is stored next to the library, so an unchanged tree is not rebuilt.
 """
@@ -16,7 +16,7 @@ CSRC = os.path.join(PKG, "csrc")
 LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libattn.so")
 SOURCES = ["attn_api.cu", "attn_fwd.cu", "attn_bwd.cu", "attn_noalloc.cu", "attn_sparse.cu", "attn_sparse_bwd.cu"]
-HEADERS = ["attn_common.cuh", "sm100_ptx.cuh"]
+HEADERS = ["attn_common.cuh", "attn_sparse.cuh", "sm100_ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v"]
 

@@ -161,3 +161,9 @@ def test_binding_fails_loudly_without_library(monkeypatch):
     monkeypatch.setattr(attn, "LIB_PATH", "/nonexistent/libattn.so")
     with pytest.raises(ImportError):
         attn.lib()
+
+
+def test_build_hash_covers_every_source_and_header():
+    from attention_fwd_bwd_gb300 import _build as B
+    present = sorted(f for f in os.listdir(B.CSRC) if f.endswith((".cu", ".cuh")))
+    assert sorted(B.SOURCES + B.HEADERS) == present

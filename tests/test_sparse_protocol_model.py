@@ -1,0 +1,234 @@
+"""A CPU model of the sparse forward kernel's barrier protocol.
+
+The kernel's roles (K producer, V producer, MMA issuer, two softmax
+warpgroups) are written as programs over mbarriers with the hardware's wait
+semantics: a wait for the phase with parity P succeeds when the barrier's
+current phase parity differs from P. Copies (TMA, cp.async) and MMA commits
+complete asynchronously -- TMA copies in any order, cp.async groups of one
+thread in order, MMA commits in issue order -- and a random scheduler
+interleaves everything. Each successful wait must be the completion of the
+phase it was meant for (no parity aliasing), and every run must finish (no
+deadlock). The same model with K and V sharing one ring under two producers
+-- a layout that misbehaved on the GPU -- must be caught: the K producer's
+closing wait for its last copies then targets slots that the V producer
+reuses afterwards, so the phase it waits for has already been passed.
+
+CPU only; no kernel code is involved.
+"""
+import random
+
+import pytest
+
+
+class Bar:
+    changes = 0  # every arrival counts as progress
+
+    def __init__(self, count):
+        self.count, self.pending, self.completed = count, count, 0
+
+    def arrive(self):
+        Bar.changes += 1
+        self.pending -= 1
+        if self.pending == 0:
+            self.completed += 1
+            self.pending = self.count
+
+
+class Aliasing(Exception):
+    pass
+
+
+class Deadlock(Exception):
+    pass
+
+
+def wait(bar, phase):
+    """A generator step: block until the hardware would report the phase with
+    parity phase & 1 complete; then check that it really is `phase`."""
+    while (bar.completed & 1) == (phase & 1):
+        yield
+    if bar.completed != phase + 1:
+        raise Aliasing(f"wait for phase {phase} passed with {bar.completed} phases completed")
+
+
+def sparse_fwd_model(n_items, nch, nslot, kslots, shared_ring=False, seed=0):
+    rnd = random.Random(seed)
+    vslots = nslot - kslots
+    full = [Bar(1) for _ in range(nslot)]
+    empty = [Bar(1) for _ in range(nslot)]
+    q_full, q_empty = Bar(1), Bar(1)
+    s_full, p_full, pv_done = [Bar(1), Bar(1)], [Bar(1), Bar(1)], [Bar(1), Bar(1)]
+    merge, o1_free = Bar(1), Bar(1)
+    nonlocal_last = [-1]
+    tma = []        # pending TMA completions (any order)
+    mma = []        # pending MMA commits (issue order)
+    cpa = []        # pending cp.async groups of the V producer (in order): [done, slot]
+
+    def kslot(g):
+        return (2 * g) % nslot if shared_ring else g % kslots
+
+    def kround(g):
+        return (2 * g) // nslot if shared_ring else g // kslots
+
+    def vslot(g):
+        return (2 * g + 1) % nslot if shared_ring else kslots + g % vslots
+
+    def vround(g):
+        return (2 * g + 1) // nslot if shared_ring else g // vslots
+
+    def k_producer():
+        for r in range(n_items):
+            def load_k(c):
+                g = r * nch + c
+                if kround(g) > 0:
+                    yield from wait(empty[kslot(g)], kround(g) - 1)
+                tma.append(full[kslot(g)])
+                nonlocal_last[0] = g
+            if r > 0:
+                yield from load_k(0)
+                yield from wait(q_empty, r - 1)
+            tma.append(q_full)
+            for c in range(1 if r > 0 else 0, nch):
+                yield from load_k(c)
+        # Before exiting, the K producer waits for its last copies to land
+        # (the kernel bounds this wait; here it must simply succeed). Its
+        # last chunks are the ones whose slots nothing reuses afterwards --
+        # unless another producer shares the slots.
+        last = nonlocal_last[0]
+        if shared_ring:  # the K chunks among the last nslot ring positions
+            tail = [g for g in range(last + 1) if 2 * g >= 2 * last - nslot]
+        else:            # the last kslots K chunks
+            tail = range(max(0, last - kslots + 1), last + 1)
+        for g in tail:
+            yield from wait(full[kslot(g)], kround(g))
+
+    def v_producer():
+        issued = signalled = 0
+        for r in range(n_items):
+            for c in range(nch):
+                g = r * nch + c
+                if vround(g) > 0:
+                    yield from wait(empty[vslot(g)], vround(g) - 1)
+                cpa.append([False, vslot(g)])
+                issued += 1
+                if issued - signalled > 1:
+                    while not cpa[signalled][0]:
+                        yield
+                    full[cpa[signalled][1]].arrive()
+                    signalled += 1
+        while signalled < issued:
+            while not cpa[signalled][0]:
+                yield
+            full[cpa[signalled][1]].arrive()
+            signalled += 1
+
+    def mma_warp():
+        p_cnt = [0, 0]
+        for r in range(n_items):
+            yield from wait(q_full, r)
+            s_left = [nch]
+
+            def issue_s(c):
+                g = r * nch + c
+                mma.append(s_full[c & 1])
+                mma.append(empty[kslot(g)])
+                s_left[0] -= 1
+                if s_left[0] == 0:
+                    mma.append(q_empty)
+            for c in range(min(2, nch)):
+                g = r * nch + c
+                yield from wait(full[kslot(g)], kround(g))
+                issue_s(c)
+            for c in range(nch):
+                w, g = c & 1, r * nch + c
+                yield from wait(p_full[w], p_cnt[w])
+                p_cnt[w] += 1
+                yield from wait(full[vslot(g)], vround(g))
+                mma.append(empty[vslot(g)])
+                if c + 2 >= nch:
+                    mma.append(pv_done[w])
+                if c + 2 < nch:
+                    g2 = g + 2
+                    yield from wait(full[kslot(g2)], kround(g2))
+                    issue_s(c + 2)
+
+    def softmax(w):
+        s_cnt = pv_cnt = 0
+        my_n = (nch - w + 1) // 2 if nch > w else 0
+        for rr in range(n_items):
+            checked = w == 0 or rr == 0
+            for _ in range(my_n):
+                yield from wait(s_full[w], s_cnt)
+                s_cnt += 1
+                if not checked:
+                    yield from wait(o1_free, rr - 1)
+                    checked = True
+                p_full[w].arrive()
+            if my_n > 0:
+                yield from wait(pv_done[w], pv_cnt)
+                pv_cnt += 1
+            if w == 1:
+                if not checked:
+                    yield from wait(o1_free, rr - 1)
+                merge.arrive()
+                continue
+            yield from wait(merge, rr)
+            o1_free.arrive()
+
+    agents = [k_producer(), v_producer(), mma_warp(), softmax(0), softmax(1)]
+    live = list(range(len(agents)))
+    idle = 0  # scheduling steps since anything changed
+    while live or tma or mma or any(not d for d, _ in cpa):
+        before = (Bar.changes, len(tma), len(mma), len(cpa), len(live))
+        events = []
+        if tma:
+            events.append("tma")
+        if mma:
+            events.append("mma")
+        if any(not d for d, _ in cpa):
+            events.append("cpa")
+        choice = rnd.choice(live + events)
+        if choice == "tma":
+            tma.pop(rnd.randrange(len(tma))).arrive()
+        elif choice == "mma":
+            mma.pop(0).arrive()
+        elif choice == "cpa":
+            next(e for e in cpa if not e[0])[0] = True
+            Bar.changes += 1
+        else:
+            try:
+                next(agents[choice])
+            except StopIteration:
+                live.remove(choice)
+        if (Bar.changes, len(tma), len(mma), len(cpa), len(live)) == before:
+            idle += 1
+            if idle > 20000:
+                raise Deadlock("every role waits and nothing is in flight")
+        else:
+            idle = 0
+    return True
+
+
+CASES = [(n_items, nch) for n_items in (1, 2, 5) for nch in (1, 2, 3, 5, 9)]
+
+
+@pytest.mark.parametrize("n_items,nch", CASES)
+def test_sparse_forward_protocol_is_sound(n_items, nch):
+    for seed in range(40):
+        assert sparse_fwd_model(n_items, nch, nslot=5, kslots=2, seed=seed)
+
+
+def test_sparse_forward_protocol_other_slot_splits():
+    for nslot, kslots in ((4, 2), (8, 2), (8, 4)):
+        for seed in range(20):
+            assert sparse_fwd_model(4, 5, nslot, kslots, seed=seed)
+
+
+def test_shared_ring_under_two_producers_is_caught():
+    caught = 0
+    for seed in range(200):
+        try:
+            sparse_fwd_model(6, 5, nslot=5, kslots=2, shared_ring=True, seed=seed)
+        except (Aliasing, Deadlock):
+            caught += 1
+    assert caught > 0

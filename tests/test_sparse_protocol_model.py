@@ -1,4 +1,4 @@
-"""A CPU model of the sparse forward kernel's barrier protocol.
+"""CPU models of the sparse kernels' barrier protocols.
 
 The kernel's roles (K producer, V producer, MMA issuer, two softmax
 warpgroups) are written as programs over mbarriers with the hardware's wait
@@ -12,6 +12,11 @@ deadlock). The same model with K and V sharing one ring under two producers
 -- a layout that misbehaved on the GPU -- must be caught: the K producer's
 closing wait for its last copies then targets slots that the V producer
 reuses afterwards, so the phase it waits for has already been passed.
+
+The backward's protocol (K producer with the token's Q/dO, V producer with
+one slot, MMA issuer, compute warps) is modelled the same way; its first
+version, one producer that waited for the previous token's products before
+issuing anything for the next token, must deadlock as it did on the GPU.
 
 CPU only; no kernel code is involved.
 """
@@ -175,38 +180,7 @@ def sparse_fwd_model(n_items, nch, nslot, kslots, shared_ring=False, seed=0):
             yield from wait(merge, rr)
             o1_free.arrive()
 
-    agents = [k_producer(), v_producer(), mma_warp(), softmax(0), softmax(1)]
-    live = list(range(len(agents)))
-    idle = 0  # scheduling steps since anything changed
-    while live or tma or mma or any(not d for d, _ in cpa):
-        before = (Bar.changes, len(tma), len(mma), len(cpa), len(live))
-        events = []
-        if tma:
-            events.append("tma")
-        if mma:
-            events.append("mma")
-        if any(not d for d, _ in cpa):
-            events.append("cpa")
-        choice = rnd.choice(live + events)
-        if choice == "tma":
-            tma.pop(rnd.randrange(len(tma))).arrive()
-        elif choice == "mma":
-            mma.pop(0).arrive()
-        elif choice == "cpa":
-            next(e for e in cpa if not e[0])[0] = True
-            Bar.changes += 1
-        else:
-            try:
-                next(agents[choice])
-            except StopIteration:
-                live.remove(choice)
-        if (Bar.changes, len(tma), len(mma), len(cpa), len(live)) == before:
-            idle += 1
-            if idle > 20000:
-                raise Deadlock("every role waits and nothing is in flight")
-        else:
-            idle = 0
-    return True
+    return _run([k_producer(), v_producer(), mma_warp(), softmax(0), softmax(1)], (tma, mma, cpa), rnd)
 
 
 CASES = [(n_items, nch) for n_items in (1, 2, 5) for nch in (1, 2, 3, 5, 9)]
@@ -232,3 +206,173 @@ def test_shared_ring_under_two_producers_is_caught():
         except (Aliasing, Deadlock):
             caught += 1
     assert caught > 0
+
+
+def _run(agents, queues, rnd):
+    """Interleave the agents and the asynchronous completions; raise Deadlock
+    when nothing changes for a long stretch."""
+    tma, mma, cpa = queues
+    live = list(range(len(agents)))
+    idle = 0
+    while live or tma or mma or any(not d for d, _ in cpa):
+        before = (Bar.changes, len(tma), len(mma), len(cpa), len(live))
+        events = (["tma"] if tma else []) + (["mma"] if mma else []) + \
+                 (["cpa"] if any(not d for d, _ in cpa) else [])
+        choice = rnd.choice(live + events)
+        if choice == "tma":
+            tma.pop(rnd.randrange(len(tma))).arrive()
+        elif choice == "mma":
+            mma.pop(0).arrive()
+        elif choice == "cpa":
+            next(e for e in cpa if not e[0])[0] = True
+            Bar.changes += 1
+        else:
+            try:
+                next(agents[choice])
+            except StopIteration:
+                live.remove(choice)
+        if (Bar.changes, len(tma), len(mma), len(cpa), len(live)) == before:
+            idle += 1
+            if idle > 20000:
+                raise Deadlock("every role waits and nothing is in flight")
+        else:
+            idle = 0
+    return True
+
+
+def sparse_bwd_model(n_items, nch, kslots=2, single_producer_no_flush=False, seed=0):
+    """The backward kernel's roles: K producer (Q/dO/row vectors per token, K
+    chunks by TMA into kslots slots), V producer (cp.async into one slot, each
+    chunk reported once it has landed), MMA issuer, and the compute warps
+    (P/dS, then the drain). With single_producer_no_flush, one producer
+    gathers K and V with cp.async into a shared ring of kslots + 1 slots,
+    keeps one position in flight and waits for the previous token's products
+    before issuing anything for the next token (the first version)."""
+    rnd = random.Random(seed)
+    nslot = kslots + 1
+    vs = kslots
+    full = [Bar(1) for _ in range(nslot)]
+    empty = [Bar(1) for _ in range(nslot)]
+    q_full, q_empty = Bar(1), Bar(1)
+    sdp_full, pds_full, grads_full, drain_done = Bar(1), Bar(1), Bar(1), Bar(1)
+    tma, mma, cpa = [], [], []
+
+    def kslot(g):
+        return (2 * g) % nslot if single_producer_no_flush else g % kslots
+
+    def kround(g):
+        return (2 * g) // nslot if single_producer_no_flush else g // kslots
+
+    def vslot(g):
+        return (2 * g + 1) % nslot if single_producer_no_flush else vs
+
+    def vround(g):
+        return (2 * g + 1) // nslot if single_producer_no_flush else g
+
+    def k_producer():
+        last = -1
+        for r in range(n_items):
+            def load_k(c):
+                nonlocal last
+                g = r * nch + c
+                if kround(g) > 0:
+                    yield from wait(empty[kslot(g)], kround(g) - 1)
+                tma.append(full[kslot(g)])
+                last = g
+            if r > 0:
+                yield from load_k(0)
+                yield from wait(q_empty, r - 1)
+            tma.append(q_full)
+            for c in range(1 if r > 0 else 0, nch):
+                yield from load_k(c)
+        for g in range(max(0, last - kslots + 1), last + 1):
+            yield from wait(full[kslot(g)], kround(g))
+        yield from wait(q_full, n_items - 1)
+
+    def v_producer():
+        for r in range(n_items):
+            for c in range(nch):
+                g = r * nch + c
+                if g > 0:
+                    yield from wait(empty[vs], g - 1)
+                cpa.append([False, vs])
+                while not cpa[-1][0]:
+                    yield
+                full[vs].arrive()
+
+    def single_producer():
+        issued, signalled, pend = 0, 0, []
+        for r in range(n_items):
+            if r > 0:
+                yield from wait(q_empty, r - 1)
+            tma.append(q_full)
+            for pos in range(2 * nch):
+                g, is_v = r * nch + pos // 2, pos & 1
+                slot, rnd_ = (vslot(g), vround(g)) if is_v else (kslot(g), kround(g))
+                if rnd_ > 0:
+                    yield from wait(empty[slot], rnd_ - 1)
+                cpa.append([False, slot])
+                pend.append(len(cpa) - 1)
+                issued += 1
+                if issued - signalled > 1:
+                    while not cpa[pend[signalled]][0]:
+                        yield
+                    full[cpa[pend[signalled]][1]].arrive()
+                    signalled += 1
+        while signalled < issued:
+            while not cpa[pend[signalled]][0]:
+                yield
+            full[cpa[pend[signalled]][1]].arrive()
+            signalled += 1
+
+    def mma_warp():
+        chunk = 0
+        for r in range(n_items):
+            yield from wait(q_full, r)
+            for c in range(nch):
+                g = r * nch + c
+                if chunk > 0:
+                    yield from wait(drain_done, chunk - 1)
+                yield from wait(full[kslot(g)], kround(g))
+                yield from wait(full[vslot(g)], vround(g))
+                mma.append(sdp_full)
+                mma.append(empty[vslot(g)])
+                yield from wait(pds_full, chunk)
+                mma.append(grads_full)
+                mma.append(empty[kslot(g)])
+                if c + 1 == nch:
+                    mma.append(q_empty)
+                chunk += 1
+
+    def compute():
+        chunk = 0
+        for r in range(n_items):
+            yield from wait(q_full, r)
+            for c in range(nch):
+                yield from wait(sdp_full, chunk)
+                pds_full.arrive()
+                yield from wait(grads_full, chunk)
+                drain_done.arrive()
+                chunk += 1
+
+    producers = [single_producer()] if single_producer_no_flush else [k_producer(), v_producer()]
+    return _run(producers + [mma_warp(), compute()], (tma, mma, cpa), rnd)
+
+
+@pytest.mark.parametrize("n_items,nch", CASES)
+def test_sparse_backward_protocol_is_sound(n_items, nch):
+    for seed in range(40):
+        assert sparse_bwd_model(n_items, nch, seed=seed)
+
+
+def test_sparse_backward_protocol_more_k_slots():
+    for seed in range(20):
+        assert sparse_bwd_model(4, 5, kslots=3, seed=seed)
+
+
+def test_single_producer_without_flush_deadlocks():
+    """The first backward version stopped on its bounded waits whenever a CTA
+    had more than one token; the model reproduces that."""
+    with pytest.raises(Deadlock):
+        sparse_bwd_model(3, 2, single_producer_no_flush=True, seed=0)
+    assert sparse_bwd_model(1, 5, single_producer_no_flush=True, seed=0)  # one token: fine

@@ -230,8 +230,8 @@ __global__ void __launch_bounds__(SparseFwdCfg<DK, DV>::THREADS, 1)
     // Each copy instruction of the warp moves UNITS 16-byte units of each of
     // 32 / UNITS rows (whole rows, contiguous in global memory); row j's unit
     // u lands at j * 128 + ((u % 8) ^ (j % 8)) * 16 in 64-column block u / 8.
-    // One position's copies stay in flight: V_c is reported once V_{c+1} has
-    // been issued (releasing any earlier position needs nothing later).
+    // V_IN_FLIGHT chunks' copies stay in flight: V_c is reported once V_{c+1}
+    // has been issued (releasing an earlier V chunk needs nothing later).
     int* idx_s = reinterpret_cast<int*>(smem + C::SMEM_IDX);
     int issued = 0, signalled = 0;
     int pend[4];
@@ -275,8 +275,8 @@ __global__ void __launch_bounds__(SparseFwdCfg<DK, DV>::THREADS, 1)
         cp_async_commit();
         pend[issued & 3] = slot;
         ++issued;
-        if (issued - signalled > 1) {
-          cp_async_wait<1>();
+        if (issued - signalled > C::V_IN_FLIGHT) {
+          cp_async_wait<C::V_IN_FLIGHT>();
           signal_oldest();
         }
       }

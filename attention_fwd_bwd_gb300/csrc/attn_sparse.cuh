@@ -35,10 +35,6 @@ struct SparseFwdCfg {
   static constexpr int SMEM_MERGE = SMEM_STG + 2 * STG_BYTES;
   static constexpr int SMEM_IDX = SMEM_MERGE + MERGE_BYTES;
   static constexpr int SMEM_BYTES = SMEM_IDX + IDX_BYTES;
-  // Ring positions whose copies may still be in flight while the producer
-  // issues the next one. Releasing position x needs positions up to x + 1
-  // (the MMA warp issues S(c+1) before P.V(c)), so it stays below NSLOT - 1.
-  static constexpr int COPY_DEPTH = 2;
   static constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;
   // Tensor memory per softmax warpgroup w: scores S_w (128 columns, later P_w
   // as bf16 hi/lo pairs) and the output accumulator O_w (DV columns).
@@ -46,13 +42,18 @@ struct SparseFwdCfg {
   __host__ __device__ static constexpr int tm_o(int w) { return 256 * w + 128; }
   static constexpr int TMEM_COLS = 512;
   // K and V come from two producers, so they use separate slots: slots
-  // 0..KSLOTS-1 hold K chunks in turn, the rest V chunks in turn. Each slot's
-  // barriers then see their phases in order.
+  // 0..KSLOTS-1 hold K chunks in turn, the rest V chunks in turn, and each
+  // producer's closing wait for its last copies finds those slots' last
+  // phases its own.
   static constexpr int KSLOTS = 2;
   static constexpr int VSLOTS = NSLOT - KSLOTS;
+  // V chunks whose copies stay in flight while the V producer issues the
+  // next one. Its next chunk waits for the release of the chunk VSLOTS back,
+  // which must not be one of them.
+  static constexpr int V_IN_FLIGHT = 1;
   static constexpr int THREADS = 352;  // 8 softmax warps, K producer, MMA issuer, V producer
   static_assert(NSLOT >= 4, "the ring needs at least two chunks of K and V");
-  static_assert(COPY_DEPTH < NSLOT - 1, "copies in flight would block the ring");
+  static_assert(V_IN_FLIGHT < VSLOTS, "copies in flight would block the V slots");
   static_assert(SMEM_ALLOC <= 232448, "shared-memory plan exceeds 227 KB");
 };
 

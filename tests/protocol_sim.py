@@ -1,0 +1,66 @@
+"""Shared pieces of the CPU protocol models (test infrastructure): mbarriers
+with the hardware's phase and parity semantics, a checked wait, and a random
+interleaver of role programs and asynchronous completions."""
+
+
+class Bar:
+    changes = 0  # every arrival counts as progress
+
+    def __init__(self, count):
+        self.count, self.pending, self.completed = count, count, 0
+
+    def arrive(self):
+        Bar.changes += 1
+        self.pending -= 1
+        if self.pending == 0:
+            self.completed += 1
+            self.pending = self.count
+
+
+class Aliasing(Exception):
+    pass
+
+
+class Deadlock(Exception):
+    pass
+
+
+def wait(bar, phase):
+    """A generator step: block until the hardware would report the phase with
+    parity phase & 1 complete; then check that it really is `phase`."""
+    while (bar.completed & 1) == (phase & 1):
+        yield
+    if bar.completed != phase + 1:
+        raise Aliasing(f"wait for phase {phase} passed with {bar.completed} phases completed")
+
+
+def run(agents, queues, rnd):
+    """Interleave the agents and the asynchronous completions; raise Deadlock
+    when nothing changes for a long stretch."""
+    tma, mma, cpa = queues
+    live = list(range(len(agents)))
+    idle = 0
+    while live or tma or mma or any(not d for d, _ in cpa):
+        before = (Bar.changes, len(tma), len(mma), len(cpa), len(live))
+        events = (["tma"] if tma else []) + (["mma"] if mma else []) + \
+                 (["cpa"] if any(not d for d, _ in cpa) else [])
+        choice = rnd.choice(live + events)
+        if choice == "tma":
+            tma.pop(rnd.randrange(len(tma))).arrive()
+        elif choice == "mma":
+            mma.pop(0).arrive()
+        elif choice == "cpa":
+            next(e for e in cpa if not e[0])[0] = True
+            Bar.changes += 1
+        else:
+            try:
+                next(agents[choice])
+            except StopIteration:
+                live.remove(choice)
+        if (Bar.changes, len(tma), len(mma), len(cpa), len(live)) == before:
+            idle += 1
+            if idle > 20000:
+                raise Deadlock("every role waits and nothing is in flight")
+        else:
+            idle = 0
+    return True

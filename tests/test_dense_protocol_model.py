@@ -1,0 +1,253 @@
+"""CPU models of the dense kernels' barrier protocols, in the same form as
+the sparse ones: the roles run as programs over mbarriers with the hardware's
+parity semantics, copies and MMA commits complete asynchronously (TMA in any
+order, MMA commits in issue order), and random interleavings must neither
+pass a wait on the wrong phase nor deadlock.
+
+Forward: the persistent kernel -- a producer that preloads the next item's
+first K/V tiles before waiting for the Q buffer, an MMA issuer that
+alternates two query tiles, and two softmax warpgroups -- over the items of
+causal, non-causal, ragged and sliding-window problems. Backward: one
+key-tile CTA with its three-stage Q/dO ring, in both dQ modes (the P/dS warps
+reading dQ^T and staging it for one reduction warp, as for D = 64; four drain
+warps, as for D = 128).
+
+CPU only; no kernel code is involved.
+"""
+import random
+
+import pytest
+
+from tests.protocol_sim import Bar, run, wait
+
+
+def fwd_items(S, causal, window=0):
+    """(n_kv[0], n_kv[1], jlo[0], jlo[1]) of every item, longest first (one
+    head; a CTA that takes them all in that order)."""
+    BQ = BK = 128
+    nkv_all = (S + BK - 1) // BK
+    n_qb = (S + 2 * BQ - 1) // (2 * BQ)
+    items = []
+    for i in range(n_qb):
+        q0 = (n_qb - 1 - i) * 2 * BQ
+        n_kv, jlo = [], []
+        for t in range(2):
+            qt0 = q0 + t * BQ
+            n = min(qt0 // BK + 1, nkv_all) if causal else nkv_all
+            n_kv.append(n)
+            jlo.append(min(max(0, qt0 - window + 1) // BK, n - 1) if window else 0)
+        items.append((n_kv[0], n_kv[1], jlo[0], jlo[1]))
+    return items
+
+
+def dense_fwd_model(items, nslot, win=False, seed=0, release_unused=False):
+    rnd = random.Random(seed)
+    kv_full = [Bar(1) for _ in range(nslot)]
+    kv_empty = [Bar(1) for _ in range(nslot)]
+    q_full, q_empty, mma_done = Bar(1), Bar(1), Bar(1)
+    s_full, p_full, pv_done = [Bar(1), Bar(1)], [Bar(1), Bar(1)], [Bar(1), Bar(1)]
+    tma, mma = [], []
+
+    def producer():
+        issued = q_loads = 0
+        for r, (n0, n1, l0, l1) in enumerate(items):
+            n_pos = 2 * (n1 - l0)
+
+            def load_kv():
+                nonlocal issued
+                slot, rnd_ = issued % nslot, issued // nslot
+                if rnd_ > 0:
+                    yield from wait(kv_empty[slot], rnd_ - 1)
+                tma.append(kv_full[slot])
+                issued += 1
+            pre = 0 if r == 0 else min(2, n_pos)
+            for _ in range(pre):
+                yield from load_kv()
+            if r > 0:
+                yield from wait(q_empty, r - 1)
+            tma.append(q_full)
+            q_loads += 1
+            for _ in range(pre, n_pos):
+                yield from load_kv()
+        for pos in range(max(0, issued - nslot), issued):
+            yield from wait(kv_full[pos % nslot], pos // nslot)
+        yield from wait(q_full, q_loads - 1)
+
+    def mma_warp():
+        ring, p_cnt = 0, [0, 0]
+        for r, (n0, n1, l0, l1) in enumerate(items):
+            n_kv, jlo, jb = (n0, n1), (l0, l1), l0
+            yield from wait(q_full, r)
+            s_left = [(n0 - l0) + (n1 - l1)]
+
+            def issue_s(t):
+                mma.append(s_full[t])
+                s_left[0] -= 1
+                if s_left[0] == 0:
+                    mma.append(q_empty)
+
+            def wait_kv(idx):
+                q = ring + idx
+                yield from wait(kv_full[q % nslot], q // nslot)
+
+            def slot(idx):
+                return (ring + idx) % nslot
+            yield from wait_kv(0)
+            issue_s(0)
+            if jlo[1] == jb:
+                issue_s(1)
+            mma.append(kv_empty[slot(0)])
+            for j in range(jb, n1):
+                v_ready = k_next = False
+                for t in range(2):
+                    if jlo[t] <= j < n_kv[t]:
+                        yield from wait(p_full[t], p_cnt[t])
+                        p_cnt[t] += 1
+                        if not v_ready:
+                            yield from wait_kv(2 * (j - jb) + 1)
+                            v_ready = True
+                        if j + 1 == n_kv[t]:
+                            mma.append(pv_done[t])
+                    if j + 1 < n_kv[t] and j + 1 >= jlo[t]:
+                        if not k_next:
+                            yield from wait_kv(2 * (j - jb) + 2)
+                            k_next = True
+                        issue_s(t)
+                # With a window, a tile that skips j still leaves no copy in flight.
+                if win and not v_ready:
+                    yield from wait_kv(2 * (j - jb) + 1)
+                if win and j + 1 < n1 and not k_next:
+                    yield from wait_kv(2 * (j - jb) + 2)
+                    k_next = True
+                mma.append(kv_empty[slot(2 * (j - jb) + 1)])
+                if k_next or release_unused:
+                    mma.append(kv_empty[slot(2 * (j - jb) + 2)])
+            ring += 2 * (n1 - jb)
+        mma.append(mma_done)
+        yield from wait(mma_done, 0)
+
+    def softmax(t):
+        s_cnt = 0
+        for item, it in enumerate(items):
+            n_kv, jlo = it[t], it[2 + t]
+            for _ in range(jlo, n_kv):
+                yield from wait(s_full[t], s_cnt)
+                s_cnt += 1
+                p_full[t].arrive()
+            yield from wait(pv_done[t], item)
+
+    return run([producer(), mma_warp(), softmax(0), softmax(1)], (tma, mma, []), rnd)
+
+
+FWD_CASES = [
+    (1024, True, 0), (1024, False, 0), (900, True, 0), (256, True, 0), (128, False, 0),
+    (2048, True, 128), (1000, True, 200), (1024, True, 1), (640, True, 384),
+]
+
+
+@pytest.mark.parametrize("S,causal,window", FWD_CASES)
+@pytest.mark.parametrize("nslot", [4, 8])
+def test_dense_forward_protocol_is_sound(S, causal, window, nslot):
+    items = fwd_items(S, causal, window)
+    for seed in range(25):
+        assert dense_fwd_model(items, nslot, win=window > 0, seed=seed)
+
+
+def dense_bwd_model(n_it, dq_in_compute, stages=3, seed=0, stage_last=True):
+    rnd = random.Random(seed)
+    kv_full, mma_done = Bar(1), Bar(1)
+    st_full = [Bar(1) for _ in range(stages)]
+    st_empty = [Bar(1) for _ in range(stages)]
+    sdp_full, sdp_free = Bar(1), Bar(2)      # two P/dS warp groups arrive
+    pds_full, pds_free = Bar(2), Bar(1)
+    dq_full, dq_free = Bar(1), Bar(1)
+    stg_full, stg_free = [Bar(1), Bar(1)], [Bar(1), Bar(1)]
+    tma, mma = [], []
+
+    def producer():
+        tma.append(kv_full)
+        for it in range(n_it):
+            s, rnd_ = it % stages, it // stages
+            if rnd_ > 0:
+                yield from wait(st_empty[s], rnd_ - 1)
+            tma.append(st_full[s])
+        for it in range(max(0, n_it - stages), n_it):
+            yield from wait(st_full[it % stages], it // stages)
+        yield from wait(kv_full, 0)
+
+    def mma_warp():
+        yield from wait(kv_full, 0)
+        if n_it > 0:
+            yield from wait(st_full[0], 0)
+            mma.append(sdp_full)
+        for it in range(n_it):
+            if it + 1 < n_it:
+                s1 = (it + 1) % stages
+                yield from wait(st_full[s1], (it + 1) // stages)
+                yield from wait(sdp_free, it)
+                mma.append(sdp_full)
+            yield from wait(pds_full, it)
+            mma.append(st_empty[it % stages])
+            if not dq_in_compute and it >= 1:
+                yield from wait(dq_free, it - 1)
+            if not dq_in_compute:
+                mma.append(dq_full)
+            mma.append(pds_free)
+        mma.append(mma_done)
+        yield from wait(mma_done, 0)
+
+    def compute(cg):
+        def stage(itq):
+            if itq >= 1:
+                yield from wait(stg_free[cg], itq - 1)
+            stg_full[cg].arrive()
+        for it in range(n_it):
+            yield from wait(sdp_full, it)
+            yield from wait(st_full[it % stages], it // stages)
+            sdp_free.arrive()
+            if it >= 1:
+                yield from wait(pds_free, it - 1)
+            if not dq_in_compute and it >= 1:
+                yield from wait(dq_free, it - 1)
+            pds_full.arrive()
+            if dq_in_compute and it >= 1:
+                yield from stage(it - 1)
+        if dq_in_compute and n_it > 0 and stage_last:
+            yield from wait(pds_free, n_it - 1)
+            yield from stage(n_it - 1)
+        yield from wait(mma_done, 0)
+
+    def reduce_warp():
+        for n in range(2 * n_it):
+            yield from wait(stg_full[n & 1], n >> 1)
+            stg_free[n & 1].arrive()
+
+    def drain_warps():
+        for it in range(n_it):
+            yield from wait(dq_full, it)
+            dq_free.arrive()
+
+    agents = [producer(), mma_warp(), compute(0), compute(1)]
+    agents.append(reduce_warp() if dq_in_compute else drain_warps())
+    return run(agents, (tma, mma, []), rnd)
+
+
+@pytest.mark.parametrize("n_it", [0, 1, 2, 3, 4, 7, 16])
+@pytest.mark.parametrize("dq_in_compute", [True, False])
+def test_dense_backward_protocol_is_sound(n_it, dq_in_compute):
+    for seed in range(40):
+        assert dense_bwd_model(n_it, dq_in_compute, seed=seed)
+
+
+def test_dense_models_catch_planted_mistakes():
+    """The models are not vacuous: a forward MMA issuer that also releases
+    the slot after an item's last V tile (which holds no K tile of this item)
+    hands out a slot phase too early, and a backward whose P/dS warps never
+    stage the last dQ tile leaves the reduction warp waiting."""
+    from tests.protocol_sim import Aliasing, Deadlock
+    for seed in range(10):
+        with pytest.raises((Aliasing, Deadlock)):
+            dense_fwd_model(fwd_items(1024, True), 4, seed=seed, release_unused=True)
+    with pytest.raises(Deadlock):
+        dense_bwd_model(3, True, seed=0, stage_last=False)
+

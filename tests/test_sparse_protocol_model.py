@@ -24,36 +24,7 @@ import random
 
 import pytest
 
-
-class Bar:
-    changes = 0  # every arrival counts as progress
-
-    def __init__(self, count):
-        self.count, self.pending, self.completed = count, count, 0
-
-    def arrive(self):
-        Bar.changes += 1
-        self.pending -= 1
-        if self.pending == 0:
-            self.completed += 1
-            self.pending = self.count
-
-
-class Aliasing(Exception):
-    pass
-
-
-class Deadlock(Exception):
-    pass
-
-
-def wait(bar, phase):
-    """A generator step: block until the hardware would report the phase with
-    parity phase & 1 complete; then check that it really is `phase`."""
-    while (bar.completed & 1) == (phase & 1):
-        yield
-    if bar.completed != phase + 1:
-        raise Aliasing(f"wait for phase {phase} passed with {bar.completed} phases completed")
+from tests.protocol_sim import Aliasing, Bar, Deadlock, run, wait
 
 
 def sparse_fwd_model(n_items, nch, nslot, kslots, shared_ring=False, seed=0):
@@ -180,7 +151,7 @@ def sparse_fwd_model(n_items, nch, nslot, kslots, shared_ring=False, seed=0):
             yield from wait(merge, rr)
             o1_free.arrive()
 
-    return _run([k_producer(), v_producer(), mma_warp(), softmax(0), softmax(1)], (tma, mma, cpa), rnd)
+    return run([k_producer(), v_producer(), mma_warp(), softmax(0), softmax(1)], (tma, mma, cpa), rnd)
 
 
 CASES = [(n_items, nch) for n_items in (1, 2, 5) for nch in (1, 2, 3, 5, 9)]
@@ -206,38 +177,6 @@ def test_shared_ring_under_two_producers_is_caught():
         except (Aliasing, Deadlock):
             caught += 1
     assert caught > 0
-
-
-def _run(agents, queues, rnd):
-    """Interleave the agents and the asynchronous completions; raise Deadlock
-    when nothing changes for a long stretch."""
-    tma, mma, cpa = queues
-    live = list(range(len(agents)))
-    idle = 0
-    while live or tma or mma or any(not d for d, _ in cpa):
-        before = (Bar.changes, len(tma), len(mma), len(cpa), len(live))
-        events = (["tma"] if tma else []) + (["mma"] if mma else []) + \
-                 (["cpa"] if any(not d for d, _ in cpa) else [])
-        choice = rnd.choice(live + events)
-        if choice == "tma":
-            tma.pop(rnd.randrange(len(tma))).arrive()
-        elif choice == "mma":
-            mma.pop(0).arrive()
-        elif choice == "cpa":
-            next(e for e in cpa if not e[0])[0] = True
-            Bar.changes += 1
-        else:
-            try:
-                next(agents[choice])
-            except StopIteration:
-                live.remove(choice)
-        if (Bar.changes, len(tma), len(mma), len(cpa), len(live)) == before:
-            idle += 1
-            if idle > 20000:
-                raise Deadlock("every role waits and nothing is in flight")
-        else:
-            idle = 0
-    return True
 
 
 def sparse_bwd_model(n_items, nch, kslots=2, single_producer_no_flush=False, seed=0):
@@ -356,7 +295,7 @@ def sparse_bwd_model(n_items, nch, kslots=2, single_producer_no_flush=False, see
                 chunk += 1
 
     producers = [single_producer()] if single_producer_no_flush else [k_producer(), v_producer()]
-    return _run(producers + [mma_warp(), compute()], (tma, mma, cpa), rnd)
+    return run(producers + [mma_warp(), compute()], (tma, mma, cpa), rnd)
 
 
 @pytest.mark.parametrize("n_items,nch", CASES)

@@ -167,3 +167,9 @@ def test_build_hash_covers_every_source_and_header():
     from attention_fwd_bwd_gb300 import _build as B
     present = sorted(f for f in os.listdir(B.CSRC) if f.endswith((".cu", ".cuh")))
     assert sorted(B.SOURCES + B.HEADERS) == present
+
+
+def test_binding_covers_every_entry_point():
+    import attention_fwd_bwd_gb300 as attn
+    for n in _declared():
+        assert n in attn.__all__ and callable(getattr(attn, n)), f"no Python binding for {n}"

@@ -524,6 +524,9 @@ def main():
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     from attention_fwd_bwd_gb300.inputs import BY_NAME, SPARSE_BY_NAME
+    if args.workload not in BY_NAME and args.workload not in SPARSE_BY_NAME:
+        ap.error(f"unknown workload {args.workload!r}; dense: {', '.join(BY_NAME)}; "
+                 f"sparse: {', '.join(SPARSE_BY_NAME)}")
     sparse = args.workload in SPARSE_BY_NAME
     w = SPARSE_BY_NAME[args.workload] if sparse else BY_NAME[args.workload]
     world, rank, local = dist_env()

@@ -471,27 +471,25 @@ __global__ void __launch_bounds__(SparseFwdCfg<DK, DV>::THREADS, 1)
         }
         mbar_arrive(smem_u32(&bar_p_full[w]));
       }
-      if (!ok) break;
-      if (my_n > 0) {
+      if (ok && my_n > 0) {
         ok = mbar_wait_warp(smem_u32(&bar_pv_done[w]), pv_cnt & 1, ctl);
         ++pv_cnt;
-        if (!ok) break;
       }
       if (w == 1) {
         // Hand (m, l) to warpgroup 0, which merges and stores the item.
-        if (!o1_checked) {
-          ok = mbar_wait_warp(smem_u32(&bar_o1_free), (rr - 1) & 1, ctl);
-          if (!ok) break;
-        }
+        if (ok && !o1_checked) ok = mbar_wait_warp(smem_u32(&bar_o1_free), (rr - 1) & 1, ctl);
+        if (!ok) break;
         merge_m[r] = m;
         merge_l[r] = l;
         tc_fence_before();
         mbar_arrive(smem_u32(&bar_merge));
         continue;
       }
-      // ---- warpgroup 0: merge, normalise, store.
-      ok = mbar_wait_warp(smem_u32(&bar_merge), rr & 1, ctl);
-      ok = named_bar_and(1, 128, ok);  // the four warps meet at named barriers below
+      // ---- warpgroup 0: merge, normalise, store. Every warp of the group
+      // reaches this consensus, also after one of its waits gave up, so none
+      // can be left at the named barriers below.
+      if (ok) ok = mbar_wait_warp(smem_u32(&bar_merge), rr & 1, ctl);
+      ok = named_bar_and(1, 128, ok);
       if (!ok) break;
       tc_fence_after();
       const float m1 = merge_m[r], l1 = merge_l[r];

@@ -33,6 +33,8 @@
  *    device status word.
  *  - Arguments are validated before any launch; a failed check launches
  *    nothing and returns the code named below.
+ *  - The sparse top-k entry points (attn_sparse_*) take their own layouts
+ *    (per-token lists over a key/value pool), stated at their declarations.
  */
 #ifndef ATTN_GB300_ATTN_H_
 #define ATTN_GB300_ATTN_H_
@@ -47,7 +49,7 @@ extern "C" {
 typedef enum {
   ATTN_OK = 0,
   ATTN_ERR_INVALID_ARG = 1, /* null or misaligned pointer, bad size or scale */
-  ATTN_ERR_UNSUPPORTED = 2, /* valid but unsupported: D not in {64,128}, no sm_100-family GPU */
+  ATTN_ERR_UNSUPPORTED = 2, /* valid but unsupported: D not in {64,128}, not an sm_103 GPU */
   ATTN_ERR_CUDA = 3,        /* a CUDA runtime or driver call failed */
   ATTN_ERR_TIMEOUT = 4,     /* a kernel's bounded pipeline wait ran out (reported via status) */
   ATTN_ERR_WORKSPACE = 5    /* workspace null, misaligned or smaller than attn_bwd_workspace_size */

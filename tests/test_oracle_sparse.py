@@ -226,3 +226,34 @@ def test_sparse_pins_catch_mutant(name, old, new):
         except Exception:
             caught.append(True)
     assert any(caught), name
+
+
+def _golden_ok(m):
+    import json
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", "sparse_closed_form_t3_d1.json")
+    with open(path) as f:
+        fx = json.load(f)
+    ev = lambda s: float(eval(s, {"__builtins__": {}}, {"ln": math.log, "inf": math.inf}))
+    vec = lambda key: np.array([ev(s) for s in fx[key]])
+    q = vec("q").reshape(1, 3, 1, 1)
+    do = vec("do").reshape(1, 3, 1, 1)
+    kp, vp = vec("kp").reshape(1, 3, 1), vec("vp").reshape(1, 3, 1)
+    idx = np.array(fx["idx"], dtype=np.int32)[None]
+    o, lse = m.sparse_ref_fwd(q, kp, vp, idx, fx["scale"])
+    dq, dkp, dvp = m.sparse_ref_bwd(q, kp, vp, idx, do, fx["scale"])
+    lse_exp = vec("lse")
+    fin = np.isfinite(lse_exp)
+    return (np.allclose(o.ravel(), vec("o"), atol=1e-12)
+            and np.array_equal(np.isfinite(lse.ravel()), fin)
+            and np.allclose(lse.ravel()[fin], lse_exp[fin], atol=1e-12)
+            and np.allclose(dq.ravel(), vec("dq"), atol=1e-12)
+            and np.allclose(dkp.ravel(), vec("dkp"), atol=1e-12)
+            and np.allclose(dvp.ravel(), vec("dvp"), atol=1e-12))
+
+
+PINS.append(_golden_ok)
+
+
+def test_sparse_oracle_golden_worked_example():
+    assert _golden_ok(sparse_mod)

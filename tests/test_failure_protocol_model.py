@@ -1,0 +1,255 @@
+"""CPU model of the sparse forward kernel's failure path.
+
+Every mbarrier wait in the kernels is bounded: it gives up after a time limit,
+or at its next poll once another role has raised the CTA's abort flag, and
+the role then leaves by its exit path. Named barriers have no time limit, so
+the warps that meet at one must all get there. This model runs the sparse
+forward's roles warp by warp (the two softmax warpgroups as four warps each)
+with waits that may give up at any moment -- a timeout racing a phase that
+completes just after it -- and with the MMA warp stalled (the testing hook),
+and requires every run to end, i.e. every warp to reach the kernel's closing
+__syncthreads. The control flow from before the epilogue-consensus fix, where
+a warp could leave the item loop before warpgroup 0's consensus, must be
+caught hanging at the named barrier.
+
+CPU only; no kernel code is involved.
+"""
+import random
+
+import pytest
+
+from tests.protocol_sim import Bar, Deadlock, run
+
+POLL_LIMIT = 400  # polls before a blocked wait runs out of time
+
+
+class Ctl:
+    def __init__(self, rnd, p_giveup, poll_limit):
+        self.abort, self.rnd, self.p, self.limit = False, rnd, p_giveup, poll_limit
+
+
+def bwait(ctl, bar, phase, abort_aware=True):
+    """A bounded wait; returns True when the phase with parity phase & 1 is
+    reported complete, False when it gives up (and then raises the abort flag)."""
+    polls = 0
+    while (bar.completed & 1) == (phase & 1):
+        polls += 1
+        if (abort_aware and ctl.abort) or ctl.rnd.random() < ctl.p or polls > ctl.limit:
+            ctl.abort = True
+            Bar.changes += 1
+            return False
+        yield
+    return True
+
+
+class NamedBar:
+    """bar.red.and / bar.sync over n warps: no time limit."""
+
+    def __init__(self, n):
+        self.n, self.gen, self.count, self.acc, self.result = n, 0, 0, True, {}
+
+    def and_(self, ok):
+        g = self.gen
+        self.acc = self.acc and ok
+        self.count += 1
+        Bar.changes += 1
+        if self.count == self.n:
+            self.result[g], self.gen, self.count, self.acc = self.acc, self.gen + 1, 0, True
+        while self.gen == g:
+            yield
+        return self.result[g]
+
+
+def sparse_fwd_failure_model(n_items, nch, seed, p_giveup, stall_mma=False, early_break=False,
+                             nslot=5, kslots=2, poll_limit=POLL_LIMIT):
+    """Runs to the end (or raises Deadlock); returns whether any wait gave up."""
+    rnd = random.Random(seed)
+    ctl = Ctl(rnd, p_giveup, poll_limit)
+    vslots = nslot - kslots
+    full = [Bar(1) for _ in range(nslot)]
+    empty = [Bar(1) for _ in range(nslot)]
+    q_full, q_empty, mma_done = Bar(1), Bar(1), Bar(1)
+    s_full, pv_done = [Bar(1), Bar(1)], [Bar(1), Bar(1)]
+    p_full = [Bar(4), Bar(4)]       # every warp of a warpgroup arrives
+    merge, o1_free = Bar(4), Bar(4)
+    nbar = NamedBar(4)              # warpgroup 0's epilogue barrier
+    tma, mma, cpa = [], [], []
+
+    def kslot(g):
+        return g % kslots
+
+    def vslot(g):
+        return kslots + g % vslots
+
+    def k_producer():
+        ok, last, q_loads = True, -1, 0
+        for r in range(n_items):
+            if not ok:
+                break
+
+            def load_k(c):
+                nonlocal last
+                g = r * nch + c
+                if g // kslots > 0:
+                    res = yield from bwait(ctl, empty[kslot(g)], g // kslots - 1)
+                    if not res:
+                        return False
+                tma.append(full[kslot(g)])
+                last = g
+                return True
+            if r > 0:
+                ok = yield from load_k(0)
+                if not ok:
+                    break
+                ok = yield from bwait(ctl, q_empty, r - 1)
+                if not ok:
+                    break
+            tma.append(q_full)
+            q_loads += 1
+            for c in range(1 if r > 0 else 0, nch):
+                ok = yield from load_k(c)
+                if not ok:
+                    break
+        # Closing waits for copies in flight: bounded, not cut short by the abort flag.
+        for g in range(max(0, last - kslots + 1), last + 1):
+            yield from bwait(ctl, full[kslot(g)], g // kslots, abort_aware=False)
+        if q_loads:
+            yield from bwait(ctl, q_full, q_loads - 1, abort_aware=False)
+
+    def v_producer():
+        ok, issued, signalled = True, 0, 0
+        for r in range(n_items):
+            for c in range(nch):
+                if not ok:
+                    break
+                g = r * nch + c
+                if g // vslots > 0:
+                    ok = yield from bwait(ctl, empty[vslot(g)], g // vslots - 1)
+                    if not ok:
+                        break
+                cpa.append([False, vslot(g)])
+                issued += 1
+                if issued - signalled > 1:
+                    while not cpa[signalled][0]:
+                        yield
+                    full[cpa[signalled][1]].arrive()
+                    signalled += 1
+        while signalled < issued:
+            while not cpa[signalled][0]:
+                yield
+            full[cpa[signalled][1]].arrive()
+            signalled += 1
+
+    def mma_warp():
+        ok, p_cnt = not stall_mma, [0, 0]
+        for r in range(n_items):
+            if not ok:
+                break
+            ok = yield from bwait(ctl, q_full, r)
+            if not ok:
+                break
+            s_left = [nch]
+
+            def issue_s(c):
+                g = r * nch + c
+                mma.append(s_full[c & 1])
+                mma.append(empty[kslot(g)])
+                s_left[0] -= 1
+                if s_left[0] == 0:
+                    mma.append(q_empty)
+            for c in range(min(2, nch)):
+                g = r * nch + c
+                ok = yield from bwait(ctl, full[kslot(g)], g // kslots)
+                if not ok:
+                    break
+                issue_s(c)
+            for c in range(nch if ok else 0):
+                w, g = c & 1, r * nch + c
+                ok = yield from bwait(ctl, p_full[w], p_cnt[w])
+                if not ok:
+                    break
+                p_cnt[w] += 1
+                ok = yield from bwait(ctl, full[vslot(g)], g // vslots)
+                if not ok:
+                    break
+                mma.append(empty[vslot(g)])
+                if c + 2 >= nch:
+                    mma.append(pv_done[w])
+                if c + 2 < nch:
+                    ok = yield from bwait(ctl, full[kslot(g + 2)], (g + 2) // kslots)
+                    if not ok:
+                        break
+                    issue_s(c + 2)
+        mma.append(mma_done)
+        yield from bwait(ctl, mma_done, 0, abort_aware=False)
+
+    def softmax_warp(w):
+        ok, s_cnt, pv_cnt = True, 0, 0
+        my_n = (nch - w + 1) // 2 if nch > w else 0
+        for rr in range(n_items):
+            if not ok:
+                break
+            checked = w == 0 or rr == 0
+            for _ in range(my_n):
+                ok = yield from bwait(ctl, s_full[w], s_cnt)
+                if not ok:
+                    break
+                s_cnt += 1
+                if not checked:
+                    ok = yield from bwait(ctl, o1_free, rr - 1)
+                    if not ok:
+                        break
+                    checked = True
+                p_full[w].arrive()
+            if early_break and not ok:
+                break  # the control flow before the fix
+            if ok and my_n > 0:
+                ok = yield from bwait(ctl, pv_done[w], pv_cnt)
+                pv_cnt += 1
+            if w == 1:
+                if ok and not checked:
+                    ok = yield from bwait(ctl, o1_free, rr - 1)
+                if not ok:
+                    break
+                merge.arrive()
+                continue
+            if ok:
+                ok = yield from bwait(ctl, merge, rr)
+            ok = yield from nbar.and_(ok)
+            if not ok:
+                break
+            for _ in range(2):  # the staging tile's two bar.sync of the epilogue
+                yield from nbar.and_(True)
+            o1_free.arrive()
+
+    agents = [k_producer(), v_producer(), mma_warp()]
+    agents += [softmax_warp(0) for _ in range(4)] + [softmax_warp(1) for _ in range(4)]
+    run(agents, (tma, mma, cpa), rnd)
+    return ctl.abort
+
+
+@pytest.mark.parametrize("nch", [1, 2, 5])
+def test_every_warp_leaves_when_waits_give_up(nch):
+    gave_up = sum(sparse_fwd_failure_model(3, nch, seed, p_giveup=0.02) for seed in range(60))
+    assert gave_up > 0  # the failure paths were exercised (and every run ended)
+
+
+@pytest.mark.parametrize("nch", [1, 3])
+def test_every_warp_leaves_with_the_mma_warp_stalled(nch):
+    for seed in range(20):
+        assert sparse_fwd_failure_model(2, nch, seed, p_giveup=0.0, stall_mma=True)
+
+
+def test_normal_runs_finish_without_giving_up():
+    for seed in range(20):
+        assert not sparse_fwd_failure_model(3, 5, seed, p_giveup=0.0, poll_limit=10 ** 9)
+
+
+def test_leaving_before_the_consensus_is_caught():
+    hangs = 0
+    for seed in range(300):
+        try:
+            sparse_fwd_failure_model(3, 2, seed, p_giveup=0.02, early_break=True)
+        except Deadlock:
+            hangs += 1
+    assert hangs > 0

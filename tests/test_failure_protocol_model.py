@@ -1,4 +1,4 @@
-"""CPU model of the sparse forward kernel's failure path.
+"""CPU models of the forward kernels' failure paths (sparse and dense).
 
 Every mbarrier wait in the kernels is bounded: it gives up after a time limit,
 or at its next poll once another role has raised the CTA's abort flag, and
@@ -10,7 +10,9 @@ completes just after it -- and with the MMA warp stalled (the testing hook),
 and requires every run to end, i.e. every warp to reach the kernel's closing
 __syncthreads. The control flow from before the epilogue-consensus fix, where
 a warp could leave the item loop before warpgroup 0's consensus, must be
-caught hanging at the named barrier.
+caught hanging at the named barrier. The dense forward, whose two softmax
+warpgroups each meet at an epilogue consensus for every item, is run the
+same way.
 
 CPU only; no kernel code is involved.
 """
@@ -253,3 +255,148 @@ def test_leaving_before_the_consensus_is_caught():
         except Deadlock:
             hangs += 1
     assert hangs > 0
+
+
+def dense_fwd_failure_model(items, seed, p_giveup, stall_mma=False, nslot=4):
+    """The dense forward's roles with bounded waits (see the sparse model above):
+    the producer, the MMA issuer and two softmax warpgroups of four warps,
+    each warpgroup meeting at its own epilogue consensus for every item."""
+    rnd = random.Random(seed)
+    ctl = Ctl(rnd, p_giveup, POLL_LIMIT)
+    kv_full = [Bar(1) for _ in range(nslot)]
+    kv_empty = [Bar(1) for _ in range(nslot)]
+    q_full, q_empty, mma_done = Bar(1), Bar(1), Bar(1)
+    s_full, pv_done = [Bar(1), Bar(1)], [Bar(1), Bar(1)]
+    p_full = [Bar(4), Bar(4)]
+    nbar = [NamedBar(4), NamedBar(4)]
+    tma, mma = [], []
+
+    def producer():
+        ok, issued, q_loads = True, 0, 0
+        for r, (n0, n1, l0, l1) in enumerate(items):
+            if not ok:
+                break
+            n_pos = 2 * (n1 - l0)
+
+            def load_kv():
+                nonlocal issued
+                slot, rnd_ = issued % nslot, issued // nslot
+                if rnd_ > 0:
+                    res = yield from bwait(ctl, kv_empty[slot], rnd_ - 1)
+                    if not res:
+                        return False
+                tma.append(kv_full[slot])
+                issued += 1
+                return True
+            pre = 0 if r == 0 else min(2, n_pos)
+            for _ in range(pre):
+                ok = yield from load_kv()
+                if not ok:
+                    break
+            if not ok:
+                break
+            if r > 0:
+                ok = yield from bwait(ctl, q_empty, r - 1)
+                if not ok:
+                    break
+            tma.append(q_full)
+            q_loads += 1
+            for _ in range(pre, n_pos):
+                ok = yield from load_kv()
+                if not ok:
+                    break
+        for pos in range(max(0, issued - nslot), issued):
+            yield from bwait(ctl, kv_full[pos % nslot], pos // nslot, abort_aware=False)
+        if q_loads:
+            yield from bwait(ctl, q_full, q_loads - 1, abort_aware=False)
+
+    def mma_warp():
+        ok, ring, p_cnt = not stall_mma, 0, [0, 0]
+        for r, (n0, n1, l0, l1) in enumerate(items):
+            if not ok:
+                break
+            n_kv, jlo, jb = (n0, n1), (l0, l1), l0
+            ok = yield from bwait(ctl, q_full, r)
+            if not ok:
+                break
+            s_left = [(n0 - l0) + (n1 - l1)]
+
+            def issue_s(t):
+                mma.append(s_full[t])
+                s_left[0] -= 1
+                if s_left[0] == 0:
+                    mma.append(q_empty)
+
+            def wait_kv(idx):
+                q = ring + idx
+                res = yield from bwait(ctl, kv_full[q % nslot], q // nslot)
+                return res
+            ok = yield from wait_kv(0)
+            if not ok:
+                break
+            issue_s(0)
+            if jlo[1] == jb:
+                issue_s(1)
+            mma.append(kv_empty[ring % nslot])
+            for j in range(jb, n1):
+                v_ready = k_next = False
+                for t in range(2):
+                    if jlo[t] <= j < n_kv[t]:
+                        ok = yield from bwait(ctl, p_full[t], p_cnt[t])
+                        if not ok:
+                            break
+                        p_cnt[t] += 1
+                        if not v_ready:
+                            ok = yield from wait_kv(2 * (j - jb) + 1)
+                            if not ok:
+                                break
+                            v_ready = True
+                        if j + 1 == n_kv[t]:
+                            mma.append(pv_done[t])
+                    if j + 1 < n_kv[t] and j + 1 >= jlo[t]:
+                        if not k_next:
+                            ok = yield from wait_kv(2 * (j - jb) + 2)
+                            if not ok:
+                                break
+                            k_next = True
+                        issue_s(t)
+                if not ok:
+                    break
+                mma.append(kv_empty[(ring + 2 * (j - jb) + 1) % nslot])
+                if k_next:
+                    mma.append(kv_empty[(ring + 2 * (j - jb) + 2) % nslot])
+            ring += 2 * (n1 - jb)
+        mma.append(mma_done)
+        yield from bwait(ctl, mma_done, 0, abort_aware=False)
+
+    def softmax_warp(t):
+        ok, s_cnt = True, 0
+        for item, it in enumerate(items):
+            if not ok:
+                break
+            for _ in range(it[2 + t], it[t]):
+                ok = yield from bwait(ctl, s_full[t], s_cnt)
+                if not ok:
+                    break
+                s_cnt += 1
+                p_full[t].arrive()
+            if ok:
+                ok = yield from bwait(ctl, pv_done[t], item)
+            ok = yield from nbar[t].and_(ok)
+            if ok:
+                for _ in range(4):  # the epilogue's staging-tile bar.sync pairs (D = 128: two chunks)
+                    yield from nbar[t].and_(True)
+
+    agents = [producer(), mma_warp()] + [softmax_warp(t) for t in (0, 1) for _ in range(4)]
+    run(agents, (tma, mma, []), rnd)
+    return ctl.abort
+
+
+@pytest.mark.parametrize("S,causal,window", [(1024, True, 0), (640, False, 0), (1000, True, 200)])
+def test_dense_forward_every_warp_leaves(S, causal, window):
+    from tests.test_dense_protocol_model import fwd_items
+    items = fwd_items(S, causal, window)
+    gave_up = sum(dense_fwd_failure_model(items, seed, p_giveup=0.02) for seed in range(40))
+    assert gave_up > 0
+    for seed in range(10):
+        assert dense_fwd_failure_model(items, seed, p_giveup=0.0, stall_mma=True)

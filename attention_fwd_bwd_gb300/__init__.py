@@ -25,6 +25,7 @@ __all__ = [
     "attn_bwd_main_ex",
     "attn_bwd_preprocess",
     "attn_bwd_main",
+    "attn_bwd_dvec",
     "attn_bwd_noalloc",
     "attn_sparse_fwd",
     "attn_sparse_bwd",
@@ -82,6 +83,8 @@ def lib():
     L.attn_bwd_preprocess.restype = i
     L.attn_bwd_main.argtypes = [vp] * 7 + [i] * 6 + [f, vp, sz, vp]
     L.attn_bwd_main.restype = i
+    L.attn_bwd_dvec.argtypes = [vp] * 4 + [i] * 7 + [f, vp, sz, vp]
+    L.attn_bwd_dvec.restype = i
     L.attn_fwd_ex.argtypes = [vp] * 6 + [i] * 7 + [f, vp]
     L.attn_fwd_ex.restype = i
     L.attn_bwd_ex.argtypes = [vp] * 10 + [i] * 7 + [f, vp, sz, vp]
@@ -300,6 +303,16 @@ def attn_bwd_preprocess(q, k, o, dO, lse, dq, workspace, o_lo=None, stream=None)
     wp, wb = _ws(workspace)
     _check("attn_bwd_preprocess", lib().attn_bwd_preprocess(_ptr(o), _opt(o_lo), _ptr(dO), _ptr(lse), _ptr(dq),
                                                             B, Hq, Hkv, S, D, wp, wb, _stream(stream)))
+
+
+def attn_bwd_dvec(q, k, v, dO, causal, scale, workspace, window=0, stream=None):
+    """Optional stage between attn_bwd_preprocess and attn_bwd_main: Dvec =
+    sum_j P_ij dP_ij from q, k, v, dO and the LSE rows in the workspace."""
+    B, Hq, Hkv, S, D = _sizes(q, k)
+    wp, wb = _ws(workspace)
+    _check("attn_bwd_dvec", lib().attn_bwd_dvec(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), B, Hq, Hkv, S, D,
+                                                int(bool(causal)), int(window), float(scale), wp, wb,
+                                                _stream(stream)))
 
 
 def attn_bwd_main(q, k, v, dO, dq, dk, dv, causal, scale, workspace, stream=None):

@@ -15,7 +15,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libattn.so")
-SOURCES = ["attn_api.cu", "attn_fwd.cu", "attn_bwd.cu", "attn_noalloc.cu", "attn_sparse.cu", "attn_sparse_bwd.cu"]
+SOURCES = ["attn_api.cu", "attn_fwd.cu", "attn_bwd.cu", "attn_bwd_dvec.cu", "attn_noalloc.cu", "attn_sparse.cu",
+           "attn_sparse_bwd.cu"]
 HEADERS = ["attn_common.cuh", "attn_sparse.cuh", "sm100_ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v"]

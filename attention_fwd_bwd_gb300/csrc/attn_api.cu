@@ -80,28 +80,82 @@ attn_status_t validate_sizes(int B, int Hq, int Hkv, int S, int D) {
   return ATTN_OK;
 }
 
+// Tensor maps already encoded, keyed by every argument of the encoding (the
+// base address, element type, sizes, strides, box and swizzle), so a key
+// that matches gives the identical map. A map only describes addresses, so it
+// stays valid after its memory is freed and reused. Fixed capacity, replaced
+// round-robin; guarded by a mutex.
+struct MapKey {
+  const void* base;
+  int dtype, rank, swizzle;
+  cuuint64_t dims[4], strides[3];
+  cuuint32_t box[4];
+};
+constexpr int kMapCache = 256;
+struct MapCache {
+  std::mutex mu;
+  uint64_t hash[kMapCache];
+  MapKey key[kMapCache];
+  CUtensorMap map[kMapCache];
+  int n = 0, next = 0;
+};
+MapCache g_map_cache;
+
+bool encode_cached(CUtensorMap* m, CUtensorMapDataType dtype, int rank, const void* base,
+                   const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box,
+                   CUtensorMapSwizzle swizzle) {
+  MapKey k;
+  std::memset(&k, 0, sizeof(k));
+  k.base = base;
+  k.dtype = static_cast<int>(dtype);
+  k.rank = rank;
+  k.swizzle = static_cast<int>(swizzle);
+  for (int i = 0; i < rank; ++i) {
+    k.dims[i] = dims[i];
+    k.box[i] = box[i];
+    if (i + 1 < rank) k.strides[i] = strides[i];
+  }
+  uint64_t h = 1469598103934665603ull;  // FNV-1a over the key's bytes
+  const unsigned char* kb = reinterpret_cast<const unsigned char*>(&k);
+  for (size_t i = 0; i < sizeof(k); ++i) h = (h ^ kb[i]) * 1099511628211ull;
+  std::lock_guard<std::mutex> lock(g_map_cache.mu);
+  for (int i = 0; i < g_map_cache.n; ++i)
+    if (g_map_cache.hash[i] == h && std::memcmp(&g_map_cache.key[i], &k, sizeof(k)) == 0) {
+      *m = g_map_cache.map[i];
+      return true;
+    }
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  if (fn(m, dtype, rank, const_cast<void*>(base), dims, strides, box, es,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  const int slot = g_map_cache.next;
+  g_map_cache.hash[slot] = h;
+  g_map_cache.key[slot] = k;
+  g_map_cache.map[slot] = *m;
+  g_map_cache.next = (slot + 1) % kMapCache;
+  if (g_map_cache.n < kMapCache) ++g_map_cache.n;
+  return true;
+}
+
 // 4-D bf16 map over a [B, S, H, D] tensor; a box is `rows` sequence rows of
 // one head and 64 columns (128 bytes), stored with 128-byte swizzle.
 bool make_bshd_map(CUtensorMap* m, const void* base, int B, int S, int H, int D, int rows) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
                               static_cast<cuuint64_t>(S), static_cast<cuuint64_t>(B)};
   const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2,
                                  static_cast<cuuint64_t>(H) * D * 2,
                                  static_cast<cuuint64_t>(S) * H * D * 2};
   const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(rows), 1};
-  const cuuint32_t es[4] = {1, 1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
-            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return encode_cached(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims, strides, box,
+                       CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 // 4-D fp32 map over the [B, S, Hq, D] dq output; a box is 32 sequence rows of
 // one head, all D columns, unswizzled (the layout the dQ staging tile uses).
 bool make_dq_map(CUtensorMap* m, void* base, int B, int S, int H, int D) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
                               static_cast<cuuint64_t>(S), static_cast<cuuint64_t>(B)};
   const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 4,
@@ -109,24 +163,18 @@ bool make_dq_map(CUtensorMap* m, void* base, int B, int S, int H, int D) {
                                  static_cast<cuuint64_t>(S) * H * D * 4};
   const cuuint32_t box[4] = {static_cast<cuuint32_t>(D), 1,
                              static_cast<cuuint32_t>(BwdCfg<128>::DQ_ROWS), 1};
-  const cuuint32_t es[4] = {1, 1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return encode_cached(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, dims, strides, box,
+                       CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 // 2-D bf16 map over `rows` rows of `cols` columns (row-major, contiguous); a
 // box is `box_rows` rows of 64 columns (128 bytes), 128-byte swizzle.
 bool make_rows_map(CUtensorMap* m, const void* base, long long rows, int cols, int box_rows) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
   const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
-  const cuuint32_t es[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return encode_cached(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box,
+                       CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 int* fwd_status_ptr() {
@@ -142,13 +190,25 @@ int* fwd_status_ptr() {
   return ptrs[dev];
 }
 
-attn_status_t finish(cudaError_t e, cudaStream_t stream, const int* status_dev) {
+// Reads and clears a status word: the forward's device global (tagless) or a
+// backward workspace's tagged word (counted only once a backward call has
+// started it). Returns the code it held, or -1 if the read failed.
+int read_clear_status(int* status_dev, bool tagged) {
+  int w[2] = {0, 0};
+  if (cudaMemcpy(w, status_dev, (tagged ? 2 : 1) * sizeof(int), cudaMemcpyDeviceToHost) !=
+      cudaSuccess)
+    return -1;
+  if (tagged && w[1] != kStatusTag) return 0;
+  if (w[0] != 0 && cudaMemset(status_dev, 0, sizeof(int)) != cudaSuccess) return -1;
+  return w[0];
+}
+
+attn_status_t finish(cudaError_t e, cudaStream_t stream, int* status_dev, bool tagged) {
   if (e != cudaSuccess) return ATTN_ERR_CUDA;
   if (check_status_env()) {
     if (cudaStreamSynchronize(stream) != cudaSuccess) return ATTN_ERR_CUDA;
-    int st = 0;
-    if (status_dev && cudaMemcpy(&st, status_dev, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
-      return ATTN_ERR_CUDA;
+    const int st = status_dev ? read_clear_status(status_dev, tagged) : 0;
+    if (st < 0) return ATTN_ERR_CUDA;
     if (st != 0) return ATTN_ERR_TIMEOUT;
   }
   return ATTN_OK;
@@ -239,7 +299,7 @@ static attn_status_t fwd_impl(const void* q, const void* k, const void* v, void*
   p.timeout_ns = g_timeout_ns;
   p.inject_stall = g_inject_stall & 1;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  return finish(launch_fwd(D, tq, tk, tv, to, tolo, p, s), s, status);
+  return finish(launch_fwd(D, tq, tk, tv, to, tolo, p, s), s, status, false);
 }
 
 attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
@@ -279,7 +339,56 @@ attn_status_t attn_bwd_preprocess(const void* o, const void* o_lo, const void* d
       static_cast<const __nv_bfloat16*>(dO), lse, reinterpret_cast<float*>(ws + w.off_nlse2),
       reinterpret_cast<float*>(ws + w.off_dvec), static_cast<float*>(dq),
       reinterpret_cast<int*>(ws + w.off_status), B, Hq, S, D, s);
-  return finish(e, s, nullptr);
+  return finish(e, s, nullptr, true);
+}
+
+// The Dvec pass (attn_bwd_dvec): reads the log2-scaled LSE rows the
+// preprocess left in the workspace, writes exact Dvec rows over them.
+static attn_status_t dvec_impl(const void* q, const void* k, const void* v, const void* dO,
+                               int B, int Hq, int Hkv, int S, int D, int causal, int window,
+                               float scale, void* workspace, size_t workspace_bytes,
+                               void* stream) {
+  attn_status_t st = validate_sizes(B, Hq, Hkv, S, D);
+  if (st != ATTN_OK) return st;
+  if ((st = validate_window(causal, window)) != ATTN_OK) return st;
+  if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (B == 0 || S == 0) return ATTN_OK;
+  if (!q || !k || !v || !dO) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO)) return ATTN_ERR_INVALID_ARG;
+  if ((st = check_workspace(workspace, workspace_bytes, B, Hq, S, D)) != ATTN_OK) return st;
+  if ((st = check_device()) != ATTN_OK) return st;
+  const BwdWorkspace w = bwd_workspace_layout(B, Hq, S);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const int BQ = DvecCfg<128>::BQ;
+  CUtensorMap tq, tk, tv, tdo;
+  if (!make_bshd_map(&tq, q, B, S, Hq, D, BQ) || !make_bshd_map(&tdo, dO, B, S, Hq, D, BQ) ||
+      !make_bshd_map(&tk, k, B, S, Hkv, D, 128) || !make_bshd_map(&tv, v, B, S, Hkv, D, 128))
+    return ATTN_ERR_CUDA;
+  DvecParams p;
+  p.nlse2 = reinterpret_cast<const float*>(ws + w.off_nlse2);
+  p.dvec = reinterpret_cast<float*>(ws + w.off_dvec);
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.S = S;
+  p.S_pad = seq_pad(S);
+  p.G = Hq / Hkv;
+  p.causal = causal ? 1 : 0;
+  p.window = window;
+  p.scale_log2 = scale * kLog2e;
+  p.n_qblocks = (S + 2 * BQ - 1) / (2 * BQ);
+  p.status = reinterpret_cast<int*>(ws + w.off_status);
+  p.timeout_ns = g_timeout_ns;
+  p.inject_stall = (g_inject_stall >> 1) & 1;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return finish(launch_bwd_dvec(D, tq, tk, tv, tdo, p, s), s, p.status, true);
+}
+
+attn_status_t attn_bwd_dvec(const void* q, const void* k, const void* v, const void* dO, int B,
+                            int Hq, int Hkv, int S, int D, int causal, int window, float scale,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+  return dvec_impl(q, k, v, dO, B, Hq, Hkv, S, D, causal, window, scale, workspace,
+                   workspace_bytes, stream);
 }
 
 attn_status_t attn_bwd_main_ex(const void* q, const void* k, const void* v, const void* dO,
@@ -325,7 +434,7 @@ attn_status_t attn_bwd_main_ex(const void* q, const void* k, const void* v, cons
   p.timeout_ns = g_timeout_ns;
   p.inject_stall = (g_inject_stall >> 1) & 1;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  return finish(launch_bwd_main(D, tq, tk, tv, tdo, tdq, p, s), s, p.status);
+  return finish(launch_bwd_main(D, tq, tk, tv, tdo, tdq, p, s), s, p.status, true);
 }
 
 attn_status_t attn_bwd_main(const void* q, const void* k, const void* v, const void* dO, void* dq,
@@ -352,8 +461,27 @@ attn_status_t attn_bwd_ex(const void* q, const void* k, const void* v, const voi
     return ATTN_ERR_INVALID_ARG;
   if ((st = check_workspace(workspace, workspace_bytes, B, Hq, S, D)) != ATTN_OK) return st;
   if ((st = check_device()) != ATTN_OK) return st;
-  st = attn_bwd_preprocess(o, o_lo, dO, lse, dq, B, Hq, Hkv, S, D, workspace, workspace_bytes,
-                           stream);
+  if (o_lo) {
+    // Dvec = rowsum(dO * (o + o_lo)) in the preprocess.
+    st = attn_bwd_preprocess(o, o_lo, dO, lse, dq, B, Hq, Hkv, S, D, workspace, workspace_bytes,
+                             stream);
+  } else {
+    // Without the residual, bf16 o gives Dvec to about 8 bits only: the
+    // preprocess writes the LSE rows and zeroes dq, and the Dvec pass
+    // computes Dvec = rowsum(P * dP) from its definition.
+    const BwdWorkspace w = bwd_workspace_layout(B, Hq, S);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    st = finish(launch_bwd_preprocess(nullptr, nullptr, static_cast<const __nv_bfloat16*>(dO), lse,
+                                      reinterpret_cast<float*>(ws + w.off_nlse2),
+                                      reinterpret_cast<float*>(ws + w.off_dvec),
+                                      static_cast<float*>(dq),
+                                      reinterpret_cast<int*>(ws + w.off_status), B, Hq, S, D, s),
+                s, nullptr, true);
+    if (st == ATTN_OK)
+      st = dvec_impl(q, k, v, dO, B, Hq, Hkv, S, D, causal, window, scale, workspace,
+                     workspace_bytes, stream);
+  }
   if (st != ATTN_OK) return st;
   return attn_bwd_main_ex(q, k, v, dO, dq, dk, dv, B, Hq, Hkv, S, D, causal, window, scale,
                           workspace, workspace_bytes, stream);
@@ -411,7 +539,8 @@ attn_status_t attn_sparse_fwd(const void* q, const void* kp, const void* vp, con
   p.timeout_ns = g_timeout_ns;
   p.inject_stall = g_inject_stall & 1;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  return finish(launch_sparse_fwd(DK, DV, tq, tk, to, tolo, o_lo != nullptr, p, s), s, status);
+  return finish(launch_sparse_fwd(DK, DV, tq, tk, to, tolo, o_lo != nullptr, p, s), s, status,
+                false);
 }
 
 size_t attn_sparse_bwd_workspace_size(int B, int T, int H) {
@@ -477,21 +606,19 @@ attn_status_t attn_sparse_bwd(const void* q, const void* kp, const void* vp, con
                                   static_cast<const __nv_bfloat16*>(o_lo),
                                   static_cast<const __nv_bfloat16*>(dO), lse, nlse2, dvec, tq, tdo, tk,
                                   p, s),
-                s, p.status);
+                s, p.status, true);
 }
 
 attn_status_t attn_check_status(void* workspace) {
   if (cudaDeviceSynchronize() != cudaSuccess) return ATTN_ERR_CUDA;
   int* fs = fwd_status_ptr();
   if (!fs) return ATTN_ERR_CUDA;
-  int a = 0, b = 0;
-  if (cudaMemcpy(&a, fs, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return ATTN_ERR_CUDA;
-  if (a != 0 && cudaMemset(fs, 0, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
-  if (workspace) {
-    if (cudaMemcpy(&b, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
-      return ATTN_ERR_CUDA;
-    if (b != 0 && cudaMemset(workspace, 0, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
-  }
+  const int a = read_clear_status(fs, false);
+  // Without a workspace: the no-allocation backward's word as well, once a
+  // call on this device has looked up its scratch array.
+  int* ws_word = workspace ? static_cast<int*>(workspace) : noalloc_status_word();
+  const int b = ws_word ? read_clear_status(ws_word, true) : 0;
+  if (a < 0 || b < 0) return ATTN_ERR_CUDA;
   return (a != 0 || b != 0) ? ATTN_ERR_TIMEOUT : ATTN_OK;
 }
 

@@ -36,34 +36,63 @@ static __device__ unsigned long long g_attn_trace[kTraceCtas * kTraceRoles * kTr
 #endif
 
 // ------------------------------------------------------------------ preprocess
+// Dvec_i = sum_d dO_id (o_id + o_lo_id) and -LSE_i log2(e) per row, the
+// padding rows of both, and dq zeroed: an HBM-bound pass. A row of D bf16
+// values is read by D/8 threads, 16 bytes each. Each warp step takes
+// kPreU row groups: it issues all their loads first, then zeroes the dq rows
+// of the same rows (so reads and writes stay interleaved over the pass), then
+// reduces. With o = NULL the Dvec rows (not their padding) are left to the
+// Dvec pass. Measured at the Llama-3-8B shape against variants with four row
+// groups in flight, streaming cache hints, or the zeroing on blocks of its
+// own: two row groups with eight blocks per SM launched was the fastest.
+constexpr int kPreU = 2;
+
+template <int D>
 __global__ void __launch_bounds__(256) attn_bwd_preprocess_kernel(
     const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ o_lo,
     const __nv_bfloat16* __restrict__ dO, const float* __restrict__ lse, float* __restrict__ nlse2,
     float* __restrict__ dvec, float4* __restrict__ dq, int* __restrict__ status, int B, int Hq,
-    int S, int S_pad, int D) {
-  if (blockIdx.x == 0 && threadIdx.x == 0) *status = 0;  // status word of the main kernel
-  const int tpr = D / 8;  // threads per row, 8 bf16 (16 bytes) each
-  const int rows_per_warp = 32 / tpr;
+    int S, int S_pad) {
+  constexpr int TPR = D / 8;        // threads per row, 8 bf16 (16 bytes) each
+  constexpr int RPW = 32 / TPR;     // rows per warp and row group
+  constexpr int RPI = RPW * kPreU;  // rows per warp step
+  constexpr int Z4 = RPI * D / 4 / 32;  // float4 zero stores per lane and step
   const long long nrows = static_cast<long long>(B) * S * Hq;
+  if (blockIdx.x == 0 && threadIdx.x == 0) init_status_word(status);
   const long long gthreads = static_cast<long long>(gridDim.x) * blockDim.x;
   const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long gwarp = tid / 32, nwarps = gthreads / 32;
   const int lane = threadIdx.x % 32;
-  const int sub = lane % tpr;
+  const int sub = lane % TPR;
+  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
   // Rows in [B, S, Hq] order, so a warp reads consecutive memory. The loop
   // condition is warp-uniform so the shuffles below see the whole warp.
-  for (long long base = gwarp * rows_per_warp; base < nrows; base += nwarps * rows_per_warp) {
-    const long long row = base + lane / tpr;
-    const bool valid = row < nrows;
-    float acc = 0.f;
-    if (valid) {
-      const uint4 a = reinterpret_cast<const uint4*>(o + row * D)[sub];
-      const uint4 c = reinterpret_cast<const uint4*>(dO + row * D)[sub];
-      uint4 r = make_uint4(0u, 0u, 0u, 0u);
-      if (o_lo) r = reinterpret_cast<const uint4*>(o_lo + row * D)[sub];
-      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
-      const __nv_bfloat162* c2 = reinterpret_cast<const __nv_bfloat162*>(&c);
-      const __nv_bfloat162* r2 = reinterpret_cast<const __nv_bfloat162*>(&r);
+  for (long long base = gwarp * RPI; base < nrows; base += nwarps * RPI) {
+    uint4 a[kPreU], c[kPreU], r[kPreU];
+#pragma unroll
+    for (int u = 0; u < kPreU; ++u) {
+      const long long row = base + u * RPW + lane / TPR;
+      a[u] = c[u] = r[u] = make_uint4(0u, 0u, 0u, 0u);
+      if (row < nrows && o) {
+        a[u] = reinterpret_cast<const uint4*>(o + row * D)[sub];
+        c[u] = reinterpret_cast<const uint4*>(dO + row * D)[sub];
+        if (o_lo) r[u] = reinterpret_cast<const uint4*>(o_lo + row * D)[sub];
+      }
+    }
+    // dq rows base .. base + RPI - 1 (the reductions of the main kernel add into them).
+    const long long f_end = min(nrows, base + RPI) * (D / 4);
+#pragma unroll
+    for (int u = 0; u < Z4; ++u) {
+      const long long f = base * (D / 4) + u * 32 + lane;
+      if (f < f_end) dq[f] = z;
+    }
+#pragma unroll
+    for (int u = 0; u < kPreU; ++u) {
+      const long long row = base + u * RPW + lane / TPR;
+      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a[u]);
+      const __nv_bfloat162* c2 = reinterpret_cast<const __nv_bfloat162*>(&c[u]);
+      const __nv_bfloat162* r2 = reinterpret_cast<const __nv_bfloat162*>(&r[u]);
+      float acc = 0.f;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const float2 fa = __bfloat1622float2(a2[i]);
@@ -72,16 +101,17 @@ __global__ void __launch_bounds__(256) attn_bwd_preprocess_kernel(
         acc = fmaf(fa.x + fr.x, fc.x, acc);
         acc = fmaf(fa.y + fr.y, fc.y, acc);
       }
-    }
-    for (int off = tpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (valid && sub == 0) {
-      const int h = static_cast<int>(row % Hq);
-      const long long bs = row / Hq;
-      const int s = static_cast<int>(bs % S);
-      const int b = static_cast<int>(bs / S);
-      const long long bh = static_cast<long long>(b) * Hq + h;
-      dvec[bh * S_pad + s] = acc;
-      nlse2[bh * S_pad + s] = -lse[bh * S + s] * kLog2e;
+#pragma unroll
+      for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      if (row < nrows && sub == 0) {
+        const int h = static_cast<int>(row % Hq);
+        const long long bs = row / Hq;
+        const int s = static_cast<int>(bs % S);
+        const int b = static_cast<int>(bs / S);
+        const long long bh = static_cast<long long>(b) * Hq + h;
+        if (o) dvec[bh * S_pad + s] = acc;
+        nlse2[bh * S_pad + s] = -lse[bh * S + s] * kLog2e;
+      }
     }
   }
   // Padding rows S..S_pad-1 of every (b, h): probability 0 (nlse2 = -inf), Dvec 0.
@@ -92,10 +122,6 @@ __global__ void __launch_bounds__(256) attn_bwd_preprocess_kernel(
     dvec[bh * S_pad + s] = 0.f;
     nlse2[bh * S_pad + s] = -INFINITY;
   }
-  // dq is accumulated by reductions in the main kernel.
-  const long long n4 = nrows * D / 4;
-  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (long long i = tid; i < n4; i += gthreads) dq[i] = z;
 }
 
 // ------------------------------------------------------------------ main
@@ -665,27 +691,25 @@ cudaError_t launch_bwd_main_t(const CUtensorMap& tq, const CUtensorMap& tk, cons
   return cudaGetLastError();
 }
 
-int grid_for(long long work_items) {
-  int dev = 0, sms = 148;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  long long blocks = (work_items + 255) / 256;
-  const long long cap = static_cast<long long>(sms) * 8;
-  if (blocks > cap) blocks = cap;
-  if (blocks < 1) blocks = 1;
-  return static_cast<int>(blocks);
-}
-
 }  // namespace
 
 cudaError_t launch_bwd_preprocess(const __nv_bfloat16* o, const __nv_bfloat16* o_lo,
                                   const __nv_bfloat16* dO, const float* lse, float* nlse2,
                                   float* dvec, float* dq, int* status, int B, int Hq, int S,
                                   int D, cudaStream_t stream) {
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  // Eight 256-thread blocks per SM: about two waves at the kernel's register
+  // use (measured faster than one wave of four, or one of six).
+  const int nblk = 8 * sms;
   const int S_pad = seq_pad(S);
-  const long long work = static_cast<long long>(B) * Hq * S * D / 4;
-  attn_bwd_preprocess_kernel<<<grid_for(work), 256, 0, stream>>>(
-      o, o_lo, dO, lse, nlse2, dvec, reinterpret_cast<float4*>(dq), status, B, Hq, S, S_pad, D);
+  if (D == 128)
+    attn_bwd_preprocess_kernel<128><<<nblk, 256, 0, stream>>>(
+        o, o_lo, dO, lse, nlse2, dvec, reinterpret_cast<float4*>(dq), status, B, Hq, S, S_pad);
+  else
+    attn_bwd_preprocess_kernel<64><<<nblk, 256, 0, stream>>>(
+        o, o_lo, dO, lse, nlse2, dvec, reinterpret_cast<float4*>(dq), status, B, Hq, S, S_pad);
   return cudaGetLastError();
 }
 

@@ -40,9 +40,8 @@ struct FwdCfg {
   static constexpr int SMEM_BYTES = SMEM_STG + 2 * STG_BYTES;
   static constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;  // slack for 1024-byte alignment
   // Tensor-memory columns per query tile t: scores S_t (128 fp32 columns,
-  // later overwritten by P_t: for keys 16k..16k+15, bf16 hi pairs in columns
-  // 16k..16k+7 and lo pairs in 16k+8..16k+15) and the output accumulator O_t
-  // (D fp32 columns).
+  // later overwritten by P_t: for keys 16k..16k+15, bf16 pairs in columns
+  // 16k..16k+7) and the output accumulator O_t (D fp32 columns).
   __host__ __device__ static constexpr int tm_s(int t) { return 256 * t; }
   __host__ __device__ static constexpr int tm_o(int t) { return 256 * t + 128; }
   static constexpr int TMEM_COLS = 512;
@@ -62,6 +61,89 @@ struct FwdParams {
   int* status;
   unsigned long long timeout_ns;
   int inject_stall;  // testing hook: the MMA warp issues nothing (waits then run out)
+};
+
+// Work items of the query-tile-parallel kernels (the forward, and the
+// backward's Dvec pass): batch b, query head hq, and the two 128-row query
+// tiles starting at q0; tile t needs K/V tiles [j_lo[t], n_kv[t]). A sliding
+// window of W keys starts row r's keys at r - W + 1.
+struct FwdItem {
+  int b, hq, g, q0;
+  int n_kv[2], j_lo[2];
+};
+
+// Items in longest-first order: index i takes head i % (B Hq) of query-block
+// pair n_qblocks - 1 - i / (B Hq) (the causal rows get shorter down the list).
+// P is a parameter block with B, Hq, G, S, causal, window and n_qblocks;
+// WIN: sliding-window instantiation (without it the window code compiles
+// away).
+template <bool WIN, class P>
+__device__ __forceinline__ FwdItem fwd_item(const P& p, int i) {
+  constexpr int BQ = 128, BK = 128;
+  FwdItem it;
+  const int bhq = p.B * p.Hq;
+  const int bh = i % bhq;
+  it.hq = bh % p.Hq;
+  it.b = bh / p.Hq;
+  it.g = it.hq / p.G;
+  it.q0 = (p.n_qblocks - 1 - i / bhq) * (2 * BQ);
+  const int nkv_all = (p.S + BK - 1) / BK;
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int qt0 = it.q0 + t * BQ;
+    it.n_kv[t] = p.causal ? min(qt0 / BK + 1, nkv_all) : nkv_all;
+    // (A tile wholly past S still runs one K/V tile; its rows are not stored.)
+    it.j_lo[t] = WIN ? min(max(0, qt0 - p.window + 1) / BK, it.n_kv[t] - 1) : 0;
+  }
+  return it;
+}
+
+// The r-th item of CTA c among G CTAs: round r hands items r G .. r G + G - 1
+// to the CTAs, in reverse order on odd rounds, which balances the
+// longest-first list (a negative result: no item left).
+__device__ __forceinline__ int fwd_item_index(int r, int c, int G, int n_items) {
+  const int i = r * G + ((r & 1) ? (G - 1 - c) : c);
+  return i < n_items ? i : -1;
+}
+
+// ---------------------------------------------------------------- backward Dvec pass
+// The backward's Dvec without the forward's output: Dvec_i = sum_j P_ij dP_ij
+// with P_ij = exp2(scale log2(e) q_i.k_j - LSE_i log2(e)) and dP = dO V^T,
+// per query row (the definition that rowsum(dO * O) equals). Items as the
+// forward's: two 128-row query tiles of one head per item, K/V tiles
+// streaming through a ring. Warps 0-3 / 4-7: rows of tile A / B (one row per
+// thread, its TMEM lane); warp 8: TMA producer; warp 9: MMA issuer.
+template <int D>
+struct DvecCfg {
+  static constexpr int BQ = 128;
+  static constexpr int BK = 128;
+  static constexpr int KCH = D / 64;
+  static constexpr int Q_BYTES = BQ * D * 2;         // one Q or dO tile
+  static constexpr int KV_BYTES = BK * D * 2;        // one K or V tile
+  static constexpr int NSLOT = (D == 128) ? 3 : 8;   // ring slots
+  static constexpr int SMEM_Q = 0;                   // Q_A, Q_B, dO_A, dO_B
+  static constexpr int SMEM_RING = 4 * Q_BYTES;
+  static constexpr int SMEM_BYTES = SMEM_RING + NSLOT * KV_BYTES;
+  static constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;
+  // Tensor-memory columns per query tile t: S_t (128 fp32) and dP_t (128 fp32).
+  __host__ __device__ static constexpr int tm_s(int t) { return 256 * t; }
+  __host__ __device__ static constexpr int tm_dp(int t) { return 256 * t + 128; }
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int THREADS = 320;
+  static_assert(SMEM_ALLOC <= 232448, "shared-memory plan exceeds 227 KB");
+};
+
+struct DvecParams {
+  const float* nlse2;  // [B, Hq, S_pad] -lse * log2(e)
+  float* dvec;         // [B, Hq, S_pad] out (rows < S)
+  int B, Hq, Hkv, S, S_pad, G;
+  int causal;
+  int window;
+  float scale_log2;
+  int n_qblocks;
+  int* status;
+  unsigned long long timeout_ns;
+  int inject_stall;
 };
 
 // ---------------------------------------------------------------- backward
@@ -157,6 +239,21 @@ struct BwdParams {
   int inject_stall;  // testing hook: the MMA warp issues nothing (waits then run out)
 };
 
+// Status word of a backward workspace (the first 8 bytes of it): int 0 holds
+// the status code (0, or 4 after a bounded wait ran out), int 1 a tag that
+// marks the word as started by this library. A backward call starts a
+// workspace that lacks the tag at status 0; on a tagged workspace it leaves
+// the code as it is, so that a timeout an earlier call recorded stays there
+// until attn_check_status reads (and clears) it, instead of being erased.
+constexpr int kStatusTag = 0x41544E31;
+__device__ __forceinline__ void init_status_word(int* status) {
+  volatile int* w = status;
+  if (w[1] != kStatusTag) {
+    w[0] = 0;
+    w[1] = kStatusTag;
+  }
+}
+
 // Workspace layout of the backward pass (all offsets 256-byte aligned).
 struct BwdWorkspace {
   size_t off_status, off_nlse2, off_dvec, total;
@@ -206,6 +303,10 @@ struct TraceCursor {};
 #define ATTN_TRACE_EV(tc, code, it) ((void)0)
 #endif
 
+// Status word of attn_bwd_noalloc's scratch array on the current device, or
+// nullptr if no call on this device has looked the array up yet.
+int* noalloc_status_word();
+
 // ---------------------------------------------------------------- launchers
 cudaError_t launch_fwd(int D, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& to, const CUtensorMap& tolo, const FwdParams& p,
@@ -214,6 +315,9 @@ cudaError_t launch_bwd_preprocess(const __nv_bfloat16* o, const __nv_bfloat16* o
                                   const __nv_bfloat16* dO, const float* lse, float* nlse2,
                                   float* dvec, float* dq, int* status, int B, int Hq, int S,
                                   int D, cudaStream_t stream);
+cudaError_t launch_bwd_dvec(int D, const CUtensorMap& tq, const CUtensorMap& tk,
+                            const CUtensorMap& tv, const CUtensorMap& tdo, const DvecParams& p,
+                            cudaStream_t stream);
 cudaError_t launch_bwd_main(int D, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
                             const BwdParams& p, cudaStream_t stream);

@@ -21,13 +21,17 @@
 //       tensor core: while one tile's softmax runs, the other tile's MMAs do.
 //   warps 0-3 / 4-7 (softmax of tile A / B): thread r owns query row r of its
 //       tile (TMEM lane r); it reads its score row, updates the running max m
-//       and sum l, writes bf16 P over the scores in TMEM and, when m grew by
-//       more than 2^8, first rescales its O row. The final m and l give
-//       O = acc / l and LSE = (m + log2 l) ln 2.
+//       and writes P, rounded to bf16, over the scores in TMEM; when m grew by
+//       more than 2^8 it first rescales its O row. It keeps two row sums: l,
+//       of the fp32 probabilities, gives LSE = (m + log2 l) ln 2, and l_b, of
+//       the bf16 values that actually enter P V, gives O = acc / l_b. Dividing
+//       by l_b makes O an exact weighted mean of V rows whose weights are
+//       within bf16 rounding of the softmax weights; dividing by l would add
+//       the rounding's mean as a common scale error, which the backward's
+//       Dvec = rowsum(dO * O) turns into a dQ error for sharp rows.
 // When the caller asks for the output residual o_lo = bf16(O - o) (training,
-// where the backward needs rowsum(dO * O) beyond bf16 accuracy), P is split
-// into bf16 hi (P truncated) and lo (the truncated residual) parts and goes
-// through a second MMA, O += P_lo V_j, so O carries about 16 significant bits.
+// where the backward needs rowsum(dO * O) beyond bf16 accuracy), the epilogue
+// also stores what the bf16 rounding of O dropped.
 #include "attn_common.cuh"
 #include "sm100_ptx.cuh"
 
@@ -42,7 +46,7 @@ static __device__ unsigned long long g_attn_trace[kTraceCtas * kTraceRoles * kTr
 
 // Rescale threshold in log2 units: the running max used for exponentiation
 // only moves when the true max exceeds it by more than this, which keeps every
-// p <= 2^8 and leaves the result exact after the final division by l.
+// p <= 2^8 and leaves the result exact after the final division by l (or l_b).
 constexpr float kRescaleThreshold = 8.0f;
 
 // Largest (MAX) or smallest value of a 128-entry row, mostly with
@@ -65,51 +69,11 @@ __device__ __forceinline__ float row_extreme128(const float (&x)[128]) {
   return MAX ? fmaxf(c0, c1) : fminf(c0, c1);
 }
 
-// WIN: sliding-window instantiation (p.window > 0); without it the window
-// code compiles away.
-// One work item: batch b, query head hq, and the two 128-row query tiles
-// starting at q0; tile t needs K/V tiles [j_lo[t], n_kv[t]). A sliding
-// window of W keys starts row r's keys at r - W + 1.
-struct FwdItem {
-  int b, hq, g, q0;
-  int n_kv[2], j_lo[2];
-};
-
-// Items in longest-first order: index i takes head i % (B Hq) of query-block
-// pair n_qblocks - 1 - i / (B Hq) (the causal rows get shorter down the list).
-template <bool WIN>
-__device__ __forceinline__ FwdItem fwd_item(const FwdParams& p, int i) {
-  constexpr int BQ = 128, BK = 128;
-  FwdItem it;
-  const int bhq = p.B * p.Hq;
-  const int bh = i % bhq;
-  it.hq = bh % p.Hq;
-  it.b = bh / p.Hq;
-  it.g = it.hq / p.G;
-  it.q0 = (p.n_qblocks - 1 - i / bhq) * (2 * BQ);
-  const int nkv_all = (p.S + BK - 1) / BK;
-#pragma unroll
-  for (int t = 0; t < 2; ++t) {
-    const int qt0 = it.q0 + t * BQ;
-    it.n_kv[t] = p.causal ? min(qt0 / BK + 1, nkv_all) : nkv_all;
-    // (A tile wholly past S still runs one K/V tile; its rows are not stored.)
-    it.j_lo[t] = WIN ? min(max(0, qt0 - p.window + 1) / BK, it.n_kv[t] - 1) : 0;
-  }
-  return it;
-}
-
-// The r-th item of CTA c among G CTAs: round r hands items r G .. r G + G - 1
-// to the CTAs, in reverse order on odd rounds, which balances the
-// longest-first list (a negative result: no item left).
-__device__ __forceinline__ int fwd_item_index(int r, int c, int G, int n_items) {
-  const int i = r * G + ((r & 1) ? (G - 1 - c) : c);
-  return i < n_items ? i : -1;
-}
-
-// WIN: sliding-window instantiation (p.window > 0); without it the window
-// code compiles away. The kernel is persistent: each CTA loops over its work
-// items, and every barrier keeps counting phases across items.
-template <int D, bool SPLIT, bool WIN>
+// RESID: the epilogue also stores o_lo. WIN: sliding-window instantiation
+// (p.window > 0); without it the window code compiles away. The kernel is
+// persistent: each CTA loops over its work items, and every barrier keeps
+// counting phases across items.
+template <int D, bool RESID, bool WIN>
 __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
@@ -289,19 +253,12 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
             tc_fence_after();
             const int vslot = kv_slot(2 * (j - jb) + 1);
             const uint64_t dv = sw128_desc(sRing + vslot * C::KV_BYTES, C::BK * 128, 1024);
-            // Keys 16kk..16kk+15: P hi in score columns 16kk..16kk+7, P lo in
-            // 16kk+8..16kk+15.
+            // Keys 16kk..16kk+15: bf16 P pairs in score columns 16kk..16kk+7.
             const uint32_t a_p = tmem + C::tm_s(t);
 #pragma unroll
             for (int kk = 0; kk < C::BK / 16; ++kk)
               mma_ts_el(tmem + C::tm_o(t), a_p + kk * 16, dv + ((kk * 2048) >> 4), idesc_o,
                         (j > jlo(it, t) || kk > 0) ? 1u : 0u);
-            if constexpr (SPLIT) {
-#pragma unroll
-              for (int kk = 0; kk < C::BK / 16; ++kk)
-                mma_ts_el(tmem + C::tm_o(t), a_p + kk * 16 + 8, dv + ((kk * 2048) >> 4), idesc_o,
-                          1u);
-            }
             if (j + 1 == it.n_kv[t]) mma_commit_el(smem_u32(&bar_pv_done[t]));
             ATTN_TRACE_EV(tc, 6 + t, j);  // PV_t(j) issued
           }
@@ -360,7 +317,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       const int qrow = q0 + t * C::BQ + r;
       const int my_kv = it.n_kv[t];
       float m = -INFINITY;  // running max in log2 units (scaled scores)
-      float l = 0.f;
+      float l = 0.f;        // row sum of the fp32 probabilities (for LSE)
+      float lb = 0.f;       // row sum of the bf16 probabilities that enter P V (for O)
       for (int j = jlo(it, t); j < my_kv; ++j) {
         ATTN_TRACE_EV(tc, 1, j);  // start waiting for S_t(j)
         // S_t(j) landed; its commit also covers PV_t(j-1), so O_t is current.
@@ -391,11 +349,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         const int c_lo = WIN ? qrow - p.window + 1 - k0 : 0;
         float alpha = 1.f;
         bool rescale = false;
-        // One tile of the online softmax: row max, exponentials, row sum and P
-        // (hi, and with SPLIT lo) into TMEM over the scores, 16 columns at a
-        // time; this thread has read all its scores already. Instantiated once
-        // for tiles that mask (the causal diagonal, keys past S) and once for
-        // tiles that do not.
+        // One tile of the online softmax: row max, exponentials, both row sums
+        // and bf16 P into TMEM over the scores, 16 columns at a time; this
+        // thread has read all its scores already.
         {
           const bool MASKED = need_mask;
           // Largest scaled score: the max of the raw scores for scale >= 0, the
@@ -419,12 +375,12 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           // m = -inf; an offset of 0 then gives its masked scores p = 0.
           const float neg_m = (WIN && m == -INFINITY) ? 0.f : -m;
           const uint64_t negm2 = f32x2(neg_m, neg_m);
-          uint64_t sums[4];
+          uint64_t sums[2], sumsb[2];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) sums[i] = f32x2(0.f, 0.f);
+          for (int i = 0; i < 2; ++i) sums[i] = sumsb[i] = f32x2(0.f, 0.f);
 #pragma unroll
           for (int ch = 0; ch < C::BK; ch += 16) {
-            uint32_t pkl[16];  // P hi pairs, then (with SPLIT) P lo pairs
+            uint32_t pk[8];  // bf16 P pairs of keys ch..ch+15
 #pragma unroll
             for (int c = 0; c < 16; c += 2) {
               float e0, e1;
@@ -432,22 +388,21 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
               // A masked score is -inf (or +inf with a negative scale): its
               // exponent is -inf and its probability 0 (the scale is never 0).
               const float p0 = ex2(e0), p1 = ex2(e1);
-              sums[(c / 2) & 3] = add_f32x2(sums[(c / 2) & 3], f32x2(p0, p1));
-              if constexpr (SPLIT) {
-                split_bf16x2(p0, p1, pkl[c / 2], pkl[8 + c / 2]);
-              } else {
-                pkl[c / 2] = pack_bf16x2(p0, p1);
-              }
+              sums[(c / 2) & 1] = add_f32x2(sums[(c / 2) & 1], f32x2(p0, p1));
+              const uint32_t w = round_bf16x2(p0, p1);
+              pk[c / 2] = w;
+              sumsb[(c / 2) & 1] =
+                  add_f32x2(sumsb[(c / 2) & 1], f32x2(__uint_as_float(w << 16),
+                                                      __uint_as_float(w & 0xFFFF0000u)));
             }
-            // Columns ch..ch+15 of the scores (already read) take these keys' P.
-            if constexpr (SPLIT)
-              tmem_st16(ts + ch, pkl);
-            else
-              tmem_st8(ts + ch, *reinterpret_cast<uint32_t(*)[8]>(&pkl[0]));
+            // Columns ch..ch+7 of the scores (already read) take these keys' P.
+            tmem_st8(ts + ch, pk);
           }
-          float s0, s1;
-          unpack_f32x2(add_f32x2(add_f32x2(sums[0], sums[1]), add_f32x2(sums[2], sums[3])), s0, s1);
+          float s0, s1, b0, b1;
+          unpack_f32x2(add_f32x2(sums[0], sums[1]), s0, s1);
+          unpack_f32x2(add_f32x2(sumsb[0], sumsb[1]), b0, b1);
           l = l * alpha + (s0 + s1);
+          lb = lb * alpha + (b0 + b1);
         }
         ATTN_TRACE_EV(tc, 3, j);  // exponentials done
         // Rescale this warp's O rows (PV_t(j-1) has completed, see above).
@@ -477,10 +432,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       ok = named_bar_and(1 + t, 128, ok);
       if (ok) {
         tc_fence_after();
-        // O = acc / l (and o_lo, what bf16 rounding of O dropped, itself in
+        // O = acc / l_b (and o_lo, what bf16 rounding of O dropped, itself in
         // bf16) leave 64 columns at a time through this tile's staging buffer
         // and a TMA store; rows past S are clipped by the store.
-        const float inv_l = 1.f / l;
+        const float inv_l = 1.f / lb;
         const uint32_t to = tmem + lane_base + C::tm_o(t);
         const uint32_t stg = sStg + t * C::STG_BYTES;
         const uint32_t bar_id = 1 + t;  // named barrier of this tile's 128 threads
@@ -504,7 +459,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
             }
           }
 #pragma unroll
-          for (int part = 0; part < (SPLIT ? 2 : 1); ++part) {
+          for (int part = 0; part < (RESID ? 2 : 1); ++part) {
             const uint32_t* v = part ? lo : hi;
             // The previous store from this buffer has read it.
             if (leader) bulk_wait_read_all();
@@ -538,7 +493,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   if (warp == 9) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
-template <int D, bool SPLIT, bool WIN>
+template <int D, bool RESID, bool WIN>
 cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const CUtensorMap& to, const CUtensorMap& tolo, const FwdParams& p,
                          cudaStream_t stream) {
@@ -547,7 +502,7 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D, SPLIT, WIN>,
+    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D, RESID, WIN>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
@@ -561,7 +516,7 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   const long long n_items = static_cast<long long>(p.B) * p.Hq * p.n_qblocks;
   const int sms = (dev < 64 && sm_count[dev] > 0) ? sm_count[dev] : 148;
   const dim3 grid(static_cast<unsigned>(n_items < sms ? n_items : sms));
-  attn_fwd_kernel<D, SPLIT, WIN><<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(tq, tk, tv, to, tolo,
+  attn_fwd_kernel<D, RESID, WIN><<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(tq, tk, tv, to, tolo,
                                                                                  p);
   return cudaGetLastError();
 }
@@ -571,7 +526,7 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
 cudaError_t launch_fwd(int D, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& to, const CUtensorMap& tolo, const FwdParams& p,
                        cudaStream_t stream) {
-  const bool split = p.o_lo != nullptr, win = p.window > 0;
+  const bool split = p.o_lo != nullptr, win = p.window > 0;  // split: store o_lo
   if (D == 128) {
     if (win)
       return split ? launch_fwd_t<128, true, true>(tq, tk, tv, to, tolo, p, stream)

@@ -36,6 +36,14 @@ attn_status_t scratch_for_current_device(void** out) {
 }
 
 }  // namespace
+
+int* noalloc_status_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  return static_cast<int*>(g_scratch_ptr[dev]);
+}
+
 }  // namespace attn
 
 extern "C" attn_status_t attn_bwd_noalloc(const void* q, const void* k, const void* v,
@@ -55,8 +63,9 @@ extern "C" attn_status_t attn_bwd_noalloc(const void* q, const void* k, const vo
   const attn_status_t st = attn::scratch_for_current_device(&scratch);
   if (st != ATTN_OK) return st;
   // The preprocess kernel rewrites every word of the scratch this call reads
-  // (status word, LSE and Dvec rows including padding), so nothing left from
-  // an earlier call leaks in.
+  // (LSE and Dvec rows including padding), so nothing left from an earlier
+  // call leaks in; the status word keeps a timeout that an earlier call
+  // recorded until attn_check_status(NULL) reads it.
   return attn_bwd(q, k, v, o, dO, lse, dq, dk, dv, o_lo, B, Hq, Hkv, S, D, causal, scale, scratch,
                   attn::kNoAllocScratchBytes, stream);
 }

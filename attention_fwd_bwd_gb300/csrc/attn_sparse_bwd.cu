@@ -78,7 +78,7 @@ __device__ __forceinline__ void red_add_v4(float* dst, float a, float b, float c
 // ------------------------------------------------------------------ preprocess
 // One warp per (batch, token, head) row: Dvec = sum_k dO * (o + o_lo) and
 // -LSE*log2(e) (-inf when LSE is -inf: no filled slot), plus the zeroing of
-// dkp and dvp and of the status word by a grid-stride loop.
+// dkp and dvp by a grid-stride loop, and the start of the status word.
 __global__ void __launch_bounds__(256) attn_sparse_bwd_preprocess_kernel(
     const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ o_lo,
     const __nv_bfloat16* __restrict__ dO, const float* __restrict__ lse, float* __restrict__ nlse2,
@@ -86,7 +86,7 @@ __global__ void __launch_bounds__(256) attn_sparse_bwd_preprocess_kernel(
     long long n_dvp4, int* __restrict__ status, int B, int T, int H, int DV) {
   const long long gt = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long nthreads = static_cast<long long>(gridDim.x) * blockDim.x;
-  if (gt == 0) *status = 0;
+  if (gt == 0) init_status_word(status);
   for (long long i = gt; i < n_dkp4; i += nthreads) dkp[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   for (long long i = gt; i < n_dvp4; i += nthreads) dvp[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   const long long rows = static_cast<long long>(B) * T * H;

@@ -43,6 +43,16 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
+# Dense bf16 tcgen05 rate per SM and clock: an M128 N256 K16 MMA from shared
+# memory (1,048,576 FLOP) completes every 128 cycles (microbenchmarked on a GB300).
+TCGEN05_BF16_FLOP_PER_CLK_SM = 8192
+
+
+def theoretical_tflops(sm_count, sm_max_mhz):
+    """SM count x maximum SM clock x the per-SM tcgen05 bf16 rate."""
+    return sm_count * sm_max_mhz * 1e6 * TCGEN05_BF16_FLOP_PER_CLK_SM / 1e12
+
+
 def load_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -216,14 +226,22 @@ def run_ours(args, w, world, rank, local):
     dq, dk, dv = torch.empty(q.shape, **f32), torch.empty(k.shape, **f32), torch.empty(k.shape, **f32)
     ws = torch.empty(attn.attn_bwd_workspace_size(B, Hq, Hkv, S, D), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
+    plain = args.path == "plain"
+    if plain:
+        o_lo = None
 
     def step(ev=None):
+        # residual path: attn_fwd_residual's kernels, then the backward's
+        # preprocess and main kernels. plain path: attn_fwd's kernel, then the
+        # preprocess, the Dvec pass and the main kernel (attn_bwd without o_lo).
         if ev is not None:
             ev[0].record(stream)
         attn.attn_fwd_ex(q, k, v, o, lse, w.causal, w.window, w.scale, o_lo=o_lo, stream=stream)
         if ev is not None:
             ev[1].record(stream)
         attn.attn_bwd_preprocess(q, k, o, do, lse, dq, ws, o_lo=o_lo, stream=stream)
+        if plain:
+            attn.attn_bwd_dvec(q, k, v, do, w.causal, w.scale, ws, window=w.window, stream=stream)
         if ev is not None:
             ev[2].record(stream)
         attn.attn_bwd_main_ex(q, k, v, do, dq, dk, dv, w.causal, w.window, w.scale, ws, stream=stream)
@@ -274,6 +292,7 @@ def run_ours(args, w, world, rank, local):
         for dst, src in ((q, hq_), (k, hk_), (v, hv_), (do, hdo_)):
             dst.copy_(src, non_blocking=True)
         attn.attn_fwd_ex(q, k, v, o, lse, w.causal, w.window, w.scale, o_lo=o_lo, stream=stream)
+        # attn_bwd_ex without o_lo runs the Dvec pass itself
         attn.attn_bwd_ex(q, k, v, o, do, lse, dq, dk, dv, w.causal, w.window, w.scale, ws, o_lo=o_lo,
                          stream=stream)
         for dst, src in ((ho, o), (hlse, lse), (hdq, dq), (hdk, dk), (hdv, dv)):
@@ -296,11 +315,17 @@ def run_ours(args, w, world, rank, local):
     peak = float(peaks["bf16_tflops"])
     main_tf = w.flops_bwd() / (main_ms / 1e3) / 1e12
     fwd_tf = w.flops_fwd() / (fwd_ms / 1e3) / 1e12
-    pre_bytes = (3 * B * S * Hq * D * 2 + B * Hq * S * 4 + 2 * B * Hq * S * 4 + B * S * Hq * D * 4)
+    # Preprocess bytes as this path moves them: o, dO (and o_lo) read, lse read,
+    # the log2-scaled LSE and Dvec rows written, dq zeroed. The survey's count
+    # leaves out o_lo and the two row vectors: o, dO and lse read, dq zeroed.
+    n_rd = 2 if plain else 3
+    pre_bytes = (n_rd * B * S * Hq * D * 2 + B * Hq * S * 4 + 2 * B * Hq * S * 4 + B * S * Hq * D * 4)
+    pre_bytes_survey = 2 * B * S * Hq * D * 2 + B * Hq * S * 4 + B * S * Hq * D * 4
     # The ncu traffic figure is for the default workload's launch.
     traffic = TRAFFIC.get(kernel_source_hash()) if w.name == DEFAULT_WORKLOAD else None
     in_bytes = sum(t.numel() * t.element_size() for t in (q, k, v, do))
     sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
+    theo = theoretical_tflops(sm_count, float(peaks.get("sm_max_mhz", 2070.0)))
 
     if rank == 0:
         line = {
@@ -313,19 +338,28 @@ def run_ours(args, w, world, rank, local):
                        "parallelism": f"replicas x{world}",
                        "l2": f"no flush: q, k, v, dO ({in_bytes / 1e6:.0f} MB) exceed the 129 MB L2",
                        "flops_per_step": flops, "sm_count": sm_count},
-            "gpu_launches": 3 * args.steps,
+            "path": args.path,
+            "gpu_launches": (4 if plain else 3) * args.steps,
             "passes": {
-                "fwd": {"ms": fwd_ms, "tflops": fwd_tf, "frac_of_peak": fwd_tf / peak},
+                "fwd": {"ms": fwd_ms, "tflops": fwd_tf, "frac_of_peak": fwd_tf / peak,
+                        "frac_of_theoretical": fwd_tf / theo},
+                # (plain path: the preprocess and the Dvec pass together)
                 "bwd_preprocess": {"ms": pre_ms, "gbs": pre_bytes / (pre_ms / 1e3) / 1e9,
-                                   "frac_of_hbm": pre_bytes / (pre_ms / 1e3) / 1e9 / float(peaks["hbm_gbs"])},
-                "bwd_main": {"ms": main_ms, "tflops": main_tf, "frac_of_peak": main_tf / peak},
+                                   "frac_of_hbm": pre_bytes / (pre_ms / 1e3) / 1e9 / float(peaks["hbm_gbs"]),
+                                   "frac_of_hbm_survey_bytes":
+                                       pre_bytes_survey / (pre_ms / 1e3) / 1e9 / float(peaks["hbm_gbs"])},
+                "bwd_main": {"ms": main_ms, "tflops": main_tf, "frac_of_peak": main_tf / peak,
+                             "frac_of_theoretical": main_tf / theo},
                 "bwd": {"ms": pre_ms + main_ms,
                         "tflops": w.flops_bwd() / ((pre_ms + main_ms) / 1e3) / 1e12,
                         "frac_of_peak": w.flops_bwd() / ((pre_ms + main_ms) / 1e3) / 1e12 / peak},
             },
             "roofline": {"kernel": "attn_bwd_main_kernel", "bound": "tensor", "achieved": main_tf, "peak": peak,
                          "unit": "TFLOP/s", "frac": main_tf / peak, "traffic": traffic,
-                         "peak_source": f"{peak_src} bf16_tflops (burst)"},
+                         "peak_source": f"{peak_src} bf16_tflops (burst)",
+                         "theoretical_peak": theo, "frac_of_theoretical": main_tf / theo,
+                         "theoretical_source": f"{sm_count} SMs x {peaks.get('sm_max_mhz', 2070.0):.0f} MHz x "
+                                               f"{TCGEN05_BF16_FLOP_PER_CLK_SM} flop/clk/SM"},
             "clocks": clocks.summary(),
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_ms},
@@ -518,6 +552,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--path", choices=["residual", "plain"], default="residual",
+                    help="residual: attn_fwd_residual + attn_bwd with o_lo (the training pair); "
+                         "plain: attn_fwd + attn_bwd without o_lo (Dvec from the Dvec pass)")
     ap.add_argument("--ref-budget", type=float, default=12.0, help="seconds of oracle work per sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

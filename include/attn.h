@@ -56,12 +56,19 @@ typedef enum {
 } attn_status_t;
 
 /*
- * Forward: o = softmax(scale * q k^T) v and the row log-sum-exp.
+ * Forward: o = softmax(scale * q k^T) v and the row log-sum-exp -- the
+ * paper's section 2.1, Eq. (1), computed as that section's Algorithm 0
+ * streams it (online softmax over K/V tiles, state kept on chip).
  *
  *   q     [B,S,Hq,D]  bf16, in
  *   k, v  [B,S,Hkv,D] bf16, in
- *   o     [B,S,Hq,D]  bf16, out (overwritten): O rounded to nearest bf16
- *   lse   [B,Hq,S]    fp32, out (overwritten); needed by attn_bwd
+ *   o     [B,S,Hq,D]  bf16, out (overwritten): O rounded to nearest bf16.
+ *                     The probabilities enter P V as bf16 values, and O is
+ *                     divided by the sum of those same bf16 values, so O is a
+ *                     weighted mean of V rows whose weights are within bf16
+ *                     rounding of the softmax weights.
+ *   lse   [B,Hq,S]    fp32, out (overwritten); needed by attn_bwd. From the
+ *                     fp32 probabilities: ln sum_j exp(scale q_i . k_j).
  *   scale finite, e.g. 1/sqrt(D)
  *
  * Errors: ATTN_ERR_INVALID_ARG for a null or non-16-byte-aligned pointer,
@@ -73,16 +80,19 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
                        int Hq, int Hkv, int S, int D, int causal, float scale, void* stream);
 
 /*
- * Forward that also writes the low-order part of the output:
+ * Forward that also writes the low-order part of the output (same passage
+ * as attn_fwd; the residual is this library's addition for the backward):
  *
  *   o_lo  [B,S,Hq,D]  bf16, out (overwritten): bf16(O_fp32 - o), so o + o_lo
- *                     carries O to about 16 significant bits.
+ *                     carries the kernel's fp32 O to about 16 significant
+ *                     bits. o and lse are bit for bit those of attn_fwd.
  *
- * Passing o_lo on to attn_bwd makes the backward's Dvec = rowsum(dO * O)
- * accurate to about 16 bits instead of bf16's 8; the gradient tolerance of
- * the test suite (max-abs error <= 5e-2 of the exact gradient's rms) needs
- * it at long causal sequences. Other arguments and errors as attn_fwd
- * (o_lo may not be NULL here).
+ * Passing o_lo on to attn_bwd gives the backward Dvec = rowsum(dO * O) from
+ * that O in its cheap preprocess pass; without it, attn_bwd computes Dvec in
+ * an extra pass (attn_bwd_dvec), because bf16 o alone holds O to about 8
+ * bits, too few for the gradient tolerance (max-abs error <= 5e-2 of the
+ * exact gradient's rms) with a sharp softmax. Other arguments and errors as
+ * attn_fwd (o_lo may not be NULL here).
  */
 attn_status_t attn_fwd_residual(const void* q, const void* k, const void* v, void* o, void* o_lo,
                                 float* lse, int B, int Hq, int Hkv, int S, int D, int causal,
@@ -98,7 +108,12 @@ size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int S, int D);
 
 /*
  * Backward: the gradients of L = sum(dO * O) with respect to q, k and v,
- * written in fp32.
+ * written in fp32. The paper gives no backward equations; this is the exact
+ * gradient of its Eq. (1) (section 2.1), with the operand layouts of its
+ * Table 3 (scores Q K^T, query gradient dS K, key gradient dS^T Q) and
+ * dV = P^T dO:
+ *   dP = dO V^T, Dvec_i = sum_j P_ij dP_ij, dS = P * (dP - Dvec),
+ *   dQ = scale dS K, dK = scale dS^T Q, dV = P^T dO.
  *
  *   q, k, v, o, lse  as passed to / returned by attn_fwd (in)
  *   dO    [B,S,Hq,D]  bf16, in
@@ -106,17 +121,24 @@ size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int S, int D);
  *   dk,dv [B,S,Hkv,D] fp32, out (overwritten; for GQA each sums over the
  *                     Hq/Hkv query heads of its group)
  *   o_lo  [B,S,Hq,D]  bf16, in, optional (NULL allowed): the residual from
- *                     attn_fwd_residual; with NULL, Dvec uses o alone.
+ *                     attn_fwd_residual. Given, Dvec = rowsum(dO * (o + o_lo))
+ *                     in the preprocess pass (two kernels run: preprocess and
+ *                     main). NULL: Dvec = sum_j P_ij dP_ij from the attn_bwd_dvec
+ *                     pass (three kernels: preprocess, Dvec pass, main; the
+ *                     Dvec pass costs about as much as a forward).
  *   workspace        device memory of at least attn_bwd_workspace_size()
  *                    bytes, 256-byte aligned, owned by the caller; its
- *                    contents on entry do not matter and are clobbered.
+ *                    contents on entry do not matter and are clobbered,
+ *                    except its status word: a timeout that an earlier call
+ *                    recorded there stays until attn_check_status(workspace)
+ *                    reads and clears it.
  *
- * Runs two kernels in order on `stream`: the preprocess pass
- * (Dvec = rowsum(dO * O), log2-scaled LSE, dq zeroed) and the KV-parallel main
- * kernel (dK and dV per key tile; dQ added into dq by fp32 reductions, so dq
- * is reproducible only up to fp32 summation order). Inside the main kernel P
- * and dS enter the gradient products as bf16 hi/lo pairs (about 16
- * significant bits).
+ * Runs its kernels in order on `stream`: the preprocess pass (Dvec as above,
+ * log2-scaled LSE, dq zeroed), the Dvec pass when o_lo is NULL, and the
+ * KV-parallel main kernel (dK and dV per key tile; dQ added into dq by fp32
+ * reductions, so dq is reproducible only up to fp32 summation order). Inside
+ * the main kernel P and dS enter the gradient products as bf16 hi/lo pairs
+ * (about 16 significant bits).
  *
  * Errors: as attn_fwd, plus ATTN_ERR_WORKSPACE for a null or misaligned
  * workspace or one smaller than attn_bwd_workspace_size().
@@ -127,15 +149,23 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
                        size_t workspace_bytes, void* stream);
 
 /*
- * The two stages of attn_bwd as separate calls, in the order attn_bwd runs
- * them, for callers that time or schedule them one by one. Arguments and
- * errors are those of attn_bwd; the main stage reads what the preprocess
- * stage left in `workspace` and `dq`, so they must run in order on one
- * stream with the same arguments.
+ * The stages of attn_bwd as separate calls, for callers that time or
+ * schedule them one by one. Arguments and errors are those of attn_bwd; each
+ * stage reads what the previous one left in `workspace` and `dq`, so they
+ * must run in order on one stream with the same arguments:
+ *   attn_bwd_preprocess: Dvec = rowsum(dO * (o + o_lo)) (o alone when o_lo is
+ *     NULL), the log2-scaled LSE rows, dq zeroed;
+ *   attn_bwd_dvec (optional, between the two): overwrites Dvec with
+ *     sum_j P_ij dP_ij computed from q, k, v, dO and the LSE rows -- what
+ *     attn_bwd runs when o_lo is NULL (window as in attn_bwd_ex, 0 = none);
+ *   attn_bwd_main: the gradient products.
  */
 attn_status_t attn_bwd_preprocess(const void* o, const void* o_lo, const void* dO,
                                   const float* lse, void* dq, int B, int Hq, int Hkv, int S, int D,
                                   void* workspace, size_t workspace_bytes, void* stream);
+attn_status_t attn_bwd_dvec(const void* q, const void* k, const void* v, const void* dO, int B,
+                            int Hq, int Hkv, int S, int D, int causal, int window, float scale,
+                            void* workspace, size_t workspace_bytes, void* stream);
 attn_status_t attn_bwd_main(const void* q, const void* k, const void* v, const void* dO, void* dq,
                             void* dk, void* dv, int B, int Hq, int Hkv, int S, int D, int causal,
                             float scale, void* workspace, size_t workspace_bytes, void* stream);

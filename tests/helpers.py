@@ -12,21 +12,25 @@ TOL_LSE = 1e-3
 TOL_GRAD_REL_RMS = 5e-2
 
 
-def gpu_fwd_bwd(q, k, v, do, causal, scale, with_bwd=True, window=0):
+def gpu_fwd_bwd(q, k, v, do, causal, scale, with_bwd=True, window=0, residual=True):
     """Run attn_fwd_residual (and attn_bwd with the residual) on cuda:0 for
     bf16 CPU tensors; returns a dict of CPU tensors (o, lse, dq, dk, dv).
-    With window > 0 the sliding-window forms (attn_fwd_ex, attn_bwd_ex) run."""
+    With window > 0 the sliding-window forms (attn_fwd_ex, attn_bwd_ex) run.
+    With residual=False the plain calls run instead: attn_fwd (o and lse only)
+    and attn_bwd with o_lo = None (or their window forms without o_lo)."""
     dev = torch.device("cuda", 0)
     qd, kd, vd, dod = (t.to(dev).contiguous() for t in (q, k, v, do))
     B, S, Hq, D = q.shape
     Hkv = k.shape[2]
     o = torch.empty_like(qd)
-    o_lo = torch.empty_like(qd)
+    o_lo = torch.empty_like(qd) if residual else None
     lse = torch.empty(B, Hq, S, dtype=torch.float32, device=dev)
     if window:
         attn.attn_fwd_ex(qd, kd, vd, o, lse, causal, window, scale, o_lo=o_lo)
-    else:
+    elif residual:
         attn.attn_fwd_residual(qd, kd, vd, o, o_lo, lse, causal, scale)
+    else:
+        attn.attn_fwd(qd, kd, vd, o, lse, causal, scale)
     out = {"o": o, "lse": lse}
     ws = None
     if with_bwd:

@@ -251,3 +251,132 @@ def test_dense_models_catch_planted_mistakes():
     with pytest.raises(Deadlock):
         dense_bwd_model(3, True, seed=0, stage_last=False)
 
+
+
+def dvec_model(items, nslot, seed=0, early_free=False):
+    """The backward's Dvec pass: the forward's producer (Q and dO of both
+    tiles per item, K/V ring), an MMA issuer that per key tile issues both
+    tiles' S products (then hands K_j back) and both tiles' dP products (then
+    hands V_j back), each tile's S/dP buffers reused only after its rows have
+    read them; two row groups. early_free plants a mistake: the row groups
+    hand their buffers back before reading them."""
+    rnd = random.Random(seed)
+    kv_full = [Bar(1) for _ in range(nslot)]
+    kv_empty = [Bar(1) for _ in range(nslot)]
+    q_full, q_empty, mma_done = Bar(1), Bar(1), Bar(1)
+    sdp_full, sdp_free = [Bar(1), Bar(1)], [Bar(1), Bar(1)]
+    tma, mma = [], []
+    # Which product pair of tile t each buffer holds, to catch a read of a
+    # buffer that the next pair has already overwritten.
+    held = [None, None]
+
+    class Overwritten(Exception):
+        pass
+
+    def producer():
+        issued = q_loads = 0
+        for r, (n0, n1, l0, l1) in enumerate(items):
+            n_pos = 2 * (n1 - l0)
+
+            def load_kv():
+                nonlocal issued
+                slot, rnd_ = issued % nslot, issued // nslot
+                if rnd_ > 0:
+                    yield from wait(kv_empty[slot], rnd_ - 1)
+                tma.append(kv_full[slot])
+                issued += 1
+            pre = 0 if r == 0 else min(2, n_pos)
+            for _ in range(pre):
+                yield from load_kv()
+            if r > 0:
+                yield from wait(q_empty, r - 1)
+            tma.append(q_full)
+            q_loads += 1
+            for _ in range(pre, n_pos):
+                yield from load_kv()
+        for pos in range(max(0, issued - nslot), issued):
+            yield from wait(kv_full[pos % nslot], pos // nslot)
+        yield from wait(q_full, q_loads - 1)
+
+    class Write:
+        """An MMA completion that overwrites tile t's buffers with pair n."""
+        def __init__(self, t, n):
+            self.t, self.n = t, n
+
+        def arrive(self):
+            held[self.t] = self.n
+            Bar.changes += 1
+
+    def mma_warp():
+        ring, n_sdp = 0, [0, 0]
+        for r, (n0, n1, l0, l1) in enumerate(items):
+            n_kv, jlo, jb = (n0, n1), (l0, l1), l0
+            yield from wait(q_full, r)
+            left = (n0 - l0) + (n1 - l1)
+
+            def wait_kv(idx):
+                q = ring + idx
+                yield from wait(kv_full[q % nslot], q // nslot)
+
+            def slot(idx):
+                return (ring + idx) % nslot
+            for j in range(jb, n1):
+                yield from wait_kv(2 * (j - jb))
+                for t in range(2):
+                    if jlo[t] <= j < n_kv[t]:
+                        if n_sdp[t] > 0:
+                            yield from wait(sdp_free[t], n_sdp[t] - 1)
+                        mma.append(Write(t, n_sdp[t]))
+                mma.append(kv_empty[slot(2 * (j - jb))])
+                yield from wait_kv(2 * (j - jb) + 1)
+                for t in range(2):
+                    if jlo[t] <= j < n_kv[t]:
+                        mma.append(sdp_full[t])
+                        n_sdp[t] += 1
+                        left -= 1
+                        if left == 0:
+                            mma.append(q_empty)
+                mma.append(kv_empty[slot(2 * (j - jb) + 1)])
+            ring += 2 * (n1 - jb)
+        mma.append(mma_done)
+        yield from wait(mma_done, 0)
+
+    def rows(t):
+        n_seen = 0
+        for it in items:
+            for _ in range(it[2 + t], it[t]):
+                yield from wait(sdp_full[t], n_seen)
+                if early_free:
+                    sdp_free[t].arrive()
+                    yield
+                if held[t] != n_seen:
+                    raise Overwritten(f"tile {t}: pair {n_seen} read after pair {held[t]} landed")
+                if not early_free:
+                    sdp_free[t].arrive()
+                n_seen += 1
+
+    agents = [producer(), mma_warp(), rows(0), rows(1)]
+    try:
+        return run(agents, (tma, mma, []), rnd)
+    except Overwritten as e:
+        from tests.protocol_sim import Aliasing
+        raise Aliasing(str(e))
+
+
+@pytest.mark.parametrize("S,causal,window", FWD_CASES)
+@pytest.mark.parametrize("nslot", [3, 8])
+def test_dvec_pass_protocol_is_sound(S, causal, window, nslot):
+    items = fwd_items(S, causal, window)
+    for seed in range(25):
+        assert dvec_model(items, nslot, seed=seed)
+
+
+def test_dvec_model_catches_an_early_buffer_release():
+    from tests.protocol_sim import Aliasing
+    caught = 0
+    for seed in range(40):
+        try:
+            dvec_model(fwd_items(1024, True), 3, seed=seed, early_free=True)
+        except Aliasing:
+            caught += 1
+    assert caught > 0

@@ -46,6 +46,20 @@ def test_stalled_pipeline_times_out_and_context_survives():
         attn.attn_bwd(q, k, v, o, do, lse, dq, dk, dv, True, scale, ws, o_lo=o_lo)
         assert attn.attn_check_status(ws) == TIMEOUT_STATUS
         assert attn.attn_check_status(ws) == 0  # reading clears the word
+        # Without o_lo the backward also runs the Dvec pass; its MMA warp
+        # takes the same hook.
+        attn.attn_bwd_preprocess(q, k, o, do, lse, dq, ws)
+        attn.attn_bwd_dvec(q, k, v, do, True, scale, ws)
+        assert attn.attn_check_status(ws) == TIMEOUT_STATUS
+        attn.attn_bwd(q, k, v, o, do, lse, dq, dk, dv, True, scale, ws)
+        assert attn.attn_check_status(ws) == TIMEOUT_STATUS
+        # A timeout stays recorded until it is read: a later call on the same
+        # workspace does not erase it.
+        attn.attn_bwd(q, k, v, o, do, lse, dq, dk, dv, True, scale, ws, o_lo=o_lo)
+        attn.attn_set_fault_injection(0)
+        attn.attn_bwd(q, k, v, o, do, lse, dq, dk, dv, True, scale, ws, o_lo=o_lo)
+        assert attn.attn_check_status(ws) == TIMEOUT_STATUS
+        assert attn.attn_check_status(ws) == 0
     finally:
         attn.attn_set_fault_injection(0)
         attn.attn_set_wait_timeout_ns(0)

@@ -32,14 +32,17 @@ SMALL = [
 ]
 
 
+# residual=True: the training pair attn_fwd_residual -> attn_bwd(o_lo);
+# residual=False: the plain pair attn_fwd -> attn_bwd(o_lo = NULL).
+@pytest.mark.parametrize("residual", [True, False], ids=["residual", "plain"])
 @pytest.mark.parametrize("B,Hq,Hkv,S,D,causal", SMALL)
-def test_small_shapes_elementwise(B, Hq, Hkv, S, D, causal):
+def test_small_shapes_elementwise(B, Hq, Hkv, S, D, causal, residual):
     scale = 1.0 / np.sqrt(D)
     q, k, v, do = make_inputs(B, Hq, Hkv, S, D, seed=100 + S + D + Hq)
-    got = gpu_fwd_bwd(q, k, v, do, causal, scale)
+    got = gpu_fwd_bwd(q, k, v, do, causal, scale, residual=residual)
     o_ref, lse_ref = attn_ref_fwd(np64(q), np64(k), np64(v), causal, scale)
     dq_ref, dk_ref, dv_ref = attn_ref_bwd(np64(q), np64(k), np64(v), np64(do), causal, scale)
-    what = f"B{B} Hq{Hq} Hkv{Hkv} S{S} D{D} causal={causal}"
+    what = f"B{B} Hq{Hq} Hkv{Hkv} S{S} D{D} causal={causal} residual={residual}"
     assert_close_fwd(got["o"], got["lse"], o_ref, lse_ref, what)
     assert_close_grad(got["dq"], dq_ref, "dQ", what)
     assert_close_grad(got["dk"], dk_ref, "dK", what)
@@ -66,10 +69,11 @@ def test_special_scales(scale, causal):
     assert_close_grad(got["dv"], dv_ref, "dV", what)
 
 
-def test_tiny_workload_full():
+@pytest.mark.parametrize("residual", [True, False], ids=["residual", "plain"])
+def test_tiny_workload_full(residual):
     w = WORKLOADS[0]
     q, k, v, do = workload_inputs(w)
-    got = gpu_fwd_bwd(q, k, v, do, w.causal, w.scale)
+    got = gpu_fwd_bwd(q, k, v, do, w.causal, w.scale, residual=residual)
     o_ref, lse_ref = attn_ref_fwd(np64(q), np64(k), np64(v), w.causal, w.scale)
     dq_ref, dk_ref, dv_ref = attn_ref_bwd(np64(q), np64(k), np64(v), np64(do), w.causal, w.scale)
     assert_close_fwd(got["o"], got["lse"], o_ref, lse_ref, w.name)
@@ -78,9 +82,9 @@ def test_tiny_workload_full():
     assert_close_grad(got["dv"], dv_ref, "dV", w.name)
 
 
-def _sampled_check(w, n_rows=64, n_key_groups=1):
+def _sampled_check(w, n_rows=64, n_key_groups=1, residual=True):
     q, k, v, do = workload_inputs(w)
-    got = gpu_fwd_bwd(q, k, v, do, w.causal, w.scale)
+    got = gpu_fwd_bwd(q, k, v, do, w.causal, w.scale, residual=residual)
     do_t = do
     # float32 copies are exact for bf16 values; the oracle upcasts to fp64.
     q, k, v, do = (t.float().numpy() for t in (q, k, v, do))
@@ -94,14 +98,15 @@ def _sampled_check(w, n_rows=64, n_key_groups=1):
     o_g = np.stack([np64(got["o"][b, i, h]) for b, h, i in rows])
     l_g = np.array([float(got["lse"][b, h, i]) for b, h, i in rows])
     dq_g = np.stack([np64(got["dq"][b, i, h]) for b, h, i in rows])
-    assert_close_fwd(o_g, l_g, o_ref, lse_ref, w.name)
-    assert_close_grad(dq_g, dq_ref, "dQ rows", w.name)
+    what = f"{w.name} residual={residual}"
+    assert_close_fwd(o_g, l_g, o_ref, lse_ref, what)
+    assert_close_grad(dq_g, dq_ref, "dQ rows", what)
     for _ in range(n_key_groups):
         b, g = int(rng.integers(w.B)), int(rng.integers(w.Hkv))
         keys = sorted(set(int(x) for x in rng.integers(0, w.S, 64)) | {0, w.S - 1})
         dk_ref, dv_ref = attn_ref_keys_dkdv(q, k, v, do, w.causal, w.scale, b, g, keys)
-        assert_close_grad(np64(got["dk"][b, keys, g]), dk_ref, "dK rows", w.name)
-        assert_close_grad(np64(got["dv"][b, keys, g]), dv_ref, "dV rows", w.name)
+        assert_close_grad(np64(got["dk"][b, keys, g]), dk_ref, "dK rows", what)
+        assert_close_grad(np64(got["dv"][b, keys, g]), dv_ref, "dV rows", what)
     # Exact invariants over all rows: sum_j dK_j = 0, sum_j dV_j = sum of the group's dO.
     G = w.Hq // w.Hkv
     dk_sum = got["dk"].to(torch.float64).sum(dim=1)          # [B, Hkv, D]
@@ -117,10 +122,21 @@ def _sampled_check(w, n_rows=64, n_key_groups=1):
     assert float((dv_sum - do_sum).abs().max()) <= bound_v, (float((dv_sum - do_sum).abs().max()), bound_v)
 
 
+@pytest.mark.parametrize("residual", [True, False], ids=["residual", "plain"])
 @pytest.mark.parametrize("name", [w.name for w in WORKLOADS[1:]])
-def test_workload_sampled(name):
+def test_workload_sampled(name, residual):
     w = {x.name: x for x in WORKLOADS}[name]
-    _sampled_check(w)
+    _sampled_check(w, residual=residual)
+
+
+def test_plain_forward_matches_residual_forward():
+    """attn_fwd and attn_fwd_residual run the same arithmetic (the residual
+    form only stores o_lo as well), so o and lse agree bit for bit."""
+    for (B, Hq, Hkv, S, D, causal) in ((1, 4, 2, 384, 128, True), (2, 2, 2, 200, 64, False)):
+        q, k, v, do = make_inputs(B, Hq, Hkv, S, D, seed=11 + S)
+        a = gpu_fwd_bwd(q, k, v, do, causal, D ** -0.5, with_bwd=False, residual=True)
+        b = gpu_fwd_bwd(q, k, v, do, causal, D ** -0.5, with_bwd=False, residual=False)
+        assert torch.equal(a["o"], b["o"]) and torch.equal(a["lse"], b["lse"])
 
 
 def test_repeatable_outputs():

@@ -30,14 +30,17 @@ CASES = [
 ]
 
 
+# residual=False: attn_fwd_ex without o_lo, then attn_bwd_ex without o_lo,
+# whose Dvec comes from the windowed Dvec pass.
+@pytest.mark.parametrize("residual", [True, False], ids=["residual", "plain"])
 @pytest.mark.parametrize("B,Hq,Hkv,S,D,W", CASES)
-def test_window_elementwise(B, Hq, Hkv, S, D, W):
+def test_window_elementwise(B, Hq, Hkv, S, D, W, residual):
     scale = 1.0 / np.sqrt(D)
     q, k, v, do = make_inputs(B, Hq, Hkv, S, D, seed=500 + S + W)
-    got = gpu_fwd_bwd(q, k, v, do, True, scale, window=W)
+    got = gpu_fwd_bwd(q, k, v, do, True, scale, window=W, residual=residual)
     o_ref, lse_ref = attn_ref_fwd(np64(q), np64(k), np64(v), True, scale, window=W)
     dq_ref, dk_ref, dv_ref = attn_ref_bwd(np64(q), np64(k), np64(v), np64(do), True, scale, window=W)
-    what = f"B{B} Hq{Hq} Hkv{Hkv} S{S} D{D} window={W}"
+    what = f"B{B} Hq{Hq} Hkv{Hkv} S{S} D{D} window={W} residual={residual}"
     assert_close_fwd(got["o"], got["lse"], o_ref, lse_ref, what)
     assert_close_grad(got["dq"], dq_ref, "dQ", what)
     assert_close_grad(got["dk"], dk_ref, "dK", what)

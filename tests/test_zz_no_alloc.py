@@ -56,3 +56,36 @@ def test_noalloc_rejects_problems_beyond_its_scratch():
     fake = ctypes.c_void_p(0x10000)
     st = L.attn_bwd_noalloc(*([fake] * 9), None, 4, 64, 8, 8192, 128, 1, 0.088, None)
     assert st == 5  # ATTN_ERR_WORKSPACE, nothing launched
+
+
+def test_noalloc_reports_a_timeout_through_check_status():
+    """A bounded wait that runs out inside attn_bwd_noalloc is reported by
+    attn_check_status(NULL), which reads the status word in the library's
+    scratch array once a call on the device has looked the array up. The
+    stall comes from the testing hook (the backward's MMA warp issues
+    nothing) with a 2 ms wait limit: no fault, trap or unbounded wait."""
+    L = attn.lib()
+    dev = torch.device("cuda", 0)
+    B, Hq, Hkv, S, D = 1, 2, 1, 256, 64
+    scale = D ** -0.5
+    q, k, v, do = (t.to(dev) for t in make_inputs(B, Hq, Hkv, S, D, seed=3))
+    o, o_lo = torch.empty_like(q), torch.empty_like(q)
+    lse = torch.empty(B, Hq, S, dtype=torch.float32, device=dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty(q.shape, **f32), torch.empty(k.shape, **f32), torch.empty(k.shape, **f32)
+    assert L.attn_fwd_residual(_p(q), _p(k), _p(v), _p(o), _p(o_lo), _p(lse), B, Hq, Hkv, S, D, 1,
+                               scale, None) == 0
+    assert attn.attn_check_status(None) == 0
+    attn.attn_set_wait_timeout_ns(2_000_000)
+    try:
+        attn.attn_set_fault_injection(2)
+        assert L.attn_bwd_noalloc(_p(q), _p(k), _p(v), _p(o), _p(do), _p(lse), _p(dq), _p(dk), _p(dv),
+                                  _p(o_lo), B, Hq, Hkv, S, D, 1, scale, None) == 0
+        assert attn.attn_check_status(None) == 4  # ATTN_ERR_TIMEOUT
+        assert attn.attn_check_status(None) == 0  # reading cleared it
+    finally:
+        attn.attn_set_fault_injection(0)
+        attn.attn_set_wait_timeout_ns(0)
+    assert L.attn_bwd_noalloc(_p(q), _p(k), _p(v), _p(o), _p(do), _p(lse), _p(dq), _p(dk), _p(dv),
+                              _p(o_lo), B, Hq, Hkv, S, D, 1, scale, None) == 0
+    assert attn.attn_check_status(None) == 0

@@ -389,7 +389,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
               // exponent is -inf and its probability 0 (the scale is never 0).
               const float p0 = ex2(e0), p1 = ex2(e1);
               sums[(c / 2) & 1] = add_f32x2(sums[(c / 2) & 1], f32x2(p0, p1));
-              const uint32_t w = round_bf16x2(p0, p1);
+              const uint32_t w = pack_bf16x2(p0, p1);  // round to nearest even
               pk[c / 2] = w;
               sumsb[(c / 2) & 1] =
                   add_f32x2(sumsb[(c / 2) & 1], f32x2(__uint_as_float(w << 16),

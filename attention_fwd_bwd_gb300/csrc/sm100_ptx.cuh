@@ -490,15 +490,6 @@ __device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, u
   lo = __byte_perm(__float_as_uint(r0), __float_as_uint(r1), 0x7632);
 }
 
-// Two non-negative finite fp32 values (x0 in the low half) as a bf16 pair,
-// each rounded to nearest with ties away from zero: adding half a bf16 unit
-// (0x8000) to the fp32 bit pattern carries into the kept upper 16 bits exactly
-// when the dropped lower half is at least half a unit. One integer add per
-// value and one byte permute per pair.
-__device__ __forceinline__ uint32_t round_bf16x2(float x0, float x1) {
-  return __byte_perm(__float_as_uint(x0) + 0x8000u, __float_as_uint(x1) + 0x8000u, 0x7632);
-}
-
 // Three-input max / min (NaN inputs are ignored, as with fmaxf / fminf).
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;

@@ -215,16 +215,23 @@ attn_status_t attn_bwd_main_ex(const void* q, const void* k, const void* v, cons
  * workspace that attn_bwd asks for.
  *
  * Instead of a caller workspace the call uses one scratch array compiled into
- * the library: 16 MiB of device memory, reserved on every GPU that loads the
- * library until the process exits. Problems whose
+ * the library: 16 MiB of device memory, held on every GPU that has made such
+ * a call until the process exits. Problems whose
  * attn_bwd_workspace_size(B, Hq, Hkv, S, D) exceeds 16 MiB (about
  * B * Hq * ceil(S/128)*128 > 2,097,000 query rows) are rejected with
  * ATTN_ERR_WORKSPACE before anything is launched.
  *
  * The first call on a device looks up the array's device address with that
- * device current (cudaGetSymbolAddress); make that first call before any
- * stream capture. The call allocates nothing: no cudaMalloc, cudaFree or
- * allocating library routine.
+ * device current (cudaGetSymbolAddress). Under CUDA's lazy module loading that
+ * first call also loads the module holding the array, which reserves its
+ * 16 MiB and may synchronise the device: make one warm-up call outside any
+ * latency-critical path, and before any stream capture. After that the call
+ * allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
+ * The address is cached per device for the life of the process, so the call
+ * does not survive cudaDeviceReset or a re-created primary context.
+ *
+ * A bounded wait that runs out inside it is reported by
+ * attn_check_status(NULL), which reads the array's status word.
  *
  * All calls on a device share the one array, and it keeps the last call's
  * contents; each call rewrites every word it reads before reading it. Calls
@@ -305,11 +312,13 @@ attn_status_t attn_sparse_bwd(const void* q, const void* kp, const void* vp, con
 const char* attn_status_string(attn_status_t status);
 
 /*
- * Reads (and clears) the device status word that the forward kernels of the
- * current device, or the backward kernels using `workspace` (may be NULL for
- * the forward word only), set when a bounded pipeline wait ran out.
- * Synchronises the device. Returns ATTN_OK or ATTN_ERR_TIMEOUT (or
- * ATTN_ERR_CUDA if the read itself failed).
+ * Reads (and clears) the device status words that the kernels set when a
+ * bounded pipeline wait ran out: the forward kernels' word of the current
+ * device, and the backward word of `workspace` -- or, with workspace NULL,
+ * the word of attn_bwd_noalloc's scratch array (once a call on this device
+ * has looked the array up). A recorded timeout stays in its word until this
+ * call reads it. Synchronises the device. Returns ATTN_OK or ATTN_ERR_TIMEOUT
+ * (or ATTN_ERR_CUDA if the read itself failed).
  */
 attn_status_t attn_check_status(void* workspace);
 

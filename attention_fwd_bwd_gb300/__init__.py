@@ -35,11 +35,14 @@ __all__ = [
     "attn_set_wait_timeout_ns",
     "attn_set_fault_injection",
     "attn_status_string",
+    "use_debug_library",
     "STATUS",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_lib", "libattn.so")
+# The bounds-checked build (index checks that report ATTN_ERR_BOUNDS), for tests.
+LIB_DEBUG_PATH = os.path.join(_HERE, "_lib", "libattn_debug.so")
 
 STATUS = {
     0: "ATTN_OK",
@@ -48,9 +51,19 @@ STATUS = {
     3: "ATTN_ERR_CUDA",
     4: "ATTN_ERR_TIMEOUT",
     5: "ATTN_ERR_WORKSPACE",
+    6: "ATTN_ERR_BOUNDS",
 }
 
 _lib = None
+_lib_debug = None
+_use_debug = False
+
+
+def use_debug_library(flag=True):
+    """Route every call of this module to the bounds-checked build
+    libattn_debug.so (flag True) or back to libattn.so."""
+    global _use_debug
+    _use_debug = bool(flag)
 
 
 class AttnError(RuntimeError):
@@ -60,16 +73,21 @@ class AttnError(RuntimeError):
 
 
 def lib():
-    """The loaded libattn.so with argument types set (raises if it is missing)."""
-    global _lib
-    if _lib is not None:
+    """The loaded libattn.so (or, after use_debug_library(True),
+    libattn_debug.so) with argument types set (raises if it is missing)."""
+    global _lib, _lib_debug
+    if _use_debug and _lib_debug is not None:
+        return _lib_debug
+    if not _use_debug and _lib is not None:
         return _lib
-    if not os.path.exists(LIB_PATH):
+    path = LIB_DEBUG_PATH if _use_debug else LIB_PATH
+    if not os.path.exists(path):
         raise ImportError(
-            f"libattn.so not found at {LIB_PATH}; build it with "
+            f"{os.path.basename(path)} not found at {path}; build it with "
             "`python -c 'import __graft_entry__ as g; g.build()'` "
-            "or `python attention_fwd_bwd_gb300/_build.py`")
-    L = ctypes.CDLL(LIB_PATH)
+            "or `python attention_fwd_bwd_gb300/_build.py`"
+            + (" (debug=True for the bounds-checked build)" if _use_debug else ""))
+    L = ctypes.CDLL(path)
     vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     L.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
     L.attn_fwd.restype = i
@@ -107,7 +125,10 @@ def lib():
     L.attn_set_wait_timeout_ns.restype = None
     L.attn_set_fault_injection.argtypes = [i]
     L.attn_set_fault_injection.restype = None
-    _lib = L
+    if _use_debug:
+        _lib_debug = L
+    else:
+        _lib = L
     return L
 
 

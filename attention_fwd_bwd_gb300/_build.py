@@ -15,6 +15,9 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libattn.so")
+# The bounds-checked build (-DATTN_DEBUG_BOUNDS): the same kernels with index
+# checks that record ATTN_ERR_BOUNDS and skip the access; for tests only.
+LIB_DEBUG = os.path.join(LIBDIR, "libattn_debug.so")
 SOURCES = ["attn_api.cu", "attn_fwd.cu", "attn_bwd.cu", "attn_bwd_dvec.cu", "attn_noalloc.cu", "attn_sparse.cu",
            "attn_sparse_bwd.cu"]
 HEADERS = ["attn_common.cuh", "attn_sparse.cuh", "sm100_ptx.cuh"]
@@ -29,34 +32,37 @@ def _nvcc():
     raise RuntimeError("nvcc not found: the CUDA toolkit is required to build libattn.so")
 
 
-def _digest():
+def _digest(extra=()):
     h = hashlib.sha256()
     for name in SOURCES + HEADERS:
         with open(os.path.join(CSRC, name), "rb") as f:
             h.update(name.encode() + f.read())
     with open(os.path.join(ROOT, "include", "attn.h"), "rb") as f:
         h.update(f.read())
-    h.update(" ".join(ARCH + FLAGS).encode())
+    h.update(" ".join(ARCH + FLAGS + list(extra)).encode())
     return h.hexdigest()
 
 
-def build(force=False, verbose=False):
-    """Compile libattn.so if missing or stale; returns its path."""
+def build(force=False, verbose=False, debug=False):
+    """Compile libattn.so (debug=True: libattn_debug.so, the bounds-checked
+    build) if missing or stale; returns its path."""
     os.makedirs(LIBDIR, exist_ok=True)
-    stamp = os.path.join(LIBDIR, "libattn.sha256")
-    digest = _digest()
-    if not force and os.path.exists(LIB) and os.path.exists(stamp):
+    lib = LIB_DEBUG if debug else LIB
+    extra = ["-DATTN_DEBUG_BOUNDS"] if debug else []
+    stamp = os.path.join(LIBDIR, "libattn_debug.sha256" if debug else "libattn.sha256")
+    digest = _digest(extra)
+    if not force and os.path.exists(lib) and os.path.exists(stamp):
         with open(stamp) as f:
             if f.read().strip() == digest:
-                return LIB
+                return lib
     nvcc = _nvcc()
-    objdir = os.path.join(LIBDIR, "obj")
+    objdir = os.path.join(LIBDIR, "obj_debug" if debug else "obj")
     os.makedirs(objdir, exist_ok=True)
 
     def compile_one(src):
         obj = os.path.join(objdir, src.replace(".cu", ".o"))
-        cmd = [nvcc] + ARCH + FLAGS + ["-I", os.path.join(ROOT, "include"), "-c",
-                                       os.path.join(CSRC, src), "-o", obj]
+        cmd = [nvcc] + ARCH + FLAGS + extra + ["-I", os.path.join(ROOT, "include"), "-c",
+                                               os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
@@ -67,15 +73,15 @@ def build(force=False, verbose=False):
     if verbose:
         for _, log in results:
             print(log)
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     cmd = [nvcc] + ARCH + ["-shared", "-o", tmp] + [o for o, _ in results]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib)
     with open(stamp, "w") as f:
         f.write(digest)
-    return LIB
+    return lib
 
 
 if __name__ == "__main__":

@@ -209,6 +209,7 @@ attn_status_t finish(cudaError_t e, cudaStream_t stream, int* status_dev, bool t
     if (cudaStreamSynchronize(stream) != cudaSuccess) return ATTN_ERR_CUDA;
     const int st = status_dev ? read_clear_status(status_dev, tagged) : 0;
     if (st < 0) return ATTN_ERR_CUDA;
+    if (st == ATTN_ERR_BOUNDS) return ATTN_ERR_BOUNDS;
     if (st != 0) return ATTN_ERR_TIMEOUT;
   }
   return ATTN_OK;
@@ -236,6 +237,7 @@ const char* attn_status_string(attn_status_t s) {
     case ATTN_ERR_CUDA: return "CUDA error";
     case ATTN_ERR_TIMEOUT: return "kernel pipeline wait timed out";
     case ATTN_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case ATTN_ERR_BOUNDS: return "index check failed (bounds-checked build)";
   }
   return "unknown status";
 }
@@ -619,6 +621,7 @@ attn_status_t attn_check_status(void* workspace) {
   int* ws_word = workspace ? static_cast<int*>(workspace) : noalloc_status_word();
   const int b = ws_word ? read_clear_status(ws_word, true) : 0;
   if (a < 0 || b < 0) return ATTN_ERR_CUDA;
+  if (a == ATTN_ERR_BOUNDS || b == ATTN_ERR_BOUNDS) return ATTN_ERR_BOUNDS;
   return (a != 0 || b != 0) ? ATTN_ERR_TIMEOUT : ATTN_OK;
 }
 

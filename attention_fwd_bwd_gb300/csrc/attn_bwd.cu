@@ -260,6 +260,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         ATTN_TRACE_EV(tc, 2, it);  // stage free, issuing loads
         const int h = g * p.G + it / niq;
         const int q0 = (i_start + it % niq) * BQ;
+        if (!bounds_ok(h < p.Hq && q0 >= 0 && q0 + BQ <= p.S_pad && s < ST, ctl)) {
+          ok = false;
+          break;
+        }
         const uint32_t full = smem_u32(&bar_st_full[s]);
         mbar_arrive_expect_tx_el(full, 2 * C::Q_BYTES + 2 * C::ROWVEC_BYTES);
         for (int c = 0; c < C::KCH; ++c) {
@@ -328,6 +332,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           const int s1 = (it + 1) % ST;
           ATTN_TRACE_EV(tc, 7, it + 1);  // start waiting for stage / sdp_free
           ok = mbar_wait_warp(smem_u32(&bar_st_full[s1]), ((it + 1) / ST) & 1, ctl);
+          ATTN_TRACE_EV(tc, 10, it + 1);  // stage landed
           if (ok) ok = mbar_wait_warp(smem_u32(&bar_sdp_free), it & 1, ctl);
           if (!ok) break;
           tc_fence_after();
@@ -539,10 +544,16 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       }
     }
     if (ok) ok = mbar_wait_warp(smem_u32(&bar_mma_done), 0, ctl);
+    // dK and dV rows in fp32; this warpgroup stores columns [cg*D/2, (cg+1)*D/2).
+    const size_t rowoff = ((static_cast<size_t>(b) * p.S + key) * p.Hkv + g) * D;
+    {
+      // (warp-uniform outcome: the TMEM loads below are .sync.aligned)
+      const bool row_in =
+          !key_valid || bounds_ok(rowoff + D <= static_cast<size_t>(p.B) * p.S * p.Hkv * D, ctl);
+      if (!__all_sync(0xffffffffu, row_in)) ok = false;
+    }
     if (ok) {
       tc_fence_after();
-      // dK and dV rows in fp32; this warpgroup stores columns [cg*D/2, (cg+1)*D/2).
-      const size_t rowoff = ((static_cast<size_t>(b) * p.S + key) * p.Hkv + g) * D;
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
         const uint32_t col0 = (t == 0 ? C::TM_DK : C::TM_DV) + cg * (D / 2);
@@ -605,7 +616,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       if (lane == 0) {
         const int h = g * p.G + itq / niq;
         const int q0 = (i_start + itq % niq) * BQ;
-        tma_reduce_add_4d(&tm_dq, 0, h, q0 + half * C::DQ_ROWS, b, sDQS + half * C::DQS_BYTES);
+        if (bounds_ok(h < p.Hq && q0 + (half + 1) * C::DQ_ROWS <= p.S_pad, ctl))
+          tma_reduce_add_4d(&tm_dq, 0, h, q0 + half * C::DQ_ROWS, b, sDQS + half * C::DQS_BYTES);
         bulk_commit_group();
         bulk_wait_read_all();
         mbar_arrive(smem_u32(&bar_stg_free[half]));
@@ -656,7 +668,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         }
         fence_async_smem();
         named_bar_sync(1, 128);
-        if (t == 0) {
+        if (t == 0 && bounds_ok(h < p.Hq && q0 + (half + 1) * C::DQ_ROWS <= p.S_pad, ctl)) {
           tma_reduce_add_4d(&tm_dq, 0, h, q0 + half * C::DQ_ROWS, b, sDQS);
           bulk_commit_group();
         }

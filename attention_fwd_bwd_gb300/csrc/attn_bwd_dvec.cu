@@ -106,6 +106,11 @@ __global__ void __launch_bounds__(DvecCfg<D>::THREADS, 1)
         const int slot = pos % C::NSLOT, round = pos / C::NSLOT;
         if (round > 0) ok = mbar_wait_warp(smem_u32(&bar_kv_empty[slot]), (round - 1) & 1, ctl);
         if (!ok) return;
+        if (!bounds_ok(jb + (idx >> 1) >= 0 && (jb + (idx >> 1)) * C::BK < p.S && it.b < p.B &&
+                           it.g < p.Hkv, ctl)) {
+          ok = false;
+          return;
+        }
         const uint32_t full = smem_u32(&bar_kv_full[slot]);
         const uint32_t dst = sRing + slot * C::KV_BYTES;
         const CUtensorMap* m = (idx & 1) ? &tm_v : &tm_k;
@@ -277,7 +282,8 @@ __global__ void __launch_bounds__(DvecCfg<D>::THREADS, 1)
       float a0, a1, b0, b1;
       unpack_f32x2(acc[0], a0, a1);
       unpack_f32x2(acc[1], b0, b1);
-      if (qrow < p.S) p.dvec[rowoff + qrow] = (a0 + a1) + (b0 + b1);
+      if (qrow < p.S && bounds_ok(rowoff + qrow < static_cast<size_t>(p.B) * p.Hq * p.S_pad, ctl))
+        p.dvec[rowoff + qrow] = (a0 + a1) + (b0 + b1);
     }
   }
 

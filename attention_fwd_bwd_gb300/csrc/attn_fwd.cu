@@ -142,6 +142,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       prefetch_tmap(&tm_v);
     }
     const uint64_t keep = policy_evict_last();  // K/V tiles are re-read by G heads x tiles
+    const int nkv_all = (p.S + C::BK - 1) / C::BK;
+    (void)nkv_all;
     int issued = 0;   // ring positions issued
     int q_loads = 0;  // Q loads issued
     bool ok = true;
@@ -157,6 +159,11 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         if (round > 0) ok = mbar_wait_warp(smem_u32(&bar_kv_empty[slot]), (round - 1) & 1, ctl);
         if (!ok) return;
         ATTN_TRACE_EV(tc, 2, pos);  // slot free, issuing the load
+        const int jl = jb + (idx >> 1);
+        if (!bounds_ok(jl >= 0 && jl < nkv_all && it.b < p.B && it.g < p.Hkv, ctl)) {
+          ok = false;
+          return;
+        }
         const uint32_t full = smem_u32(&bar_kv_full[slot]);
         const uint32_t dst = sRing + slot * C::KV_BYTES;
         const CUtensorMap* m = (idx & 1) ? &tm_v : &tm_k;
@@ -171,6 +178,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       if (!ok) break;
       if (r > 0) ok = mbar_wait_warp(smem_u32(&bar_q_empty), (r - 1) & 1, ctl);
       if (!ok) break;
+      if (!bounds_ok(it.hq < p.Hq && it.q0 >= 0 && it.q0 < p.n_qblocks * 2 * C::BQ, ctl)) break;
       mbar_arrive_expect_tx_el(smem_u32(&bar_q_full), 2 * C::Q_BYTES);
       for (int t = 0; t < 2; ++t)
         for (int c = 0; c < C::KCH; ++c)
@@ -251,6 +259,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
               v_ready = true;
             }
             tc_fence_after();
+            if (!bounds_ok(j >= 0 && j * C::BK < p.S, ctl)) {
+              ok = false;
+              break;
+            }
             const int vslot = kv_slot(2 * (j - jb) + 1);
             const uint64_t dv = sw128_desc(sRing + vslot * C::KV_BYTES, C::BK * 128, 1024);
             // Keys 16kk..16kk+15: bf16 P pairs in score columns 16kk..16kk+7.
@@ -474,13 +486,13 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
             }
             fence_async_smem();
             named_bar_sync(bar_id, 128);
-            if (leader) {
+            if (leader && bounds_ok(hq < p.Hq && b < p.B && q0 + t * C::BQ >= 0, ctl)) {
               tma_store_4d(part ? &tm_olo : &tm_o, c, hq, q0 + t * C::BQ, b, stg);
               bulk_commit_group();
             }
           }
         }
-        if (qrow < p.S)
+        if (qrow < p.S && bounds_ok(b < p.B && hq < p.Hq && qrow >= 0, ctl))
           p.lse[(static_cast<size_t>(b) * p.Hq + hq) * p.S + qrow] = (m + __log2f(l)) * kLn2;
       }
     }

@@ -71,6 +71,27 @@ struct WaitCtl {
 // Error codes written to the status word (match attn_status_t).
 constexpr int kStatusTimeout = 4;
 
+// Status code of a failed index check in the bounds-checked build (matches
+// ATTN_ERR_BOUNDS).
+constexpr int kStatusBounds = 6;
+
+// Index check of the bounds-checked build (-DATTN_DEBUG_BOUNDS): a false
+// condition records kStatusBounds in the status word (unless a code is
+// already there), raises the CTA's abort flag so that every bounded wait
+// gives up, and returns false; the caller then skips the access it guards.
+// The regular build compiles every check away.
+#ifdef ATTN_DEBUG_BOUNDS
+__device__ __forceinline__ bool bounds_ok(bool cond, const WaitCtl& ctl) {
+  if (!cond) {
+    *ctl.abort_flag = 1;
+    atomicCAS(ctl.status, 0, kStatusBounds);
+  }
+  return cond;
+}
+#else
+__device__ __forceinline__ bool bounds_ok(bool, const WaitCtl&) { return true; }
+#endif
+
 // Slow path of mbar_wait: keeps polling, checking the abort flag and the time
 // limit every 64 polls. Returns false if the CTA was told to abort or the time
 // limit ran out (then it raises the abort flag and records a timeout in the

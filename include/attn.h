@@ -52,7 +52,9 @@ typedef enum {
   ATTN_ERR_UNSUPPORTED = 2, /* valid but unsupported: D not in {64,128}, not an sm_103 GPU */
   ATTN_ERR_CUDA = 3,        /* a CUDA runtime or driver call failed */
   ATTN_ERR_TIMEOUT = 4,     /* a kernel's bounded pipeline wait ran out (reported via status) */
-  ATTN_ERR_WORKSPACE = 5    /* workspace null, misaligned or smaller than attn_bwd_workspace_size */
+  ATTN_ERR_WORKSPACE = 5,   /* workspace null, misaligned or smaller than attn_bwd_workspace_size */
+  ATTN_ERR_BOUNDS = 6       /* bounds-checked build only (ATTN_DEBUG_BOUNDS): an index check
+                               failed, the access was skipped (reported via status) */
 } attn_status_t;
 
 /*
@@ -317,8 +319,10 @@ const char* attn_status_string(attn_status_t status);
  * device, and the backward word of `workspace` -- or, with workspace NULL,
  * the word of attn_bwd_noalloc's scratch array (once a call on this device
  * has looked the array up). A recorded timeout stays in its word until this
- * call reads it. Synchronises the device. Returns ATTN_OK or ATTN_ERR_TIMEOUT
- * (or ATTN_ERR_CUDA if the read itself failed).
+ * call reads it. Synchronises the device. Returns ATTN_OK, ATTN_ERR_TIMEOUT,
+ * ATTN_ERR_BOUNDS (a library built with ATTN_DEBUG_BOUNDS whose index check
+ * failed; that code takes precedence), or ATTN_ERR_CUDA if the read itself
+ * failed.
  */
 attn_status_t attn_check_status(void* workspace);
 

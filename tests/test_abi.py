@@ -37,8 +37,8 @@ def test_library_exports_every_declared_symbol(L):
 
 
 def test_status_strings(L):
-    for code in range(6):
-        assert L.attn_status_string(code)
+    for code in range(7):
+        assert L.attn_status_string(code) != b"unknown status"
     assert L.attn_status_string(99) == b"unknown status"
 
 
@@ -173,3 +173,16 @@ def test_binding_covers_every_entry_point():
     import attention_fwd_bwd_gb300 as attn
     for n in _declared():
         assert n in attn.__all__ and callable(getattr(attn, n)), f"no Python binding for {n}"
+
+
+def test_bounds_checked_build_compiles_and_exports_the_same_symbols():
+    """The bounds-checked build (-DATTN_DEBUG_BOUNDS) compiles for sm_103a and
+    exports every declared entry point; its argument checks are the same."""
+    from attention_fwd_bwd_gb300._build import build
+    path = build(debug=True)
+    D = ctypes.CDLL(path)
+    for n in _declared():
+        assert hasattr(D, n), f"libattn_debug.so does not export {n}"
+    D.attn_fwd.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_int] * 6 + [ctypes.c_float, ctypes.c_void_p]
+    assert D.attn_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 2, 1, 128, 96, 1, 0.125, None) == 2
+    assert D.attn_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 3, 2, 128, 64, 1, 0.125, None) == 1

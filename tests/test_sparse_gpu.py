@@ -201,3 +201,17 @@ def test_sparse_bwd_full_size_sampled():
     sum_dkp = np64(got["dkp"]).sum(axis=1)
     mag_dkp = np.abs(np64(got["dkp"])).sum(axis=1)
     assert np.max(np.abs(sum_dkp) / mag_dkp) < 1e-3
+    # Pool rows j < T are token j's own row, which only the windows of
+    # tokens j .. j+127 list (the compressed rows are T and beyond); the
+    # oracle over those tokens gives their dkp and dvp row in full.
+    rows = [0, 1, 127, 5000, 9000, w.T - 128, w.T - 1]
+    dk_got, dv_got, dk_ref, dv_ref = [], [], [], []
+    for j in rows:
+        toks = list(range(j, min(j + w.window, w.T)))
+        sel = idx[:, toks].numpy()
+        assert not np.isin(j, np.delete(idx.numpy(), toks, axis=1)), "row listed outside its window"
+        _, dkp_r, dvp_r = sparse_ref_bwd(np64(q[:, toks]), np64(kp), np64(vp), sel, np64(do[:, toks]), w.scale)
+        dk_ref.append(dkp_r[:, j]); dv_ref.append(dvp_r[:, j])
+        dk_got.append(np64(got["dkp"][:, j])); dv_got.append(np64(got["dvp"][:, j]))
+    assert_close_grad(np.stack(dk_got), np.stack(dk_ref), "dkp", w.name + " (window-only pool rows)")
+    assert_close_grad(np.stack(dv_got), np.stack(dv_ref), "dvp", w.name + " (window-only pool rows)")

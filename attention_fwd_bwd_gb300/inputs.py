@@ -134,6 +134,9 @@ SPARSE_WORKLOADS = [
     SparseWorkload("csa_flash_cr4_t8192", 1, 8192, 64, 128, 128, 128, 512, 4, 2025),
     # Small case the oracle finishes in seconds; d_v != d.
     SparseWorkload("csa_small_t512", 2, 512, 128, 128, 64, 128, 96, 4, 2026),
+    # The Pro cr4 list structure at a quarter of the tokens (top-1024 of T/4:
+    # the later tokens' lists are full), a size for detailed profiler captures.
+    SparseWorkload("csa_pro_cr4_t4096", 1, 4096, 128, 128, 128, 128, 1024, 4, 2027),
 ]
 SPARSE_BY_NAME = {w.name: w for w in SPARSE_WORKLOADS}
 

@@ -102,6 +102,7 @@ attn_status_t attn_fwd_residual(const void* q, const void* k, const void* v, voi
 
 /*
  * Size in bytes of the device workspace attn_bwd needs for these sizes (the
+ * paper has no counterpart: this library's workspace convention; the
  * status word, and fp32 Dvec and log2-scaled LSE rows with the sequence
  * padded to a multiple of 128). Returns 0 for invalid or unsupported sizes,
  * and for empty problems.
@@ -152,7 +153,8 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
 
 /*
  * The stages of attn_bwd as separate calls, for callers that time or
- * schedule them one by one. Arguments and errors are those of attn_bwd; each
+ * schedule them one by one (the same gradient of Eq. (1), section 2.1; the
+ * split into stages is this library's). Arguments and errors are those of attn_bwd; each
  * stage reads what the previous one left in `workspace` and `dq`, so they
  * must run in order on one stream with the same arguments:
  *   attn_bwd_preprocess: Dvec = rowsum(dO * (o + o_lo)) (o alone when o_lo is
@@ -310,10 +312,12 @@ attn_status_t attn_sparse_bwd(const void* q, const void* kp, const void* vp, con
                               int DK, int DV, float scale, void* workspace, size_t workspace_bytes,
                               void* stream);
 
-/* Static, human-readable name of a status code. */
+/* Static, human-readable name of a status code (library convention; the paper
+ * has no counterpart). */
 const char* attn_status_string(attn_status_t status);
 
 /*
+ * Failure reporting of this library (the paper has no counterpart).
  * Reads (and clears) the device status words that the kernels set when a
  * bounded pipeline wait ran out: the forward kernels' word of the current
  * device, and the backward word of `workspace` -- or, with workspace NULL,
@@ -327,6 +331,7 @@ const char* attn_status_string(attn_status_t status);
 attn_status_t attn_check_status(void* workspace);
 
 /*
+ * (Library control; the paper has no counterpart.)
  * Sets the time limit of every bounded wait inside the kernels launched after
  * this call on this process, in nanoseconds (default 2e9, i.e. 2 s; 0 restores
  * the default). A limit shorter than a pipeline step makes the kernels give

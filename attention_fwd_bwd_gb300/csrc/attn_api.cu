@@ -432,6 +432,7 @@ attn_status_t attn_bwd_main_ex(const void* q, const void* k, const void* v, cons
   p.scale_log2 = scale * kLog2e;
   p.scale = scale;
   p.n_ktiles = (S + 127) / 128;
+  p.split = 1;  // chosen by the launcher
   p.status = reinterpret_cast<int*>(ws + w.off_status);
   p.timeout_ns = g_timeout_ns;
   p.inject_stall = (g_inject_stall >> 1) & 1;

@@ -33,6 +33,10 @@ namespace {
 
 #ifdef ATTN_TRACE
 static __device__ unsigned long long g_attn_trace[kTraceCtas * kTraceRoles * kTraceEvents];
+// Per CTA of the main kernel (linear block index, up to kSpanCtas): global
+// timer at entry and at exit (ns), and the SM it ran on.
+constexpr int kSpanCtas = 16384;
+static __device__ unsigned long long g_attn_spans[kSpanCtas * 4];
 #endif
 
 // ------------------------------------------------------------------ preprocess
@@ -135,6 +139,17 @@ __device__ __forceinline__ void tma_reduce_add_4d(const CUtensorMap* m, int c0, 
       : "memory");
 }
 
+// dk and dv zeroed before a split backward adds into them.
+__global__ void __launch_bounds__(256) zero_f32x4_kernel(float4* __restrict__ a,
+                                                         float4* __restrict__ b, long long n4) {
+  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    a[i] = z;
+    b[i] = z;
+  }
+}
+
 // Writes 16 bytes to unit `u` (0..7) of 128-byte row `row` of a tile stored
 // with 128-byte swizzle (8-row atoms on 1024-byte boundaries).
 __device__ __forceinline__ void st_sw128(uint32_t tile, int row, int u, uint4 v) {
@@ -142,6 +157,23 @@ __device__ __forceinline__ void st_sw128(uint32_t tile, int row, int u, uint4 v)
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
                "r"(v.z), "r"(v.w)
                : "memory");
+}
+
+// CTAs per key tile (1 or 2): 2 splits the group's query heads in halves,
+// so the longest key tiles, which the grid starts first but which end last,
+// take half as long. It pays only where that tail is a large part of the run
+// and the extra prologue/epilogue per key tile and the zeroing of dk/dv are
+// small against a CTA's work: measured (same-box A/B, causal, D = 128) 3-5%
+// faster at B = 1, Hq = 64, Hkv = 8, S = 8192 (512 CTAs unsplit, 1024
+// iterations in the longest); 0-1% slower at B = 2, Hq = 32, S = 4096 (256
+// iterations), and 1-3% slower at S = 16384 and 32768 (1024 and 2048 CTAs).
+// Hence: an even group, at least 512 (head, query tile) iterations in the
+// longest CTA, and at most four waves of unsplit CTAs.
+int bwd_split(const BwdParams& p, int bq, int sms) {
+  const int nq = (p.S + bq - 1) / bq;
+  const int niq0 = p.window > 0 ? min(nq, (128 + p.window - 2) / bq + 1) : nq;
+  const long long ctas = static_cast<long long>(p.B) * p.Hkv * p.n_ktiles;
+  return (p.G % 2 == 0 && p.G * niq0 >= 512 && ctas <= 4LL * sms) ? 2 : 1;
 }
 
 // WIN: sliding-window instantiation (p.window > 0).
@@ -155,6 +187,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   using C = BwdCfg<D>;
   constexpr int BQ = C::BQ, BK = C::BK, ST = C::STAGES;
   constexpr int HALF = BQ / 2;  // query columns per compute warpgroup
+#ifdef ATTN_TRACE
+  const unsigned long long t_entry = globaltimer();
+#endif
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -168,9 +203,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
-  const int bg = blockIdx.x;  // b * Hkv + g
+  // blockIdx.x = (b * Hkv + g) * split + part: part takes the query heads
+  // g G + part G / split .. of the group (x varies fastest in the launch
+  // order, so every key tile's parts start together, longest first).
+  const int part = blockIdx.x % p.split;
+  const int bg = blockIdx.x / p.split;  // b * Hkv + g
   const int g = bg % p.Hkv;
   const int b = bg / p.Hkv;
+  const int hpc = p.G / p.split;        // query heads of this CTA
+  const int h0 = g * p.G + part * hpc;  // its first query head
   const int j = blockIdx.y;   // key tile; j = 0 has the most causal work
   const int k0 = j * BK;
   const int nq = (p.S + BQ - 1) / BQ;
@@ -179,7 +220,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   // k0 + BK - 1 + W - 1.
   const int i_end = WIN ? min(nq, (k0 + BK + p.window - 2) / BQ + 1) : nq;
   const int niq = i_end - i_start;
-  const int n_it = p.G * niq;
+  const int n_it = hpc * niq;
 
   const uint32_t sK = smem_u32(smem + C::SMEM_K);
   const uint32_t sV = smem_u32(smem + C::SMEM_V);
@@ -258,7 +299,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         if (round > 0) ok = mbar_wait_warp(smem_u32(&bar_st_empty[s]), (round - 1) & 1, ctl);
         if (!ok) break;
         ATTN_TRACE_EV(tc, 2, it);  // stage free, issuing loads
-        const int h = g * p.G + it / niq;
+        const int h = h0 + it / niq;
         const int q0 = (i_start + it % niq) * BQ;
         if (!bounds_ok(h < p.Hq && q0 >= 0 && q0 + BQ <= p.S_pad && s < ST, ctl)) {
           ok = false;
@@ -564,11 +605,20 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           tmem_ld32(tmem + lane_base + col0 + c, u);
           tmem_wait_ld();
           if (key_valid) {
-            float4* d4 = reinterpret_cast<float4*>(dst + c);
+            if (p.split > 1) {
+              // Two CTAs add their head halves into the zeroed row: two
+              // additions onto zero give the same sum in either order.
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              d4[i] = make_float4(__uint_as_float(u[4 * i]), __uint_as_float(u[4 * i + 1]),
-                                  __uint_as_float(u[4 * i + 2]), __uint_as_float(u[4 * i + 3]));
+              for (int i = 0; i < 8; ++i)
+                red_add_v4(dst + c + 4 * i, __uint_as_float(u[4 * i]), __uint_as_float(u[4 * i + 1]),
+                           __uint_as_float(u[4 * i + 2]), __uint_as_float(u[4 * i + 3]));
+            } else {
+              float4* d4 = reinterpret_cast<float4*>(dst + c);
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                d4[i] = make_float4(__uint_as_float(u[4 * i]), __uint_as_float(u[4 * i + 1]),
+                                    __uint_as_float(u[4 * i + 2]), __uint_as_float(u[4 * i + 3]));
+            }
           }
         }
       }
@@ -614,7 +664,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       if (!ok) break;
       ATTN_TRACE_EV(tc, 1, n);  // half staged
       if (lane == 0) {
-        const int h = g * p.G + itq / niq;
+        const int h = h0 + itq / niq;
         const int q0 = (i_start + itq % niq) * BQ;
         if (bounds_ok(h < p.Hq && q0 + (half + 1) * C::DQ_ROWS <= p.S_pad, ctl))
           tma_reduce_add_4d(&tm_dq, 0, h, q0 + half * C::DQ_ROWS, b, sDQS + half * C::DQS_BYTES);
@@ -634,7 +684,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     TraceCursor tc;
     if (lane == 0) ATTN_TRACE_INIT(tc, 10 + (warp - 8));
     for (int it = 0; it < n_it; ++it) {
-      const int h = g * p.G + it / niq;
+      const int h = h0 + it / niq;
       const int q0 = (i_start + it % niq) * BQ;
       ok = mbar_wait_warp(smem_u32(&bar_dq_full), it & 1, ctl);
       // The four drain warps meet at bar.sync below: agree first on going on.
@@ -681,6 +731,19 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   tc_fence_before();
   __syncthreads();
   if (warp == C::W_MMA) tmem_dealloc(tmem, C::TMEM_COLS);
+#ifdef ATTN_TRACE
+  if (threadIdx.x == 0) {
+    const unsigned lin = blockIdx.y * gridDim.x + blockIdx.x;
+    if (lin < kSpanCtas) {
+      unsigned smid;
+      asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+      g_attn_spans[4 * lin] = t_entry;
+      g_attn_spans[4 * lin + 1] = globaltimer();
+      g_attn_spans[4 * lin + 2] = smid;
+      g_attn_spans[4 * lin + 3] = n_it;
+    }
+  }
+#endif
 }
 
 template <int D, bool WIN>
@@ -698,8 +761,17 @@ cudaError_t launch_bwd_main_t(const CUtensorMap& tq, const CUtensorMap& tk, cons
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  dim3 grid(p.B * p.Hkv, p.n_ktiles);
-  attn_bwd_main_kernel<D, WIN><<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(tq, tk, tv, tdo, tdq, p);
+  int sms = 148;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  BwdParams pp = p;
+  pp.split = bwd_split(p, C::BQ, sms);
+  if (pp.split > 1) {
+    const long long n4 = static_cast<long long>(p.B) * p.S * p.Hkv * D / 4;
+    zero_f32x4_kernel<<<4 * sms, 256, 0, stream>>>(reinterpret_cast<float4*>(p.dk),
+                                                   reinterpret_cast<float4*>(p.dv), n4);
+  }
+  dim3 grid(p.B * p.Hkv * pp.split, p.n_ktiles);
+  attn_bwd_main_kernel<D, WIN><<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(tq, tk, tv, tdo, tdq, pp);
   return cudaGetLastError();
 }
 
@@ -739,6 +811,17 @@ cudaError_t launch_bwd_main(int D, const CUtensorMap& tq, const CUtensorMap& tk,
 }  // namespace attn
 
 #ifdef ATTN_TRACE
+// Trace build only: copies the backward main kernel's per-CTA spans out and clears them.
+extern "C" int attn_trace_copy_spans(void* host, size_t bytes) {
+  const size_t total = sizeof(attn::g_attn_spans);
+  if (bytes < total) return 1;
+  if (cudaDeviceSynchronize() != cudaSuccess) return 3;
+  if (cudaMemcpyFromSymbol(host, attn::g_attn_spans, total) != cudaSuccess) return 3;
+  static unsigned long long zeros[4096];
+  for (size_t off = 0; off < total; off += sizeof(zeros))
+    if (cudaMemcpyToSymbol(attn::g_attn_spans, zeros, sizeof(zeros), off) != cudaSuccess) return 3;
+  return 0;
+}
 // Trace build only: copies the backward main kernel's timeline records out and clears them.
 extern "C" int attn_trace_copy_bwd(void* host, size_t bytes) {
   const size_t total = sizeof(attn::g_attn_trace);

@@ -234,6 +234,10 @@ struct BwdParams {
   float scale_log2;
   float scale;
   int n_ktiles;
+  // Query heads of a kv head's group are split over `split` CTAs per key tile
+  // (1 or 2), each taking G / split consecutive heads; with 2 the dK and dV
+  // rows are added into zeroed dk and dv. Set by the launcher.
+  int split;
   int* status;
   unsigned long long timeout_ns;
   int inject_stall;  // testing hook: the MMA warp issues nothing (waits then run out)

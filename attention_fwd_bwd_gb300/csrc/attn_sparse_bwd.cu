@@ -68,12 +68,6 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
-// dst[0..3] += v (fp32, one 16-byte vector reduction in L2).
-__device__ __forceinline__ void red_add_v4(float* dst, float a, float b, float c, float d) {
-  asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(a),
-               "f"(b), "f"(c), "f"(d)
-               : "memory");
-}
 
 // ------------------------------------------------------------------ preprocess
 // One warp per (batch, token, head) row: Dvec = sum_k dO * (o + o_lo) and

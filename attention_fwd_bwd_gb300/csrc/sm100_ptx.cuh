@@ -511,6 +511,13 @@ __device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, u
   lo = __byte_perm(__float_as_uint(r0), __float_as_uint(r1), 0x7632);
 }
 
+// dst[0..3] += (a, b, c, d): one 16-byte fp32 vector reduction in L2.
+__device__ __forceinline__ void red_add_v4(float* dst, float a, float b, float c, float d) {
+  asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(a),
+               "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+
 // Three-input max / min (NaN inputs are ignored, as with fmaxf / fminf).
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;

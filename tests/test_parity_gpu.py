@@ -151,6 +151,27 @@ def test_repeatable_outputs():
     assert float((a["dq"].float() - b["dq"].float()).abs().max()) <= TOL_GRAD_REL_RMS * rms
 
 
+# Shapes where the backward splits each key tile's query heads over two CTAs
+# (an even group, >= 512 (head, query tile) iterations in the longest key
+# tile, at most four waves of key tiles): 16 heads x 32 query tiles. The two
+# halves of dK and dV are added into zeroed rows.
+@pytest.mark.parametrize("residual", [True, False], ids=["residual", "plain"])
+@pytest.mark.parametrize("S", [2048, 2000])
+def test_split_heads_elementwise(S, residual):
+    B, Hq, Hkv, D = 1, 16, 1, 128
+    scale = 1.0 / np.sqrt(D)
+    q, k, v, do = make_inputs(B, Hq, Hkv, S, D, seed=31 + S)
+    got = gpu_fwd_bwd(q, k, v, do, True, scale, residual=residual)
+    again = gpu_fwd_bwd(q, k, v, do, True, scale, residual=residual)
+    # Two additions onto zero give the same sum in either order.
+    assert torch.equal(got["dk"], again["dk"]) and torch.equal(got["dv"], again["dv"])
+    dq_ref, dk_ref, dv_ref = attn_ref_bwd(np64(q), np64(k), np64(v), np64(do), True, scale)
+    what = f"split heads S{S} residual={residual}"
+    assert_close_grad(got["dq"], dq_ref, "dQ", what)
+    assert_close_grad(got["dk"], dk_ref, "dK", what)
+    assert_close_grad(got["dv"], dv_ref, "dV", what)
+
+
 def test_empty_inputs_are_noops():
     # B == 0 or S == 0 returns ATTN_OK without reading any pointer.
     import attention_fwd_bwd_gb300 as attn

@@ -23,6 +23,13 @@
 //      before they store P^T(i+1) / dS^T(i+1) over it; D = 128: by four drain
 //      warps), staged in shared memory and added into dq with asynchronous
 //      TMA tensor reductions (fp32 add in L2).
+#include <algorithm>
+#include <map>
+#include <memory>
+#include <mutex>
+#include <utility>
+#include <vector>
+
 #include "attn_common.cuh"
 #include "sm100_ptx.cuh"
 
@@ -159,31 +166,52 @@ __device__ __forceinline__ void st_sw128(uint32_t tile, int row, int u, uint4 v)
                : "memory");
 }
 
-// CTAs per key tile (1 or 2): 2 splits the group's query heads in halves,
-// so the longest key tiles, which the grid starts first but which end last,
-// take half as long. It pays only where that tail is a large part of the run
-// and the extra prologue/epilogue per key tile and the zeroing of dk/dv are
-// small against a CTA's work: measured (same-box A/B, causal, D = 128) 3-5%
-// faster at B = 1, Hq = 64, Hkv = 8, S = 8192 (512 CTAs unsplit, 1024
-// iterations in the longest); 0-1% slower at B = 2, Hq = 32, S = 4096 (256
-// iterations), and 1-3% slower at S = 16384 and 32768 (1024 and 2048 CTAs).
-// Hence: an even group, at least 512 (head, query tile) iterations in the
-// longest CTA, and at most four waves of unsplit CTAs.
-int bwd_split(const BwdParams& p, int bq, int sms) {
+// One item of the backward main kernel: key tile j of one (batch b, kv head
+// g) and `hpc` consecutive query heads h0.. of its group (all of them, or
+// one half when the group is split), over the query tiles that see the tile.
+// Item code = (j * B * Hkv + b * Hkv + g) * split + part.
+struct BwdItem {
+  int b, g, h0, hpc, k0, i_start, niq, n_it;
+};
+template <bool WIN>
+__host__ __device__ __forceinline__ BwdItem bwd_item(const BwdParams& p, int code, int bq, int bk) {
+  BwdItem t;
+  const int part = code % p.split;
+  const int rest = code / p.split;
+  const int bg = rest % (p.B * p.Hkv);
+  const int j = rest / (p.B * p.Hkv);
+  t.g = bg % p.Hkv;
+  t.b = bg / p.Hkv;
+  t.hpc = p.G / p.split;
+  t.h0 = t.g * p.G + part * t.hpc;
+  t.k0 = j * bk;
   const int nq = (p.S + bq - 1) / bq;
-  const int niq0 = p.window > 0 ? min(nq, (128 + p.window - 2) / bq + 1) : nq;
-  const long long ctas = static_cast<long long>(p.B) * p.Hkv * p.n_ktiles;
-  return (p.G % 2 == 0 && p.G * niq0 >= 512 && ctas <= 4LL * sms) ? 2 : 1;
+  t.i_start = p.causal ? t.k0 / bq : 0;
+  // With a window of W keys, the last row that sees this tile's keys is
+  // k0 + BK - 1 + W - 1.
+  const int i_last = (t.k0 + bk + p.window - 2) / bq + 1;
+  const int i_end = WIN ? (i_last < nq ? i_last : nq) : nq;
+  t.niq = i_end - t.i_start;
+  t.n_it = t.hpc * t.niq;
+  return t;
 }
 
-// WIN: sliding-window instantiation (p.window > 0).
-template <int D, bool WIN>
+// Head and query tile of an item's iteration `it`: heads outer, query tiles
+// inner (measured as fast as or faster than query-tile-outer orders).
+__device__ __forceinline__ int bwd_head(const BwdItem& t, int it) { return t.h0 + it / t.niq; }
+__device__ __forceinline__ int bwd_qtile(const BwdItem& t, int it) { return t.i_start + it % t.niq; }
+
+// WIN: sliding-window instantiation (p.window > 0). PERSIST: one CTA per SM
+// running its list of items from the schedule; otherwise one CTA per item,
+// named by the block index (and `sched` is unused).
+template <int D, bool WIN, bool PERSIST>
 __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v,
                          const __grid_constant__ CUtensorMap tm_do,
-                         const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
+                         const __grid_constant__ CUtensorMap tm_dq, const BwdParams p,
+                         const __grid_constant__ BwdSchedArg<PERSIST> sched) {
   using C = BwdCfg<D>;
   constexpr int BQ = C::BQ, BK = C::BK, ST = C::STAGES;
   constexpr int HALF = BQ / 2;  // query columns per compute warpgroup
@@ -194,7 +222,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
 
-  __shared__ uint64_t bar_kv_full, bar_mma_done;
+  __shared__ uint64_t bar_kv_full, bar_kv_free, bar_mma_done, bar_dkv_free, bar_fin;
   __shared__ uint64_t bar_st_full[ST], bar_st_empty[ST];
   __shared__ uint64_t bar_sdp_full, bar_sdp_free, bar_pds_full, bar_pds_free, bar_dq_full,
       bar_dq_free, bar_stg_full[2], bar_stg_free[2];
@@ -203,24 +231,19 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
-  // blockIdx.x = (b * Hkv + g) * split + part: part takes the query heads
-  // g G + part G / split .. of the group (x varies fastest in the launch
-  // order, so every key tile's parts start together, longest first).
-  const int part = blockIdx.x % p.split;
-  const int bg = blockIdx.x / p.split;  // b * Hkv + g
-  const int g = bg % p.Hkv;
-  const int b = bg / p.Hkv;
-  const int hpc = p.G / p.split;        // query heads of this CTA
-  const int h0 = g * p.G + part * hpc;  // its first query head
-  const int j = blockIdx.y;   // key tile; j = 0 has the most causal work
-  const int k0 = j * BK;
-  const int nq = (p.S + BQ - 1) / BQ;
-  const int i_start = p.causal ? (k0 / BQ) : 0;
-  // With a window of W keys, the last row that sees this tile's keys is
-  // k0 + BK - 1 + W - 1.
-  const int i_end = WIN ? min(nq, (k0 + BK + p.window - 2) / BQ + 1) : nq;
-  const int niq = i_end - i_start;
-  const int n_it = hpc * niq;
+  // This CTA's items, in order: a slice of the host's schedule (persistent
+  // launch), or the one item the block index names (grid launch).
+  int n_items = 1, e0 = 0;
+  if constexpr (PERSIST) {
+    n_items = sched.off[blockIdx.x + 1] - sched.off[blockIdx.x];
+    e0 = sched.off[blockIdx.x];
+  }
+  auto item_at = [&](int ii) {
+    if constexpr (PERSIST)
+      return bwd_item<WIN>(p, static_cast<int>(sched.code[e0 + ii]), BQ, BK);
+    else
+      return bwd_item<WIN>(p, static_cast<int>(blockIdx.y * gridDim.x + blockIdx.x), BQ, BK);
+  };
 
   const uint32_t sK = smem_u32(smem + C::SMEM_K);
   const uint32_t sV = smem_u32(smem + C::SMEM_V);
@@ -231,7 +254,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 
   if (D == 64) {
     // Rows 64..127 of K^T (the second 64-column chunk of K) are zero, so the
-    // M = 128 dQ^T product carries zeros in its unused upper half.
+    // M = 128 dQ^T product carries zeros in its unused upper half. The K
+    // loads fill only the first chunk, so this holds for every item.
     uint4* z = reinterpret_cast<uint4*>(smem + C::SMEM_K + BK * 128);
     for (int i = threadIdx.x; i < BK * 128 / 16; i += blockDim.x) z[i] = make_uint4(0u, 0u, 0u, 0u);
     fence_async_smem();
@@ -239,7 +263,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(smem_u32(&bar_kv_full), 1);
+    mbar_init(smem_u32(&bar_kv_free), 1);
     mbar_init(smem_u32(&bar_mma_done), 1);
+    mbar_init(smem_u32(&bar_dkv_free), 256);
+    mbar_init(smem_u32(&bar_fin), 1);
     for (int s = 0; s < ST; ++s) {
       mbar_init(smem_u32(&bar_st_full[s]), 1);
       mbar_init(smem_u32(&bar_st_empty[s]), 1);
@@ -273,10 +300,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         C::DQ_IN_COMPUTE ? smem + C::SMEM_ROWS + s * 2 * C::ROWVEC_BYTES
                          : smem + C::SMEM_STAGE + s * C::STAGE_BYTES + 2 * C::Q_BYTES);
   };
+  // Barrier phases run on across items: `git` counts the (head, query tile)
+  // iterations of earlier items, `ii` the items.
 
   if (warp == C::W_PROD) {
     // ------------------------------------------------------------ producer
     // The whole warp runs this loop; each copy is issued by one elected lane.
+    // An item's K and V replace the previous item's once its last MMA has
+    // run (kv_free); its first query stages are issued before that wait, so
+    // they load while the previous item finishes.
     {
       TraceCursor tc;
       if (lane == 0) ATTN_TRACE_INIT(tc, 0);
@@ -287,42 +319,70 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         prefetch_tmap(&tm_v);
         prefetch_tmap(&tm_do);
       }
-      mbar_arrive_expect_tx_el(smem_u32(&bar_kv_full), 2 * C::V_BYTES);
-      for (int c = 0; c < C::KCH; ++c) {
-        tma_load_4d_el(sK + c * (BK * 128), &tm_k, smem_u32(&bar_kv_full), c * 64, g, k0, b);
-        tma_load_4d_el(sV + c * (BK * 128), &tm_v, smem_u32(&bar_kv_full), c * 64, g, k0, b);
-      }
       bool ok = true;
-      int issued = 0;
-      for (int it = 0; it < n_it; ++it) {
-        const int s = it % ST, round = it / ST;
-        if (round > 0) ok = mbar_wait_warp(smem_u32(&bar_st_empty[s]), (round - 1) & 1, ctl);
-        if (!ok) break;
-        ATTN_TRACE_EV(tc, 2, it);  // stage free, issuing loads
-        const int h = h0 + it / niq;
-        const int q0 = (i_start + it % niq) * BQ;
-        if (!bounds_ok(h < p.Hq && q0 >= 0 && q0 + BQ <= p.S_pad && s < ST, ctl)) {
+      int issued = 0, kv_issued = 0, git = 0;
+      auto load_kv = [&](const BwdItem& t) {
+        mbar_arrive_expect_tx_el(smem_u32(&bar_kv_full), 2 * C::V_BYTES);
+        for (int c = 0; c < C::KCH; ++c) {
+          tma_load_4d_el(sK + c * (BK * 128), &tm_k, smem_u32(&bar_kv_full), c * 64, t.g, t.k0, t.b);
+          tma_load_4d_el(sV + c * (BK * 128), &tm_v, smem_u32(&bar_kv_full), c * 64, t.g, t.k0, t.b);
+        }
+      };
+      for (int ii = 0; ii < n_items && ok; ++ii) {
+        const BwdItem t = item_at(ii);
+        if (!bounds_ok(t.b < p.B && t.g < p.Hkv && t.k0 < p.S, ctl)) {
           ok = false;
           break;
         }
-        const uint32_t full = smem_u32(&bar_st_full[s]);
-        mbar_arrive_expect_tx_el(full, 2 * C::Q_BYTES + 2 * C::ROWVEC_BYTES);
-        for (int c = 0; c < C::KCH; ++c) {
-          tma_load_4d_el(stage_q(s) + c * (BQ * 128), &tm_q, full, c * 64, h, q0, b);
-          tma_load_4d_el(stage_do(s) + c * (BQ * 128), &tm_do, full, c * 64, h, q0, b);
+        const int n_early = ii == 0 ? 0 : min(ST, t.n_it);  // stages issued before K/V
+        if (ii == 0) {
+          load_kv(t);
+          ++kv_issued;
         }
-        const size_t rowoff = (static_cast<size_t>(b) * p.Hq + h) * p.S_pad + q0;
-        const uint32_t rows = smem_u32(stage_rows(s));
-        bulk_load_el(rows, p.nlse2 + rowoff, C::ROWVEC_BYTES, full);
-        bulk_load_el(rows + C::ROWVEC_BYTES, p.dvec + rowoff, C::ROWVEC_BYTES, full);
-        issued = it + 1;
+        for (int it = 0; it < t.n_it; ++it) {
+          if (ii > 0 && it == n_early) {
+            ok = mbar_wait_warp(smem_u32(&bar_kv_free), (ii - 1) & 1, ctl);
+            if (!ok) break;
+            load_kv(t);
+            ++kv_issued;
+          }
+          const int gi = git + it;
+          const int s = gi % ST, round = gi / ST;
+          if (round > 0) ok = mbar_wait_warp(smem_u32(&bar_st_empty[s]), (round - 1) & 1, ctl);
+          if (!ok) break;
+          ATTN_TRACE_EV(tc, 2, gi);  // stage free, issuing loads
+          const int h = bwd_head(t, it);
+          const int q0 = bwd_qtile(t, it) * BQ;
+          if (!bounds_ok(h < p.Hq && q0 >= 0 && q0 + BQ <= p.S_pad && s < ST, ctl)) {
+            ok = false;
+            break;
+          }
+          const uint32_t full = smem_u32(&bar_st_full[s]);
+          mbar_arrive_expect_tx_el(full, 2 * C::Q_BYTES + 2 * C::ROWVEC_BYTES);
+          for (int c = 0; c < C::KCH; ++c) {
+            tma_load_4d_el(stage_q(s) + c * (BQ * 128), &tm_q, full, c * 64, h, q0, t.b);
+            tma_load_4d_el(stage_do(s) + c * (BQ * 128), &tm_do, full, c * 64, h, q0, t.b);
+          }
+          const size_t rowoff = (static_cast<size_t>(t.b) * p.Hq + h) * p.S_pad + q0;
+          const uint32_t rows = smem_u32(stage_rows(s));
+          bulk_load_el(rows, p.nlse2 + rowoff, C::ROWVEC_BYTES, full);
+          bulk_load_el(rows + C::ROWVEC_BYTES, p.dvec + rowoff, C::ROWVEC_BYTES, full);
+          issued = gi + 1;
+        }
+        if (ok && ii > 0 && t.n_it <= n_early) {  // an item of at most ST iterations
+          ok = mbar_wait_warp(smem_u32(&bar_kv_free), (ii - 1) & 1, ctl);
+          if (!ok) break;
+          load_kv(t);
+          ++kv_issued;
+        }
+        git += t.n_it;
       }
       if (lane == 0) {
         // Let every copy issued land before the CTA's shared memory goes away
         // (immediate in a normal run, where the MMA warp consumed them all).
-        for (int it = max(0, issued - ST); it < issued; ++it)
-          mbar_wait_drain(smem_u32(&bar_st_full[it % ST]), (it / ST) & 1, 50000000ull);
-        mbar_wait_drain(smem_u32(&bar_kv_full), 0, 50000000ull);
+        for (int gi = max(0, issued - ST); gi < issued; ++gi)
+          mbar_wait_drain(smem_u32(&bar_st_full[gi % ST]), (gi / ST) & 1, 50000000ull);
+        if (kv_issued > 0) mbar_wait_drain(smem_u32(&bar_kv_full), (kv_issued - 1) & 1, 50000000ull);
       }
       (void)ok;
       __syncwarp();
@@ -333,57 +393,64 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     if (lane == 0) ATTN_TRACE_INIT(tc, 1);
     // The whole warp runs this loop and builds the (warp-uniform) descriptors;
     // each MMA and commit is issued by one elected lane.
-    bool ok = !p.inject_stall && mbar_wait_warp(smem_u32(&bar_kv_full), 0, ctl);
-    if (ok) {
-      ATTN_TRACE_EV(tc, 1, 0);
-      constexpr uint32_t idesc_sdp = idesc_bf16_f32(128, BQ, 0, 0);
-      constexpr uint32_t idesc_kv = idesc_bf16_f32(128, D, 0, 1);
-      constexpr uint32_t idesc_dq = idesc_bf16_f32(128, 2 * BQ, 1, 1);
-      // Descriptor bases; each step below only adds a constant byte offset
-      // (>> 4) to the start-address field.
-      const uint64_t dK_kmaj = sw128_desc(sK, 16, 1024);
-      const uint64_t dV_kmaj = sw128_desc(sV, 16, 1024);
-      const uint64_t dK_mn = sw128_desc(sK, BK * 128, 1024);
-      // [dS_hi^T | dS_lo^T] as one MN-major operand of N = 128: the second
-      // 64-column block (dS_lo^T) sits DS_BYTES after the first.
-      const uint64_t dDs_mn = sw128_desc(sDsHi, C::DS_BYTES, 1024);
-      auto add = [](uint64_t d, uint32_t bytes) { return d + (bytes >> 4); };
-      auto issue_sdp = [&](int s) {
-        const uint64_t dq_k = sw128_desc(stage_q(s), 16, 1024);
-        const uint64_t ddo_k = sw128_desc(stage_do(s), 16, 1024);
+    bool ok = !p.inject_stall;
+    constexpr uint32_t idesc_sdp = idesc_bf16_f32(128, BQ, 0, 0);
+    constexpr uint32_t idesc_kv = idesc_bf16_f32(128, D, 0, 1);
+    constexpr uint32_t idesc_dq = idesc_bf16_f32(128, 2 * BQ, 1, 1);
+    // Descriptor bases; each step below only adds a constant byte offset
+    // (>> 4) to the start-address field.
+    const uint64_t dK_kmaj = sw128_desc(sK, 16, 1024);
+    const uint64_t dV_kmaj = sw128_desc(sV, 16, 1024);
+    const uint64_t dK_mn = sw128_desc(sK, BK * 128, 1024);
+    // [dS_hi^T | dS_lo^T] as one MN-major operand of N = 128: the second
+    // 64-column block (dS_lo^T) sits DS_BYTES after the first.
+    const uint64_t dDs_mn = sw128_desc(sDsHi, C::DS_BYTES, 1024);
+    auto add = [](uint64_t d, uint32_t bytes) { return d + (bytes >> 4); };
+    auto issue_sdp = [&](int s) {
+      const uint64_t dq_k = sw128_desc(stage_q(s), 16, 1024);
+      const uint64_t ddo_k = sw128_desc(stage_do(s), 16, 1024);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t ka = (kk >> 2) * (BK * 128) + (kk & 3) * 32;
-          const uint32_t kb = (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
-          mma_ss_el(tmem + C::TM_ST, add(dK_kmaj, ka), add(dq_k, kb), idesc_sdp, kk > 0);
-          mma_ss_el(tmem + C::TM_DPT, add(dV_kmaj, ka), add(ddo_k, kb), idesc_sdp, kk > 0);
-        }
-        mma_commit_el(smem_u32(&bar_sdp_full));
-      };
-      if (n_it > 0) {
-        ok = mbar_wait_warp(smem_u32(&bar_st_full[0]), 0, ctl);
-        if (ok) {
-          tc_fence_after();
-          issue_sdp(0);
-        }
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t ka = (kk >> 2) * (BK * 128) + (kk & 3) * 32;
+        const uint32_t kb = (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
+        mma_ss_el(tmem + C::TM_ST, add(dK_kmaj, ka), add(dq_k, kb), idesc_sdp, kk > 0);
+        mma_ss_el(tmem + C::TM_DPT, add(dV_kmaj, ka), add(ddo_k, kb), idesc_sdp, kk > 0);
       }
+      mma_commit_el(smem_u32(&bar_sdp_full));
+    };
+    int git = 0;
+    for (int ii = 0; ii < n_items && ok; ++ii) {
+      const int n_it = item_at(ii).n_it;
+      ok = mbar_wait_warp(smem_u32(&bar_kv_full), ii & 1, ctl);
+      ATTN_TRACE_EV(tc, 1, ii);
+      // The item's first S^T/dP^T: once its stage has landed and the compute
+      // warps have read the previous S^T/dP^T out of their columns.
+      if (ok) ok = mbar_wait_warp(smem_u32(&bar_st_full[git % ST]), (git / ST) & 1, ctl);
+      if (ok && git > 0) ok = mbar_wait_warp(smem_u32(&bar_sdp_free), (git - 1) & 1, ctl);
+      if (!ok) break;
+      tc_fence_after();
+      issue_sdp(git % ST);
       for (int it = 0; it < n_it && ok; ++it) {  // ok is warp-uniform
-        const int s = it % ST;
+        const int gi = git + it;
+        const int s = gi % ST;
         if (it + 1 < n_it) {
-          const int s1 = (it + 1) % ST;
-          ATTN_TRACE_EV(tc, 7, it + 1);  // start waiting for stage / sdp_free
-          ok = mbar_wait_warp(smem_u32(&bar_st_full[s1]), ((it + 1) / ST) & 1, ctl);
-          ATTN_TRACE_EV(tc, 10, it + 1);  // stage landed
-          if (ok) ok = mbar_wait_warp(smem_u32(&bar_sdp_free), it & 1, ctl);
+          const int s1 = (gi + 1) % ST;
+          ATTN_TRACE_EV(tc, 7, gi + 1);  // start waiting for stage / sdp_free
+          ok = mbar_wait_warp(smem_u32(&bar_st_full[s1]), ((gi + 1) / ST) & 1, ctl);
+          ATTN_TRACE_EV(tc, 10, gi + 1);  // stage landed
+          if (ok) ok = mbar_wait_warp(smem_u32(&bar_sdp_free), gi & 1, ctl);
           if (!ok) break;
           tc_fence_after();
           issue_sdp(s1);
-          ATTN_TRACE_EV(tc, 3, it + 1);  // S^T, dP^T issued
+          ATTN_TRACE_EV(tc, 3, gi + 1);  // S^T, dP^T issued
         }
-        ATTN_TRACE_EV(tc, 8, it);  // start waiting for P, dS
-        ok = mbar_wait_warp(smem_u32(&bar_pds_full), it & 1, ctl);
+        ATTN_TRACE_EV(tc, 8, gi);  // start waiting for P, dS
+        ok = mbar_wait_warp(smem_u32(&bar_pds_full), gi & 1, ctl);
+        // The item's first dV/dK products overwrite the accumulators: the
+        // compute warps must have read the previous item's dK/dV out.
+        if (ok && it == 0 && ii > 0) ok = mbar_wait_warp(smem_u32(&bar_dkv_free), (ii - 1) & 1, ctl);
         if (!ok) break;
-        ATTN_TRACE_EV(tc, 4, it);  // P, dS ready seen
+        ATTN_TRACE_EV(tc, 4, gi);  // P, dS ready seen
         tc_fence_after();
         const uint64_t dq_mn = sw128_desc(stage_q(s), BQ * 128, 1024);
         const uint64_t ddo_mn = sw128_desc(stage_do(s), BQ * 128, 1024);
@@ -402,19 +469,19 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         }
         // Q_i and dO_i are not read again: hand the stage back to the producer.
         mma_commit_el(smem_u32(&bar_st_empty[s]));
-        ATTN_TRACE_EV(tc, 5, it);  // dV, dK issued
+        ATTN_TRACE_EV(tc, 5, gi);  // dV, dK issued
         if constexpr (!C::DQ_IN_COMPUTE) {
-          if (it >= 1) {
-            ok = mbar_wait_warp(smem_u32(&bar_dq_free), (it - 1) & 1, ctl);
+          if (gi >= 1) {
+            ok = mbar_wait_warp(smem_u32(&bar_dq_free), (gi - 1) & 1, ctl);
             if (!ok) break;
             tc_fence_after();
           }
         }
-        ATTN_TRACE_EV(tc, 9, it);  // issuing dQ
+        ATTN_TRACE_EV(tc, 9, gi);  // issuing dQ
         // dQ^T[d][q] (+ 64 columns for the lo part) = sum over keys of
         // K[key][d] [dS_hi^T | dS_lo^T][key][q]. It overwrites P^T and dS^T,
-        // which dV(it) and dK(it) above have read (MMAs run in issue order).
-        // dQ^T(it-1) has been read out of these columns before P/dS(it) were
+        // which dV(gi) and dK(gi) above have read (MMAs run in issue order).
+        // dQ^T(gi-1) has been read out of these columns before P/dS(gi) were
         // stored (pds_full above) or, with drain warps, before dq_free.
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk)
@@ -422,20 +489,24 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
                     kk > 0);
         if constexpr (!C::DQ_IN_COMPUTE) mma_commit_el(smem_u32(&bar_dq_full));
         mma_commit_el(smem_u32(&bar_pds_free));
-        ATTN_TRACE_EV(tc, 6, it);  // dQ issued
+        ATTN_TRACE_EV(tc, 6, gi);  // dQ issued
       }
+      if (!ok) break;
+      // The item's last products are issued: K and V may be replaced, and
+      // dK/dV are complete once these run.
+      mma_commit_el(smem_u32(&bar_kv_free));
       mma_commit_el(smem_u32(&bar_mma_done));
-      // Every MMA issued finishes before TMEM is released.
-      mbar_wait_drain(smem_u32(&bar_mma_done), 0, 50000000ull);
+      git += n_it;
     }
+    mma_commit_el(smem_u32(&bar_fin));
+    // Every MMA issued finishes before TMEM is released.
+    mbar_wait_drain(smem_u32(&bar_fin), 0, 50000000ull);
     __syncwarp();
   } else if (warp < 8) {
     // ------------------------------------------------------------ P^T / dS^T warps 0-7
     const int r = threadIdx.x % 128;  // key row within the tile == TMEM lane
     const int cg = warp / 4;          // query-column half
-    const int key = k0 + r;
     const uint32_t lane_base = static_cast<uint32_t>((warp % 4) * 32) << 16;
-    const bool key_valid = key < p.S;
     bool ok = true;
     TraceCursor tc;
     if (lane == 0) ATTN_TRACE_INIT(tc, 2 + warp);
@@ -452,11 +523,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 #pragma unroll
       for (int i = 0; i < HALF; ++i) v[i] = add ? v[i] + __uint_as_float(a[i]) : __uint_as_float(a[i]);
     };
-    // Hand dQ(itq)'s rows cg*32.. (this half) to the reduction warp through
+    // Hand dQ(gq)'s rows cg*32.. (this half) to the reduction warp through
     // this half's staging tile [32 q][D] fp32, once the reduction has read
     // the half's previous tile out of it.
-    auto stage_dq = [&](int itq, const float (&v)[HALF]) {
-      if (itq >= 1 && !mbar_wait_warp(smem_u32(&bar_stg_free[cg]), (itq - 1) & 1, ctl))
+    auto stage_dq = [&](int gq, const float (&v)[HALF]) {
+      if (gq >= 1 && !mbar_wait_warp(smem_u32(&bar_stg_free[cg]), (gq - 1) & 1, ctl))
         return false;
       if (r < D) {
 #pragma unroll
@@ -466,144 +537,161 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       mbar_arrive(smem_u32(&bar_stg_full[cg]));
       return true;
     };
-    for (int it = 0; it < n_it; ++it) {
-      const int s = it % ST;
-      const int q0 = (i_start + it % niq) * BQ;
-      ATTN_TRACE_EV(tc, 1, it);
-      ok = mbar_wait_warp(smem_u32(&bar_sdp_full), it & 1, ctl);
-      if (ok) ok = mbar_wait_warp(smem_u32(&bar_st_full[s]), (it / ST) & 1, ctl);
-      if (!ok) break;
-      tc_fence_after();
-      // This warpgroup's query columns of -LSE*log2(e) and Dvec, four at a time.
-      const float4* nl4 = reinterpret_cast<const float4*>(stage_rows(s) + cg * HALF);
-      const float4* dv4 = reinterpret_cast<const float4*>(stage_rows(s) + BQ + cg * HALF);
-      // Only tiles that cross the causal diagonal, hold keys past S, or hold
-      // keys below some row's window mask.
-      const bool need_mask = (p.causal && (q0 < k0 + BK - 1)) || (k0 + BK > p.S) ||
-                             (WIN && k0 <= q0 + BQ - 1 - p.window);
-      uint32_t us[HALF], ud[HALF];
-      tmem_ld32(tmem + lane_base + C::TM_ST + cg * HALF, us);
-      tmem_ld32(tmem + lane_base + C::TM_DPT + cg * HALF, ud);
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(smem_u32(&bar_sdp_free));
-      ATTN_TRACE_EV(tc, 2, it);  // S^T, dP^T loaded
-      // bf16 pairs of this half's 32 query columns: P hi then P lo, dS hi then dS lo.
-      uint32_t pp[HALF], dd[HALF];
-      // P = exp2(S * scale*log2(e) - LSE*log2(e)); dS = scale * P * (dP - Dvec),
-      // two query columns per packed instruction.
-      const uint64_t sl2 = f32x2(p.scale_log2, p.scale_log2);
-      const uint64_t sc2 = f32x2(p.scale, p.scale);
-      // Key position relative to this half's first query row, and the first
-      // query column past the key's window (no window: never).
-      const int rel = key - (q0 + cg * HALF);
-      const int relw = WIN ? rel + p.window : (1 << 30);
-      auto p_ds = [&](auto masked) {
+    int git = 0;
+    for (int ii = 0; ii < n_items && ok; ++ii) {
+      const BwdItem t = item_at(ii);
+      const int key = t.k0 + r;
+      const bool key_valid = key < p.S;
+      for (int it = 0; it < t.n_it; ++it) {
+        const int gi = git + it;
+        const int s = gi % ST;
+        const int q0 = bwd_qtile(t, it) * BQ;
+        ATTN_TRACE_EV(tc, 1, gi);
+        ok = mbar_wait_warp(smem_u32(&bar_sdp_full), gi & 1, ctl);
+        if (ok) ok = mbar_wait_warp(smem_u32(&bar_st_full[s]), (gi / ST) & 1, ctl);
+        if (!ok) break;
+        tc_fence_after();
+        // This warpgroup's query columns of -LSE*log2(e) and Dvec, four at a time.
+        const float4* nl4 = reinterpret_cast<const float4*>(stage_rows(s) + cg * HALF);
+        const float4* dv4 = reinterpret_cast<const float4*>(stage_rows(s) + BQ + cg * HALF);
+        // Only tiles that cross the causal diagonal, hold keys past S, or hold
+        // keys below some row's window mask.
+        const bool need_mask = (p.causal && (q0 < t.k0 + BK - 1)) || (t.k0 + BK > p.S) ||
+                               (WIN && t.k0 <= q0 + BQ - 1 - p.window);
+        uint32_t us[HALF], ud[HALF];
+        tmem_ld32(tmem + lane_base + C::TM_ST + cg * HALF, us);
+        tmem_ld32(tmem + lane_base + C::TM_DPT + cg * HALF, ud);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bar_sdp_free));
+        ATTN_TRACE_EV(tc, 2, gi);  // S^T, dP^T loaded
+        // bf16 pairs of this half's 32 query columns: P hi then P lo, dS hi then dS lo.
+        uint32_t pp[HALF], dd[HALF];
+        // P = exp2(S * scale*log2(e) - LSE*log2(e)); dS = scale * P * (dP - Dvec),
+        // two query columns per packed instruction.
+        const uint64_t sl2 = f32x2(p.scale_log2, p.scale_log2);
+        const uint64_t sc2 = f32x2(p.scale, p.scale);
+        // Key position relative to this half's first query row, and the first
+        // query column past the key's window (no window: never).
+        const int rel = key - (q0 + cg * HALF);
+        const int relw = WIN ? rel + p.window : (1 << 30);
+        auto p_ds = [&](auto masked) {
 #pragma unroll
-        for (int c = 0; c < HALF; c += 4) {
-          const float4 nl = nl4[c / 4];
-          const float4 dv = dv4[c / 4];
+          for (int c = 0; c < HALF; c += 4) {
+            const float4 nl = nl4[c / 4];
+            const float4 dv = dv4[c / 4];
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int cc = c + 2 * h;  // columns cc, cc + 1 of this half
-            float x0, x1;
-            unpack_f32x2(fma_f32x2(f32x2(__uint_as_float(us[cc]), __uint_as_float(us[cc + 1])), sl2,
-                                   h ? f32x2(nl.z, nl.w) : f32x2(nl.x, nl.y)),
-                         x0, x1);
-            float p0 = ex2(x0), p1 = ex2(x1);
-            if (decltype(masked)::value) {
-              // Query column cc of this half sees the key iff rel <= cc
-              // (causal) and cc < rel + W (window); rel, relw below.
-              if (!key_valid || (p.causal && cc < rel) || cc >= relw) p0 = 0.f;
-              if (!key_valid || (p.causal && cc + 1 < rel) || cc + 1 >= relw) p1 = 0.f;
+            for (int h = 0; h < 2; ++h) {
+              const int cc = c + 2 * h;  // columns cc, cc + 1 of this half
+              float x0, x1;
+              unpack_f32x2(fma_f32x2(f32x2(__uint_as_float(us[cc]), __uint_as_float(us[cc + 1])), sl2,
+                                     h ? f32x2(nl.z, nl.w) : f32x2(nl.x, nl.y)),
+                           x0, x1);
+              float p0 = ex2(x0), p1 = ex2(x1);
+              if (decltype(masked)::value) {
+                // Query column cc of this half sees the key iff rel <= cc
+                // (causal) and cc < rel + W (window); rel, relw below.
+                if (!key_valid || (p.causal && cc < rel) || cc >= relw) p0 = 0.f;
+                if (!key_valid || (p.causal && cc + 1 < rel) || cc + 1 >= relw) p1 = 0.f;
+              }
+              const uint64_t dpv = sub_f32x2(f32x2(__uint_as_float(ud[cc]), __uint_as_float(ud[cc + 1])),
+                                             h ? f32x2(dv.z, dv.w) : f32x2(dv.x, dv.y));
+              float d0, d1;
+              unpack_f32x2(mul_f32x2(mul_f32x2(f32x2(p0, p1), sc2), dpv), d0, d1);
+              split_bf16x2(p0, p1, pp[cc / 2], pp[HALF / 2 + cc / 2]);
+              split_bf16x2(d0, d1, dd[cc / 2], dd[HALF / 2 + cc / 2]);
             }
-            const uint64_t t = sub_f32x2(f32x2(__uint_as_float(ud[cc]), __uint_as_float(ud[cc + 1])),
-                                         h ? f32x2(dv.z, dv.w) : f32x2(dv.x, dv.y));
-            float d0, d1;
-            unpack_f32x2(mul_f32x2(mul_f32x2(f32x2(p0, p1), sc2), t), d0, d1);
-            split_bf16x2(p0, p1, pp[cc / 2], pp[HALF / 2 + cc / 2]);
-            split_bf16x2(d0, d1, dd[cc / 2], dd[HALF / 2 + cc / 2]);
+          }
+        };
+        if (need_mask)
+          p_ds(BoolConst<true>{});
+        else
+          p_ds(BoolConst<false>{});
+        ATTN_TRACE_EV(tc, 3, gi);  // P, dS computed
+        // pds_free(gi-1): the MMAs of iteration gi-1 are done, so dS^T in
+        // shared memory is free and dQ^T(gi-1) is complete in TMEM. With
+        // D = 64 this thread reads its part of dQ^T(gi-1) (lane = head dim d,
+        // this half's query columns) before storing P/dS(gi) over those same
+        // TMEM cells; the item's last dQ^T is read after its loop.
+        float dqv[HALF];
+        if (gi >= 1) {
+          ok = mbar_wait_warp(smem_u32(&bar_pds_free), (gi - 1) & 1, ctl);
+          if (!ok) break;
+        }
+        // Row r of dS^T, K-major with 128-byte swizzle: 64 query columns per
+        // 128-byte row, 8 per 16-byte unit; this half owns units cg*4..cg*4+3.
+#pragma unroll
+        for (int u = 0; u < HALF / 8; ++u) {
+          const int unit = cg * (HALF / 8) + u;
+          const uint32_t* h = dd + u * 4;
+          const uint32_t* lo = dd + HALF / 2 + u * 4;
+          st_sw128(sDsHi, r, unit, make_uint4(h[0], h[1], h[2], h[3]));
+          st_sw128(sDsLo, r, unit, make_uint4(lo[0], lo[1], lo[2], lo[3]));
+        }
+        ATTN_TRACE_EV(tc, 4, gi);  // previous MMAs done
+        if constexpr (!C::DQ_IN_COMPUTE) {
+          // The drain warps hand back the dQ^T(gi-1) columns.
+          if (gi >= 1) {
+            ok = mbar_wait_warp(smem_u32(&bar_dq_free), (gi - 1) & 1, ctl);
+            if (!ok) break;
           }
         }
-      };
-      if (need_mask)
-        p_ds(BoolConst<true>{});
-      else
-        p_ds(BoolConst<false>{});
-      ATTN_TRACE_EV(tc, 3, it);  // P, dS computed
-      // pds_free(it-1): the MMAs of tile it-1 are done, so dS^T in shared
-      // memory is free and dQ^T(it-1) is complete in TMEM. This thread reads
-      // its part of dQ^T(it-1) (lane = head dim d, this half's query columns)
-      // before storing P/dS(it) over those same TMEM cells.
-      float dqv[HALF];
-      if (it >= 1) {
-        ok = mbar_wait_warp(smem_u32(&bar_pds_free), (it - 1) & 1, ctl);
-        if (!ok) break;
-      }
-      // Row r of dS^T, K-major with 128-byte swizzle: 64 query columns per
-      // 128-byte row, 8 per 16-byte unit; this half owns units cg*4..cg*4+3.
-#pragma unroll
-      for (int u = 0; u < HALF / 8; ++u) {
-        const int unit = cg * (HALF / 8) + u;
-        const uint32_t* h = dd + u * 4;
-        const uint32_t* lo = dd + HALF / 2 + u * 4;
-        st_sw128(sDsHi, r, unit, make_uint4(h[0], h[1], h[2], h[3]));
-        st_sw128(sDsLo, r, unit, make_uint4(lo[0], lo[1], lo[2], lo[3]));
-      }
-      ATTN_TRACE_EV(tc, 4, it);  // previous MMAs done
-      if constexpr (!C::DQ_IN_COMPUTE) {
-        // The drain warps hand back the dQ^T(it-1) columns.
-        if (it >= 1) {
-          ok = mbar_wait_warp(smem_u32(&bar_dq_free), (it - 1) & 1, ctl);
+        tc_fence_after();
+        if (C::DQ_IN_COMPUTE && it >= 1) read_dq_part(0, dqv, false);
+        tmem_st32(tmem + lane_base + C::TM_P + cg * HALF, pp);
+        if (C::DQ_IN_COMPUTE && it >= 1) read_dq_part(1, dqv, true);
+        tmem_st32(tmem + lane_base + C::TM_DS + cg * HALF, dd);
+        tmem_wait_st();
+        fence_async_smem();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bar_pds_full));
+        ATTN_TRACE_EV(tc, 5, gi);  // P, dS stored and signalled
+        if (C::DQ_IN_COMPUTE && it >= 1) {
+          ok = stage_dq(gi - 1, dqv);
           if (!ok) break;
         }
       }
-      tc_fence_after();
-      if (C::DQ_IN_COMPUTE && it >= 1) read_dq_part(0, dqv, false);
-      tmem_st32(tmem + lane_base + C::TM_P + cg * HALF, pp);
-      if (C::DQ_IN_COMPUTE && it >= 1) read_dq_part(1, dqv, true);
-      tmem_st32(tmem + lane_base + C::TM_DS + cg * HALF, dd);
-      tmem_wait_st();
-      fence_async_smem();
-      tc_fence_before();
-      mbar_arrive(smem_u32(&bar_pds_full));
-      ATTN_TRACE_EV(tc, 5, it);  // P, dS stored and signalled
-      if (C::DQ_IN_COMPUTE && it >= 1) {
-        ok = stage_dq(it - 1, dqv);
+      if (!ok) break;
+      // The item's last dQ^T, once its MMA has run.
+      if (C::DQ_IN_COMPUTE && t.n_it > 0) {
+        const int gl = git + t.n_it - 1;
+        ok = mbar_wait_warp(smem_u32(&bar_pds_free), gl & 1, ctl);
+        if (ok) {
+          tc_fence_after();
+          float dqv[HALF];
+          read_dq_part(0, dqv, false);
+          read_dq_part(1, dqv, true);
+          ok = stage_dq(gl, dqv);
+        }
         if (!ok) break;
       }
-    }
-    // The last tile's dQ^T, once its MMA has run.
-    if (C::DQ_IN_COMPUTE && ok && n_it > 0) {
-      ok = mbar_wait_warp(smem_u32(&bar_pds_free), (n_it - 1) & 1, ctl);
-      if (ok) {
-        tc_fence_after();
-        float dqv[HALF];
-        read_dq_part(0, dqv, false);
-        read_dq_part(1, dqv, true);
-        ok = stage_dq(n_it - 1, dqv);
+      ok = mbar_wait_warp(smem_u32(&bar_mma_done), ii & 1, ctl);
+      if (!ok) break;
+      // dK and dV rows in fp32; this warpgroup stores columns [cg*D/2, (cg+1)*D/2).
+      const size_t rowoff = ((static_cast<size_t>(t.b) * p.S + key) * p.Hkv + t.g) * D;
+      {
+        // (warp-uniform outcome: the TMEM loads below are .sync.aligned)
+        const bool row_in =
+            !key_valid || bounds_ok(rowoff + D <= static_cast<size_t>(p.B) * p.S * p.Hkv * D, ctl);
+        if (!__all_sync(0xffffffffu, row_in)) ok = false;
       }
-    }
-    if (ok) ok = mbar_wait_warp(smem_u32(&bar_mma_done), 0, ctl);
-    // dK and dV rows in fp32; this warpgroup stores columns [cg*D/2, (cg+1)*D/2).
-    const size_t rowoff = ((static_cast<size_t>(b) * p.S + key) * p.Hkv + g) * D;
-    {
-      // (warp-uniform outcome: the TMEM loads below are .sync.aligned)
-      const bool row_in =
-          !key_valid || bounds_ok(rowoff + D <= static_cast<size_t>(p.B) * p.S * p.Hkv * D, ctl);
-      if (!__all_sync(0xffffffffu, row_in)) ok = false;
-    }
-    if (ok) {
+      if (!ok) break;
       tc_fence_after();
 #pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        const uint32_t col0 = (t == 0 ? C::TM_DK : C::TM_DV) + cg * (D / 2);
-        float* dst = (t == 0 ? p.dk : p.dv) + rowoff + cg * (D / 2);
+      for (int tt = 0; tt < 2; ++tt) {
+        const uint32_t col0 = (tt == 0 ? C::TM_DK : C::TM_DV) + cg * (D / 2);
+        float* dst = (tt == 0 ? p.dk : p.dv) + rowoff + cg * (D / 2);
 #pragma unroll
         for (int c = 0; c < D / 2; c += 32) {
           uint32_t u[32];
           tmem_ld32(tmem + lane_base + col0 + c, u);
           tmem_wait_ld();
+          if (tt == 1 && c + 32 >= D / 2) {
+            // The last read of this thread's dK/dV cells: the next item's
+            // first dV/dK products may overwrite them.
+            tc_fence_before();
+            mbar_arrive(smem_u32(&bar_dkv_free));
+          }
           if (key_valid) {
             if (p.split > 1) {
               // Two CTAs add their head halves into the zeroed row: two
@@ -622,12 +710,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           }
         }
       }
+      git += t.n_it;
     }
 #ifdef ATTN_TRACE
   } else if (warp == C::W_MMA + 1) {
     // ------------------------------------------------------------ trace observer
     // Timestamps the completion of S^T/dP^T (1), dV/dK (2) and dQ^T (3) of
-    // every tile by polling their barriers without blocking.
+    // every iteration by polling their barriers without blocking.
     TraceCursor tc;
     if (lane == 0) ATTN_TRACE_INIT(tc, 14);
     auto done = [](uint32_t bar, uint32_t parity) {
@@ -640,12 +729,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           : "memory");
       return ok != 0;
     };
+    int total = 0;
+    for (int ii = 0; ii < n_items; ++ii) total += item_at(ii).n_it;
     int i1 = 0, i2 = 0, i3 = 0;
     const uint64_t t0 = globaltimer();
-    while (i1 < n_it || i2 < n_it || i3 < n_it) {
-      if (i1 < n_it && done(smem_u32(&bar_sdp_full), i1 & 1)) ATTN_TRACE_EV(tc, 1, i1++);
-      if (i2 < n_it && done(smem_u32(&bar_st_empty[i2 % ST]), (i2 / ST) & 1)) ATTN_TRACE_EV(tc, 2, i2++);
-      if (i3 < n_it && done(smem_u32(&bar_pds_free), i3 & 1)) ATTN_TRACE_EV(tc, 3, i3++);
+    while (i1 < total || i2 < total || i3 < total) {
+      if (i1 < total && done(smem_u32(&bar_sdp_full), i1 & 1)) ATTN_TRACE_EV(tc, 1, i1++);
+      if (i2 < total && done(smem_u32(&bar_st_empty[i2 % ST]), (i2 / ST) & 1)) ATTN_TRACE_EV(tc, 2, i2++);
+      if (i3 < total && done(smem_u32(&bar_pds_free), i3 & 1)) ATTN_TRACE_EV(tc, 3, i3++);
       if (abort_flag || globaltimer() - t0 > 2000000000ull) break;
     }
 #endif
@@ -656,76 +747,88 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     bool ok = true;
     TraceCursor tc;
     if (lane == 0) ATTN_TRACE_INIT(tc, 10);
-    // Half 0 of each tile, then half 1; each half's staging tile cycles
-    // through its own pair of barriers.
-    for (int n = 0; n < 2 * n_it && ok; ++n) {
-      const int itq = n >> 1, half = n & 1;
-      ok = mbar_wait_warp(smem_u32(&bar_stg_full[half]), itq & 1, ctl);
-      if (!ok) break;
-      ATTN_TRACE_EV(tc, 1, n);  // half staged
-      if (lane == 0) {
-        const int h = h0 + itq / niq;
-        const int q0 = (i_start + itq % niq) * BQ;
-        if (bounds_ok(h < p.Hq && q0 + (half + 1) * C::DQ_ROWS <= p.S_pad, ctl))
-          tma_reduce_add_4d(&tm_dq, 0, h, q0 + half * C::DQ_ROWS, b, sDQS + half * C::DQS_BYTES);
-        bulk_commit_group();
-        bulk_wait_read_all();
-        mbar_arrive(smem_u32(&bar_stg_free[half]));
+    int git = 0;
+    for (int ii = 0; ii < n_items && ok; ++ii) {
+      const BwdItem t = item_at(ii);
+      // Half 0 of each tile, then half 1; each half's staging tile cycles
+      // through its own pair of barriers.
+      for (int n = 0; n < 2 * t.n_it && ok; ++n) {
+        const int it = n >> 1, half = n & 1;
+        const int gq = git + it;
+        ok = mbar_wait_warp(smem_u32(&bar_stg_full[half]), gq & 1, ctl);
+        if (!ok) break;
+        ATTN_TRACE_EV(tc, 1, 2 * gq + half);  // half staged
+        if (lane == 0) {
+          const int h = bwd_head(t, it);
+          const int q0 = bwd_qtile(t, it) * BQ;
+          if (bounds_ok(h < p.Hq && q0 + (half + 1) * C::DQ_ROWS <= p.S_pad, ctl))
+            tma_reduce_add_4d(&tm_dq, 0, h, q0 + half * C::DQ_ROWS, t.b, sDQS + half * C::DQS_BYTES);
+          bulk_commit_group();
+          bulk_wait_read_all();
+          mbar_arrive(smem_u32(&bar_stg_free[half]));
+        }
+        __syncwarp();
       }
-      __syncwarp();
+      git += t.n_it;
     }
     if (lane == 0) bulk_wait_all();
     __syncwarp();
   } else {
     // ------------------------------------------------------------ dQ drain warps 8-11
-    const int t = threadIdx.x - 256;  // TMEM lane = head-dim index d of dQ^T
+    const int tid = threadIdx.x - 256;  // TMEM lane = head-dim index d of dQ^T
     const uint32_t lane_base = static_cast<uint32_t>((warp % 4) * 32) << 16;
     bool ok = true;
     TraceCursor tc;
     if (lane == 0) ATTN_TRACE_INIT(tc, 10 + (warp - 8));
-    for (int it = 0; it < n_it; ++it) {
-      const int h = h0 + it / niq;
-      const int q0 = (i_start + it % niq) * BQ;
-      ok = mbar_wait_warp(smem_u32(&bar_dq_full), it & 1, ctl);
-      // The four drain warps meet at bar.sync below: agree first on going on.
-      ok = named_bar_and(1, 128, ok);
-      if (!ok) break;
-      ATTN_TRACE_EV(tc, 1, it);  // dQ landed
-      tc_fence_after();
-      // dQ^T = hi part (columns 0..63) + lo part (64..127).
-      float u[BQ];
+    int git = 0;
+    for (int ii = 0; ii < n_items && ok; ++ii) {
+      const BwdItem t = item_at(ii);
+      for (int it = 0; it < t.n_it; ++it) {
+        const int gi = git + it;
+        const int h = bwd_head(t, it);
+        const int q0 = bwd_qtile(t, it) * BQ;
+        ok = mbar_wait_warp(smem_u32(&bar_dq_full), gi & 1, ctl);
+        // The four drain warps meet at bar.sync below: agree first on going on.
+        ok = named_bar_and(1, 128, ok);
+        if (!ok) break;
+        ATTN_TRACE_EV(tc, 1, gi);  // dQ landed
+        tc_fence_after();
+        // dQ^T = hi part (columns 0..63) + lo part (64..127).
+        float u[BQ];
 #pragma unroll
-      for (int c = 0; c < BQ; c += 32) {
-        uint32_t a[32], bl[32];
-        tmem_ld32(tmem + lane_base + C::TM_DQ + c, a);
-        tmem_ld32(tmem + lane_base + C::TM_DQ + BQ + c, bl);
-        tmem_wait_ld();
+        for (int c = 0; c < BQ; c += 32) {
+          uint32_t a[32], bl[32];
+          tmem_ld32(tmem + lane_base + C::TM_DQ + c, a);
+          tmem_ld32(tmem + lane_base + C::TM_DQ + BQ + c, bl);
+          tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) u[c + i] = __uint_as_float(a[i]) + __uint_as_float(bl[i]);
-      }
-      tc_fence_before();
-      mbar_arrive(smem_u32(&bar_dq_free));
-      ATTN_TRACE_EV(tc, 3, it);  // dQ^T read, TMEM handed back
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        if (t == 0) bulk_wait_read_all();  // the previous reduction has read the staging tile
-        named_bar_sync(1, 128);
-        float* stg = reinterpret_cast<float*>(smem + C::SMEM_DQS);
-        if (t < D) {
-          // staging [32 q][D] fp32, row-major (the TMA box layout); lane t holds column d = t.
-#pragma unroll
-          for (int q = 0; q < C::DQ_ROWS; ++q) stg[q * D + t] = u[half * C::DQ_ROWS + q];
+          for (int i = 0; i < 32; ++i) u[c + i] = __uint_as_float(a[i]) + __uint_as_float(bl[i]);
         }
-        fence_async_smem();
-        named_bar_sync(1, 128);
-        if (t == 0 && bounds_ok(h < p.Hq && q0 + (half + 1) * C::DQ_ROWS <= p.S_pad, ctl)) {
-          tma_reduce_add_4d(&tm_dq, 0, h, q0 + half * C::DQ_ROWS, b, sDQS);
-          bulk_commit_group();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bar_dq_free));
+        ATTN_TRACE_EV(tc, 3, gi);  // dQ^T read, TMEM handed back
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          if (tid == 0) bulk_wait_read_all();  // the previous reduction has read the staging tile
+          named_bar_sync(1, 128);
+          float* stg = reinterpret_cast<float*>(smem + C::SMEM_DQS);
+          if (tid < D) {
+            // staging [32 q][D] fp32, row-major (the TMA box layout); lane tid holds column d = tid.
+#pragma unroll
+            for (int q = 0; q < C::DQ_ROWS; ++q) stg[q * D + tid] = u[half * C::DQ_ROWS + q];
+          }
+          fence_async_smem();
+          named_bar_sync(1, 128);
+          if (tid == 0 && bounds_ok(h < p.Hq && q0 + (half + 1) * C::DQ_ROWS <= p.S_pad, ctl)) {
+            tma_reduce_add_4d(&tm_dq, 0, h, q0 + half * C::DQ_ROWS, t.b, sDQS);
+            bulk_commit_group();
+          }
         }
+        ATTN_TRACE_EV(tc, 2, gi);  // both halves handed to the reduction
       }
-      ATTN_TRACE_EV(tc, 2, it);  // both halves handed to the reduction
+      git += t.n_it;
     }
-    if (t == 0) bulk_wait_all();
+    if (tid == 0) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -737,13 +840,110 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     if (lin < kSpanCtas) {
       unsigned smid;
       asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+      int total = 0;
+      for (int ii = 0; ii < n_items; ++ii) total += item_at(ii).n_it;
       g_attn_spans[4 * lin] = t_entry;
       g_attn_spans[4 * lin + 1] = globaltimer();
       g_attn_spans[4 * lin + 2] = smid;
-      g_attn_spans[4 * lin + 3] = n_it;
+      g_attn_spans[4 * lin + 3] = total;
     }
   }
 #endif
+}
+
+// The grid launch's head split (CTAs per key tile, 1 or 2): 2 splits the
+// group's query heads in halves, so the longest key tiles, which the grid
+// starts first but which end last, take half as long. It pays only where that
+// tail is a large part of the run and the extra prologue/epilogue per key
+// tile and the zeroing of dk/dv are small against a CTA's work: measured
+// (same-box A/B, causal, D = 128) 3-5% faster at B = 1, Hq = 64, Hkv = 8,
+// S = 8192 (512 CTAs unsplit, 1024 iterations in the longest); 0-1% slower at
+// B = 2, Hq = 32, S = 4096 (256 iterations), and 1-3% slower at S = 16384 and
+// 32768 (1024 and 2048 CTAs). Hence: an even group, at least 512 (head,
+// query tile) iterations in the longest CTA, and at most four waves.
+int bwd_grid_split(const BwdParams& p, int bq, int sms) {
+  const int nq = (p.S + bq - 1) / bq;
+  const int niq0 = p.window > 0 ? std::min(nq, (128 + p.window - 2) / bq + 1) : nq;
+  const long long ctas = static_cast<long long>(p.B) * p.Hkv * p.n_ktiles;
+  return (p.G % 2 == 0 && p.G * niq0 >= 512 && ctas <= 4LL * sms) ? 2 : 1;
+}
+
+// Launch plan of the backward main kernel for one problem shape.
+struct BwdPlan {
+  bool persist = false;
+  int split = 1;
+  BwdSchedArg<true> sched{};
+};
+
+// Items of at most this many iterations on average run on a persistent grid:
+// a CTA's own prologue and epilogue (about 9 us at D = 128 against 1.8 us per
+// iteration) then outweigh what a grid launch's dynamic dispatch gives.
+// Measured (same-box A/B): persistent 7% faster at D = 64, B = 8, H = 16,
+// S = 2048 (16 iterations per item) and 6% faster with a 128-key window at
+// D = 128 (32 per item); 4-12% slower at the Llama-3-8B, 70B and S = 32768
+// shapes (132 to 1028 per item), where the hardware's dispatch of the next
+// CTA to whichever SM is free adapts to SMs that run slower, which a static
+// list cannot, and keeps the running CTAs on neighbouring key tiles.
+constexpr int kBwdPersistMaxMeanIters = 64;
+
+// The plan for the shape of p on `sms` SMs. The persistent schedule is the
+// list schedule of the items in the grid's order (key tiles longest first),
+// each item weighted by its iterations plus two for its prologue/epilogue:
+// item by item to the CTA with the least work so far.
+template <bool WIN>
+std::shared_ptr<const BwdPlan> bwd_plan(const BwdParams& p, int bq, int bk, int sms) {
+  static std::mutex mu;
+  static std::map<std::vector<long long>, std::shared_ptr<const BwdPlan>> cache;
+  const std::vector<long long> key = {p.B, p.Hkv, p.G, p.S, p.causal, p.window, bq, bk, sms};
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto f = cache.find(key);
+    if (f != cache.end()) return f->second;
+  }
+  auto plan = std::make_shared<BwdPlan>();
+  BwdParams q = p;
+  q.split = 1;
+  const long long n = static_cast<long long>(p.B) * p.Hkv * p.n_ktiles;
+  long long total = 0;
+  for (int code = 0; code < n && n <= kBwdSchedMaxItems; ++code) total += bwd_item<WIN>(q, code, bq, bk).n_it;
+  plan->persist = sms > 0 && sms <= kBwdSchedMaxCtas && n <= kBwdSchedMaxItems &&
+                  total <= static_cast<long long>(kBwdPersistMaxMeanIters) * n;
+  if (plan->persist) {
+    std::vector<long long> load(sms, 0);
+    std::vector<std::vector<int>> bins(sms);
+    for (int code = 0; code < n; ++code) {
+      const int b = static_cast<int>(std::min_element(load.begin(), load.end()) - load.begin());
+      load[b] += bwd_item<WIN>(q, code, bq, bk).n_it + 2;
+      bins[b].push_back(code);
+    }
+    int c = 0, e = 0;
+    for (const auto& bin : bins) {
+      if (bin.empty()) continue;
+      plan->sched.off[c++] = static_cast<uint16_t>(e);
+      for (int code : bin) plan->sched.code[e++] = static_cast<uint16_t>(code);
+    }
+    plan->sched.off[c] = static_cast<uint16_t>(e);
+    plan->sched.n_ctas = c;
+  } else {
+    plan->split = bwd_grid_split(p, bq, sms);
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache.size() >= 64) cache.clear();
+  cache[key] = plan;
+  return plan;
+}
+
+template <int D, bool WIN, bool PERSIST>
+cudaError_t set_bwd_smem(int dev) {
+  static bool attr_set[64] = {};
+  if (dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(attn_bwd_main_kernel<D, WIN, PERSIST>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         BwdCfg<D>::SMEM_ALLOC);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  return cudaSuccess;
 }
 
 template <int D, bool WIN>
@@ -751,27 +951,29 @@ cudaError_t launch_bwd_main_t(const CUtensorMap& tq, const CUtensorMap& tk, cons
                               const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p,
                               cudaStream_t stream) {
   using C = BwdCfg<D>;
-  static bool attr_set[64] = {};
-  int dev = 0;
+  int dev = 0, sms = 148;
   cudaGetDevice(&dev);
-  if (dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(attn_bwd_main_kernel<D, WIN>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::SMEM_ALLOC);
-    if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
-  }
-  int sms = 148;
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const std::shared_ptr<const BwdPlan> plan = bwd_plan<WIN>(p, C::BQ, C::BK, sms);
   BwdParams pp = p;
-  pp.split = bwd_split(p, C::BQ, sms);
+  pp.split = plan->split;
+  if (plan->persist) {
+    cudaError_t e = set_bwd_smem<D, WIN, true>(dev);
+    if (e != cudaSuccess) return e;
+    attn_bwd_main_kernel<D, WIN, true><<<plan->sched.n_ctas, C::THREADS, C::SMEM_ALLOC, stream>>>(
+        tq, tk, tv, tdo, tdq, pp, plan->sched);
+    return cudaGetLastError();
+  }
+  cudaError_t e = set_bwd_smem<D, WIN, false>(dev);
+  if (e != cudaSuccess) return e;
   if (pp.split > 1) {
     const long long n4 = static_cast<long long>(p.B) * p.S * p.Hkv * D / 4;
     zero_f32x4_kernel<<<4 * sms, 256, 0, stream>>>(reinterpret_cast<float4*>(p.dk),
                                                    reinterpret_cast<float4*>(p.dv), n4);
   }
-  dim3 grid(p.B * p.Hkv * pp.split, p.n_ktiles);
-  attn_bwd_main_kernel<D, WIN><<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(tq, tk, tv, tdo, tdq, pp);
+  const dim3 grid(p.B * p.Hkv * pp.split, p.n_ktiles);
+  attn_bwd_main_kernel<D, WIN, false>
+      <<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(tq, tk, tv, tdo, tdq, pp, BwdSchedArg<false>{});
   return cudaGetLastError();
 }
 

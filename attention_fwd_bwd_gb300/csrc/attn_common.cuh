@@ -223,6 +223,24 @@ struct BwdCfg {
   static_assert(SMEM_ALLOC <= 232448, "shared-memory plan exceeds 227 KB");
 };
 
+// Schedule of the persistent backward main kernel (a kernel parameter): CTA
+// c runs the items code[off[c]] .. code[off[c+1] - 1] in order.
+constexpr int kBwdSchedMaxCtas = 256;
+constexpr int kBwdSchedMaxItems = 4096;
+struct BwdSched {
+  int n_ctas;
+  uint16_t off[kBwdSchedMaxCtas + 1];
+  uint16_t code[kBwdSchedMaxItems];
+};
+// The kernel's schedule argument: the schedule for a persistent launch, an
+// empty stand-in for a grid launch (one CTA per item).
+template <bool PERSIST>
+struct BwdSchedArg : BwdSched {};
+template <>
+struct BwdSchedArg<false> {
+  int n_ctas;
+};
+
 struct BwdParams {
   const float* nlse2;  // [B, Hq, S_pad] -lse * log2(e); -inf on padding rows
   const float* dvec;   // [B, Hq, S_pad] rowsum(dO * O); 0 on padding rows
@@ -234,9 +252,9 @@ struct BwdParams {
   float scale_log2;
   float scale;
   int n_ktiles;
-  // Query heads of a kv head's group are split over `split` CTAs per key tile
-  // (1 or 2), each taking G / split consecutive heads; with 2 the dK and dV
-  // rows are added into zeroed dk and dv. Set by the launcher.
+  // Query heads of a kv head's group are split over `split` items per key
+  // tile (1 or 2), each taking G / split consecutive heads; with 2 the dK and
+  // dV rows are added into zeroed dk and dv. Set by the launcher.
   int split;
   int* status;
   unsigned long long timeout_ns;
@@ -275,8 +293,9 @@ inline BwdWorkspace bwd_workspace_layout(int B, int Hq, int S) {
 
 // ---------------------------------------------------------------- tracing
 // Timeline tracing for kernel tuning, compiled in only with -DATTN_TRACE (the
-// regular build has none of it). Each traced CTA (blockIdx.x == 0, first
-// kTraceCtas values of blockIdx.y) gets kTraceRoles streams of
+// regular build has none of it). Each traced CTA (a 2-D grid: blockIdx.x ==
+// 0 and the first kTraceCtas values of blockIdx.y; a 1-D grid: the first
+// kTraceCtas blocks) gets kTraceRoles streams of
 // kTraceEvents 64-bit records: event code (bits 56..63), iteration
 // (bits 40..55) and the SM clock (bits 0..39).
 constexpr int kTraceCtas = 32;
@@ -288,8 +307,8 @@ struct TraceCursor {
   unsigned long long* base = nullptr;
   int n = 0;
   __device__ void init(unsigned long long* buf, int role) {
-    if (blockIdx.x == 0 && blockIdx.y < kTraceCtas)
-      base = buf + (static_cast<size_t>(blockIdx.y) * kTraceRoles + role) * kTraceEvents;
+    const unsigned idx = gridDim.y > 1 ? (blockIdx.x == 0 ? blockIdx.y : kTraceCtas) : blockIdx.x;
+    if (idx < kTraceCtas) base = buf + (static_cast<size_t>(idx) * kTraceRoles + role) * kTraceEvents;
   }
   __device__ void ev(int code, int it) {
     if (base && n < kTraceEvents) {

@@ -7,10 +7,11 @@ pass a wait on the wrong phase nor deadlock.
 Forward: the persistent kernel -- a producer that preloads the next item's
 first K/V tiles before waiting for the Q buffer, an MMA issuer that
 alternates two query tiles, and two softmax warpgroups -- over the items of
-causal, non-causal, ragged and sliding-window problems. Backward: one
-key-tile CTA with its three-stage Q/dO ring, in both dQ modes (the P/dS warps
-reading dQ^T and staging it for one reduction warp, as for D = 64; four drain
-warps, as for D = 128).
+causal, non-causal, ragged and sliding-window problems. Backward: the
+persistent key-tile CTA over lists of items (K/V replaced per item, the
+three-stage Q/dO ring and every other barrier running on across items), in
+both dQ modes (the P/dS warps reading dQ^T and staging it for one reduction
+warp, as for D = 64; four drain warps, as for D = 128).
 
 CPU only; no kernel code is involved.
 """
@@ -18,7 +19,7 @@ import random
 
 import pytest
 
-from tests.protocol_sim import Bar, run, wait
+from tests.protocol_sim import Aliasing, Bar, Deadlock, run, wait
 
 
 def fwd_items(S, causal, window=0):
@@ -153,78 +154,140 @@ def test_dense_forward_protocol_is_sound(S, causal, window, nslot):
         assert dense_fwd_model(items, nslot, win=window > 0, seed=seed)
 
 
-def dense_bwd_model(n_it, dq_in_compute, stages=3, seed=0, stage_last=True):
+def dense_bwd_model(items, dq_in_compute, stages=3, seed=0, stage_last=True, early_kv=False):
+    """The persistent backward main kernel over one CTA's items (n_it of
+    each): K/V replaced per item after kv_free, the item's first query stages
+    issued before that wait, per-item mma_done and dkv_free (the compute
+    warps' dK/dV read-out before the next item's first dV/dK products).
+    early_kv plants a mistake: the next item's K/V load does not wait."""
     rnd = random.Random(seed)
-    kv_full, mma_done = Bar(1), Bar(1)
+    kv_full, kv_free, mma_done, fin = Bar(1), Bar(1), Bar(1), Bar(1)
+    dkv_free = Bar(2)                         # both P/dS warp groups arrive
     st_full = [Bar(1) for _ in range(stages)]
     st_empty = [Bar(1) for _ in range(stages)]
-    sdp_full, sdp_free = Bar(1), Bar(2)      # two P/dS warp groups arrive
+    sdp_full, sdp_free = Bar(1), Bar(2)
     pds_full, pds_free = Bar(2), Bar(1)
     dq_full, dq_free = Bar(1), Bar(1)
     stg_full, stg_free = [Bar(1), Bar(1)], [Bar(1), Bar(1)]
     tma, mma = [], []
+    state = {"kv_item": -1, "mma_item_reading_kv": None}
+
+    class KvLoad:  # a K/V load landing: the buffer now holds item ii
+        def __init__(self, ii):
+            self.ii = ii
+
+        def arrive(self):
+            if state["mma_item_reading_kv"] is not None and state["mma_item_reading_kv"] != self.ii:
+                raise Aliasing(f"K/V of item {self.ii} landed under item {state['mma_item_reading_kv']}'s products")
+            state["kv_item"] = self.ii
+            kv_full.arrive()
+
+    class KvUse:  # an MMA reading K/V of item ii completes
+        def __init__(self, ii, last, bar):
+            self.ii, self.last, self.bar = ii, last, bar
+
+        def arrive(self):
+            if state["kv_item"] != self.ii:
+                raise Aliasing(f"a product of item {self.ii} read item {state['kv_item']}'s K/V")
+            if self.last:
+                state["mma_item_reading_kv"] = None
+            if self.bar is not None:
+                self.bar.arrive()
 
     def producer():
-        tma.append(kv_full)
-        for it in range(n_it):
-            s, rnd_ = it % stages, it // stages
-            if rnd_ > 0:
-                yield from wait(st_empty[s], rnd_ - 1)
-            tma.append(st_full[s])
-        for it in range(max(0, n_it - stages), n_it):
-            yield from wait(st_full[it % stages], it // stages)
-        yield from wait(kv_full, 0)
+        git, issued, kv_issued = 0, 0, 0
+        for ii, n_it in enumerate(items):
+            n_early = 0 if ii == 0 else min(stages, n_it)
+            if ii == 0:
+                tma.append(KvLoad(0))
+                kv_issued += 1
+            for it in range(n_it):
+                if ii > 0 and it == n_early:
+                    if not early_kv:
+                        yield from wait(kv_free, ii - 1)
+                    tma.append(KvLoad(ii))
+                    kv_issued += 1
+                gi = git + it
+                s, rnd_ = gi % stages, gi // stages
+                if rnd_ > 0:
+                    yield from wait(st_empty[s], rnd_ - 1)
+                tma.append(st_full[s])
+                issued = gi + 1
+            if ii > 0 and n_it <= n_early:
+                if not early_kv:
+                    yield from wait(kv_free, ii - 1)
+                tma.append(KvLoad(ii))
+                kv_issued += 1
+            git += n_it
+        for gi in range(max(0, issued - stages), issued):
+            yield from wait(st_full[gi % stages], gi // stages)
+        if kv_issued:
+            yield from wait(kv_full, kv_issued - 1)
 
     def mma_warp():
-        yield from wait(kv_full, 0)
-        if n_it > 0:
-            yield from wait(st_full[0], 0)
-            mma.append(sdp_full)
-        for it in range(n_it):
-            if it + 1 < n_it:
-                s1 = (it + 1) % stages
-                yield from wait(st_full[s1], (it + 1) // stages)
-                yield from wait(sdp_free, it)
-                mma.append(sdp_full)
-            yield from wait(pds_full, it)
-            mma.append(st_empty[it % stages])
-            if not dq_in_compute and it >= 1:
-                yield from wait(dq_free, it - 1)
-            if not dq_in_compute:
-                mma.append(dq_full)
-            mma.append(pds_free)
-        mma.append(mma_done)
-        yield from wait(mma_done, 0)
+        git = 0
+        for ii, n_it in enumerate(items):
+            yield from wait(kv_full, ii)
+            yield from wait(st_full[git % stages], git // stages)
+            if git > 0:
+                yield from wait(sdp_free, git - 1)
+            state["mma_item_reading_kv"] = ii
+            mma.append(KvUse(ii, False, sdp_full))
+            for it in range(n_it):
+                gi = git + it
+                if it + 1 < n_it:
+                    yield from wait(st_full[(gi + 1) % stages], (gi + 1) // stages)
+                    yield from wait(sdp_free, gi)
+                    mma.append(KvUse(ii, False, sdp_full))
+                yield from wait(pds_full, gi)
+                if it == 0 and ii > 0:
+                    yield from wait(dkv_free, ii - 1)
+                mma.append(st_empty[gi % stages])
+                if not dq_in_compute and gi >= 1:
+                    yield from wait(dq_free, gi - 1)
+                mma.append(KvUse(ii, it == n_it - 1, dq_full if not dq_in_compute else None))
+                mma.append(pds_free)
+            mma.append(kv_free)
+            mma.append(mma_done)
+            git += n_it
+        mma.append(fin)
+        yield from wait(fin, 0)
 
     def compute(cg):
-        def stage(itq):
-            if itq >= 1:
-                yield from wait(stg_free[cg], itq - 1)
+        def stage(gq):
+            if gq >= 1:
+                yield from wait(stg_free[cg], gq - 1)
             stg_full[cg].arrive()
-        for it in range(n_it):
-            yield from wait(sdp_full, it)
-            yield from wait(st_full[it % stages], it // stages)
-            sdp_free.arrive()
-            if it >= 1:
-                yield from wait(pds_free, it - 1)
-            if not dq_in_compute and it >= 1:
-                yield from wait(dq_free, it - 1)
-            pds_full.arrive()
-            if dq_in_compute and it >= 1:
-                yield from stage(it - 1)
-        if dq_in_compute and n_it > 0 and stage_last:
-            yield from wait(pds_free, n_it - 1)
-            yield from stage(n_it - 1)
-        yield from wait(mma_done, 0)
+        git = 0
+        for ii, n_it in enumerate(items):
+            for it in range(n_it):
+                gi = git + it
+                yield from wait(sdp_full, gi)
+                yield from wait(st_full[gi % stages], gi // stages)
+                sdp_free.arrive()
+                if gi >= 1:
+                    yield from wait(pds_free, gi - 1)
+                if not dq_in_compute and gi >= 1:
+                    yield from wait(dq_free, gi - 1)
+                pds_full.arrive()
+                if dq_in_compute and it >= 1:
+                    yield from stage(gi - 1)
+            if dq_in_compute and n_it > 0 and stage_last:
+                yield from wait(pds_free, git + n_it - 1)
+                yield from stage(git + n_it - 1)
+            yield from wait(mma_done, ii)
+            dkv_free.arrive()
+            git += n_it
 
     def reduce_warp():
-        for n in range(2 * n_it):
-            yield from wait(stg_full[n & 1], n >> 1)
-            stg_free[n & 1].arrive()
+        for gq in range(sum(items)):
+            for half in range(2):
+                yield from wait(stg_full[half], gq)
+                stg_free[half].arrive()
 
     def drain_warps():
-        for it in range(n_it):
-            yield from wait(dq_full, it)
+        for gi in range(sum(items)):
+            yield from wait(dq_full, gi)
             dq_free.arrive()
 
     agents = [producer(), mma_warp(), compute(0), compute(1)]
@@ -232,11 +295,14 @@ def dense_bwd_model(n_it, dq_in_compute, stages=3, seed=0, stage_last=True):
     return run(agents, (tma, mma, []), rnd)
 
 
-@pytest.mark.parametrize("n_it", [0, 1, 2, 3, 4, 7, 16])
+BWD_ITEM_LISTS = [[1], [2], [3], [4], [7], [16], [5, 1, 1], [1, 1, 1, 1], [2, 7, 3], [4, 4, 2, 1], [9, 3, 2, 2, 1]]
+
+
+@pytest.mark.parametrize("items", BWD_ITEM_LISTS, ids=[",".join(map(str, x)) for x in BWD_ITEM_LISTS])
 @pytest.mark.parametrize("dq_in_compute", [True, False])
-def test_dense_backward_protocol_is_sound(n_it, dq_in_compute):
+def test_dense_backward_protocol_is_sound(items, dq_in_compute):
     for seed in range(40):
-        assert dense_bwd_model(n_it, dq_in_compute, seed=seed)
+        assert dense_bwd_model(items, dq_in_compute, seed=seed)
 
 
 def test_dense_models_catch_planted_mistakes():
@@ -244,12 +310,20 @@ def test_dense_models_catch_planted_mistakes():
     the slot after an item's last V tile (which holds no K tile of this item)
     hands out a slot phase too early, and a backward whose P/dS warps never
     stage the last dQ tile leaves the reduction warp waiting."""
-    from tests.protocol_sim import Aliasing, Deadlock
     for seed in range(10):
         with pytest.raises((Aliasing, Deadlock)):
             dense_fwd_model(fwd_items(1024, True), 4, seed=seed, release_unused=True)
     with pytest.raises(Deadlock):
-        dense_bwd_model(3, True, seed=0, stage_last=False)
+        dense_bwd_model([3], True, seed=0, stage_last=False)
+    # A next item's K/V load that does not wait for kv_free lands under the
+    # previous item's products in some interleaving.
+    caught = 0
+    for seed in range(30):
+        try:
+            dense_bwd_model([4, 4], False, seed=seed, early_kv=True)
+        except (Aliasing, Deadlock):
+            caught += 1
+    assert caught > 0
 
 
 

@@ -127,7 +127,11 @@ struct SparseBwdCfg {
   // TMEM columns: S^T (then P^T, then dK_c), dP^T (then dS^T), dV_c, dQ^T.
   static constexpr int TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DQ = 384;
   static constexpr int TMEM_COLS = 512;
-  static constexpr int THREADS = 224;  // 4 compute warps, K producer, MMA issuer, V producer
+  // Warps 0-7 compute (warps w and w + 4 share TMEM lanes and split the
+  // heads, then the gradient columns), then the K producer, the MMA issuer
+  // and the V producer.
+  static constexpr int W_KPROD = 8, W_MMA = 9, W_VPROD = 10;
+  static constexpr int THREADS = 352;
   static_assert(NSLOT >= 3, "the ring needs K and V of one chunk plus one");
   static_assert(SMEM_ALLOC <= 232448, "shared-memory plan exceeds 227 KB");
 };

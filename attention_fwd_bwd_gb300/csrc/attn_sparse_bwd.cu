@@ -12,22 +12,24 @@
 //   1. preprocess: Dvec from o (+ o_lo) and dO, -LSE*log2(e) per (token, head),
 //      and zeroed dkp / dvp (HBM-bound).
 //   2. main, one persistent CTA per SM over (batch, token) items:
-//      warp 4 (K producer): the token's Q and dO rows (TMA tiles) and row
+//      warp 8 (K producer): the token's Q and dO rows (TMA tiles) and row
 //          vectors, then each chunk's K rows through the tensor engine's
 //          four-row gather, into K slots used in turn.
-//      warp 6 (V producer): each chunk's V rows through cp.async, into one V
+//      warp 10 (V producer): each chunk's V rows through cp.async, into one V
 //          slot. (Two copy paths at once, as in the forward.)
-//      warp 5 (MMA issuer), per chunk c: S^T = K_c Q^T and dP^T = V_c dO^T
+//      warp 9 (MMA issuer), per chunk c: S^T = K_c Q^T and dP^T = V_c dO^T
 //          (slot-major: TMEM lane = slot), then dV_c = P^T dO and
 //          dK_c = dS^T Q with A from TMEM, and dQ^T += K_c^T dS^T with dS^T
 //          from shared memory (dQ^T stays in TMEM over the token's chunks).
-//      warps 0-3 (thread = slot): P^T and scale * dS^T as bf16 hi/lo pairs
-//          into TMEM and (dS^T) shared memory; then the per-slot dV_c and dK_c
-//          rows are added into the pool gradients with vector fp32 reductions
-//          (red.global.add.v4.f32); after the token's last chunk, dQ^T
-//          (thread = head-dim index) is written to dq.
-// The phases of one chunk run one after another; the gathers of the next
-// chunks overlap them.
+//      warps 0-7 (thread = slot; warps w and w + 4 take one half of the heads
+//          each): P^T and scale * dS^T as bf16 hi/lo pairs into TMEM and
+//          (dS^T) shared memory; then (one half of the columns each) the
+//          per-slot dK_c and dV_c rows are added into the pool gradients with
+//          vector fp32 reductions (red.global.add.v4.f32); after the token's
+//          last chunk, dQ^T (thread = head-dim index) is written to dq.
+// A chunk's products wait for its P^T / dS^T; the next chunk's S^T and dP^T
+// start once dK_c (which sits in the S^T columns) has been read out, so they
+// run while dV_c is drained. The gathers of the next chunks overlap it all.
 #include <type_traits>
 
 #include "attn_common.cuh"
@@ -120,7 +122,7 @@ __global__ void __launch_bounds__(SparseBwdCfg<DK, DV>::THREADS, 1)
 
   __shared__ uint64_t bar_q_full, bar_q_empty, bar_mma_done;
   __shared__ uint64_t bar_kv_full[C::NSLOT], bar_kv_empty[C::NSLOT];
-  __shared__ uint64_t bar_sdp_full, bar_pds_full, bar_grads_full, bar_drain_done;
+  __shared__ uint64_t bar_sdp_full, bar_pds_full, bar_grads_full, bar_dk_drained, bar_dv_drained;
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_flag;
 
@@ -140,12 +142,13 @@ __global__ void __launch_bounds__(SparseBwdCfg<DK, DV>::THREADS, 1)
       mbar_init(smem_u32(&bar_kv_empty[i]), 1);
     }
     mbar_init(smem_u32(&bar_sdp_full), 1);
-    mbar_init(smem_u32(&bar_pds_full), 128);
+    mbar_init(smem_u32(&bar_pds_full), 256);
     mbar_init(smem_u32(&bar_grads_full), 1);
-    mbar_init(smem_u32(&bar_drain_done), 128);
+    mbar_init(smem_u32(&bar_dk_drained), 256);
+    mbar_init(smem_u32(&bar_dv_drained), 256);
     fence_barrier_init();
   }
-  if (warp == 5) {
+  if (warp == C::W_MMA) {
     tmem_alloc(smem_u32(&tmem_base_s), C::TMEM_COLS);
     tmem_relinquish();
   }
@@ -162,7 +165,7 @@ __global__ void __launch_bounds__(SparseBwdCfg<DK, DV>::THREADS, 1)
   const uint32_t sRing = smem_u32(smem + C::SMEM_RING);
   float* rows_s = reinterpret_cast<float*>(smem + C::SMEM_ROWS);  // nlse2[128], then dvec[128]
 
-  if (warp == 4) {
+  if (warp == C::W_KPROD) {
     // ------------------------------------------------------------ K producer
     if (lane == 0) {
       prefetch_tmap(&tm_q);
@@ -232,7 +235,7 @@ __global__ void __launch_bounds__(SparseBwdCfg<DK, DV>::THREADS, 1)
       if (q_loads > 0) mbar_wait_drain(smem_u32(&bar_q_full), (q_loads - 1) & 1, 50000000ull);
     }
     __syncwarp();
-  } else if (warp == 6) {
+  } else if (warp == C::W_VPROD) {
     // ------------------------------------------------------------ V producer
     // Row j's 16-byte unit u lands at j * 128 + ((u % 8) ^ (j % 8)) * 16 in
     // 64-column block u / 8 (the 128-byte swizzle the MMA descriptors expect).
@@ -276,7 +279,7 @@ __global__ void __launch_bounds__(SparseBwdCfg<DK, DV>::THREADS, 1)
     }
     cp_async_wait<0>();
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == C::W_MMA) {
     // ------------------------------------------------------------ MMA issuer
     bool ok = !p.inject_stall;
     constexpr uint32_t idesc_sdp = idesc_bf16_f32(128, 128, 0, 0);  // K-major A and B
@@ -298,9 +301,9 @@ __global__ void __launch_bounds__(SparseBwdCfg<DK, DV>::THREADS, 1)
       if (!ok) break;
       for (int c = 0; c < nch && ok; ++c, ++chunk) {
         const int sk = chunk % C::KSLOTS, sv = C::VSLOT;
-        // S^T / P^T / dK columns and dV's are free once the compute warps have
-        // drained the previous chunk.
-        if (chunk > 0) ok = mbar_wait_warp(smem_u32(&bar_drain_done), (chunk - 1) & 1, ctl);
+        // The S^T / P^T / dK columns are free once the compute warps have
+        // read the previous chunk's dK_c out of them.
+        if (chunk > 0) ok = mbar_wait_warp(smem_u32(&bar_dk_drained), (chunk - 1) & 1, ctl);
         if (ok) ok = mbar_wait_warp(smem_u32(&bar_kv_full[sk]), (chunk / C::KSLOTS) & 1, ctl);
         if (ok) ok = mbar_wait_warp(smem_u32(&bar_kv_full[sv]), chunk & 1, ctl);
         if (!ok) break;
@@ -320,6 +323,9 @@ __global__ void __launch_bounds__(SparseBwdCfg<DK, DV>::THREADS, 1)
         mma_commit_el(smem_u32(&bar_sdp_full));
         mma_commit_el(smem_u32(&bar_kv_empty[sv]));  // V_c is not read again
         ok = mbar_wait_warp(smem_u32(&bar_pds_full), chunk & 1, ctl);
+        // dV_c's columns (and, at a token's first chunk, dQ^T's) are free once
+        // the previous chunk's dV_c (and the token's dq) have been read out.
+        if (ok && chunk > 0) ok = mbar_wait_warp(smem_u32(&bar_dv_drained), (chunk - 1) & 1, ctl);
         if (!ok) break;
         tc_fence_after();
         // dV_c = P^T dO and dK_c = dS^T Q: heads 16kk..16kk+15 are TMEM columns
@@ -354,12 +360,20 @@ __global__ void __launch_bounds__(SparseBwdCfg<DK, DV>::THREADS, 1)
     mbar_wait_drain(smem_u32(&bar_mma_done), 0, 50000000ull);
     __syncwarp();
   } else {
-    // ------------------------------------------------------------ compute warps 0-3
-    const int j = threadIdx.x;  // slot within the chunk == TMEM lane (later: head-dim index)
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    const float sl2 = p.scale_log2, scale = p.scale;
-    const float* nlse2_s = rows_s;
-    const float* dvec_s = rows_s + C::BQ;
+    // ------------------------------------------------------------ compute warps 0-7
+    const int j = threadIdx.x % 128;  // slot within the chunk == TMEM lane (later: head-dim index)
+    const int cg = warp / 4;          // this warp's half: heads 64 cg.., gradient columns
+    const uint32_t lane_base = static_cast<uint32_t>((warp % 4) * 32) << 16;
+    const uint64_t sl2 = f32x2(p.scale_log2, p.scale_log2);
+    const uint64_t sc2 = f32x2(p.scale, p.scale);
+    const float4* nl4 = reinterpret_cast<const float4*>(rows_s);        // -LSE*log2(e) per head
+    const float4* dv4 = reinterpret_cast<const float4*>(rows_s + C::BQ);  // Dvec per head
+    // This warp's part of the dS^T tiles: rows j of head block cg, 4 KB in the
+    // hi tile and 4 KB in the lo tile. Only this warp writes them, so it can
+    // stage its gradient rows there once the chunk's dQ^T product has read
+    // them, with no other warp touching them until its own next stores.
+    const uint32_t stA = sDsHi + cg * (C::BK * 128) + (warp % 4) * 4096;
+    const uint32_t stB = sDsLo + cg * (C::BK * 128) + (warp % 4) * 4096;
     bool ok = true;
     int chunk = 0;
     for (int r = 0; ok; ++r) {
@@ -381,21 +395,32 @@ __global__ void __launch_bounds__(SparseBwdCfg<DK, DV>::THREADS, 1)
         // memory (row j of the MN-major B operand of dQ^T: heads 0..63 in the
         // first 64-column block, 64..127 in the second, 128-byte swizzle).
 #pragma unroll 1
-        for (int h0 = 0; h0 < C::BQ; h0 += 16) {
+        for (int h0 = 64 * cg; h0 < 64 * cg + 64; h0 += 16) {
           uint32_t su[16], du[16];
           tmem_ld16(tmem + lane_base + C::TM_S + h0, su);
           tmem_ld16(tmem + lane_base + C::TM_DP + h0, du);
           tmem_wait_ld();
           uint32_t pp[16], dd[16];
 #pragma unroll
-          for (int k = 0; k < 16; k += 2) {
-            float p0 = ex2(fmaf(__uint_as_float(su[k]), sl2, nlse2_s[h0 + k]));
-            float p1 = ex2(fmaf(__uint_as_float(su[k + 1]), sl2, nlse2_s[h0 + k + 1]));
-            if (!filled) p0 = p1 = 0.f;
-            const float d0 = p0 * (__uint_as_float(du[k]) - dvec_s[h0 + k]) * scale;
-            const float d1 = p1 * (__uint_as_float(du[k + 1]) - dvec_s[h0 + k + 1]) * scale;
-            split_bf16x2(p0, p1, pp[k / 2], pp[8 + k / 2]);
-            split_bf16x2(d0, d1, dd[k / 2], dd[8 + k / 2]);
+          for (int k = 0; k < 16; k += 4) {
+            const float4 nl = nl4[(h0 + k) / 4];
+            const float4 dv = dv4[(h0 + k) / 4];
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              const int kk = k + 2 * hh;  // heads h0 + kk, h0 + kk + 1
+              float x0, x1;
+              unpack_f32x2(fma_f32x2(f32x2(__uint_as_float(su[kk]), __uint_as_float(su[kk + 1])), sl2,
+                                     hh ? f32x2(nl.z, nl.w) : f32x2(nl.x, nl.y)),
+                           x0, x1);
+              float p0 = ex2(x0), p1 = ex2(x1);
+              if (!filled) p0 = p1 = 0.f;
+              const uint64_t dpv = sub_f32x2(f32x2(__uint_as_float(du[kk]), __uint_as_float(du[kk + 1])),
+                                             hh ? f32x2(dv.z, dv.w) : f32x2(dv.x, dv.y));
+              float d0, d1;
+              unpack_f32x2(mul_f32x2(mul_f32x2(f32x2(p0, p1), sc2), dpv), d0, d1);
+              split_bf16x2(p0, p1, pp[kk / 2], pp[8 + kk / 2]);
+              split_bf16x2(d0, d1, dd[kk / 2], dd[8 + kk / 2]);
+            }
           }
           tmem_st16(tmem + lane_base + C::TM_S + h0, pp);
           tmem_st16(tmem + lane_base + C::TM_DP + h0, dd);
@@ -418,60 +443,69 @@ __global__ void __launch_bounds__(SparseBwdCfg<DK, DV>::THREADS, 1)
         fence_async_smem();
         tc_fence_before();
         mbar_arrive(smem_u32(&bar_pds_full));
-        // The chunk's products are done: add row j of dV_c and dK_c into the
-        // pool gradients of pool row e.
+        // The chunk's products are done: add row j of dK_c and dV_c (this
+        // warp's half of the columns) into the pool gradients of pool row e.
         ok = mbar_wait_warp(smem_u32(&bar_grads_full), chunk & 1, ctl);
         if (!ok) break;
         tc_fence_after();
-        // Each warp stages its 32 rows in its quarter of the dS^T tiles (free
-        // until the next chunk: dQ^T, their last reader, has run), 16-byte unit
-        // u of row i at unit position u ^ (i mod UNITS), then adds one whole
-        // row per instruction -- lane l takes unit l -- so each reduction
-        // covers one contiguous row instead of 32 scattered ones.
-        const uint32_t stage = sDsHi + warp * (32 * 512);
+        // Staging: the warp's 32 rows in its own 8 KB of the dS^T tiles, row i
+        // (HC fp32 columns) in piece stA or stB, 16-byte unit u at unit
+        // position u ^ (i mod UNITS); then each reduction instruction adds
+        // RPI whole rows, lane l taking unit l mod UNITS of row l / UNITS, so
+        // each one covers contiguous row segments instead of scattered words.
         auto drain = [&](uint32_t col, float* pool, auto dcols) {
           constexpr int DC = decltype(dcols)::value;
-          constexpr int UNITS = DC / 4;  // 16-byte units per fp32 row
-          constexpr int ROWB = DC * 4;
-#pragma unroll 1
-          for (int k0 = 0; k0 < DC; k0 += 32) {
+          constexpr int HC = DC / 2;        // this warp's columns: cg * HC ..
+          constexpr int ROWB = HC * 4;      // bytes of a staged row
+          constexpr int UNITS = HC / 4;     // 16-byte units of a staged row
+          constexpr int RPP = 4096 / ROWB;  // rows per 4 KB piece
+          constexpr int RPI = 32 / UNITS;   // rows per reduction instruction
+          auto row_addr = [&](int i) { return (i < RPP ? stA : stB) + (i % RPP) * ROWB; };
+#pragma unroll
+          for (int k0 = 0; k0 < HC; k0 += 32) {
             uint32_t u[32];
-            tmem_ld32(tmem + lane_base + col + k0, u);
+            tmem_ld32(tmem + lane_base + col + cg * HC + k0, u);
             tmem_wait_ld();
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
               const int unit = k0 / 4 + q;
-              const uint32_t addr = stage + lane * ROWB + ((unit ^ (lane & (UNITS - 1))) << 4);
+              const uint32_t addr = row_addr(lane) + ((unit ^ (lane & (UNITS - 1))) << 4);
               asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(u[4 * q]),
                            "r"(u[4 * q + 1]), "r"(u[4 * q + 2]), "r"(u[4 * q + 3])
                            : "memory");
             }
           }
           __syncwarp();
-#pragma unroll 1
-          for (int i = 0; i < 32; ++i) {
+          const int sub = lane % UNITS, rr = lane / UNITS;
+#pragma unroll 4
+          for (int i0 = 0; i0 < 32; i0 += RPI) {
+            const int i = i0 + rr;
             const int ei = __shfl_sync(0xffffffffu, e, i);
             const bool fi = __shfl_sync(0xffffffffu, filled ? 1 : 0, i) != 0;
-            if (fi && lane < UNITS) {
-              const uint32_t addr = stage + i * ROWB + ((lane ^ (i & (UNITS - 1))) << 4);
+            if (fi) {
+              const uint32_t addr = row_addr(i) + ((sub ^ (i & (UNITS - 1))) << 4);
               float4 v;
               asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
                            : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
                            : "r"(addr));
-              red_add_v4(pool + (static_cast<size_t>(b) * p.P + ei) * DC + 4 * lane, v.x, v.y, v.z, v.w);
+              red_add_v4(pool + (static_cast<size_t>(b) * p.P + ei) * DC + cg * HC + 4 * sub, v.x, v.y,
+                         v.z, v.w);
             }
           }
           __syncwarp();
         };
-        drain(C::TM_DV, p.dvp, std::integral_constant<int, DV>{});
         drain(C::TM_S, p.dkp, std::integral_constant<int, DK>{});
+        // dK_c is read: the next chunk's S^T may overwrite its columns.
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bar_dk_drained));
+        drain(C::TM_DV, p.dvp, std::integral_constant<int, DV>{});
         if (c + 1 == nch) {
           // dQ^T is complete for this token: thread j < DK writes column j of
-          // dq for every head (row j of dQ^T). j < DK is warp-uniform.
+          // dq for this warp's heads (row j of dQ^T). j < DK is warp-uniform.
           if (j < DK) {
             float* dqb = p.dq + static_cast<size_t>(item) * p.H * DK + j;
 #pragma unroll 1
-            for (int h0 = 0; h0 < C::BQ; h0 += 32) {
+            for (int h0 = 64 * cg; h0 < 64 * cg + 64; h0 += 32) {
               uint32_t u[32];
               tmem_ld32(tmem + lane_base + C::TM_DQ + h0, u);
               tmem_wait_ld();
@@ -482,14 +516,14 @@ __global__ void __launch_bounds__(SparseBwdCfg<DK, DV>::THREADS, 1)
           }
         }
         tc_fence_before();
-        mbar_arrive(smem_u32(&bar_drain_done));
+        mbar_arrive(smem_u32(&bar_dv_drained));
       }
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) tmem_dealloc(tmem, C::TMEM_COLS);
+  if (warp == C::W_MMA) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
 template <int DK, int DV>

@@ -193,7 +193,8 @@ def sparse_bwd_model(n_items, nch, kslots=2, single_producer_no_flush=False, see
     full = [Bar(1) for _ in range(nslot)]
     empty = [Bar(1) for _ in range(nslot)]
     q_full, q_empty = Bar(1), Bar(1)
-    sdp_full, pds_full, grads_full, drain_done = Bar(1), Bar(1), Bar(1), Bar(1)
+    sdp_full, pds_full, grads_full = Bar(1), Bar(1), Bar(1)
+    dk_drained, dv_drained = Bar(1), Bar(1)
     tma, mma, cpa = [], [], []
 
     def kslot(g):
@@ -271,12 +272,16 @@ def sparse_bwd_model(n_items, nch, kslots=2, single_producer_no_flush=False, see
             for c in range(nch):
                 g = r * nch + c
                 if chunk > 0:
-                    yield from wait(drain_done, chunk - 1)
+                    # S^T(c) overwrites the columns dK_(c-1) was drained from
+                    yield from wait(dk_drained, chunk - 1)
                 yield from wait(full[kslot(g)], kround(g))
                 yield from wait(full[vslot(g)], vround(g))
                 mma.append(sdp_full)
                 mma.append(empty[vslot(g)])
                 yield from wait(pds_full, chunk)
+                if chunk > 0:
+                    # dV_c (and a token's first dQ^T) overwrite dV_(c-1) / dq's columns
+                    yield from wait(dv_drained, chunk - 1)
                 mma.append(grads_full)
                 mma.append(empty[kslot(g)])
                 if c + 1 == nch:
@@ -291,7 +296,9 @@ def sparse_bwd_model(n_items, nch, kslots=2, single_producer_no_flush=False, see
                 yield from wait(sdp_full, chunk)
                 pds_full.arrive()
                 yield from wait(grads_full, chunk)
-                drain_done.arrive()
+                dk_drained.arrive()
+                yield
+                dv_drained.arrive()
                 chunk += 1
 
     producers = [single_producer()] if single_producer_no_flush else [k_producer(), v_producer()]

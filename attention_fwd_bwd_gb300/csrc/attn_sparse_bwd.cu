@@ -41,6 +41,10 @@ using namespace ptx;
 
 namespace {
 
+#ifdef ATTN_TRACE
+static __device__ unsigned long long g_attn_trace[kTraceCtas * kTraceRoles * kTraceEvents];
+#endif
+
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, uint32_t bar,
                                             int c0, int c1) {
   asm volatile(
@@ -173,6 +177,8 @@ __global__ void __launch_bounds__(SparseBwdCfg<DK, DV>::THREADS, 1)
       prefetch_tmap(&tm_k);
     }
     const uint64_t keep = policy_evict_last();  // pool rows recur in nearby tokens' lists
+    TraceCursor tc;
+    if (lane == 0) ATTN_TRACE_INIT(tc, 0);
     int q_loads = 0, last_k = -1;
     bool ok = true;
     for (int r = 0; ok; ++r) {
@@ -191,6 +197,7 @@ __global__ void __launch_bounds__(SparseBwdCfg<DK, DV>::THREADS, 1)
         auto row = [&](int x) { return row0 + ((x >= 0 && x < p.P) ? x : 0); };
         if (round > 0) ok = mbar_wait_warp(smem_u32(&bar_kv_empty[slot]), (round - 1) & 1, ctl);
         if (!ok) return;
+        ATTN_TRACE_EV(tc, 1, gc);  // K slot free, gather issued
         const uint32_t full = smem_u32(&bar_kv_full[slot]);
         const uint32_t dst = sRing + slot * C::SLOT_BYTES + lane * 4 * 128;
         mbar_arrive_expect_tx_el(full, C::K_BYTES);
@@ -240,6 +247,8 @@ __global__ void __launch_bounds__(SparseBwdCfg<DK, DV>::THREADS, 1)
     // Row j's 16-byte unit u lands at j * 128 + ((u % 8) ^ (j % 8)) * 16 in
     // 64-column block u / 8 (the 128-byte swizzle the MMA descriptors expect).
     int* idx_s = reinterpret_cast<int*>(smem + C::SMEM_IDX);
+    TraceCursor tc;
+    if (lane == 0) ATTN_TRACE_INIT(tc, 10);
     bool ok = true;
     for (int r = 0; ok; ++r) {
       const int item = r * n_cta + cta;
@@ -257,6 +266,7 @@ __global__ void __launch_bounds__(SparseBwdCfg<DK, DV>::THREADS, 1)
         __syncwarp();
         if (gc > 0) ok = mbar_wait_warp(smem_u32(&bar_kv_empty[C::VSLOT]), (gc - 1) & 1, ctl);
         if (!ok) break;
+        ATTN_TRACE_EV(tc, 1, gc);  // V slot free, copies issued
         const uint32_t dst = sRing + C::VSLOT * C::SLOT_BYTES;
         constexpr int UNITS = DV / 8;
         constexpr int RPI = 32 / UNITS;
@@ -275,6 +285,7 @@ __global__ void __launch_bounds__(SparseBwdCfg<DK, DV>::THREADS, 1)
         fence_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&bar_kv_full[C::VSLOT]));
+        ATTN_TRACE_EV(tc, 2, gc);  // V landed
       }
     }
     cp_async_wait<0>();
@@ -282,6 +293,8 @@ __global__ void __launch_bounds__(SparseBwdCfg<DK, DV>::THREADS, 1)
   } else if (warp == C::W_MMA) {
     // ------------------------------------------------------------ MMA issuer
     bool ok = !p.inject_stall;
+    TraceCursor tc;
+    if (lane == 0) ATTN_TRACE_INIT(tc, 1);
     constexpr uint32_t idesc_sdp = idesc_bf16_f32(128, 128, 0, 0);  // K-major A and B
     constexpr uint32_t idesc_dv = idesc_bf16_f32(128, DV, 0, 1);    // B = dO, MN-major
     constexpr uint32_t idesc_dk = idesc_bf16_f32(128, DK, 0, 1);    // B = Q, MN-major
@@ -307,6 +320,7 @@ __global__ void __launch_bounds__(SparseBwdCfg<DK, DV>::THREADS, 1)
         if (ok) ok = mbar_wait_warp(smem_u32(&bar_kv_full[sk]), (chunk / C::KSLOTS) & 1, ctl);
         if (ok) ok = mbar_wait_warp(smem_u32(&bar_kv_full[sv]), chunk & 1, ctl);
         if (!ok) break;
+        ATTN_TRACE_EV(tc, 1, chunk);  // dK drained, K and V landed: issuing S^T, dP^T
         tc_fence_after();
         const uint32_t kb = sRing + sk * C::SLOT_BYTES, vb = sRing + sv * C::SLOT_BYTES;
         const uint64_t dk_k = sw128_desc(kb, 16, 1024), dv_k = sw128_desc(vb, 16, 1024);
@@ -327,6 +341,7 @@ __global__ void __launch_bounds__(SparseBwdCfg<DK, DV>::THREADS, 1)
         // the previous chunk's dV_c (and the token's dq) have been read out.
         if (ok && chunk > 0) ok = mbar_wait_warp(smem_u32(&bar_dv_drained), (chunk - 1) & 1, ctl);
         if (!ok) break;
+        ATTN_TRACE_EV(tc, 2, chunk);  // P/dS stored, dV drained: issuing dV, dK, dQ
         tc_fence_after();
         // dV_c = P^T dO and dK_c = dS^T Q: heads 16kk..16kk+15 are TMEM columns
         // 16kk..16kk+7 (hi pairs) and 16kk+8..16kk+15 (lo pairs). dK_c goes into
@@ -375,6 +390,8 @@ __global__ void __launch_bounds__(SparseBwdCfg<DK, DV>::THREADS, 1)
     const uint32_t stA = sDsHi + cg * (C::BK * 128) + (warp % 4) * 4096;
     const uint32_t stB = sDsLo + cg * (C::BK * 128) + (warp % 4) * 4096;
     bool ok = true;
+    TraceCursor tc;
+    if (lane == 0 && warp % 4 == 0) ATTN_TRACE_INIT(tc, 2 + cg);
     int chunk = 0;
     for (int r = 0; ok; ++r) {
       const int item = r * n_cta + cta;
@@ -389,6 +406,7 @@ __global__ void __launch_bounds__(SparseBwdCfg<DK, DV>::THREADS, 1)
         const bool filled = e >= 0 && e < p.P;
         ok = mbar_wait_warp(smem_u32(&bar_sdp_full), chunk & 1, ctl);
         if (!ok) break;
+        ATTN_TRACE_EV(tc, 1, chunk);  // S^T, dP^T landed
         tc_fence_after();
         // Row j of S^T and dP^T, 16 heads at a time: P^T and scale * dS^T as
         // bf16 hi/lo pairs into TMEM over the scores, and dS^T into shared
@@ -443,10 +461,12 @@ __global__ void __launch_bounds__(SparseBwdCfg<DK, DV>::THREADS, 1)
         fence_async_smem();
         tc_fence_before();
         mbar_arrive(smem_u32(&bar_pds_full));
+        ATTN_TRACE_EV(tc, 2, chunk);  // P^T, dS^T stored
         // The chunk's products are done: add row j of dK_c and dV_c (this
         // warp's half of the columns) into the pool gradients of pool row e.
         ok = mbar_wait_warp(smem_u32(&bar_grads_full), chunk & 1, ctl);
         if (!ok) break;
+        ATTN_TRACE_EV(tc, 3, chunk);  // dV_c, dK_c, dQ^T done
         tc_fence_after();
         // Staging: the warp's 32 rows in its own 8 KB of the dS^T tiles, row i
         // (HC fp32 columns) in piece stA or stB, 16-byte unit u at unit
@@ -498,6 +518,7 @@ __global__ void __launch_bounds__(SparseBwdCfg<DK, DV>::THREADS, 1)
         // dK_c is read: the next chunk's S^T may overwrite its columns.
         tc_fence_before();
         mbar_arrive(smem_u32(&bar_dk_drained));
+        ATTN_TRACE_EV(tc, 4, chunk);  // dK_c drained
         drain(C::TM_DV, p.dvp, std::integral_constant<int, DV>{});
         if (c + 1 == nch) {
           // dQ^T is complete for this token: thread j < DK writes column j of
@@ -517,6 +538,7 @@ __global__ void __launch_bounds__(SparseBwdCfg<DK, DV>::THREADS, 1)
         }
         tc_fence_before();
         mbar_arrive(smem_u32(&bar_dv_drained));
+        ATTN_TRACE_EV(tc, 5, chunk);  // dV_c (and dq) drained
       }
     }
   }
@@ -571,3 +593,18 @@ cudaError_t launch_sparse_bwd(int DK, int DV, const __nv_bfloat16* o, const __nv
 }
 
 }  // namespace attn
+
+#ifdef ATTN_TRACE
+// Copies the sparse backward's timeline records to the host and clears them
+// (traced build only).
+extern "C" int attn_trace_copy_sparse_bwd(void* host, size_t bytes) {
+  const size_t total = sizeof(attn::g_attn_trace);
+  if (bytes < total) return 1;
+  if (cudaDeviceSynchronize() != cudaSuccess) return 3;
+  if (cudaMemcpyFromSymbol(host, attn::g_attn_trace, total) != cudaSuccess) return 3;
+  static unsigned long long zeros[4096];
+  for (size_t off = 0; off < total; off += sizeof(zeros))
+    if (cudaMemcpyToSymbol(attn::g_attn_trace, zeros, sizeof(zeros), off) != cudaSuccess) return 3;
+  return 0;
+}
+#endif

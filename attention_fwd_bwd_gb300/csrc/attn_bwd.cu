@@ -24,11 +24,7 @@
 //      warps), staged in shared memory and added into dq with asynchronous
 //      TMA tensor reductions (fp32 add in L2).
 #include <algorithm>
-#include <map>
-#include <memory>
-#include <mutex>
 #include <utility>
-#include <vector>
 
 #include "attn_common.cuh"
 #include "sm100_ptx.cuh"
@@ -69,7 +65,10 @@ __global__ void __launch_bounds__(256) attn_bwd_preprocess_kernel(
   constexpr int RPI = RPW * kPreU;  // rows per warp step
   constexpr int Z4 = RPI * D / 4 / 32;  // float4 zero stores per lane and step
   const long long nrows = static_cast<long long>(B) * S * Hq;
-  if (blockIdx.x == 0 && threadIdx.x == 0) init_status_word(status);
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    init_status_word(status);
+    status[kBwdWorkWord] = 0;  // the main kernel's work counter
+  }
   const long long gthreads = static_cast<long long>(gridDim.x) * blockDim.x;
   const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long gwarp = tid / 32, nwarps = gthreads / 32;
@@ -202,16 +201,15 @@ __device__ __forceinline__ int bwd_head(const BwdItem& t, int it) { return t.h0 
 __device__ __forceinline__ int bwd_qtile(const BwdItem& t, int it) { return t.i_start + it % t.niq; }
 
 // WIN: sliding-window instantiation (p.window > 0). PERSIST: one CTA per SM
-// running its list of items from the schedule; otherwise one CTA per item,
-// named by the block index (and `sched` is unused).
+// taking items from the work counter until none is left; otherwise one CTA
+// per item, named by the block index.
 template <int D, bool WIN, bool PERSIST>
 __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v,
                          const __grid_constant__ CUtensorMap tm_do,
-                         const __grid_constant__ CUtensorMap tm_dq, const BwdParams p,
-                         const __grid_constant__ BwdSchedArg<PERSIST> sched) {
+                         const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
   using C = BwdCfg<D>;
   constexpr int BQ = C::BQ, BK = C::BK, ST = C::STAGES;
   constexpr int HALF = BQ / 2;  // query columns per compute warpgroup
@@ -228,22 +226,19 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       bar_dq_free, bar_stg_full[2], bar_stg_free[2];
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_flag;
+  // Persistent launch: the codes of this CTA's items, in the order taken, in
+  // a 4-slot ring (bar_item[s] completes when slot s holds the next code; -1
+  // ends the run). Four slots suffice: the producer starts item ii + 4 only
+  // after the MMA warp has issued all of item ii + 3 (kv_free), by when the
+  // compute and dQ warps have passed the start of item ii + 2.
+  __shared__ int item_code_s[4];
+  __shared__ uint64_t bar_item[4];
+#ifdef ATTN_TRACE
+  __shared__ int trace_iters;  // iterations the MMA warp issued (for the observer)
+#endif
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
-  // This CTA's items, in order: a slice of the host's schedule (persistent
-  // launch), or the one item the block index names (grid launch).
-  int n_items = 1, e0 = 0;
-  if constexpr (PERSIST) {
-    n_items = sched.off[blockIdx.x + 1] - sched.off[blockIdx.x];
-    e0 = sched.off[blockIdx.x];
-  }
-  auto item_at = [&](int ii) {
-    if constexpr (PERSIST)
-      return bwd_item<WIN>(p, static_cast<int>(sched.code[e0 + ii]), BQ, BK);
-    else
-      return bwd_item<WIN>(p, static_cast<int>(blockIdx.y * gridDim.x + blockIdx.x), BQ, BK);
-  };
 
   const uint32_t sK = smem_u32(smem + C::SMEM_K);
   const uint32_t sV = smem_u32(smem + C::SMEM_V);
@@ -277,6 +272,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     mbar_init(smem_u32(&bar_pds_free), 1);
     mbar_init(smem_u32(&bar_dq_full), 1);
     mbar_init(smem_u32(&bar_dq_free), 128);
+    for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&bar_item[i]), 1);
+#ifdef ATTN_TRACE
+    trace_iters = -1;
+#endif
     for (int h = 0; h < 2; ++h) {
       mbar_init(smem_u32(&bar_stg_full[h]), 128);
       mbar_init(smem_u32(&bar_stg_free[h]), 1);
@@ -292,6 +291,35 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_base_s;
   const WaitCtl ctl{&abort_flag, p.status, p.timeout_ns};
+
+  // Code of this CTA's item ii, -1 past its last item, -2 if the wait for it
+  // gave up. Grid launch: the one item the block index names. Persistent
+  // launch: items are taken in code order (key tiles longest first) from a
+  // work counter that the preprocess zeroes; the producer takes the next one
+  // when it starts an item (take_item) and the other roles read it from the
+  // ring (item_code).
+  auto item_code = [&](int ii) -> int {
+    if constexpr (PERSIST) {
+      if (!mbar_wait_warp(smem_u32(&bar_item[ii & 3]), (ii >> 2) & 1, ctl)) return -2;
+      return reinterpret_cast<volatile int*>(item_code_s)[ii & 3];
+    } else {
+      return ii == 0 ? static_cast<int>(blockIdx.y * gridDim.x + blockIdx.x) : -1;
+    }
+  };
+  auto take_item = [&](int ii) -> int {
+    if constexpr (PERSIST) {
+      int code = 0;
+      if (lane == 0) {
+        code = atomicAdd(p.work, 1);
+        if (code >= p.n_items) code = -1;
+        reinterpret_cast<volatile int*>(item_code_s)[ii & 3] = code;
+        mbar_arrive(smem_u32(&bar_item[ii & 3]));
+      }
+      return __shfl_sync(0xffffffffu, code, 0);
+    } else {
+      return item_code(ii);
+    }
+  };
 
   auto stage_q = [&](int s) { return sStage + s * C::STAGE_BYTES; };
   auto stage_do = [&](int s) { return sStage + s * C::STAGE_BYTES + C::Q_BYTES; };
@@ -328,8 +356,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           tma_load_4d_el(sV + c * (BK * 128), &tm_v, smem_u32(&bar_kv_full), c * 64, t.g, t.k0, t.b);
         }
       };
-      for (int ii = 0; ii < n_items && ok; ++ii) {
-        const BwdItem t = item_at(ii);
+      for (int ii = 0; ok && (PERSIST || ii == 0); ++ii) {
+        const int code = take_item(ii);
+        if (code < 0) break;
+        const BwdItem t = bwd_item<WIN>(p, code, BQ, BK);
         if (!bounds_ok(t.b < p.B && t.g < p.Hkv && t.k0 < p.S, ctl)) {
           ok = false;
           break;
@@ -419,8 +449,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       mma_commit_el(smem_u32(&bar_sdp_full));
     };
     int git = 0;
-    for (int ii = 0; ii < n_items && ok; ++ii) {
-      const int n_it = item_at(ii).n_it;
+    for (int ii = 0; ok && (PERSIST || ii == 0); ++ii) {
+      const int code = item_code(ii);
+      if (code < 0) {
+        ok = code == -1;
+        break;
+      }
+      const int n_it = bwd_item<WIN>(p, code, BQ, BK).n_it;
       ok = mbar_wait_warp(smem_u32(&bar_kv_full), ii & 1, ctl);
       ATTN_TRACE_EV(tc, 1, ii);
       // The item's first S^T/dP^T: once its stage has landed and the compute
@@ -498,6 +533,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       mma_commit_el(smem_u32(&bar_mma_done));
       git += n_it;
     }
+#ifdef ATTN_TRACE
+    if (lane == 0) reinterpret_cast<volatile int*>(&trace_iters)[0] = git;
+#endif
     mma_commit_el(smem_u32(&bar_fin));
     // Every MMA issued finishes before TMEM is released.
     mbar_wait_drain(smem_u32(&bar_fin), 0, 50000000ull);
@@ -538,8 +576,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       return true;
     };
     int git = 0;
-    for (int ii = 0; ii < n_items && ok; ++ii) {
-      const BwdItem t = item_at(ii);
+    for (int ii = 0; ok && (PERSIST || ii == 0); ++ii) {
+      const int code = item_code(ii);
+      if (code < 0) {
+        ok = code == -1;
+        break;
+      }
+      const BwdItem t = bwd_item<WIN>(p, code, BQ, BK);
       const int key = t.k0 + r;
       const bool key_valid = key < p.S;
       for (int it = 0; it < t.n_it; ++it) {
@@ -729,14 +772,17 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           : "memory");
       return ok != 0;
     };
-    int total = 0;
-    for (int ii = 0; ii < n_items; ++ii) total += item_at(ii).n_it;
+    // Runs until the MMA warp has published its iteration count and every
+    // iteration has been seen (or the CTA aborts, or 2 s pass).
     int i1 = 0, i2 = 0, i3 = 0;
     const uint64_t t0 = globaltimer();
-    while (i1 < total || i2 < total || i3 < total) {
-      if (i1 < total && done(smem_u32(&bar_sdp_full), i1 & 1)) ATTN_TRACE_EV(tc, 1, i1++);
-      if (i2 < total && done(smem_u32(&bar_st_empty[i2 % ST]), (i2 / ST) & 1)) ATTN_TRACE_EV(tc, 2, i2++);
-      if (i3 < total && done(smem_u32(&bar_pds_free), i3 & 1)) ATTN_TRACE_EV(tc, 3, i3++);
+    for (;;) {
+      const int total = reinterpret_cast<volatile int*>(&trace_iters)[0];
+      if (total >= 0 && i1 >= total && i2 >= total && i3 >= total) break;
+      if ((total < 0 || i1 < total) && done(smem_u32(&bar_sdp_full), i1 & 1)) ATTN_TRACE_EV(tc, 1, i1++);
+      if ((total < 0 || i2 < total) && done(smem_u32(&bar_st_empty[i2 % ST]), (i2 / ST) & 1))
+        ATTN_TRACE_EV(tc, 2, i2++);
+      if ((total < 0 || i3 < total) && done(smem_u32(&bar_pds_free), i3 & 1)) ATTN_TRACE_EV(tc, 3, i3++);
       if (abort_flag || globaltimer() - t0 > 2000000000ull) break;
     }
 #endif
@@ -748,8 +794,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     TraceCursor tc;
     if (lane == 0) ATTN_TRACE_INIT(tc, 10);
     int git = 0;
-    for (int ii = 0; ii < n_items && ok; ++ii) {
-      const BwdItem t = item_at(ii);
+    for (int ii = 0; ok && (PERSIST || ii == 0); ++ii) {
+      const int code = item_code(ii);
+      if (code < 0) {
+        ok = code == -1;
+        break;
+      }
+      const BwdItem t = bwd_item<WIN>(p, code, BQ, BK);
       // Half 0 of each tile, then half 1; each half's staging tile cycles
       // through its own pair of barriers.
       for (int n = 0; n < 2 * t.n_it && ok; ++n) {
@@ -781,8 +832,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     TraceCursor tc;
     if (lane == 0) ATTN_TRACE_INIT(tc, 10 + (warp - 8));
     int git = 0;
-    for (int ii = 0; ii < n_items && ok; ++ii) {
-      const BwdItem t = item_at(ii);
+    for (int ii = 0; ok && (PERSIST || ii == 0); ++ii) {
+      const int code = item_code(ii);
+      if (code < 0) {
+        ok = code == -1;
+        break;
+      }
+      const BwdItem t = bwd_item<WIN>(p, code, BQ, BK);
       for (int it = 0; it < t.n_it; ++it) {
         const int gi = git + it;
         const int h = bwd_head(t, it);
@@ -840,8 +896,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     if (lin < kSpanCtas) {
       unsigned smid;
       asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
-      int total = 0;
-      for (int ii = 0; ii < n_items; ++ii) total += item_at(ii).n_it;
+      const int total = trace_iters;
       g_attn_spans[4 * lin] = t_entry;
       g_attn_spans[4 * lin + 1] = globaltimer();
       g_attn_spans[4 * lin + 2] = smid;
@@ -868,71 +923,6 @@ int bwd_grid_split(const BwdParams& p, int bq, int sms) {
   return (p.G % 2 == 0 && p.G * niq0 >= 512 && ctas <= 4LL * sms) ? 2 : 1;
 }
 
-// Launch plan of the backward main kernel for one problem shape.
-struct BwdPlan {
-  bool persist = false;
-  int split = 1;
-  BwdSchedArg<true> sched{};
-};
-
-// Items of at most this many iterations on average run on a persistent grid:
-// a CTA's own prologue and epilogue (about 9 us at D = 128 against 1.8 us per
-// iteration) then outweigh what a grid launch's dynamic dispatch gives.
-// Measured (same-box A/B): persistent 7% faster at D = 64, B = 8, H = 16,
-// S = 2048 (16 iterations per item) and 6% faster with a 128-key window at
-// D = 128 (32 per item); 4-12% slower at the Llama-3-8B, 70B and S = 32768
-// shapes (132 to 1028 per item), where the hardware's dispatch of the next
-// CTA to whichever SM is free adapts to SMs that run slower, which a static
-// list cannot, and keeps the running CTAs on neighbouring key tiles.
-constexpr int kBwdPersistMaxMeanIters = 64;
-
-// The plan for the shape of p on `sms` SMs. The persistent schedule is the
-// list schedule of the items in the grid's order (key tiles longest first),
-// each item weighted by its iterations plus two for its prologue/epilogue:
-// item by item to the CTA with the least work so far.
-template <bool WIN>
-std::shared_ptr<const BwdPlan> bwd_plan(const BwdParams& p, int bq, int bk, int sms) {
-  static std::mutex mu;
-  static std::map<std::vector<long long>, std::shared_ptr<const BwdPlan>> cache;
-  const std::vector<long long> key = {p.B, p.Hkv, p.G, p.S, p.causal, p.window, bq, bk, sms};
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    auto f = cache.find(key);
-    if (f != cache.end()) return f->second;
-  }
-  auto plan = std::make_shared<BwdPlan>();
-  BwdParams q = p;
-  q.split = 1;
-  const long long n = static_cast<long long>(p.B) * p.Hkv * p.n_ktiles;
-  long long total = 0;
-  for (int code = 0; code < n && n <= kBwdSchedMaxItems; ++code) total += bwd_item<WIN>(q, code, bq, bk).n_it;
-  plan->persist = sms > 0 && sms <= kBwdSchedMaxCtas && n <= kBwdSchedMaxItems &&
-                  total <= static_cast<long long>(kBwdPersistMaxMeanIters) * n;
-  if (plan->persist) {
-    std::vector<long long> load(sms, 0);
-    std::vector<std::vector<int>> bins(sms);
-    for (int code = 0; code < n; ++code) {
-      const int b = static_cast<int>(std::min_element(load.begin(), load.end()) - load.begin());
-      load[b] += bwd_item<WIN>(q, code, bq, bk).n_it + 2;
-      bins[b].push_back(code);
-    }
-    int c = 0, e = 0;
-    for (const auto& bin : bins) {
-      if (bin.empty()) continue;
-      plan->sched.off[c++] = static_cast<uint16_t>(e);
-      for (int code : bin) plan->sched.code[e++] = static_cast<uint16_t>(code);
-    }
-    plan->sched.off[c] = static_cast<uint16_t>(e);
-    plan->sched.n_ctas = c;
-  } else {
-    plan->split = bwd_grid_split(p, bq, sms);
-  }
-  std::lock_guard<std::mutex> lock(mu);
-  if (cache.size() >= 64) cache.clear();
-  cache[key] = plan;
-  return plan;
-}
-
 template <int D, bool WIN, bool PERSIST>
 cudaError_t set_bwd_smem(int dev) {
   static bool attr_set[64] = {};
@@ -946,6 +936,16 @@ cudaError_t set_bwd_smem(int dev) {
   return cudaSuccess;
 }
 
+// Items of at most this many (head, query tile) iterations on average run on
+// a persistent grid (one CTA per SM taking items from the work counter): a
+// CTA's own prologue and epilogue (about 9 us at D = 128 against 1.8 us per
+// iteration) then outweigh what a launch of one CTA per item gives. Measured
+// (same-box A/B): persistent 7% faster at D = 64, B = 8, H = 16, S = 2048 (16
+// iterations per item) and 6% faster with a 128-key window at D = 128 (32
+// per item); 3% slower at the Llama-3-8B, 70B and S = 32768 shapes (132 to
+// 1028 per item), where the grid launch of one CTA per item stays.
+constexpr int kBwdPersistMaxMeanIters = 64;
+
 template <int D, bool WIN>
 cudaError_t launch_bwd_main_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                               const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p,
@@ -954,26 +954,33 @@ cudaError_t launch_bwd_main_t(const CUtensorMap& tq, const CUtensorMap& tk, cons
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const std::shared_ptr<const BwdPlan> plan = bwd_plan<WIN>(p, C::BQ, C::BK, sms);
   BwdParams pp = p;
-  pp.split = plan->split;
-  if (plan->persist) {
-    cudaError_t e = set_bwd_smem<D, WIN, true>(dev);
-    if (e != cudaSuccess) return e;
-    attn_bwd_main_kernel<D, WIN, true><<<plan->sched.n_ctas, C::THREADS, C::SMEM_ALLOC, stream>>>(
-        tq, tk, tv, tdo, tdq, pp, plan->sched);
-    return cudaGetLastError();
-  }
-  cudaError_t e = set_bwd_smem<D, WIN, false>(dev);
-  if (e != cudaSuccess) return e;
+  pp.split = bwd_grid_split(p, C::BQ, sms);
+  const int per_tile = p.B * p.Hkv * pp.split;  // items per key tile
+  pp.n_items = per_tile * p.n_ktiles;
+  pp.work = p.status + kBwdWorkWord;
+  // Iterations of all items: those of the first item of each key tile (all
+  // items of a key tile have the same count) times the items per key tile.
+  long long total = 0;
+  for (int j = 0; j < p.n_ktiles; ++j) total += bwd_item<WIN>(pp, j * per_tile, C::BQ, C::BK).n_it;
+  total *= per_tile;
+  const bool persist = total <= static_cast<long long>(kBwdPersistMaxMeanIters) * pp.n_items;
   if (pp.split > 1) {
     const long long n4 = static_cast<long long>(p.B) * p.S * p.Hkv * D / 4;
     zero_f32x4_kernel<<<4 * sms, 256, 0, stream>>>(reinterpret_cast<float4*>(p.dk),
                                                    reinterpret_cast<float4*>(p.dv), n4);
   }
-  const dim3 grid(p.B * p.Hkv * pp.split, p.n_ktiles);
-  attn_bwd_main_kernel<D, WIN, false>
-      <<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(tq, tk, tv, tdo, tdq, pp, BwdSchedArg<false>{});
+  if (persist) {
+    cudaError_t e = set_bwd_smem<D, WIN, true>(dev);
+    if (e != cudaSuccess) return e;
+    const int grid = pp.n_items < sms ? pp.n_items : sms;
+    attn_bwd_main_kernel<D, WIN, true><<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(tq, tk, tv, tdo, tdq, pp);
+    return cudaGetLastError();
+  }
+  cudaError_t e = set_bwd_smem<D, WIN, false>(dev);
+  if (e != cudaSuccess) return e;
+  const dim3 grid(per_tile, p.n_ktiles);
+  attn_bwd_main_kernel<D, WIN, false><<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(tq, tk, tv, tdo, tdq, pp);
   return cudaGetLastError();
 }
 

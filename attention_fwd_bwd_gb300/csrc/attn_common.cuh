@@ -223,24 +223,6 @@ struct BwdCfg {
   static_assert(SMEM_ALLOC <= 232448, "shared-memory plan exceeds 227 KB");
 };
 
-// Schedule of the persistent backward main kernel (a kernel parameter): CTA
-// c runs the items code[off[c]] .. code[off[c+1] - 1] in order.
-constexpr int kBwdSchedMaxCtas = 256;
-constexpr int kBwdSchedMaxItems = 4096;
-struct BwdSched {
-  int n_ctas;
-  uint16_t off[kBwdSchedMaxCtas + 1];
-  uint16_t code[kBwdSchedMaxItems];
-};
-// The kernel's schedule argument: the schedule for a persistent launch, an
-// empty stand-in for a grid launch (one CTA per item).
-template <bool PERSIST>
-struct BwdSchedArg : BwdSched {};
-template <>
-struct BwdSchedArg<false> {
-  int n_ctas;
-};
-
 struct BwdParams {
   const float* nlse2;  // [B, Hq, S_pad] -lse * log2(e); -inf on padding rows
   const float* dvec;   // [B, Hq, S_pad] rowsum(dO * O); 0 on padding rows
@@ -256,6 +238,10 @@ struct BwdParams {
   // tile (1 or 2), each taking G / split consecutive heads; with 2 the dK and
   // dV rows are added into zeroed dk and dv. Set by the launcher.
   int split;
+  // Persistent launch: the work counter (the status region's word
+  // kBwdWorkWord, zeroed by the preprocess) and the number of item codes.
+  int* work;
+  int n_items;
   int* status;
   unsigned long long timeout_ns;
   int inject_stall;  // testing hook: the MMA warp issues nothing (waits then run out)
@@ -280,6 +266,11 @@ __device__ __forceinline__ void init_status_word(int* status) {
 struct BwdWorkspace {
   size_t off_status, off_nlse2, off_dvec, total;
 };
+// Word of the workspace's 256-byte status region that counts the items the
+// persistent backward main kernel has taken (words 0 and 1: status word and
+// its tag).
+constexpr int kBwdWorkWord = 4;
+
 inline BwdWorkspace bwd_workspace_layout(int B, int Hq, int S) {
   auto al = [](size_t x) { return (x + 255) / 256 * 256; };
   BwdWorkspace w;

@@ -154,13 +154,27 @@ def test_dense_forward_protocol_is_sound(S, causal, window, nslot):
         assert dense_fwd_model(items, nslot, win=window > 0, seed=seed)
 
 
-def dense_bwd_model(items, dq_in_compute, stages=3, seed=0, stage_last=True, early_kv=False):
+def dense_bwd_model(items, dq_in_compute, stages=3, seed=0, stage_last=True, early_kv=False, ring=4):
     """The persistent backward main kernel over one CTA's items (n_it of
-    each): K/V replaced per item after kv_free, the item's first query stages
-    issued before that wait, per-item mma_done and dkv_free (the compute
-    warps' dK/dV read-out before the next item's first dV/dK products).
-    early_kv plants a mistake: the next item's K/V load does not wait."""
+    each): the producer takes each item's code and publishes it in a ring of
+    `ring` slots that the other roles read (a read that finds a later item's
+    code there is aliasing), K/V replaced per item after kv_free, the item's
+    first query stages issued before that wait, per-item mma_done and dkv_free
+    (the compute warps' dK/dV read-out before the next item's first dV/dK
+    products). early_kv plants a mistake: the next item's K/V load does not
+    wait; ring=1 another: a one-slot ring."""
     rnd = random.Random(seed)
+    item_bar = [Bar(1) for _ in range(ring)]
+    slot_item = [None] * ring
+
+    def publish(ii):
+        slot_item[ii % ring] = ii
+        item_bar[ii % ring].arrive()
+
+    def take(ii, who):
+        yield from wait(item_bar[ii % ring], ii // ring)
+        if slot_item[ii % ring] != ii:
+            raise Aliasing(f"{who} read item slot {ii % ring} for item {ii}, found {slot_item[ii % ring]}")
     kv_full, kv_free, mma_done, fin = Bar(1), Bar(1), Bar(1), Bar(1)
     dkv_free = Bar(2)                         # both P/dS warp groups arrive
     st_full = [Bar(1) for _ in range(stages)]
@@ -197,6 +211,7 @@ def dense_bwd_model(items, dq_in_compute, stages=3, seed=0, stage_last=True, ear
     def producer():
         git, issued, kv_issued = 0, 0, 0
         for ii, n_it in enumerate(items):
+            publish(ii)
             n_early = 0 if ii == 0 else min(stages, n_it)
             if ii == 0:
                 tma.append(KvLoad(0))
@@ -219,6 +234,7 @@ def dense_bwd_model(items, dq_in_compute, stages=3, seed=0, stage_last=True, ear
                 tma.append(KvLoad(ii))
                 kv_issued += 1
             git += n_it
+        publish(len(items))  # the end of the list
         for gi in range(max(0, issued - stages), issued):
             yield from wait(st_full[gi % stages], gi // stages)
         if kv_issued:
@@ -227,6 +243,7 @@ def dense_bwd_model(items, dq_in_compute, stages=3, seed=0, stage_last=True, ear
     def mma_warp():
         git = 0
         for ii, n_it in enumerate(items):
+            yield from take(ii, "mma")
             yield from wait(kv_full, ii)
             yield from wait(st_full[git % stages], git // stages)
             if git > 0:
@@ -250,6 +267,7 @@ def dense_bwd_model(items, dq_in_compute, stages=3, seed=0, stage_last=True, ear
             mma.append(kv_free)
             mma.append(mma_done)
             git += n_it
+        yield from take(len(items), "mma")
         mma.append(fin)
         yield from wait(fin, 0)
 
@@ -260,6 +278,7 @@ def dense_bwd_model(items, dq_in_compute, stages=3, seed=0, stage_last=True, ear
             stg_full[cg].arrive()
         git = 0
         for ii, n_it in enumerate(items):
+            yield from take(ii, f"compute {cg}")
             for it in range(n_it):
                 gi = git + it
                 yield from wait(sdp_full, gi)
@@ -278,17 +297,28 @@ def dense_bwd_model(items, dq_in_compute, stages=3, seed=0, stage_last=True, ear
             yield from wait(mma_done, ii)
             dkv_free.arrive()
             git += n_it
+        yield from take(len(items), f"compute {cg}")
 
     def reduce_warp():
-        for gq in range(sum(items)):
-            for half in range(2):
-                yield from wait(stg_full[half], gq)
-                stg_free[half].arrive()
+        gq = 0
+        for ii, n_it in enumerate(items):
+            yield from take(ii, "reduce")
+            for _ in range(n_it):
+                for half in range(2):
+                    yield from wait(stg_full[half], gq)
+                    stg_free[half].arrive()
+                gq += 1
+        yield from take(len(items), "reduce")
 
     def drain_warps():
-        for gi in range(sum(items)):
-            yield from wait(dq_full, gi)
-            dq_free.arrive()
+        gi = 0
+        for ii, n_it in enumerate(items):
+            yield from take(ii, "drain")
+            for _ in range(n_it):
+                yield from wait(dq_full, gi)
+                dq_free.arrive()
+                gi += 1
+        yield from take(len(items), "drain")
 
     agents = [producer(), mma_warp(), compute(0), compute(1)]
     agents.append(reduce_warp() if dq_in_compute else drain_warps())
@@ -323,6 +353,16 @@ def test_dense_models_catch_planted_mistakes():
             dense_bwd_model([4, 4], False, seed=seed, early_kv=True)
         except (Aliasing, Deadlock):
             caught += 1
+    assert caught > 0
+    # A one-slot ring of item codes: the producer publishes the next item's
+    # code before a slower role has read the current one.
+    caught = 0
+    for seed in range(40):
+        for dq_in_compute in (True, False):
+            try:
+                dense_bwd_model([1, 1, 3, 1], dq_in_compute, seed=seed, ring=1)
+            except (Aliasing, Deadlock):
+                caught += 1
     assert caught > 0
 
 

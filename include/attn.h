@@ -163,6 +163,10 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
  *     sum_j P_ij dP_ij computed from q, k, v, dO and the LSE rows -- what
  *     attn_bwd runs when o_lo is NULL (window as in attn_bwd_ex, 0 = none);
  *   attn_bwd_main: the gradient products.
+ * Each attn_bwd_main call needs a fresh attn_bwd_preprocess before it: the
+ * main stage adds into the dq that the preprocess zeroed, and the preprocess
+ * also restarts the item counter that the main stage's persistent launch
+ * takes its work from (a word of the workspace's status region).
  */
 attn_status_t attn_bwd_preprocess(const void* o, const void* o_lo, const void* dO,
                                   const float* lse, void* dq, int B, int Hq, int Hkv, int S, int D,

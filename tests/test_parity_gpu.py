@@ -210,3 +210,35 @@ def test_long_causal_elementwise(D, residual):
     assert_close_grad(got["dq"], dq_ref, "dQ", what)
     assert_close_grad(got["dk"], dk_ref, "dK", what)
     assert_close_grad(got["dv"], dv_ref, "dV", what)
+
+
+# The staged entry points (preprocess, optionally the Dvec pass, then the
+# main kernel) compute what attn_bwd computes, and can run again on the same
+# workspace: the preprocess restarts the main kernel's item counter each time
+# (short items, D = 64: one CTA per SM taking items from that counter; long
+# items, D = 128: one CTA per item).
+@pytest.mark.parametrize("residual", [True, False], ids=["residual", "plain"])
+@pytest.mark.parametrize("B,Hq,Hkv,S,D", [(2, 4, 4, 1024, 64), (1, 8, 2, 2048, 128)])
+def test_staged_backward_matches_attn_bwd(B, Hq, Hkv, S, D, residual):
+    import attention_fwd_bwd_gb300 as attn
+    scale = 1.0 / np.sqrt(D)
+    q, k, v, do = (t.cuda() for t in make_inputs(B, Hq, Hkv, S, D, seed=91 + D))
+    o, o_lo = torch.empty_like(q), torch.empty_like(q)
+    lse = torch.empty(B, Hq, S, dtype=torch.float32, device=q.device)
+    attn.attn_fwd_residual(q, k, v, o, o_lo, lse, True, scale)
+    ws = torch.empty(attn.attn_bwd_workspace_size(B, Hq, Hkv, S, D), dtype=torch.uint8, device=q.device)
+    f32 = lambda t: torch.empty(t.shape, dtype=torch.float32, device=t.device)
+    ref = [f32(q), f32(k), f32(k)]
+    attn.attn_bwd(q, k, v, o, do, lse, *ref, True, scale, ws, o_lo=o_lo if residual else None)
+    rms = float(ref[0].double().pow(2).mean().sqrt())
+    for _ in range(2):
+        got = [f32(q), f32(k), f32(k)]
+        attn.attn_bwd_preprocess(q, k, o, do, lse, got[0], ws, o_lo=o_lo if residual else None)
+        if not residual:
+            attn.attn_bwd_dvec(q, k, v, do, True, scale, ws)
+        attn.attn_bwd_main(q, k, v, do, *got, True, scale, ws)
+        torch.cuda.synchronize()
+        assert attn.attn_check_status(ws) == 0
+        assert torch.equal(got[1], ref[1]) and torch.equal(got[2], ref[2])
+        # dq: fp32 reductions in varying order
+        assert float((got[0] - ref[0]).abs().max()) <= 1e-5 * rms

@@ -360,7 +360,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         const int c_hi = (p.causal ? min(qrow, p.S - 1) : (p.S - 1)) - k0;
         const int c_lo = WIN ? qrow - p.window + 1 - k0 : 0;
         float alpha = 1.f;
-        bool rescale = false;
+        bool rescale = false, o_rescale = false;
         // One tile of the online softmax: row max, exponentials, both row sums
         // and bf16 P into TMEM over the scores, 16 columns at a time; this
         // thread has read all its scores already.
@@ -370,15 +370,39 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           // min for scale < 0 (masked keys pushed to the losing end).
           if (MASKED) {
             const float lose = pos ? -INFINITY : INFINITY;
+            if constexpr (WIN) {
+              // A window tile usually needs one side of the interval only (the
+              // diagonal tile the causal end, the tile before it the window's
+              // start): test only the sides some row of the warp needs.
+              const bool lo_side = __any_sync(0xffffffffu, c_lo > 0);
+              const bool hi_side = __any_sync(0xffffffffu, c_hi < C::BK - 1);
+              if (lo_side && hi_side) {
 #pragma unroll
-            for (int c = 0; c < C::BK; ++c)
-              if (c > c_hi || (WIN && c < c_lo)) x[c] = lose;
+                for (int c = 0; c < C::BK; ++c)
+                  if (c > c_hi || c < c_lo) x[c] = lose;
+              } else if (lo_side) {
+#pragma unroll
+                for (int c = 0; c < C::BK; ++c)
+                  if (c < c_lo) x[c] = lose;
+              } else if (hi_side) {
+#pragma unroll
+                for (int c = 0; c < C::BK; ++c)
+                  if (c > c_hi) x[c] = lose;
+              }
+            } else {
+#pragma unroll
+              for (int c = 0; c < C::BK; ++c)
+                if (c > c_hi) x[c] = lose;
+            }
           }
           static_assert(C::BK == 128, "row_extreme128 covers one 128-key tile");
           const float mraw = pos ? row_extreme128<true>(x) : row_extreme128<false>(x);
           const float mx = mraw * sl2;
           rescale = mx > m + kRescaleThreshold;
           if (rescale) {
+            // A row whose max was still -inf has O = 0 (all its p were 0), so
+            // only rows with a finite max need their O rescaled below.
+            o_rescale = m > -INFINITY;
             alpha = ex2(m - mx);  // m = -inf on the first tile gives 0
             m = mx;
           }
@@ -418,7 +442,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         }
         ATTN_TRACE_EV(tc, 3, j);  // exponentials done
         // Rescale this warp's O rows (PV_t(j-1) has completed, see above).
-        if (j > jlo(it, t) && __any_sync(0xffffffffu, rescale)) {
+        if (j > jlo(it, t) && __any_sync(0xffffffffu, o_rescale)) {
           const uint32_t to = tmem + lane_base + C::tm_o(t);
 #pragma unroll
           for (int c = 0; c < D; c += 32) {
@@ -439,6 +463,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       // TMEM columns are free again once this epilogue has read them, which
       // is before this warpgroup signals the next item's first P.)
       if (ok) ok = mbar_wait_warp(smem_u32(&bar_pv_done[t]), item & 1, ctl);
+      ATTN_TRACE_EV(tc, 5, item);  // the item's O_t final: epilogue starts
       // The tile's four warps meet at named barriers in the epilogue: agree
       // first on going on.
       ok = named_bar_and(1 + t, 128, ok);
@@ -494,6 +519,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         }
         if (qrow < p.S && bounds_ok(b < p.B && hq < p.Hq && qrow >= 0, ctl))
           p.lse[(static_cast<size_t>(b) * p.Hq + hq) * p.S + qrow] = (m + __log2f(l)) * kLn2;
+        ATTN_TRACE_EV(tc, 6, item);  // epilogue done
       }
     }
   }

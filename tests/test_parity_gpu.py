@@ -242,3 +242,22 @@ def test_staged_backward_matches_attn_bwd(B, Hq, Hkv, S, D, residual):
         assert torch.equal(got[1], ref[1]) and torch.equal(got[2], ref[2])
         # dq: fp32 reductions in varying order
         assert float((got[0] - ref[0]).abs().max()) <= 1e-5 * rms
+
+
+# Non-causal attention over a long sequence, element by element: every key
+# tile sees every query tile, so the backward's items are long (G x 64
+# iterations) and run as one CTA per item -- the launch the short shapes
+# above do not reach without the causal mask.
+@pytest.mark.parametrize("Hq,Hkv,D", [(4, 1, 128), (4, 2, 64)])
+def test_long_noncausal_elementwise(Hq, Hkv, D):
+    B, S = 1, 4096
+    scale = 1.0 / np.sqrt(D)
+    q, k, v, do = make_inputs(B, Hq, Hkv, S, D, seed=211 + D)
+    got = gpu_fwd_bwd(q, k, v, do, False, scale)
+    o_ref, lse_ref = attn_ref_fwd(np64(q), np64(k), np64(v), False, scale)
+    dq_ref, dk_ref, dv_ref = attn_ref_bwd(np64(q), np64(k), np64(v), np64(do), False, scale)
+    what = f"non-causal S{S} Hq{Hq} Hkv{Hkv} D{D}"
+    assert_close_fwd(got["o"], got["lse"], o_ref, lse_ref, what)
+    assert_close_grad(got["dq"], dq_ref, "dQ", what)
+    assert_close_grad(got["dk"], dk_ref, "dK", what)
+    assert_close_grad(got["dv"], dv_ref, "dV", what)

@@ -24,6 +24,7 @@
 //      warps), staged in shared memory and added into dq with asynchronous
 //      TMA tensor reductions (fp32 add in L2).
 #include <algorithm>
+#include <type_traits>
 #include <utility>
 
 #include "attn_common.cuh"
@@ -631,11 +632,18 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
                                      h ? f32x2(nl.z, nl.w) : f32x2(nl.x, nl.y)),
                            x0, x1);
               float p0 = ex2(x0), p1 = ex2(x1);
-              if (decltype(masked)::value) {
-                // Query column cc of this half sees the key iff rel <= cc
-                // (causal) and cc < rel + W (window); rel, relw below.
+              // Query column cc of this half sees the key iff rel <= cc
+              // (causal) and cc < rel + W (window); rel, relw above.
+              constexpr int MODE = decltype(masked)::value;
+              if (MODE == 1) {  // every condition
                 if (!key_valid || (p.causal && cc < rel) || cc >= relw) p0 = 0.f;
                 if (!key_valid || (p.causal && cc + 1 < rel) || cc + 1 >= relw) p1 = 0.f;
+              } else if (MODE == 2) {  // the causal side only
+                if (cc < rel) p0 = 0.f;
+                if (cc + 1 < rel) p1 = 0.f;
+              } else if (MODE == 3) {  // the window side only
+                if (cc >= relw) p0 = 0.f;
+                if (cc + 1 >= relw) p1 = 0.f;
               }
               const uint64_t dpv = sub_f32x2(f32x2(__uint_as_float(ud[cc]), __uint_as_float(ud[cc + 1])),
                                              h ? f32x2(dv.z, dv.w) : f32x2(dv.x, dv.y));
@@ -646,10 +654,23 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
             }
           }
         };
-        if (need_mask)
-          p_ds(BoolConst<true>{});
+        // Mask modes, decided per warp: 0 none, 1 every condition, 2 the
+        // causal side only (the diagonal tiles), 3 the window's far side only.
+        int mode = 0;
+        if (need_mask) {
+          const bool all_valid = __all_sync(0xffffffffu, key_valid);
+          const bool c_side = p.causal && __any_sync(0xffffffffu, rel > 0);
+          const bool w_side = WIN && __any_sync(0xffffffffu, relw < HALF);
+          mode = (!all_valid || (c_side && w_side)) ? 1 : c_side ? 2 : w_side ? 3 : 0;
+        }
+        if (mode == 0)
+          p_ds(std::integral_constant<int, 0>{});
+        else if (mode == 2)
+          p_ds(std::integral_constant<int, 2>{});
+        else if (WIN && mode == 3)
+          p_ds(std::integral_constant<int, 3>{});
         else
-          p_ds(BoolConst<false>{});
+          p_ds(std::integral_constant<int, 1>{});
         ATTN_TRACE_EV(tc, 3, gi);  // P, dS computed
         // pds_free(gi-1): the MMAs of iteration gi-1 are done, so dS^T in
         // shared memory is free and dQ^T(gi-1) is complete in TMEM. With

@@ -40,12 +40,21 @@ struct FwdCfg {
   static constexpr int SMEM_BYTES = SMEM_STG + 2 * STG_BYTES;
   static constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;  // slack for 1024-byte alignment
   // Tensor-memory columns per query tile t: scores S_t (128 fp32 columns,
-  // later overwritten by P_t: for keys 16k..16k+15, bf16 pairs in columns
-  // 16k..16k+7) and the output accumulator O_t (D fp32 columns).
+  // for D = 128 later overwritten by P_t: for keys 16k..16k+15, bf16 pairs in
+  // columns 16k..16k+7) and the output accumulator O_t (D fp32 columns).
   __host__ __device__ static constexpr int tm_s(int t) { return 256 * t; }
   __host__ __device__ static constexpr int tm_o(int t) { return 256 * t + 128; }
+  // D = 64: O_t uses 64 of its 128 columns and P_t (keys 16k..16k+15 as bf16
+  // pairs in columns 8k..8k+7) the other 64, so the softmax frees S_t as soon
+  // as it has read it and the next score product runs while the exponentials
+  // are computed. D = 128: P_t is written over S_t.
+  // Also D = 64: one MMA-issuing warp per query tile (measured faster there;
+  // at D = 128 one warp alternating the tiles is faster).
+  static constexpr bool SEP_P = (D == 64);
+  static constexpr int N_MMA = SEP_P ? 2 : 1;  // MMA-issuing warps
+  __host__ __device__ static constexpr int tm_p(int t) { return SEP_P ? 256 * t + 192 : 256 * t; }
   static constexpr int TMEM_COLS = 512;
-  static constexpr int THREADS = 320;
+  static constexpr int THREADS = 32 * (9 + N_MMA);  // 8 softmax warps, producer, MMA warps
   static_assert(SMEM_ALLOC <= 232448, "shared-memory plan exceeds 227 KB");
 };
 

@@ -19,9 +19,13 @@
 //       (the transposed-operand case of section 3.1.2, handled by the
 //       descriptor instead of a transpose). The two tiles alternate on the
 //       tensor core: while one tile's softmax runs, the other tile's MMAs do.
+//       At D = 64, where each product is half as long and the issuer's own
+//       waits dominate, warps 9 and 10 issue tile A's and tile B's products.
 //   warps 0-3 / 4-7 (softmax of tile A / B): thread r owns query row r of its
 //       tile (TMEM lane r); it reads its score row, updates the running max m
-//       and writes P, rounded to bf16, over the scores in TMEM; when m grew by
+//       and writes P, rounded to bf16, over the scores in TMEM (at D = 64 into
+//       TMEM columns of its own, so that the next score product need not wait
+//       for the exponentials); when m grew by
 //       more than 2^8 it first rescales its O row. It keeps two row sums: l,
 //       of the fp32 probabilities, gives LSE = (m + log2 l) ln 2, and l_b, of
 //       the bf16 values that actually enter P V, gives O = acc / l_b. Dividing
@@ -88,6 +92,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   __shared__ uint64_t bar_q_full, bar_q_empty, bar_mma_done;
   __shared__ uint64_t bar_kv_full[C::NSLOT], bar_kv_empty[C::NSLOT];
   __shared__ uint64_t bar_s_full[2], bar_p_full[2], bar_pv_done[2];
+  // Separate P columns only: S_t read out (s_free) and each P_t V done (pv_step).
+  __shared__ uint64_t bar_s_free[2], bar_pv_step[2];
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_flag;
 
@@ -100,16 +106,18 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(smem_u32(&bar_q_full), 1);
-    mbar_init(smem_u32(&bar_q_empty), 1);
-    mbar_init(smem_u32(&bar_mma_done), 1);
+    mbar_init(smem_u32(&bar_q_empty), C::N_MMA);  // one commit per MMA warp
+    mbar_init(smem_u32(&bar_mma_done), C::N_MMA);
     for (int i = 0; i < C::NSLOT; ++i) {
       mbar_init(smem_u32(&bar_kv_full[i]), 1);
-      mbar_init(smem_u32(&bar_kv_empty[i]), 1);
+      mbar_init(smem_u32(&bar_kv_empty[i]), C::N_MMA);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(smem_u32(&bar_s_full[t]), 1);
       mbar_init(smem_u32(&bar_p_full[t]), 128);
       mbar_init(smem_u32(&bar_pv_done[t]), 1);
+      mbar_init(smem_u32(&bar_s_free[t]), 128);
+      mbar_init(smem_u32(&bar_pv_step[t]), 1);
     }
     fence_barrier_init();
   }
@@ -196,68 +204,219 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     }
     (void)ok;
     __syncwarp();
-  } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
-    // The whole warp runs this loop and builds the (warp-uniform) descriptors;
-    // each MMA and commit is issued by one elected lane.
-    TraceCursor tc;
-    if (lane == 0) ATTN_TRACE_INIT(tc, 1);
-    bool ok = !p.inject_stall;
-    constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
-    constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, 0, 1);
-    const uint64_t dq_desc = sw128_desc(sQ, 16, 1024);
-    int ring = 0;                // ring position of the item's first K/V tile
-    int p_cnt[2] = {0, 0};       // P tiles consumed per query tile, over all items
-    for (int r = 0; ok; ++r) {
-      const int ii = fwd_item_index(r, cta, n_cta, n_items);
-      if (ii < 0) break;
-      const FwdItem it = fwd_item<WIN>(p, ii);
-      const int jb = jlo(it, 0);
-      const int n_kv = it.n_kv[1];  // tile B ends last; tile A starts first
-      ok = mbar_wait_warp(smem_u32(&bar_q_full), r & 1, ctl);
-      if (!ok) break;
-      ATTN_TRACE_EV(tc, 1, r);
-      // S products left in this item; the last one hands the Q buffer back.
-      int s_left = (it.n_kv[0] - jlo(it, 0)) + (it.n_kv[1] - jlo(it, 1));
-      // Ring position of K_j is ring + 2 (j - jb), of V_j the one after it.
-      // S_t = Q_t K_j^T into tile t's score buffer.
-      auto issue_s = [&](int t, int j) {
-        const int slot = (ring + 2 * (j - jb)) % C::NSLOT;
-        const uint64_t dk = sw128_desc(sRing + slot * C::KV_BYTES, 16, 1024);
-        const uint64_t dq = dq_desc + ((t * C::Q_BYTES) >> 4);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t koff = ((kk >> 2) * (128 * 128) + (kk & 3) * 32) >> 4;
-          mma_ss_el(tmem + C::tm_s(t), dq + koff, dk + koff, idesc_s, kk > 0);
-        }
-        mma_commit_el(smem_u32(&bar_s_full[t]));
-        if (--s_left == 0) mma_commit_el(smem_u32(&bar_q_empty));
-      };
-      auto wait_kv = [&](int idx) {
-        const int pos = ring + idx;
-        return mbar_wait_warp(smem_u32(&bar_kv_full[pos % C::NSLOT]), (pos / C::NSLOT) & 1, ctl);
-      };
-      auto kv_slot = [&](int idx) { return (ring + idx) % C::NSLOT; };
-      ok = wait_kv(0);
-      if (!ok) break;
-      tc_fence_after();
-      issue_s(0, jb);
-      if (jlo(it, 1) == jb) issue_s(1, jb);
-      mma_commit_el(smem_u32(&bar_kv_empty[kv_slot(0)]));  // K_jb is done once its S products ran
-      ATTN_TRACE_EV(tc, 3, r);
-      for (int j = jb; j < n_kv && ok; ++j) {
-        bool v_ready = false, k_next_ready = false;
-        for (int t = 0; t < 2 && ok; ++t) {
-          if (j >= jlo(it, t) && j < it.n_kv[t]) {
-            ok = mbar_wait_warp(smem_u32(&bar_p_full[t]), p_cnt[t] & 1, ctl);
-            if (!ok) break;
-            ++p_cnt[t];
-            ATTN_TRACE_EV(tc, 4 + t, j);  // P_t(j) ready seen
-            if (!v_ready) {
-              ok = wait_kv(2 * (j - jb) + 1);
+  } else if (warp == 9 || (C::SEP_P && warp == 10)) {
+    if constexpr (!C::SEP_P) {
+      // ------------------------------------------------------------ MMA issuer
+      // The whole warp runs this loop and builds the (warp-uniform) descriptors;
+      // each MMA and commit is issued by one elected lane.
+      TraceCursor tc;
+      if (lane == 0) ATTN_TRACE_INIT(tc, 1);
+      bool ok = !p.inject_stall;
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
+      constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, 0, 1);
+      const uint64_t dq_desc = sw128_desc(sQ, 16, 1024);
+      int ring = 0;                // ring position of the item's first K/V tile
+      int p_cnt[2] = {0, 0};       // P tiles consumed per query tile, over all items
+      for (int r = 0; ok; ++r) {
+        const int ii = fwd_item_index(r, cta, n_cta, n_items);
+        if (ii < 0) break;
+        const FwdItem it = fwd_item<WIN>(p, ii);
+        const int jb = jlo(it, 0);
+        const int n_kv = it.n_kv[1];  // tile B ends last; tile A starts first
+        ok = mbar_wait_warp(smem_u32(&bar_q_full), r & 1, ctl);
+        if (!ok) break;
+        ATTN_TRACE_EV(tc, 1, r);
+        // S products left in this item; the last one hands the Q buffer back.
+        int s_left = (it.n_kv[0] - jlo(it, 0)) + (it.n_kv[1] - jlo(it, 1));
+        // Ring position of K_j is ring + 2 (j - jb), of V_j the one after it.
+        // S_t = Q_t K_j^T into tile t's score buffer.
+        auto issue_s = [&](int t, int j) {
+          const int slot = (ring + 2 * (j - jb)) % C::NSLOT;
+          const uint64_t dk = sw128_desc(sRing + slot * C::KV_BYTES, 16, 1024);
+          const uint64_t dq = dq_desc + ((t * C::Q_BYTES) >> 4);
+  #pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t koff = ((kk >> 2) * (128 * 128) + (kk & 3) * 32) >> 4;
+            mma_ss_el(tmem + C::tm_s(t), dq + koff, dk + koff, idesc_s, kk > 0);
+          }
+          mma_commit_el(smem_u32(&bar_s_full[t]));
+          if (--s_left == 0) mma_commit_el(smem_u32(&bar_q_empty));
+        };
+        auto wait_kv = [&](int idx) {
+          const int pos = ring + idx;
+          return mbar_wait_warp(smem_u32(&bar_kv_full[pos % C::NSLOT]), (pos / C::NSLOT) & 1, ctl);
+        };
+        auto kv_slot = [&](int idx) { return (ring + idx) % C::NSLOT; };
+        ok = wait_kv(0);
+        if (!ok) break;
+        tc_fence_after();
+        issue_s(0, jb);
+        if (jlo(it, 1) == jb) issue_s(1, jb);
+        mma_commit_el(smem_u32(&bar_kv_empty[kv_slot(0)]));  // K_jb is done once its S products ran
+        ATTN_TRACE_EV(tc, 3, r);
+        for (int j = jb; j < n_kv && ok; ++j) {
+          bool v_ready = false, k_next_ready = false;
+          for (int t = 0; t < 2 && ok; ++t) {
+            if (j >= jlo(it, t) && j < it.n_kv[t]) {
+              ok = mbar_wait_warp(smem_u32(&bar_p_full[t]), p_cnt[t] & 1, ctl);
               if (!ok) break;
-              v_ready = true;
+              ++p_cnt[t];
+              ATTN_TRACE_EV(tc, 4 + t, j);  // P_t(j) ready seen
+              if (!v_ready) {
+                ok = wait_kv(2 * (j - jb) + 1);
+                if (!ok) break;
+                v_ready = true;
+              }
+              tc_fence_after();
+              if (!bounds_ok(j >= 0 && j * C::BK < p.S, ctl)) {
+                ok = false;
+                break;
+              }
+              const int vslot = kv_slot(2 * (j - jb) + 1);
+              const uint64_t dv = sw128_desc(sRing + vslot * C::KV_BYTES, C::BK * 128, 1024);
+              // Keys 16kk..16kk+15: bf16 P pairs in score columns 16kk..16kk+7.
+              const uint32_t a_p = tmem + C::tm_s(t);
+  #pragma unroll
+              for (int kk = 0; kk < C::BK / 16; ++kk)
+                mma_ts_el(tmem + C::tm_o(t), a_p + kk * 16, dv + ((kk * 2048) >> 4), idesc_o,
+                          (j > jlo(it, t) || kk > 0) ? 1u : 0u);
+              if (j + 1 == it.n_kv[t]) mma_commit_el(smem_u32(&bar_pv_done[t]));
+              ATTN_TRACE_EV(tc, 6 + t, j);  // PV_t(j) issued
             }
+            // The next score tile of t overwrites P_t(j) in TMEM; MMAs execute in
+            // issue order, so it runs after PV_t(j) has read P_t(j).
+            if (j + 1 < it.n_kv[t] && j + 1 >= jlo(it, t)) {
+              if (!k_next_ready) {
+                ok = wait_kv(2 * (j - jb) + 2);
+                if (!ok) break;
+                k_next_ready = true;
+                tc_fence_after();
+              }
+              issue_s(t, j + 1);
+            }
+          }
+          if (!ok) break;
+          // Release V_j and K_{j+1} when the MMAs issued on them complete. Every
+          // ring tile has a use (with a window too, the tiles' ranges leave no
+          // gap), so with a window these waits only make sure that no copy is in
+          // flight when its slot is handed back.
+          if constexpr (WIN) {
+            if (!v_ready) ok = wait_kv(2 * (j - jb) + 1);
+            if (ok && j + 1 < n_kv && !k_next_ready) {
+              ok = wait_kv(2 * (j - jb) + 2);
+              k_next_ready = ok;
+            }
+            if (!ok) break;
+          }
+          mma_commit_el(smem_u32(&bar_kv_empty[kv_slot(2 * (j - jb) + 1)]));
+          if (k_next_ready) mma_commit_el(smem_u32(&bar_kv_empty[kv_slot(2 * (j - jb) + 2)]));
+        }
+        ring += 2 * (n_kv - jb);
+      }
+      // Every MMA issued finishes before TMEM is released (in a normal run the
+      // epilogues have already waited for them).
+      mma_commit_el(smem_u32(&bar_mma_done));
+      mbar_wait_drain(smem_u32(&bar_mma_done), 0, 50000000ull);
+      __syncwarp();
+    } else {
+      // ------------------------------------------------------------ MMA issuers
+      // Warp 9 issues query tile A's products, warp 10 tile B's, so that each
+      // tile's chain of waits and issues runs on its own and the two overlap on
+      // the tensor core. The whole warp runs the loop and builds the
+      // (warp-uniform) descriptors; one elected lane issues each run of MMAs
+      // and commits. Ring slots and the Q buffer are handed back when both
+      // warps' commits have arrived (barrier count 2).
+      const int t = warp - 9;
+      TraceCursor tc;
+      if (lane == 0) ATTN_TRACE_INIT(tc, t == 0 ? 1 : 4);
+      bool ok = !p.inject_stall;
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
+      constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, 0, 1);
+      const uint64_t dq = sw128_desc(sQ + t * C::Q_BYTES, 16, 1024);
+      int ring = 0;   // ring position of the item's first K/V tile
+      int p_cnt = 0;  // P tiles of this query tile consumed, over all items
+      int s_iss = 0;  // score products of this query tile issued, over all items
+      for (int r = 0; ok; ++r) {
+        const int ii = fwd_item_index(r, cta, n_cta, n_items);
+        if (ii < 0) break;
+        const FwdItem it = fwd_item<WIN>(p, ii);
+        const int jb = jlo(it, 0);
+        const int n_kv = it.n_kv[1];  // tile B ends last; tile A starts first
+        const int my_lo = jlo(it, t), my_n = it.n_kv[t];
+        ok = mbar_wait_warp(smem_u32(&bar_q_full), r & 1, ctl);
+        if (!ok) break;
+        ATTN_TRACE_EV(tc, 1, r);
+        // This tile's S products left in the item; its last one hands this
+        // warp's share of the Q buffer back.
+        int s_left = my_n - my_lo;
+        // Ring position of K_j is ring + 2 (j - jb), of V_j the one after it.
+        // S_t = Q_t K_j^T into the tile's score columns. With separate P columns
+        // it waits until the softmax has read the previous S_t out of them (with
+        // P over S, issue order does: see the loop below).
+        auto issue_s = [&](int j) {
+          if constexpr (C::SEP_P) {
+            if (s_iss > 0) {
+              ok = mbar_wait_warp(smem_u32(&bar_s_free[t]), (s_iss - 1) & 1, ctl);
+              if (!ok) return;
+              tc_fence_after();
+            }
+          }
+          ++s_iss;
+          const int slot = (ring + 2 * (j - jb)) % C::NSLOT;
+          const uint64_t dk = sw128_desc(sRing + slot * C::KV_BYTES, 16, 1024);
+          const bool last_s = --s_left == 0;
+          if (elect_one()) {
+  #pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t koff = ((kk >> 2) * (128 * 128) + (kk & 3) * 32) >> 4;
+              mma_ss(tmem + C::tm_s(t), dq + koff, dk + koff, idesc_s, kk > 0);
+            }
+            mma_commit(smem_u32(&bar_s_full[t]));
+            if (last_s) mma_commit(smem_u32(&bar_q_empty));
+          }
+          __syncwarp();
+          ATTN_TRACE_EV(tc, 8, j);  // S_t(j) issued
+        };
+        auto wait_kv = [&](int idx) {
+          const int pos = ring + idx;
+          return mbar_wait_warp(smem_u32(&bar_kv_full[pos % C::NSLOT]), (pos / C::NSLOT) & 1, ctl);
+        };
+        auto kv_slot = [&](int idx) { return (ring + idx) % C::NSLOT; };
+        // S_t(j+1), if this tile has it.
+        auto next_s = [&](int j) {
+          if (j + 1 < my_n && j + 1 >= my_lo) {
+            ok = wait_kv(2 * (j - jb) + 2);
+            if (!ok) return;
+            tc_fence_after();
+            issue_s(j + 1);
+          }
+        };
+        if (my_lo == jb) {
+          ok = wait_kv(0);
+          if (!ok) break;
+          tc_fence_after();
+          issue_s(jb);
+          if (!ok) break;
+        }
+        // K_jb is done once the S products on it ran. A slot is handed back
+        // when both warps have committed; the warp that reads a tile waited for
+        // its copy first, and every ring tile has a reader (with a window too,
+        // the tiles' ranges leave no gap), so no copy is in flight then.
+        mma_commit_el(smem_u32(&bar_kv_empty[kv_slot(0)]));
+        ATTN_TRACE_EV(tc, 3, r);
+        for (int j = jb; j < n_kv && ok; ++j) {
+          // Separate P columns: the next score product goes first, as soon as
+          // the softmax has read the current scores.
+          if constexpr (C::SEP_P) next_s(j);
+          if (!ok) break;
+          if (j >= my_lo && j < my_n) {
+            // V_j first: it landed long before P_t(j) is ready.
+            ok = wait_kv(2 * (j - jb) + 1);
+            if (!ok) break;
+            ok = mbar_wait_warp(smem_u32(&bar_p_full[t]), p_cnt & 1, ctl);
+            if (!ok) break;
+            ++p_cnt;
+            ATTN_TRACE_EV(tc, 4, j);  // P_t(j) ready seen
             tc_fence_after();
             if (!bounds_ok(j >= 0 && j * C::BK < p.S, ctl)) {
               ok = false;
@@ -265,50 +424,45 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
             }
             const int vslot = kv_slot(2 * (j - jb) + 1);
             const uint64_t dv = sw128_desc(sRing + vslot * C::KV_BYTES, C::BK * 128, 1024);
-            // Keys 16kk..16kk+15: bf16 P pairs in score columns 16kk..16kk+7.
-            const uint32_t a_p = tmem + C::tm_s(t);
-#pragma unroll
-            for (int kk = 0; kk < C::BK / 16; ++kk)
-              mma_ts_el(tmem + C::tm_o(t), a_p + kk * 16, dv + ((kk * 2048) >> 4), idesc_o,
-                        (j > jlo(it, t) || kk > 0) ? 1u : 0u);
-            if (j + 1 == it.n_kv[t]) mma_commit_el(smem_u32(&bar_pv_done[t]));
-            ATTN_TRACE_EV(tc, 6 + t, j);  // PV_t(j) issued
-          }
-          // The next score tile of t overwrites P_t(j) in TMEM; MMAs execute in
-          // issue order, so it runs after PV_t(j) has read P_t(j).
-          if (j + 1 < it.n_kv[t] && j + 1 >= jlo(it, t)) {
-            if (!k_next_ready) {
-              ok = wait_kv(2 * (j - jb) + 2);
-              if (!ok) break;
-              k_next_ready = true;
-              tc_fence_after();
+            // Keys 16kk..16kk+15: bf16 P pairs in score columns 16kk..16kk+7
+            // (P over S), or in P columns 8kk..8kk+7 (separate P).
+            const uint32_t a_p = tmem + C::tm_p(t);
+            constexpr int P_STEP = C::SEP_P ? 8 : 16;
+            const uint32_t acc0 = j > my_lo ? 1u : 0u;
+            const bool last_pv = j + 1 == my_n;
+            if (elect_one()) {
+  #pragma unroll
+              for (int kk = 0; kk < C::BK / 16; ++kk)
+                mma_ts(tmem + C::tm_o(t), a_p + kk * P_STEP, dv + ((kk * 2048) >> 4), idesc_o,
+                       kk > 0 ? 1u : acc0);
+              if constexpr (C::SEP_P) mma_commit(smem_u32(&bar_pv_step[t]));
+              if (last_pv) mma_commit(smem_u32(&bar_pv_done[t]));
             }
-            issue_s(t, j + 1);
+            __syncwarp();
+            ATTN_TRACE_EV(tc, 6, j);  // PV_t(j) issued
           }
-        }
-        if (!ok) break;
-        // Release V_j and K_{j+1} when the MMAs issued on them complete. Every
-        // ring tile has a use (with a window too, the tiles' ranges leave no
-        // gap), so with a window these waits only make sure that no copy is in
-        // flight when its slot is handed back.
-        if constexpr (WIN) {
-          if (!v_ready) ok = wait_kv(2 * (j - jb) + 1);
-          if (ok && j + 1 < n_kv && !k_next_ready) {
-            ok = wait_kv(2 * (j - jb) + 2);
-            k_next_ready = ok;
-          }
+          // P over S: the next score tile overwrites P_t(j) in TMEM; MMAs issued
+          // by one thread execute in issue order, so it runs after PV_t(j) has
+          // read P_t(j).
+          if constexpr (!C::SEP_P) next_s(j);
           if (!ok) break;
+          // This warp's share of handing back V_j and K_{j+1}: arrives when the
+          // MMAs it issued so far complete.
+          if (elect_one()) {
+            mma_commit(smem_u32(&bar_kv_empty[kv_slot(2 * (j - jb) + 1)]));
+            if (j + 1 < n_kv) mma_commit(smem_u32(&bar_kv_empty[kv_slot(2 * (j - jb) + 2)]));
+          }
+          __syncwarp();
         }
-        mma_commit_el(smem_u32(&bar_kv_empty[kv_slot(2 * (j - jb) + 1)]));
-        if (k_next_ready) mma_commit_el(smem_u32(&bar_kv_empty[kv_slot(2 * (j - jb) + 2)]));
+        ring += 2 * (n_kv - jb);
       }
-      ring += 2 * (n_kv - jb);
+      // Every MMA issued finishes before TMEM is released (in a normal run the
+      // epilogues have already waited for them); the barrier completes once
+      // both warps' commits have arrived.
+      mma_commit_el(smem_u32(&bar_mma_done));
+      mbar_wait_drain(smem_u32(&bar_mma_done), 0, 50000000ull);
+      __syncwarp();
     }
-    // Every MMA issued finishes before TMEM is released (in a normal run the
-    // epilogues have already waited for them).
-    mma_commit_el(smem_u32(&bar_mma_done));
-    mbar_wait_drain(smem_u32(&bar_mma_done), 0, 50000000ull);
-    __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax warps 0-7
     const int t = warp / 4;           // query tile of this warpgroup
@@ -333,7 +487,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       float lb = 0.f;       // row sum of the bf16 probabilities that enter P V (for O)
       for (int j = jlo(it, t); j < my_kv; ++j) {
         ATTN_TRACE_EV(tc, 1, j);  // start waiting for S_t(j)
-        // S_t(j) landed; its commit also covers PV_t(j-1), so O_t is current.
+        // S_t(j) landed. With P over S its commit also covers PV_t(j-1), so O_t
+        // is current; with separate P columns that is waited for below.
         ok = mbar_wait_warp(smem_u32(&bar_s_full[t]), s_cnt & 1, ctl);
         if (!ok) break;
         ++s_cnt;
@@ -350,6 +505,12 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
 #pragma unroll
           for (int c = 0; c < C::BK; ++c) x[c] = __uint_as_float(u[c]);
         }
+        if constexpr (C::SEP_P) {
+          // S_t(j) is in registers: the next score product may overwrite it.
+          tc_fence_before();
+          mbar_arrive(smem_u32(&bar_s_free[t]));
+          ATTN_TRACE_EV(tc, 7, j);  // S_t(j) read out
+        }
         const int k0 = j * C::BK;
         const int qt0 = q0 + t * C::BQ;
         // Tiles that cross the causal diagonal, hold keys past S, or hold keys
@@ -361,9 +522,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         const int c_lo = WIN ? qrow - p.window + 1 - k0 : 0;
         float alpha = 1.f;
         bool rescale = false, o_rescale = false;
+        uint32_t pk[C::BK / 2];  // bf16 P pairs of the tile's keys
         // One tile of the online softmax: row max, exponentials, both row sums
-        // and bf16 P into TMEM over the scores, 16 columns at a time; this
-        // thread has read all its scores already.
+        // and bf16 P; with P over S it goes into TMEM 16 columns at a time
+        // (this thread has read all its scores already).
         {
           const bool MASKED = need_mask;
           // Largest scaled score: the max of the raw scores for scale >= 0, the
@@ -416,7 +578,6 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           for (int i = 0; i < 2; ++i) sums[i] = sumsb[i] = f32x2(0.f, 0.f);
 #pragma unroll
           for (int ch = 0; ch < C::BK; ch += 16) {
-            uint32_t pk[8];  // bf16 P pairs of keys ch..ch+15
 #pragma unroll
             for (int c = 0; c < 16; c += 2) {
               float e0, e1;
@@ -426,13 +587,14 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
               const float p0 = ex2(e0), p1 = ex2(e1);
               sums[(c / 2) & 1] = add_f32x2(sums[(c / 2) & 1], f32x2(p0, p1));
               const uint32_t w = pack_bf16x2(p0, p1);  // round to nearest even
-              pk[c / 2] = w;
+              pk[(ch + c) / 2] = w;
               sumsb[(c / 2) & 1] =
                   add_f32x2(sumsb[(c / 2) & 1], f32x2(__uint_as_float(w << 16),
                                                       __uint_as_float(w & 0xFFFF0000u)));
             }
             // Columns ch..ch+7 of the scores (already read) take these keys' P.
-            tmem_st8(ts + ch, pk);
+            if constexpr (!C::SEP_P)
+              tmem_st8(ts + ch, *reinterpret_cast<const uint32_t(*)[8]>(&pk[ch / 2]));
           }
           float s0, s1, b0, b1;
           unpack_f32x2(add_f32x2(sums[0], sums[1]), s0, s1);
@@ -441,6 +603,20 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           lb = lb * alpha + (b0 + b1);
         }
         ATTN_TRACE_EV(tc, 3, j);  // exponentials done
+        if constexpr (C::SEP_P) {
+          // PV_t of the previous P (this item's or, for its first tile, the
+          // previous item's last) has read the P columns and written O_t.
+          if (s_cnt > 1) {
+            ok = mbar_wait_warp(smem_u32(&bar_pv_step[t]), (s_cnt - 2) & 1, ctl);
+            if (!ok) break;
+            tc_fence_after();
+          }
+          ATTN_TRACE_EV(tc, 8, j);  // PV_t(j-1) seen done
+          const uint32_t tp = tmem + lane_base + C::tm_p(t);
+#pragma unroll
+          for (int c = 0; c < C::BK / 2; c += 32)
+            tmem_st32(tp + c, *reinterpret_cast<const uint32_t(*)[32]>(&pk[c]));
+        }
         // Rescale this warp's O rows (PV_t(j-1) has completed, see above).
         if (j > jlo(it, t) && __any_sync(0xffffffffu, o_rescale)) {
           const uint32_t to = tmem + lane_base + C::tm_o(t);

@@ -350,6 +350,18 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 }
 
 // ------------------------------------------------------------------ elected issue
+// True in one lane of the converged warp (elect.sync). For a run of several
+// MMAs and commits: one election, then that lane issues them all (the warp
+// reconverges after the branch).
+__device__ __forceinline__ bool elect_one() {
+  uint32_t e;
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, e;\n\t}"
+      : "=r"(e));
+  return e != 0;
+}
 // The forms below are executed by a whole converged warp; inside each asm a
 // single lane is elected (elect.sync) and only it issues the operation. The
 // warp thus stays converged, its operands stay warp-uniform, and the issue

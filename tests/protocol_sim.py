@@ -36,19 +36,23 @@ def wait(bar, phase):
 
 def run(agents, queues, rnd):
     """Interleave the agents and the asynchronous completions; raise Deadlock
-    when nothing changes for a long stretch."""
+    when nothing changes for a long stretch. `mma` is one in-order queue of
+    MMA completions, or a tuple of them (one per issuing thread: each in
+    order, the queues in any interleaving)."""
     tma, mma, cpa = queues
+    fifos = mma if isinstance(mma, tuple) else (mma,)
     live = list(range(len(agents)))
     idle = 0
-    while live or tma or mma or any(not d for d, _ in cpa):
-        before = (Bar.changes, len(tma), len(mma), len(cpa), len(live))
-        events = (["tma"] if tma else []) + (["mma"] if mma else []) + \
+    n_mma = lambda: sum(len(q) for q in fifos)
+    while live or tma or n_mma() or any(not d for d, _ in cpa):
+        before = (Bar.changes, len(tma), n_mma(), len(cpa), len(live))
+        events = (["tma"] if tma else []) + (["mma"] if n_mma() else []) + \
                  (["cpa"] if any(not d for d, _ in cpa) else [])
         choice = rnd.choice(live + events)
         if choice == "tma":
             tma.pop(rnd.randrange(len(tma))).arrive()
         elif choice == "mma":
-            mma.pop(0).arrive()
+            rnd.choice([q for q in fifos if q]).pop(0).arrive()
         elif choice == "cpa":
             next(e for e in cpa if not e[0])[0] = True
             Bar.changes += 1
@@ -57,7 +61,7 @@ def run(agents, queues, rnd):
                 next(agents[choice])
             except StopIteration:
                 live.remove(choice)
-        if (Bar.changes, len(tma), len(mma), len(cpa), len(live)) == before:
+        if (Bar.changes, len(tma), n_mma(), len(cpa), len(live)) == before:
             idle += 1
             if idle > 20000:
                 raise Deadlock("every role waits and nothing is in flight")

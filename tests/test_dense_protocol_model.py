@@ -5,9 +5,11 @@ order, MMA commits in issue order), and random interleavings must neither
 pass a wait on the wrong phase nor deadlock.
 
 Forward: the persistent kernel -- a producer that preloads the next item's
-first K/V tiles before waiting for the Q buffer, an MMA issuer that
-alternates two query tiles, and two softmax warpgroups -- over the items of
-causal, non-causal, ragged and sliding-window problems. Backward: the
+first K/V tiles before waiting for the Q buffer, MMA issue, and two softmax
+warpgroups -- over the items of causal, non-causal, ragged and
+sliding-window problems: with P over S and one issuer alternating the query
+tiles (D = 128), and with P in columns of its own and one issuer per query
+tile (D = 64). Backward: the
 persistent key-tile CTA over lists of items (K/V replaced per item, the
 three-stage Q/dO ring and every other barrier running on across items), in
 both dQ modes (the P/dS warps reading dQ^T and staging it for one reduction
@@ -152,6 +154,178 @@ def test_dense_forward_protocol_is_sound(S, causal, window, nslot):
     items = fwd_items(S, causal, window)
     for seed in range(25):
         assert dense_fwd_model(items, nslot, win=window > 0, seed=seed)
+
+
+def dense_fwd_sep_p_model(items, nslot, win=False, seed=0, skip_s_free=False, skip_pv_step=False,
+                          release_count=2):
+    """The forward when P_t has tensor-memory columns of its own (D = 64, where
+    O_t takes 64 of its 128 columns and P_t the other 64): the softmax frees
+    S_t as soon as it has read it (s_free), so the tile's MMA issuer runs S_t(j+1)
+    while the exponentials of S_t(j) are computed; P_t(j) is stored only
+    after P_t V(j-1) has read P_t(j-1) (pv_step, one commit per P V). The
+    tensor-memory regions are tracked: a score product that lands on unread
+    scores, a P store over a P that its product has not read, an O rescale or
+    epilogue read before the last P V landed, or an item's first P V (which
+    overwrites O) before the previous epilogue read O, raises Aliasing.
+    Each query tile has its own MMA issuer (with its own in-order
+    completions); ring slots, the Q buffer and the final drain complete once
+    both issuers have committed (count 2). skip_s_free and skip_pv_step plant
+    the two missing waits, release_count=1 a slot handed back on either
+    issuer's commit."""
+    rnd = random.Random(seed)
+    kv_full = [Bar(1) for _ in range(nslot)]
+    kv_empty = [Bar(release_count) for _ in range(nslot)]
+    q_full, q_empty, mma_done = Bar(1), Bar(2), Bar(2)
+    s_full, s_free = [Bar(1), Bar(1)], [Bar(1), Bar(1)]
+    p_full, pv_step, pv_done = [Bar(1), Bar(1)], [Bar(1), Bar(1)], [Bar(1), Bar(1)]
+    tma, mma = [], ([], [])
+    # Per query tile: score tiles written / read, P tiles stored / read by P V,
+    # and epilogues done.
+    st = [{"s_w": 0, "s_r": 0, "p_w": 0, "p_r": 0, "epi": 0} for _ in range(2)]
+
+    class Done:  # an asynchronous MMA completing: check the regions, then signal
+        def __init__(self, fn, bar):
+            self.fn, self.bar = fn, bar
+
+        def arrive(self):
+            self.fn()
+            self.bar.arrive()
+
+    def s_lands(t):
+        def fn():
+            if st[t]["s_w"] != st[t]["s_r"]:
+                raise Aliasing(f"S_{t} product landed on scores not yet read")
+            st[t]["s_w"] += 1
+        return fn
+
+    def pv_lands(t, item, first):
+        def fn():
+            if st[t]["p_r"] + 1 != st[t]["p_w"]:
+                raise Aliasing(f"P_{t} V read a P that was not (or no longer) there")
+            if first and st[t]["epi"] != item:
+                raise Aliasing(f"item {item}'s first P_{t} V overwrote O before the epilogue read it")
+            st[t]["p_r"] += 1
+        return fn
+
+    def producer():
+        issued = q_loads = 0
+        for r, (n0, n1, l0, l1) in enumerate(items):
+            n_pos = 2 * (n1 - l0)
+
+            def load_kv():
+                nonlocal issued
+                slot, rnd_ = issued % nslot, issued // nslot
+                if rnd_ > 0:
+                    yield from wait(kv_empty[slot], rnd_ - 1)
+                tma.append(kv_full[slot])
+                issued += 1
+            pre = 0 if r == 0 else min(2, n_pos)
+            for _ in range(pre):
+                yield from load_kv()
+            if r > 0:
+                yield from wait(q_empty, r - 1)
+            tma.append(q_full)
+            q_loads += 1
+            for _ in range(pre, n_pos):
+                yield from load_kv()
+        for pos in range(max(0, issued - nslot), issued):
+            yield from wait(kv_full[pos % nslot], pos // nslot)
+        yield from wait(q_full, q_loads - 1)
+
+    def mma_warp(t):
+        ring, p_cnt, s_iss, q = 0, 0, 0, mma[t]
+        for r, it in enumerate(items):
+            n1, jb = it[1], it[2]
+            my_n, my_lo = it[t], it[2 + t]
+            yield from wait(q_full, r)
+            s_left = [my_n - my_lo]
+
+            def issue_s():
+                nonlocal s_iss
+                if s_iss > 0 and not skip_s_free:
+                    yield from wait(s_free[t], s_iss - 1)
+                s_iss += 1
+                q.append(Done(s_lands(t), s_full[t]))
+                s_left[0] -= 1
+                if s_left[0] == 0:
+                    q.append(q_empty)
+
+            def wait_kv(idx):
+                pos = ring + idx
+                yield from wait(kv_full[pos % nslot], pos // nslot)
+
+            def slot(idx):
+                return (ring + idx) % nslot
+            if my_lo == jb:
+                yield from wait_kv(0)
+                yield from issue_s()
+            q.append(kv_empty[slot(0)])
+            for j in range(jb, n1):
+                if my_lo <= j + 1 < my_n:  # the next scores first
+                    yield from wait_kv(2 * (j - jb) + 2)
+                    yield from issue_s()
+                if my_lo <= j < my_n:
+                    yield from wait_kv(2 * (j - jb) + 1)
+                    yield from wait(p_full[t], p_cnt)
+                    p_cnt += 1
+                    q.append(Done(pv_lands(t, r, j == my_lo), pv_step[t]))
+                    if j + 1 == my_n:
+                        q.append(pv_done[t])
+                q.append(kv_empty[slot(2 * (j - jb) + 1)])
+                if j + 1 < n1:
+                    q.append(kv_empty[slot(2 * (j - jb) + 2)])
+            ring += 2 * (n1 - jb)
+        q.append(mma_done)
+        yield from wait(mma_done, 0)
+
+    def softmax(t):
+        s_cnt = 0
+        for item, it in enumerate(items):
+            n_kv, jlo = it[t], it[2 + t]
+            for _ in range(jlo, n_kv):
+                yield from wait(s_full[t], s_cnt)
+                s_cnt += 1
+                if st[t]["s_r"] + 1 != st[t]["s_w"]:
+                    raise Aliasing(f"softmax {t} read scores that were not there")
+                st[t]["s_r"] += 1
+                s_free[t].arrive()
+                yield  # the exponentials
+                if s_cnt > 1 and not skip_pv_step:
+                    yield from wait(pv_step[t], s_cnt - 2)
+                # O rescale and the P store: every earlier P V has landed.
+                if st[t]["p_r"] != st[t]["p_w"]:
+                    raise Aliasing(f"softmax {t} stored P (or rescaled O) under a pending P V")
+                st[t]["p_w"] += 1
+                p_full[t].arrive()
+            yield from wait(pv_done[t], item)
+            if st[t]["p_r"] != st[t]["p_w"]:
+                raise Aliasing(f"epilogue {t} read O before its last P V landed")
+            st[t]["epi"] += 1
+
+    return run([producer(), mma_warp(0), mma_warp(1), softmax(0), softmax(1)], (tma, mma, []), rnd)
+
+
+@pytest.mark.parametrize("S,causal,window", FWD_CASES)
+@pytest.mark.parametrize("nslot", [8])
+def test_dense_forward_separate_p_protocol_is_sound(S, causal, window, nslot):
+    items = fwd_items(S, causal, window)
+    for seed in range(25):
+        assert dense_fwd_sep_p_model(items, nslot, win=window > 0, seed=seed)
+
+
+def test_separate_p_model_catches_the_missing_waits():
+    """Without the s_free wait a score product lands on scores the softmax has
+    not read; without the pv_step wait a P store overwrites a P that its
+    product has not read; with ring slots handed back on one issuer's commit
+    a slot's barrier completes twice per use (each in some interleaving)."""
+    for kw in ({"skip_s_free": True}, {"skip_pv_step": True}, {"release_count": 1}):
+        caught = 0
+        for seed in range(30):
+            try:
+                dense_fwd_sep_p_model(fwd_items(1024, True), 8, seed=seed, **kw)
+            except (Aliasing, Deadlock):
+                caught += 1
+        assert caught > 0, kw
 
 
 def dense_bwd_model(items, dq_in_compute, stages=3, seed=0, stage_last=True, early_kv=False, ring=4):

@@ -48,15 +48,32 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                "r"(bytes)
                : "memory");
 }
+// SUSPEND: pass a suspend-time hint, so that a thread whose phase has not
+// completed sleeps until it completes (or the hint runs out) rather than
+// returning at once; its warp then takes no issue slots from the warps that
+// share its scheduler. Measured 1-2% faster in the backward main kernel and
+// 1% slower in the D = 128 forward.
+constexpr uint32_t kSuspendHintNs = 20000;
+template <bool SUSPEND = false>
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
+  if constexpr (SUSPEND) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+  }
   return ok != 0;
 }
 
@@ -96,11 +113,12 @@ __device__ __forceinline__ bool bounds_ok(bool, const WaitCtl&) { return true; }
 // limit every 64 polls. Returns false if the CTA was told to abort or the time
 // limit ran out (then it raises the abort flag and records a timeout in the
 // status word).
+template <bool SUSPEND = false>
 static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity,
                                                    const WaitCtl& ctl) {
   const uint64_t t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait<SUSPEND>(bar, parity)) return true;
     if ((it & 63u) == 0) {
       if (*ctl.abort_flag) return false;
       if (globaltimer() - t0 > ctl.timeout_ns) {
@@ -114,17 +132,19 @@ static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity
 
 // Waits for the phase with the given parity to complete. The common case -- a
 // phase that completes within a few polls -- stays inline, with no call.
+template <bool SUSPEND = false>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl& ctl) {
 #pragma unroll 1
   for (int i = 0; i < 16; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
-  return mbar_wait_slow(bar, parity, ctl);
+    if (mbar_try_wait<SUSPEND>(bar, parity)) return true;
+  return mbar_wait_slow<SUSPEND>(bar, parity, ctl);
 }
 
 // Warp-uniform form: every lane polls, and the warp agrees on the outcome, so
 // the warp never diverges before a .sync.aligned instruction.
+template <bool SUSPEND = false>
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, const WaitCtl& ctl) {
-  const bool ok = mbar_wait(bar, parity, ctl);
+  const bool ok = mbar_wait<SUSPEND>(bar, parity, ctl);
   return __all_sync(0xffffffffu, ok);
 }
 

@@ -234,7 +234,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           const int slot = (ring + 2 * (j - jb)) % C::NSLOT;
           const uint64_t dk = sw128_desc(sRing + slot * C::KV_BYTES, 16, 1024);
           const uint64_t dq = dq_desc + ((t * C::Q_BYTES) >> 4);
-  #pragma unroll
+#pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t koff = ((kk >> 2) * (128 * 128) + (kk & 3) * 32) >> 4;
             mma_ss_el(tmem + C::tm_s(t), dq + koff, dk + koff, idesc_s, kk > 0);
@@ -276,7 +276,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
               const uint64_t dv = sw128_desc(sRing + vslot * C::KV_BYTES, C::BK * 128, 1024);
               // Keys 16kk..16kk+15: bf16 P pairs in score columns 16kk..16kk+7.
               const uint32_t a_p = tmem + C::tm_s(t);
-  #pragma unroll
+#pragma unroll
               for (int kk = 0; kk < C::BK / 16; ++kk)
                 mma_ts_el(tmem + C::tm_o(t), a_p + kk * 16, dv + ((kk * 2048) >> 4), idesc_o,
                           (j > jlo(it, t) || kk > 0) ? 1u : 0u);
@@ -319,7 +319,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       mbar_wait_drain(smem_u32(&bar_mma_done), 0, 50000000ull);
       __syncwarp();
     } else {
-      // ------------------------------------------------------------ MMA issuers
+      // ------------------------------------------------------------ MMA issuers (D = 64)
       // Warp 9 issues query tile A's products, warp 10 tile B's, so that each
       // tile's chain of waits and issues runs on its own and the two overlap on
       // the tensor core. The whole warp runs the loop and builds the
@@ -350,23 +350,20 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         // warp's share of the Q buffer back.
         int s_left = my_n - my_lo;
         // Ring position of K_j is ring + 2 (j - jb), of V_j the one after it.
-        // S_t = Q_t K_j^T into the tile's score columns. With separate P columns
-        // it waits until the softmax has read the previous S_t out of them (with
-        // P over S, issue order does: see the loop below).
+        // S_t = Q_t K_j^T into the tile's score columns, once the softmax has
+        // read the previous S_t out of them.
         auto issue_s = [&](int j) {
-          if constexpr (C::SEP_P) {
-            if (s_iss > 0) {
-              ok = mbar_wait_warp(smem_u32(&bar_s_free[t]), (s_iss - 1) & 1, ctl);
-              if (!ok) return;
-              tc_fence_after();
-            }
+          if (s_iss > 0) {
+            ok = mbar_wait_warp(smem_u32(&bar_s_free[t]), (s_iss - 1) & 1, ctl);
+            if (!ok) return;
+            tc_fence_after();
           }
           ++s_iss;
           const int slot = (ring + 2 * (j - jb)) % C::NSLOT;
           const uint64_t dk = sw128_desc(sRing + slot * C::KV_BYTES, 16, 1024);
           const bool last_s = --s_left == 0;
           if (elect_one()) {
-  #pragma unroll
+#pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
               const uint32_t koff = ((kk >> 2) * (128 * 128) + (kk & 3) * 32) >> 4;
               mma_ss(tmem + C::tm_s(t), dq + koff, dk + koff, idesc_s, kk > 0);
@@ -405,9 +402,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         mma_commit_el(smem_u32(&bar_kv_empty[kv_slot(0)]));
         ATTN_TRACE_EV(tc, 3, r);
         for (int j = jb; j < n_kv && ok; ++j) {
-          // Separate P columns: the next score product goes first, as soon as
-          // the softmax has read the current scores.
-          if constexpr (C::SEP_P) next_s(j);
+          // The next score product goes first, as soon as the softmax has read
+          // the current scores.
+          next_s(j);
           if (!ok) break;
           if (j >= my_lo && j < my_n) {
             // V_j first: it landed long before P_t(j) is ready.
@@ -424,27 +421,21 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
             }
             const int vslot = kv_slot(2 * (j - jb) + 1);
             const uint64_t dv = sw128_desc(sRing + vslot * C::KV_BYTES, C::BK * 128, 1024);
-            // Keys 16kk..16kk+15: bf16 P pairs in score columns 16kk..16kk+7
-            // (P over S), or in P columns 8kk..8kk+7 (separate P).
+            // Keys 16kk..16kk+15: bf16 P pairs in P columns 8kk..8kk+7.
             const uint32_t a_p = tmem + C::tm_p(t);
-            constexpr int P_STEP = C::SEP_P ? 8 : 16;
             const uint32_t acc0 = j > my_lo ? 1u : 0u;
             const bool last_pv = j + 1 == my_n;
             if (elect_one()) {
-  #pragma unroll
+#pragma unroll
               for (int kk = 0; kk < C::BK / 16; ++kk)
-                mma_ts(tmem + C::tm_o(t), a_p + kk * P_STEP, dv + ((kk * 2048) >> 4), idesc_o,
+                mma_ts(tmem + C::tm_o(t), a_p + kk * 8, dv + ((kk * 2048) >> 4), idesc_o,
                        kk > 0 ? 1u : acc0);
-              if constexpr (C::SEP_P) mma_commit(smem_u32(&bar_pv_step[t]));
+              mma_commit(smem_u32(&bar_pv_step[t]));
               if (last_pv) mma_commit(smem_u32(&bar_pv_done[t]));
             }
             __syncwarp();
             ATTN_TRACE_EV(tc, 6, j);  // PV_t(j) issued
           }
-          // P over S: the next score tile overwrites P_t(j) in TMEM; MMAs issued
-          // by one thread execute in issue order, so it runs after PV_t(j) has
-          // read P_t(j).
-          if constexpr (!C::SEP_P) next_s(j);
           if (!ok) break;
           // This warp's share of handing back V_j and K_{j+1}: arrives when the
           // MMAs it issued so far complete.

@@ -30,17 +30,36 @@ sys.path.insert(0, ROOT)
 METRIC = "causal bf16 attention fwd+bwd TFLOP/s at 1 GB300; % of dense BF16 tensor peak"
 DEFAULT_WORKLOAD = "llama3_8b_s4096"
 
-# DRAM traffic of the backward main kernel per launch, from an ncu capture,
-# keyed by the hash of the kernel sources it was taken on (null once they change).
-TRAFFIC = {"e41e272fa0d7bac1": 970.27e6}  # dram__bytes_read.sum + dram__bytes_write.sum, one launch
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of each workload's
+# roofline kernel per launch, from one ncu capture per workload: workload ->
+# (hash of the kernel sources it was taken on, bytes). It reads null once the
+# sources change.
+DENSE_SOURCES = ("attn_bwd.cu", "attn_common.cuh", "sm100_ptx.cuh")
+SPARSE_SOURCES = ("attn_sparse_bwd.cu", "attn_sparse.cuh", "attn_common.cuh", "sm100_ptx.cuh")
+TRAFFIC = {
+    "llama3_8b_s4096": ("e41e272fa0d7bac1", 970.27e6),
+    "mha_d64_s2048": ("e41e272fa0d7bac1", 1016.00e6),
+    "swa_w128_s4096": ("e41e272fa0d7bac1", 929.43e6),
+    "llama3_70b_s8192": ("e41e272fa0d7bac1", 3485.71e6),
+    "long_s32768": ("e41e272fa0d7bac1", 13298.78e6),
+    "csa_flash_cr4_t8192": ("54c0877c021529aa", 546.79e6),
+    "csa_pro_cr4_t16384": ("54c0877c021529aa", 2249.01e6),
+}
 
 
-def kernel_source_hash():
+def kernel_source_hash(names=DENSE_SOURCES):
     h = hashlib.sha256()
-    for name in ("attn_bwd.cu", "attn_common.cuh", "sm100_ptx.cuh"):
+    for name in names:
         with open(os.path.join(ROOT, "attention_fwd_bwd_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
+
+
+def traffic_for(workload, names):
+    """Bytes per launch of the workload's roofline kernel, or None if there is
+    no capture for the current sources."""
+    key, nbytes = TRAFFIC.get(workload, (None, None))
+    return nbytes if key is not None and key == kernel_source_hash(names) else None
 
 
 # Dense bf16 tcgen05 rate per SM and clock: an M128 N256 K16 MMA from shared
@@ -350,8 +369,7 @@ def run_ours(args, w, world, rank, local):
     n_rd = 2 if plain else 3
     pre_bytes = (n_rd * B * S * Hq * D * 2 + B * Hq * S * 4 + 2 * B * Hq * S * 4 + B * S * Hq * D * 4)
     pre_bytes_survey = 2 * B * S * Hq * D * 2 + B * Hq * S * 4 + B * S * Hq * D * 4
-    # The ncu traffic figure is for the default workload's launch.
-    traffic = TRAFFIC.get(kernel_source_hash()) if w.name == DEFAULT_WORKLOAD else None
+    traffic = traffic_for(w.name, DENSE_SOURCES)
     in_bytes = sum(t.numel() * t.element_size() for t in (q, k, v, do))
     sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
     theo = theoretical_tflops(sm_count, float(peaks.get("sm_max_mhz", 2070.0)))
@@ -560,7 +578,8 @@ def run_sparse(args, w, world, rank, local):
                        "sparse_bwd": {"ms": bwd_ms, "tflops": bwd_tf, "frac_of_peak": bwd_tf / peak,
                                       "gathered_gbs": gathered / (bwd_ms / 1e3) / 1e9}},
             "roofline": {"kernel": "attn_sparse_bwd_kernel", "bound": "tensor", "achieved": bwd_tf, "peak": peak,
-                         "unit": "TFLOP/s", "frac": bwd_tf / peak, "traffic": None,
+                         "unit": "TFLOP/s", "frac": bwd_tf / peak,
+                         "traffic": traffic_for(w.name, SPARSE_SOURCES),
                          "peak_source": f"{peak_src} bf16_tflops (burst)"},
             "clocks": clocks.summary(),
             "e2e": {"value": whole_job_value(flops, e2e_ms / 1e3, world) / 1e12, "unit": "TFLOP/s",

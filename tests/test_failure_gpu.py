@@ -31,8 +31,11 @@ def _buffers(B, Hq, Hkv, S, D, seed):
     return q, k, v, do, o, o_lo, lse, dq, dk, dv, ws
 
 
-def test_stalled_pipeline_times_out_and_context_survives():
-    B, Hq, Hkv, S, D = 1, 4, 2, 512, 128
+@pytest.mark.parametrize("D", [128, 64])
+def test_stalled_pipeline_times_out_and_context_survives(D):
+    # D = 64 takes the forward with one MMA warp per query tile and the
+    # backward whose P/dS warps read dQ^T themselves.
+    B, Hq, Hkv, S = 1, 4, 2, 512
     q, k, v, do, o, o_lo, lse, dq, dk, dv, ws = _buffers(B, Hq, Hkv, S, D, seed=5)
     scale = D ** -0.5
     assert attn.attn_check_status(None) == 0

@@ -380,28 +380,35 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         };
         auto kv_slot = [&](int idx) { return (ring + idx) % C::NSLOT; };
         // S_t(j+1), if this tile has it.
+        bool k_done = false;  // this step's K_{j+1} copy waited for
         auto next_s = [&](int j) {
           if (j + 1 < my_n && j + 1 >= my_lo) {
             ok = wait_kv(2 * (j - jb) + 2);
             if (!ok) return;
+            k_done = true;
             tc_fence_after();
             issue_s(j + 1);
           }
         };
+        // A slot is handed back once both warps have committed its release
+        // (count 2). Each warp first waits for the copy of every ring tile it
+        // releases, the tiles it does not read included: that copy lands only
+        // after both warps released the slot's previous tile, so a warp that
+        // runs ahead cannot arrive twice on one phase of the slot's barrier
+        // (and hand back a tile the other warp has still to read).
+        ok = wait_kv(0);
+        if (!ok) break;
+        tc_fence_after();
         if (my_lo == jb) {
-          ok = wait_kv(0);
-          if (!ok) break;
-          tc_fence_after();
           issue_s(jb);
           if (!ok) break;
         }
-        // K_jb is done once the S products on it ran. A slot is handed back
-        // when both warps have committed; the warp that reads a tile waited for
-        // its copy first, and every ring tile has a reader (with a window too,
-        // the tiles' ranges leave no gap), so no copy is in flight then.
+        // K_jb is done once the S products on it ran.
         mma_commit_el(smem_u32(&bar_kv_empty[kv_slot(0)]));
         ATTN_TRACE_EV(tc, 3, r);
         for (int j = jb; j < n_kv && ok; ++j) {
+          k_done = false;
+          bool v_done = false;
           // The next score product goes first, as soon as the softmax has read
           // the current scores.
           next_s(j);
@@ -410,6 +417,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
             // V_j first: it landed long before P_t(j) is ready.
             ok = wait_kv(2 * (j - jb) + 1);
             if (!ok) break;
+            v_done = true;
             ok = mbar_wait_warp(smem_u32(&bar_p_full[t]), p_cnt & 1, ctl);
             if (!ok) break;
             ++p_cnt;
@@ -437,8 +445,12 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
             ATTN_TRACE_EV(tc, 6, j);  // PV_t(j) issued
           }
           if (!ok) break;
-          // This warp's share of handing back V_j and K_{j+1}: arrives when the
-          // MMAs it issued so far complete.
+          // This warp's share of handing back V_j and K_{j+1} (arrives when the
+          // MMAs it issued so far complete), after waiting for their copies if
+          // it did not read them.
+          if (!v_done) ok = wait_kv(2 * (j - jb) + 1);
+          if (ok && j + 1 < n_kv && !k_done) ok = wait_kv(2 * (j - jb) + 2);
+          if (!ok) break;
           if (elect_one()) {
             mma_commit(smem_u32(&bar_kv_empty[kv_slot(2 * (j - jb) + 1)]));
             if (j + 1 < n_kv) mma_commit(smem_u32(&bar_kv_empty[kv_slot(2 * (j - jb) + 2)]));

@@ -157,7 +157,7 @@ def test_dense_forward_protocol_is_sound(S, causal, window, nslot):
 
 
 def dense_fwd_sep_p_model(items, nslot, win=False, seed=0, skip_s_free=False, skip_pv_step=False,
-                          release_count=2):
+                          release_count=2, wait_unread=True):
     """The forward when P_t has tensor-memory columns of its own (D = 64, where
     O_t takes 64 of its 128 columns and P_t the other 64): the softmax frees
     S_t as soon as it has read it (s_free), so the tile's MMA issuer runs S_t(j+1)
@@ -169,9 +169,13 @@ def dense_fwd_sep_p_model(items, nslot, win=False, seed=0, skip_s_free=False, sk
     overwrites O) before the previous epilogue read O, raises Aliasing.
     Each query tile has its own MMA issuer (with its own in-order
     completions); ring slots, the Q buffer and the final drain complete once
-    both issuers have committed (count 2). skip_s_free and skip_pv_step plant
-    the two missing waits, release_count=1 a slot handed back on either
-    issuer's commit."""
+    both issuers have committed (count 2); an issuer waits for every ring
+    tile's copy before committing its release, including the tiles it does not
+    read, so that its commit cannot land on the slot's previous phase. The
+    ring is tracked too: a copy issued into a slot whose previous tile still
+    has a pending read raises Aliasing. skip_s_free and skip_pv_step plant the
+    two missing waits, release_count=1 a slot handed back on either issuer's
+    commit, wait_unread=False releases of unread tiles without their waits."""
     rnd = random.Random(seed)
     kv_full = [Bar(1) for _ in range(nslot)]
     kv_empty = [Bar(release_count) for _ in range(nslot)]
@@ -182,6 +186,19 @@ def dense_fwd_sep_p_model(items, nslot, win=False, seed=0, skip_s_free=False, sk
     # Per query tile: score tiles written / read, P tiles stored / read by P V,
     # and epilogues done.
     st = [{"s_w": 0, "s_r": 0, "p_w": 0, "p_r": 0, "epi": 0} for _ in range(2)]
+    # Ring positions: the tiles whose products read each one, and those done.
+    readers, done_reads = {}, {}
+    base = 0
+    for n0, n1, l0, l1 in items:
+        for j in range(l0, n1):
+            for t, (lo, n) in enumerate(((l0, n0), (l1, n1))):
+                if lo <= j < n:
+                    readers.setdefault(base + 2 * (j - l0), set()).add(t)
+                    readers.setdefault(base + 2 * (j - l0) + 1, set()).add(t)
+        base += 2 * (n1 - l0)
+
+    def read_done(t, pos):
+        done_reads.setdefault(pos, set()).add(t)
 
     class Done:  # an asynchronous MMA completing: check the regions, then signal
         def __init__(self, fn, bar):
@@ -191,15 +208,17 @@ def dense_fwd_sep_p_model(items, nslot, win=False, seed=0, skip_s_free=False, sk
             self.fn()
             self.bar.arrive()
 
-    def s_lands(t):
+    def s_lands(t, pos):
         def fn():
             if st[t]["s_w"] != st[t]["s_r"]:
                 raise Aliasing(f"S_{t} product landed on scores not yet read")
             st[t]["s_w"] += 1
+            read_done(t, pos)
         return fn
 
-    def pv_lands(t, item, first):
+    def pv_lands(t, item, first, pos):
         def fn():
+            read_done(t, pos)
             if st[t]["p_r"] + 1 != st[t]["p_w"]:
                 raise Aliasing(f"P_{t} V read a P that was not (or no longer) there")
             if first and st[t]["epi"] != item:
@@ -217,6 +236,9 @@ def dense_fwd_sep_p_model(items, nslot, win=False, seed=0, skip_s_free=False, sk
                 slot, rnd_ = issued % nslot, issued // nslot
                 if rnd_ > 0:
                     yield from wait(kv_empty[slot], rnd_ - 1)
+                    prev = issued - nslot
+                    if readers.get(prev, set()) - done_reads.get(prev, set()):
+                        raise Aliasing(f"ring slot {slot} reloaded while tile {prev} has a pending read")
                 tma.append(kv_full[slot])
                 issued += 1
             pre = 0 if r == 0 else min(2, n_pos)
@@ -240,12 +262,12 @@ def dense_fwd_sep_p_model(items, nslot, win=False, seed=0, skip_s_free=False, sk
             yield from wait(q_full, r)
             s_left = [my_n - my_lo]
 
-            def issue_s():
+            def issue_s(pos):
                 nonlocal s_iss
                 if s_iss > 0 and not skip_s_free:
                     yield from wait(s_free[t], s_iss - 1)
                 s_iss += 1
-                q.append(Done(s_lands(t), s_full[t]))
+                q.append(Done(s_lands(t, pos), s_full[t]))
                 s_left[0] -= 1
                 if s_left[0] == 0:
                     q.append(q_empty)
@@ -256,21 +278,29 @@ def dense_fwd_sep_p_model(items, nslot, win=False, seed=0, skip_s_free=False, sk
 
             def slot(idx):
                 return (ring + idx) % nslot
-            if my_lo == jb:
+            if my_lo == jb or wait_unread:
                 yield from wait_kv(0)
-                yield from issue_s()
+            if my_lo == jb:
+                yield from issue_s(ring)
             q.append(kv_empty[slot(0)])
             for j in range(jb, n1):
+                k_done = v_done = False
                 if my_lo <= j + 1 < my_n:  # the next scores first
                     yield from wait_kv(2 * (j - jb) + 2)
-                    yield from issue_s()
+                    k_done = True
+                    yield from issue_s(ring + 2 * (j + 1 - jb))
                 if my_lo <= j < my_n:
                     yield from wait_kv(2 * (j - jb) + 1)
+                    v_done = True
                     yield from wait(p_full[t], p_cnt)
                     p_cnt += 1
-                    q.append(Done(pv_lands(t, r, j == my_lo), pv_step[t]))
+                    q.append(Done(pv_lands(t, r, j == my_lo, ring + 2 * (j - jb) + 1), pv_step[t]))
                     if j + 1 == my_n:
                         q.append(pv_done[t])
+                if wait_unread and not v_done:
+                    yield from wait_kv(2 * (j - jb) + 1)
+                if wait_unread and j + 1 < n1 and not k_done:
+                    yield from wait_kv(2 * (j - jb) + 2)
                 q.append(kv_empty[slot(2 * (j - jb) + 1)])
                 if j + 1 < n1:
                     q.append(kv_empty[slot(2 * (j - jb) + 2)])
@@ -306,7 +336,7 @@ def dense_fwd_sep_p_model(items, nslot, win=False, seed=0, skip_s_free=False, sk
 
 
 @pytest.mark.parametrize("S,causal,window", FWD_CASES)
-@pytest.mark.parametrize("nslot", [8])
+@pytest.mark.parametrize("nslot", [4, 8])
 def test_dense_forward_separate_p_protocol_is_sound(S, causal, window, nslot):
     items = fwd_items(S, causal, window)
     for seed in range(25):
@@ -326,6 +356,22 @@ def test_separate_p_model_catches_the_missing_waits():
             except (Aliasing, Deadlock):
                 caught += 1
         assert caught > 0, kw
+
+
+def test_separate_p_model_catches_an_unwaited_release():
+    """An issuer that commits the release of a ring tile it does not read
+    without waiting for its copy can arrive twice on one phase of the slot's
+    barrier (when it runs far enough ahead of the other issuer); the slot is
+    then reloaded under the other tile's pending read."""
+    caught = 0
+    for seed in range(60):
+        for S, window in ((1024, 0), (2048, 300)):
+            try:
+                dense_fwd_sep_p_model(fwd_items(S, True, window), 4, win=window > 0, seed=seed,
+                                      wait_unread=False)
+            except (Aliasing, Deadlock):
+                caught += 1
+    assert caught > 0
 
 
 def dense_bwd_model(items, dq_in_compute, stages=3, seed=0, stage_last=True, early_kv=False, ring=4):

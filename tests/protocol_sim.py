@@ -8,13 +8,33 @@ class Bar:
 
     def __init__(self, count):
         self.count, self.pending, self.completed = count, count, 0
+        self.arrived = set()
 
-    def arrive(self):
+    def arrive(self, who=None):
+        """One arrival. With `who` (the arriving agent), a second arrival by
+        the same agent within one phase raises Aliasing: it would complete the
+        phase without an agent that has not arrived yet."""
+        if who is not None:
+            if who in self.arrived:
+                raise Aliasing(f"{who} arrived twice within one phase (phase {self.completed})")
+            self.arrived.add(who)
         Bar.changes += 1
         self.pending -= 1
         if self.pending == 0:
             self.completed += 1
             self.pending = self.count
+            self.arrived = set()
+
+
+class By:
+    """An arrival on `bar` by agent `who`, for the asynchronous completion
+    queues (a commit that arrives when the agent's earlier MMAs complete)."""
+
+    def __init__(self, bar, who):
+        self.bar, self.who = bar, who
+
+    def arrive(self):
+        self.bar.arrive(self.who)
 
 
 class Aliasing(Exception):

@@ -21,7 +21,19 @@ import random
 
 import pytest
 
-from tests.protocol_sim import Aliasing, Bar, Deadlock, run, wait
+from tests.protocol_sim import Aliasing, Bar, By, Deadlock, run, wait
+
+
+def test_barrier_flags_a_second_arrival_by_one_agent():
+    """A count-2 barrier completes on two different agents' arrivals; the
+    same agent arriving twice within one phase is an error."""
+    b = Bar(2)
+    b.arrive(0)
+    b.arrive(1)
+    assert b.completed == 1
+    b.arrive(0)
+    with pytest.raises(Aliasing):
+        b.arrive(0)
 
 
 def fwd_items(S, causal, window=0):
@@ -270,7 +282,7 @@ def dense_fwd_sep_p_model(items, nslot, win=False, seed=0, skip_s_free=False, sk
                 q.append(Done(s_lands(t, pos), s_full[t]))
                 s_left[0] -= 1
                 if s_left[0] == 0:
-                    q.append(q_empty)
+                    q.append(By(q_empty, t))
 
             def wait_kv(idx):
                 pos = ring + idx
@@ -282,7 +294,7 @@ def dense_fwd_sep_p_model(items, nslot, win=False, seed=0, skip_s_free=False, sk
                 yield from wait_kv(0)
             if my_lo == jb:
                 yield from issue_s(ring)
-            q.append(kv_empty[slot(0)])
+            q.append(By(kv_empty[slot(0)], t))
             for j in range(jb, n1):
                 k_done = v_done = False
                 if my_lo <= j + 1 < my_n:  # the next scores first
@@ -301,11 +313,11 @@ def dense_fwd_sep_p_model(items, nslot, win=False, seed=0, skip_s_free=False, sk
                     yield from wait_kv(2 * (j - jb) + 1)
                 if wait_unread and j + 1 < n1 and not k_done:
                     yield from wait_kv(2 * (j - jb) + 2)
-                q.append(kv_empty[slot(2 * (j - jb) + 1)])
+                q.append(By(kv_empty[slot(2 * (j - jb) + 1)], t))
                 if j + 1 < n1:
-                    q.append(kv_empty[slot(2 * (j - jb) + 2)])
+                    q.append(By(kv_empty[slot(2 * (j - jb) + 2)], t))
             ring += 2 * (n1 - jb)
-        q.append(mma_done)
+        q.append(By(mma_done, t))
         yield from wait(mma_done, 0)
 
     def softmax(t):
@@ -503,19 +515,19 @@ def dense_bwd_model(items, dq_in_compute, stages=3, seed=0, stage_last=True, ear
                 gi = git + it
                 yield from wait(sdp_full, gi)
                 yield from wait(st_full[gi % stages], gi // stages)
-                sdp_free.arrive()
+                sdp_free.arrive(cg)
                 if gi >= 1:
                     yield from wait(pds_free, gi - 1)
                 if not dq_in_compute and gi >= 1:
                     yield from wait(dq_free, gi - 1)
-                pds_full.arrive()
+                pds_full.arrive(cg)
                 if dq_in_compute and it >= 1:
                     yield from stage(gi - 1)
             if dq_in_compute and n_it > 0 and stage_last:
                 yield from wait(pds_free, git + n_it - 1)
                 yield from stage(git + n_it - 1)
             yield from wait(mma_done, ii)
-            dkv_free.arrive()
+            dkv_free.arrive(cg)
             git += n_it
         yield from take(len(items), f"compute {cg}")
 

@@ -185,7 +185,7 @@ def sparse_fwd_failure_model(n_items, nch, seed, p_giveup, stall_mma=False, earl
         mma.append(mma_done)
         yield from bwait(ctl, mma_done, 0, abort_aware=False)
 
-    def softmax_warp(w):
+    def softmax_warp(w, k):  # warp k of warpgroup w
         ok, s_cnt, pv_cnt = True, 0, 0
         my_n = (nch - w + 1) // 2 if nch > w else 0
         for rr in range(n_items):
@@ -202,7 +202,7 @@ def sparse_fwd_failure_model(n_items, nch, seed, p_giveup, stall_mma=False, earl
                     if not ok:
                         break
                     checked = True
-                p_full[w].arrive()
+                p_full[w].arrive((w, k))
             if early_break and not ok:
                 break  # the control flow before the fix
             if ok and my_n > 0:
@@ -213,7 +213,7 @@ def sparse_fwd_failure_model(n_items, nch, seed, p_giveup, stall_mma=False, earl
                     ok = yield from bwait(ctl, o1_free, rr - 1)
                 if not ok:
                     break
-                merge.arrive()
+                merge.arrive((w, k))
                 continue
             if ok:
                 ok = yield from bwait(ctl, merge, rr)
@@ -222,10 +222,10 @@ def sparse_fwd_failure_model(n_items, nch, seed, p_giveup, stall_mma=False, earl
                 break
             for _ in range(2):  # the staging tile's two bar.sync of the epilogue
                 yield from nbar.and_(True)
-            o1_free.arrive()
+            o1_free.arrive((w, k))
 
     agents = [k_producer(), v_producer(), mma_warp()]
-    agents += [softmax_warp(0) for _ in range(4)] + [softmax_warp(1) for _ in range(4)]
+    agents += [softmax_warp(w, k) for w in (0, 1) for k in range(4)]
     run(agents, (tma, mma, cpa), rnd)
     return ctl.abort
 
@@ -369,7 +369,7 @@ def dense_fwd_failure_model(items, seed, p_giveup, stall_mma=False, nslot=4):
         mma.append(mma_done)
         yield from bwait(ctl, mma_done, 0, abort_aware=False)
 
-    def softmax_warp(t):
+    def softmax_warp(t, k):  # warp k of warpgroup t
         ok, s_cnt = True, 0
         for item, it in enumerate(items):
             if not ok:
@@ -379,7 +379,7 @@ def dense_fwd_failure_model(items, seed, p_giveup, stall_mma=False, nslot=4):
                 if not ok:
                     break
                 s_cnt += 1
-                p_full[t].arrive()
+                p_full[t].arrive((t, k))
             if ok:
                 ok = yield from bwait(ctl, pv_done[t], item)
             ok = yield from nbar[t].and_(ok)
@@ -387,7 +387,7 @@ def dense_fwd_failure_model(items, seed, p_giveup, stall_mma=False, nslot=4):
                 for _ in range(4):  # the epilogue's staging-tile bar.sync pairs (D = 128: two chunks)
                     yield from nbar[t].and_(True)
 
-    agents = [producer(), mma_warp()] + [softmax_warp(t) for t in (0, 1) for _ in range(4)]
+    agents = [producer(), mma_warp()] + [softmax_warp(t, k) for t in (0, 1) for k in range(4)]
     run(agents, (tma, mma, []), rnd)
     return ctl.abort
 

@@ -576,9 +576,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           // m = -inf; an offset of 0 then gives its masked scores p = 0.
           const float neg_m = (WIN && m == -INFINITY) ? 0.f : -m;
           const uint64_t negm2 = f32x2(neg_m, neg_m);
-          uint64_t sums[2], sumsb[2];
+          uint64_t sums[2];
+          float sb[4] = {0.f, 0.f, 0.f, 0.f};  // the bf16 values' sums, same grouping as sums
 #pragma unroll
-          for (int i = 0; i < 2; ++i) sums[i] = sumsb[i] = f32x2(0.f, 0.f);
+          for (int i = 0; i < 2; ++i) sums[i] = f32x2(0.f, 0.f);
 #pragma unroll
           for (int ch = 0; ch < C::BK; ch += 16) {
 #pragma unroll
@@ -591,9 +592,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
               sums[(c / 2) & 1] = add_f32x2(sums[(c / 2) & 1], f32x2(p0, p1));
               const uint32_t w = pack_bf16x2(p0, p1);  // round to nearest even
               pk[(ch + c) / 2] = w;
-              sumsb[(c / 2) & 1] =
-                  add_f32x2(sumsb[(c / 2) & 1], f32x2(__uint_as_float(w << 16),
-                                                      __uint_as_float(w & 0xFFFF0000u)));
+              add_bf16x2_f32(w, sb[2 * ((c / 2) & 1)], sb[2 * ((c / 2) & 1) + 1]);
             }
             // Columns ch..ch+7 of the scores (already read) take these keys' P.
             if constexpr (!C::SEP_P)
@@ -601,7 +600,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           }
           float s0, s1, b0, b1;
           unpack_f32x2(add_f32x2(sums[0], sums[1]), s0, s1);
-          unpack_f32x2(add_f32x2(sumsb[0], sumsb[1]), b0, b1);
+          b0 = sb[0] + sb[2];
+          b1 = sb[1] + sb[3];
           l = l * alpha + (s0 + s1);
           lb = lb * alpha + (b0 + b1);
         }

@@ -551,6 +551,17 @@ __device__ __forceinline__ void red_add_v4(float* dst, float a, float b, float c
 }
 
 // Three-input max / min (NaN inputs are ignored, as with fmaxf / fminf).
+// s_lo += bf16 low half of w, s_hi += bf16 high half (mixed-precision adds:
+// each bf16 value enters exactly, the sum is rounded to nearest in fp32).
+__device__ __forceinline__ void add_bf16x2_f32(uint32_t w, float& s_lo, float& s_hi) {
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "mov.b32 {lo, hi}, %2;\n\t"
+      "add.rn.f32.bf16 %0, lo, %0;\n\t"
+      "add.rn.f32.bf16 %1, hi, %1;\n\t}"
+      : "+f"(s_lo), "+f"(s_hi)
+      : "r"(w));
+}
+
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));

@@ -440,7 +440,7 @@ __global__ void __launch_bounds__(SparseFwdCfg<DK, DV>::THREADS, 1)
             unpack_f32x2(fma_f32x2(f32x2(x[ch + cc], x[ch + cc + 1]), sl2x2, negm2), e0, e1);
             const float p0 = ex2(e0), p1 = ex2(e1);
             sums[(cc / 2) & 3] = add_f32x2(sums[(cc / 2) & 3], f32x2(p0, p1));
-            split_bf16x2(p0, p1, pkl[cc / 2], pkl[8 + cc / 2]);
+            split_bf16x2_fma(p0, p1, pkl[cc / 2], pkl[8 + cc / 2]);
           }
           tmem_st16(ts + ch, pkl);
         }

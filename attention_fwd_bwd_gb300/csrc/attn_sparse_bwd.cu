@@ -436,8 +436,8 @@ __global__ void __launch_bounds__(SparseBwdCfg<DK, DV>::THREADS, 1)
                                              hh ? f32x2(dv.z, dv.w) : f32x2(dv.x, dv.y));
               float d0, d1;
               unpack_f32x2(mul_f32x2(mul_f32x2(f32x2(p0, p1), sc2), dpv), d0, d1);
-              split_bf16x2(p0, p1, pp[kk / 2], pp[8 + kk / 2]);
-              split_bf16x2(d0, d1, dd[kk / 2], dd[8 + kk / 2]);
+              split_bf16x2_fma(p0, p1, pp[kk / 2], pp[8 + kk / 2]);
+              split_bf16x2_fma(d0, d1, dd[kk / 2], dd[8 + kk / 2]);
             }
           }
           tmem_st16(tmem + lane_base + C::TM_S + h0, pp);

@@ -37,13 +37,13 @@ DEFAULT_WORKLOAD = "llama3_8b_s4096"
 DENSE_SOURCES = ("attn_bwd.cu", "attn_common.cuh", "sm100_ptx.cuh")
 SPARSE_SOURCES = ("attn_sparse_bwd.cu", "attn_sparse.cuh", "attn_common.cuh", "sm100_ptx.cuh")
 TRAFFIC = {
-    "llama3_8b_s4096": ("e41e272fa0d7bac1", 970.27e6),
-    "mha_d64_s2048": ("e41e272fa0d7bac1", 1016.00e6),
-    "swa_w128_s4096": ("e41e272fa0d7bac1", 929.43e6),
-    "llama3_70b_s8192": ("e41e272fa0d7bac1", 3485.71e6),
-    "long_s32768": ("e41e272fa0d7bac1", 13298.78e6),
-    "csa_flash_cr4_t8192": ("54c0877c021529aa", 546.79e6),
-    "csa_pro_cr4_t16384": ("54c0877c021529aa", 2249.01e6),
+    "llama3_8b_s4096": ("ccfec240ad5645db", 973.71e6),
+    "mha_d64_s2048": ("ccfec240ad5645db", 1017.44e6),
+    "swa_w128_s4096": ("ccfec240ad5645db", 929.02e6),
+    "llama3_70b_s8192": ("ccfec240ad5645db", 3388.44e6),
+    "long_s32768": ("ccfec240ad5645db", 12870.36e6),
+    "csa_flash_cr4_t8192": ("8ab932384a96e3be", 546.67e6),
+    "csa_pro_cr4_t16384": ("8ab932384a96e3be", 2249.29e6),
 }
 
 

@@ -130,6 +130,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_base_s;
   const WaitCtl ctl{&abort_flag, p.status, p.timeout_ns};
+  // At D = 64 the waits sleep until their phase completes (suspend-time hint),
+  // so that waiting warps leave issue slots to the softmax warps (1% faster
+  // there; no change at D = 128, which polls).
 
   const uint32_t sQ = smem_u32(smem + C::SMEM_Q);  // tile t at sQ + t * Q_BYTES
   const uint32_t sRing = smem_u32(smem + C::SMEM_RING);
@@ -164,7 +167,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       auto load_kv = [&](int idx) {
         const int pos = issued;
         const int slot = pos % C::NSLOT, round = pos / C::NSLOT;
-        if (round > 0) ok = mbar_wait_warp(smem_u32(&bar_kv_empty[slot]), (round - 1) & 1, ctl);
+        if (round > 0) ok = mbar_wait_warp<C::SEP_P>(smem_u32(&bar_kv_empty[slot]), (round - 1) & 1, ctl);
         if (!ok) return;
         ATTN_TRACE_EV(tc, 2, pos);  // slot free, issuing the load
         const int jl = jb + (idx >> 1);
@@ -184,7 +187,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       const int pre = (r == 0) ? 0 : min(2, n_pos);
       for (int idx = 0; idx < pre && ok; ++idx) load_kv(idx);
       if (!ok) break;
-      if (r > 0) ok = mbar_wait_warp(smem_u32(&bar_q_empty), (r - 1) & 1, ctl);
+      if (r > 0) ok = mbar_wait_warp<C::SEP_P>(smem_u32(&bar_q_empty), (r - 1) & 1, ctl);
       if (!ok) break;
       if (!bounds_ok(it.hq < p.Hq && it.q0 >= 0 && it.q0 < p.n_qblocks * 2 * C::BQ, ctl)) break;
       mbar_arrive_expect_tx_el(smem_u32(&bar_q_full), 2 * C::Q_BYTES);
@@ -223,7 +226,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         const FwdItem it = fwd_item<WIN>(p, ii);
         const int jb = jlo(it, 0);
         const int n_kv = it.n_kv[1];  // tile B ends last; tile A starts first
-        ok = mbar_wait_warp(smem_u32(&bar_q_full), r & 1, ctl);
+        ok = mbar_wait_warp<C::SEP_P>(smem_u32(&bar_q_full), r & 1, ctl);
         if (!ok) break;
         ATTN_TRACE_EV(tc, 1, r);
         // S products left in this item; the last one hands the Q buffer back.
@@ -244,7 +247,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         };
         auto wait_kv = [&](int idx) {
           const int pos = ring + idx;
-          return mbar_wait_warp(smem_u32(&bar_kv_full[pos % C::NSLOT]), (pos / C::NSLOT) & 1, ctl);
+          return mbar_wait_warp<C::SEP_P>(smem_u32(&bar_kv_full[pos % C::NSLOT]), (pos / C::NSLOT) & 1, ctl);
         };
         auto kv_slot = [&](int idx) { return (ring + idx) % C::NSLOT; };
         ok = wait_kv(0);
@@ -258,7 +261,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           bool v_ready = false, k_next_ready = false;
           for (int t = 0; t < 2 && ok; ++t) {
             if (j >= jlo(it, t) && j < it.n_kv[t]) {
-              ok = mbar_wait_warp(smem_u32(&bar_p_full[t]), p_cnt[t] & 1, ctl);
+              ok = mbar_wait_warp<C::SEP_P>(smem_u32(&bar_p_full[t]), p_cnt[t] & 1, ctl);
               if (!ok) break;
               ++p_cnt[t];
               ATTN_TRACE_EV(tc, 4 + t, j);  // P_t(j) ready seen
@@ -343,7 +346,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         const int jb = jlo(it, 0);
         const int n_kv = it.n_kv[1];  // tile B ends last; tile A starts first
         const int my_lo = jlo(it, t), my_n = it.n_kv[t];
-        ok = mbar_wait_warp(smem_u32(&bar_q_full), r & 1, ctl);
+        ok = mbar_wait_warp<C::SEP_P>(smem_u32(&bar_q_full), r & 1, ctl);
         if (!ok) break;
         ATTN_TRACE_EV(tc, 1, r);
         // This tile's S products left in the item; its last one hands this
@@ -354,7 +357,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         // read the previous S_t out of them.
         auto issue_s = [&](int j) {
           if (s_iss > 0) {
-            ok = mbar_wait_warp(smem_u32(&bar_s_free[t]), (s_iss - 1) & 1, ctl);
+            ok = mbar_wait_warp<C::SEP_P>(smem_u32(&bar_s_free[t]), (s_iss - 1) & 1, ctl);
             if (!ok) return;
             tc_fence_after();
           }
@@ -376,7 +379,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         };
         auto wait_kv = [&](int idx) {
           const int pos = ring + idx;
-          return mbar_wait_warp(smem_u32(&bar_kv_full[pos % C::NSLOT]), (pos / C::NSLOT) & 1, ctl);
+          return mbar_wait_warp<C::SEP_P>(smem_u32(&bar_kv_full[pos % C::NSLOT]), (pos / C::NSLOT) & 1, ctl);
         };
         auto kv_slot = [&](int idx) { return (ring + idx) % C::NSLOT; };
         // S_t(j+1), if this tile has it.
@@ -418,7 +421,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
             ok = wait_kv(2 * (j - jb) + 1);
             if (!ok) break;
             v_done = true;
-            ok = mbar_wait_warp(smem_u32(&bar_p_full[t]), p_cnt & 1, ctl);
+            ok = mbar_wait_warp<C::SEP_P>(smem_u32(&bar_p_full[t]), p_cnt & 1, ctl);
             if (!ok) break;
             ++p_cnt;
             ATTN_TRACE_EV(tc, 4, j);  // P_t(j) ready seen
@@ -492,7 +495,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         ATTN_TRACE_EV(tc, 1, j);  // start waiting for S_t(j)
         // S_t(j) landed. With P over S its commit also covers PV_t(j-1), so O_t
         // is current; with separate P columns that is waited for below.
-        ok = mbar_wait_warp(smem_u32(&bar_s_full[t]), s_cnt & 1, ctl);
+        ok = mbar_wait_warp<C::SEP_P>(smem_u32(&bar_s_full[t]), s_cnt & 1, ctl);
         if (!ok) break;
         ++s_cnt;
         ATTN_TRACE_EV(tc, 2, j);  // S_t(j) landed
@@ -610,7 +613,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           // PV_t of the previous P (this item's or, for its first tile, the
           // previous item's last) has read the P columns and written O_t.
           if (s_cnt > 1) {
-            ok = mbar_wait_warp(smem_u32(&bar_pv_step[t]), (s_cnt - 2) & 1, ctl);
+            ok = mbar_wait_warp<C::SEP_P>(smem_u32(&bar_pv_step[t]), (s_cnt - 2) & 1, ctl);
             if (!ok) break;
             tc_fence_after();
           }
@@ -641,7 +644,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       // The item's last P.V product of this tile has run: O_t is final. (Its
       // TMEM columns are free again once this epilogue has read them, which
       // is before this warpgroup signals the next item's first P.)
-      if (ok) ok = mbar_wait_warp(smem_u32(&bar_pv_done[t]), item & 1, ctl);
+      if (ok) ok = mbar_wait_warp<C::SEP_P>(smem_u32(&bar_pv_done[t]), item & 1, ctl);
       ATTN_TRACE_EV(tc, 5, item);  // the item's O_t final: epilogue starts
       // The tile's four warps meet at named barriers in the epilogue: agree
       // first on going on.

@@ -21,6 +21,9 @@ namespace {
 __device__ int g_fwd_status;
 
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;
+// Rows of the forward's output TMA stores: each epilogue warp stores its own
+// 32 rows of a query tile.
+constexpr int kFwdStoreRows = 32;
 unsigned long long g_timeout_ns = kDefaultTimeoutNs;
 int g_inject_stall = 0;
 
@@ -274,8 +277,8 @@ static attn_status_t fwd_impl(const void* q, const void* k, const void* v, void*
   if (!make_bshd_map(&tq, q, B, S, Hq, D, FwdCfg<128>::BQ) ||
       !make_bshd_map(&tk, k, B, S, Hkv, D, FwdCfg<128>::BK) ||
       !make_bshd_map(&tv, v, B, S, Hkv, D, FwdCfg<128>::BK) ||
-      !make_bshd_map(&to, o, B, S, Hq, D, FwdCfg<128>::BQ) ||
-      !make_bshd_map(&tolo, o_lo ? o_lo : o, B, S, Hq, D, FwdCfg<128>::BQ))
+      !make_bshd_map(&to, o, B, S, Hq, D, kFwdStoreRows) ||
+      !make_bshd_map(&tolo, o_lo ? o_lo : o, B, S, Hq, D, kFwdStoreRows))
     return ATTN_ERR_CUDA;
   int* status = fwd_status_ptr();
   if (!status) return ATTN_ERR_CUDA;

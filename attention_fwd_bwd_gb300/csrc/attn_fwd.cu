@@ -73,6 +73,61 @@ __device__ __forceinline__ float row_extreme128(const float (&x)[128]) {
   return MAX ? fmaxf(c0, c1) : fminf(c0, c1);
 }
 
+// Eight K-steps of S = Q K^T (M = N = 128, D = 128) issued by one elected lane
+// in a single asm block (one election, no branch): the descriptors advance
+// 32 bytes per step inside a 128-byte swizzle row (+2 in the descriptor's
+// 16-byte address units) and 16 KB per 64-column chunk (+1024).
+__device__ __forceinline__ void mma_s8_el(uint32_t d, uint64_t a0, uint64_t b0, uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred e, t, f;\n\t.reg .b64 a, b;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.eq.u32 t, 1, 1;\n\tsetp.eq.u32 f, 1, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, f;\n\t"
+      "add.s64 a, %1, 2;\n\tadd.s64 b, %2, 2;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t"
+      "add.s64 a, %1, 4;\n\tadd.s64 b, %2, 4;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t"
+      "add.s64 a, %1, 6;\n\tadd.s64 b, %2, 6;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t"
+      "add.s64 a, %1, 1024;\n\tadd.s64 b, %2, 1024;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t"
+      "add.s64 a, %1, 1026;\n\tadd.s64 b, %2, 1026;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t"
+      "add.s64 a, %1, 1028;\n\tadd.s64 b, %2, 1028;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t"
+      "add.s64 a, %1, 1030;\n\tadd.s64 b, %2, 1030;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t}"
+      ::"r"(d), "l"(a0), "l"(b0), "r"(idesc)
+      : "memory");
+}
+// Eight K-steps of O += P V (A = P from tensor memory, 16 columns a step; B = V,
+// 2048 bytes a step), one elected lane, one asm block; acc0 enables the
+// accumulation of the first step.
+__device__ __forceinline__ void mma_pv8_el(uint32_t d, uint32_t a0, uint64_t b0, uint32_t idesc,
+                                           uint32_t acc0) {
+  asm volatile(
+      "{\n\t.reg .pred e, t, p;\n\t.reg .b32 a;\n\t.reg .b64 b;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.eq.u32 t, 1, 1;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+      "add.u32 a, %1, 16;\n\tadd.s64 b, %2, 128;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n\t"
+      "add.u32 a, %1, 32;\n\tadd.s64 b, %2, 256;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n\t"
+      "add.u32 a, %1, 48;\n\tadd.s64 b, %2, 384;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n\t"
+      "add.u32 a, %1, 64;\n\tadd.s64 b, %2, 512;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n\t"
+      "add.u32 a, %1, 80;\n\tadd.s64 b, %2, 640;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n\t"
+      "add.u32 a, %1, 96;\n\tadd.s64 b, %2, 768;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n\t"
+      "add.u32 a, %1, 112;\n\tadd.s64 b, %2, 896;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n\t}"
+      ::"r"(d), "r"(a0), "l"(b0), "r"(idesc), "r"(acc0)
+      : "memory");
+}
+
 // RESID: the epilogue also stores o_lo. WIN: sliding-window instantiation
 // (p.window > 0); without it the window code compiles away. The kernel is
 // persistent: each CTA loops over its work items, and every barrier keeps
@@ -237,11 +292,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           const int slot = (ring + 2 * (j - jb)) % C::NSLOT;
           const uint64_t dk = sw128_desc(sRing + slot * C::KV_BYTES, 16, 1024);
           const uint64_t dq = dq_desc + ((t * C::Q_BYTES) >> 4);
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t koff = ((kk >> 2) * (128 * 128) + (kk & 3) * 32) >> 4;
-            mma_ss_el(tmem + C::tm_s(t), dq + koff, dk + koff, idesc_s, kk > 0);
-          }
+          static_assert(D == 128, "the batched issue covers D = 128");
+          mma_s8_el(tmem + C::tm_s(t), dq, dk, idesc_s);
           mma_commit_el(smem_u32(&bar_s_full[t]));
           if (--s_left == 0) mma_commit_el(smem_u32(&bar_q_empty));
         };
@@ -279,10 +331,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
               const uint64_t dv = sw128_desc(sRing + vslot * C::KV_BYTES, C::BK * 128, 1024);
               // Keys 16kk..16kk+15: bf16 P pairs in score columns 16kk..16kk+7.
               const uint32_t a_p = tmem + C::tm_s(t);
-#pragma unroll
-              for (int kk = 0; kk < C::BK / 16; ++kk)
-                mma_ts_el(tmem + C::tm_o(t), a_p + kk * 16, dv + ((kk * 2048) >> 4), idesc_o,
-                          (j > jlo(it, t) || kk > 0) ? 1u : 0u);
+              mma_pv8_el(tmem + C::tm_o(t), a_p, dv, idesc_o, j > jlo(it, t) ? 1u : 0u);
               if (j + 1 == it.n_kv[t]) mma_commit_el(smem_u32(&bar_pv_done[t]));
               ATTN_TRACE_EV(tc, 6 + t, j);  // PV_t(j) issued
             }

@@ -69,3 +69,19 @@ def test_sparse_work_counts_filled_slots():
     w = SPARSE_BY_NAME["csa_small_t512"]
     idx = torch.tensor([[[0, -1, 3, -1], [-1, -1, -1, -1]]], dtype=torch.int32)
     assert bench.sparse_flops(w, idx) == 2.0 * w.H * (w.DK + w.DV) * 2
+
+
+def test_traffic_is_keyed_to_workload_and_kernel_sources(monkeypatch):
+    """The roofline's DRAM traffic reads only for a workload with a capture
+    taken on the current kernel sources: a different workload, or sources
+    whose hash changed since, give None."""
+    dense = bench.kernel_source_hash(bench.DENSE_SOURCES)
+    sparse = bench.kernel_source_hash(bench.SPARSE_SOURCES)
+    assert dense != sparse
+    monkeypatch.setattr(bench, "TRAFFIC", {"w_dense": (dense, 1.5e9), "w_sparse": (sparse, 2.5e9),
+                                           "w_stale": ("0" * 16, 3.5e9)})
+    assert bench.traffic_for("w_dense", bench.DENSE_SOURCES) == 1.5e9
+    assert bench.traffic_for("w_sparse", bench.SPARSE_SOURCES) == 2.5e9
+    assert bench.traffic_for("w_sparse", bench.DENSE_SOURCES) is None
+    assert bench.traffic_for("w_stale", bench.DENSE_SOURCES) is None
+    assert bench.traffic_for("w_missing", bench.DENSE_SOURCES) is None

@@ -1,6 +1,7 @@
 """bench.py's host logic on the CPU: the reference arm's JSON line (the oracle
 timed on host cores) for a dense and a sparse workload, the clock-sample
-filter, and the sparse work count. No GPU is touched."""
+filter, the sparse work count and the DRAM-traffic lookup. No GPU is
+touched."""
 import datetime
 import json
 import os

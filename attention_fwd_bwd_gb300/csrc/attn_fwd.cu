@@ -128,6 +128,62 @@ __device__ __forceinline__ void mma_pv8_el(uint32_t d, uint32_t a0, uint64_t b0,
       : "memory");
 }
 
+// The two 128-row query tiles of one work item: tile t holds rows qs[t].. of
+// query head hq[t] (both heads in kv group g of batch b) and needs K/V tiles
+// [j_lo[t], n_kv[t]). Unpaired, the tiles are consecutive row blocks of one
+// head (FwdItem). Head-paired (causal masking with an even number of query
+// heads per kv head), they are the same rows of two heads of one group: both
+// need the same K/V tiles, so every K/V step feeds both tiles, where the
+// consecutive tiles' key ranges are one tile apart (with a 128-key window a
+// step of tile A alone, one of both and one of tile B alone).
+struct TileItem {
+  int b, g;
+  int hq[2], qs[2];
+  int n_kv[2], j_lo[2];
+};
+
+__host__ __device__ __forceinline__ int fwd_n_items(const FwdParams& p, bool pair) {
+  return pair ? p.B * (p.Hq / 2) * ((p.S + 127) / 128) : p.B * p.Hq * p.n_qblocks;
+}
+
+// Item i, longest first: paired items take head pair i % (B Hq / 2) of query
+// tile n_qt - 1 - i / (B Hq / 2).
+template <bool WIN>
+__device__ __forceinline__ TileItem tile_item(const FwdParams& p, bool pair, int i) {
+  constexpr int BT = 128;  // rows of a query tile, keys of a K/V tile
+  TileItem it;
+  if (!pair) {
+    const FwdItem f = fwd_item<WIN>(p, i);
+    it.b = f.b;
+    it.g = f.g;
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      it.hq[t] = f.hq;
+      it.qs[t] = f.q0 + t * BT;
+      it.n_kv[t] = f.n_kv[t];
+      it.j_lo[t] = f.j_lo[t];
+    }
+    return it;
+  }
+  const int hp = p.Hq / 2, bhp = p.B * hp;
+  const int nt = (p.S + BT - 1) / BT;
+  const int bh = i % bhp;
+  const int h0 = 2 * (bh % hp);
+  const int qs = (nt - 1 - i / bhp) * BT;
+  const int n_kv = p.causal ? min(qs / BT + 1, nt) : nt;
+  const int j_lo = WIN ? min(max(0, qs - p.window + 1) / BT, n_kv - 1) : 0;
+  it.b = bh / hp;
+  it.g = h0 / p.G;
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    it.hq[t] = h0 + t;
+    it.qs[t] = qs;
+    it.n_kv[t] = n_kv;
+    it.j_lo[t] = j_lo;
+  }
+  return it;
+}
+
 // RESID: the epilogue also stores o_lo. WIN: sliding-window instantiation
 // (p.window > 0); without it the window code compiles away. The kernel is
 // persistent: each CTA loops over its work items, and every barrier keeps
@@ -138,7 +194,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v,
                     const __grid_constant__ CUtensorMap tm_o,
-                    const __grid_constant__ CUtensorMap tm_olo, const FwdParams p) {
+                    const __grid_constant__ CUtensorMap tm_olo, const FwdParams p,
+                    const int pair) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -154,9 +211,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
-  const int n_items = p.B * p.Hq * p.n_qblocks;
+  const int n_items = fwd_n_items(p, pair != 0);
   const int cta = blockIdx.x, n_cta = gridDim.x;
-  auto jlo = [&](const FwdItem& it, int t) { return WIN ? it.j_lo[t] : 0; };
+  auto jlo = [&](const TileItem& it, int t) { return WIN ? it.j_lo[t] : 0; };
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
@@ -216,7 +273,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     for (int r = 0; ok; ++r) {
       const int ii = fwd_item_index(r, cta, n_cta, n_items);
       if (ii < 0) break;
-      const FwdItem it = fwd_item<WIN>(p, ii);
+      const TileItem it = tile_item<WIN>(p, pair != 0, ii);
       const int jb = jlo(it, 0);
       const int n_pos = 2 * (it.n_kv[1] - jb);
       auto load_kv = [&](int idx) {
@@ -244,12 +301,14 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       if (!ok) break;
       if (r > 0) ok = mbar_wait_warp<C::SEP_P>(smem_u32(&bar_q_empty), (r - 1) & 1, ctl);
       if (!ok) break;
-      if (!bounds_ok(it.hq < p.Hq && it.q0 >= 0 && it.q0 < p.n_qblocks * 2 * C::BQ, ctl)) break;
+      if (!bounds_ok(it.hq[0] >= 0 && it.hq[1] < p.Hq && it.qs[0] >= 0 &&
+                         it.qs[1] < p.n_qblocks * 2 * C::BQ, ctl))
+        break;
       mbar_arrive_expect_tx_el(smem_u32(&bar_q_full), 2 * C::Q_BYTES);
       for (int t = 0; t < 2; ++t)
         for (int c = 0; c < C::KCH; ++c)
           tma_load_4d_el(sQ + t * C::Q_BYTES + c * (C::BQ * 128), &tm_q, smem_u32(&bar_q_full),
-                         c * 64, it.hq, it.q0 + t * C::BQ, it.b);
+                         c * 64, it.hq[t], it.qs[t], it.b);
       ++q_loads;
       for (int idx = pre; idx < n_pos && ok; ++idx) load_kv(idx);
     }
@@ -278,7 +337,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       for (int r = 0; ok; ++r) {
         const int ii = fwd_item_index(r, cta, n_cta, n_items);
         if (ii < 0) break;
-        const FwdItem it = fwd_item<WIN>(p, ii);
+        const TileItem it = tile_item<WIN>(p, pair != 0, ii);
         const int jb = jlo(it, 0);
         const int n_kv = it.n_kv[1];  // tile B ends last; tile A starts first
         ok = mbar_wait_warp<C::SEP_P>(smem_u32(&bar_q_full), r & 1, ctl);
@@ -391,7 +450,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       for (int r = 0; ok; ++r) {
         const int ii = fwd_item_index(r, cta, n_cta, n_items);
         if (ii < 0) break;
-        const FwdItem it = fwd_item<WIN>(p, ii);
+        const TileItem it = tile_item<WIN>(p, pair != 0, ii);
         const int jb = jlo(it, 0);
         const int n_kv = it.n_kv[1];  // tile B ends last; tile A starts first
         const int my_lo = jlo(it, t), my_n = it.n_kv[t];
@@ -533,9 +592,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     for (int item = 0; ok; ++item) {
       const int ii = fwd_item_index(item, cta, n_cta, n_items);
       if (ii < 0) break;
-      const FwdItem it = fwd_item<WIN>(p, ii);
-      const int q0 = it.q0, b = it.b, hq = it.hq;
-      const int qrow = q0 + t * C::BQ + r;
+      const TileItem it = tile_item<WIN>(p, pair != 0, ii);
+      const int qt0 = it.qs[t], b = it.b, hq = it.hq[t];  // this tile's first row, its head
+      const int qrow = qt0 + r;
       const int my_kv = it.n_kv[t];
       float m = -INFINITY;  // running max in log2 units (scaled scores)
       float l = 0.f;        // row sum of the fp32 probabilities (for LSE)
@@ -567,7 +626,6 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           ATTN_TRACE_EV(tc, 7, j);  // S_t(j) read out
         }
         const int k0 = j * C::BK;
-        const int qt0 = q0 + t * C::BQ;
         // Tiles that cross the causal diagonal, hold keys past S, or hold keys
         // below some row's window mask; the rest skip masking.
         const bool need_mask = (p.causal && k0 + C::BK - 1 > qt0) || (k0 + C::BK > p.S) ||
@@ -746,8 +804,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
             }
             fence_async_smem();
             __syncwarp();
-            if (leader && bounds_ok(hq < p.Hq && b < p.B && q0 + t * C::BQ >= 0, ctl)) {
-              tma_store_4d(part ? &tm_olo : &tm_o, c, hq, q0 + t * C::BQ + wr, b, stg);
+            if (leader && bounds_ok(hq < p.Hq && b < p.B && qt0 >= 0, ctl)) {
+              tma_store_4d(part ? &tm_olo : &tm_o, c, hq, qt0 + wr, b, stg);
               bulk_commit_group();
             }
           }
@@ -786,11 +844,14 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   static int sm_count[64] = {};
   if (dev < 64 && sm_count[dev] == 0)
     cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
-  const long long n_items = static_cast<long long>(p.B) * p.Hq * p.n_qblocks;
+  // Head pairing with causal masking and an even number of query heads per
+  // kv head (see TileItem).
+  const bool pair = p.causal && p.G % 2 == 0;
+  const long long n_items = fwd_n_items(p, pair);
   const int sms = (dev < 64 && sm_count[dev] > 0) ? sm_count[dev] : 148;
   const dim3 grid(static_cast<unsigned>(n_items < sms ? n_items : sms));
   attn_fwd_kernel<D, RESID, WIN><<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(tq, tk, tv, to, tolo,
-                                                                                 p);
+                                                                                 p, pair ? 1 : 0);
   return cudaGetLastError();
 }
 

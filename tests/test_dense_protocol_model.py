@@ -36,22 +36,27 @@ def test_barrier_flags_a_second_arrival_by_one_agent():
         b.arrive(0)
 
 
-def fwd_items(S, causal, window=0):
-    """(n_kv[0], n_kv[1], jlo[0], jlo[1]) of every item, longest first (one
-    head; a CTA that takes them all in that order)."""
+def fwd_items(S, causal, window=0, paired=False):
+    """(n_kv[0], n_kv[1], jlo[0], jlo[1]) of every item, longest first (a CTA
+    that takes them all in that order). Unpaired, an item is two consecutive
+    128-row tiles of one head; paired, the same 128 rows of two heads of one
+    kv group, so both tiles need the same K/V tiles."""
     BQ = BK = 128
     nkv_all = (S + BK - 1) // BK
+
+    def tile(qt0):
+        n = min(qt0 // BK + 1, nkv_all) if causal else nkv_all
+        return n, (min(max(0, qt0 - window + 1) // BK, n - 1) if window else 0)
+
+    if paired:
+        n_qt = (S + BQ - 1) // BQ
+        return [(n, n, lo, lo) for n, lo in (tile((n_qt - 1 - i) * BQ) for i in range(n_qt))]
     n_qb = (S + 2 * BQ - 1) // (2 * BQ)
     items = []
     for i in range(n_qb):
         q0 = (n_qb - 1 - i) * 2 * BQ
-        n_kv, jlo = [], []
-        for t in range(2):
-            qt0 = q0 + t * BQ
-            n = min(qt0 // BK + 1, nkv_all) if causal else nkv_all
-            n_kv.append(n)
-            jlo.append(min(max(0, qt0 - window + 1) // BK, n - 1) if window else 0)
-        items.append((n_kv[0], n_kv[1], jlo[0], jlo[1]))
+        (n0, l0), (n1, l1) = tile(q0), tile(q0 + BQ)
+        items.append((n0, n1, l0, l1))
     return items
 
 
@@ -160,10 +165,11 @@ FWD_CASES = [
 ]
 
 
+@pytest.mark.parametrize("paired", [False, True], ids=["consecutive", "paired"])
 @pytest.mark.parametrize("S,causal,window", FWD_CASES)
 @pytest.mark.parametrize("nslot", [4, 8])
-def test_dense_forward_protocol_is_sound(S, causal, window, nslot):
-    items = fwd_items(S, causal, window)
+def test_dense_forward_protocol_is_sound(S, causal, window, nslot, paired):
+    items = fwd_items(S, causal, window, paired)
     for seed in range(25):
         assert dense_fwd_model(items, nslot, win=window > 0, seed=seed)
 
@@ -347,10 +353,11 @@ def dense_fwd_sep_p_model(items, nslot, win=False, seed=0, skip_s_free=False, sk
     return run([producer(), mma_warp(0), mma_warp(1), softmax(0), softmax(1)], (tma, mma, []), rnd)
 
 
+@pytest.mark.parametrize("paired", [False, True], ids=["consecutive", "paired"])
 @pytest.mark.parametrize("S,causal,window", FWD_CASES)
 @pytest.mark.parametrize("nslot", [4, 8])
-def test_dense_forward_separate_p_protocol_is_sound(S, causal, window, nslot):
-    items = fwd_items(S, causal, window)
+def test_dense_forward_separate_p_protocol_is_sound(S, causal, window, nslot, paired):
+    items = fwd_items(S, causal, window, paired)
     for seed in range(25):
         assert dense_fwd_sep_p_model(items, nslot, win=window > 0, seed=seed)
 

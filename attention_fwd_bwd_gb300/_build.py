@@ -20,7 +20,7 @@ LIB = os.path.join(LIBDIR, "libattn.so")
 LIB_DEBUG = os.path.join(LIBDIR, "libattn_debug.so")
 SOURCES = ["attn_api.cu", "attn_fwd.cu", "attn_bwd.cu", "attn_bwd_dvec.cu", "attn_noalloc.cu", "attn_sparse.cu",
            "attn_sparse_bwd.cu"]
-HEADERS = ["attn_common.cuh", "attn_sparse.cuh", "sm100_ptx.cuh"]
+HEADERS = ["attn_common.cuh", "attn_items.cuh", "attn_sparse.cuh", "sm100_ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v"]
 

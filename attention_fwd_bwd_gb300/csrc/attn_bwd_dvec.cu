@@ -21,6 +21,7 @@
 //       lane r): P = exp2(S scale log2(e) - LSE log2(e)) with the mask, and
 //       the row sum of P dP, accumulated over the row's key tiles.
 #include "attn_common.cuh"
+#include "attn_items.cuh"
 #include "sm100_ptx.cuh"
 
 namespace attn {
@@ -33,7 +34,8 @@ __global__ void __launch_bounds__(DvecCfg<D>::THREADS, 1)
     attn_bwd_dvec_kernel(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v,
-                         const __grid_constant__ CUtensorMap tm_do, const DvecParams p) {
+                         const __grid_constant__ CUtensorMap tm_do, const DvecParams p,
+                         const int pair) {
   using C = DvecCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -47,9 +49,9 @@ __global__ void __launch_bounds__(DvecCfg<D>::THREADS, 1)
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
-  const int n_items = p.B * p.Hq * p.n_qblocks;
+  const int n_items = tile_n_items(p, pair != 0);
   const int cta = blockIdx.x, n_cta = gridDim.x;
-  auto jlo = [&](const FwdItem& it, int t) { return WIN ? it.j_lo[t] : 0; };
+  auto jlo = [&](const TileItem& it, int t) { return WIN ? it.j_lo[t] : 0; };
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
@@ -98,7 +100,7 @@ __global__ void __launch_bounds__(DvecCfg<D>::THREADS, 1)
     for (int r = 0; ok; ++r) {
       const int ii = fwd_item_index(r, cta, n_cta, n_items);
       if (ii < 0) break;
-      const FwdItem it = fwd_item<WIN>(p, ii);
+      const TileItem it = tile_item<WIN>(p, pair != 0, ii);
       const int jb = jlo(it, 0);
       const int n_pos = 2 * (it.n_kv[1] - jb);
       auto load_kv = [&](int idx) {
@@ -129,7 +131,7 @@ __global__ void __launch_bounds__(DvecCfg<D>::THREADS, 1)
       for (int n = 0; n < 4; ++n)
         for (int c = 0; c < C::KCH; ++c)
           tma_load_4d_el(sQ + n * C::Q_BYTES + c * (C::BQ * 128), n < 2 ? &tm_q : &tm_do,
-                         smem_u32(&bar_q_full), c * 64, it.hq, it.q0 + (n & 1) * C::BQ, it.b);
+                         smem_u32(&bar_q_full), c * 64, it.hq[n & 1], it.qs[n & 1], it.b);
       ++q_loads;
       for (int idx = pre; idx < n_pos && ok; ++idx) load_kv(idx);
     }
@@ -152,7 +154,7 @@ __global__ void __launch_bounds__(DvecCfg<D>::THREADS, 1)
     for (int r = 0; ok; ++r) {
       const int ii = fwd_item_index(r, cta, n_cta, n_items);
       if (ii < 0) break;
-      const FwdItem it = fwd_item<WIN>(p, ii);
+      const TileItem it = tile_item<WIN>(p, pair != 0, ii);
       const int jb = jlo(it, 0);
       const int n_kv = it.n_kv[1];
       ok = mbar_wait_warp(smem_u32(&bar_q_full), r & 1, ctl);
@@ -226,10 +228,10 @@ __global__ void __launch_bounds__(DvecCfg<D>::THREADS, 1)
     for (int item = 0; ok; ++item) {
       const int ii = fwd_item_index(item, cta, n_cta, n_items);
       if (ii < 0) break;
-      const FwdItem it = fwd_item<WIN>(p, ii);
-      const int qt0 = it.q0 + t * C::BQ;
+      const TileItem it = tile_item<WIN>(p, pair != 0, ii);
+      const int qt0 = it.qs[t];
       const int qrow = qt0 + r;
-      const size_t rowoff = (static_cast<size_t>(it.b) * p.Hq + it.hq) * p.S_pad;
+      const size_t rowoff = (static_cast<size_t>(it.b) * p.Hq + it.hq[t]) * p.S_pad;
       // Rows past S (padding) have -LSE log2(e) = -inf: P = 0; they are not stored.
       const float nl = p.nlse2[rowoff + min(qrow, p.S_pad - 1)];
       const uint64_t nl2 = f32x2(nl, nl);
@@ -309,10 +311,12 @@ cudaError_t launch_dvec_t(const CUtensorMap& tq, const CUtensorMap& tk, const CU
   }
   if (dev < 64 && sm_count[dev] == 0)
     cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
-  const long long n_items = static_cast<long long>(p.B) * p.Hq * p.n_qblocks;
+  const bool pair = tile_pair_heads(p);  // see TileItem
+  const long long n_items = tile_n_items(p, pair);
   const int sms = (dev < 64 && sm_count[dev] > 0) ? sm_count[dev] : 148;
   const dim3 grid(static_cast<unsigned>(n_items < sms ? n_items : sms));
-  attn_bwd_dvec_kernel<D, WIN><<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(tq, tk, tv, tdo, p);
+  attn_bwd_dvec_kernel<D, WIN><<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(tq, tk, tv, tdo, p,
+                                                                           pair ? 1 : 0);
   return cudaGetLastError();
 }
 

@@ -37,6 +37,7 @@
 // where the backward needs rowsum(dO * O) beyond bf16 accuracy), the epilogue
 // also stores what the bf16 rounding of O dropped.
 #include "attn_common.cuh"
+#include "attn_items.cuh"
 #include "sm100_ptx.cuh"
 
 namespace attn {
@@ -128,62 +129,6 @@ __device__ __forceinline__ void mma_pv8_el(uint32_t d, uint32_t a0, uint64_t b0,
       : "memory");
 }
 
-// The two 128-row query tiles of one work item: tile t holds rows qs[t].. of
-// query head hq[t] (both heads in kv group g of batch b) and needs K/V tiles
-// [j_lo[t], n_kv[t]). Unpaired, the tiles are consecutive row blocks of one
-// head (FwdItem). Head-paired (causal masking with an even number of query
-// heads per kv head), they are the same rows of two heads of one group: both
-// need the same K/V tiles, so every K/V step feeds both tiles, where the
-// consecutive tiles' key ranges are one tile apart (with a 128-key window a
-// step of tile A alone, one of both and one of tile B alone).
-struct TileItem {
-  int b, g;
-  int hq[2], qs[2];
-  int n_kv[2], j_lo[2];
-};
-
-__host__ __device__ __forceinline__ int fwd_n_items(const FwdParams& p, bool pair) {
-  return pair ? p.B * (p.Hq / 2) * ((p.S + 127) / 128) : p.B * p.Hq * p.n_qblocks;
-}
-
-// Item i, longest first: paired items take head pair i % (B Hq / 2) of query
-// tile n_qt - 1 - i / (B Hq / 2).
-template <bool WIN>
-__device__ __forceinline__ TileItem tile_item(const FwdParams& p, bool pair, int i) {
-  constexpr int BT = 128;  // rows of a query tile, keys of a K/V tile
-  TileItem it;
-  if (!pair) {
-    const FwdItem f = fwd_item<WIN>(p, i);
-    it.b = f.b;
-    it.g = f.g;
-#pragma unroll
-    for (int t = 0; t < 2; ++t) {
-      it.hq[t] = f.hq;
-      it.qs[t] = f.q0 + t * BT;
-      it.n_kv[t] = f.n_kv[t];
-      it.j_lo[t] = f.j_lo[t];
-    }
-    return it;
-  }
-  const int hp = p.Hq / 2, bhp = p.B * hp;
-  const int nt = (p.S + BT - 1) / BT;
-  const int bh = i % bhp;
-  const int h0 = 2 * (bh % hp);
-  const int qs = (nt - 1 - i / bhp) * BT;
-  const int n_kv = p.causal ? min(qs / BT + 1, nt) : nt;
-  const int j_lo = WIN ? min(max(0, qs - p.window + 1) / BT, n_kv - 1) : 0;
-  it.b = bh / hp;
-  it.g = h0 / p.G;
-#pragma unroll
-  for (int t = 0; t < 2; ++t) {
-    it.hq[t] = h0 + t;
-    it.qs[t] = qs;
-    it.n_kv[t] = n_kv;
-    it.j_lo[t] = j_lo;
-  }
-  return it;
-}
-
 // RESID: the epilogue also stores o_lo. WIN: sliding-window instantiation
 // (p.window > 0); without it the window code compiles away. The kernel is
 // persistent: each CTA loops over its work items, and every barrier keeps
@@ -211,7 +156,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
-  const int n_items = fwd_n_items(p, pair != 0);
+  const int n_items = tile_n_items(p, pair != 0);
   const int cta = blockIdx.x, n_cta = gridDim.x;
   auto jlo = [&](const TileItem& it, int t) { return WIN ? it.j_lo[t] : 0; };
 
@@ -844,10 +789,8 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   static int sm_count[64] = {};
   if (dev < 64 && sm_count[dev] == 0)
     cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
-  // Head pairing with causal masking and an even number of query heads per
-  // kv head (see TileItem).
-  const bool pair = p.causal && p.G % 2 == 0;
-  const long long n_items = fwd_n_items(p, pair);
+  const bool pair = tile_pair_heads(p);  // see TileItem
+  const long long n_items = tile_n_items(p, pair);
   const int sms = (dev < 64 && sm_count[dev] > 0) ? sm_count[dev] : 148;
   const dim3 grid(static_cast<unsigned>(n_items < sms ? n_items : sms));
   attn_fwd_kernel<D, RESID, WIN><<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(tq, tk, tv, to, tolo,

@@ -716,10 +716,11 @@ def dvec_model(items, nslot, seed=0, early_free=False):
         raise Aliasing(str(e))
 
 
+@pytest.mark.parametrize("paired", [False, True], ids=["consecutive", "paired"])
 @pytest.mark.parametrize("S,causal,window", FWD_CASES)
 @pytest.mark.parametrize("nslot", [3, 8])
-def test_dvec_pass_protocol_is_sound(S, causal, window, nslot):
-    items = fwd_items(S, causal, window)
+def test_dvec_pass_protocol_is_sound(S, causal, window, nslot, paired):
+    items = fwd_items(S, causal, window, paired)
     for seed in range(25):
         assert dvec_model(items, nslot, seed=seed)
 

@@ -392,10 +392,11 @@ def dense_fwd_failure_model(items, seed, p_giveup, stall_mma=False, nslot=4):
     return ctl.abort
 
 
+@pytest.mark.parametrize("paired", [False, True], ids=["consecutive", "paired"])
 @pytest.mark.parametrize("S,causal,window", [(1024, True, 0), (640, False, 0), (1000, True, 200)])
-def test_dense_forward_every_warp_leaves(S, causal, window):
+def test_dense_forward_every_warp_leaves(S, causal, window, paired):
     from tests.test_dense_protocol_model import fwd_items
-    items = fwd_items(S, causal, window)
+    items = fwd_items(S, causal, window, paired)
     gave_up = sum(dense_fwd_failure_model(items, seed, p_giveup=0.02) for seed in range(40))
     assert gave_up > 0
     for seed in range(10):

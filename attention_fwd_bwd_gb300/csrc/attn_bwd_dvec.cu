@@ -9,8 +9,8 @@
 // definition instead, in fp32, at the cost of two GEMM units (Q K^T and
 // dO V^T).
 //
-// Per CTA (persistent, items as the forward's: two 128-row query tiles of one
-// head, longest first):
+// Per CTA (persistent, items as the forward's: two 128-row query tiles that
+// share their K/V tiles, longest first; see TileItem):
 //   warp 8 (TMA producer): Q_A, Q_B, dO_A, dO_B once per item, then K_j and
 //       V_j into a ring of shared-memory slots (full/empty mbarrier pairs).
 //   warp 9 (MMA issuer): S_t = Q_t K_j^T and dP_t = dO_t V_j^T into tile t's

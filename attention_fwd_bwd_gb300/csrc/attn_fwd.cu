@@ -6,8 +6,9 @@
 // with the query-tile loop outside and the key/value loop inside so the state
 // never leaves the SM.
 //
-// Per CTA: two 128-row query tiles (A and B) of one head, sharing every K/V
-// tile that streams in.
+// Per item: two 128-row query tiles (A and B) that share every K/V tile that
+// streams in -- the same rows of two query heads of one kv group under causal
+// GQA, else consecutive rows of one head (TileItem).
 //   warp 8 (TMA producer): Q_A and Q_B once, then K_0, V_0, K_1, V_1, ... into
 //       a ring of shared-memory slots, each guarded by a full/empty mbarrier
 //       pair (the GB300 counterpart of the paper's "issue N+1 loads, wait

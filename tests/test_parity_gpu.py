@@ -261,3 +261,20 @@ def test_long_noncausal_elementwise(Hq, Hkv, D):
     assert_close_grad(got["dq"], dq_ref, "dQ", what)
     assert_close_grad(got["dk"], dk_ref, "dK", what)
     assert_close_grad(got["dv"], dv_ref, "dV", what)
+
+
+@pytest.mark.parametrize("D,window", [(128, 0), (128, 200), (64, 0), (64, 77)])
+def test_head_pairing_leaves_rows_unchanged(D, window):
+    # With causal masking and an even number of query heads per kv head, a
+    # forward item holds the same rows of two heads; with one query head per
+    # kv head it holds two consecutive row blocks of one head. Each row's
+    # arithmetic is the same either way, so GQA equals the same problem with
+    # K/V repeated per query head, bit for bit.
+    B, Hq, Hkv, S = 1, 4, 2, 520
+    scale = 1.0 / np.sqrt(D)
+    q, k, v, do = make_inputs(B, Hq, Hkv, S, D, seed=900 + D + window)
+    kr, vr = (t.repeat_interleave(Hq // Hkv, dim=2).contiguous() for t in (k, v))
+    for residual in (True, False):
+        a = gpu_fwd_bwd(q, k, v, do, True, scale, with_bwd=False, window=window, residual=residual)
+        b = gpu_fwd_bwd(q, kr, vr, do, True, scale, with_bwd=False, window=window, residual=residual)
+        assert torch.equal(a["o"], b["o"]) and torch.equal(a["lse"], b["lse"]), (D, window, residual)
